@@ -1,0 +1,364 @@
+"""Plain, slow CPU float64 oracle of the routed (optionally latent) MoE layer forward.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference leg of ``bench.py`` may import this module.  It
+shares no code with the CUDA path and imports nothing from the product package.
+
+Source of every definition below: the page "Как устроен Olmo-core 3: обучение
+больших MoE-моделей" (sarnas.ru blog), cited as [Olmo-core 3] plus its section
+heading.  All arithmetic is numpy float64; bf16 inputs are upcast exactly.
+
+Readings where the page is silent (each is also listed in the design notes):
+  * top-k order: descending key, equal keys -> lower expert index first (the
+    intent of ``_break_ties`` in [Olmo-core 3, §"Разрешение равенства логитов
+    и квантизация"]);
+  * order inside an expert group: ascending flat assignment index t*k + j
+    (a stable sort; [Olmo-core 3, §"Пересылка токенов между экспертами"] only
+    says "sorted");
+  * the router reads the layer input x (shape (..., d_model)), not the latent
+    projection;
+  * combine happens in latent space, then RMSNorm, then one up-projection per
+    token ([Olmo-core 3, §"Латентная проекция экспертов"]: the experts' output
+    is restored as a whole);
+  * RMSNorm: z / sqrt(mean(z^2) + eps) * gamma, eps = 1e-6 and gamma = 1
+    unless given ("bias-free" only rules out a bias);
+  * SwiGLU: expert up-projection rows [0, h) are "up", rows [h, 2h) are "gate",
+    activation = silu(gate) * up ([Olmo-core 3, §"SwiGLU с квантизацией"]
+    splits the last dim in half into up and gate);
+  * unset router options (p, scales, epsilon, biases) mean "not applied".
+
+Parity pins: every function here is checked in ``tests/test_oracle_*.py``
+against closed forms, library routines, brute force or invariants.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass
+from typing import Callable, Optional, Sequence
+
+import numpy as np
+
+GATING_SOFTMAX = 0
+GATING_TOPK_SOFTMAX = 1
+GATING_SIGMOID = 2
+
+
+@dataclass
+class OracleConfig:
+    """Fields of MoEConfig / MoERouterConfigV2 / LatentMoEConfig.
+
+    [Olmo-core 3, §"Как задаётся конфигурация MoE"] (num_experts, hidden_size,
+    d_model, top_k), §"Латентная проекция экспертов" (latent_dim, up-proj input
+    norm) and §"Маршрутизация: как роутер выбирает экспертов" (gating,
+    sigmoid_stability_epsilon, normalize_expert_weights, restore_weight_scale,
+    expert_weight_scale, original_top_k, score_bias).
+    """
+
+    d_model: int
+    num_experts: int
+    top_k: int
+    hidden_size: int
+    latent_dim: int = 0            # 0: no latent MoE (latent_dim = d_model)
+    up_proj_norm: bool = True      # latent only: bias-free RMSNorm before up-proj
+    rms_eps: float = 1e-6
+    gating: int = GATING_SOFTMAX
+    sigmoid_stability_epsilon: float = 0.0   # 0: unset
+    normalize_expert_weights: float = 0.0    # p; 0: unset
+    restore_weight_scale: bool = False
+    expert_weight_scale: float = 0.0         # 0: unset
+    original_top_k: int = 0                  # 0 or == top_k: unset
+    router_bias: bool = False
+    has_score_bias: bool = False
+
+    @property
+    def is_latent(self) -> bool:
+        return self.latent_dim > 0
+
+    @property
+    def routed_dim(self) -> int:
+        return self.latent_dim if self.latent_dim > 0 else self.d_model
+
+
+# --------------------------------------------------------------------------
+# Parameter counts  [Olmo-core 3, §"Как задаётся конфигурация MoE"]
+# --------------------------------------------------------------------------
+
+def up_factor(activation: str = "swiglu") -> int:
+    """2 for the gated activations (swiglu, gpt_oss_swiglu), 1 otherwise."""
+    return 2 if activation in ("swiglu", "gpt_oss_swiglu") else 1
+
+
+def router_params(cfg: OracleConfig) -> int:
+    """Router: d_model * num_experts weights, plus num_experts if it has a bias."""
+    return cfg.d_model * cfg.num_experts + (cfg.num_experts if cfg.router_bias else 0)
+
+
+def expert_params_each(cfg: OracleConfig, activation: str = "swiglu") -> int:
+    """One routed expert: (up_factor + 1) * dim * hidden_size (no expert bias).
+
+    The experts are built with d_model = latent_dim when latent
+    ([Olmo-core 3, §"Латентная проекция экспертов"]).
+    """
+    return (up_factor(activation) + 1) * cfg.routed_dim * cfg.hidden_size
+
+
+def num_params(cfg: OracleConfig, shared_params: int = 0) -> int:
+    """Total = router + 3 * latent_dim * hidden_size * num_experts + shared modules."""
+    return router_params(cfg) + 3 * cfg.routed_dim * cfg.hidden_size * cfg.num_experts + shared_params
+
+
+def num_active_params(cfg: OracleConfig, shared_params: int = 0) -> int:
+    """Active = total - all expert params + top_k experts' params."""
+    experts_all = 3 * cfg.routed_dim * cfg.hidden_size * cfg.num_experts
+    experts_active = 3 * cfg.routed_dim * cfg.hidden_size * cfg.top_k
+    return num_params(cfg, shared_params) - experts_all + experts_active
+
+
+def latent_proj_params(cfg: OracleConfig) -> int:
+    """Down (latent_dim x d_model) + up (d_model x latent_dim) projections.
+
+    The page's total does not name them; they are reported separately.
+    """
+    if not cfg.is_latent:
+        return 0
+    return 2 * cfg.d_model * cfg.latent_dim
+
+
+# --------------------------------------------------------------------------
+# Router  [Olmo-core 3, §"Маршрутизация: как роутер выбирает экспертов"]
+# --------------------------------------------------------------------------
+
+def router_logits(x: np.ndarray, w_router: np.ndarray, b_router: Optional[np.ndarray] = None) -> np.ndarray:
+    """Linear layer with weight (num_experts, d_model): logits (T, num_experts)."""
+    logits = np.asarray(x, np.float64) @ np.asarray(w_router, np.float64).T
+    if b_router is not None:
+        logits = logits + np.asarray(b_router, np.float64)[None, :]
+    return logits
+
+
+def gate_scores(logits: np.ndarray, gating: int, sigmoid_eps: float = 0.0) -> np.ndarray:
+    """softmax / topk_softmax: softmax over the experts axis; sigmoid: sigmoid + epsilon."""
+    logits = np.asarray(logits, np.float64)
+    if gating in (GATING_SOFTMAX, GATING_TOPK_SOFTMAX):
+        shifted = logits - logits.max(axis=-1, keepdims=True)
+        ex = np.exp(shifted)
+        return ex / ex.sum(axis=-1, keepdims=True)
+    if gating == GATING_SIGMOID:
+        return 1.0 / (1.0 + np.exp(-logits)) + sigmoid_eps
+    raise ValueError(f"unknown gating {gating}")
+
+
+def selection_keys(logits: np.ndarray, scores: np.ndarray, gating: int,
+                   score_bias: Optional[np.ndarray]) -> np.ndarray:
+    """What top-k ranks: logits (+score_bias) for topk_softmax, else scores (+score_bias)."""
+    base = logits if gating == GATING_TOPK_SOFTMAX else scores
+    if score_bias is None:
+        return np.array(base, np.float64, copy=True)
+    return base + np.asarray(score_bias, np.float64)[None, :]
+
+
+def top_k(keys: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the k largest keys per row, descending; equal keys: lower index first.
+
+    k == 1 is an argmax (first maximum), as the page takes ``max`` for one expert.
+    """
+    keys = np.asarray(keys, np.float64)
+    T, E = keys.shape
+    if k == 1:
+        return np.argmax(keys, axis=1).astype(np.int64)[:, None]
+    out = np.empty((T, k), np.int64)
+    expert_ids = np.arange(E)
+    for t in range(T):
+        # primary key: -keys (descending); secondary: expert index (ascending)
+        order = np.lexsort((expert_ids, -keys[t]))
+        out[t] = order[:k]
+    return out
+
+
+def routing_weights(logits: np.ndarray, scores: np.ndarray, idx: np.ndarray, gating: int) -> np.ndarray:
+    """Unbiased weights of the chosen experts.
+
+    topk_softmax: softmax over the selected logits only; otherwise the scores
+    gathered at the chosen indices (never the bias-shifted keys).
+    """
+    if gating == GATING_TOPK_SOFTMAX:
+        sel = np.take_along_axis(logits, idx, axis=1)
+        sel = sel - sel.max(axis=1, keepdims=True)
+        ex = np.exp(sel)
+        return ex / ex.sum(axis=1, keepdims=True)
+    return np.take_along_axis(scores, idx, axis=1).astype(np.float64)
+
+
+def normalise_and_scale(w: np.ndarray, cfg: OracleConfig) -> np.ndarray:
+    """Divide by the p-norm along the last axis, then the optional scalings in the page's order:
+    x top_k (restore_weight_scale), x expert_weight_scale, x (original_top_k / top_k) ** 0.5.
+    """
+    w = np.array(w, np.float64, copy=True)
+    p = cfg.normalize_expert_weights
+    if p:
+        norm = (np.abs(w) ** p).sum(axis=1, keepdims=True) ** (1.0 / p)
+        w = w / norm
+    if cfg.restore_weight_scale:
+        w = w * cfg.top_k
+    if cfg.expert_weight_scale:
+        w = w * cfg.expert_weight_scale
+    if cfg.original_top_k and cfg.original_top_k != cfg.top_k:
+        w = w * math.sqrt(cfg.original_top_k / cfg.top_k)
+    return w
+
+
+@dataclass
+class Routing:
+    logits: np.ndarray   # (T, E) float64
+    scores: np.ndarray   # (T, E) float64
+    keys: np.ndarray     # (T, E) float64, what top-k ranked
+    idx: np.ndarray      # (T, k) int64
+    weights: np.ndarray  # (T, k) float64, after normalisation and scaling
+
+
+def route(cfg: OracleConfig, x: np.ndarray, w_router: np.ndarray,
+          b_router: Optional[np.ndarray] = None, score_bias: Optional[np.ndarray] = None,
+          forced_idx: Optional[np.ndarray] = None) -> Routing:
+    """The router's forward (inference: no jitter).
+
+    ``forced_idx`` replaces the selection (for tokens whose choice is a
+    near-tie); weights are still this oracle's, computed for those indices.
+    """
+    logits = router_logits(x, w_router, b_router if cfg.router_bias else None)
+    scores = gate_scores(logits, cfg.gating, cfg.sigmoid_stability_epsilon)
+    keys = selection_keys(logits, scores, cfg.gating, score_bias if cfg.has_score_bias else None)
+    idx = top_k(keys, cfg.top_k) if forced_idx is None else np.asarray(forced_idx, np.int64)
+    w = routing_weights(logits, scores, idx, cfg.gating)
+    w = normalise_and_scale(w, cfg)
+    return Routing(logits, scores, keys, idx, w)
+
+
+# --------------------------------------------------------------------------
+# Permutation  [Olmo-core 3, §"Пересылка токенов между экспертами"]
+# --------------------------------------------------------------------------
+
+@dataclass
+class Permutation:
+    counts: np.ndarray        # (E,) tokens per expert (the histogram)
+    offsets: np.ndarray       # (E+1,) bins: exclusive cumulative sum of counts
+    gather_token: np.ndarray  # (R,) token index of permuted row p
+    scatter_pos: np.ndarray   # (R,) permuted row of assignment t*k + j
+
+
+def permute(idx: np.ndarray, num_experts: int) -> Permutation:
+    """Counting sort of the flat assignments t*k + j by expert.
+
+    Histogram, exclusive cumulative sum (the bins), then placement in
+    ascending flat order inside each expert's bin.
+    """
+    idx = np.asarray(idx, np.int64)
+    T, k = idx.shape
+    flat = idx.reshape(-1)
+    counts = np.zeros(num_experts, np.int64)
+    for e in flat:
+        counts[e] += 1
+    offsets = np.zeros(num_experts + 1, np.int64)
+    for e in range(num_experts):
+        offsets[e + 1] = offsets[e] + counts[e]
+    cursor = offsets[:-1].copy()
+    gather_token = np.empty(T * k, np.int64)
+    scatter_pos = np.empty(T * k, np.int64)
+    for f, e in enumerate(flat):
+        p = cursor[e]
+        cursor[e] += 1
+        gather_token[p] = f // k
+        scatter_pos[f] = p
+    return Permutation(counts, offsets, gather_token, scatter_pos)
+
+
+# --------------------------------------------------------------------------
+# Experts  [Olmo-core 3, §"Вычисления экспертов и точность", §"SwiGLU с квантизацией"]
+# --------------------------------------------------------------------------
+
+def silu(g: np.ndarray) -> np.ndarray:
+    return g / (1.0 + np.exp(-g))
+
+
+def swiglu_mlp(rows: np.ndarray, w_up: np.ndarray, w_gate: np.ndarray, w_out: np.ndarray) -> np.ndarray:
+    """y = W_out (silu(W_gate r) * (W_up r)) for each row r."""
+    u = rows @ w_up.T
+    g = rows @ w_gate.T
+    return (silu(g) * u) @ w_out.T
+
+
+def rms_norm(z: np.ndarray, eps: float, gamma: Optional[np.ndarray] = None) -> np.ndarray:
+    """Bias-free RMSNorm along the last axis."""
+    z = np.asarray(z, np.float64)
+    inv = 1.0 / np.sqrt((z * z).mean(axis=-1, keepdims=True) + eps)
+    out = z * inv
+    if gamma is not None:
+        out = out * np.asarray(gamma, np.float64)
+    return out
+
+
+ExpertFn = Callable[[int], Sequence[np.ndarray]]
+
+
+@dataclass
+class OracleWeights:
+    """Layer weights as float64 (or a per-expert provider for large layers).
+
+    expert(e) -> (w_up (h, L), w_gate (h, L), w_out (L, h)).
+    """
+
+    w_router: np.ndarray
+    expert: ExpertFn
+    b_router: Optional[np.ndarray] = None
+    score_bias: Optional[np.ndarray] = None
+    w_down_latent: Optional[np.ndarray] = None   # (L, D)
+    w_up_latent: Optional[np.ndarray] = None     # (D, L)
+    rms_weight: Optional[np.ndarray] = None      # (L,) or None for ones
+
+
+@dataclass
+class LayerResult:
+    routing: Routing
+    perm: Permutation
+    x_routed: np.ndarray  # (T, L) input of the experts
+    y: np.ndarray         # (R, L) expert outputs in permuted order
+    z: np.ndarray         # (T, L) weighted combine
+    out: np.ndarray       # (T, D)
+
+
+def layer_forward(cfg: OracleConfig, x: np.ndarray, wts: OracleWeights,
+                  forced_idx: Optional[np.ndarray] = None) -> LayerResult:
+    """The MoE layer forward, step by step.
+
+    1. prepare_routed_input: latent down-projection (identity when not latent).
+    2. router on the layer input x.
+    3. permutation into per-expert bins.
+    4. each expert's SwiGLU MLP on its bin.
+    5. weighted un-permute / combine.
+    6. restore_routed_output: RMSNorm then up-projection (identity when not latent).
+    """
+    x = np.asarray(x, np.float64)
+    if cfg.is_latent:
+        x_routed = x @ np.asarray(wts.w_down_latent, np.float64).T
+    else:
+        x_routed = x
+    r = route(cfg, x, wts.w_router, wts.b_router, wts.score_bias, forced_idx)
+    T, k = r.idx.shape
+    perm = permute(r.idx, cfg.num_experts)
+    L = x_routed.shape[1]
+    y = np.zeros((T * k, L), np.float64)
+    for e in range(cfg.num_experts):
+        lo, hi = int(perm.offsets[e]), int(perm.offsets[e + 1])
+        if hi == lo:
+            continue
+        w_up, w_gate, w_out = (np.asarray(a, np.float64) for a in wts.expert(e))
+        y[lo:hi] = swiglu_mlp(x_routed[perm.gather_token[lo:hi]], w_up, w_gate, w_out)
+    z = np.zeros((T, L), np.float64)
+    for j in range(k):
+        z += r.weights[:, j:j + 1] * y[perm.scatter_pos[np.arange(T) * k + j]]
+    if cfg.is_latent:
+        n = rms_norm(z, cfg.rms_eps, wts.rms_weight) if cfg.up_proj_norm else z
+        out = n @ np.asarray(wts.w_up_latent, np.float64).T
+    else:
+        out = z
+    return LayerResult(r, perm, x_routed, y, z, out)
+

@@ -1,0 +1,56 @@
+"""Test-side glue: turn a drawn workload into the oracle's config and float64 weights."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import moe_ref as ref
+from token_routing_expert_gb300.workloads import GATING_NAMES, WorkloadSpec
+
+
+def f64(t):
+    if t is None:
+        return None
+    return t.to(torch.float64).numpy()
+
+
+def oracle_config(spec: WorkloadSpec) -> ref.OracleConfig:
+    return ref.OracleConfig(
+        d_model=spec.d_model, num_experts=spec.num_experts, top_k=spec.top_k,
+        hidden_size=spec.hidden_size, latent_dim=spec.latent_dim,
+        up_proj_norm=spec.up_proj_norm, rms_eps=spec.rms_eps,
+        gating=GATING_NAMES[spec.gating],
+        sigmoid_stability_epsilon=spec.sigmoid_stability_epsilon,
+        normalize_expert_weights=spec.normalize_expert_weights,
+        restore_weight_scale=spec.restore_weight_scale,
+        expert_weight_scale=spec.expert_weight_scale,
+        original_top_k=spec.original_top_k,
+        router_bias=spec.skew, has_score_bias=spec.score_bias_std > 0)
+
+
+def oracle_weights(spec: WorkloadSpec, inp) -> ref.OracleWeights:
+    h = spec.hidden_size
+    w_ug, w_o = inp["w_up_gate"], inp["w_out"]
+
+    def expert(e):
+        ug = f64(w_ug[e])
+        return ug[:h], ug[h:], f64(w_o[e])
+
+    return ref.OracleWeights(
+        w_router=f64(inp["w_router"]), expert=expert, b_router=f64(inp["b_router"]),
+        score_bias=f64(inp["score_bias"]), w_down_latent=f64(inp["w_down"]),
+        w_up_latent=f64(inp["w_up_latent"]))
+
+
+def near_tie_tokens(keys: np.ndarray, k: int, gap: float = 1e-5) -> np.ndarray:
+    """Tokens whose top-(k+1) sorted keys have a consecutive gap below ``gap``.
+
+    Such a token's choice or order may legitimately differ between float32
+    and float64 evaluation.
+    """
+    T, E = keys.shape
+    m = min(k + 1, E)
+    part = -np.sort(-keys, axis=1)[:, :m]
+    if m < 2:
+        return np.zeros(T, bool)
+    return (np.diff(-part, axis=1) < gap).any(axis=1)

@@ -1,0 +1,104 @@
+"""Planted mistakes in the oracle (on the CPU) must each fail one of its pins.
+
+Each case swaps one oracle function for a plausible wrong version and runs
+the pin that should catch it.
+"""
+import numpy as np
+import pytest
+
+from oracle import moe_ref as ref
+from tests import test_oracle_layer as L
+from tests import test_oracle_permute as P
+from tests import test_oracle_router as R
+
+_ORIG_PERMUTE = ref.permute
+_ORIG_GATE_SCORES = ref.gate_scores
+_ORIG_TOP_K = ref.top_k
+
+
+def _silu_dropped(g):
+    return g
+
+
+def _swapped_swiglu(rows, w_up, w_gate, w_out):
+    u = rows @ w_gate.T
+    g = rows @ w_up.T
+    return (ref.silu(g) * u) @ w_out.T
+
+
+def _weights_from_keys(logits, scores, idx, gating):
+    # wrong: gathers the bias-shifted keys instead of the scores
+    keys = ref.selection_keys(logits, scores, gating, _weights_from_keys.bias)
+    return np.take_along_axis(keys, idx, axis=1)
+
+
+_weights_from_keys.bias = np.array([1.0, 0.0, 0.0, -1.0])
+
+
+def _topk_full_softmax(logits, scores, idx, gating):
+    # wrong: topk_softmax weights taken from the softmax over all experts
+    return np.take_along_axis(scores, idx, axis=1)
+
+
+def _topk_high_index_wins(keys, k):
+    # wrong: equal keys resolved in favour of the higher expert index
+    E = keys.shape[1]
+    rev = _ORIG_TOP_K(keys[:, ::-1], k)
+    return (E - 1) - rev
+
+
+def _unstable_permute(idx, E):
+    # wrong: each expert's bin in reverse flat order
+    p = _ORIG_PERMUTE(idx, E)
+    g = p.gather_token.copy()
+    s = np.empty_like(p.scatter_pos)
+    flat = np.asarray(idx).reshape(-1)
+    for e in range(E):
+        lo, hi = p.offsets[e], p.offsets[e + 1]
+        g[lo:hi] = p.gather_token[lo:hi][::-1]
+    for f in range(flat.size):
+        e = flat[f]
+        lo, hi = p.offsets[e], p.offsets[e + 1]
+        s[f] = lo + hi - 1 - p.scatter_pos[f]
+    return ref.Permutation(p.counts, p.offsets, g, s)
+
+
+def _rms_sum(z, eps, gamma=None):
+    z = np.asarray(z, np.float64)
+    return z / np.sqrt((z * z).sum(axis=-1, keepdims=True) + eps)
+
+
+def _scale_then_normalise(w, cfg):
+    w = np.array(w, np.float64)
+    if cfg.restore_weight_scale:
+        w = w * cfg.top_k
+    p = cfg.normalize_expert_weights
+    if p:
+        w = w / (np.abs(w) ** p).sum(axis=1, keepdims=True) ** (1.0 / p)
+    return w
+
+
+def _no_epsilon_scores(logits, gating, sigmoid_eps=0.0):
+    # wrong: the stability epsilon is dropped
+    return _ORIG_GATE_SCORES(logits, gating, 0.0)
+
+
+CASES = [
+    ("silu", _silu_dropped, lambda: L.test_single_expert_is_dense_swiglu_mlp()),
+    ("swiglu_mlp", _swapped_swiglu, lambda: L.test_single_expert_is_dense_swiglu_mlp()),
+    ("routing_weights", _weights_from_keys, lambda: R.test_sigmoid_bias_for_selection_only()),
+    ("routing_weights", _topk_full_softmax,
+     lambda: R.test_topk_softmax_selects_on_biased_logits_and_weights_on_selected_logits()),
+    ("top_k", _topk_high_index_wins, lambda: R.test_topk_ties_lower_index_first(6, 3)),
+    ("permute", _unstable_permute, lambda: P.test_permutation_matches_stable_argsort(64, 8, 16)),
+    ("rms_norm", _rms_sum, lambda: L.test_rms_norm_matches_library()),
+    ("normalise_and_scale", _scale_then_normalise, lambda: R.test_normalisation_and_scalings(ref.GATING_SIGMOID)),
+    ("gate_scores", _no_epsilon_scores, lambda: R.test_sigmoid_scores_match_library_plus_epsilon()),
+]
+
+
+@pytest.mark.parametrize("name,bad,pin", CASES, ids=[f"{c[0]}-{c[1].__name__}" for c in CASES])
+def test_planted_mistake_is_caught(monkeypatch, name, bad, pin):
+    monkeypatch.setattr(ref, name, bad)
+    with pytest.raises(AssertionError):
+        pin()

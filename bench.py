@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Benchmark of the MoE layer forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl native|reference]
+
+A step is one moe_layer_forward (latent down-projection, router GEMM, top-k,
+permutation, grouped SwiGLU GEMMs, combine, RMSNorm + up-projection) over
+one batch of T synthetic tokens resident in HBM.  The default workload is
+the OlmoE-shaped layer (T=8192, d_model=2048, 64 experts, top-8, hidden
+1024, topk_softmax gating).  With N > 1 (torchrun), every rank runs its own
+replica on its own batch: tokens are independent, so there is no collective
+on the data path (weak scaling); the barrier and the max over ranks are the
+only communication.
+
+``--impl reference`` times the float64 CPU oracle, as it stands, on a
+bounded sample of the same workload on the host cores (rank 0 only).
+
+Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from token_routing_expert_gb300 import workloads as W  # noqa: E402
+
+METRIC = "MoE layer fwd tokens/s and TFLOP/s (frac of bf16 peak); decode GB/s vs HBM peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(spec: W.WorkloadSpec) -> str:
+    s = (f"{spec.name}: T={spec.T} d_model={spec.d_model} experts={spec.num_experts} top_k={spec.top_k} "
+         f"hidden={spec.hidden_size} gating={spec.gating}")
+    if spec.latent_dim:
+        s += f" latent_dim={spec.latent_dim} rmsnorm"
+    if spec.score_bias_std:
+        s += f" score_bias~N(0,{spec.score_bias_std})"
+    if spec.normalize_expert_weights:
+        s += f" p={spec.normalize_expert_weights:g}"
+    if spec.restore_weight_scale:
+        s += " restore_weight_scale"
+    if spec.skew:
+        s += " skewed_load"
+    return s
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 20 ms; keeps the samples inside [t0, t1]."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def stop(self, t0: float, t1: float):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        inside = [r for r in rows if t0 - 0.02 <= r[0] <= t1 + 0.02]
+        window = "timed region"
+        if not inside:  # region shorter than the sampling period: nearest samples
+            inside = sorted(rows, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))[:3]
+            window = "nearest samples to a short timed region"
+        reasons = sorted({self.REASONS[i] for r in inside for i in range(4) if r[3][i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": reasons, "samples": len(inside), "window": window}
+
+
+def kernel_traffic(workload: str):
+    """Per-launch DRAM bytes of the grouped SwiGLU GEMM from the committed ncu summary,
+    if the kernel source has not changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", f"grouped_gemm1_swiglu_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "token_routing_expert_gb300", "csrc", "gemm_tc.cu")
+    digest = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    if vals.get("gemm_tc_cu_sha256") != digest or "dram_bytes_per_launch" not in vals:
+        return None
+    return float(vals["dram_bytes_per_launch"])
+
+
+def oracle_sample_rate(spec: W.WorkloadSpec, inp, n_tokens: int, min_seconds: float, max_reps: int = 50):
+    """Times the float64 oracle on the first n_tokens tokens; returns (tokens/s, reps, seconds)."""
+    from oracle import moe_ref as ref  # the CPU baseline leg is the only user of the oracle here
+
+    h = spec.hidden_size
+
+    def f64(t):
+        return None if t is None else t.to(torch.float64).numpy()
+
+    cfg = ref.OracleConfig(d_model=spec.d_model, num_experts=spec.num_experts, top_k=spec.top_k, hidden_size=h,
+                           latent_dim=spec.latent_dim, up_proj_norm=spec.up_proj_norm, rms_eps=spec.rms_eps,
+                           gating=W.GATING_NAMES[spec.gating],
+                           sigmoid_stability_epsilon=spec.sigmoid_stability_epsilon,
+                           normalize_expert_weights=spec.normalize_expert_weights,
+                           restore_weight_scale=spec.restore_weight_scale,
+                           expert_weight_scale=spec.expert_weight_scale, original_top_k=spec.original_top_k,
+                           router_bias=spec.skew, has_score_bias=spec.score_bias_std > 0)
+    wug, wo = inp["w_up_gate"], inp["w_out"]
+    wts = ref.OracleWeights(w_router=f64(inp["w_router"]),
+                            expert=lambda e: (f64(wug[e][:h]), f64(wug[e][h:]), f64(wo[e])),
+                            b_router=f64(inp["b_router"]), score_bias=f64(inp["score_bias"]),
+                            w_down_latent=f64(inp["w_down"]), w_up_latent=f64(inp["w_up_latent"]))
+    x = f64(inp["x"][:n_tokens])
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        ref.layer_forward(cfg, x, wts)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= min_seconds or reps >= max_reps:
+            break
+    return n_tokens * reps / el, reps, el
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    spec = W.WORKLOADS[args.config]
+    inp = W.generate(spec)
+    n = min(spec.T, args.ref_tokens)
+    for _ in range(args.warmup):
+        oracle_sample_rate(spec, inp, n, 0.0, max_reps=1)
+    rates = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        r, _, _ = oracle_sample_rate(spec, inp, n, 0.0, max_reps=1)
+        rates.append(r)
+    el = time.perf_counter() - t_all
+    value = n * args.steps / el
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_desc(spec), "T": spec.T, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} of {spec.T} tokens per step, full layer in float64 numpy"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def run_native(args):
+    from token_routing_expert_gb300 import native
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    native.load()
+    spec = W.WORKLOADS[args.config]
+    # each rank draws its own batch of tokens (weak scaling); weights are shared replicas
+    inp = W.generate(spec)
+    if world > 1 and rank > 0:
+        inp["x"] = W.generate(spec.with_(seed=spec.seed * 1000 + rank), experts=False)["x"]
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp)
+    T = spec.T
+    x = inp["x"].cuda()
+    ws = native.workspace(cfg, T)
+    out = torch.empty((T, spec.d_model), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    # working set: does it exceed L2?  (otherwise flush L2 between steps)
+    L2 = torch.cuda.get_device_properties(local).L2_cache_size
+    for _ in range(max(args.warmup, 1)):
+        native.moe_layer_forward(cfg, wts, x, ws, out=out)
+    torch.cuda.synchronize()
+    if native.moe_get_status() != 0:
+        raise SystemExit("device status error during warm-up")
+    inter = native.layer_intermediates(cfg, T, ws)
+    touched = int((inter["counts"] > 0).sum().item())
+    alg_bytes = W.algorithmic_bytes(spec, touched)
+    flush = alg_bytes < 2 * L2
+    flush_buf = torch.empty(2 * L2 // 4 + 1024, dtype=torch.float32, device="cuda") if flush else None
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(10)] for _ in range(args.steps)]
+    for row in evs:  # create the underlying CUDA events
+        for e in row:
+            e.record(stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local).start() if rank == 0 else None
+    time.sleep(0.5 if clocks else 0)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        if flush:
+            flush_buf.fill_(float(i))
+        native.moe_layer_forward_staged(cfg, wts, x, ws, evs[i], out=out)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    time.sleep(0.1 if clocks else 0)
+    clock_info = clocks.stop(t_wall0, t_wall1) if clocks else None
+    if native.moe_get_status() != 0:
+        raise SystemExit("device status error in the timed region")
+
+    step_ms = [evs[i][0].elapsed_time(evs[i][9]) for i in range(args.steps)]
+    ms = sum(step_ms) / args.steps if flush else start.elapsed_time(end) / args.steps
+    stage_ms = {}
+    for s, name in enumerate(native.STAGES, start=1):
+        stage_ms[name] = sum(evs[i][s - 1].elapsed_time(evs[i][s]) for i in range(args.steps)) / args.steps
+    if dist is not None:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # end to end: pinned host input -> device, forward, output -> pinned host, every step
+    x_host = inp["x"].pin_memory()
+    out_host = torch.empty((T, spec.d_model), dtype=torch.bfloat16).pin_memory()
+    x_dev = torch.empty_like(x)
+    for _ in range(2):
+        x_dev.copy_(x_host, non_blocking=True)
+        native.moe_layer_forward(cfg, wts, x_dev, ws, out=out)
+        out_host.copy_(out, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        if flush:
+            flush_buf.fill_(float(i))
+        x_dev.copy_(x_host, non_blocking=True)
+        native.moe_layer_forward(cfg, wts, x_dev, ws, out=out)
+        out_host.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if dist is not None:
+        t = torch.tensor([e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if native.moe_get_status() != 0:
+        raise SystemExit("device status error in the end-to-end region")
+
+    peaks, peak_kind = read_peaks()
+    flops = W.algorithmic_flops(spec)
+    tflops = flops / (ms * 1e-3) / 1e12
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    gemm1_flops = 4 * spec.rows * spec.routed_dim * spec.hidden_size
+    gemm1_ms = stage_ms["grouped_gemm1_swiglu"]
+    achieved = gemm1_flops / (gemm1_ms * 1e-3) / 1e12
+    peak_tf = peaks["bf16_tflops"]
+    bound_layer = "hbm" if (alg_bytes / (peaks["hbm_gbs"] * 1e9)) > (flops / (peak_tf * 1e12)) else "tensor"
+    roof_ms = 1e3 * max(alg_bytes / (peaks["hbm_gbs"] * 1e9), flops / (peak_tf * 1e12))
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": world * T / (ms * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded numpy PCG64 normals rounded to bf16; random-init weights)",
+        "config": {"workload": workload_desc(spec), "T_per_gpu": T, "global_tokens": world * T,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": ("flushed between steps (working set below 2x L2)" if flush else
+                          f"no flush: algorithmic bytes per step {alg_bytes / 1e6:.0f} MB > L2 "
+                          f"{L2 / 1e6:.0f} MB")},
+        "layer": {"tflops": tflops, "frac_bf16_peak": tflops / peak_tf, "gbs": gbs,
+                  "frac_hbm_peak": gbs / peaks["hbm_gbs"], "bound": bound_layer,
+                  "roofline_ms": roof_ms, "frac_of_roofline": roof_ms / ms, "experts_touched": touched,
+                  "algorithmic_flops": flops, "algorithmic_bytes": alg_bytes},
+        "stages_ms": stage_ms,
+        "roofline": {"kernel": "grouped GEMM 1 (SwiGLU fused, tcgen05)", "bound": "tensor",
+                     "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
+                     "traffic": kernel_traffic(spec.name),
+                     "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)" if peak_kind == "measured"
+                     else "fallback 1.9 PFLOP/s bf16"},
+        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
+        "gpu_launches": args.steps * native.moe_layer_forward_launches(cfg, T),
+        "clocks": clock_info,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        n = min(T, args.cpu_tokens)
+        rate, reps, secs = oracle_sample_rate(spec, inp, n, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"first {n} of {T} tokens, full float64 layer, {reps} reps in "
+                                          f"{secs:.1f} s (numpy BLAS on all host cores)"}
+    print(json.dumps(line))
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default="olmoe", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--ref-tokens", type=int, default=256, help="oracle tokens per step (reference arm)")
+    ap.add_argument("--cpu-tokens", type=int, default=512, help="oracle sample for the cpu_baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,239 @@
+/*
+ * moe.h — C ABI of the GB300 (sm_103a) routed / latent Mixture-of-Experts
+ * layer forward.
+ *
+ * The operations follow the page "Как устроен Olmo-core 3: обучение больших
+ * MoE-моделей" (sarnas.ru); each entry point names the section it implements.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ *  - Pointers named "device" point to GPU memory the caller allocated; the
+ *    library never allocates, frees or retains them past the call.
+ *  - Every array is dense row-major.  Activations and weights are bf16
+ *    (passed as void*), logits / routing weights / biases are fp32, indices
+ *    are int32.  Weights follow the linear-layer layout (out, in).
+ *  - Device work is enqueued on `stream` and is asynchronous; no entry point
+ *    synchronises, except moe_get_status.
+ *  - `ws` is a caller-owned device workspace of at least
+ *    moe_workspace_size(cfg, T) bytes, 256-byte aligned.  Its contents on
+ *    entry are irrelevant; entry points overwrite parts of it.
+ *  - Return value: MOE_OK, or an error code for bad arguments detected on the
+ *    host (nothing is enqueued then) or a launch failure.  Errors found on
+ *    the device (an expert index out of range, a pipeline wait that ran out
+ *    of time) are recorded in a per-device status word that moe_get_status
+ *    reads; a kernel that records an error skips the bad access and returns.
+ *  - Calls on one stream are ordered; concurrent calls sharing one workspace
+ *    on different streams race.
+ */
+#ifndef MOE_GB300_H_
+#define MOE_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same handle as cudaStream_t; NULL = legacy default stream */
+
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1, /* null pointer, negative size, inconsistent config */
+  MOE_ERR_UNSUPPORTED = 2, /* valid per the page but outside this library's kernels (see moe_validate_config) */
+  MOE_ERR_WORKSPACE = 3,   /* ws smaller than moe_workspace_size, or misaligned */
+  MOE_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  MOE_ERR_TIMEOUT = 5,     /* device: a pipeline wait ran out of time (kernel returned early) */
+  MOE_ERR_BOUNDS = 6,      /* device: an index outside its range was met and skipped */
+  MOE_ERR_NO_DEVICE = 7    /* no usable sm_103 device for this call */
+};
+
+/* Gating functions, section "Маршрутизация: как роутер выбирает экспертов". */
+typedef enum {
+  MOE_GATING_SOFTMAX = 0,      /* scores = softmax(logits) over experts; weights gathered from scores */
+  MOE_GATING_TOPK_SOFTMAX = 1, /* select on logits (+score_bias); weights = softmax over selected logits */
+  MOE_GATING_SIGMOID = 2       /* scores = sigmoid(logits) + sigmoid_stability_epsilon, per expert */
+} moe_gating_t;
+
+/*
+ * Layer configuration: the fields of MoEConfig / MoERouterConfigV2 (section
+ * "Как задаётся конфигурация MoE") and LatentMoEConfig (section "Латентная
+ * проекция экспертов").  A zero in an optional field means "unset".
+ */
+typedef struct {
+  int32_t d_model;     /* D: model width */
+  int32_t num_experts; /* E: routed experts */
+  int32_t top_k;       /* k: experts per token */
+  int32_t hidden_size; /* h: expert MLP width */
+  int32_t latent_dim;  /* L: 0 = no latent MoE (experts run in d_model) */
+  int32_t up_proj_norm;/* latent only: 1 = bias-free RMSNorm before the up-projection, 0 = none */
+  float rms_eps;       /* RMSNorm epsilon (the page gives none; 1e-6 is this library's default) */
+  int32_t gating;      /* moe_gating_t */
+  float sigmoid_stability_epsilon; /* added to sigmoid scores; 0 = unset */
+  float normalize_expert_weights;  /* p of the p-norm dividing the weights; 0 = unset */
+  int32_t restore_weight_scale;    /* 1: weights x top_k after normalisation */
+  float expert_weight_scale;       /* weights x this; 0 = unset */
+  int32_t original_top_k;          /* != top_k and > 0: weights x sqrt(original_top_k / top_k) */
+  int32_t router_bias;             /* 1: the router linear layer has a bias (E fp32) */
+  int32_t has_score_bias;          /* 1: a score_bias (E fp32) is added for selection only */
+  int32_t activation;              /* 0 = swiglu (the only expert activation supported) */
+} moe_config_t;
+
+/*
+ * Device pointers to the layer's weights (bf16 unless noted).
+ */
+typedef struct {
+  const void* w_router;      /* (E, D) */
+  const float* b_router;     /* (E) fp32; read only when cfg.router_bias */
+  const float* score_bias;   /* (E) fp32; read only when cfg.has_score_bias */
+  const void* w_down_latent; /* (L, D); latent only */
+  const void* w_up_latent;   /* (D, L); latent only */
+  const void* rms_weight;    /* (L) bf16 gain, or NULL for ones; latent with up_proj_norm only */
+  const void* w_up_gate;     /* (E, 2h, L'): per expert rows [0,h) = up, rows [h,2h) = gate; L' = L or D */
+  const void* w_out;         /* (E, L', h): expert down-projection */
+} moe_weights_t;
+
+/* ---- host-only functions (no device, no stream) ------------------------- */
+
+/* Checks a configuration.  MOE_ERR_INVALID_ARG: sizes < 1, top_k > num_experts,
+ * unknown gating, negative options.  MOE_ERR_UNSUPPORTED: activation != swiglu,
+ * d_model / latent_dim / hidden_size not multiples of 64, num_experts > 1024,
+ * top_k > 32. */
+int moe_validate_config(const moe_config_t* cfg);
+
+/* Total parameters: router (D*E, +E with a router bias) + 3 * L' * h * E
+ * (section "Как задаётся конфигурация MoE"; L' = latent_dim or d_model).
+ * The latent projections are not part of it; see moe_latent_proj_params. */
+int moe_num_params(const moe_config_t* cfg, int64_t* out);
+
+/* Active parameters per token: total - 3*L'*h*E + 3*L'*h*top_k (same section). */
+int moe_num_active_params(const moe_config_t* cfg, int64_t* out);
+
+/* Latent down- and up-projection weights: 2 * d_model * latent_dim (+ L with an RMSNorm gain). */
+int moe_latent_proj_params(const moe_config_t* cfg, int with_norm_gain, int64_t* out);
+
+/* Workspace bytes that every entry point below needs for T tokens. */
+int moe_workspace_size(const moe_config_t* cfg, int64_t T, size_t* bytes);
+
+/* ---- device entry points ------------------------------------------------ */
+
+/*
+ * Router, section "Маршрутизация: как роутер выбирает экспертов".
+ * logits = x W_router^T (+ b_router) in fp32; scores by the gating function;
+ * top-k on the selection key (score, or logit for topk_softmax, + score_bias),
+ * descending, equal keys -> lower expert index first (section "Разрешение
+ * равенства логитов и квантизация"); weights from the unbiased scores (or a
+ * softmax over the selected logits); p-norm normalisation and the scalings
+ * restore_weight_scale, expert_weight_scale, original_top_k in that order.
+ *   x       device (T, D) bf16
+ *   logits  device (T, E) fp32 output, or NULL to keep them in ws only
+ *   idx     device (T, k) int32 output: chosen experts, best first
+ *   weights device (T, k) fp32 output: routing weights matching idx
+ */
+int moe_router(const moe_config_t* cfg, const moe_weights_t* w, const void* x, int64_t T, float* logits,
+               int32_t* idx, float* weights, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Token permutation, section "Пересылка токенов между экспертами", and the
+ * tokens-per-expert histogram, section "Балансировка нагрузки и
+ * вспомогательные штрафы".  Assignment f = t*k + j (token t, choice j) goes
+ * to expert idx[f]; rows are grouped by expert, ascending f inside a group.
+ *   idx         device (T, k) int32 input, values in [0, E) (others: MOE_ERR_BOUNDS, skipped)
+ *   counts      device (E) int32 output: assignments per expert
+ *   offsets     device (E+1) int32 output: exclusive prefix sum of counts (the bins)
+ *   gather_idx  device (T*k) int32 output: token of permuted row p
+ *   scatter_idx device (T*k) int32 output: permuted row of assignment f
+ */
+int moe_permute(const moe_config_t* cfg, const int32_t* idx, int64_t T, int32_t* counts, int32_t* offsets,
+                int32_t* gather_idx, int32_t* scatter_idx, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Grouped SwiGLU experts, sections "Вычисления экспертов и точность" and
+ * "SwiGLU с квантизацией": for permuted row p of expert e's group
+ * [offsets[e], offsets[e+1]):  u = W_up[e] r, g = W_gate[e] r with
+ * r = x_routed[gather_idx[p]];  H = silu(g) * u rounded to bf16;
+ * y[p] = W_out[e] H rounded to bf16 (the experts return bf16).
+ *   x_routed   device (T, L') bf16: the experts' input (x, or the latent projection)
+ *   gather_idx device (T*k) int32, offsets device (E+1) int32 (as from moe_permute)
+ *   y          device (T*k, L') bf16 output, permuted row order
+ */
+int moe_grouped_swiglu(const moe_config_t* cfg, const moe_weights_t* w, const void* x_routed,
+                       const int32_t* gather_idx, const int32_t* offsets, int64_t T, void* y, void* ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * Weighted un-permute / combine, section "Пересылка токенов между экспертами":
+ * z[t] = sum_j weights[t, j] * y[scatter_idx[t*k + j]], accumulated in fp32, stored bf16.
+ *   y device (T*k, L') bf16, scatter_idx device (T*k) int32, weights device (T, k) fp32
+ *   z device (T, L') bf16 output
+ */
+int moe_combine(const moe_config_t* cfg, const void* y, const int32_t* scatter_idx, const float* weights,
+                int64_t T, void* z, moe_stream_t stream);
+
+/*
+ * prepare_routed_input, section "Латентная проекция экспертов":
+ * x_routed = x W_down^T (fp32 accumulate, bf16 out).  Latent configs only.
+ *   x device (T, D) bf16;  x_routed device (T, L) bf16 output
+ */
+int moe_latent_down(const moe_config_t* cfg, const moe_weights_t* w, const void* x, int64_t T, void* x_routed,
+                    void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * restore_routed_output, section "Латентная проекция экспертов":
+ * n = z / sqrt(mean(z^2) + rms_eps) * gain in fp32, cast to bf16 (the
+ * up-projection's dtype), out = n W_up^T.  Without up_proj_norm, n = z.
+ * Latent configs only.
+ *   z device (T, L) bf16;  out device (T, D) bf16 output
+ */
+int moe_latent_restore(const moe_config_t* cfg, const moe_weights_t* w, const void* z, int64_t T, void* out,
+                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * The whole layer forward: [latent down] -> router -> permutation -> grouped
+ * SwiGLU experts -> weighted combine -> [RMSNorm + latent up].  No host
+ * synchronisation: per-expert counts stay on the device.
+ *   x device (T, D) bf16;  out device (T, D) bf16 output (may not alias x)
+ * Intermediate results stay in ws; moe_workspace_layout reports where.
+ */
+int moe_layer_forward(const moe_config_t* cfg, const moe_weights_t* w, const void* x, int64_t T, void* out,
+                      void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_layer_forward with stage timing: when stage_events is not NULL it
+ * points to 10 cudaEvent_t handles (created by the caller on the current
+ * device; a NULL handle is skipped) that are recorded on `stream` at the
+ * stage boundaries:
+ *   [0] start, [1] after the latent down-projection, [2] after the router
+ *   GEMM, [3] after top-k, [4] after the permutation, [5] after the row
+ *   gather, [6] after grouped GEMM 1 (SwiGLU), [7] after grouped GEMM 2,
+ *   [8] after the combine (+ RMSNorm), [9] after the latent up-projection.
+ * Stages that a configuration does not have record at the same point as the
+ * previous boundary.  Results are identical to moe_layer_forward.
+ */
+int moe_layer_forward_staged(const moe_config_t* cfg, const moe_weights_t* w, const void* x, int64_t T, void* out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream, void* const* stage_events);
+
+/* Host only: number of kernels one moe_layer_forward launches for T tokens on
+ * the current device (the split-K choices depend on its SM count). */
+int moe_layer_forward_launches(const moe_config_t* cfg, int64_t T, int32_t* n);
+
+/* Byte offsets in ws of the layer forward's intermediates, for inspection:
+ * [0] router GEMM output (split-K partial logits without the router bias),
+ * [1] idx (T,k) int32, [2] weights (T,k) fp32,
+ * [3] counts (E), [4] offsets (E+1), [5] gather_idx (T*k), [6] scatter_idx (T*k),
+ * [7] x_routed (T,L) bf16 (latent only, else -1), [8] y (T*k, L') bf16,
+ * [9] z or normalised z (T, L') bf16 (latent only, else -1). */
+int moe_workspace_layout(const moe_config_t* cfg, int64_t T, int64_t offsets_out[10]);
+
+/* Synchronises `stream`, then returns (and clears, if `clear`) the device
+ * status word of the current device in *device_status. */
+int moe_get_status(moe_stream_t stream, int32_t* device_status, int clear);
+
+/* Static, human-readable name of a status code. */
+const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H_ */

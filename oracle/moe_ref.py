@@ -325,6 +325,48 @@ class LayerResult:
     out: np.ndarray       # (T, D)
 
 
+def prepare_routed_input(cfg: OracleConfig, x: np.ndarray, w_down_latent: Optional[np.ndarray]) -> np.ndarray:
+    """Latent down-projection (*, d_model) -> (*, latent_dim); identity when not latent."""
+    x = np.asarray(x, np.float64)
+    if not cfg.is_latent:
+        return x
+    return x @ np.asarray(w_down_latent, np.float64).T
+
+
+def expert_outputs(cfg: OracleConfig, x_routed: np.ndarray, perm: Permutation, expert: ExpertFn) -> np.ndarray:
+    """y[p] = expert e's SwiGLU MLP of the token in permuted row p, for each bin e."""
+    x_routed = np.asarray(x_routed, np.float64)
+    y = np.zeros((perm.gather_token.size, x_routed.shape[1]), np.float64)
+    for e in range(cfg.num_experts):
+        lo, hi = int(perm.offsets[e]), int(perm.offsets[e + 1])
+        if hi == lo:
+            continue
+        w_up, w_gate, w_out = (np.asarray(a, np.float64) for a in expert(e))
+        y[lo:hi] = swiglu_mlp(x_routed[perm.gather_token[lo:hi]], w_up, w_gate, w_out)
+    return y
+
+
+def combine(y: np.ndarray, scatter_pos: np.ndarray, weights: np.ndarray) -> np.ndarray:
+    """z[t] = sum_j weights[t, j] * y[scatter_pos[t*k + j]]: scatter back and weight."""
+    y = np.asarray(y, np.float64)
+    weights = np.asarray(weights, np.float64)
+    T, k = weights.shape
+    z = np.zeros((T, y.shape[1]), np.float64)
+    for j in range(k):
+        z += weights[:, j:j + 1] * y[np.asarray(scatter_pos)[np.arange(T) * k + j]]
+    return z
+
+
+def restore_routed_output(cfg: OracleConfig, z: np.ndarray, w_up_latent: Optional[np.ndarray],
+                          rms_weight: Optional[np.ndarray] = None) -> np.ndarray:
+    """RMSNorm (if configured), then the up-projection (*, latent_dim) -> (*, d_model); identity when not latent."""
+    z = np.asarray(z, np.float64)
+    if not cfg.is_latent:
+        return z
+    n = rms_norm(z, cfg.rms_eps, rms_weight) if cfg.up_proj_norm else z
+    return n @ np.asarray(w_up_latent, np.float64).T
+
+
 def layer_forward(cfg: OracleConfig, x: np.ndarray, wts: OracleWeights,
                   forced_idx: Optional[np.ndarray] = None) -> LayerResult:
     """The MoE layer forward, step by step.
@@ -337,28 +379,10 @@ def layer_forward(cfg: OracleConfig, x: np.ndarray, wts: OracleWeights,
     6. restore_routed_output: RMSNorm then up-projection (identity when not latent).
     """
     x = np.asarray(x, np.float64)
-    if cfg.is_latent:
-        x_routed = x @ np.asarray(wts.w_down_latent, np.float64).T
-    else:
-        x_routed = x
+    x_routed = prepare_routed_input(cfg, x, wts.w_down_latent)
     r = route(cfg, x, wts.w_router, wts.b_router, wts.score_bias, forced_idx)
-    T, k = r.idx.shape
     perm = permute(r.idx, cfg.num_experts)
-    L = x_routed.shape[1]
-    y = np.zeros((T * k, L), np.float64)
-    for e in range(cfg.num_experts):
-        lo, hi = int(perm.offsets[e]), int(perm.offsets[e + 1])
-        if hi == lo:
-            continue
-        w_up, w_gate, w_out = (np.asarray(a, np.float64) for a in wts.expert(e))
-        y[lo:hi] = swiglu_mlp(x_routed[perm.gather_token[lo:hi]], w_up, w_gate, w_out)
-    z = np.zeros((T, L), np.float64)
-    for j in range(k):
-        z += r.weights[:, j:j + 1] * y[perm.scatter_pos[np.arange(T) * k + j]]
-    if cfg.is_latent:
-        n = rms_norm(z, cfg.rms_eps, wts.rms_weight) if cfg.up_proj_norm else z
-        out = n @ np.asarray(wts.w_up_latent, np.float64).T
-    else:
-        out = z
+    y = expert_outputs(cfg, x_routed, perm, wts.expert)
+    z = combine(y, perm.scatter_pos, r.weights)
+    out = restore_routed_output(cfg, z, wts.w_up_latent, wts.rms_weight)
     return LayerResult(r, perm, x_routed, y, z, out)
-

@@ -54,3 +54,29 @@ def near_tie_tokens(keys: np.ndarray, k: int, gap: float = 1e-5) -> np.ndarray:
     if m < 2:
         return np.zeros(T, bool)
     return (np.diff(-part, axis=1) < gap).any(axis=1)
+
+
+# Parity bars (layer output against float64; top-k near-tie rule).
+REL_L2 = 1e-2
+MAX_ABS = 3e-2
+TIE_GAP = 1e-5
+TIE_FRAC = 1e-3
+
+
+def assert_close_layer(got, want, what):
+    got = np.asarray(got, np.float64)
+    want = np.asarray(want, np.float64)
+    rel = np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-30)
+    mx = np.abs(got - want).max() if got.size else 0.0
+    assert rel <= REL_L2 and mx <= MAX_ABS, f"{what}: rel_l2={rel:.3e} max_abs={mx:.3e}"
+    return rel, mx
+
+
+def check_topk(gpu_idx, oracle_keys, oracle_idx, k):
+    """Top-k indices equal except near-ties, which must stay under 0.1% of the tokens."""
+    mism = (gpu_idx != oracle_idx).any(axis=1)
+    ties = near_tie_tokens(oracle_keys, k, TIE_GAP)
+    bad = mism & ~ties
+    assert not bad.any(), f"{bad.sum()} top-k mismatches that are not near-ties, e.g. token {np.nonzero(bad)[0][:5]}"
+    assert mism.sum() <= TIE_FRAC * len(mism), f"{mism.sum()} near-tie mismatches > 0.1%"
+    return mism

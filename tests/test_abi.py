@@ -1,0 +1,122 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+and its host-only functions (parameter counts, config checks, workspace plan)
+behave as the header states.  No device entry point is called here.
+"""
+import os
+import re
+
+import pytest
+
+from token_routing_expert_gb300 import native
+from token_routing_expert_gb300.workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(native.LIB_PATH):
+        from token_routing_expert_gb300 import build
+        build.build()
+    return native.load()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/moe.h but not exported"
+    assert sorted(native.EXPORTS) == names
+
+
+def test_library_has_no_cuda_runtime_dependency():
+    # the runtime is linked statically: loading needs neither a toolkit nor a GPU
+    import subprocess
+    out = subprocess.run(["ldd", native.LIB_PATH], capture_output=True, text=True).stdout
+    assert "libcudart" not in out
+
+
+def _golden_rows():
+    rows = []
+    for line in open(os.path.join(ROOT, "tests", "golden", "param_counts.txt")):
+        line = line.split("#")[0].strip()
+        if line:
+            rows.append(line.split())
+    return rows
+
+
+@pytest.mark.parametrize("row", _golden_rows(), ids=lambda r: r[0])
+def test_param_counts_match_closed_forms(lib, row):
+    name, D, L, E, k, h, router, total, active, proj = row[0], *map(int, row[1:])
+    cfg = native.make_config(D, E, k, h, latent_dim=L)
+    assert native.moe_num_params(cfg) == total
+    assert native.moe_num_active_params(cfg) == active
+    assert native.moe_latent_proj_params(cfg) == proj
+    if L:
+        assert native.moe_latent_proj_params(cfg, with_norm_gain=True) == proj + L
+    cfgb = native.make_config(D, E, k, h, latent_dim=L, router_bias=True)
+    assert native.moe_num_params(cfgb) == total + E
+
+
+def test_validate_config_codes(lib):
+    ok = native.make_config(256, 8, 2, 128)
+    assert native.moe_validate_config(ok) == 0
+    bad = [
+        native.make_config(256, 8, 9, 128),               # top_k > num_experts
+        native.make_config(0, 8, 2, 128),                 # d_model < 1
+        native.make_config(256, 8, 2, 128, gating=7),     # unknown gating
+        native.make_config(256, 8, 2, 128, normalize_expert_weights=-1.0),
+        native.make_config(256, 8, 2, 128, latent_dim=-64),
+    ]
+    for c in bad:
+        assert native.moe_validate_config(c) == 1
+    unsupported = [
+        native.make_config(200, 8, 2, 128),               # d_model not a multiple of 64
+        native.make_config(256, 8, 2, 100),               # hidden not a multiple of 64
+        native.make_config(256, 8, 2, 128, latent_dim=96),
+        native.make_config(256, 2000, 2, 128),            # more experts than the kernels hold
+        native.make_config(256, 64, 33, 128),             # top_k > 32
+    ]
+    for c in unsupported:
+        assert native.moe_validate_config(c) == 2
+    c = native.make_config(256, 8, 2, 128)
+    c.activation = 1
+    assert native.moe_validate_config(c) == 2
+
+
+@pytest.mark.parametrize("name", list(WORKLOADS))
+def test_workspace_plan(lib, name):
+    spec = WORKLOADS[name]
+    cfg = native.config_from_spec(spec)
+    size = native.moe_workspace_size(cfg, spec.T)
+    R, Lr = spec.rows, spec.routed_dim
+    # at least: permuted input, H and Y (bf16) plus the routing arrays
+    assert size >= R * (2 * Lr + spec.hidden_size) * 2 + R * 16
+    assert size % 256 == 0
+    assert native.moe_workspace_size(cfg, 2 * spec.T) > size
+    lay = native.moe_workspace_layout(cfg, spec.T)
+    present = [o for o in lay if o >= 0]
+    assert all(o % 256 == 0 and o < size for o in present)
+    assert (lay[7] >= 0) == bool(spec.latent_dim) and (lay[9] >= 0) == bool(spec.latent_dim)
+
+
+def test_host_errors_enqueue_nothing(lib):
+    import ctypes
+    cfg = native.make_config(256, 8, 2, 128)
+    out = ctypes.c_size_t()
+    assert lib.moe_workspace_size(ctypes.byref(cfg), -1, ctypes.byref(out)) == 1
+    assert lib.moe_workspace_size(None, 4, ctypes.byref(out)) == 1
+    # a device entry point with a workspace that is too small fails on the host
+    w = native.moe_weights_t()
+    assert lib.moe_router(ctypes.byref(cfg), ctypes.byref(w), 16, 4, None, 16, 16, 256, 8, None) == 3
+    # misaligned workspace
+    assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 16, 4, 32, 1000, 1 << 30, None) == 3
+    # empty batch: nothing to do, and no device needed
+    assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 16, 0, 32, None, 0, None) == 0
+    assert native.load().moe_status_string(5) == b"device wait timed out"

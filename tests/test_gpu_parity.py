@@ -1,0 +1,277 @@
+"""GPU parity: every C-ABI entry point against the float64 oracle on seeded inputs.
+
+Sizes are small enough for the oracle to finish in seconds but span several
+128-row tiles, ragged group tails, split-K paths and the degenerate cases
+(one expert, one token, top_k = num_experts, 1024 experts with top_k 32,
+an empty batch).
+
+Tolerances:
+  * indices, counts, offsets, gather / scatter: bit-exact;
+  * top-k: bit-exact except tokens whose float64 top-(k+1) keys have a
+    consecutive gap below 1e-5; such mismatches must stay under 0.1% of T;
+  * layer output (and each bf16-producing stage): relative L2 <= 1e-2 and
+    max abs <= 3e-2 against float64;
+  * logits: fp32 accumulation of exact bf16 products, |err| <= 1e-5 + 1e-5 |logit|;
+  * routing weights: fp32 arithmetic, |err| <= 1e-5 + 1e-5 |w|.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_ref as ref
+from tests.oracle_bridge import assert_close_layer, check_topk, f64, oracle_config, oracle_weights
+from token_routing_expert_gb300 import native
+from token_routing_expert_gb300.workloads import WORKLOADS, WorkloadSpec, generate
+
+pytestmark = pytest.mark.gpu
+
+CASES = {
+    "tiny": WORKLOADS["tiny"],
+    "ragged_topk_softmax": WorkloadSpec("ragged_topk_softmax", T=1000, d_model=512, num_experts=16, top_k=4,
+                                        hidden_size=256, gating="topk_softmax", seed=11),
+    "sigmoid_bias_restore": WorkloadSpec("sigmoid_bias_restore", T=777, d_model=512, num_experts=64, top_k=8,
+                                         hidden_size=320, gating="sigmoid", sigmoid_stability_epsilon=1e-6,
+                                         score_bias_std=0.01, normalize_expert_weights=1.0,
+                                         restore_weight_scale=True, seed=12),
+    "latent_skew": WorkloadSpec("latent_skew", T=600, d_model=1024, num_experts=40, top_k=6, hidden_size=192,
+                                latent_dim=512, gating="sigmoid", skew=True, seed=13),
+    "latent_decode_small": WorkloadSpec("latent_decode_small", T=5, d_model=1024, num_experts=100, top_k=8,
+                                        hidden_size=128, latent_dim=256, gating="sigmoid", seed=14),
+    "softmax_p2_scales": WorkloadSpec("softmax_p2_scales", T=300, d_model=256, num_experts=24, top_k=3,
+                                      hidden_size=128, gating="softmax", normalize_expert_weights=2.0,
+                                      expert_weight_scale=2.5, original_top_k=12, seed=15),
+    "single_expert": WorkloadSpec("single_expert", T=130, d_model=128, num_experts=1, top_k=1, hidden_size=64,
+                                  seed=16),
+    "all_experts_dense": WorkloadSpec("all_experts_dense", T=150, d_model=192, num_experts=6, top_k=6,
+                                      hidden_size=128, gating="softmax", seed=19),
+    "max_experts": WorkloadSpec("max_experts", T=200, d_model=128, num_experts=1024, top_k=32, hidden_size=64,
+                                gating="sigmoid", seed=17),
+    "one_token": WorkloadSpec("one_token", T=1, d_model=256, num_experts=8, top_k=2, hidden_size=128, seed=18),
+}
+
+_cache = {}
+
+
+def setup(name):
+    if name not in _cache:
+        spec = CASES[name]
+        inp = generate(spec)
+        _cache[name] = (spec, inp, native.config_from_spec(spec), native.DeviceWeights.from_inputs(inp))
+    return _cache[name]
+
+
+def expect_ok():
+    assert native.moe_get_status() == 0
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_router(name):
+    spec, inp, cfg, wts = setup(name)
+    T, E, k = spec.T, spec.num_experts, spec.top_k
+    x = inp["x"].cuda()
+    ws = native.workspace(cfg, T)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    _, idx, w = native.moe_router(cfg, wts, x, ws, logits=logits)
+    expect_ok()
+    oc, ow = oracle_config(spec), oracle_weights(spec, inp)
+    r = ref.route(oc, f64(inp["x"]), ow.w_router, ow.b_router, ow.score_bias)
+    lg = logits.double().cpu().numpy()
+    assert np.all(np.abs(lg - r.logits) <= 1e-5 + 1e-5 * np.abs(r.logits)), np.abs(lg - r.logits).max()
+    gi = idx.cpu().numpy().astype(np.int64)
+    check_topk(gi, r.keys, r.idx, k)
+    # the weights of the GPU's own choice, computed by the oracle
+    rf = ref.route(oc, f64(inp["x"]), ow.w_router, ow.b_router, ow.score_bias, forced_idx=gi)
+    gw = w.double().cpu().numpy()
+    assert np.all(np.abs(gw - rf.weights) <= 1e-5 + 1e-5 * np.abs(rf.weights)), np.abs(gw - rf.weights).max()
+    # without a logits output the choice is the same
+    _, idx2, w2 = native.moe_router(cfg, wts, x, ws)
+    expect_ok()
+    assert torch.equal(idx2, idx) and torch.equal(w2, w)
+
+
+def _check_permute(idx_dev, E, k):
+    cfg = native.make_config(64, E, k, 64)
+    T = idx_dev.shape[0]
+    ws = native.workspace(cfg, T)
+    counts, offsets, gather, scatter = native.moe_permute(cfg, idx_dev, ws)
+    expect_ok()
+    p = ref.permute(idx_dev.cpu().numpy().astype(np.int64), E)
+    np.testing.assert_array_equal(counts.cpu().numpy(), p.counts)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), p.offsets)
+    np.testing.assert_array_equal(gather.cpu().numpy(), p.gather_token)
+    np.testing.assert_array_equal(scatter.cpu().numpy(), p.scatter_pos)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_permute_on_router_output(name):
+    spec, inp, cfg, wts = setup(name)
+    ws = native.workspace(cfg, spec.T)
+    _, idx, _ = native.moe_router(cfg, wts, inp["x"].cuda(), ws)
+    _check_permute(idx, spec.num_experts, spec.top_k)
+
+
+@pytest.mark.parametrize("T,k,E,kind", [(40000, 8, 896, "uniform"), (9000, 8, 64, "one_hot"),
+                                         (5000, 4, 1000, "few"), (1, 1, 1, "uniform"), (3, 2, 1024, "uniform"),
+                                         (33000, 8, 256, "skew")])
+def test_permute_patterns(T, k, E, kind):
+    g = np.random.default_rng(T + E)
+    if kind == "uniform":
+        idx = g.integers(0, E, size=(T, k))
+    elif kind == "one_hot":
+        idx = np.full((T, k), E - 1)
+    elif kind == "few":
+        idx = g.choice([0, 7, E - 1], size=(T, k))
+    else:
+        p = 1.0 / np.arange(1, E + 1)
+        idx = g.choice(E, size=(T, k), p=p / p.sum())
+    _check_permute(torch.from_numpy(idx.astype(np.int32)).cuda(), E, k)
+
+
+def test_permute_empty_batch():
+    cfg = native.make_config(64, 12, 3, 64)
+    ws = native.workspace(cfg, 0)
+    idx = torch.empty((0, 3), dtype=torch.int32, device="cuda")
+    counts, offsets, _, _ = native.moe_permute(cfg, idx, ws)
+    expect_ok()
+    assert counts.cpu().tolist() == [0] * 12 and offsets.cpu().tolist() == [0] * 13
+
+
+def test_permute_out_of_range_index_is_reported():
+    cfg = native.make_config(64, 8, 2, 64)
+    idx = torch.tensor([[0, 1], [8, 3], [2, -1]], dtype=torch.int32, device="cuda")
+    ws = native.workspace(cfg, 3)
+    counts, offsets, _, _ = native.moe_permute(cfg, idx, ws)
+    assert native.moe_get_status() == 6   # MOE_ERR_BOUNDS, and the kernel skipped the two bad entries
+    assert counts.sum().item() == 4 and offsets[-1].item() == 4
+    assert native.moe_get_status() == 0   # cleared by the previous read
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_grouped_swiglu(name):
+    spec, inp, cfg, wts = setup(name)
+    T, Lr, h = spec.T, spec.routed_dim, spec.hidden_size
+    ws = native.workspace(cfg, T)
+    _, idx, _ = native.moe_router(cfg, wts, inp["x"].cuda(), ws)
+    counts, offsets, gather, scatter = native.moe_permute(cfg, idx, ws)
+    xr = torch.from_numpy(np.random.default_rng(spec.seed + 100).standard_normal((T, Lr), dtype=np.float32)).to(
+        torch.bfloat16)
+    y = native.moe_grouped_swiglu(cfg, wts, xr.cuda(), gather, offsets, ws)
+    expect_ok()
+    perm = ref.Permutation(counts.cpu().numpy(), offsets.cpu().numpy(), gather.cpu().numpy(), scatter.cpu().numpy())
+    ow = oracle_weights(spec, inp)
+    want = ref.expert_outputs(oracle_config(spec), f64(xr), perm, ow.expert)
+    assert_close_layer(y.double().cpu().numpy(), want, "grouped swiglu")
+
+
+@pytest.mark.parametrize("name", ["tiny", "sigmoid_bias_restore", "latent_skew", "max_experts", "one_token"])
+def test_combine(name):
+    spec, inp, cfg, wts = setup(name)
+    T, k, Lr = spec.T, spec.top_k, spec.routed_dim
+    ws = native.workspace(cfg, T)
+    _, idx, w = native.moe_router(cfg, wts, inp["x"].cuda(), ws)
+    _, _, _, scatter = native.moe_permute(cfg, idx, ws)
+    y = torch.from_numpy(np.random.default_rng(spec.seed + 200).standard_normal((T * k, Lr), dtype=np.float32)).to(
+        torch.bfloat16)
+    z = native.moe_combine(cfg, y.cuda(), scatter, w, T)
+    expect_ok()
+    want = ref.combine(f64(y), scatter.cpu().numpy(), w.double().cpu().numpy())
+    got = z.double().cpu().numpy()
+    # fp32 accumulation then one bf16 rounding
+    assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-5), np.abs(got - want).max()
+
+
+@pytest.mark.parametrize("name", ["latent_skew", "latent_decode_small"])
+def test_latent_down_and_restore(name):
+    spec, inp, cfg, wts = setup(name)
+    T, D, L = spec.T, spec.d_model, spec.latent_dim
+    ws = native.workspace(cfg, T)
+    oc, ow = oracle_config(spec), oracle_weights(spec, inp)
+    xr = native.moe_latent_down(cfg, wts, inp["x"].cuda(), ws)
+    expect_ok()
+    want = ref.prepare_routed_input(oc, f64(inp["x"]), ow.w_down_latent)
+    got = xr.double().cpu().numpy()
+    assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-4), np.abs(got - want).max()
+    z = torch.from_numpy(np.random.default_rng(spec.seed + 300).standard_normal((T, L), dtype=np.float32) * 0.3).to(
+        torch.bfloat16)
+    out = native.moe_latent_restore(cfg, wts, z.cuda(), ws)
+    expect_ok()
+    assert_close_layer(out.double().cpu().numpy(), ref.restore_routed_output(oc, f64(z), ow.w_up_latent),
+                       "latent restore")
+
+
+def run_layer_and_compare(spec, inp, cfg, wts):
+    T, k = spec.T, spec.top_k
+    ws = native.workspace(cfg, T)
+    out = native.moe_layer_forward(cfg, wts, inp["x"].cuda(), ws)
+    expect_ok()
+    inter = native.layer_intermediates(cfg, T, ws)
+    oc, ow = oracle_config(spec), oracle_weights(spec, inp)
+    r = ref.route(oc, f64(inp["x"]), ow.w_router, ow.b_router, ow.score_bias)
+    gi = inter["idx"].cpu().numpy().astype(np.int64)
+    mism = check_topk(gi, r.keys, r.idx, k)
+    forced = r.idx.copy()
+    forced[mism] = gi[mism]   # a legitimate near-tie flip: the oracle follows the GPU's choice
+    res = ref.layer_forward(oc, f64(inp["x"]), ow, forced_idx=forced)
+    p = ref.permute(gi, spec.num_experts)
+    np.testing.assert_array_equal(inter["counts"].cpu().numpy(), p.counts)
+    np.testing.assert_array_equal(inter["offsets"].cpu().numpy(), p.offsets)
+    np.testing.assert_array_equal(inter["gather_idx"].cpu().numpy(), p.gather_token)
+    np.testing.assert_array_equal(inter["scatter_idx"].cpu().numpy(), p.scatter_pos)
+    return assert_close_layer(out.double().cpu().numpy(), res.out, "layer output")
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_layer_forward(name):
+    spec, inp, cfg, wts = setup(name)
+    run_layer_and_compare(spec, inp, cfg, wts)
+
+
+def test_layer_forward_repeatable_and_stream_ordered():
+    spec, inp, cfg, wts = setup("ragged_topk_softmax")
+    ws = native.workspace(cfg, spec.T)
+    x = inp["x"].cuda()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        a = native.moe_layer_forward(cfg, wts, x, ws, stream=s)
+        b = native.moe_layer_forward(cfg, wts, x, ws, stream=s)
+    s.synchronize()
+    expect_ok()
+    assert torch.equal(a, b)
+
+
+def test_layer_forward_empty_batch():
+    spec = CASES["tiny"]
+    _, _, cfg, wts = setup("tiny")
+    x = torch.empty((0, spec.d_model), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    out = native.moe_layer_forward(cfg, wts, x, ws)
+    assert out.shape == (0, spec.d_model)
+    expect_ok()
+
+
+def test_bad_workspace_raises():
+    spec, inp, cfg, wts = setup("tiny")
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    with pytest.raises(native.MoEError) as e:
+        native.moe_layer_forward(cfg, wts, inp["x"].cuda(), ws)
+    assert e.value.code == 3
+
+
+@pytest.mark.parametrize("name", ["ragged_topk_softmax", "latent_skew"])
+def test_staged_forward_matches_and_records_every_stage(name):
+    spec, inp, cfg, wts = setup(name)
+    ws = native.workspace(cfg, spec.T)
+    x = inp["x"].cuda()
+    plain = native.moe_layer_forward(cfg, wts, x, ws)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+    for e in evs:
+        e.record()
+    staged = native.moe_layer_forward_staged(cfg, wts, x, ws, evs)
+    torch.cuda.synchronize()
+    expect_ok()
+    assert torch.equal(plain, staged)
+    times = [evs[i].elapsed_time(evs[i + 1]) for i in range(9)]
+    assert all(t >= 0 for t in times) and times[5] > 0   # grouped GEMM 1 took time
+    n = native.moe_layer_forward_launches(cfg, spec.T)
+    # 10 kernels; a latent layer adds the two projections, each with a split-K reduce when split
+    assert n == 10 if not spec.latent_dim else 12 <= n <= 14

@@ -1,0 +1,526 @@
+// C ABI of the MoE layer forward: argument checks, workspace plan, and the
+// order of kernel launches.  See include/moe.h for the contract.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// Per-device status word (first error recorded by any kernel).
+__device__ int g_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {nullptr};
+
+int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (!g_status_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    g_status_ptr[dev] = static_cast<int*>(p);
+  }
+  return g_status_ptr[dev];
+}
+
+// Bound on the SM count used to size split-K buffers (the GPU's own count is
+// used at launch, and never needs more).
+constexpr int kSizingSms = 256;
+
+int splits_for(int tiles, int K, int sms) {
+  const int kt = (K + 63) / 64;
+  if (tiles * 2 > sms) return 1;
+  int s = std::max(1, sms / std::max(1, tiles));
+  s = std::min(s, std::max(1, kt / 4));
+  const int per = (kt + s - 1) / s;
+  return (kt + per - 1) / per;
+}
+
+struct Plan {
+  int64_t T, R;
+  int D, E, k, h, L, Lr;   // Lr: routed dim (L or D)
+  bool latent;
+  int router_bn, n_router_tiles;
+  int router_splits, down_splits, up_splits;
+  size_t logits, idx, wts, counts, offsets, tile_off, blk, gather, scatter, xr, xp, H, Y, zn, part, total;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
+  p->T = T;
+  p->D = c->d_model;
+  p->E = c->num_experts;
+  p->k = c->top_k;
+  p->h = c->hidden_size;
+  p->latent = c->latent_dim > 0;
+  p->L = c->latent_dim;
+  p->Lr = p->latent ? c->latent_dim : c->d_model;
+  p->R = T * p->k;
+  const int mt = (int)((T + 127) / 128);
+  p->router_bn = pick_bn_f32(p->E);
+  p->n_router_tiles = (p->E + p->router_bn - 1) / p->router_bn;
+  p->router_splits = splits_for(mt * p->n_router_tiles, p->D, sms);
+  p->down_splits = p->latent ? splits_for(mt * ((p->L + 255) / 256), p->D, sms) : 1;
+  p->up_splits = p->latent ? splits_for(mt * ((p->D + 255) / 256), p->L, sms) : 1;
+
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  p->logits = take((size_t)p->router_splits * T * p->E * 4);
+  p->idx = take((size_t)p->R * 4);
+  p->wts = take((size_t)p->R * 4);
+  p->counts = take((size_t)p->E * 4);
+  p->offsets = take((size_t)(p->E + 1) * 4);
+  p->tile_off = take((size_t)(p->E + 1) * 4);
+  p->blk = take((size_t)std::max(1, permute_blocks((int)p->R)) * p->E * 4);
+  p->gather = take((size_t)p->R * 4);
+  p->scatter = take((size_t)p->R * 4);
+  p->xr = p->latent ? take((size_t)T * p->L * 2) : (size_t)-1;
+  p->xp = take((size_t)p->R * p->Lr * 2);
+  p->H = take((size_t)p->R * p->h * 2);
+  p->Y = take((size_t)p->R * p->Lr * 2);
+  p->zn = p->latent ? take((size_t)T * p->L * 2) : (size_t)-1;
+  size_t part = 0;
+  if (p->down_splits > 1) part = std::max(part, (size_t)p->down_splits * T * p->L * 4);
+  if (p->up_splits > 1) part = std::max(part, (size_t)p->up_splits * T * p->D * 4);
+  p->part = take(part);
+  p->total = o;
+}
+
+int check_config(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->d_model < 1 || c->num_experts < 1 || c->top_k < 1 || c->hidden_size < 1 || c->latent_dim < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (c->top_k > c->num_experts) return MOE_ERR_INVALID_ARG;
+  if (c->gating < MOE_GATING_SOFTMAX || c->gating > MOE_GATING_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (c->normalize_expert_weights < 0.f || c->sigmoid_stability_epsilon < 0.f || c->original_top_k < 0 ||
+      !(c->rms_eps >= 0.f) || std::isnan(c->expert_weight_scale))
+    return MOE_ERR_INVALID_ARG;
+  if (c->activation != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->d_model % 64 || c->hidden_size % 64 || (c->latent_dim > 0 && c->latent_dim % 64)) return MOE_ERR_UNSUPPORTED;
+  if (c->num_experts > 1024 || c->top_k > 32) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int check_call(const moe_config_t* c, int64_t T, void* ws, size_t ws_bytes, Plan* plan) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)T * c->top_k > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  make_plan(c, T, std::min(num_sms(), kSizingSms), plan);
+  Plan sizing;
+  make_plan(c, T, kSizingSms, &sizing);
+  if (T > 0 && (!ws || ((uintptr_t)ws & 255) || ws_bytes < sizing.total)) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// C = A * B^T, dense, with split-K through fp32 partials when the output has few tiles.
+int dense_gemm_bf16(const void* A, const void* B, int M, int N, int K, void* out, int splits, float* part,
+                    int* status, cudaStream_t st) {
+  GemmProblem q{};
+  q.A = A;
+  q.B = B;
+  q.b_rows_total = N;
+  q.M = M;
+  q.N = N;
+  q.K = K;
+  q.num_groups = 0;
+  q.b_rows_per_group = 0;
+  q.bn = 256;
+  q.status = status;
+  if (splits > 1) {
+    q.epilogue = EPI_F32;
+    q.splits = splits;
+    q.out = part;
+    q.ldo = N;
+    q.split_stride = (int64_t)M * N;
+    int s = cuda_status(launch_gemm(q, st));
+    if (s != MOE_OK) return s;
+    return cuda_status(launch_splitk_reduce_bf16(part, splits, (int64_t)M * N, out, st));
+  }
+  q.epilogue = EPI_BF16;
+  q.splits = 1;
+  q.out = out;
+  q.ldo = N;
+  q.split_stride = 0;
+  return cuda_status(launch_gemm(q, st));
+}
+
+void mark(cudaEvent_t* ev, int i, cudaStream_t st) {
+  if (ev && ev[i]) cudaEventRecord(ev[i], st);
+}
+
+int run_router(const moe_config_t* c, const moe_weights_t* w, const void* x, const Plan& p, float* logits_user,
+               int32_t* idx, float* wts, void* ws, int* status, cudaStream_t st, cudaEvent_t* ev = nullptr) {
+  float* gemm_out = (p.router_splits == 1 && logits_user) ? logits_user : at<float>(ws, p.logits);
+  GemmProblem q{};
+  q.A = x;
+  q.B = w->w_router;
+  q.b_rows_total = p.E;
+  q.M = (int)p.T;
+  q.N = p.E;
+  q.K = p.D;
+  q.num_groups = 0;
+  q.epilogue = EPI_F32;
+  q.bn = p.router_bn;
+  q.splits = p.router_splits;
+  q.out = gemm_out;
+  q.ldo = p.E;
+  q.split_stride = p.T * p.E;
+  q.status = status;
+  int s = cuda_status(launch_gemm(q, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 2, st);
+  const bool rewrite = logits_user && (p.router_splits > 1 || (c->router_bias && w->b_router));
+  float* logits_out = rewrite ? logits_user : nullptr;
+  return cuda_status(launch_topk(gemm_out, p.router_splits, p.T * p.E, c->router_bias ? w->b_router : nullptr,
+                                 c->has_score_bias ? w->score_bias : nullptr, (int)p.T, p.E, p.k, c->gating,
+                                 c->sigmoid_stability_epsilon, c->normalize_expert_weights,
+                                 c->restore_weight_scale, c->expert_weight_scale, c->original_top_k, logits_out, idx,
+                                 wts, status, st));
+}
+
+int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
+                const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
+                cudaEvent_t* ev = nullptr) {
+  int32_t* tile_off = at<int32_t>(ws, p.tile_off);
+  void* xp = at<void>(ws, p.xp);
+  void* H = at<void>(ws, p.H);
+  int s = cuda_status(launch_tile_table(offsets, p.E, tile_off, st));
+  if (s != MOE_OK) return s;
+  s = cuda_status(launch_gather_rows(xr, gather, (int)p.R, (int)p.T, p.Lr, xp, status, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 5, st);
+  GemmProblem g1{};
+  g1.A = xp;
+  g1.B = w->w_up_gate;
+  g1.b_rows_total = (int64_t)p.E * 2 * p.h;
+  g1.M = (int)p.R;
+  g1.N = p.h;
+  g1.K = p.Lr;
+  g1.num_groups = p.E;
+  g1.group_off = offsets;
+  g1.tile_off = tile_off;
+  g1.b_rows_per_group = 2 * p.h;
+  g1.b_gate_offset = p.h;
+  g1.epilogue = EPI_SWIGLU;
+  g1.bn = 256;
+  g1.splits = 1;
+  g1.out = H;
+  g1.ldo = p.h;
+  g1.status = status;
+  s = cuda_status(launch_gemm(g1, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 6, st);
+  GemmProblem g2{};
+  g2.A = H;
+  g2.B = w->w_out;
+  g2.b_rows_total = (int64_t)p.E * p.Lr;
+  g2.M = (int)p.R;
+  g2.N = p.Lr;
+  g2.K = p.h;
+  g2.num_groups = p.E;
+  g2.group_off = offsets;
+  g2.tile_off = tile_off;
+  g2.b_rows_per_group = p.Lr;
+  g2.epilogue = EPI_BF16;
+  g2.bn = 256;
+  g2.splits = 1;
+  g2.out = y;
+  g2.ldo = p.Lr;
+  g2.status = status;
+  s = cuda_status(launch_gemm(g2, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 7, st);
+  return MOE_OK;
+}
+
+int run_restore(const moe_config_t* c, const moe_weights_t* w, const void* z, bool z_is_normalised, const Plan& p,
+                void* out, void* ws, int* status, cudaStream_t st) {
+  const void* n = z;
+  if (c->up_proj_norm && !z_is_normalised) {
+    void* zn = at<void>(ws, p.zn);
+    int s = cuda_status(launch_rmsnorm(z, (int)p.T, p.L, c->rms_eps, w->rms_weight, zn, st));
+    if (s != MOE_OK) return s;
+    n = zn;
+  }
+  return dense_gemm_bf16(n, w->w_up_latent, (int)p.T, p.D, p.L, out, p.up_splits, at<float>(ws, p.part), status, st);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_validate_config(const moe_config_t* cfg) { return check_config(cfg); }
+
+int moe_num_params(const moe_config_t* c, int64_t* out) {
+  if (!c || !out) return MOE_ERR_INVALID_ARG;
+  if (c->d_model < 1 || c->num_experts < 1 || c->top_k < 1 || c->hidden_size < 1 || c->latent_dim < 0)
+    return MOE_ERR_INVALID_ARG;
+  const int64_t Lr = c->latent_dim > 0 ? c->latent_dim : c->d_model;
+  const int64_t router = (int64_t)c->d_model * c->num_experts + (c->router_bias ? c->num_experts : 0);
+  *out = router + 3 * Lr * c->hidden_size * c->num_experts;
+  return MOE_OK;
+}
+
+int moe_num_active_params(const moe_config_t* c, int64_t* out) {
+  int64_t total = 0;
+  int s = moe_num_params(c, &total);
+  if (s != MOE_OK) return s;
+  const int64_t Lr = c->latent_dim > 0 ? c->latent_dim : c->d_model;
+  *out = total - 3 * Lr * c->hidden_size * c->num_experts + 3 * Lr * c->hidden_size * c->top_k;
+  return MOE_OK;
+}
+
+int moe_latent_proj_params(const moe_config_t* c, int with_norm_gain, int64_t* out) {
+  if (!c || !out || c->d_model < 1 || c->latent_dim < 0) return MOE_ERR_INVALID_ARG;
+  if (c->latent_dim == 0) {
+    *out = 0;
+    return MOE_OK;
+  }
+  *out = 2 * (int64_t)c->d_model * c->latent_dim + (with_norm_gain && c->up_proj_norm ? c->latent_dim : 0);
+  return MOE_OK;
+}
+
+int moe_workspace_size(const moe_config_t* c, int64_t T, size_t* bytes) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0 || !bytes) return MOE_ERR_INVALID_ARG;
+  Plan p;
+  make_plan(c, T, kSizingSms, &p);
+  *bytes = p.total;
+  return MOE_OK;
+}
+
+int moe_workspace_layout(const moe_config_t* c, int64_t T, int64_t o[10]) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0 || !o) return MOE_ERR_INVALID_ARG;
+  Plan p;
+  make_plan(c, T, std::min(num_sms(), kSizingSms), &p);
+  o[0] = (int64_t)p.logits;
+  o[1] = (int64_t)p.idx;
+  o[2] = (int64_t)p.wts;
+  o[3] = (int64_t)p.counts;
+  o[4] = (int64_t)p.offsets;
+  o[5] = (int64_t)p.gather;
+  o[6] = (int64_t)p.scatter;
+  o[7] = p.latent ? (int64_t)p.xr : -1;
+  o[8] = (int64_t)p.Y;
+  o[9] = p.latent ? (int64_t)p.zn : -1;
+  return MOE_OK;
+}
+
+int moe_router(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, float* logits, int32_t* idx,
+               float* weights, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Plan p;
+  int s = check_call(c, T, ws, ws_bytes, &p);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!w || !w->w_router || !x || !idx || !weights) return MOE_ERR_INVALID_ARG;
+  if ((c->router_bias && !w->b_router) || (c->has_score_bias && !w->score_bias)) return MOE_ERR_INVALID_ARG;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  return run_router(c, w, x, p, logits, idx, weights, ws, status, (cudaStream_t)stream);
+}
+
+int moe_permute(const moe_config_t* c, const int32_t* idx, int64_t T, int32_t* counts, int32_t* offsets,
+                int32_t* gather_idx, int32_t* scatter_idx, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Plan p;
+  int s = check_call(c, T, ws, ws_bytes, &p);
+  if (s != MOE_OK) return s;
+  if (!counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!idx || !gather_idx || !scatter_idx || !ws)) return MOE_ERR_INVALID_ARG;
+  if (T == 0 && (!ws || ((uintptr_t)ws & 255))) return MOE_ERR_WORKSPACE;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  return cuda_status(launch_permute(idx, (int)p.R, p.E, counts, offsets, gather_idx, scatter_idx, p.k,
+                                    at<int32_t>(ws, p.blk), status, (cudaStream_t)stream));
+}
+
+int moe_grouped_swiglu(const moe_config_t* c, const moe_weights_t* w, const void* x_routed, const int32_t* gather_idx,
+                       const int32_t* offsets, int64_t T, void* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Plan p;
+  int s = check_call(c, T, ws, ws_bytes, &p);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!w || !w->w_up_gate || !w->w_out || !x_routed || !gather_idx || !offsets || !y) return MOE_ERR_INVALID_ARG;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  return run_experts(c, w, x_routed, gather_idx, offsets, p, y, ws, status, (cudaStream_t)stream);
+}
+
+int moe_combine(const moe_config_t* c, const void* y, const int32_t* scatter_idx, const float* weights, int64_t T,
+                void* z, moe_stream_t stream) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!y || !scatter_idx || !weights || !z) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)T * c->top_k > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  const int Lr = c->latent_dim > 0 ? c->latent_dim : c->d_model;
+  return cuda_status(launch_combine(y, scatter_idx, weights, (int)T, c->top_k, Lr, (int)(T * c->top_k), 0, 0.f,
+                                    nullptr, z, status, (cudaStream_t)stream));
+}
+
+int moe_latent_down(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* x_routed, void* ws,
+                    size_t ws_bytes, moe_stream_t stream) {
+  Plan p;
+  int s = check_call(c, T, ws, ws_bytes, &p);
+  if (s != MOE_OK) return s;
+  if (!p.latent) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!w || !w->w_down_latent || !x || !x_routed) return MOE_ERR_INVALID_ARG;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  return dense_gemm_bf16(x, w->w_down_latent, (int)T, p.L, p.D, x_routed, p.down_splits, at<float>(ws, p.part),
+                         status, (cudaStream_t)stream);
+}
+
+int moe_latent_restore(const moe_config_t* c, const moe_weights_t* w, const void* z, int64_t T, void* out, void* ws,
+                       size_t ws_bytes, moe_stream_t stream) {
+  Plan p;
+  int s = check_call(c, T, ws, ws_bytes, &p);
+  if (s != MOE_OK) return s;
+  if (!p.latent) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!w || !w->w_up_latent || !z || !out) return MOE_ERR_INVALID_ARG;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  return run_restore(c, w, z, false, p, out, ws, status, (cudaStream_t)stream);
+}
+
+int moe_layer_forward_staged(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream, void* const* stage_events) {
+  Plan p;
+  int s = check_call(c, T, ws, ws_bytes, &p);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  if (!w || !x || !out || !w->w_router || !w->w_up_gate || !w->w_out) return MOE_ERR_INVALID_ARG;
+  if (p.latent && (!w->w_down_latent || !w->w_up_latent)) return MOE_ERR_INVALID_ARG;
+  if ((c->router_bias && !w->b_router) || (c->has_score_bias && !w->score_bias)) return MOE_ERR_INVALID_ARG;
+  if (x == out) return MOE_ERR_INVALID_ARG;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  cudaEvent_t* ev = reinterpret_cast<cudaEvent_t*>(const_cast<void**>(stage_events));
+
+  mark(ev, 0, st);
+  const void* xr = x;
+  if (p.latent) {
+    void* xl = at<void>(ws, p.xr);
+    s = dense_gemm_bf16(x, w->w_down_latent, (int)T, p.L, p.D, xl, p.down_splits, at<float>(ws, p.part), status, st);
+    if (s != MOE_OK) return s;
+    xr = xl;
+  }
+  mark(ev, 1, st);
+  int32_t* idx = at<int32_t>(ws, p.idx);
+  float* wts = at<float>(ws, p.wts);
+  s = run_router(c, w, x, p, nullptr, idx, wts, ws, status, st, ev);
+  if (s != MOE_OK) return s;
+  mark(ev, 3, st);
+  int32_t* counts = at<int32_t>(ws, p.counts);
+  int32_t* offsets = at<int32_t>(ws, p.offsets);
+  int32_t* gather = at<int32_t>(ws, p.gather);
+  int32_t* scatter = at<int32_t>(ws, p.scatter);
+  s = cuda_status(launch_permute(idx, (int)p.R, p.E, counts, offsets, gather, scatter, p.k, at<int32_t>(ws, p.blk),
+                                 status, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 4, st);
+  void* Y = at<void>(ws, p.Y);
+  s = run_experts(c, w, xr, gather, offsets, p, Y, ws, status, st, ev);
+  if (s != MOE_OK) return s;
+  if (!p.latent) {
+    s = cuda_status(launch_combine(Y, scatter, wts, (int)T, p.k, p.Lr, (int)p.R, 0, 0.f, nullptr, out, status, st));
+    mark(ev, 8, st);
+    mark(ev, 9, st);
+    return s;
+  }
+  void* zn = at<void>(ws, p.zn);
+  s = cuda_status(launch_combine(Y, scatter, wts, (int)T, p.k, p.L, (int)p.R, c->up_proj_norm, c->rms_eps,
+                                 w->rms_weight, zn, status, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 8, st);
+  s = run_restore(c, w, zn, true, p, out, ws, status, st);
+  mark(ev, 9, st);
+  return s;
+}
+
+int moe_layer_forward(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* out, void* ws,
+                      size_t ws_bytes, moe_stream_t stream) {
+  return moe_layer_forward_staged(c, w, x, T, out, ws, ws_bytes, stream, nullptr);
+}
+
+int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0 || !n) return MOE_ERR_INVALID_ARG;
+  if (T == 0) {
+    *n = 0;
+    return MOE_OK;
+  }
+  Plan p;
+  make_plan(c, T, std::min(num_sms(), kSizingSms), &p);
+  int k = 0;
+  if (p.latent) k += p.down_splits > 1 ? 2 : 1;  // latent down (+ split-K reduce)
+  k += 2;                                        // router GEMM, top-k
+  k += 3;                                        // permute: count, scan, place
+  k += 2;                                        // tile table, row gather
+  k += 2;                                        // grouped GEMM 1 (SwiGLU), grouped GEMM 2
+  k += 1;                                        // combine (+ RMSNorm when latent)
+  if (p.latent) k += p.up_splits > 1 ? 2 : 1;    // latent up (+ split-K reduce)
+  *n = k;
+  return MOE_OK;
+}
+
+int moe_get_status(moe_stream_t stream, int32_t* device_status, int clear) {
+  if (!device_status) return MOE_ERR_INVALID_ARG;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  int host = 0;
+  if (cudaMemcpyAsync(&host, status, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (clear) {
+    if (cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  *device_status = host;
+  return MOE_OK;
+}
+
+const char* moe_status_string(int s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_BOUNDS: return "index out of range on the device";
+    case MOE_ERR_NO_DEVICE: return "no CUDA device";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,437 @@
+// Persistent, warp-specialised tcgen05 GEMM for sm_103a, dense or grouped.
+//
+// One CTA per SM walks a static round-robin list of 128 x BN output tiles.
+//   warp 0 (one lane)  : TMA producer, STAGES-deep ring of (A, B) k-tiles
+//   warp 1 (one lane)  : UMMA issuer (M=128, N=BN, K=16 per instruction),
+//                        accumulates into one of two TMEM accumulators
+//   warps 2..5         : epilogue, TMEM -> registers -> global, overlapping
+//                        the next tile's mainloop through the second accumulator
+// Grouped mode: the row ranges of the groups and their tile prefix sums are
+// read on the device, so no host synchronisation is needed to schedule them.
+// Epilogues: fp32 (router logits, split-K partials), bf16, and SwiGLU, where
+// the B tile holds BN/2 "up" rows and BN/2 "gate" rows of the same expert and
+// the epilogue writes silu(gate) * up as bf16.
+#include <algorithm>
+#include <cstdio>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int BM = 128;
+constexpr int BK = 64;                 // 64 bf16 = 128 bytes: one 128-byte swizzle row
+constexpr int UMMA_K = 16;
+constexpr int kMaxGroups = 1024;
+constexpr int kThreads = 192;
+
+struct GemmParams {
+  int M, N, K;
+  int num_groups;          // 0 = dense
+  const int* group_off;
+  const int* tile_off;
+  int b_rows_per_group;
+  int b_gate_offset;
+  int n_tiles;
+  int splits;
+  int kt_per_split;
+  int kt_total;
+  void* out;
+  long long ldo;
+  long long split_stride;
+  int* status;
+};
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_RAW = (196 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int ACC_STRIDE = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
+  static constexpr int TMEM_COLS = 2 * ACC_STRIDE < 32 ? 32 : 2 * ACC_STRIDE;
+  // ring | barriers (full, empty, tmem_full x2, tmem_empty x2) | tmem holder | abort | group tables
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 4;
+  static constexpr int HOLDER_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int ABORT_OFF = HOLDER_OFF + 4;
+  static constexpr int TABLE_OFF = (ABORT_OFF + 4 + 15) & ~15;
+  static constexpr int SMEM_BYTES = TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 1024;  // + alignment slack
+  static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
+  static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=128, whole 32-column epilogue chunks");
+};
+
+struct TileCoord {
+  int row0;     // first row of A / C
+  int rows;     // valid rows (<= BM)
+  int group;
+  int nt;       // n tile
+  int split;
+  int kt0, kt1; // k-tile range
+};
+
+__device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, const int* s_toff,
+                                                 const int* s_goff) {
+  TileCoord c;
+  c.split = t % p.splits;
+  const int rest = t / p.splits;
+  c.nt = rest % p.n_tiles;
+  const int mt = rest / p.n_tiles;
+  int row_base = 0, row_end = p.M, mt_local = mt;
+  c.group = 0;
+  if (p.num_groups > 0) {
+    // last group g with tile_off[g] <= mt (it is non-empty because mt < tile_off[G])
+    int lo = 0, hi = p.num_groups - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_toff[mid] <= mt) lo = mid; else hi = mid - 1;
+    }
+    c.group = lo;
+    mt_local = mt - s_toff[lo];
+    row_base = s_goff[lo];
+    row_end = s_goff[lo + 1];
+  }
+  c.row0 = row_base + mt_local * BM;
+  c.rows = min(BM, row_end - c.row0);
+  c.kt0 = c.split * p.kt_per_split;
+  c.kt1 = min(p.kt_total, c.kt0 + p.kt_per_split);
+  return c;
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  using C = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty_bar = full_bar + C::STAGES;
+  uint64_t* tfull_bar = empty_bar + C::STAGES;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::HOLDER_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
+  int* s_toff = reinterpret_cast<int*>(smem + C::TABLE_OFF);
+  int* s_goff = s_toff + (kMaxGroups + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Group tables into shared memory.
+  int total_tiles;
+  if (p.num_groups > 0) {
+    for (int i = threadIdx.x; i <= p.num_groups; i += blockDim.x) {
+      s_toff[i] = p.tile_off[i];
+      s_goff[i] = p.group_off[i];
+    }
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 4 * 32);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  {
+    const int mtiles = p.num_groups > 0 ? s_toff[p.num_groups] : (p.M + BM - 1) / BM;
+    total_tiles = mtiles * p.n_tiles * p.splits;
+  }
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      uint32_t stage = 0, phase = 0;
+      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+        const TileCoord c = decode_tile(t, p, s_toff, s_goff);
+        const int brow = c.group * p.b_rows_per_group + c.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+        bool ok = true;
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          uint8_t* sa = smem + stage * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::A_BYTES;
+          mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+          tma_load_2d(sa, &tmA, &full_bar[stage], kt * BK, c.row0);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_2d(sb, &tmB, &full_bar[stage], kt * BK, brow);
+            tma_load_2d(sb + C::B_BYTES / 2, &tmB, &full_bar[stage], kt * BK, brow + p.b_gate_offset);
+          } else {
+            tma_load_2d(sb, &tmB, &full_bar[stage], kt * BK, brow);
+          }
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- UMMA issuer ----------------
+      constexpr uint32_t idesc = umma_idesc_bf16_f32(BM, BN);
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+        const TileCoord c = decode_tile(t, p, s_toff, s_goff);
+        const int acc = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!mbar_wait(&tempty_bar[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::ACC_STRIDE);
+        bool ok = true;
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint64_t a_desc = umma_sdesc_sw128(sa);
+          const uint64_t b_desc = umma_sdesc_sw128(sa + C::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            // advancing K by 16 bf16 = 32 bytes inside the swizzled row: +2 in 16-byte units
+            umma_bf16(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[acc]);
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5 ----------------
+    const int quad = warp & 3;                    // TMEM lanes this warp may read
+    const int row_in_tile = quad * 32 + lane;
+    int it = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+      const TileCoord c = decode_tile(t, p, s_toff, s_goff);
+      const int acc = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull_bar[acc], use & 1u, abort_flag, p.status) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
+      const bool row_ok = row_in_tile < c.rows;
+      const long long row = (long long)c.row0 + row_in_tile;
+      if (EPI == EPI_SWIGLU) {
+        constexpr int HALF = BN / 2;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+        for (int cc = 0; cc < HALF / 32; ++cc) {
+          uint32_t u[32], g[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(tbase + cc * 32, u);
+          tmem_ld_32x32b_x32(tbase + HALF + cc * 32, g);
+          tmem_ld_wait();
+          const int col0 = c.nt * HALF + cc * 32;
+          if (row_ok && col0 < p.N) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+              const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+              const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+              const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+              packed[i] = pack_bf16x2(h0, h1);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + row * p.ldo + col0);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          uint32_t v[32];
+          __syncwarp();
+          tmem_ld_32x32b_x32(tbase + cc * 32, v);
+          tmem_ld_wait();
+          const int col0 = c.nt * BN + cc * 32;
+          if (!row_ok || col0 >= p.N) continue;
+          if (EPI == EPI_F32) {
+            float* out = reinterpret_cast<float*>(p.out) + (long long)c.split * p.split_stride + row * p.ldo + col0;
+            if (col0 + 32 <= p.N && (p.ldo & 3) == 0) {
+              float4* dst = reinterpret_cast<float4*>(out);
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (col0 + i < p.N) out[i] = __uint_as_float(v[i]);
+            }
+          } else {
+            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + row * p.ldo + col0;
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+            uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    // let copies and MMAs already in flight land before the CTA's shared memory and TMEM go away
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) { }
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*PFN_tmapEncodeTiled)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                         const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                         CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                         CUtensorMapFloatOOBfill);
+
+static PFN_tmapEncodeTiled get_encoder() {
+  static PFN_tmapEncodeTiled fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_tmapEncodeTiled>(ptr);
+  }
+  return fn;
+}
+
+// bf16 (rows, cols) row-major matrix, box of box_rows x 64 columns, 128-byte swizzle.
+static bool make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+  PFN_tmapEncodeTiled enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+int pick_bn_f32(int n_cols) {
+  static const int cands[] = {256, 224, 128, 64, 32};
+  int best = 256;
+  long long best_cols = 1ll << 60;
+  for (int bn : cands) {
+    const long long padded = (long long)((n_cols + bn - 1) / bn) * bn;
+    if (padded < best_cols) { best_cols = padded; best = bn; }
+  }
+  return best;
+}
+
+int pick_splits(int tiles, int K) {
+  const int kt = (K + BK - 1) / BK;
+  const int sms = num_sms();
+  if (tiles * 2 > sms) return 1;
+  int s = std::max(1, sms / std::max(1, tiles));
+  s = std::min(s, std::max(1, kt / 4));  // at least 4 k-tiles per split
+  const int per = (kt + s - 1) / s;
+  return (kt + per - 1) / per;           // no empty split
+}
+
+template <int BN, int EPI>
+static cudaError_t launch_impl(const GemmProblem& q, const CUtensorMap& ta, const CUtensorMap& tb,
+                               const GemmParams& gp, int grid, cudaStream_t stream) {
+  using C = GemmCfg<BN>;
+  auto kern = gemm_tc_kernel<BN, EPI>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  (void)q;
+  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(ta, tb, gp);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
+  if (q.num_groups > kMaxGroups) return cudaErrorInvalidValue;
+  const int b_box = q.epilogue == EPI_SWIGLU ? q.bn / 2 : q.bn;
+  CUtensorMap ta, tb;
+  if (!make_tmap_bf16(&ta, q.A, q.M, q.K, BM)) return cudaErrorInvalidValue;
+  if (!make_tmap_bf16(&tb, q.B, q.b_rows_total, q.K, b_box)) return cudaErrorInvalidValue;
+
+  GemmParams gp;
+  gp.M = q.M;
+  gp.N = q.N;
+  gp.K = q.K;
+  gp.num_groups = q.num_groups;
+  gp.group_off = q.group_off;
+  gp.tile_off = q.tile_off;
+  gp.b_rows_per_group = q.b_rows_per_group;
+  gp.b_gate_offset = q.b_gate_offset;
+  const int out_cols_per_tile = q.epilogue == EPI_SWIGLU ? q.bn / 2 : q.bn;
+  gp.n_tiles = (q.N + out_cols_per_tile - 1) / out_cols_per_tile;
+  gp.kt_total = (q.K + BK - 1) / BK;
+  gp.splits = std::max(1, q.splits);
+  gp.kt_per_split = (gp.kt_total + gp.splits - 1) / gp.splits;
+  gp.out = q.out;
+  gp.ldo = q.ldo;
+  gp.split_stride = q.split_stride;
+  gp.status = q.status;
+
+  int grid = num_sms();
+  if (q.num_groups == 0) {
+    const int tiles = ((q.M + BM - 1) / BM) * gp.n_tiles * gp.splits;
+    grid = std::min(grid, std::max(1, tiles));
+  }
+
+  switch (q.epilogue) {
+    case EPI_SWIGLU:
+      if (q.bn == 256) return launch_impl<256, EPI_SWIGLU>(q, ta, tb, gp, grid, stream);
+      break;
+    case EPI_BF16:
+      if (q.bn == 256) return launch_impl<256, EPI_BF16>(q, ta, tb, gp, grid, stream);
+      break;
+    case EPI_F32:
+      switch (q.bn) {
+        case 256: return launch_impl<256, EPI_F32>(q, ta, tb, gp, grid, stream);
+        case 224: return launch_impl<224, EPI_F32>(q, ta, tb, gp, grid, stream);
+        case 128: return launch_impl<128, EPI_F32>(q, ta, tb, gp, grid, stream);
+        case 64: return launch_impl<64, EPI_F32>(q, ta, tb, gp, grid, stream);
+        case 32: return launch_impl<32, EPI_F32>(q, ta, tb, gp, grid, stream);
+      }
+      break;
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -1,0 +1,63 @@
+// Launchers shared between the translation units of the library (host side).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+enum GemmEpilogue { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2 };
+
+// C[M, N] = A[M, K] * B[N, K]^T per group, A and B bf16 K-major, fp32 accumulate.
+// Groups (optional) are contiguous row ranges of A / C given by device
+// offsets; group g multiplies with B rows [g * b_rows_per_group, ...).
+struct GemmProblem {
+  const void* A;          // (M, K) bf16
+  const void* B;          // (b_rows_total, K) bf16
+  int64_t b_rows_total;
+  int M, N, K;            // N: valid output columns per group
+  int num_groups;         // 0 = dense (one group of M rows)
+  const int* group_off;   // device (G+1) row offsets, grouped only
+  const int* tile_off;    // device (G+1) prefix sums of ceil(rows_g / 128), grouped only
+  int b_rows_per_group;
+  int b_gate_offset;      // swiglu: offset of the gate rows inside a group (= h)
+  int epilogue;           // GemmEpilogue
+  int bn;                 // UMMA N / B rows per tile (swiglu: up rows + gate rows)
+  int splits;             // split-K: >1 writes fp32 partial slices
+  void* out;
+  int64_t ldo;            // elements
+  int64_t split_stride;   // elements between split-K slices
+  int* status;
+};
+
+int num_sms();
+cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t stream);
+// UMMA N chosen for a dense fp32 GEMM with n_cols output columns.
+int pick_bn_f32(int n_cols);
+// split-K factor that fills the GPU for a dense GEMM with `tiles` output tiles and K.
+int pick_splits(int tiles, int K);
+
+cudaError_t launch_topk(const float* logits, int n_partials, int64_t partial_stride, const float* b_router,
+                        const float* score_bias, int T, int E, int k, int gating, float sig_eps, float p_norm,
+                        int restore, float ews, int orig_k, float* logits_out, int32_t* idx, float* w,
+                        int* status, cudaStream_t stream);
+
+cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, int32_t* offsets,
+                           int32_t* gather_idx, int32_t* scatter_idx, int k, int32_t* blk_scratch, int* status,
+                           cudaStream_t stream);
+int permute_blocks(int R);
+
+cudaError_t launch_tile_table(const int32_t* offsets, int E, int32_t* tile_off, cudaStream_t stream);
+cudaError_t launch_gather_rows(const void* src, const int32_t* gather_idx, int R, int T, int cols, void* dst,
+                               int* status, cudaStream_t stream);
+
+cudaError_t launch_combine(const void* y, const int32_t* scatter_idx, const float* w, int T, int k, int L,
+                           int R, int rms, float eps, const void* gain, void* z, int* status,
+                           cudaStream_t stream);
+cudaError_t launch_rmsnorm(const void* z, int T, int L, float eps, const void* gain, void* out,
+                           cudaStream_t stream);
+cudaError_t launch_splitk_reduce_bf16(const float* partials, int splits, int64_t slice, void* out,
+                                      cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,199 @@
+// Token permutation: histogram, scan and stable placement of the assignments.
+//
+// Assignment f = t*k + j of expert idx[f] goes to row
+//   offsets[e] + #{f' < f : idx[f'] == e}
+// (page "Как устроен Olmo-core 3: обучение больших MoE-моделей",
+// §"Пересылка токенов между экспертами": indices sorted by expert, bins =
+// cumulative sum of the per-expert counts).  Three passes over chunks of
+// kChunk assignments: per-chunk histograms; per-expert scan over chunks plus
+// the exclusive scan over experts; placement, where each warp walks its
+// slice of the chunk in order and ranks equal experts with __match_any_sync.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int kChunk = 4096;
+constexpr int kPermThreads = 256;
+constexpr int kPermWarps = kPermThreads / 32;
+constexpr int kSub = kChunk / kPermWarps;
+
+int permute_blocks(int R) { return (R + kChunk - 1) / kChunk; }
+
+__global__ void __launch_bounds__(kPermThreads) perm_count_kernel(const int32_t* __restrict__ idx, int R, int E,
+                                                                   int32_t* __restrict__ blk, int* status) {
+  extern __shared__ int32_t hist[];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kChunk;
+  const int end = min(R, base + kChunk);
+  for (int r = base + threadIdx.x; r < end; r += blockDim.x) {
+    const int e = idx[r];
+    if (e < 0 || e >= E) set_status(status, MOE_ERR_BOUNDS);
+    else atomicAdd(&hist[e], 1);
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x) blk[(long long)blockIdx.x * E + i] = hist[i];
+}
+
+// Block-wide exclusive scan of one value per thread (blockDim.x == 1024).
+__device__ int block_exclusive_scan(int v, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = warp > 0 ? s_warp[warp - 1] : 0;
+  return before + x - v;
+}
+
+// One block of 1024 threads: thread e owns expert e.
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ blk, int nblk, int E,
+                                                          int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets) {
+  __shared__ int s_warp[32];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int b = 0; b < nblk; ++b) {
+      const int c = blk[(long long)b * E + e];
+      blk[(long long)b * E + e] = run;
+      run += c;
+    }
+    counts[e] = run;
+  }
+  const int excl = block_exclusive_scan(e < E ? run : 0, s_warp);
+  if (e < E) {
+    offsets[e] = excl;
+    if (e == E - 1) offsets[E] = excl + run;
+    for (int b = 0; b < nblk; ++b) blk[(long long)b * E + e] += excl;
+  }
+}
+
+__global__ void __launch_bounds__(kPermThreads) perm_place_kernel(const int32_t* __restrict__ idx, int R, int E,
+                                                                   int k, const int32_t* __restrict__ blk,
+                                                                   int32_t* __restrict__ gather_idx,
+                                                                   int32_t* __restrict__ scatter_idx) {
+  extern __shared__ int32_t wh[];  // [kPermWarps][E]
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) wh[i] = 0;
+  __syncthreads();
+  const int base = blockIdx.x * kChunk;
+  const int end = min(R, base + kChunk);
+  const int s0 = base + warp * kSub;
+  const int s1 = min(end, s0 + kSub);
+  int32_t* mine = wh + warp * E;
+
+  // pass 1: this warp's per-expert counts
+  for (int r0 = s0; r0 < s1; r0 += 32) {
+    const int r = r0 + lane;
+    const int e = r < s1 ? idx[r] : -1;
+    const bool valid = e >= 0 && e < E;
+    const unsigned grp = __match_any_sync(0xffffffffu, valid ? e : -1);
+    if (valid && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
+  }
+  __syncthreads();
+  // bases: the chunk's base for expert e plus the counts of earlier warps
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = blk[(long long)blockIdx.x * E + e];
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int c = wh[w * E + e];
+      wh[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // pass 2: stable placement
+  const unsigned lt = (1u << lane) - 1u;
+  for (int r0 = s0; r0 < s1; r0 += 32) {
+    const int r = r0 + lane;
+    const int e = r < s1 ? idx[r] : -1;
+    const bool valid = e >= 0 && e < E;
+    const unsigned grp = __match_any_sync(0xffffffffu, valid ? e : -1);
+    int pos = 0;
+    if (valid) pos = mine[e] + __popc(grp & lt);
+    __syncwarp();
+    if (valid && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
+    __syncwarp();
+    if (valid) {
+      gather_idx[pos] = r / k;
+      scatter_idx[r] = pos;
+    }
+  }
+}
+
+cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, int32_t* offsets,
+                           int32_t* gather_idx, int32_t* scatter_idx, int k, int32_t* blk, int* status,
+                           cudaStream_t stream) {
+  const int nb = permute_blocks(R);
+  if (nb > 0) {
+    perm_count_kernel<<<nb, kPermThreads, E * sizeof(int32_t), stream>>>(idx, R, E, blk, status);
+  }
+  perm_scan_kernel<<<1, 1024, 0, stream>>>(blk, nb, E, counts, offsets);
+  if (nb > 0) {
+    const size_t sm = (size_t)kPermWarps * E * sizeof(int32_t);
+    perm_place_kernel<<<nb, kPermThreads, sm, stream>>>(idx, R, E, k, blk, gather_idx, scatter_idx);
+  }
+  return cudaGetLastError();
+}
+
+// tile_off[e] = sum over e' < e of ceil(count[e'] / 128); tile_off[E] = total tiles.
+__global__ void __launch_bounds__(1024) tile_table_kernel(const int32_t* __restrict__ offsets, int E,
+                                                           int32_t* __restrict__ tile_off) {
+  __shared__ int s_warp[32];
+  const int e = threadIdx.x;
+  const int tiles = e < E ? (offsets[e + 1] - offsets[e] + 127) / 128 : 0;
+  const int excl = block_exclusive_scan(tiles, s_warp);
+  if (e < E) {
+    tile_off[e] = excl;
+    if (e == E - 1) tile_off[E] = excl + tiles;
+  }
+}
+
+cudaError_t launch_tile_table(const int32_t* offsets, int E, int32_t* tile_off, cudaStream_t stream) {
+  tile_table_kernel<<<1, 1024, 0, stream>>>(offsets, E, tile_off);
+  return cudaGetLastError();
+}
+
+// dst[p, :] = src[gather_idx[p], :] for p < R; one warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
+                                                           const int32_t* __restrict__ gather_idx, int R, int T,
+                                                           int vec_per_row, uint4* __restrict__ dst,
+                                                           int* status) {
+  const int lane = threadIdx.x & 31;
+  const long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (p >= R) return;
+  const int t = gather_idx[p];
+  if (t < 0 || t >= T) {
+    if (lane == 0) set_status(status, MOE_ERR_BOUNDS);
+    return;
+  }
+  const uint4* s = src + (long long)t * vec_per_row;
+  uint4* d = dst + p * vec_per_row;
+  for (int c = lane; c < vec_per_row; c += 32) d[c] = s[c];
+}
+
+cudaError_t launch_gather_rows(const void* src, const int32_t* gather_idx, int R, int T, int cols, void* dst,
+                               int* status, cudaStream_t stream) {
+  if (R <= 0) return cudaSuccess;
+  const int warps = 8;
+  gather_rows_kernel<<<(R + warps - 1) / warps, 32 * warps, 0, stream>>>(
+      static_cast<const uint4*>(src), gather_idx, R, T, cols / 8, static_cast<uint4*>(dst), status);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

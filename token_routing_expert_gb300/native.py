@@ -1,0 +1,353 @@
+"""ctypes binding of ``libmoe_gb300.so``: argument marshalling only.
+
+Every function here has the name of the C entry point it calls and takes
+torch CUDA tensors; all arithmetic happens in the library's kernels.  There
+is no fallback: if the library is missing or no GPU is present, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from .workloads import GATING_NAMES, WorkloadSpec
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmoe_gb300.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_WORKSPACE",
+                4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_BOUNDS", 7: "MOE_ERR_NO_DEVICE"}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)} ({_status_string(code)})")
+
+
+class moe_config_t(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int32), ("num_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("hidden_size", ctypes.c_int32), ("latent_dim", ctypes.c_int32), ("up_proj_norm", ctypes.c_int32),
+                ("rms_eps", ctypes.c_float), ("gating", ctypes.c_int32),
+                ("sigmoid_stability_epsilon", ctypes.c_float), ("normalize_expert_weights", ctypes.c_float),
+                ("restore_weight_scale", ctypes.c_int32), ("expert_weight_scale", ctypes.c_float),
+                ("original_top_k", ctypes.c_int32), ("router_bias", ctypes.c_int32),
+                ("has_score_bias", ctypes.c_int32), ("activation", ctypes.c_int32)]
+
+
+class moe_weights_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("w_router", "b_router", "score_bias", "w_down_latent",
+                                                  "w_up_latent", "rms_weight", "w_up_gate", "w_out")]
+
+
+EXPORTS = ["moe_validate_config", "moe_num_params", "moe_num_active_params", "moe_latent_proj_params",
+           "moe_workspace_size", "moe_router", "moe_permute", "moe_grouped_swiglu", "moe_combine",
+           "moe_latent_down", "moe_latent_restore", "moe_layer_forward", "moe_layer_forward_staged",
+           "moe_layer_forward_launches", "moe_workspace_layout", "moe_get_status", "moe_status_string"]
+
+_lib = None
+
+
+def load() -> ctypes.CDLL:
+    """Loads the library (once).  Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with token_routing_expert_gb300.build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I64, SZ, VP = ctypes.POINTER, ctypes.c_int64, ctypes.c_size_t, ctypes.c_void_p
+    cfgp, wp = P(moe_config_t), P(moe_weights_t)
+    sig = {
+        "moe_validate_config": [cfgp],
+        "moe_num_params": [cfgp, P(I64)],
+        "moe_num_active_params": [cfgp, P(I64)],
+        "moe_latent_proj_params": [cfgp, ctypes.c_int, P(I64)],
+        "moe_workspace_size": [cfgp, I64, P(SZ)],
+        "moe_router": [cfgp, wp, VP, I64, VP, VP, VP, VP, SZ, VP],
+        "moe_permute": [cfgp, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
+        "moe_grouped_swiglu": [cfgp, wp, VP, VP, VP, I64, VP, VP, SZ, VP],
+        "moe_combine": [cfgp, VP, VP, VP, I64, VP, VP],
+        "moe_latent_down": [cfgp, wp, VP, I64, VP, VP, SZ, VP],
+        "moe_latent_restore": [cfgp, wp, VP, I64, VP, VP, SZ, VP],
+        "moe_layer_forward": [cfgp, wp, VP, I64, VP, VP, SZ, VP],
+        "moe_layer_forward_staged": [cfgp, wp, VP, I64, VP, VP, SZ, VP, P(VP)],
+        "moe_layer_forward_launches": [cfgp, I64, P(ctypes.c_int32)],
+        "moe_workspace_layout": [cfgp, I64, P(I64)],
+        "moe_get_status": [VP, P(ctypes.c_int32), ctypes.c_int],
+        "moe_status_string": [ctypes.c_int],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_char_p if name == "moe_status_string" else ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _status_string(code: int) -> str:
+    try:
+        return load().moe_status_string(code).decode()
+    except Exception:  # noqa: BLE001 - only for messages
+        return "?"
+
+
+def _check(code: int, where: str) -> None:
+    if code != MOE_OK:
+        raise MoEError(code, where)
+
+
+def make_config(d_model, num_experts, top_k, hidden_size, latent_dim=0, up_proj_norm=True, rms_eps=1e-6,
+                gating="softmax", sigmoid_stability_epsilon=0.0, normalize_expert_weights=0.0,
+                restore_weight_scale=False, expert_weight_scale=0.0, original_top_k=0, router_bias=False,
+                has_score_bias=False) -> moe_config_t:
+    g = GATING_NAMES[gating] if isinstance(gating, str) else int(gating)
+    return moe_config_t(d_model, num_experts, top_k, hidden_size, latent_dim, int(up_proj_norm), rms_eps, g,
+                        sigmoid_stability_epsilon, normalize_expert_weights, int(restore_weight_scale),
+                        expert_weight_scale, original_top_k, int(router_bias), int(has_score_bias), 0)
+
+
+def config_from_spec(spec: WorkloadSpec) -> moe_config_t:
+    return make_config(spec.d_model, spec.num_experts, spec.top_k, spec.hidden_size, spec.latent_dim,
+                       spec.up_proj_norm, spec.rms_eps, spec.gating, spec.sigmoid_stability_epsilon,
+                       spec.normalize_expert_weights, spec.restore_weight_scale, spec.expert_weight_scale,
+                       spec.original_top_k, spec.skew, spec.score_bias_std > 0)
+
+
+# ---------------------------------------------------------------------------
+# host-only functions
+# ---------------------------------------------------------------------------
+
+def moe_validate_config(cfg: moe_config_t) -> int:
+    return load().moe_validate_config(ctypes.byref(cfg))
+
+
+def moe_num_params(cfg: moe_config_t) -> int:
+    out = ctypes.c_int64()
+    _check(load().moe_num_params(ctypes.byref(cfg), ctypes.byref(out)), "moe_num_params")
+    return out.value
+
+
+def moe_num_active_params(cfg: moe_config_t) -> int:
+    out = ctypes.c_int64()
+    _check(load().moe_num_active_params(ctypes.byref(cfg), ctypes.byref(out)), "moe_num_active_params")
+    return out.value
+
+
+def moe_latent_proj_params(cfg: moe_config_t, with_norm_gain: bool = False) -> int:
+    out = ctypes.c_int64()
+    _check(load().moe_latent_proj_params(ctypes.byref(cfg), int(with_norm_gain), ctypes.byref(out)),
+           "moe_latent_proj_params")
+    return out.value
+
+
+def moe_workspace_size(cfg: moe_config_t, T: int) -> int:
+    out = ctypes.c_size_t()
+    _check(load().moe_workspace_size(ctypes.byref(cfg), T, ctypes.byref(out)), "moe_workspace_size")
+    return out.value
+
+
+def moe_workspace_layout(cfg: moe_config_t, T: int):
+    arr = (ctypes.c_int64 * 10)()
+    _check(load().moe_workspace_layout(ctypes.byref(cfg), T, arr), "moe_workspace_layout")
+    return list(arr)
+
+
+# ---------------------------------------------------------------------------
+# device entry points
+# ---------------------------------------------------------------------------
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, name="tensor") -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+@dataclass
+class DeviceWeights:
+    """The layer's weights on the device (bf16, fp32 for biases), kept alive by this object."""
+
+    w_router: torch.Tensor
+    w_up_gate: torch.Tensor
+    w_out: torch.Tensor
+    b_router: Optional[torch.Tensor] = None
+    score_bias: Optional[torch.Tensor] = None
+    w_down_latent: Optional[torch.Tensor] = None
+    w_up_latent: Optional[torch.Tensor] = None
+    rms_weight: Optional[torch.Tensor] = None
+
+    @staticmethod
+    def from_inputs(inp, device="cuda") -> "DeviceWeights":
+        def dev(name):
+            t = inp.get(name)
+            return None if t is None else t.to(device).contiguous()
+
+        return DeviceWeights(w_router=dev("w_router"), w_up_gate=dev("w_up_gate"), w_out=dev("w_out"),
+                             b_router=dev("b_router"), score_bias=dev("score_bias"),
+                             w_down_latent=dev("w_down"), w_up_latent=dev("w_up_latent"),
+                             rms_weight=dev("rms_weight"))
+
+    def struct(self) -> moe_weights_t:
+        bf, f32 = torch.bfloat16, torch.float32
+        return moe_weights_t(
+            _ptr(self.w_router, bf, "w_router"), _ptr(self.b_router, f32, "b_router"),
+            _ptr(self.score_bias, f32, "score_bias"), _ptr(self.w_down_latent, bf, "w_down_latent"),
+            _ptr(self.w_up_latent, bf, "w_up_latent"), _ptr(self.rms_weight, bf, "rms_weight"),
+            _ptr(self.w_up_gate, bf, "w_up_gate"), _ptr(self.w_out, bf, "w_out"))
+
+
+def workspace(cfg: moe_config_t, T: int, device="cuda") -> torch.Tensor:
+    """A device workspace of moe_workspace_size bytes (torch allocations are 256-byte aligned)."""
+    return torch.empty(max(1, moe_workspace_size(cfg, T)), dtype=torch.uint8, device=device)
+
+
+def moe_router(cfg, weights: DeviceWeights, x, ws, logits=None, idx=None, w=None, stream=None):
+    T = x.shape[0]
+    dev = x.device
+    idx = torch.empty((T, cfg.top_k), dtype=torch.int32, device=dev) if idx is None else idx
+    w = torch.empty((T, cfg.top_k), dtype=torch.float32, device=dev) if w is None else w
+    ws_ = weights.struct()
+    _check(load().moe_router(ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x, torch.bfloat16, "x"), T,
+                             _ptr(logits, torch.float32, "logits"), _ptr(idx, torch.int32, "idx"),
+                             _ptr(w, torch.float32, "weights"), _ptr(ws, None, "ws"), ws.numel(), _stream(stream)),
+           "moe_router")
+    return logits, idx, w
+
+
+def moe_permute(cfg, idx, ws, counts=None, offsets=None, gather_idx=None, scatter_idx=None, stream=None):
+    T = idx.shape[0]
+    R = T * cfg.top_k
+    dev = idx.device
+    E = cfg.num_experts
+    counts = torch.empty(E, dtype=torch.int32, device=dev) if counts is None else counts
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
+    gather_idx = torch.empty(max(R, 1), dtype=torch.int32, device=dev) if gather_idx is None else gather_idx
+    scatter_idx = torch.empty(max(R, 1), dtype=torch.int32, device=dev) if scatter_idx is None else scatter_idx
+    _check(load().moe_permute(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"), T,
+                              _ptr(counts, torch.int32, "counts"), _ptr(offsets, torch.int32, "offsets"),
+                              _ptr(gather_idx, torch.int32, "gather_idx"), _ptr(scatter_idx, torch.int32, "scatter_idx"),
+                              _ptr(ws, None, "ws"), ws.numel(), _stream(stream)), "moe_permute")
+    return counts, offsets, gather_idx[:R], scatter_idx[:R]
+
+
+def moe_grouped_swiglu(cfg, weights: DeviceWeights, x_routed, gather_idx, offsets, ws, y=None, stream=None):
+    T = x_routed.shape[0]
+    Lr = x_routed.shape[1]
+    y = torch.empty((T * cfg.top_k, Lr), dtype=torch.bfloat16, device=x_routed.device) if y is None else y
+    ws_ = weights.struct()
+    _check(load().moe_grouped_swiglu(ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x_routed, torch.bfloat16, "x_routed"),
+                                     _ptr(gather_idx, torch.int32, "gather_idx"), _ptr(offsets, torch.int32, "offsets"),
+                                     T, _ptr(y, torch.bfloat16, "y"), _ptr(ws, None, "ws"), ws.numel(),
+                                     _stream(stream)), "moe_grouped_swiglu")
+    return y
+
+
+def moe_combine(cfg, y, scatter_idx, w, T, z=None, stream=None):
+    Lr = y.shape[1]
+    z = torch.empty((T, Lr), dtype=torch.bfloat16, device=y.device) if z is None else z
+    _check(load().moe_combine(ctypes.byref(cfg), _ptr(y, torch.bfloat16, "y"), _ptr(scatter_idx, torch.int32, "scatter_idx"),
+                              _ptr(w, torch.float32, "weights"), T, _ptr(z, torch.bfloat16, "z"), _stream(stream)),
+           "moe_combine")
+    return z
+
+
+def moe_latent_down(cfg, weights: DeviceWeights, x, ws, x_routed=None, stream=None):
+    T = x.shape[0]
+    x_routed = torch.empty((T, cfg.latent_dim), dtype=torch.bfloat16, device=x.device) if x_routed is None else x_routed
+    ws_ = weights.struct()
+    _check(load().moe_latent_down(ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x, torch.bfloat16, "x"), T,
+                                  _ptr(x_routed, torch.bfloat16, "x_routed"), _ptr(ws, None, "ws"), ws.numel(),
+                                  _stream(stream)), "moe_latent_down")
+    return x_routed
+
+
+def moe_latent_restore(cfg, weights: DeviceWeights, z, ws, out=None, stream=None):
+    T = z.shape[0]
+    out = torch.empty((T, cfg.d_model), dtype=torch.bfloat16, device=z.device) if out is None else out
+    ws_ = weights.struct()
+    _check(load().moe_latent_restore(ctypes.byref(cfg), ctypes.byref(ws_), _ptr(z, torch.bfloat16, "z"), T,
+                                     _ptr(out, torch.bfloat16, "out"), _ptr(ws, None, "ws"), ws.numel(),
+                                     _stream(stream)), "moe_latent_restore")
+    return out
+
+
+def moe_layer_forward(cfg, weights: DeviceWeights, x, ws, out=None, stream=None):
+    T = x.shape[0]
+    out = torch.empty((T, cfg.d_model), dtype=torch.bfloat16, device=x.device) if out is None else out
+    ws_ = weights.struct()
+    _check(load().moe_layer_forward(ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x, torch.bfloat16, "x"), T,
+                                    _ptr(out, torch.bfloat16, "out"), _ptr(ws, None, "ws"), ws.numel(),
+                                    _stream(stream)), "moe_layer_forward")
+    return out
+
+
+STAGES = ["latent_down", "router_gemm", "topk", "permute", "gather", "grouped_gemm1_swiglu",
+          "grouped_gemm2", "combine", "latent_up"]
+
+
+def moe_layer_forward_staged(cfg, weights: DeviceWeights, x, ws, events, out=None, stream=None):
+    """moe_layer_forward recording 10 torch.cuda.Event objects at the stage boundaries."""
+    T = x.shape[0]
+    out = torch.empty((T, cfg.d_model), dtype=torch.bfloat16, device=x.device) if out is None else out
+    handles = (ctypes.c_void_p * 10)(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    ws_ = weights.struct()
+    _check(load().moe_layer_forward_staged(ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x, torch.bfloat16, "x"), T,
+                                           _ptr(out, torch.bfloat16, "out"), _ptr(ws, None, "ws"), ws.numel(),
+                                           _stream(stream), handles), "moe_layer_forward_staged")
+    return out
+
+
+def moe_layer_forward_launches(cfg, T: int) -> int:
+    n = ctypes.c_int32()
+    _check(load().moe_layer_forward_launches(ctypes.byref(cfg), T, ctypes.byref(n)), "moe_layer_forward_launches")
+    return n.value
+
+
+def moe_get_status(stream=None, clear: bool = True) -> int:
+    """Synchronises the stream and returns (and by default clears) the device status word."""
+    out = ctypes.c_int32()
+    _check(load().moe_get_status(_stream(stream), ctypes.byref(out), int(clear)), "moe_get_status")
+    return out.value
+
+
+def layer_intermediates(cfg, T, ws):
+    """Views into the workspace of the layer forward's intermediates (after moe_layer_forward)."""
+    o = moe_workspace_layout(cfg, T)
+    E, k = cfg.num_experts, cfg.top_k
+    Lr = cfg.latent_dim or cfg.d_model
+    R = T * k
+
+    def view(off, n, dtype, shape):
+        size = torch.tensor([], dtype=dtype).element_size()
+        return ws[off:off + n * size].view(dtype).view(*shape)
+
+    out = {
+        "idx": view(o[1], R, torch.int32, (T, k)),
+        "weights": view(o[2], R, torch.float32, (T, k)),
+        "counts": view(o[3], E, torch.int32, (E,)),
+        "offsets": view(o[4], E + 1, torch.int32, (E + 1,)),
+        "gather_idx": view(o[5], R, torch.int32, (R,)),
+        "scatter_idx": view(o[6], R, torch.int32, (R,)),
+        "y": view(o[8], R * Lr, torch.bfloat16, (R, Lr)),
+    }
+    if o[7] >= 0:
+        out["x_routed"] = view(o[7], T * cfg.latent_dim, torch.bfloat16, (T, cfg.latent_dim))
+    if o[9] >= 0:
+        out["z_normalised"] = view(o[9], T * cfg.latent_dim, torch.bfloat16, (T, cfg.latent_dim))
+    return out

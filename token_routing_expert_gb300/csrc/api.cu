@@ -47,6 +47,7 @@ struct Plan {
   bool latent;
   int router_bn, n_router_tiles;
   int router_splits, down_splits, up_splits;
+  int64_t logit_slice;
   size_t logits, idx, wts, counts, offsets, tile_off, blk, gather, scatter, xr, xp, H, Y, zn, part, total;
 };
 
@@ -75,7 +76,9 @@ void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
     o += align256(bytes);
     return at;
   };
-  p->logits = take((size_t)p->router_splits * T * p->E * 4);
+  // split-K: router_splits partial slices plus one for their sum (slices padded to 16 bytes)
+  p->logit_slice = ((int64_t)T * p->E + 3) & ~int64_t(3);
+  p->logits = take((size_t)(p->router_splits > 1 ? p->router_splits + 1 : 1) * p->logit_slice * 4);
   p->idx = take((size_t)p->R * 4);
   p->wts = take((size_t)p->R * 4);
   p->counts = take((size_t)p->E * 4);
@@ -182,14 +185,14 @@ int run_router(const moe_config_t* c, const moe_weights_t* w, const void* x, con
   q.splits = p.router_splits;
   q.out = gemm_out;
   q.ldo = p.E;
-  q.split_stride = p.T * p.E;
+  q.split_stride = p.logit_slice;
   q.status = status;
   int s = cuda_status(launch_gemm(q, st));
   if (s != MOE_OK) return s;
   mark(ev, 2, st);
   const bool rewrite = logits_user && (p.router_splits > 1 || (c->router_bias && w->b_router));
   float* logits_out = rewrite ? logits_user : nullptr;
-  return cuda_status(launch_topk(gemm_out, p.router_splits, p.T * p.E, c->router_bias ? w->b_router : nullptr,
+  return cuda_status(launch_topk(gemm_out, p.router_splits, p.logit_slice, c->router_bias ? w->b_router : nullptr,
                                  c->has_score_bias ? w->score_bias : nullptr, (int)p.T, p.E, p.k, c->gating,
                                  c->sigmoid_stability_epsilon, c->normalize_expert_weights,
                                  c->restore_weight_scale, c->expert_weight_scale, c->original_top_k, logits_out, idx,
@@ -204,6 +207,8 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   void* H = at<void>(ws, p.H);
   int s = cuda_status(launch_tile_table(offsets, p.E, tile_off, st));
   if (s != MOE_OK) return s;
+  // rows of the experts' input in permuted order (a TMA tile::gather4 A-load was
+  // measured 3x slower than this copy plus tiled loads)
   s = cuda_status(launch_gather_rows(xr, gather, (int)p.R, (int)p.T, p.Lr, xp, status, st));
   if (s != MOE_OK) return s;
   mark(ev, 5, st);
@@ -484,7 +489,7 @@ int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
   make_plan(c, T, std::min(num_sms(), kSizingSms), &p);
   int k = 0;
   if (p.latent) k += p.down_splits > 1 ? 2 : 1;  // latent down (+ split-K reduce)
-  k += 2;                                        // router GEMM, top-k
+  k += p.router_splits > 1 ? 3 : 2;              // router GEMM, (split-K sum,) top-k
   k += 3;                                        // permute: count, scan, place
   k += 2;                                        // tile table, row gather
   k += 2;                                        // grouped GEMM 1 (SwiGLU), grouped GEMM 2

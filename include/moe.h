@@ -226,6 +226,31 @@ int moe_layer_forward_launches(const moe_config_t* cfg, int64_t T, int32_t* n);
  * [9] z or normalised z (T, L') bf16 (latent only, else -1). */
 int moe_workspace_layout(const moe_config_t* cfg, int64_t T, int64_t offsets_out[10]);
 
+/*
+ * moe_permute without a workspace: for callers that may not allocate device
+ * memory at all.  The page has no counterpart; this is a library convenience.
+ * Such callers include serving loops that hand every byte of device memory to
+ * their own pool at start-up (cudaMalloc later would fail, or block the device
+ * while it synchronises), and plug-in hosts that give a library only its
+ * input and output buffers.
+ *
+ * Same arguments, results and device-side checks as moe_permute, minus ws.
+ * The histogram scratch lives in one 2 MiB array of static device memory,
+ * which every GPU that loads this library keeps until the process exits.
+ * Limit: ceil(T * top_k / 4096) * num_experts <= 524288 (for 896 experts,
+ * T * top_k up to about 2.39 million); larger calls return
+ * MOE_ERR_UNSUPPORTED and enqueue nothing.
+ * The first call on each device looks up the array's device address (a
+ * runtime query, no allocation); make that first call before any stream
+ * capture.  The call allocates and frees nothing.
+ * All calls share the one array and it keeps the last call's contents (each
+ * call overwrites every entry it reads, so no clearing is needed): calls that
+ * can overlap on the GPU -- different streams, or different host threads --
+ * race on it and must be ordered by the caller.
+ */
+int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* idx, int64_t T, int32_t* counts, int32_t* offsets,
+                        int32_t* gather_idx, int32_t* scatter_idx, moe_stream_t stream);
+
 /* Synchronises `stream`, then returns (and clears, if `clear`) the device
  * status word of the current device in *device_status. */
 int moe_get_status(moe_stream_t stream, int32_t* device_status, int clear);

@@ -269,6 +269,9 @@ int run_restore(const moe_config_t* c, const moe_weights_t* w, const void* z, bo
 }
 
 }  // namespace
+
+int* device_status() { return status_ptr(); }
+
 }  // namespace moe
 
 using namespace moe;

@@ -32,6 +32,8 @@ struct GemmProblem {
 };
 
 int num_sms();
+// Device address of the per-device status word on the current device (NULL without a device).
+int* device_status();
 cudaError_t launch_gemm(const GemmProblem& p, cudaStream_t stream);
 // UMMA N chosen for a dense fp32 GEMM with n_cols output columns.
 int pick_bn_f32(int n_cols);

@@ -8,6 +8,8 @@
 // kChunk assignments: per-chunk histograms; per-expert scan over chunks plus
 // the exclusive scan over experts; placement, where each warp walks its
 // slice of the chunk in order and ranks equal experts with __match_any_sync.
+#include <algorithm>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -196,4 +198,56 @@ cudaError_t launch_gather_rows(const void* src, const int32_t* gather_idx, int R
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// moe_permute_noalloc: the same permutation with its scratch in static device memory
+// ---------------------------------------------------------------------------
+
+// Per-chunk expert histograms of moe_permute_noalloc.  Every GPU that loads the
+// library reserves this array until the process exits.
+constexpr int64_t kNoAllocScratchInts = int64_t(1) << 19;  // 2 MiB
+static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
+
+namespace {
+constexpr int kMaxScratchDevices = 64;
+int32_t* g_permute_scratch_addr[kMaxScratchDevices] = {nullptr};
+}  // namespace
+
+// Device address of g_permute_scratch on the current device, looked up once per
+// device (the host-side symbol is only a stand-in, never a device address).
+static int scratch_address(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return MOE_ERR_NO_DEVICE;
+  if (!g_permute_scratch_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_permute_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
+    g_permute_scratch_addr[dev] = static_cast<int32_t*>(ptr);
+  }
+  *out = g_permute_scratch_addr[dev];
+  return MOE_OK;
+}
+
 }  // namespace moe
+
+extern "C" int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* idx, int64_t T, int32_t* counts,
+                                   int32_t* offsets, int32_t* gather_idx, int32_t* scatter_idx,
+                                   moe_stream_t stream) {
+  int s = moe_validate_config(cfg);
+  if (s != MOE_OK) return s;
+  if (T < 0 || !counts || !offsets) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!idx || !gather_idx || !scatter_idx)) return MOE_ERR_INVALID_ARG;
+  if (T * cfg->top_k > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  const int R = (int)(T * cfg->top_k);
+  // the histograms need one int per (chunk, expert): beyond the static array, refuse
+  const int64_t need = (int64_t)std::max(1, moe::permute_blocks(R)) * cfg->num_experts;
+  if (need > moe::kNoAllocScratchInts) return MOE_ERR_UNSUPPORTED;
+  int32_t* scratch = nullptr;
+  s = moe::scratch_address(&scratch);
+  if (s != MOE_OK) return s;
+  int* status = moe::device_status();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  // every histogram entry the scan reads is written by this call first: nothing to clear
+  return moe::launch_permute(idx, R, cfg->num_experts, counts, offsets, gather_idx, scatter_idx, cfg->top_k, scratch,
+                             status, (cudaStream_t)stream) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}

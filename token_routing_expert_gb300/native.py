@@ -47,7 +47,8 @@ class moe_weights_t(ctypes.Structure):
 EXPORTS = ["moe_validate_config", "moe_num_params", "moe_num_active_params", "moe_latent_proj_params",
            "moe_workspace_size", "moe_router", "moe_permute", "moe_grouped_swiglu", "moe_combine",
            "moe_latent_down", "moe_latent_restore", "moe_layer_forward", "moe_layer_forward_staged",
-           "moe_layer_forward_launches", "moe_workspace_layout", "moe_get_status", "moe_status_string"]
+           "moe_layer_forward_launches", "moe_workspace_layout", "moe_get_status", "moe_status_string",
+           "moe_permute_noalloc"]
 
 _lib = None
 
@@ -80,6 +81,7 @@ def load() -> ctypes.CDLL:
         "moe_workspace_layout": [cfgp, I64, P(I64)],
         "moe_get_status": [VP, P(ctypes.c_int32), ctypes.c_int],
         "moe_status_string": [ctypes.c_int],
+        "moe_permute_noalloc": [cfgp, VP, I64, VP, VP, VP, VP, VP],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -244,6 +246,17 @@ def moe_permute(cfg, idx, ws, counts=None, offsets=None, gather_idx=None, scatte
                               _ptr(gather_idx, torch.int32, "gather_idx"), _ptr(scatter_idx, torch.int32, "scatter_idx"),
                               _ptr(ws, None, "ws"), ws.numel(), _stream(stream)), "moe_permute")
     return counts, offsets, gather_idx[:R], scatter_idx[:R]
+
+
+def moe_permute_noalloc(cfg, idx, counts, offsets, gather_idx, scatter_idx, stream=None):
+    """moe_permute with no workspace (the library's static scratch); outputs are the caller's tensors."""
+    T = idx.shape[0]
+    _check(load().moe_permute_noalloc(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"), T,
+                                      _ptr(counts, torch.int32, "counts"), _ptr(offsets, torch.int32, "offsets"),
+                                      _ptr(gather_idx, torch.int32, "gather_idx"),
+                                      _ptr(scatter_idx, torch.int32, "scatter_idx"), _stream(stream)),
+           "moe_permute_noalloc")
+    return counts, offsets, gather_idx, scatter_idx
 
 
 def moe_grouped_swiglu(cfg, weights: DeviceWeights, x_routed, gather_idx, offsets, ws, y=None, stream=None):

@@ -124,6 +124,34 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(inside), "window": window}
 
 
+def bench_config(spec: W.WorkloadSpec, world: int) -> dict:
+    """The `config` object of the JSON line (identical keys in both arms)."""
+    return {"workload": workload_desc(spec), "T_per_gpu": spec.T, "global_tokens": world * spec.T,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
+def rank_inputs(spec: W.WorkloadSpec, rank: int, experts: bool = True):
+    """Inputs of one replica: shared weights, and a batch of tokens of the rank's own."""
+    inp = W.generate(spec, experts=experts)
+    if rank > 0:
+        inp["x"] = W.generate(spec.with_(seed=spec.seed * 1000 + rank), experts=False)["x"]
+    return inp
+
+
+def max_over_ranks(value: float, dist, device) -> float:
+    """The slowest rank's value (the job's time); identity without a process group."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job throughput: all ranks' tokens over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 def kernel_traffic(workload: str):
     """Per-launch DRAM bytes of the grouped SwiGLU GEMM from the committed ncu summary,
     if the kernel source has not changed since it was captured."""
@@ -198,7 +226,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_desc(spec), "T": spec.T, "parallelism": "replicas"},
+        "config": bench_config(spec, args.gpus),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"first {n} of {spec.T} tokens per step, full layer in float64 numpy"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -227,9 +255,7 @@ def run_native(args):
     native.load()
     spec = W.WORKLOADS[args.config]
     # each rank draws its own batch of tokens (weak scaling); weights are shared replicas
-    inp = W.generate(spec)
-    if world > 1 and rank > 0:
-        inp["x"] = W.generate(spec.with_(seed=spec.seed * 1000 + rank), experts=False)["x"]
+    inp = rank_inputs(spec, rank)
     cfg = native.config_from_spec(spec)
     wts = native.DeviceWeights.from_inputs(inp)
     T = spec.T
@@ -281,10 +307,7 @@ def run_native(args):
     stage_ms = {}
     for s, name in enumerate(native.STAGES, start=1):
         stage_ms[name] = sum(evs[i][s - 1].elapsed_time(evs[i][s]) for i in range(args.steps)) / args.steps
-    if dist is not None:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dist, "cuda")
 
     # end to end: pinned host input -> device, forward, output -> pinned host, every step
     x_host = inp["x"].pin_memory()
@@ -307,11 +330,7 @@ def run_native(args):
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = e0.elapsed_time(e1) / args.steps
-    if dist is not None:
-        t = torch.tensor([e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, dist, "cuda")
     if native.moe_get_status() != 0:
         raise SystemExit("device status error in the end-to-end region")
 
@@ -330,7 +349,7 @@ def run_native(args):
         return
     line = {
         "metric": METRIC,
-        "value": world * T / (ms * 1e-3),
+        "value": job_tokens_per_s(world, T, ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -341,11 +360,9 @@ def run_native(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded numpy PCG64 normals rounded to bf16; random-init weights)",
-        "config": {"workload": workload_desc(spec), "T_per_gpu": T, "global_tokens": world * T,
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": ("flushed between steps (working set below 2x L2)" if flush else
-                          f"no flush: algorithmic bytes per step {alg_bytes / 1e6:.0f} MB > L2 "
-                          f"{L2 / 1e6:.0f} MB")},
+        "config": dict(bench_config(spec, world),
+                       l2=("flushed between steps (working set below 2x L2)" if flush else
+                           f"no flush: algorithmic bytes per step {alg_bytes / 1e6:.0f} MB > L2 {L2 / 1e6:.0f} MB")),
         "layer": {"tflops": tflops, "frac_bf16_peak": tflops / peak_tf, "gbs": gbs,
                   "frac_hbm_peak": gbs / peaks["hbm_gbs"], "bound": bound_layer,
                   "roofline_ms": roof_ms, "frac_of_roofline": roof_ms / ms, "experts_touched": touched,
@@ -356,7 +373,7 @@ def run_native(args):
                      "traffic": kernel_traffic(spec.name),
                      "peak_source": f"{peak_kind} bf16 burst (MEASURED_PEAKS.json)" if peak_kind == "measured"
                      else "fallback 1.9 PFLOP/s bf16"},
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": job_tokens_per_s(world, T, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
         "gpu_launches": args.steps * native.moe_layer_forward_launches(cfg, T),
         "clocks": clock_info,

@@ -47,6 +47,13 @@ CASES = {
     "max_experts": WorkloadSpec("max_experts", T=200, d_model=128, num_experts=1024, top_k=32, hidden_size=64,
                                 gating="sigmoid", seed=17),
     "one_token": WorkloadSpec("one_token", T=1, d_model=256, num_experts=8, top_k=2, hidden_size=128, seed=18),
+    # >= 384 rows per expert: the grouped GEMMs run on CTA pairs with 256-row tiles
+    "pair_tiles": WorkloadSpec("pair_tiles", T=3000, d_model=512, num_experts=8, top_k=4, hidden_size=256,
+                               gating="topk_softmax", seed=20),
+    "pair_tiles_ragged_h": WorkloadSpec("pair_tiles_ragged_h", T=2500, d_model=512, num_experts=8, top_k=2,
+                                        hidden_size=320, gating="sigmoid", normalize_expert_weights=1.0, seed=21),
+    "pair_tiles_latent": WorkloadSpec("pair_tiles_latent", T=2000, d_model=768, num_experts=4, top_k=2,
+                                      hidden_size=192, latent_dim=256, gating="softmax", skew=True, seed=22),
 }
 
 _cache = {}
@@ -163,7 +170,8 @@ def test_grouped_swiglu(name):
     assert_close_layer(y.double().cpu().numpy(), want, "grouped swiglu")
 
 
-@pytest.mark.parametrize("name", ["tiny", "sigmoid_bias_restore", "latent_skew", "max_experts", "one_token"])
+@pytest.mark.parametrize("name", ["tiny", "sigmoid_bias_restore", "latent_skew", "max_experts", "one_token",
+                                  "pair_tiles"])
 def test_combine(name):
     spec, inp, cfg, wts = setup(name)
     T, k, Lr = spec.T, spec.top_k, spec.routed_dim
@@ -180,7 +188,7 @@ def test_combine(name):
     assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-5), np.abs(got - want).max()
 
 
-@pytest.mark.parametrize("name", ["latent_skew", "latent_decode_small"])
+@pytest.mark.parametrize("name", ["latent_skew", "latent_decode_small", "pair_tiles_latent"])
 def test_latent_down_and_restore(name):
     spec, inp, cfg, wts = setup(name)
     T, D, L = spec.T, spec.d_model, spec.latent_dim

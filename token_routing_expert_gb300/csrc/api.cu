@@ -128,6 +128,9 @@ int check_call(const moe_config_t* c, int64_t T, void* ws, size_t ws_bytes, Plan
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// CTA-pair tiles (256 rows) pay off when the average group holds several of them.
+int use_pair_tiles(const Plan& p) { return p.R >= (int64_t)384 * p.E ? 1 : 0; }
+
 template <typename T>
 T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
@@ -205,7 +208,10 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   int32_t* tile_off = at<int32_t>(ws, p.tile_off);
   void* xp = at<void>(ws, p.xp);
   void* H = at<void>(ws, p.H);
-  int s = cuda_status(launch_tile_table(offsets, p.E, tile_off, st));
+  // large groups run on CTA pairs with 256-row tiles; small ones keep 128-row tiles,
+  // which waste less of the last partial tile of each group
+  const int pair = use_pair_tiles(p);
+  int s = cuda_status(launch_tile_table(offsets, p.E, pair ? 256 : 128, tile_off, st));
   if (s != MOE_OK) return s;
   // rows of the experts' input in permuted order (a TMA tile::gather4 A-load was
   // measured 3x slower than this copy plus tiled loads)
@@ -227,6 +233,7 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   g1.epilogue = EPI_SWIGLU;
   g1.bn = 256;
   g1.splits = 1;
+  g1.pair_tiles = pair;
   g1.out = H;
   g1.ldo = p.h;
   g1.status = status;
@@ -247,6 +254,7 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   g2.epilogue = EPI_BF16;
   g2.bn = 256;
   g2.splits = 1;
+  g2.pair_tiles = pair;
   g2.out = y;
   g2.ldo = p.Lr;
   g2.status = status;

@@ -71,6 +71,7 @@ struct TileCoord {
   int kt0, kt1; // k-tile range
 };
 
+template <int ROWS = BM>
 __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, const int* s_toff,
                                                  const int* s_goff) {
   TileCoord c;
@@ -92,11 +93,81 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
     row_base = s_goff[lo];
     row_end = s_goff[lo + 1];
   }
-  c.row0 = row_base + mt_local * BM;
-  c.rows = min(BM, row_end - c.row0);
+  c.row0 = row_base + mt_local * ROWS;
+  c.rows = min(ROWS, row_end - c.row0);
   c.kt0 = c.split * p.kt_per_split;
   c.kt1 = min(p.kt_total, c.kt0 + p.kt_per_split);
   return c;
+}
+
+// Epilogue of one tile for the 32 rows a warp owns: TMEM -> registers -> global.
+// row_in_tile: this thread's row of the 128-row accumulator; rows: valid rows from row0.
+template <int BN, int EPI>
+__device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, int row_in_tile, int nt, int split,
+                                           const GemmParams& p) {
+  const bool row_ok = row_in_tile < rows;
+  const long long row = (long long)row0 + row_in_tile;
+  if (EPI == EPI_SWIGLU) {
+    constexpr int HALF = BN / 2;
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 1
+    for (int cc = 0; cc < HALF / 32; ++cc) {
+      uint32_t u[32], g[32];
+      __syncwarp();
+      tmem_ld_32x32b_x32(tbase + cc * 32, u);
+      tmem_ld_32x32b_x32(tbase + HALF + cc * 32, g);
+      tmem_ld_wait();
+      const int col0 = nt * HALF + cc * 32;
+      if (row_ok && col0 < p.N) {
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+          const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
+          const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
+          const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+          packed[i] = pack_bf16x2(h0, h1);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(out + row * p.ldo + col0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      }
+    }
+  } else {
+#pragma unroll 1
+    for (int cc = 0; cc < BN / 32; ++cc) {
+      uint32_t v[32];
+      __syncwarp();
+      tmem_ld_32x32b_x32(tbase + cc * 32, v);
+      tmem_ld_wait();
+      const int col0 = nt * BN + cc * 32;
+      if (!row_ok || col0 >= p.N) continue;
+      if (EPI == EPI_F32) {
+        float* out = reinterpret_cast<float*>(p.out) + (long long)split * p.split_stride + row * p.ldo + col0;
+        if (col0 + 32 <= p.N && (p.ldo & 3) == 0) {
+          float4* dst = reinterpret_cast<float4*>(out);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (col0 + i < p.N) out[i] = __uint_as_float(v[i]);
+        }
+      } else {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + row * p.ldo + col0;
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+        uint4* dst = reinterpret_cast<uint4*>(out);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+      }
+    }
+  }
 }
 
 template <int BN, int EPI>
@@ -224,69 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
-      const bool row_ok = row_in_tile < c.rows;
-      const long long row = (long long)c.row0 + row_in_tile;
-      if (EPI == EPI_SWIGLU) {
-        constexpr int HALF = BN / 2;
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-#pragma unroll 1
-        for (int cc = 0; cc < HALF / 32; ++cc) {
-          uint32_t u[32], g[32];
-          __syncwarp();
-          tmem_ld_32x32b_x32(tbase + cc * 32, u);
-          tmem_ld_32x32b_x32(tbase + HALF + cc * 32, g);
-          tmem_ld_wait();
-          const int col0 = c.nt * HALF + cc * 32;
-          if (row_ok && col0 < p.N) {
-            uint32_t packed[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
-              const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-              const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-              const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
-              packed[i] = pack_bf16x2(h0, h1);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(out + row * p.ldo + col0);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-          }
-        }
-      } else {
-#pragma unroll 1
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          uint32_t v[32];
-          __syncwarp();
-          tmem_ld_32x32b_x32(tbase + cc * 32, v);
-          tmem_ld_wait();
-          const int col0 = c.nt * BN + cc * 32;
-          if (!row_ok || col0 >= p.N) continue;
-          if (EPI == EPI_F32) {
-            float* out = reinterpret_cast<float*>(p.out) + (long long)c.split * p.split_stride + row * p.ldo + col0;
-            if (col0 + 32 <= p.N && (p.ldo & 3) == 0) {
-              float4* dst = reinterpret_cast<float4*>(out);
-#pragma unroll
-              for (int i = 0; i < 8; ++i)
-                dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-            } else {
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (col0 + i < p.N) out[i] = __uint_as_float(v[i]);
-            }
-          } else {
-            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + row * p.ldo + col0;
-            uint32_t packed[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-            uint4* dst = reinterpret_cast<uint4*>(out);
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
-          }
-        }
-      }
+      store_tile<BN, EPI>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
@@ -301,6 +310,172 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_after();
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
+}
+
+
+// ---------------------------------------------------------------------------
+// CTA-pair variant: a cluster of two CTAs computes 256 x 256 tiles with
+// tcgen05.mma.cta_group::2.  CTA r stages A rows [128r, 128r+128) of the tile
+// and B rows [128r, 128r+128) of the 256-row B tile (for SwiGLU: CTA 0 the 128
+// "up" rows, CTA 1 the 128 "gate" rows), so a stage is 32 KB per CTA and the
+// ring is 6 deep.  Only CTA 0 issues MMAs; both CTAs' TMA loads complete on
+// CTA 0's full barrier; MMA completion is multicast to both CTAs' empty and
+// accumulator-full barriers; both epilogues release the accumulator on CTA 0.
+// ---------------------------------------------------------------------------
+constexpr int BM2 = 256;
+
+struct PairCfg {
+  static constexpr int BN = 256;
+  static constexpr int A_BYTES = 128 * BK * 2;
+  static constexpr int B_BYTES = (BN / 2) * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = 6;
+  static constexpr int ACC_STRIDE = 256;
+  static constexpr int TMEM_COLS = 512;
+  static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 4;
+  static constexpr int HOLDER_OFF = BAR_OFF + NUM_BARS * 8;
+  static constexpr int ABORT_OFF = HOLDER_OFF + 4;
+  static constexpr int TABLE_OFF = (ABORT_OFF + 4 + 15) & ~15;
+  static constexpr int SMEM_BYTES = TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 1024;
+};
+
+template <int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmParams p) {
+  using C = PairCfg;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty_bar = full_bar + C::STAGES;
+  uint64_t* tfull_bar = empty_bar + C::STAGES;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::HOLDER_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
+  int* s_toff = reinterpret_cast<int*>(smem + C::TABLE_OFF);
+  int* s_goff = s_toff + (kMaxGroups + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1;
+  const int npairs = gridDim.x >> 1;
+
+  if (p.num_groups > 0) {
+    for (int i = threadIdx.x; i <= p.num_groups; i += blockDim.x) {
+      s_toff[i] = p.tile_off[i];
+      s_goff[i] = p.group_off[i];
+    }
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);     // CTA 0 only: its producer's arrive + both CTAs' bytes
+      mbar_init(&empty_bar[s], 1);    // one multicast commit per use
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);    // one multicast commit per tile
+      mbar_init(&tempty_bar[a], 8);   // CTA 0 only: one lane of each of the 2 x 4 epilogue warps
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int mtiles = p.num_groups > 0 ? s_toff[p.num_groups] : (p.M + BM2 - 1) / BM2;
+  const int total_tiles = mtiles * p.n_tiles;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs) ----------------
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = pair; t < total_tiles && ok; t += npairs) {
+        const TileCoord c = decode_tile<BM2>(t, p, s_toff, s_goff);
+        const int arow = c.row0 + 128 * (int)rank;
+        const int brow = EPI == EPI_SWIGLU
+                             ? c.group * p.b_rows_per_group + c.nt * 128 + (rank ? p.b_gate_offset : 0)
+                             : c.group * p.b_rows_per_group + c.nt * C::BN + 128 * (int)rank;
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          if (!mbar_wait_cluster(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          uint8_t* sa = smem + stage * C::STAGE_BYTES;
+          const uint32_t full0 = map_to_cta(smem_u32(&full_bar[stage]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE_BYTES);
+          tma_load_2d_pair(sa, &tmA, full0, kt * BK, arow);
+          tma_load_2d_pair(sa + C::A_BYTES, &tmB, full0, kt * BK, brow);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- UMMA issuer (CTA 0) ----------------
+      constexpr uint32_t idesc = umma_idesc_bf16_f32(BM2, C::BN);
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      for (int t = pair; t < total_tiles; t += npairs, ++it) {
+        const TileCoord c = decode_tile<BM2>(t, p, s_toff, s_goff);
+        const int acc = it & 1;
+        const uint32_t use = (uint32_t)(it >> 1);
+        if (!mbar_wait_cluster(&tempty_bar[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::ACC_STRIDE);
+        bool ok = true;
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          if (!mbar_wait_cluster(&full_bar[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint64_t a_desc = umma_sdesc_sw128(sa);
+          const uint64_t b_desc = umma_sdesc_sw128(sa + C::A_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / UMMA_K; ++kk)
+            umma_bf16_pair(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+          umma_commit_pair(&empty_bar[stage], 0x3);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull_bar[acc], 0x3);
+      }
+    }
+  } else {
+    // ---------------- epilogue: warps 2..5 of both CTAs ----------------
+    const int quad = warp & 3;
+    const int row_in_tile = quad * 32 + lane;
+    int it = 0;
+    for (int t = pair; t < total_tiles; t += npairs, ++it) {
+      const TileCoord c = decode_tile<BM2>(t, p, s_toff, s_goff);
+      const int acc = it & 1;
+      const uint32_t use = (uint32_t)(it >> 1);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait_cluster(&tfull_bar[acc], use & 1u, abort_flag, p.status) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
+      store_tile<C::BN, EPI>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt, 0, p);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&tempty_bar[acc]), 0));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync_all();   // no CTA leaves while its partner may still touch its shared memory or TMEM
+  if (*abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) { }
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
 }
 
 // ---------------------------------------------------------------------------
@@ -382,9 +557,43 @@ static cudaError_t launch_impl(const GemmProblem& q, const CUtensorMap& ta, cons
   return cudaGetLastError();
 }
 
+template <int EPI>
+static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp, int tiles,
+                                    cudaStream_t stream) {
+  auto kern = gemm_tc_pair_kernel<EPI>;
+  static bool attr_set = false;
+  static int max_pairs = 0;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * num_sms());
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = 2;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    max_pairs = n > 0 ? n : 1;
+    attr_set = true;
+  }
+  int pairs = max_pairs;
+  if (tiles > 0) pairs = std::min(pairs, tiles);
+  kern<<<2 * pairs, kThreads, PairCfg::SMEM_BYTES, stream>>>(ta, tb, gp);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   if (q.num_groups > kMaxGroups) return cudaErrorInvalidValue;
-  const int b_box = q.epilogue == EPI_SWIGLU ? q.bn / 2 : q.bn;
+  const bool pair = q.pair_tiles != 0;
+  if (pair && (q.bn != 256 || q.splits > 1 || q.epilogue == EPI_F32)) return cudaErrorInvalidValue;
+  const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
   CUtensorMap ta, tb;
   if (!make_tmap_bf16(&ta, q.A, q.M, q.K, BM)) return cudaErrorInvalidValue;
   if (!make_tmap_bf16(&tb, q.B, q.b_rows_total, q.K, b_box)) return cudaErrorInvalidValue;
@@ -408,6 +617,11 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.split_stride = q.split_stride;
   gp.status = q.status;
 
+  if (pair) {
+    const int tiles = q.num_groups == 0 ? ((q.M + BM2 - 1) / BM2) * gp.n_tiles : 0;
+    if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU>(ta, tb, gp, tiles, stream);
+    return launch_pair_impl<EPI_BF16>(ta, tb, gp, tiles, stream);
+  }
   int grid = num_sms();
   if (q.num_groups == 0) {
     const int tiles = ((q.M + BM - 1) / BM) * gp.n_tiles * gp.splits;

@@ -25,6 +25,8 @@ struct GemmProblem {
   int epilogue;           // GemmEpilogue
   int bn;                 // UMMA N / B rows per tile (swiglu: up rows + gate rows)
   int splits;             // split-K: >1 writes fp32 partial slices
+  int pair_tiles;         // 1: 256-row tiles on CTA pairs (tcgen05 cta_group::2); bn 256, no split-K,
+                          //    and tile_off counts 256-row tiles
   void* out;
   int64_t ldo;            // elements
   int64_t split_stride;   // elements between split-K slices
@@ -50,7 +52,8 @@ cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, in
                            cudaStream_t stream);
 int permute_blocks(int R);
 
-cudaError_t launch_tile_table(const int32_t* offsets, int E, int32_t* tile_off, cudaStream_t stream);
+cudaError_t launch_tile_table(const int32_t* offsets, int E, int rows_per_tile, int32_t* tile_off,
+                              cudaStream_t stream);
 cudaError_t launch_gather_rows(const void* src, const int32_t* gather_idx, int R, int T, int cols, void* dst,
                                int* status, cudaStream_t stream);
 

@@ -153,12 +153,12 @@ cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, in
   return cudaGetLastError();
 }
 
-// tile_off[e] = sum over e' < e of ceil(count[e'] / 128); tile_off[E] = total tiles.
-__global__ void __launch_bounds__(1024) tile_table_kernel(const int32_t* __restrict__ offsets, int E,
+// tile_off[e] = sum over e' < e of ceil(count[e'] / rows_per_tile); tile_off[E] = total tiles.
+__global__ void __launch_bounds__(1024) tile_table_kernel(const int32_t* __restrict__ offsets, int E, int rows_per_tile,
                                                            int32_t* __restrict__ tile_off) {
   __shared__ int s_warp[32];
   const int e = threadIdx.x;
-  const int tiles = e < E ? (offsets[e + 1] - offsets[e] + 127) / 128 : 0;
+  const int tiles = e < E ? (offsets[e + 1] - offsets[e] + rows_per_tile - 1) / rows_per_tile : 0;
   const int excl = block_exclusive_scan(tiles, s_warp);
   if (e < E) {
     tile_off[e] = excl;
@@ -166,8 +166,9 @@ __global__ void __launch_bounds__(1024) tile_table_kernel(const int32_t* __restr
   }
 }
 
-cudaError_t launch_tile_table(const int32_t* offsets, int E, int32_t* tile_off, cudaStream_t stream) {
-  tile_table_kernel<<<1, 1024, 0, stream>>>(offsets, E, tile_off);
+cudaError_t launch_tile_table(const int32_t* offsets, int E, int rows_per_tile, int32_t* tile_off,
+                              cudaStream_t stream) {
+  tile_table_kernel<<<1, 1024, 0, stream>>>(offsets, E, rows_per_tile, tile_off);
   return cudaGetLastError();
 }
 

@@ -218,6 +218,25 @@ int moe_layer_forward_staged(const moe_config_t* cfg, const moe_weights_t* w, co
  * the current device (the split-K choices depend on its SM count). */
 int moe_layer_forward_launches(const moe_config_t* cfg, int64_t T, int32_t* n);
 
+/*
+ * Load-balancing counters, section "Счётчики и bias-корректировка" (run between
+ * training steps or batches; E <= 1024, one small kernel each).
+ *
+ * moe_accumulate_counts: accum[e] += counts[e] (counts as from moe_permute).
+ *   counts device (E) int32; accum device (E) int64, in / out.
+ * moe_load_imbalance: *imbalance = max(counts) / mean(counts), NaN when no token
+ *   was routed.  counts device (E), int32 or int64 (counts_are_int64 = 1);
+ *   imbalance device float scalar.
+ * moe_score_bias_update: ideal = mean(accum); score_bias[e] += bias_gamma *
+ *   sign(ideal - accum[e]) (the sign decided exactly in integers); then accum
+ *   is zeroed.  accum device (E) int64 in / out; score_bias device (E) fp32 in / out.
+ */
+int moe_accumulate_counts(const int32_t* counts, int32_t num_experts, int64_t* accum, moe_stream_t stream);
+int moe_load_imbalance(const void* counts, int32_t counts_are_int64, int32_t num_experts, float* imbalance,
+                       moe_stream_t stream);
+int moe_score_bias_update(int64_t* accum, int32_t num_experts, float bias_gamma, float* score_bias,
+                          moe_stream_t stream);
+
 /* Byte offsets in ws of the layer forward's intermediates, for inspection:
  * [0] router GEMM output (split-K partial logits without the router bias),
  * [1] idx (T,k) int32, [2] weights (T,k) fp32,

@@ -386,3 +386,30 @@ def layer_forward(cfg: OracleConfig, x: np.ndarray, wts: OracleWeights,
     z = combine(y, perm.scatter_pos, r.weights)
     out = restore_routed_output(cfg, z, wts.w_up_latent, wts.rms_weight)
     return LayerResult(r, perm, x_routed, y, z, out)
+
+
+# --------------------------------------------------------------------------
+# Load balancing counters  [Olmo-core 3, §"Счётчики и bias-корректировка"]
+# --------------------------------------------------------------------------
+
+def accumulate_counts(accum: np.ndarray, counts: np.ndarray) -> np.ndarray:
+    """The per-expert accumulator adds each step's tokens-per-expert histogram."""
+    return np.asarray(accum, np.int64) + np.asarray(counts, np.int64)
+
+
+def load_imbalance(counts: np.ndarray) -> float:
+    """Maximum of the per-expert counter divided by its mean (NaN when no token was routed)."""
+    c = np.asarray(counts, np.float64)
+    mean = c.mean()
+    return float(c.max() / mean) if mean > 0 else float("nan")
+
+
+def score_bias_update(score_bias: np.ndarray, accum: np.ndarray, bias_gamma: float):
+    """score_bias += bias_gamma * sign(ideal - actual), ideal = the mean count; then the accumulator is zeroed.
+
+    Returns (new score_bias, zeroed accumulator).
+    """
+    a = np.asarray(accum, np.float64)
+    ideal = a.mean()
+    new = np.asarray(score_bias, np.float64) + bias_gamma * np.sign(ideal - a)
+    return new, np.zeros_like(np.asarray(accum))

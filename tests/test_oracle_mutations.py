@@ -9,6 +9,7 @@ import pytest
 from oracle import moe_ref as ref
 from tests import test_oracle_layer as L
 from tests import test_oracle_permute as P
+from tests import test_oracle_balance as B
 from tests import test_oracle_router as R
 
 _ORIG_PERMUTE = ref.permute
@@ -83,7 +84,21 @@ def _no_epsilon_scores(logits, gating, sigmoid_eps=0.0):
     return _ORIG_GATE_SCORES(logits, gating, 0.0)
 
 
+def _bias_update_wrong_sign(score_bias, accum, bias_gamma):
+    # wrong: pushes over-loaded experts up
+    a = np.asarray(accum, np.float64)
+    return np.asarray(score_bias, np.float64) + bias_gamma * np.sign(a - a.mean()), np.zeros_like(accum)
+
+
+def _imbalance_min_over_mean(counts):
+    # wrong: minimum instead of maximum
+    c = np.asarray(counts, np.float64)
+    return float(c.min() / c.mean()) if c.mean() > 0 else float("nan")
+
+
 CASES = [
+    ("score_bias_update", _bias_update_wrong_sign, lambda: B.test_score_bias_update_hand_values()),
+    ("load_imbalance", _imbalance_min_over_mean, lambda: B.test_load_imbalance_hand_values()),
     ("silu", _silu_dropped, lambda: L.test_single_expert_is_dense_swiglu_mlp()),
     ("swiglu_mlp", _swapped_swiglu, lambda: L.test_single_expert_is_dense_swiglu_mlp()),
     ("routing_weights", _weights_from_keys, lambda: R.test_sigmoid_bias_for_selection_only()),

@@ -48,7 +48,7 @@ EXPORTS = ["moe_validate_config", "moe_num_params", "moe_num_active_params", "mo
            "moe_workspace_size", "moe_router", "moe_permute", "moe_grouped_swiglu", "moe_combine",
            "moe_latent_down", "moe_latent_restore", "moe_layer_forward", "moe_layer_forward_staged",
            "moe_layer_forward_launches", "moe_workspace_layout", "moe_get_status", "moe_status_string",
-           "moe_permute_noalloc"]
+           "moe_permute_noalloc", "moe_accumulate_counts", "moe_load_imbalance", "moe_score_bias_update"]
 
 _lib = None
 
@@ -82,6 +82,9 @@ def load() -> ctypes.CDLL:
         "moe_get_status": [VP, P(ctypes.c_int32), ctypes.c_int],
         "moe_status_string": [ctypes.c_int],
         "moe_permute_noalloc": [cfgp, VP, I64, VP, VP, VP, VP, VP],
+        "moe_accumulate_counts": [VP, ctypes.c_int32, VP, VP],
+        "moe_load_imbalance": [VP, ctypes.c_int32, ctypes.c_int32, VP, VP],
+        "moe_score_bias_update": [VP, ctypes.c_int32, ctypes.c_float, VP, VP],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -330,6 +333,31 @@ def moe_layer_forward_launches(cfg, T: int) -> int:
     n = ctypes.c_int32()
     _check(load().moe_layer_forward_launches(ctypes.byref(cfg), T, ctypes.byref(n)), "moe_layer_forward_launches")
     return n.value
+
+
+def moe_accumulate_counts(counts, accum, stream=None):
+    """accum (E, int64) += counts (E, int32), on the device."""
+    _check(load().moe_accumulate_counts(_ptr(counts, torch.int32, "counts"), counts.numel(),
+                                        _ptr(accum, torch.int64, "accum"), _stream(stream)), "moe_accumulate_counts")
+    return accum
+
+
+def moe_load_imbalance(counts, out=None, stream=None):
+    """max / mean of a per-expert counter (int32 or int64), as a device float scalar."""
+    out = torch.empty(1, dtype=torch.float32, device=counts.device) if out is None else out
+    if counts.dtype not in (torch.int32, torch.int64):
+        raise ValueError("counts must be int32 or int64")
+    _check(load().moe_load_imbalance(_ptr(counts, None, "counts"), int(counts.dtype == torch.int64), counts.numel(),
+                                     _ptr(out, torch.float32, "imbalance"), _stream(stream)), "moe_load_imbalance")
+    return out
+
+
+def moe_score_bias_update(accum, bias_gamma: float, score_bias, stream=None):
+    """score_bias += gamma * sign(mean(accum) - accum); accum = 0 (both in place, on the device)."""
+    _check(load().moe_score_bias_update(_ptr(accum, torch.int64, "accum"), accum.numel(), bias_gamma,
+                                        _ptr(score_bias, torch.float32, "score_bias"), _stream(stream)),
+           "moe_score_bias_update")
+    return score_bias
 
 
 def moe_get_status(stream=None, clear: bool = True) -> int:

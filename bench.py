@@ -52,6 +52,7 @@ def read_peaks():
 
 
 def workload_desc(spec: W.WorkloadSpec) -> str:
+    """One-line description of the workload."""
     s = (f"{spec.name}: T={spec.T} d_model={spec.d_model} experts={spec.num_experts} top_k={spec.top_k} "
          f"hidden={spec.hidden_size} gating={spec.gating}")
     if spec.latent_dim:
@@ -64,6 +65,8 @@ def workload_desc(spec: W.WorkloadSpec) -> str:
         s += " restore_weight_scale"
     if spec.skew:
         s += " skewed_load"
+    if spec.capacity_factor:
+        s += f" capacity_factor={spec.capacity_factor:g}"
     return s
 
 
@@ -254,6 +257,8 @@ def run_native(args):
 
     native.load()
     spec = W.WORKLOADS[args.config]
+    if args.capacity_factor > 0:
+        spec = spec.with_(capacity_factor=args.capacity_factor)
     # each rank draws its own batch of tokens (weak scaling); weights are shared replicas
     inp = rank_inputs(spec, rank)
     cfg = native.config_from_spec(spec)
@@ -365,6 +370,12 @@ def run_native(args):
 
     peaks, peak_kind = read_peaks()
     flops = W.algorithmic_flops(spec)
+    dropped = 0
+    if spec.capacity_factor > 0:
+        cap = native.moe_expert_capacity(cfg, T)
+        kept = int(torch.clamp(inter["counts"].long(), max=cap).sum().item())
+        dropped = spec.rows - kept
+        flops -= 6 * spec.routed_dim * spec.hidden_size * dropped   # dropped assignments do no expert work
     tflops = flops / (ms * 1e-3) / 1e12
     gbs = alg_bytes / (ms * 1e-3) / 1e9
     gemm1_flops = 4 * spec.rows * spec.routed_dim * spec.hidden_size
@@ -400,7 +411,8 @@ def run_native(args):
         "layer": {"tflops": tflops, "frac_bf16_peak": tflops / peak_tf, "bf16_peak": peak_tf, "gbs": gbs,
                   "frac_hbm_peak": gbs / peaks["hbm_gbs"], "bound": bound_layer,
                   "roofline_ms": roof_ms, "frac_of_roofline": roof_ms / ms, "experts_touched": touched,
-                  "algorithmic_flops": flops, "algorithmic_bytes": alg_bytes},
+                  "algorithmic_flops": flops, "algorithmic_bytes": alg_bytes,
+                  "dropped_assignments": dropped},
         "stages_ms": stage_ms,
         "balance": bal,
         "roofline": {"kernel": "grouped GEMM 1 (SwiGLU fused, tcgen05)", "bound": "tensor",
@@ -430,6 +442,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="olmoe", choices=sorted(W.WORKLOADS))
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--capacity-factor", type=float, default=0.0,
+                    help="> 0: capacity-limited experts (dropping); default dropless")
     ap.add_argument("--ref-tokens", type=int, default=256, help="oracle tokens per step (reference arm)")
     ap.add_argument("--cpu-tokens", type=int, default=512, help="oracle sample for the cpu_baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -77,6 +77,8 @@ typedef struct {
   int32_t router_bias;             /* 1: the router linear layer has a bias (E fp32) */
   int32_t has_score_bias;          /* 1: a score_bias (E fp32) is added for selection only */
   int32_t activation;              /* 0 = swiglu (the only expert activation supported) */
+  float capacity_factor;           /* > 0: capacity-limited experts (section "Ёмкость эксперта и
+                                      переполнение"); 0 = dropless */
 } moe_config_t;
 
 /*
@@ -112,6 +114,14 @@ int moe_num_active_params(const moe_config_t* cfg, int64_t* out);
 /* Latent down- and up-projection weights: 2 * d_model * latent_dim (+ L with an RMSNorm gain). */
 int moe_latent_proj_params(const moe_config_t* cfg, int with_norm_gain, int64_t* out);
 
+/* Expert capacity for T tokens, section "Ёмкость эксперта и переполнение":
+ * roundup8(capacity_factor * top_k * T / num_experts) (single device: EP degree 1),
+ * computed in double precision; 0 in dropless mode. */
+int moe_expert_capacity(const moe_config_t* cfg, int64_t T, int64_t* capacity);
+
+/* Rows of the permuted order: T * top_k (dropless) or num_experts * capacity. */
+int moe_permuted_rows(const moe_config_t* cfg, int64_t T, int64_t* rows);
+
 /* Workspace bytes that every entry point below needs for T tokens. */
 int moe_workspace_size(const moe_config_t* cfg, int64_t T, size_t* bytes);
 
@@ -143,6 +153,11 @@ int moe_router(const moe_config_t* cfg, const moe_weights_t* w, const void* x, i
  *   offsets     device (E+1) int32 output: exclusive prefix sum of counts (the bins)
  *   gather_idx  device (T*k) int32 output: token of permuted row p
  *   scatter_idx device (T*k) int32 output: permuted row of assignment f
+ * Capacity mode (cfg.capacity_factor > 0): every expert owns exactly C =
+ * moe_expert_capacity slots; its assignments fill them in the same ascending
+ * order and the ones beyond C are dropped.  Then offsets[e] = e * C,
+ * gather_idx has E * C entries (-1 = padding slot), scatter_idx[f] is the
+ * slot or -1 (dropped), and counts still holds the choices before dropping.
  */
 int moe_permute(const moe_config_t* cfg, const int32_t* idx, int64_t T, int32_t* counts, int32_t* offsets,
                 int32_t* gather_idx, int32_t* scatter_idx, void* ws, size_t ws_bytes, moe_stream_t stream);
@@ -154,8 +169,9 @@ int moe_permute(const moe_config_t* cfg, const int32_t* idx, int64_t T, int32_t*
  * r = x_routed[gather_idx[p]];  H = silu(g) * u rounded to bf16;
  * y[p] = W_out[e] H rounded to bf16 (the experts return bf16).
  *   x_routed   device (T, L') bf16: the experts' input (x, or the latent projection)
- *   gather_idx device (T*k) int32, offsets device (E+1) int32 (as from moe_permute)
- *   y          device (T*k, L') bf16 output, permuted row order
+ *   gather_idx device (rows) int32, offsets device (E+1) int32 (as from moe_permute)
+ *   y          device (rows, L') bf16 output, permuted row order
+ * rows = moe_permuted_rows(cfg, T); a padding slot (capacity mode) computes a zero row.
  */
 int moe_grouped_swiglu(const moe_config_t* cfg, const moe_weights_t* w, const void* x_routed,
                        const int32_t* gather_idx, const int32_t* offsets, int64_t T, void* y, void* ws,
@@ -164,7 +180,8 @@ int moe_grouped_swiglu(const moe_config_t* cfg, const moe_weights_t* w, const vo
 /*
  * Weighted un-permute / combine, section "Пересылка токенов между экспертами":
  * z[t] = sum_j weights[t, j] * y[scatter_idx[t*k + j]], accumulated in fp32, stored bf16.
- *   y device (T*k, L') bf16, scatter_idx device (T*k) int32, weights device (T, k) fp32
+ * In capacity mode a dropped assignment (scatter_idx -1) adds nothing.
+ *   y device (rows, L') bf16, scatter_idx device (T*k) int32, weights device (T, k) fp32
  *   z device (T, L') bf16 output
  */
 int moe_combine(const moe_config_t* cfg, const void* y, const int32_t* scatter_idx, const float* weights,
@@ -257,8 +274,8 @@ int moe_workspace_layout(const moe_config_t* cfg, int64_t T, int64_t offsets_out
  * The histogram scratch lives in one 2 MiB array of static device memory,
  * which every GPU that loads this library keeps until the process exits.
  * Limit: ceil(T * top_k / 4096) * num_experts <= 524288 (for 896 experts,
- * T * top_k up to about 2.39 million); larger calls return
- * MOE_ERR_UNSUPPORTED and enqueue nothing.
+ * T * top_k up to about 2.39 million); larger calls, and capacity-mode
+ * configurations, return MOE_ERR_UNSUPPORTED and enqueue nothing.
  * The first call on each device looks up the array's device address (a
  * runtime query, no allocation); make that first call before any stream
  * capture.  The call allocates and frees nothing.

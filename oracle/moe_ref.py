@@ -413,3 +413,87 @@ def score_bias_update(score_bias: np.ndarray, accum: np.ndarray, bias_gamma: flo
     ideal = a.mean()
     new = np.asarray(score_bias, np.float64) + bias_gamma * np.sign(ideal - a)
     return new, np.zeros_like(np.asarray(accum))
+
+
+# --------------------------------------------------------------------------
+# Expert capacity  [Olmo-core 3, §"Ёмкость эксперта и переполнение"]
+# --------------------------------------------------------------------------
+
+def expert_capacity(cfg: OracleConfig, T: int, capacity_factor: float, ep_degree: int = 1) -> int:
+    """EP degree x (capacity_factor x ideal inputs per expert, rounded up to a multiple of 8),
+    ideal inputs = top_k x local batch / num_experts."""
+    ideal = cfg.top_k * T / cfg.num_experts
+    local = 8 * math.ceil(capacity_factor * ideal / 8)
+    return ep_degree * local
+
+
+@dataclass
+class CapacityPermutation:
+    capacity: int
+    counts: np.ndarray        # (E,) tokens chosen per expert, before dropping
+    kept: np.ndarray          # (E,) min(count, capacity)
+    slot_token: np.ndarray    # (E * capacity,) token in slot e*capacity + r; -1 = padding
+    scatter_slot: np.ndarray  # (T*k,) slot of assignment t*k + j; -1 = dropped
+
+
+def permute_with_capacity(idx: np.ndarray, num_experts: int, capacity: int) -> CapacityPermutation:
+    """Every expert gets exactly `capacity` slots.  Its assignments fill them in
+    ascending flat order; the ones beyond the capacity are dropped, free slots are padding."""
+    idx = np.asarray(idx, np.int64)
+    flat = idx.reshape(-1)
+    E = num_experts
+    counts = np.zeros(E, np.int64)
+    slot_token = np.full(E * capacity, -1, np.int64)
+    scatter_slot = np.full(flat.size, -1, np.int64)
+    k = idx.shape[1] if idx.ndim == 2 else 1
+    for f, e in enumerate(flat):
+        r = counts[e]
+        counts[e] += 1
+        if r < capacity:
+            s = e * capacity + r
+            slot_token[s] = f // k
+            scatter_slot[f] = s
+    return CapacityPermutation(capacity, counts, np.minimum(counts, capacity), slot_token, scatter_slot)
+
+
+def expert_outputs_capacity(cfg: OracleConfig, x_routed: np.ndarray, perm: CapacityPermutation,
+                            expert: ExpertFn) -> np.ndarray:
+    """y for every slot; a padding slot holds a zero row, whose SwiGLU output is zero."""
+    x_routed = np.asarray(x_routed, np.float64)
+    cap = perm.capacity
+    y = np.zeros((cfg.num_experts * cap, x_routed.shape[1]), np.float64)
+    for e in range(cfg.num_experts):
+        n = int(perm.kept[e])
+        if n == 0:
+            continue
+        w_up, w_gate, w_out = (np.asarray(a, np.float64) for a in expert(e))
+        y[e * cap:e * cap + n] = swiglu_mlp(x_routed[perm.slot_token[e * cap:e * cap + n]], w_up, w_gate, w_out)
+    return y
+
+
+def combine_capacity(y: np.ndarray, scatter_slot: np.ndarray, weights: np.ndarray) -> np.ndarray:
+    """z[t] = sum over the kept assignments j of weights[t, j] * y[slot]; dropped ones add nothing."""
+    y = np.asarray(y, np.float64)
+    weights = np.asarray(weights, np.float64)
+    T, k = weights.shape
+    z = np.zeros((T, y.shape[1]), np.float64)
+    for t in range(T):
+        for j in range(k):
+            s = scatter_slot[t * k + j]
+            if s >= 0:
+                z[t] += weights[t, j] * y[s]
+    return z
+
+
+def layer_forward_capacity(cfg: OracleConfig, x: np.ndarray, wts: OracleWeights, capacity_factor: float,
+                           forced_idx: Optional[np.ndarray] = None):
+    """The layer forward with capacity-limited experts (dropping at the permutation)."""
+    x = np.asarray(x, np.float64)
+    x_routed = prepare_routed_input(cfg, x, wts.w_down_latent)
+    r = route(cfg, x, wts.w_router, wts.b_router, wts.score_bias, forced_idx)
+    cap = expert_capacity(cfg, x.shape[0], capacity_factor)
+    perm = permute_with_capacity(r.idx, cfg.num_experts, cap)
+    y = expert_outputs_capacity(cfg, x_routed, perm, wts.expert)
+    z = combine_capacity(y, perm.scatter_slot, r.weights)
+    out = restore_routed_output(cfg, z, wts.w_up_latent, wts.rms_weight)
+    return r, perm, y, z, out

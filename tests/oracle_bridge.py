@@ -100,3 +100,8 @@ def check_topk(gpu_idx, oracle_keys, oracle_idx, k):
     assert not bad.any(), f"{bad.sum()} top-k mismatches that are not near-ties, e.g. token {np.nonzero(bad)[0][:5]}"
     assert mism.sum() <= TIE_FRAC * len(mism), f"{mism.sum()} near-tie mismatches > 0.1%"
     return mism
+
+
+def capacity_factor_f32(spec) -> float:
+    """The capacity factor as the library sees it (a float32 field)."""
+    return float(np.float32(spec.capacity_factor))

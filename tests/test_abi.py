@@ -120,3 +120,15 @@ def test_host_errors_enqueue_nothing(lib):
     # empty batch: nothing to do, and no device needed
     assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 16, 0, 32, None, 0, None) == 0
     assert native.load().moe_status_string(5) == b"device wait timed out"
+
+
+def test_capacity_and_permuted_rows(lib):
+    # roundup8(capacity_factor * top_k * T / E), hand-evaluated
+    assert native.moe_expert_capacity(native.make_config(256, 64, 8, 128, capacity_factor=1.25), 8192) == 1280
+    assert native.moe_expert_capacity(native.make_config(256, 8, 2, 128, capacity_factor=1.0), 100) == 32
+    assert native.moe_expert_capacity(native.make_config(256, 8, 2, 128, capacity_factor=0.5), 100) == 16
+    assert native.moe_expert_capacity(native.make_config(256, 8, 2, 128, capacity_factor=1.0), 96) == 24
+    assert native.moe_expert_capacity(native.make_config(256, 8, 2, 128), 96) == 0        # dropless
+    assert native.moe_permuted_rows(native.make_config(256, 8, 2, 128), 96) == 192
+    assert native.moe_permuted_rows(native.make_config(256, 8, 2, 128, capacity_factor=1.0), 100) == 8 * 32
+    assert native.moe_validate_config(native.make_config(256, 8, 2, 128, capacity_factor=-1.0)) == 1

@@ -72,8 +72,9 @@ def test_bias_correction_loop_on_router_output():
         native.moe_accumulate_counts(counts, accum)
         accum_np = ref.accumulate_counts(accum_np, ref.permute(idx.cpu().numpy(), spec.num_experts).counts)
     bias0 = wts.score_bias.cpu().numpy()
-    native.moe_score_bias_update(accum, 0.001, wts.score_bias)
+    gamma = float(np.float32(0.001))                # the value the kernel receives (a float argument)
+    native.moe_score_bias_update(accum, gamma, wts.score_bias)
     assert native.moe_get_status() == 0
-    want, _ = ref.score_bias_update(bias0.astype(np.float64), accum_np, 0.001)
+    want, _ = ref.score_bias_update(bias0.astype(np.float64), accum_np, gamma)
     np.testing.assert_array_equal(wts.score_bias.cpu().numpy(), want.astype(np.float32))
     assert accum.abs().sum().item() == 0

@@ -43,6 +43,10 @@ int splits_for(int tiles, int K, int sms) {
 
 struct Plan {
   int64_t T, R;
+  bool capacity;      // capacity-limited experts
+  int64_t cap;        // slots per expert (capacity mode)
+  int64_t rows;       // rows of the permuted order: R, or E * cap
+  size_t gdense, sdense, odense;   // capacity mode: the dense stable permutation before slotting
   int D, E, k, h, L, Lr;   // Lr: routed dim (L or D)
   bool latent;
   int router_bn, n_router_tiles;
@@ -52,6 +56,14 @@ struct Plan {
 };
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// roundup8(capacity_factor * top_k * T / E), in double precision; 0 when dropless.
+int64_t capacity_of(const moe_config_t* c, int64_t T) {
+  if (!(c->capacity_factor > 0.f)) return 0;
+  const double ideal = (double)c->top_k * (double)T / (double)c->num_experts;
+  const double x = (double)c->capacity_factor * ideal;
+  return 8 * (int64_t)std::ceil(x / 8.0);
+}
 
 void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->T = T;
@@ -63,6 +75,9 @@ void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->L = c->latent_dim;
   p->Lr = p->latent ? c->latent_dim : c->d_model;
   p->R = T * p->k;
+  p->capacity = c->capacity_factor > 0.f;
+  p->cap = capacity_of(c, T);
+  p->rows = p->capacity ? (int64_t)p->E * p->cap : p->R;
   const int mt = (int)((T + 127) / 128);
   p->router_bn = pick_bn_f32(p->E);
   p->n_router_tiles = (p->E + p->router_bn - 1) / p->router_bn;
@@ -84,13 +99,20 @@ void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->counts = take((size_t)p->E * 4);
   p->offsets = take((size_t)(p->E + 1) * 4);
   p->tile_off = take((size_t)(p->E + 1) * 4);
-  p->blk = take((size_t)std::max(1, permute_blocks((int)p->R)) * p->E * 4);
-  p->gather = take((size_t)p->R * 4);
+  p->blk = take((size_t)std::max(1, permute_blocks((int)p->R, permute_chunk((int)p->R))) * p->E * 4);
+  p->gather = take((size_t)std::max(p->R, p->rows) * 4);
   p->scatter = take((size_t)p->R * 4);
+  if (p->capacity) {
+    p->gdense = take((size_t)p->R * 4);
+    p->sdense = take((size_t)p->R * 4);
+    p->odense = take((size_t)(p->E + 1) * 4);
+  } else {
+    p->gdense = p->sdense = p->odense = (size_t)-1;
+  }
   p->xr = p->latent ? take((size_t)T * p->L * 2) : (size_t)-1;
-  p->xp = take((size_t)p->R * p->Lr * 2);
-  p->H = take((size_t)p->R * p->h * 2);
-  p->Y = take((size_t)p->R * p->Lr * 2);
+  p->xp = take((size_t)p->rows * p->Lr * 2);
+  p->H = take((size_t)p->rows * p->h * 2);
+  p->Y = take((size_t)p->rows * p->Lr * 2);
   p->zn = p->latent ? take((size_t)T * p->L * 2) : (size_t)-1;
   size_t part = 0;
   if (p->down_splits > 1) part = std::max(part, (size_t)p->down_splits * T * p->L * 4);
@@ -106,7 +128,8 @@ int check_config(const moe_config_t* c) {
   if (c->top_k > c->num_experts) return MOE_ERR_INVALID_ARG;
   if (c->gating < MOE_GATING_SOFTMAX || c->gating > MOE_GATING_SIGMOID) return MOE_ERR_INVALID_ARG;
   if (c->normalize_expert_weights < 0.f || c->sigmoid_stability_epsilon < 0.f || c->original_top_k < 0 ||
-      !(c->rms_eps >= 0.f) || std::isnan(c->expert_weight_scale))
+      !(c->rms_eps >= 0.f) || std::isnan(c->expert_weight_scale) || !(c->capacity_factor >= 0.f) ||
+      std::isinf(c->capacity_factor))
     return MOE_ERR_INVALID_ARG;
   if (c->activation != 0) return MOE_ERR_UNSUPPORTED;
   if (c->d_model % 64 || c->hidden_size % 64 || (c->latent_dim > 0 && c->latent_dim % 64)) return MOE_ERR_UNSUPPORTED;
@@ -119,6 +142,8 @@ int check_call(const moe_config_t* c, int64_t T, void* ws, size_t ws_bytes, Plan
   if (s != MOE_OK) return s;
   if (T < 0) return MOE_ERR_INVALID_ARG;
   if ((int64_t)T * c->top_k > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  if (c->capacity_factor > 0.f && (double)c->num_experts * (double)capacity_of(c, T) > 2147483000.0)
+    return MOE_ERR_UNSUPPORTED;
   make_plan(c, T, std::min(num_sms(), kSizingSms), plan);
   Plan sizing;
   make_plan(c, T, kSizingSms, &sizing);
@@ -129,7 +154,7 @@ int check_call(const moe_config_t* c, int64_t T, void* ws, size_t ws_bytes, Plan
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // CTA-pair tiles (256 rows) pay off when the average group holds several of them.
-int use_pair_tiles(const Plan& p) { return p.R >= (int64_t)384 * p.E ? 1 : 0; }
+int use_pair_tiles(const Plan& p) { return p.rows >= (int64_t)384 * p.E ? 1 : 0; }
 
 template <typename T>
 T* at(void* ws, size_t off) {
@@ -215,14 +240,14 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   if (s != MOE_OK) return s;
   // rows of the experts' input in permuted order (a TMA tile::gather4 A-load was
   // measured 3x slower than this copy plus tiled loads)
-  s = cuda_status(launch_gather_rows(xr, gather, (int)p.R, (int)p.T, p.Lr, xp, status, st));
+  s = cuda_status(launch_gather_rows(xr, gather, (int)p.rows, (int)p.T, p.Lr, xp, p.capacity ? 1 : 0, status, st));
   if (s != MOE_OK) return s;
   mark(ev, 5, st);
   GemmProblem g1{};
   g1.A = xp;
   g1.B = w->w_up_gate;
   g1.b_rows_total = (int64_t)p.E * 2 * p.h;
-  g1.M = (int)p.R;
+  g1.M = (int)p.rows;
   g1.N = p.h;
   g1.K = p.Lr;
   g1.num_groups = p.E;
@@ -244,7 +269,7 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   g2.A = H;
   g2.B = w->w_out;
   g2.b_rows_total = (int64_t)p.E * p.Lr;
-  g2.M = (int)p.R;
+  g2.M = (int)p.rows;
   g2.N = p.Lr;
   g2.K = p.h;
   g2.num_groups = p.E;
@@ -262,6 +287,22 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   if (s != MOE_OK) return s;
   mark(ev, 7, st);
   return MOE_OK;
+}
+
+// The permutation, dense or into capacity slots.
+int run_permute(const int32_t* idx, const Plan& p, int32_t* counts, int32_t* offsets, int32_t* gather,
+                int32_t* scatter, void* ws, int* status, cudaStream_t st) {
+  if (!p.capacity)
+    return cuda_status(launch_permute(idx, (int)p.R, p.E, counts, offsets, gather, scatter, p.k,
+                                      permute_chunk((int)p.R), at<int32_t>(ws, p.blk), status, st));
+  int32_t* gd = at<int32_t>(ws, p.gdense);
+  int32_t* sd = at<int32_t>(ws, p.sdense);
+  int32_t* od = at<int32_t>(ws, p.odense);
+  int s = cuda_status(launch_permute(idx, (int)p.R, p.E, counts, od, gd, sd, p.k, permute_chunk((int)p.R),
+                                     at<int32_t>(ws, p.blk), status, st));
+  if (s != MOE_OK) return s;
+  return cuda_status(launch_capacity_remap(idx, (int)p.R, p.E, (int)p.cap, counts, od, gd, sd, offsets, gather, scatter,
+                                           st));
 }
 
 int run_restore(const moe_config_t* c, const moe_weights_t* w, const void* z, bool z_is_normalised, const Plan& p,
@@ -317,6 +358,22 @@ int moe_latent_proj_params(const moe_config_t* c, int with_norm_gain, int64_t* o
   return MOE_OK;
 }
 
+int moe_expert_capacity(const moe_config_t* c, int64_t T, int64_t* capacity) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0 || !capacity) return MOE_ERR_INVALID_ARG;
+  *capacity = capacity_of(c, T);
+  return MOE_OK;
+}
+
+int moe_permuted_rows(const moe_config_t* c, int64_t T, int64_t* rows) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0 || !rows) return MOE_ERR_INVALID_ARG;
+  *rows = c->capacity_factor > 0.f ? (int64_t)c->num_experts * capacity_of(c, T) : T * c->top_k;
+  return MOE_OK;
+}
+
 int moe_workspace_size(const moe_config_t* c, int64_t T, size_t* bytes) {
   int s = check_config(c);
   if (s != MOE_OK) return s;
@@ -369,8 +426,7 @@ int moe_permute(const moe_config_t* c, const int32_t* idx, int64_t T, int32_t* c
   if (T == 0 && (!ws || ((uintptr_t)ws & 255))) return MOE_ERR_WORKSPACE;
   int* status = status_ptr();
   if (!status) return MOE_ERR_NO_DEVICE;
-  return cuda_status(launch_permute(idx, (int)p.R, p.E, counts, offsets, gather_idx, scatter_idx, p.k,
-                                    at<int32_t>(ws, p.blk), status, (cudaStream_t)stream));
+  return run_permute(idx, p, counts, offsets, gather_idx, scatter_idx, ws, status, (cudaStream_t)stream);
 }
 
 int moe_grouped_swiglu(const moe_config_t* c, const moe_weights_t* w, const void* x_routed, const int32_t* gather_idx,
@@ -396,8 +452,11 @@ int moe_combine(const moe_config_t* c, const void* y, const int32_t* scatter_idx
   int* status = status_ptr();
   if (!status) return MOE_ERR_NO_DEVICE;
   const int Lr = c->latent_dim > 0 ? c->latent_dim : c->d_model;
-  return cuda_status(launch_combine(y, scatter_idx, weights, (int)T, c->top_k, Lr, (int)(T * c->top_k), 0, 0.f,
-                                    nullptr, z, status, (cudaStream_t)stream));
+  const bool capacity = c->capacity_factor > 0.f;
+  const int64_t rows = capacity ? (int64_t)c->num_experts * capacity_of(c, T) : T * c->top_k;
+  if (rows > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  return cuda_status(launch_combine(y, scatter_idx, weights, (int)T, c->top_k, Lr, (int)rows, 0, 0.f, nullptr, z,
+                                    capacity ? 1 : 0, status, (cudaStream_t)stream));
 }
 
 int moe_latent_down(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* x_routed, void* ws,
@@ -460,22 +519,22 @@ int moe_layer_forward_staged(const moe_config_t* c, const moe_weights_t* w, cons
   int32_t* offsets = at<int32_t>(ws, p.offsets);
   int32_t* gather = at<int32_t>(ws, p.gather);
   int32_t* scatter = at<int32_t>(ws, p.scatter);
-  s = cuda_status(launch_permute(idx, (int)p.R, p.E, counts, offsets, gather, scatter, p.k, at<int32_t>(ws, p.blk),
-                                 status, st));
+  s = run_permute(idx, p, counts, offsets, gather, scatter, ws, status, st);
   if (s != MOE_OK) return s;
   mark(ev, 4, st);
   void* Y = at<void>(ws, p.Y);
   s = run_experts(c, w, xr, gather, offsets, p, Y, ws, status, st, ev);
   if (s != MOE_OK) return s;
   if (!p.latent) {
-    s = cuda_status(launch_combine(Y, scatter, wts, (int)T, p.k, p.Lr, (int)p.R, 0, 0.f, nullptr, out, status, st));
+    s = cuda_status(launch_combine(Y, scatter, wts, (int)T, p.k, p.Lr, (int)p.rows, 0, 0.f, nullptr, out,
+                                   p.capacity ? 1 : 0, status, st));
     mark(ev, 8, st);
     mark(ev, 9, st);
     return s;
   }
   void* zn = at<void>(ws, p.zn);
-  s = cuda_status(launch_combine(Y, scatter, wts, (int)T, p.k, p.L, (int)p.R, c->up_proj_norm, c->rms_eps,
-                                 w->rms_weight, zn, status, st));
+  s = cuda_status(launch_combine(Y, scatter, wts, (int)T, p.k, p.L, (int)p.rows, c->up_proj_norm, c->rms_eps,
+                                 w->rms_weight, zn, p.capacity ? 1 : 0, status, st));
   if (s != MOE_OK) return s;
   mark(ev, 8, st);
   s = run_restore(c, w, zn, true, p, out, ws, status, st);
@@ -501,7 +560,7 @@ int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
   int k = 0;
   if (p.latent) k += p.down_splits > 1 ? 2 : 1;  // latent down (+ split-K reduce)
   k += p.router_splits > 1 ? 3 : 2;              // router GEMM, (split-K sum,) top-k
-  k += 3;                                        // permute: count, scan, place
+  k += p.capacity ? 4 : 3;                       // permute: count, scan, place (, capacity slots)
   k += 2;                                        // tile table, row gather
   k += 2;                                        // grouped GEMM 1 (SwiGLU), grouped GEMM 2
   k += 1;                                        // combine (+ RMSNorm when latent)

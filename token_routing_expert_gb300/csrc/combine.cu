@@ -58,7 +58,7 @@ template <bool RMS>
 __global__ void __launch_bounds__(32 * kRowWarps)
     combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ scatter_idx, const float* __restrict__ w,
                    int T, int k, int vec, int R, float eps, const uint4* __restrict__ gain, uint4* __restrict__ z,
-                   int* status) {
+                   int allow_dropped, int* status) {
   extern __shared__ uint4 zs_all[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(32 * kRowWarps)
     my_p = scatter_idx[t * k + lane];
     my_w = w[t * k + lane];
     if (my_p < 0 || my_p >= R) {
-      set_status(status, MOE_ERR_BOUNDS);
+      if (!(allow_dropped && my_p == -1)) set_status(status, MOE_ERR_BOUNDS);  // -1: dropped, adds nothing
       my_p = 0;
       my_w = 0.f;
     }
@@ -147,7 +147,8 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __rest
 }
 
 cudaError_t launch_combine(const void* y, const int32_t* scatter_idx, const float* w, int T, int k, int L, int R,
-                           int rms, float eps, const void* gain, void* z, int* status, cudaStream_t stream) {
+                           int rms, float eps, const void* gain, void* z, int allow_dropped, int* status,
+                           cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
   const int vec = L / 8;
   const dim3 grid((T + kRowWarps - 1) / kRowWarps), block(32 * kRowWarps);
@@ -159,10 +160,10 @@ cudaError_t launch_combine(const void* y, const int32_t* scatter_idx, const floa
     }
     combine_kernel<true><<<grid, block, sm, stream>>>(static_cast<const uint4*>(y), scatter_idx, w, T, k, vec, R,
                                                       eps, static_cast<const uint4*>(gain), static_cast<uint4*>(z),
-                                                      status);
+                                                      allow_dropped, status);
   } else {
     combine_kernel<false><<<grid, block, 0, stream>>>(static_cast<const uint4*>(y), scatter_idx, w, T, k, vec, R,
-                                                      eps, nullptr, static_cast<uint4*>(z), status);
+                                                      eps, nullptr, static_cast<uint4*>(z), allow_dropped, status);
   }
   return cudaGetLastError();
 }

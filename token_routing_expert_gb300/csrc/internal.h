@@ -47,18 +47,26 @@ cudaError_t launch_topk(const float* logits, int n_partials, int64_t partial_str
                         int restore, float ews, int orig_k, float* logits_out, int32_t* idx, float* w,
                         int* status, cudaStream_t stream);
 
+// chunk: assignments per block, a multiple of 256 in [256, 4096]; blk_scratch holds
+// permute_blocks(R, chunk) * E ints.
 cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, int32_t* offsets,
-                           int32_t* gather_idx, int32_t* scatter_idx, int k, int32_t* blk_scratch, int* status,
-                           cudaStream_t stream);
-int permute_blocks(int R);
+                           int32_t* gather_idx, int32_t* scatter_idx, int k, int chunk, int32_t* blk_scratch,
+                           int* status, cudaStream_t stream);
+int permute_blocks(int R, int chunk);
+int permute_chunk(int R);
 
 cudaError_t launch_tile_table(const int32_t* offsets, int E, int rows_per_tile, int32_t* tile_off,
                               cudaStream_t stream);
 cudaError_t launch_gather_rows(const void* src, const int32_t* gather_idx, int R, int T, int cols, void* dst,
-                               int* status, cudaStream_t stream);
+                               int allow_padding, int* status, cudaStream_t stream);
+// Capacity slots from a dense stable permutation (see moe_permute in moe.h).
+cudaError_t launch_capacity_remap(const int32_t* idx, int R, int E, int cap, const int32_t* counts,
+                                  const int32_t* off_dense, const int32_t* gather_dense,
+                                  const int32_t* scatter_dense, int32_t* offsets, int32_t* gather_idx,
+                                  int32_t* scatter_idx, cudaStream_t stream);
 
 cudaError_t launch_combine(const void* y, const int32_t* scatter_idx, const float* w, int T, int k, int L,
-                           int R, int rms, float eps, const void* gain, void* z, int* status,
+                           int R, int rms, float eps, const void* gain, void* z, int allow_dropped, int* status,
                            cudaStream_t stream);
 cudaError_t launch_rmsnorm(const void* z, int T, int L, float eps, const void* gain, void* out,
                            cudaStream_t stream);

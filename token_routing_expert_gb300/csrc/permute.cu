@@ -5,7 +5,7 @@
 // (page "Как устроен Olmo-core 3: обучение больших MoE-моделей",
 // §"Пересылка токенов между экспертами": indices sorted by expert, bins =
 // cumulative sum of the per-expert counts).  Three passes over chunks of
-// kChunk assignments: per-chunk histograms; per-expert scan over chunks plus
+// assignments (256 to 4096 per block): per-chunk histograms; per-expert scan over chunks plus
 // the exclusive scan over experts; placement, where each warp walks its
 // slice of the chunk in order and ranks equal experts with __match_any_sync.
 #include <algorithm>
@@ -15,20 +15,27 @@
 
 namespace moe {
 
-constexpr int kChunk = 4096;
+constexpr int kMaxChunk = 4096;
 constexpr int kPermThreads = 256;
 constexpr int kPermWarps = kPermThreads / 32;
-constexpr int kSub = kChunk / kPermWarps;
 
-int permute_blocks(int R) { return (R + kChunk - 1) / kChunk; }
+int permute_blocks(int R, int chunk) { return (R + chunk - 1) / chunk; }
+
+// Assignments per block: about two blocks per SM, 256 to 4096, a multiple of 256
+// (each of the 8 warps walks chunk / 8 assignments).
+int permute_chunk(int R) {
+  int c = (R / 304 + 255) / 256 * 256;
+  return c < 256 ? 256 : (c > kMaxChunk ? kMaxChunk : c);
+}
 
 __global__ void __launch_bounds__(kPermThreads) perm_count_kernel(const int32_t* __restrict__ idx, int R, int E,
-                                                                   int32_t* __restrict__ blk, int* status) {
+                                                                   int chunk, int32_t* __restrict__ blk,
+                                                                   int* status) {
   extern __shared__ int32_t hist[];
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  const int base = blockIdx.x * kChunk;
-  const int end = min(R, base + kChunk);
+  const int base = blockIdx.x * chunk;
+  const int end = min(R, base + chunk);
   for (int r = base + threadIdx.x; r < end; r += blockDim.x) {
     const int e = idx[r];
     if (e < 0 || e >= E) set_status(status, MOE_ERR_BOUNDS);
@@ -87,17 +94,18 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ b
 }
 
 __global__ void __launch_bounds__(kPermThreads) perm_place_kernel(const int32_t* __restrict__ idx, int R, int E,
-                                                                   int k, const int32_t* __restrict__ blk,
+                                                                   int k, int chunk, const int32_t* __restrict__ blk,
                                                                    int32_t* __restrict__ gather_idx,
                                                                    int32_t* __restrict__ scatter_idx) {
   extern __shared__ int32_t wh[];  // [kPermWarps][E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) wh[i] = 0;
   __syncthreads();
-  const int base = blockIdx.x * kChunk;
-  const int end = min(R, base + kChunk);
-  const int s0 = base + warp * kSub;
-  const int s1 = min(end, s0 + kSub);
+  const int base = blockIdx.x * chunk;
+  const int end = min(R, base + chunk);
+  const int sub = chunk / kPermWarps;
+  const int s0 = base + warp * sub;
+  const int s1 = min(end, s0 + sub);
   int32_t* mine = wh + warp * E;
 
   // pass 1: this warp's per-expert counts
@@ -139,16 +147,17 @@ __global__ void __launch_bounds__(kPermThreads) perm_place_kernel(const int32_t*
 }
 
 cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, int32_t* offsets,
-                           int32_t* gather_idx, int32_t* scatter_idx, int k, int32_t* blk, int* status,
+                           int32_t* gather_idx, int32_t* scatter_idx, int k, int chunk, int32_t* blk, int* status,
                            cudaStream_t stream) {
-  const int nb = permute_blocks(R);
+  if (chunk < 256 || chunk > kMaxChunk || chunk % 256) return cudaErrorInvalidValue;
+  const int nb = permute_blocks(R, chunk);
   if (nb > 0) {
-    perm_count_kernel<<<nb, kPermThreads, E * sizeof(int32_t), stream>>>(idx, R, E, blk, status);
+    perm_count_kernel<<<nb, kPermThreads, E * sizeof(int32_t), stream>>>(idx, R, E, chunk, blk, status);
   }
   perm_scan_kernel<<<1, 1024, 0, stream>>>(blk, nb, E, counts, offsets);
   if (nb > 0) {
     const size_t sm = (size_t)kPermWarps * E * sizeof(int32_t);
-    perm_place_kernel<<<nb, kPermThreads, sm, stream>>>(idx, R, E, k, blk, gather_idx, scatter_idx);
+    perm_place_kernel<<<nb, kPermThreads, sm, stream>>>(idx, R, E, k, chunk, blk, gather_idx, scatter_idx);
   }
   return cudaGetLastError();
 }
@@ -176,13 +185,18 @@ cudaError_t launch_tile_table(const int32_t* offsets, int E, int rows_per_tile, 
 __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restrict__ src,
                                                            const int32_t* __restrict__ gather_idx, int R, int T,
                                                            int vec_per_row, uint4* __restrict__ dst,
-                                                           int* status) {
+                                                           int allow_padding, int* status) {
   const int lane = threadIdx.x & 31;
   const long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (p >= R) return;
   const int t = gather_idx[p];
   if (t < 0 || t >= T) {
-    if (lane == 0) set_status(status, MOE_ERR_BOUNDS);
+    if (allow_padding && t == -1) {  // a padding slot of a capacity-limited expert: a zero row
+      uint4* d = dst + p * vec_per_row;
+      for (int c = lane; c < vec_per_row; c += 32) d[c] = make_uint4(0u, 0u, 0u, 0u);
+    } else if (lane == 0) {
+      set_status(status, MOE_ERR_BOUNDS);
+    }
     return;
   }
   const uint4* s = src + (long long)t * vec_per_row;
@@ -191,11 +205,55 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
 }
 
 cudaError_t launch_gather_rows(const void* src, const int32_t* gather_idx, int R, int T, int cols, void* dst,
-                               int* status, cudaStream_t stream) {
+                               int allow_padding, int* status, cudaStream_t stream) {
   if (R <= 0) return cudaSuccess;
   const int warps = 8;
   gather_rows_kernel<<<(R + warps - 1) / warps, 32 * warps, 0, stream>>>(
-      static_cast<const uint4*>(src), gather_idx, R, T, cols / 8, static_cast<uint4*>(dst), status);
+      static_cast<const uint4*>(src), gather_idx, R, T, cols / 8, static_cast<uint4*>(dst), allow_padding, status);
+  return cudaGetLastError();
+}
+
+// Capacity slots (page "Как устроен Olmo-core 3: обучение больших MoE-моделей",
+// §"Ёмкость эксперта и переполнение"): expert e owns slots [e*cap, (e+1)*cap);
+// its r-th assignment in the stable order goes to slot e*cap + r if r < cap,
+// otherwise it is dropped (-1); unused slots are padding (-1).
+__global__ void __launch_bounds__(256) capacity_remap_kernel(const int32_t* __restrict__ idx, int R, int E, int cap,
+                                                              const int32_t* __restrict__ counts,
+                                                              const int32_t* __restrict__ off_dense,
+                                                              const int32_t* __restrict__ gather_dense,
+                                                              const int32_t* __restrict__ scatter_dense,
+                                                              int32_t* __restrict__ offsets,
+                                                              int32_t* __restrict__ gather_idx,
+                                                              int32_t* __restrict__ scatter_idx) {
+  const long long slots = (long long)E * cap;
+  const long long n = max(max(slots, (long long)R), (long long)E + 1);
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+    if (i <= E) offsets[i] = (int32_t)(i * cap);
+    if (i < slots) {
+      const int e = (int)(i / cap);
+      const int r = (int)(i - (long long)e * cap);
+      gather_idx[i] = r < counts[e] ? gather_dense[off_dense[e] + r] : -1;
+    }
+    if (i < R) {
+      const int e = idx[i];
+      int slot = -1;
+      if (e >= 0 && e < E) {
+        const int r = scatter_dense[i] - off_dense[e];
+        if (r < cap) slot = e * cap + r;
+      }
+      scatter_idx[i] = slot;
+    }
+  }
+}
+
+cudaError_t launch_capacity_remap(const int32_t* idx, int R, int E, int cap, const int32_t* counts,
+                                  const int32_t* off_dense, const int32_t* gather_dense,
+                                  const int32_t* scatter_dense, int32_t* offsets, int32_t* gather_idx,
+                                  int32_t* scatter_idx, cudaStream_t stream) {
+  const long long n = std::max(std::max((long long)E * cap, (long long)R), (long long)E + 1);
+  const int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
+  capacity_remap_kernel<<<blocks, 256, 0, stream>>>(idx, R, E, cap, counts, off_dense, gather_dense, scatter_dense,
+                                                    offsets, gather_idx, scatter_idx);
   return cudaGetLastError();
 }
 
@@ -234,12 +292,13 @@ extern "C" int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* idx, 
                                    moe_stream_t stream) {
   int s = moe_validate_config(cfg);
   if (s != MOE_OK) return s;
+  if (cfg->capacity_factor > 0.f) return MOE_ERR_UNSUPPORTED;  // capacity slots need the workspace path
   if (T < 0 || !counts || !offsets) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!idx || !gather_idx || !scatter_idx)) return MOE_ERR_INVALID_ARG;
   if (T * cfg->top_k > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
   const int R = (int)(T * cfg->top_k);
   // the histograms need one int per (chunk, expert): beyond the static array, refuse
-  const int64_t need = (int64_t)std::max(1, moe::permute_blocks(R)) * cfg->num_experts;
+  const int64_t need = (int64_t)std::max(1, moe::permute_blocks(R, moe::kMaxChunk)) * cfg->num_experts;
   if (need > moe::kNoAllocScratchInts) return MOE_ERR_UNSUPPORTED;
   int32_t* scratch = nullptr;
   s = moe::scratch_address(&scratch);
@@ -247,8 +306,8 @@ extern "C" int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* idx, 
   int* status = moe::device_status();
   if (!status) return MOE_ERR_NO_DEVICE;
   // every histogram entry the scan reads is written by this call first: nothing to clear
-  return moe::launch_permute(idx, R, cfg->num_experts, counts, offsets, gather_idx, scatter_idx, cfg->top_k, scratch,
-                             status, (cudaStream_t)stream) == cudaSuccess
+  return moe::launch_permute(idx, R, cfg->num_experts, counts, offsets, gather_idx, scatter_idx, cfg->top_k,
+                             moe::kMaxChunk, scratch, status, (cudaStream_t)stream) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }

@@ -36,7 +36,8 @@ class moe_config_t(ctypes.Structure):
                 ("sigmoid_stability_epsilon", ctypes.c_float), ("normalize_expert_weights", ctypes.c_float),
                 ("restore_weight_scale", ctypes.c_int32), ("expert_weight_scale", ctypes.c_float),
                 ("original_top_k", ctypes.c_int32), ("router_bias", ctypes.c_int32),
-                ("has_score_bias", ctypes.c_int32), ("activation", ctypes.c_int32)]
+                ("has_score_bias", ctypes.c_int32), ("activation", ctypes.c_int32),
+                ("capacity_factor", ctypes.c_float)]
 
 
 class moe_weights_t(ctypes.Structure):
@@ -44,7 +45,7 @@ class moe_weights_t(ctypes.Structure):
                                                   "w_up_latent", "rms_weight", "w_up_gate", "w_out")]
 
 
-EXPORTS = ["moe_validate_config", "moe_num_params", "moe_num_active_params", "moe_latent_proj_params",
+EXPORTS = ["moe_expert_capacity", "moe_permuted_rows", "moe_validate_config", "moe_num_params", "moe_num_active_params", "moe_latent_proj_params",
            "moe_workspace_size", "moe_router", "moe_permute", "moe_grouped_swiglu", "moe_combine",
            "moe_latent_down", "moe_latent_restore", "moe_layer_forward", "moe_layer_forward_staged",
            "moe_layer_forward_launches", "moe_workspace_layout", "moe_get_status", "moe_status_string",
@@ -69,6 +70,8 @@ def load() -> ctypes.CDLL:
         "moe_num_active_params": [cfgp, P(I64)],
         "moe_latent_proj_params": [cfgp, ctypes.c_int, P(I64)],
         "moe_workspace_size": [cfgp, I64, P(SZ)],
+        "moe_expert_capacity": [cfgp, I64, P(I64)],
+        "moe_permuted_rows": [cfgp, I64, P(I64)],
         "moe_router": [cfgp, wp, VP, I64, VP, VP, VP, VP, SZ, VP],
         "moe_permute": [cfgp, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
         "moe_grouped_swiglu": [cfgp, wp, VP, VP, VP, I64, VP, VP, SZ, VP],
@@ -109,18 +112,19 @@ def _check(code: int, where: str) -> None:
 def make_config(d_model, num_experts, top_k, hidden_size, latent_dim=0, up_proj_norm=True, rms_eps=1e-6,
                 gating="softmax", sigmoid_stability_epsilon=0.0, normalize_expert_weights=0.0,
                 restore_weight_scale=False, expert_weight_scale=0.0, original_top_k=0, router_bias=False,
-                has_score_bias=False) -> moe_config_t:
+                has_score_bias=False, capacity_factor=0.0) -> moe_config_t:
     g = GATING_NAMES[gating] if isinstance(gating, str) else int(gating)
     return moe_config_t(d_model, num_experts, top_k, hidden_size, latent_dim, int(up_proj_norm), rms_eps, g,
                         sigmoid_stability_epsilon, normalize_expert_weights, int(restore_weight_scale),
-                        expert_weight_scale, original_top_k, int(router_bias), int(has_score_bias), 0)
+                        expert_weight_scale, original_top_k, int(router_bias), int(has_score_bias), 0,
+                        capacity_factor)
 
 
 def config_from_spec(spec: WorkloadSpec) -> moe_config_t:
     return make_config(spec.d_model, spec.num_experts, spec.top_k, spec.hidden_size, spec.latent_dim,
                        spec.up_proj_norm, spec.rms_eps, spec.gating, spec.sigmoid_stability_epsilon,
                        spec.normalize_expert_weights, spec.restore_weight_scale, spec.expert_weight_scale,
-                       spec.original_top_k, spec.skew, spec.score_bias_std > 0)
+                       spec.original_top_k, spec.skew, spec.score_bias_std > 0, spec.capacity_factor)
 
 
 # ---------------------------------------------------------------------------
@@ -153,6 +157,18 @@ def moe_latent_proj_params(cfg: moe_config_t, with_norm_gain: bool = False) -> i
 def moe_workspace_size(cfg: moe_config_t, T: int) -> int:
     out = ctypes.c_size_t()
     _check(load().moe_workspace_size(ctypes.byref(cfg), T, ctypes.byref(out)), "moe_workspace_size")
+    return out.value
+
+
+def moe_expert_capacity(cfg: moe_config_t, T: int) -> int:
+    out = ctypes.c_int64()
+    _check(load().moe_expert_capacity(ctypes.byref(cfg), T, ctypes.byref(out)), "moe_expert_capacity")
+    return out.value
+
+
+def moe_permuted_rows(cfg: moe_config_t, T: int) -> int:
+    out = ctypes.c_int64()
+    _check(load().moe_permuted_rows(ctypes.byref(cfg), T, ctypes.byref(out)), "moe_permuted_rows")
     return out.value
 
 
@@ -238,17 +254,18 @@ def moe_router(cfg, weights: DeviceWeights, x, ws, logits=None, idx=None, w=None
 def moe_permute(cfg, idx, ws, counts=None, offsets=None, gather_idx=None, scatter_idx=None, stream=None):
     T = idx.shape[0]
     R = T * cfg.top_k
+    rows = moe_permuted_rows(cfg, T)
     dev = idx.device
     E = cfg.num_experts
     counts = torch.empty(E, dtype=torch.int32, device=dev) if counts is None else counts
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
-    gather_idx = torch.empty(max(R, 1), dtype=torch.int32, device=dev) if gather_idx is None else gather_idx
+    gather_idx = torch.empty(max(rows, 1), dtype=torch.int32, device=dev) if gather_idx is None else gather_idx
     scatter_idx = torch.empty(max(R, 1), dtype=torch.int32, device=dev) if scatter_idx is None else scatter_idx
     _check(load().moe_permute(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"), T,
                               _ptr(counts, torch.int32, "counts"), _ptr(offsets, torch.int32, "offsets"),
                               _ptr(gather_idx, torch.int32, "gather_idx"), _ptr(scatter_idx, torch.int32, "scatter_idx"),
                               _ptr(ws, None, "ws"), ws.numel(), _stream(stream)), "moe_permute")
-    return counts, offsets, gather_idx[:R], scatter_idx[:R]
+    return counts, offsets, gather_idx[:rows], scatter_idx[:R]
 
 
 def moe_permute_noalloc(cfg, idx, counts, offsets, gather_idx, scatter_idx, stream=None):
@@ -265,7 +282,8 @@ def moe_permute_noalloc(cfg, idx, counts, offsets, gather_idx, scatter_idx, stre
 def moe_grouped_swiglu(cfg, weights: DeviceWeights, x_routed, gather_idx, offsets, ws, y=None, stream=None):
     T = x_routed.shape[0]
     Lr = x_routed.shape[1]
-    y = torch.empty((T * cfg.top_k, Lr), dtype=torch.bfloat16, device=x_routed.device) if y is None else y
+    rows = moe_permuted_rows(cfg, T)
+    y = torch.empty((max(rows, 1), Lr), dtype=torch.bfloat16, device=x_routed.device) if y is None else y
     ws_ = weights.struct()
     _check(load().moe_grouped_swiglu(ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x_routed, torch.bfloat16, "x_routed"),
                                      _ptr(gather_idx, torch.int32, "gather_idx"), _ptr(offsets, torch.int32, "offsets"),
@@ -373,6 +391,7 @@ def layer_intermediates(cfg, T, ws):
     E, k = cfg.num_experts, cfg.top_k
     Lr = cfg.latent_dim or cfg.d_model
     R = T * k
+    rows = moe_permuted_rows(cfg, T)
 
     def view(off, n, dtype, shape):
         size = torch.tensor([], dtype=dtype).element_size()
@@ -383,9 +402,9 @@ def layer_intermediates(cfg, T, ws):
         "weights": view(o[2], R, torch.float32, (T, k)),
         "counts": view(o[3], E, torch.int32, (E,)),
         "offsets": view(o[4], E + 1, torch.int32, (E + 1,)),
-        "gather_idx": view(o[5], R, torch.int32, (R,)),
+        "gather_idx": view(o[5], rows, torch.int32, (rows,)),
         "scatter_idx": view(o[6], R, torch.int32, (R,)),
-        "y": view(o[8], R * Lr, torch.bfloat16, (R, Lr)),
+        "y": view(o[8], rows * Lr, torch.bfloat16, (rows, Lr)),
     }
     if o[7] >= 0:
         out["x_routed"] = view(o[7], T * cfg.latent_dim, torch.bfloat16, (T, cfg.latent_dim))

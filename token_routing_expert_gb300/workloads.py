@@ -54,6 +54,7 @@ class WorkloadSpec:
     skew: bool = False                   # per-expert logit offset 0.5*ln(1/rank)
     up_proj_norm: bool = True
     rms_eps: float = 1e-6
+    capacity_factor: float = 0.0         # > 0: capacity-limited experts
     x_std: float = 1.0
     w_std: float = 0.02
     seed: int = 0

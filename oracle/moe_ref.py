@@ -497,3 +497,74 @@ def layer_forward_capacity(cfg: OracleConfig, x: np.ndarray, wts: OracleWeights,
     z = combine_capacity(y, perm.scatter_slot, r.weights)
     out = restore_routed_output(cfg, z, wts.w_up_latent, wts.rms_weight)
     return r, perm, y, z, out
+
+
+# --------------------------------------------------------------------------
+# Backward of the experts and of the combine (training)
+# [Olmo-core 3, §"SwiGLU с квантизацией": the SwiGLU backward computes the
+#  sigmoid, gate*sigmoid, its derivative and the two gradients in float32]
+# --------------------------------------------------------------------------
+
+def silu_grad(g: np.ndarray) -> np.ndarray:
+    """d silu / d g = sigmoid(g) * (1 + g * (1 - sigmoid(g)))."""
+    s = 1.0 / (1.0 + np.exp(-g))
+    return s * (1.0 + g * (1.0 - s))
+
+
+def swiglu_mlp_backward(rows: np.ndarray, w_up: np.ndarray, w_gate: np.ndarray, w_out: np.ndarray,
+                        dy: np.ndarray):
+    """Gradients of y = W_out (silu(W_gate r) * W_up r) for a batch of rows r.
+
+    Returns (d rows, d W_up, d W_gate, d W_out, H) where H = silu(g) * u is the
+    activation the W_out gradient contracts with.
+    """
+    u = rows @ w_up.T
+    g = rows @ w_gate.T
+    h = silu(g) * u
+    dh = dy @ w_out
+    du = dh * silu(g)
+    dg = dh * u * silu_grad(g)
+    d_rows = du @ w_up + dg @ w_gate
+    return d_rows, du.T @ rows, dg.T @ rows, dy.T @ h, h
+
+
+def combine_backward(dz: np.ndarray, y: np.ndarray, scatter_pos: np.ndarray, weights: np.ndarray):
+    """Gradients of z[t] = sum_j w[t, j] y[scatter_pos[t*k + j]]:
+    dy[p] = w[t, j] dz[t] for the assignment (t, j) in row p; dw[t, j] = <dz[t], y[p]>."""
+    dz = np.asarray(dz, np.float64)
+    y = np.asarray(y, np.float64)
+    weights = np.asarray(weights, np.float64)
+    T, k = weights.shape
+    dy = np.zeros_like(y)
+    dw = np.zeros((T, k), np.float64)
+    for t in range(T):
+        for j in range(k):
+            p = scatter_pos[t * k + j]
+            if p < 0:
+                continue
+            dy[p] = weights[t, j] * dz[t]
+            dw[t, j] = dz[t] @ y[p]
+    return dy, dw
+
+
+def experts_backward(cfg: OracleConfig, x_routed: np.ndarray, perm: Permutation, expert: ExpertFn, dy: np.ndarray):
+    """Gradients of the grouped SwiGLU experts (y in permuted order, as expert_outputs).
+
+    Returns (d x_routed (T, L), {e: (dW_up, dW_gate, dW_out)}): a token's input
+    gradient sums its k assignments' row gradients.
+    """
+    x_routed = np.asarray(x_routed, np.float64)
+    dy = np.asarray(dy, np.float64)
+    dx = np.zeros_like(x_routed)
+    grads = {}
+    for e in range(cfg.num_experts):
+        lo, hi = int(perm.offsets[e]), int(perm.offsets[e + 1])
+        w_up, w_gate, w_out = (np.asarray(a, np.float64) for a in expert(e))
+        if hi == lo:
+            grads[e] = (np.zeros_like(w_up), np.zeros_like(w_gate), np.zeros_like(w_out))
+            continue
+        tokens = perm.gather_token[lo:hi]
+        d_rows, dwu, dwg, dwo, _ = swiglu_mlp_backward(x_routed[tokens], w_up, w_gate, w_out, dy[lo:hi])
+        np.add.at(dx, tokens, d_rows)
+        grads[e] = (dwu, dwg, dwo)
+    return dx, grads

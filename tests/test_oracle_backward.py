@@ -1,0 +1,67 @@
+"""Pins of the oracle's backward: the hand-derived gradients of the SwiGLU expert, the grouped
+experts and the combine against central finite differences of the forward oracle (float64,
+tiny sizes), and silu' against torch autograd."""
+import numpy as np
+import torch
+
+from oracle import moe_ref as ref
+
+
+def _fd(f, x, eps=1e-6):
+    g = np.zeros_like(x)
+    it = np.nditer(x, flags=["multi_index"])
+    for _ in it:
+        i = it.multi_index
+        old = x[i]
+        x[i] = old + eps
+        fp = f()
+        x[i] = old - eps
+        fm = f()
+        x[i] = old
+        g[i] = (fp - fm) / (2 * eps)
+    return g
+
+
+def test_silu_grad_matches_autograd():
+    g = torch.linspace(-20, 20, 401, dtype=torch.float64, requires_grad=True)
+    torch.nn.functional.silu(g).sum().backward()
+    np.testing.assert_allclose(ref.silu_grad(g.detach().numpy()), g.grad.numpy(), rtol=1e-12, atol=1e-15)
+
+
+def test_swiglu_mlp_backward_finite_differences():
+    rng = np.random.default_rng(0)
+    n, L, h = 3, 5, 4
+    rows, wu, wg = rng.standard_normal((n, L)), rng.standard_normal((h, L)), rng.standard_normal((h, L))
+    wo, probe = rng.standard_normal((L, h)), rng.standard_normal((n, L))
+    loss = lambda: float((ref.swiglu_mlp(rows, wu, wg, wo) * probe).sum())   # noqa: E731
+    d_rows, dwu, dwg, dwo, h_act = ref.swiglu_mlp_backward(rows, wu, wg, wo, probe)
+    for got, arr in ((d_rows, rows), (dwu, wu), (dwg, wg), (dwo, wo)):
+        np.testing.assert_allclose(got, _fd(loss, arr), rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(h_act, ref.silu(rows @ wg.T) * (rows @ wu.T), rtol=1e-14)
+
+
+def test_experts_and_combine_backward_finite_differences():
+    rng = np.random.default_rng(1)
+    T, L, E, h, k = 6, 4, 3, 3, 2
+    ups, gates, outs = rng.standard_normal((E, h, L)), rng.standard_normal((E, h, L)), rng.standard_normal((E, L, h))
+    x = rng.standard_normal((T, L))
+    idx = np.array([[0, 2], [1, 0], [2, 1], [0, 1], [2, 0], [1, 2]])
+    w = rng.random((T, k))
+    perm = ref.permute(idx, E)
+    cfg = ref.OracleConfig(d_model=L, num_experts=E, top_k=k, hidden_size=h)
+    expert = lambda e: (ups[e], gates[e], outs[e])   # noqa: E731
+    probe = rng.standard_normal((T, L))
+
+    def loss():
+        y = ref.expert_outputs(cfg, x, perm, expert)
+        return float((ref.combine(y, perm.scatter_pos, w) * probe).sum())
+
+    y = ref.expert_outputs(cfg, x, perm, expert)
+    dy, dw = ref.combine_backward(probe, y, perm.scatter_pos, w)
+    np.testing.assert_allclose(dw, _fd(loss, w), rtol=1e-6, atol=1e-8)
+    dx, grads = ref.experts_backward(cfg, x, perm, expert, dy)
+    np.testing.assert_allclose(dx, _fd(loss, x), rtol=1e-6, atol=1e-8)
+    for e in range(E):
+        np.testing.assert_allclose(grads[e][0], _fd(loss, ups[e]), rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(grads[e][1], _fd(loss, gates[e]), rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(grads[e][2], _fd(loss, outs[e]), rtol=1e-6, atol=1e-8)

@@ -39,6 +39,8 @@ struct GemmParams {
   void* out;
   long long ldo;
   long long split_stride;
+  int k_groups;            // > 0: K-grouped (group g contracts k-tiles [k_off[g], k_off[g+1]))
+  const int* k_off;        // device (k_groups+1) k-tile offsets
   int* status;
 };
 
@@ -75,6 +77,20 @@ template <int ROWS = BM>
 __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, const int* s_toff,
                                                  const int* s_goff) {
   TileCoord c;
+  if (p.k_groups > 0) {
+    // K-grouped: tile t = ((g * mtiles) + mt) * n_tiles + nt; the group's output is the g-th "split" slice
+    const int mtiles = (p.M + ROWS - 1) / ROWS;
+    c.nt = t % p.n_tiles;
+    const int rest = t / p.n_tiles;
+    const int mt = rest % mtiles;
+    c.group = rest / mtiles;
+    c.split = c.group;
+    c.row0 = mt * ROWS;
+    c.rows = min(ROWS, p.M - c.row0);
+    c.kt0 = s_goff[c.group];
+    c.kt1 = s_goff[c.group + 1];
+    return c;
+  }
   c.split = t % p.splits;
   const int rest = t / p.splits;
   c.nt = rest % p.n_tiles;
@@ -104,7 +120,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
 // row_in_tile: this thread's row of the 128-row accumulator; rows: valid rows from row0.
 template <int BN, int EPI>
 __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, int row_in_tile, int nt, int split,
-                                           const GemmParams& p) {
+                                           const GemmParams& p, bool zero = false) {
   const bool row_ok = row_in_tile < rows;
   const long long row = (long long)row0 + row_in_tile;
   if (EPI == EPI_SWIGLU) {
@@ -139,8 +155,13 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
     for (int cc = 0; cc < BN / 32; ++cc) {
       uint32_t v[32];
       __syncwarp();
-      tmem_ld_32x32b_x32(tbase + cc * 32, v);
-      tmem_ld_wait();
+      if (zero) {  // empty contraction (a K-grouped group without rows): the product is zero
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = 0u;
+      } else {
+        tmem_ld_32x32b_x32(tbase + cc * 32, v);
+        tmem_ld_wait();
+      }
       const int col0 = nt * BN + cc * 32;
       if (!row_ok || col0 >= p.N) continue;
       if (EPI == EPI_F32) {
@@ -196,6 +217,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_toff[i] = p.tile_off[i];
       s_goff[i] = p.group_off[i];
     }
+  } else if (p.k_groups > 0) {
+    for (int i = threadIdx.x; i <= p.k_groups; i += blockDim.x) s_goff[i] = p.k_off[i];
   }
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -220,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem_base = *tmem_holder;
   {
     const int mtiles = p.num_groups > 0 ? s_toff[p.num_groups] : (p.M + BM - 1) / BM;
-    total_tiles = mtiles * p.n_tiles * p.splits;
+    total_tiles = mtiles * p.n_tiles * (p.k_groups > 0 ? p.k_groups : p.splits);
   }
 
   if (warp == 0) {
@@ -295,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
-      store_tile<BN, EPI>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p);
+      store_tile<BN, EPI>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p, c.kt1 <= c.kt0);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
@@ -590,7 +613,9 @@ static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb
 }
 
 cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
-  if (q.num_groups > kMaxGroups) return cudaErrorInvalidValue;
+  if (q.num_groups > kMaxGroups || q.k_groups > kMaxGroups) return cudaErrorInvalidValue;
+  if (q.k_groups > 0 && (q.num_groups > 0 || q.pair_tiles || q.splits > 1 || q.epilogue != EPI_F32))
+    return cudaErrorInvalidValue;
   const bool pair = q.pair_tiles != 0;
   if (pair && (q.bn != 256 || q.splits > 1 || q.epilogue == EPI_F32)) return cudaErrorInvalidValue;
   const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
@@ -615,6 +640,8 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.out = q.out;
   gp.ldo = q.ldo;
   gp.split_stride = q.split_stride;
+  gp.k_groups = q.k_groups;
+  gp.k_off = q.k_off;
   gp.status = q.status;
 
   if (pair) {
@@ -624,7 +651,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   }
   int grid = num_sms();
   if (q.num_groups == 0) {
-    const int tiles = ((q.M + BM - 1) / BM) * gp.n_tiles * gp.splits;
+    const int tiles = ((q.M + BM - 1) / BM) * gp.n_tiles * (q.k_groups > 0 ? q.k_groups : gp.splits);
     grid = std::min(grid, std::max(1, tiles));
   }
 

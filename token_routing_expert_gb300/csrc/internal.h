@@ -30,6 +30,9 @@ struct GemmProblem {
   void* out;
   int64_t ldo;            // elements
   int64_t split_stride;   // elements between split-K slices
+  int k_groups;           // > 0: K-grouped GEMM (fp32 out only): group g multiplies A[:, K_g] by B[:, K_g]^T
+                          //      and writes slice g (split_stride apart); K_g = k-tiles [k_off[g], k_off[g+1])
+  const int* k_off;       // device (k_groups+1) offsets in 64-column k-tiles
   int* status;
 };
 

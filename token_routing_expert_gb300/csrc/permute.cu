@@ -21,10 +21,11 @@ constexpr int kPermWarps = kPermThreads / 32;
 
 int permute_blocks(int R, int chunk) { return (R + chunk - 1) / chunk; }
 
-// Assignments per block: about two blocks per SM, 256 to 4096, a multiple of 256
-// (each of the 8 warps walks chunk / 8 assignments).
+// Assignments per block: about 76 blocks (the scan walks one histogram per block,
+// so more blocks cost more than they gain), 256 to 4096, a multiple of 256 (each
+// of the 8 warps walks chunk / 8 assignments).
 int permute_chunk(int R) {
-  int c = (R / 304 + 255) / 256 * 256;
+  int c = (R / 76 + 255) / 256 * 256;
   return c < 256 ? 256 : (c > kMaxChunk ? kMaxChunk : c);
 }
 
@@ -78,7 +79,19 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ b
   const int e = threadIdx.x;
   int run = 0;
   if (e < E) {
-    for (int b = 0; b < nblk; ++b) {
+    // eight independent loads in flight, then their running sums
+    int b = 0;
+    for (; b + 8 <= nblk; b += 8) {
+      int c[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = blk[(long long)(b + i) * E + e];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        blk[(long long)(b + i) * E + e] = run;
+        run += c[i];
+      }
+    }
+    for (; b < nblk; ++b) {
       const int c = blk[(long long)b * E + e];
       blk[(long long)b * E + e] = run;
       run += c;

@@ -339,6 +339,44 @@ def run_native(args):
     if native.moe_get_status() != 0:
         raise SystemExit("device status error in the end-to-end region")
 
+    bwd = None
+    if args.backward:
+        # backward of the combine and of the grouped SwiGLU experts on this batch (fresh dz each run)
+        counts_d, offsets_d = inter["counts"], inter["offsets"]
+        gather_d, scatter_d, w_d = inter["gather_idx"], inter["scatter_idx"], inter["weights"]
+        y_d = inter["y"]
+        xr_d = inter["x_routed"] if spec.latent_dim else x
+        dz = torch.randn((T, spec.routed_dim), device="cuda").to(torch.bfloat16)
+        dy_d = torch.empty_like(y_d)
+        dw_d = torch.empty_like(w_d)
+        bws = native.backward_workspace(cfg, T)
+        dx_d = torch.empty((T, spec.routed_dim), dtype=torch.bfloat16, device="cuda")
+        dwug = torch.empty((spec.num_experts, 2 * spec.hidden_size, spec.routed_dim), dtype=torch.float32, device="cuda")
+        dwo = torch.empty((spec.num_experts, spec.routed_dim, spec.hidden_size), dtype=torch.float32, device="cuda")
+
+        def backward_step():
+            native.moe_combine_backward(cfg, dz, y_d, scatter_d, w_d, gather_idx=gather_d, dy=dy_d, dweights=dw_d)
+            native.moe_grouped_swiglu_backward(cfg, wts, xr_d, gather_d, offsets_d, scatter_d, dy_d, bws,
+                                               dx_routed=dx_d, dw_up_gate=dwug, dw_out=dwo)
+
+        for _ in range(3):
+            backward_step()
+        torch.cuda.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(args.steps):
+            backward_step()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        if native.moe_get_status() != 0:
+            raise SystemExit("device status error in the backward")
+        bms = c0.elapsed_time(c1) / args.steps
+        bflops = 12 * spec.rows * spec.routed_dim * spec.hidden_size
+        bwd = {"ms": bms, "tflops": bflops / (bms * 1e-3) / 1e12, "algorithmic_flops": bflops,
+               "note": "combine backward + experts backward (dH, dX, dW_out, dW_up_gate GEMMs = 12 R L h FLOPs; "
+                       "the pre-activations are recomputed, 4 R L h more)"}
+        del bws
+
     # load-balancing counters on this batch's histogram (between-step work, timed on its own)
     counts = inter["counts"].clone()
     accum = torch.zeros(spec.num_experts, dtype=torch.int64, device="cuda")
@@ -415,6 +453,7 @@ def run_native(args):
                   "dropped_assignments": dropped},
         "stages_ms": stage_ms,
         "balance": bal,
+        "backward": bwd,
         "roofline": {"kernel": "grouped GEMM 1 (SwiGLU fused, tcgen05)", "bound": "tensor",
                      "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
                      "traffic": kernel_traffic(spec.name),
@@ -448,6 +487,7 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=512, help="oracle sample for the cpu_baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--backward", action="store_true", help="also time the combine + experts backward")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

@@ -236,6 +236,34 @@ int moe_layer_forward_staged(const moe_config_t* cfg, const moe_weights_t* w, co
 int moe_layer_forward_launches(const moe_config_t* cfg, int64_t T, int32_t* n);
 
 /*
+ * Backward of the weighted combine and of the grouped SwiGLU experts (training).
+ * The page's SwiGLU backward (section "SwiGLU с квантизацией"): split into up
+ * and gate, sigmoid, gate * sigmoid, its derivative and the two gradients in
+ * fp32, stored back in bf16.  rows = moe_permuted_rows(cfg, T).
+ *
+ * moe_combine_backward: for each assignment (t, j) with row p:
+ *   dy[p] = weights[t, j] * dz[t] (bf16) and dweights[t, j] = <dz[t], y[p]> (fp32);
+ *   dropped assignments (capacity mode) get dweights 0; padding rows of dy are zeroed.
+ *   dz device (T, L') bf16; y device (rows, L') bf16 (the forward's expert outputs);
+ *   scatter_idx (T*k), gather_idx (rows, capacity mode only, else may be NULL),
+ *   weights (T, k) fp32; dy device (rows, L') bf16 out; dweights device (T, k) fp32 out.
+ *
+ * moe_grouped_swiglu_backward: given the forward's inputs and dy (rows, L'):
+ *   dx_routed (T, L') bf16 out: each token's input gradient, summed over its rows;
+ *   dw_up_gate (E, 2h, L') fp32 out and dw_out (E, L', h) fp32 out: weight
+ *   gradients (an expert without rows gets zeros).  Pre-activations are
+ *   recomputed; ws must hold moe_backward_workspace_size(cfg, T) bytes.
+ */
+int moe_backward_workspace_size(const moe_config_t* cfg, int64_t T, size_t* bytes);
+int moe_combine_backward(const moe_config_t* cfg, const void* dz, const void* y, const int32_t* scatter_idx,
+                         const int32_t* gather_idx, const float* weights, int64_t T, void* dy, float* dweights,
+                         moe_stream_t stream);
+int moe_grouped_swiglu_backward(const moe_config_t* cfg, const moe_weights_t* w, const void* x_routed,
+                                const int32_t* gather_idx, const int32_t* offsets, const int32_t* scatter_idx,
+                                int64_t T, const void* dy, void* dx_routed, float* dw_up_gate, float* dw_out,
+                                void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * Load-balancing counters, section "Счётчики и bias-корректировка" (run between
  * training steps or batches; E <= 1024, one small kernel each).
  *

@@ -317,6 +317,88 @@ int run_restore(const moe_config_t* c, const moe_weights_t* w, const void* z, bo
   return dense_gemm_bf16(n, w->w_up_latent, (int)p.T, p.D, p.L, out, p.up_splits, at<float>(ws, p.part), status, st);
 }
 
+// Workspace of the experts' backward.
+struct BwdPlan {
+  int64_t rows, kpad;
+  size_t xp, ug, dh, h, dug, dxp, wo_t, wug_t, dy_t, h_t, dug_t, xp_t, k_off, tile_off, total;
+};
+
+void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
+  const int64_t E = c->num_experts, h = c->hidden_size;
+  const int64_t Lr = c->latent_dim > 0 ? c->latent_dim : c->d_model;
+  b->rows = c->capacity_factor > 0.f ? E * capacity_of(c, T) : T * c->top_k;
+  b->kpad = ((b->rows + 64 * E) + 63) / 64 * 64;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  b->xp = take((size_t)b->rows * Lr * 2);
+  b->ug = take((size_t)b->rows * 2 * h * 2);
+  b->dh = take((size_t)b->rows * h * 2);
+  b->h = take((size_t)b->rows * h * 2);
+  b->dug = take((size_t)b->rows * 2 * h * 2);
+  b->dxp = take((size_t)b->rows * Lr * 2);
+  b->wo_t = take((size_t)E * h * Lr * 2);
+  b->wug_t = take((size_t)E * 2 * h * Lr * 2);
+  b->dy_t = take((size_t)Lr * b->kpad * 2);
+  b->h_t = take((size_t)h * b->kpad * 2);
+  b->dug_t = take((size_t)2 * h * b->kpad * 2);
+  b->xp_t = take((size_t)Lr * b->kpad * 2);
+  b->k_off = take((size_t)(E + 1) * 4);
+  b->tile_off = take((size_t)(E + 1) * 4);
+  b->total = o;
+}
+
+// M-grouped bf16 GEMM out = A B^T over the experts' row groups.
+int grouped_bf16(const void* A, int64_t rows, const void* B, int64_t b_rows_total, int b_rows_per_group, int N, int K,
+                 const int32_t* offsets, const int32_t* tile_off, int E, int pair, void* out, int* status,
+                 cudaStream_t st) {
+  GemmProblem g{};
+  g.A = A;
+  g.B = B;
+  g.b_rows_total = b_rows_total;
+  g.M = (int)rows;
+  g.N = N;
+  g.K = K;
+  g.num_groups = E;
+  g.group_off = offsets;
+  g.tile_off = tile_off;
+  g.b_rows_per_group = b_rows_per_group;
+  g.epilogue = EPI_BF16;
+  g.bn = 256;
+  g.splits = 1;
+  g.pair_tiles = pair;
+  g.out = out;
+  g.ldo = N;
+  g.status = status;
+  return cuda_status(launch_gemm(g, st));
+}
+
+// K-grouped fp32 GEMM: out[e] (M x N) = A[:, K_e] B[:, K_e]^T.
+int kgrouped_f32(const void* A, int M, const void* B, int N, int64_t kpad, const int32_t* k_off, int E, float* out,
+                 int* status, cudaStream_t st) {
+  GemmProblem g{};
+  g.A = A;
+  g.B = B;
+  g.b_rows_total = N;
+  g.M = M;
+  g.N = N;
+  g.K = (int)kpad;
+  g.num_groups = 0;
+  g.epilogue = EPI_F32;
+  g.bn = pick_bn_f32(N);
+  g.splits = 1;
+  g.k_groups = E;
+  g.k_off = k_off;
+  g.out = out;
+  g.ldo = N;
+  g.split_stride = (int64_t)M * N;
+  g.status = status;
+  return cuda_status(launch_gemm(g, st));
+}
+
 }  // namespace
 
 int* device_status() { return status_ptr(); }
@@ -567,6 +649,110 @@ int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
   if (p.latent) k += p.up_splits > 1 ? 2 : 1;    // latent up (+ split-K reduce)
   *n = k;
   return MOE_OK;
+}
+
+int moe_backward_workspace_size(const moe_config_t* c, int64_t T, size_t* bytes) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0 || !bytes) return MOE_ERR_INVALID_ARG;
+  BwdPlan b;
+  make_bwd_plan(c, T, &b);
+  *bytes = b.total;
+  return MOE_OK;
+}
+
+int moe_combine_backward(const moe_config_t* c, const void* dz, const void* y, const int32_t* scatter_idx,
+                         const int32_t* gather_idx, const float* weights, int64_t T, void* dy, float* dweights,
+                         moe_stream_t stream) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!dz || !y || !scatter_idx || !weights || !dy || !dweights) return MOE_ERR_INVALID_ARG;
+  const bool capacity = c->capacity_factor > 0.f;
+  if (capacity && !gather_idx) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)T * c->top_k > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  const int64_t rows = capacity ? (int64_t)c->num_experts * capacity_of(c, T) : T * c->top_k;
+  if (rows > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int Lr = c->latent_dim > 0 ? c->latent_dim : c->d_model;
+  if (capacity) {
+    s = cuda_status(launch_zero_padding_rows(gather_idx, (int)rows, Lr, dy, st));
+    if (s != MOE_OK) return s;
+  }
+  return cuda_status(
+      launch_combine_backward(dz, y, scatter_idx, weights, (int)T, c->top_k, Lr, (int)rows, dy, dweights, status, st));
+}
+
+int moe_grouped_swiglu_backward(const moe_config_t* c, const moe_weights_t* w, const void* x_routed,
+                                const int32_t* gather_idx, const int32_t* offsets, const int32_t* scatter_idx,
+                                int64_t T, const void* dy, void* dx_routed, float* dw_up_gate, float* dw_out,
+                                void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if ((int64_t)T * c->top_k > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  BwdPlan b;
+  make_bwd_plan(c, T, &b);
+  if (b.rows > (int64_t)0x7fffffff - 128 || b.kpad > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!ws || ((uintptr_t)ws & 255) || ws_bytes < b.total) return MOE_ERR_WORKSPACE;
+  if (!w || !w->w_up_gate || !w->w_out || !x_routed || !gather_idx || !offsets || !scatter_idx || !dy ||
+      !dx_routed || !dw_up_gate || !dw_out)
+    return MOE_ERR_INVALID_ARG;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int E = c->num_experts, h = c->hidden_size, k = c->top_k;
+  const int Lr = c->latent_dim > 0 ? c->latent_dim : c->d_model;
+  const bool capacity = c->capacity_factor > 0.f;
+  const int rows = (int)b.rows;
+  const int pair = rows >= 384 * E ? 1 : 0;
+  int32_t* tile_off = at<int32_t>(ws, b.tile_off);
+  int32_t* k_off = at<int32_t>(ws, b.k_off);
+  void* xp = at<void>(ws, b.xp);
+  void* UG = at<void>(ws, b.ug);
+  void* dH = at<void>(ws, b.dh);
+  void* H = at<void>(ws, b.h);
+  void* dUG = at<void>(ws, b.dug);
+  void* dXp = at<void>(ws, b.dxp);
+  void* woT = at<void>(ws, b.wo_t);
+  void* wugT = at<void>(ws, b.wug_t);
+  void* dyT = at<void>(ws, b.dy_t);
+  void* hT = at<void>(ws, b.h_t);
+  void* dugT = at<void>(ws, b.dug_t);
+  void* xpT = at<void>(ws, b.xp_t);
+
+  s = cuda_status(launch_tile_table(offsets, E, pair ? 256 : 128, tile_off, st));
+  if (s == MOE_OK) s = cuda_status(launch_tile_table(offsets, E, 64, k_off, st));  // 64-row k-tiles per expert
+  if (s == MOE_OK) s = cuda_status(launch_gather_rows(x_routed, gather_idx, rows, (int)T, Lr, xp, capacity, status, st));
+  // recomputed pre-activations [u | g]
+  if (s == MOE_OK)
+    s = grouped_bf16(xp, rows, w->w_up_gate, (int64_t)E * 2 * h, 2 * h, 2 * h, Lr, offsets, tile_off, E, pair, UG,
+                     status, st);
+  // per-expert transposes of the weights
+  if (s == MOE_OK) s = cuda_status(launch_transpose_experts(w->w_out, E, Lr, h, woT, st));
+  if (s == MOE_OK) s = cuda_status(launch_transpose_experts(w->w_up_gate, E, 2 * h, Lr, wugT, st));
+  // dH = dY W_out ; SwiGLU backward ; dXp = dUG W_up_gate ; dx = sum over a token's rows
+  if (s == MOE_OK)
+    s = grouped_bf16(dy, rows, woT, (int64_t)E * h, h, h, Lr, offsets, tile_off, E, pair, dH, status, st);
+  if (s == MOE_OK) s = cuda_status(launch_swiglu_backward(UG, dH, rows, h, dUG, H, st));
+  if (s == MOE_OK)
+    s = grouped_bf16(dUG, rows, wugT, (int64_t)E * Lr, Lr, Lr, 2 * h, offsets, tile_off, E, pair, dXp, status, st);
+  if (s == MOE_OK)
+    s = cuda_status(launch_combine(dXp, scatter_idx, nullptr, (int)T, k, Lr, rows, 0, 0.f, nullptr, dx_routed,
+                                   capacity ? 1 : 0, status, st));
+  // weight gradients: K-grouped over each expert's rows
+  const long long maxc = b.kpad;
+  if (s == MOE_OK) s = cuda_status(launch_group_transpose(dy, Lr, offsets, k_off, E, maxc, b.kpad, dyT, st));
+  if (s == MOE_OK) s = cuda_status(launch_group_transpose(H, h, offsets, k_off, E, maxc, b.kpad, hT, st));
+  if (s == MOE_OK) s = cuda_status(launch_group_transpose(dUG, 2 * h, offsets, k_off, E, maxc, b.kpad, dugT, st));
+  if (s == MOE_OK) s = cuda_status(launch_group_transpose(xp, Lr, offsets, k_off, E, maxc, b.kpad, xpT, st));
+  if (s == MOE_OK) s = kgrouped_f32(dyT, Lr, hT, h, b.kpad, k_off, E, dw_out, status, st);
+  if (s == MOE_OK) s = kgrouped_f32(dugT, 2 * h, xpT, Lr, b.kpad, k_off, E, dw_up_gate, status, st);
+  return s;
 }
 
 int moe_get_status(moe_stream_t stream, int32_t* device_status, int clear) {

@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(32 * kRowWarps)
   float my_w = 0.f;
   if (lane < k) {
     my_p = scatter_idx[t * k + lane];
-    my_w = w[t * k + lane];
+    my_w = w ? w[t * k + lane] : 1.0f;   // no weights: plain sum of the k rows
     if (my_p < 0 || my_p >= R) {
       if (!(allow_dropped && my_p == -1)) set_status(status, MOE_ERR_BOUNDS);  // -1: dropped, adds nothing
       my_p = 0;

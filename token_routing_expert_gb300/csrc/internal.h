@@ -73,6 +73,14 @@ cudaError_t launch_combine(const void* y, const int32_t* scatter_idx, const floa
                            cudaStream_t stream);
 cudaError_t launch_rmsnorm(const void* z, int T, int L, float eps, const void* gain, void* out,
                            cudaStream_t stream);
+cudaError_t launch_transpose_experts(const void* in, int E, int A, int B, void* out, cudaStream_t st);
+cudaError_t launch_group_transpose(const void* X, int C, const int32_t* off, const int32_t* k_off, int E,
+                                   long long max_cols, long long ld_out, void* XT, cudaStream_t st);
+cudaError_t launch_swiglu_backward(const void* UG, const void* dH, long long rows, int h, void* dUG, void* H,
+                                   cudaStream_t st);
+cudaError_t launch_combine_backward(const void* dz, const void* y, const int32_t* scatter_idx, const float* w, int T,
+                                    int k, int L, int rows, void* dy, float* dw, int* status, cudaStream_t st);
+cudaError_t launch_zero_padding_rows(const int32_t* gather_idx, int rows, int cols, void* dst, cudaStream_t st);
 cudaError_t launch_splitk_reduce_bf16(const float* partials, int splits, int64_t slice, void* out,
                                       cudaStream_t stream);
 

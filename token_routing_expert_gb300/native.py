@@ -49,7 +49,8 @@ EXPORTS = ["moe_expert_capacity", "moe_permuted_rows", "moe_validate_config", "m
            "moe_workspace_size", "moe_router", "moe_permute", "moe_grouped_swiglu", "moe_combine",
            "moe_latent_down", "moe_latent_restore", "moe_layer_forward", "moe_layer_forward_staged",
            "moe_layer_forward_launches", "moe_workspace_layout", "moe_get_status", "moe_status_string",
-           "moe_permute_noalloc", "moe_accumulate_counts", "moe_load_imbalance", "moe_score_bias_update"]
+           "moe_permute_noalloc", "moe_accumulate_counts", "moe_load_imbalance", "moe_score_bias_update",
+           "moe_backward_workspace_size", "moe_combine_backward", "moe_grouped_swiglu_backward"]
 
 _lib = None
 
@@ -86,6 +87,9 @@ def load() -> ctypes.CDLL:
         "moe_status_string": [ctypes.c_int],
         "moe_permute_noalloc": [cfgp, VP, I64, VP, VP, VP, VP, VP],
         "moe_accumulate_counts": [VP, ctypes.c_int32, VP, VP],
+        "moe_backward_workspace_size": [cfgp, I64, P(SZ)],
+        "moe_combine_backward": [cfgp, VP, VP, VP, VP, VP, I64, VP, VP, VP],
+        "moe_grouped_swiglu_backward": [cfgp, wp, VP, VP, VP, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
         "moe_load_imbalance": [VP, ctypes.c_int32, ctypes.c_int32, VP, VP],
         "moe_score_bias_update": [VP, ctypes.c_int32, ctypes.c_float, VP, VP],
     }
@@ -351,6 +355,49 @@ def moe_layer_forward_launches(cfg, T: int) -> int:
     n = ctypes.c_int32()
     _check(load().moe_layer_forward_launches(ctypes.byref(cfg), T, ctypes.byref(n)), "moe_layer_forward_launches")
     return n.value
+
+
+def moe_backward_workspace_size(cfg: moe_config_t, T: int) -> int:
+    out = ctypes.c_size_t()
+    _check(load().moe_backward_workspace_size(ctypes.byref(cfg), T, ctypes.byref(out)), "moe_backward_workspace_size")
+    return out.value
+
+
+def backward_workspace(cfg, T, device="cuda") -> torch.Tensor:
+    return torch.empty(max(1, moe_backward_workspace_size(cfg, T)), dtype=torch.uint8, device=device)
+
+
+def moe_combine_backward(cfg, dz, y, scatter_idx, weights, gather_idx=None, dy=None, dweights=None, stream=None):
+    """dy (rows, L') bf16 and dweights (T, k) fp32 of the weighted combine."""
+    T = dz.shape[0]
+    dy = torch.empty_like(y) if dy is None else dy
+    dweights = torch.empty((T, cfg.top_k), dtype=torch.float32, device=dz.device) if dweights is None else dweights
+    _check(load().moe_combine_backward(ctypes.byref(cfg), _ptr(dz, torch.bfloat16, "dz"), _ptr(y, torch.bfloat16, "y"),
+                                       _ptr(scatter_idx, torch.int32, "scatter_idx"),
+                                       _ptr(gather_idx, torch.int32, "gather_idx"), _ptr(weights, torch.float32, "weights"),
+                                       T, _ptr(dy, torch.bfloat16, "dy"), _ptr(dweights, torch.float32, "dweights"),
+                                       _stream(stream)), "moe_combine_backward")
+    return dy, dweights
+
+
+def moe_grouped_swiglu_backward(cfg, weights: DeviceWeights, x_routed, gather_idx, offsets, scatter_idx, dy, bws,
+                                dx_routed=None, dw_up_gate=None, dw_out=None, stream=None):
+    """Input and weight gradients of the grouped SwiGLU experts (bws: backward_workspace)."""
+    T, Lr = x_routed.shape
+    E, h = cfg.num_experts, cfg.hidden_size
+    dev = x_routed.device
+    dx_routed = torch.empty((T, Lr), dtype=torch.bfloat16, device=dev) if dx_routed is None else dx_routed
+    dw_up_gate = torch.empty((E, 2 * h, Lr), dtype=torch.float32, device=dev) if dw_up_gate is None else dw_up_gate
+    dw_out = torch.empty((E, Lr, h), dtype=torch.float32, device=dev) if dw_out is None else dw_out
+    ws_ = weights.struct()
+    _check(load().moe_grouped_swiglu_backward(
+        ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x_routed, torch.bfloat16, "x_routed"),
+        _ptr(gather_idx, torch.int32, "gather_idx"), _ptr(offsets, torch.int32, "offsets"),
+        _ptr(scatter_idx, torch.int32, "scatter_idx"), T, _ptr(dy, torch.bfloat16, "dy"),
+        _ptr(dx_routed, torch.bfloat16, "dx_routed"), _ptr(dw_up_gate, torch.float32, "dw_up_gate"),
+        _ptr(dw_out, torch.float32, "dw_out"), _ptr(bws, None, "ws"), bws.numel(), _stream(stream)),
+        "moe_grouped_swiglu_backward")
+    return dx_routed, dw_up_gate, dw_out
 
 
 def moe_accumulate_counts(counts, accum, stream=None):

@@ -255,6 +255,22 @@ int moe_layer_forward_launches(const moe_config_t* cfg, int64_t T, int32_t* n);
  *   recomputed; ws must hold moe_backward_workspace_size(cfg, T) bytes.
  */
 int moe_backward_workspace_size(const moe_config_t* cfg, int64_t T, size_t* bytes);
+
+/*
+ * Router backward for the forward's choice of experts (section "Маршрутизация:
+ * как роутер выбирает экспертов"; the selection is discrete, score_bias only
+ * moves it and gets no gradient).  The routing-weight gradient is taken back
+ * through the scalings, the p-norm and the gating function to the logits, then
+ * through the linear layer:
+ *   x (T, D) bf16; logits (T, E) fp32 as moe_router returned them (with bias);
+ *   idx (T, k); dweights (T, k) fp32;
+ *   dlogits (T, E) fp32 out; dx (T, D) bf16 out (the router's share of the
+ *   input gradient); dw_router (E, D) fp32 out; db_router (E) fp32 out, or NULL
+ *   (written only with a router bias).  ws: moe_backward_workspace_size bytes.
+ */
+int moe_router_backward(const moe_config_t* cfg, const moe_weights_t* w, const void* x, int64_t T, const float* logits,
+                        const int32_t* idx, const float* dweights, float* dlogits, void* dx, float* dw_router,
+                        float* db_router, void* ws, size_t ws_bytes, moe_stream_t stream);
 int moe_combine_backward(const moe_config_t* cfg, const void* dz, const void* y, const int32_t* scatter_idx,
                          const int32_t* gather_idx, const float* weights, int64_t T, void* dy, float* dweights,
                          moe_stream_t stream);

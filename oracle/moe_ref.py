@@ -568,3 +568,49 @@ def experts_backward(cfg: OracleConfig, x_routed: np.ndarray, perm: Permutation,
         np.add.at(dx, tokens, d_rows)
         grads[e] = (dwu, dwg, dwo)
     return dx, grads
+
+
+def router_backward(cfg: OracleConfig, x: np.ndarray, w_router: np.ndarray, b_router: Optional[np.ndarray],
+                    score_bias: Optional[np.ndarray], idx: np.ndarray, dweights: np.ndarray):
+    """Gradients of the routing weights for a fixed choice of experts.
+
+    The selection itself is discrete; score_bias only moves the selection and
+    gets no gradient.  Returns (dlogits (T, E), dx (T, D), dW_router (E, D),
+    db_router (E,)).
+    """
+    x = np.asarray(x, np.float64)
+    idx = np.asarray(idx, np.int64)
+    r = route(cfg, x, w_router, b_router, score_bias, forced_idx=idx)
+    T, k = idx.shape
+    E = cfg.num_experts
+    scale = 1.0
+    if cfg.restore_weight_scale:
+        scale *= cfg.top_k
+    if cfg.expert_weight_scale:
+        scale *= cfg.expert_weight_scale
+    if cfg.original_top_k and cfg.original_top_k != cfg.top_k:
+        scale *= math.sqrt(cfg.original_top_k / cfg.top_k)
+    d_norm = np.asarray(dweights, np.float64) * scale
+    w_raw = routing_weights(r.logits, r.scores, idx, cfg.gating)
+    p = cfg.normalize_expert_weights
+    if p:
+        n = ((np.abs(w_raw) ** p).sum(axis=1, keepdims=True)) ** (1.0 / p)
+        dn_dw = np.sign(w_raw) * np.abs(w_raw) ** (p - 1) * n ** (1 - p)
+        d_raw = d_norm / n - (d_norm * w_raw).sum(axis=1, keepdims=True) / n ** 2 * dn_dw
+    else:
+        d_raw = d_norm
+    dlogits = np.zeros((T, E), np.float64)
+    rows = np.arange(T)[:, None]
+    if cfg.gating == GATING_SOFTMAX:
+        ds = np.zeros((T, E), np.float64)
+        np.add.at(ds, (np.broadcast_to(rows, idx.shape), idx), d_raw)
+        s = r.scores
+        dlogits = s * (ds - (ds * s).sum(axis=1, keepdims=True))
+    elif cfg.gating == GATING_TOPK_SOFTMAX:
+        dsel = w_raw * (d_raw - (d_raw * w_raw).sum(axis=1, keepdims=True))
+        np.add.at(dlogits, (np.broadcast_to(rows, idx.shape), idx), dsel)
+    else:
+        sig = 1.0 / (1.0 + np.exp(-np.take_along_axis(r.logits, idx, axis=1)))
+        np.add.at(dlogits, (np.broadcast_to(rows, idx.shape), idx), d_raw * sig * (1.0 - sig))
+    w_router = np.asarray(w_router, np.float64)
+    return dlogits, dlogits @ w_router, dlogits.T @ x, dlogits.sum(axis=0)

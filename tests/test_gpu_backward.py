@@ -81,3 +81,51 @@ def test_combine_and_experts_backward(name):
         close(got_wug, np.concatenate([dwu, dwg]), f"dW_up_gate[{e}]")
         close(got_wo, dwo_e, f"dW_out[{e}]")
     close(dx.double().cpu().numpy(), dx_want, "dx_routed")
+
+
+ROUTER_CASES = {
+    "softmax_p1": WorkloadSpec("softmax_p1", T=300, d_model=256, num_experts=8, top_k=2, hidden_size=128,
+                               gating="softmax", normalize_expert_weights=1.0, seed=61),
+    "topk_softmax_skew": WorkloadSpec("topk_softmax_skew", T=700, d_model=512, num_experts=40, top_k=6,
+                                      hidden_size=128, gating="topk_softmax", skew=True, seed=62),
+    "sigmoid_restore_bias": WorkloadSpec("sigmoid_restore_bias", T=500, d_model=512, num_experts=64, top_k=8,
+                                         hidden_size=128, gating="sigmoid", sigmoid_stability_epsilon=1e-6,
+                                         score_bias_std=0.01, normalize_expert_weights=1.0,
+                                         restore_weight_scale=True, seed=63),
+    "sigmoid_896_decode": WorkloadSpec("sigmoid_896_decode", T=64, d_model=1024, num_experts=896, top_k=8,
+                                       hidden_size=128, gating="sigmoid", skew=True, original_top_k=16, seed=64),
+    "few_experts": WorkloadSpec("few_experts", T=130, d_model=128, num_experts=6, top_k=6, hidden_size=64,
+                                gating="softmax", expert_weight_scale=2.5, normalize_expert_weights=2.0, seed=65),
+}
+
+
+@pytest.mark.parametrize("name", list(ROUTER_CASES))
+def test_router_backward(name):
+    spec = ROUTER_CASES[name]
+    inp = generate(spec, experts=False)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights(w_router=inp["w_router"].cuda(), w_up_gate=torch.empty(1, dtype=torch.bfloat16, device="cuda"),
+                               w_out=torch.empty(1, dtype=torch.bfloat16, device="cuda"),
+                               b_router=None if inp["b_router"] is None else inp["b_router"].cuda(),
+                               score_bias=None if inp["score_bias"] is None else inp["score_bias"].cuda())
+    T, D, E, k = spec.T, spec.d_model, spec.num_experts, spec.top_k
+    x = inp["x"].cuda()
+    ws = native.workspace(cfg, T)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    _, idx, _ = native.moe_router(cfg, wts, x, ws, logits=logits)
+    g = np.random.default_rng(spec.seed + 5)
+    dweights = torch.from_numpy(g.standard_normal((T, k), dtype=np.float32)).cuda()
+    bws = native.backward_workspace(cfg, T)
+    dl, dx, dw, db = native.moe_router_backward(cfg, wts, x, logits, idx, dweights, bws)
+    assert native.moe_get_status() == 0
+    oc, ow = oracle_config(spec), oracle_weights(spec, {**inp, "w_up_gate": None, "w_out": None})
+    want_dl, want_dx, want_dw, want_db = ref.router_backward(oc, f64(inp["x"]), ow.w_router, ow.b_router,
+                                                             ow.score_bias, idx.cpu().numpy(),
+                                                             dweights.double().cpu().numpy())
+    got_dl = dl.double().cpu().numpy()
+    # fp32 recomputation of the same formulas
+    assert np.abs(got_dl - want_dl).max() <= 1e-5 * np.abs(want_dl).max() + 1e-6
+    close(dx.double().cpu().numpy(), want_dx, "router dx")
+    close(dw.double().cpu().numpy(), want_dw, "dW_router")
+    if spec.skew:
+        close(db.double().cpu().numpy(), want_db, "db_router")

@@ -65,3 +65,31 @@ def test_experts_and_combine_backward_finite_differences():
         np.testing.assert_allclose(grads[e][0], _fd(loss, ups[e]), rtol=1e-6, atol=1e-8)
         np.testing.assert_allclose(grads[e][1], _fd(loss, gates[e]), rtol=1e-6, atol=1e-8)
         np.testing.assert_allclose(grads[e][2], _fd(loss, outs[e]), rtol=1e-6, atol=1e-8)
+
+
+import pytest  # noqa: E402
+
+
+@pytest.mark.parametrize("gating,extra", [
+    (ref.GATING_SOFTMAX, dict(normalize_expert_weights=1.0)),
+    (ref.GATING_TOPK_SOFTMAX, dict(restore_weight_scale=True)),
+    (ref.GATING_SIGMOID, dict(sigmoid_stability_epsilon=1e-3, normalize_expert_weights=1.0, expert_weight_scale=2.0)),
+    (ref.GATING_SIGMOID, dict(normalize_expert_weights=2.0, original_top_k=8)),
+    (ref.GATING_SOFTMAX, dict()),
+])
+def test_router_backward_finite_differences(gating, extra):
+    rng = np.random.default_rng(3)
+    T, D, E, k = 4, 5, 6, 2
+    x, w, b = rng.standard_normal((T, D)), rng.standard_normal((E, D)) * 0.5, rng.standard_normal(E) * 0.1
+    sb = rng.standard_normal(E)
+    cfg = ref.OracleConfig(d_model=D, num_experts=E, top_k=k, hidden_size=4, gating=gating, router_bias=True,
+                           has_score_bias=True, **extra)
+    idx = ref.route(cfg, x, w, b, sb).idx               # the choice is held fixed
+    probe = rng.standard_normal((T, k))
+    loss = lambda: float((ref.route(cfg, x, w, b, sb, forced_idx=idx).weights * probe).sum())   # noqa: E731
+    dl, dx, dw, db = ref.router_backward(cfg, x, w, b, sb, idx, probe)
+    np.testing.assert_allclose(dx, _fd(loss, x), rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dw, _fd(loss, w), rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(db, _fd(loss, b), rtol=1e-6, atol=1e-8)
+    # the selection-only bias carries no gradient
+    np.testing.assert_allclose(_fd(loss, sb), 0.0, atol=1e-9)

@@ -351,6 +351,35 @@ void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
   b->total = o;
 }
 
+// Workspace of the router backward.
+struct RouterBwdPlan {
+  int64_t Epad, Tpad;
+  int dx_splits, dw_splits;
+  size_t dl, wr_t, dl_t, x_t, part, total;
+};
+
+void make_router_bwd_plan(const moe_config_t* c, int64_t T, int sms, RouterBwdPlan* b) {
+  const int64_t E = c->num_experts, D = c->d_model;
+  b->Epad = (E + 63) / 64 * 64;
+  b->Tpad = (T + 63) / 64 * 64;
+  b->dx_splits = splits_for((int)(((T + 127) / 128) * ((D + 255) / 256)), (int)b->Epad, sms);
+  b->dw_splits = splits_for((int)(((E + 127) / 128) * ((D + 255) / 256)), (int)b->Tpad, sms);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  b->dl = take((size_t)T * b->Epad * 2);
+  b->wr_t = take((size_t)D * b->Epad * 2);
+  b->dl_t = take((size_t)b->Epad * b->Tpad * 2);
+  b->x_t = take((size_t)D * b->Tpad * 2);
+  const size_t dx_part = b->dx_splits > 1 ? (size_t)b->dx_splits * T * D * 4 : 0;
+  const size_t dw_part = b->dw_splits > 1 ? (size_t)b->dw_splits * ((E * D + 3) / 4 * 4) * 4 : 0;
+  b->part = take(std::max(dx_part, dw_part));
+  b->total = o;
+}
+
 // M-grouped bf16 GEMM out = A B^T over the experts' row groups.
 int grouped_bf16(const void* A, int64_t rows, const void* B, int64_t b_rows_total, int b_rows_per_group, int N, int K,
                  const int32_t* offsets, const int32_t* tile_off, int E, int pair, void* out, int* status,
@@ -657,8 +686,75 @@ int moe_backward_workspace_size(const moe_config_t* c, int64_t T, size_t* bytes)
   if (T < 0 || !bytes) return MOE_ERR_INVALID_ARG;
   BwdPlan b;
   make_bwd_plan(c, T, &b);
-  *bytes = b.total;
+  RouterBwdPlan r;
+  make_router_bwd_plan(c, T, kSizingSms, &r);
+  *bytes = std::max(b.total, r.total);
   return MOE_OK;
+}
+
+int moe_router_backward(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, const float* logits,
+                        const int32_t* idx, const float* dweights, float* dlogits, void* dx, float* dw_router,
+                        float* db_router, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if ((int64_t)T * c->top_k > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  if (!w || !w->w_router || !x || !logits || !idx || !dweights || !dlogits || !dx || !dw_router)
+    return MOE_ERR_INVALID_ARG;
+  RouterBwdPlan sizing, r;
+  make_router_bwd_plan(c, T, kSizingSms, &sizing);
+  make_router_bwd_plan(c, T, std::min(num_sms(), kSizingSms), &r);
+  if (!ws || ((uintptr_t)ws & 255) || ws_bytes < sizing.total) return MOE_ERR_WORKSPACE;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int E = c->num_experts, D = c->d_model;
+  float scale = 1.f;
+  if (c->restore_weight_scale) scale *= (float)c->top_k;
+  if (c->expert_weight_scale != 0.f) scale *= c->expert_weight_scale;
+  if (c->original_top_k > 0 && c->original_top_k != c->top_k) scale *= sqrtf((float)c->original_top_k / (float)c->top_k);
+  void* dl = at<void>(ws, r.dl);
+  void* wrT = at<void>(ws, r.wr_t);
+  void* dlT = at<void>(ws, r.dl_t);
+  void* xT = at<void>(ws, r.x_t);
+  float* part = at<float>(ws, r.part);
+  s = cuda_status(launch_router_backward(logits, idx, dweights, (int)T, E, c->top_k, c->gating,
+                                         c->sigmoid_stability_epsilon, c->normalize_expert_weights, scale, dlogits, dl,
+                                         (int)r.Epad, st));
+  // dx = dlogits W_router
+  if (s == MOE_OK) s = cuda_status(launch_transpose_pad(w->w_router, E, D, D, r.Epad, wrT, st));
+  if (s == MOE_OK) s = dense_gemm_bf16(dl, wrT, (int)T, D, (int)r.Epad, dx, r.dx_splits, part, status, st);
+  // dW_router = dlogits^T x, contracted over the tokens
+  if (s == MOE_OK) s = cuda_status(launch_transpose_pad(dl, (int)T, (int)r.Epad, r.Epad, r.Tpad, dlT, st));
+  if (s == MOE_OK) s = cuda_status(launch_transpose_pad(x, (int)T, D, D, r.Tpad, xT, st));
+  if (s == MOE_OK) {
+    GemmProblem g{};
+    g.A = dlT;
+    g.B = xT;
+    g.b_rows_total = D;
+    g.M = E;
+    g.N = D;
+    g.K = (int)r.Tpad;
+    g.num_groups = 0;
+    g.epilogue = EPI_F32;
+    g.bn = pick_bn_f32(D);
+    g.splits = r.dw_splits;
+    g.ldo = D;
+    g.status = status;
+    if (r.dw_splits > 1) {
+      const int64_t slice = ((int64_t)E * D + 3) / 4 * 4;
+      g.out = part;
+      g.split_stride = slice;
+      s = cuda_status(launch_gemm(g, st));
+      if (s == MOE_OK) s = cuda_status(launch_sum_slices_f32(part, r.dw_splits, slice, dw_router, st));
+    } else {
+      g.out = dw_router;
+      s = cuda_status(launch_gemm(g, st));
+    }
+  }
+  if (s == MOE_OK && c->router_bias && db_router) s = cuda_status(launch_column_sum(dlogits, (int)T, E, db_router, st));
+  return s;
 }
 
 int moe_combine_backward(const moe_config_t* c, const void* dz, const void* y, const int32_t* scatter_idx,

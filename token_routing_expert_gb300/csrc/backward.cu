@@ -20,64 +20,114 @@
 
 namespace moe {
 
-// out[e] = in[e]^T for in (E, A, B) -> out (E, B, A), bf16; A, B multiples of 32.
-__global__ void __launch_bounds__(256) transpose_experts_kernel(const uint16_t* __restrict__ in, int A, int B,
-                                                                 uint16_t* __restrict__ out) {
-  __shared__ uint16_t tile[32][33];
-  const long long e = blockIdx.z;
-  const int b0 = blockIdx.x * 32, a0 = blockIdx.y * 32;
-  const uint16_t* src = in + e * (long long)A * B;
-  uint16_t* dst = out + e * (long long)A * B;
-  for (int i = threadIdx.y; i < 32; i += 8) tile[i][threadIdx.x] = src[(long long)(a0 + i) * B + b0 + threadIdx.x];
+// ---------------------------------------------------------------------------
+// bf16 transposes: out[c][col] = in[src(col)][c] (zero where src(col) = -1).
+// A block moves a 64 (col) x 64 (c) tile: 16-byte coalesced loads of 64 source
+// rows into padded shared memory, an 8 x 8 register transpose per thread
+// (byte permutes), 16-byte coalesced stores of 64 output rows.
+// ---------------------------------------------------------------------------
+enum TransposeMode { TR_BATCHED = 0, TR_GROUPED = 1, TR_PADDED = 2 };
+
+struct TransposeArgs {
+  const uint16_t* in;
+  uint16_t* out;
+  long long ld_in;      // elements per input row
+  long long ld_out;     // elements per output row (a multiple of 64)
+  long long in_batch;   // batched: elements between input matrices
+  long long out_batch;  // batched: elements between output matrices
+  int A;                // batched / padded: source rows
+  const int32_t* off;   // grouped: row offsets of the experts (E+1)
+  const int32_t* k_off; // grouped: 64-column tile offsets of the experts (E+1)
+  int E;
+};
+
+template <int MODE>
+__global__ void __launch_bounds__(64) transpose_tile_kernel(const TransposeArgs a) {
+  __shared__ uint4 tile[64][9];   // 64 source rows x 8 x 16 B, padded against bank conflicts
+  __shared__ int s_src[64];
+  const int tid = threadIdx.x;
+  const long long col0 = (long long)blockIdx.x * 64;
+  const long long c0 = (long long)blockIdx.y * 64;
+  const uint16_t* in = a.in;
+  uint16_t* out = a.out;
+  if (MODE == TR_BATCHED) {
+    in += (long long)blockIdx.z * a.in_batch;
+    out += (long long)blockIdx.z * a.out_batch;
+  }
+  {
+    const long long col = col0 + tid;
+    int src;
+    if (MODE == TR_GROUPED) {
+      if (col0 >= 64ll * a.k_off[a.E]) return;   // whole block past the last expert
+      int lo = 0, hi = a.E - 1;                  // last expert e with 64 * k_off[e] <= col
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (64ll * a.k_off[mid] <= col) lo = mid; else hi = mid - 1;
+      }
+      const long long r = col - 64ll * a.k_off[lo];
+      src = r < (long long)(a.off[lo + 1] - a.off[lo]) ? a.off[lo] + (int)r : -1;
+    } else {
+      src = col < a.A ? (int)col : -1;
+    }
+    s_src[tid] = src;
+  }
   __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) dst[(long long)(b0 + i) * A + a0 + threadIdx.x] = tile[threadIdx.x][i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int lin = i * 64 + tid;
+    const int r = lin >> 3, q = lin & 7;
+    const int src = s_src[r];
+    tile[r][q] = src >= 0 ? *reinterpret_cast<const uint4*>(in + (long long)src * a.ld_in + c0 + 8 * q)
+                          : make_uint4(0u, 0u, 0u, 0u);
+  }
+  __syncthreads();
+  const int ib = tid & 7;    // block of 8 source rows = 8 output columns
+  const int jb = tid >> 3;   // block of 8 channels = 8 output rows
+  uint32_t w[8][4];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const uint4 v = tile[8 * ib + r][jb];
+    w[r][0] = v.x; w[r][1] = v.y; w[r][2] = v.z; w[r][3] = v.w;
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;   // high or low halves of two source words
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[q] = __byte_perm(w[2 * q][j >> 1], w[2 * q + 1][j >> 1], sel);
+    *reinterpret_cast<uint4*>(out + (c0 + 8 * jb + j) * a.ld_out + col0 + 8 * ib) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
+// out[e] = in[e]^T for in (E, A, B) -> out (E, B, A); A, B multiples of 64.
 cudaError_t launch_transpose_experts(const void* in, int E, int A, int B, void* out, cudaStream_t st) {
-  if ((A % 32) || (B % 32)) return cudaErrorInvalidValue;
-  dim3 grid(B / 32, A / 32, E), block(32, 8);
-  transpose_experts_kernel<<<grid, block, 0, st>>>(static_cast<const uint16_t*>(in), A, B,
-                                                   static_cast<uint16_t*>(out));
+  if ((A % 64) || (B % 64)) return cudaErrorInvalidValue;
+  TransposeArgs a{};
+  a.in = static_cast<const uint16_t*>(in);
+  a.out = static_cast<uint16_t*>(out);
+  a.ld_in = B;
+  a.ld_out = A;
+  a.in_batch = (long long)A * B;
+  a.out_batch = (long long)A * B;
+  a.A = A;
+  transpose_tile_kernel<TR_BATCHED><<<dim3(A / 64, B / 64, E), 64, 0, st>>>(a);
   return cudaGetLastError();
 }
 
 // XT[c][col] for col in [0, 64 * k_off[E]): expert e's columns start at 64 * k_off[e];
 // its r-th column is row off[e] + r of X (rows x C) while r < off[e+1] - off[e], zero after.
-__global__ void __launch_bounds__(256) group_transpose_kernel(const uint16_t* __restrict__ X, int C,
-                                                               const int32_t* __restrict__ off,
-                                                               const int32_t* __restrict__ k_off, int E,
-                                                               long long ld_out, uint16_t* __restrict__ XT) {
-  __shared__ uint16_t tile[32][33];
-  __shared__ int s_src[32];
-  const long long col0 = (long long)blockIdx.x * 32;
-  const int c0 = blockIdx.y * 32;
-  if (col0 >= 64ll * k_off[E]) return;
-  if (threadIdx.y == 0) {
-    const long long col = col0 + threadIdx.x;
-    // expert of this column: last e with 64 * k_off[e] <= col
-    int lo = 0, hi = E - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (64ll * k_off[mid] <= col) lo = mid; else hi = mid - 1;
-    }
-    const long long r = col - 64ll * k_off[lo];
-    s_src[threadIdx.x] = r < (long long)(off[lo + 1] - off[lo]) ? off[lo] + (int)r : -1;
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) {
-    const int src = s_src[i];
-    tile[i][threadIdx.x] = src >= 0 ? X[(long long)src * C + c0 + threadIdx.x] : (uint16_t)0;
-  }
-  __syncthreads();
-  for (int i = threadIdx.y; i < 32; i += 8) XT[(long long)(c0 + i) * ld_out + col0 + threadIdx.x] = tile[threadIdx.x][i];
-}
-
 cudaError_t launch_group_transpose(const void* X, int C, const int32_t* off, const int32_t* k_off, int E,
                                    long long max_cols, long long ld_out, void* XT, cudaStream_t st) {
-  if (C % 32) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)((max_cols + 31) / 32), C / 32), block(32, 8);
-  group_transpose_kernel<<<grid, block, 0, st>>>(static_cast<const uint16_t*>(X), C, off, k_off, E, ld_out,
-                                                 static_cast<uint16_t*>(XT));
+  if ((C % 64) || (ld_out % 64) || max_cols > ld_out) return cudaErrorInvalidValue;
+  TransposeArgs a{};
+  a.in = static_cast<const uint16_t*>(X);
+  a.out = static_cast<uint16_t*>(XT);
+  a.ld_in = C;
+  a.ld_out = ld_out;
+  a.off = off;
+  a.k_off = k_off;
+  a.E = E;
+  transpose_tile_kernel<TR_GROUPED><<<dim3((unsigned)((max_cols + 63) / 64), C / 64), 64, 0, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -187,5 +237,188 @@ cudaError_t launch_zero_padding_rows(const int32_t* gather_idx, int rows, int co
   zero_padding_rows_kernel<<<(rows + 7) / 8, 256, 0, st>>>(gather_idx, rows, cols / 8, static_cast<uint4*>(dst));
   return cudaGetLastError();
 }
+
+}  // namespace moe
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Router backward (for a fixed choice of experts; score_bias gets no gradient)
+// ---------------------------------------------------------------------------
+struct RouterBwdParams {
+  const float* logits;   // (T, E) with the router bias
+  const int32_t* idx;    // (T, k)
+  const float* dw;       // (T, k)
+  int T, E, k, gating;
+  float sig_eps, p_norm, scale;
+  float* dlogits;        // (T, E) fp32 out
+  uint16_t* dl_bf16;     // (T, Epad) bf16 out, zero padded
+  int Epad;
+};
+
+__device__ __forceinline__ float wsum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float wmax(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+template <int NI>
+__global__ void __launch_bounds__(256) router_backward_kernel(const RouterBwdParams p) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= p.T) return;
+  const int E = p.E, k = p.k;
+  const float* lrow = p.logits + (long long)t * E;
+  const bool mine = lane < k;
+  const int my_e = mine ? p.idx[(long long)t * k + lane] : 0;
+  const float my_lg = mine ? lrow[my_e] : 0.f;
+  // raw weight of the chosen expert (before normalisation and scaling)
+  float s_all[NI];
+  float w_raw = 0.f, sig = 0.f;
+  if (p.gating == MOE_GATING_SOFTMAX) {
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int e = lane + 32 * i;
+      s_all[i] = e < E ? lrow[e] : -INFINITY;
+      m = fmaxf(m, s_all[i]);
+    }
+    m = wmax(m);
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      s_all[i] = (lane + 32 * i < E) ? expf(s_all[i] - m) : 0.f;
+      sum += s_all[i];
+    }
+    sum = wsum(sum);
+#pragma unroll
+    for (int i = 0; i < NI; ++i) s_all[i] /= sum;
+    w_raw = mine ? expf(my_lg - m) / sum : 0.f;
+  } else if (p.gating == MOE_GATING_TOPK_SOFTMAX) {
+    const float m = wmax(mine ? my_lg : -INFINITY);
+    const float ex = mine ? expf(my_lg - m) : 0.f;
+    w_raw = ex / wsum(ex);
+  } else {
+    sig = 1.0f / (1.0f + expf(-my_lg));
+    w_raw = mine ? sig + p.sig_eps : 0.f;
+  }
+  // undo the scalings, then the p-norm
+  const float d_norm = mine ? p.dw[(long long)t * k + lane] * p.scale : 0.f;
+  float d_raw = d_norm;
+  if (p.p_norm > 0.f) {
+    const float pp = p.p_norm;
+    const float n = powf(wsum(mine ? powf(fabsf(w_raw), pp) : 0.f), 1.0f / pp);
+    const float dot = wsum(d_norm * w_raw);
+    const float dn_dw = mine ? copysignf(powf(fabsf(w_raw), pp - 1.f), w_raw) * powf(n, 1.f - pp) : 0.f;
+    d_raw = d_norm / n - dot / (n * n) * dn_dw;
+  }
+  // gradient with respect to the selected scores / logits
+  float d_sel = 0.f;
+  if (p.gating == MOE_GATING_TOPK_SOFTMAX) {
+    d_sel = w_raw * (d_raw - wsum(d_raw * w_raw));
+  } else if (p.gating == MOE_GATING_SIGMOID) {
+    d_sel = d_raw * sig * (1.f - sig);
+  } else {
+    d_sel = d_raw;   // gradient of the full softmax's score at the chosen expert
+  }
+  float dsoft_dot = 0.f;
+  float row[NI];
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int e = lane + 32 * i;
+    float v = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int ej = __shfl_sync(0xffffffffu, my_e, j);
+      const float dj = __shfl_sync(0xffffffffu, d_sel, j);
+      if (ej == e) v += dj;
+    }
+    row[i] = v;
+    if (p.gating == MOE_GATING_SOFTMAX && e < E) dsoft_dot += v * s_all[i];
+  }
+  if (p.gating == MOE_GATING_SOFTMAX) {
+    dsoft_dot = wsum(dsoft_dot);
+#pragma unroll
+    for (int i = 0; i < NI; ++i) row[i] = s_all[i] * (row[i] - dsoft_dot);
+  }
+  float* drow = p.dlogits + (long long)t * E;
+  uint16_t* brow = p.dl_bf16 + (long long)t * p.Epad;
+#pragma unroll
+  for (int i = 0; i < NI; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) drow[e] = row[i];
+  }
+  for (int e = lane; e < p.Epad; e += 32) {
+    float v = 0.f;
+#pragma unroll
+    for (int i = 0; i < NI; ++i)
+      if (lane + 32 * i == e) v = row[i];
+    __nv_bfloat16 b = __float2bfloat16_rn(e < E ? v : 0.f);
+    brow[e] = *reinterpret_cast<uint16_t*>(&b);
+  }
+}
+
+cudaError_t launch_router_backward(const float* logits, const int32_t* idx, const float* dw, int T, int E, int k,
+                                   int gating, float sig_eps, float p_norm, float scale, float* dlogits,
+                                   void* dl_bf16, int Epad, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  RouterBwdParams p{logits, idx, dw, T, E, k, gating, sig_eps, p_norm, scale, dlogits,
+                    static_cast<uint16_t*>(dl_bf16), Epad};
+  const dim3 grid((T + 7) / 8), block(256);
+  const int ni = (E + 31) / 32;
+  if (ni <= 1) router_backward_kernel<1><<<grid, block, 0, st>>>(p);
+  else if (ni <= 2) router_backward_kernel<2><<<grid, block, 0, st>>>(p);
+  else if (ni <= 4) router_backward_kernel<4><<<grid, block, 0, st>>>(p);
+  else if (ni <= 8) router_backward_kernel<8><<<grid, block, 0, st>>>(p);
+  else if (ni <= 16) router_backward_kernel<16><<<grid, block, 0, st>>>(p);
+  else if (ni <= 28) router_backward_kernel<28><<<grid, block, 0, st>>>(p);
+  else if (ni <= 32) router_backward_kernel<32><<<grid, block, 0, st>>>(p);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+// out (B x ld_out) = in (A x B, leading dimension ld_in)^T, columns A..ld_out-1 zero; bf16.
+// B and ld_out multiples of 64, ld_in a multiple of 8.
+cudaError_t launch_transpose_pad(const void* in, int A, int B, long long ld_in, long long ld_out, void* out,
+                                 cudaStream_t st) {
+  if ((B % 64) || (ld_out % 64) || (ld_in % 8) || ld_out < A) return cudaErrorInvalidValue;
+  TransposeArgs a{};
+  a.in = static_cast<const uint16_t*>(in);
+  a.out = static_cast<uint16_t*>(out);
+  a.ld_in = ld_in;
+  a.ld_out = ld_out;
+  a.A = A;
+  transpose_tile_kernel<TR_PADDED><<<dim3((unsigned)(ld_out / 64), B / 64), 64, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// db[e] = sum over t of d[t, e]: 32 columns per block, 8 row groups reduced in shared memory.
+__global__ void __launch_bounds__(256) column_sum_kernel(const float* __restrict__ d, int T, int E,
+                                                          float* __restrict__ out) {
+  __shared__ float part[8][33];
+  const int e = blockIdx.x * 32 + threadIdx.x;
+  float s = 0.f;
+  if (e < E)
+    for (int t = threadIdx.y; t < T; t += 8) s += d[(long long)t * E + e];
+  part[threadIdx.y][threadIdx.x] = s;
+  __syncthreads();
+  if (threadIdx.y == 0 && e < E) {
+    float tot = 0.f;
+    for (int i = 0; i < 8; ++i) tot += part[i][threadIdx.x];
+    out[e] = tot;
+  }
+}
+
+cudaError_t launch_column_sum(const float* d, int T, int E, float* out, cudaStream_t st) {
+  column_sum_kernel<<<(E + 31) / 32, dim3(32, 8), 0, st>>>(d, T, E, out);
+  return cudaGetLastError();
+}
+
+// out = sum over s of part[s] (fp32), slices of n4 float4.
+cudaError_t launch_sum_slices_f32(const float* part, int splits, long long n, float* out, cudaStream_t st);
 
 }  // namespace moe

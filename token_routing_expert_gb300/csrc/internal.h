@@ -81,6 +81,14 @@ cudaError_t launch_swiglu_backward(const void* UG, const void* dH, long long row
 cudaError_t launch_combine_backward(const void* dz, const void* y, const int32_t* scatter_idx, const float* w, int T,
                                     int k, int L, int rows, void* dy, float* dw, int* status, cudaStream_t st);
 cudaError_t launch_zero_padding_rows(const int32_t* gather_idx, int rows, int cols, void* dst, cudaStream_t st);
+cudaError_t launch_router_backward(const float* logits, const int32_t* idx, const float* dw, int T, int E, int k,
+                                   int gating, float sig_eps, float p_norm, float scale, float* dlogits,
+                                   void* dl_bf16, int Epad, cudaStream_t st);
+cudaError_t launch_transpose_pad(const void* in, int A, int B, long long ld_in, long long ld_out, void* out,
+                                 cudaStream_t st);
+cudaError_t launch_column_sum(const float* d, int T, int E, float* out, cudaStream_t st);
+// out = sum of `splits` fp32 slices of n floats (n a multiple of 4), in slice order.
+cudaError_t launch_sum_slices_f32(const float* part, int splits, long long n, float* out, cudaStream_t st);
 cudaError_t launch_splitk_reduce_bf16(const float* partials, int splits, int64_t slice, void* out,
                                       cudaStream_t stream);
 

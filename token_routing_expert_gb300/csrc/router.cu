@@ -269,6 +269,15 @@ __global__ void __launch_bounds__(256) sum_partials_kernel(const float4* __restr
   }
 }
 
+cudaError_t launch_sum_slices_f32(const float* part, int splits, long long n, float* out, cudaStream_t st) {
+  const long long n4 = n / 4;
+  if (n4 <= 0) return cudaSuccess;
+  const int blocks = (int)std::min<long long>((n4 + 255) / 256, 2048);
+  sum_partials_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(part), splits, n4,
+                                              reinterpret_cast<float4*>(out));
+  return cudaGetLastError();
+}
+
 cudaError_t launch_topk(const float* logits, int n_partials, int64_t partial_stride, const float* b_router,
                         const float* score_bias, int T, int E, int k, int gating, float sig_eps, float p_norm,
                         int restore, float ews, int orig_k, float* logits_out, int32_t* idx, float* w,

@@ -50,7 +50,8 @@ EXPORTS = ["moe_expert_capacity", "moe_permuted_rows", "moe_validate_config", "m
            "moe_latent_down", "moe_latent_restore", "moe_layer_forward", "moe_layer_forward_staged",
            "moe_layer_forward_launches", "moe_workspace_layout", "moe_get_status", "moe_status_string",
            "moe_permute_noalloc", "moe_accumulate_counts", "moe_load_imbalance", "moe_score_bias_update",
-           "moe_backward_workspace_size", "moe_combine_backward", "moe_grouped_swiglu_backward"]
+           "moe_backward_workspace_size", "moe_combine_backward", "moe_grouped_swiglu_backward",
+           "moe_router_backward"]
 
 _lib = None
 
@@ -88,6 +89,7 @@ def load() -> ctypes.CDLL:
         "moe_permute_noalloc": [cfgp, VP, I64, VP, VP, VP, VP, VP],
         "moe_accumulate_counts": [VP, ctypes.c_int32, VP, VP],
         "moe_backward_workspace_size": [cfgp, I64, P(SZ)],
+        "moe_router_backward": [cfgp, wp, VP, I64, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP],
         "moe_combine_backward": [cfgp, VP, VP, VP, VP, VP, I64, VP, VP, VP],
         "moe_grouped_swiglu_backward": [cfgp, wp, VP, VP, VP, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
         "moe_load_imbalance": [VP, ctypes.c_int32, ctypes.c_int32, VP, VP],
@@ -398,6 +400,24 @@ def moe_grouped_swiglu_backward(cfg, weights: DeviceWeights, x_routed, gather_id
         _ptr(dw_out, torch.float32, "dw_out"), _ptr(bws, None, "ws"), bws.numel(), _stream(stream)),
         "moe_grouped_swiglu_backward")
     return dx_routed, dw_up_gate, dw_out
+
+
+def moe_router_backward(cfg, weights: DeviceWeights, x, logits, idx, dweights, bws, stream=None):
+    """(dlogits (T,E) fp32, dx (T,D) bf16, dw_router (E,D) fp32, db_router (E,) fp32 or None)."""
+    T, D = x.shape
+    E = cfg.num_experts
+    dev = x.device
+    dlogits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    dx = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((E, D), dtype=torch.float32, device=dev)
+    db = torch.empty(E, dtype=torch.float32, device=dev) if cfg.router_bias else None
+    ws_ = weights.struct()
+    _check(load().moe_router_backward(
+        ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x, torch.bfloat16, "x"), T, _ptr(logits, torch.float32, "logits"),
+        _ptr(idx, torch.int32, "idx"), _ptr(dweights, torch.float32, "dweights"), _ptr(dlogits, torch.float32, "dlogits"),
+        _ptr(dx, torch.bfloat16, "dx"), _ptr(dw, torch.float32, "dw_router"), _ptr(db, torch.float32, "db_router"),
+        _ptr(bws, None, "ws"), bws.numel(), _stream(stream)), "moe_router_backward")
+    return dlogits, dx, dw, db
 
 
 def moe_accumulate_counts(counts, accum, stream=None):

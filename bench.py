@@ -67,6 +67,8 @@ def workload_desc(spec: W.WorkloadSpec) -> str:
         s += " skewed_load"
     if spec.capacity_factor:
         s += f" capacity_factor={spec.capacity_factor:g}"
+    if spec.expert_fp8:
+        s += " experts_e4m3_rowwise"
     return s
 
 
@@ -259,10 +261,14 @@ def run_native(args):
     spec = W.WORKLOADS[args.config]
     if args.capacity_factor > 0:
         spec = spec.with_(capacity_factor=args.capacity_factor)
+    if args.fp8:
+        spec = spec.with_(expert_fp8=True)
     # each rank draws its own batch of tokens (weak scaling); weights are shared replicas
     inp = rank_inputs(spec, rank)
     cfg = native.config_from_spec(spec)
     wts = native.DeviceWeights.from_inputs(inp)
+    if spec.expert_fp8:
+        wts.quantize_experts_fp8()   # pre-quantised expert weights, outside the timed region
     T = spec.T
     x = inp["x"].cuda()
     ws = native.workspace(cfg, T)
@@ -425,6 +431,10 @@ def run_native(args):
     peak_tf = peaks["bf16_tflops_sustained"] if sustained else peaks["bf16_tflops"]
     peak_label = (f"{peak_kind} bf16 {'sustained' if sustained else 'burst'} (MEASURED_PEAKS.json; timed region "
                   f"{region_s:.2f} s)") if peak_kind == "measured" else "fallback 1.9 PFLOP/s bf16"
+    gemm_peak, gemm_label = peak_tf, peak_label
+    if spec.expert_fp8:
+        # e4m3 tensor peak: the measured bf16 figure x the nominal e4m3 / bf16 ratio (4.5 / 2.25 PFLOP/s)
+        gemm_peak, gemm_label = 2.0 * peak_tf, peak_label + " x 2 (nominal e4m3 / bf16 ratio)"
     bound_layer = "hbm" if (alg_bytes / (peaks["hbm_gbs"] * 1e9)) > (flops / (peak_tf * 1e12)) else "tensor"
     roof_ms = 1e3 * max(alg_bytes / (peaks["hbm_gbs"] * 1e9), flops / (peak_tf * 1e12))
 
@@ -441,7 +451,7 @@ def run_native(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16 (experts e4m3 rowwise)" if spec.expert_fp8 else "bf16",
         "data": "synthetic (seeded numpy PCG64 normals rounded to bf16; random-init weights)",
         "config": dict(bench_config(spec, world),
                        l2=("flushed between steps (working set below 2x L2)" if flush else
@@ -454,10 +464,11 @@ def run_native(args):
         "stages_ms": stage_ms,
         "balance": bal,
         "backward": bwd,
-        "roofline": {"kernel": "grouped GEMM 1 (SwiGLU fused, tcgen05)", "bound": "tensor",
-                     "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s", "frac": achieved / peak_tf,
-                     "traffic": kernel_traffic(spec.name),
-                     "peak_source": peak_label},
+        "roofline": {"kernel": "grouped GEMM 1 (SwiGLU fused, tcgen05" + (", e4m3 operands)" if spec.expert_fp8 else ")"),
+                     "bound": "tensor", "achieved": achieved, "peak": gemm_peak, "unit": "TFLOP/s",
+                     "frac": achieved / gemm_peak,
+                     "traffic": None if spec.expert_fp8 or spec.capacity_factor else kernel_traffic(spec.name),
+                     "peak_source": gemm_label},
         "e2e": {"value": job_tokens_per_s(world, T, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_host.numel() * 2},
         "gpu_launches": args.steps * native.moe_layer_forward_launches(cfg, T),
@@ -488,6 +499,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--backward", action="store_true", help="also time the combine + experts backward")
+    ap.add_argument("--fp8", action="store_true", help="experts on rowwise e4m3 operands")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

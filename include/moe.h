@@ -79,6 +79,8 @@ typedef struct {
   int32_t activation;              /* 0 = swiglu (the only expert activation supported) */
   float capacity_factor;           /* > 0: capacity-limited experts (section "Ёмкость эксперта и
                                       переполнение"); 0 = dropless */
+  int32_t expert_fp8;              /* 1: the experts' GEMMs run on rowwise e4m3 operands (section
+                                      "Rowwise FP8 и MXFP8"; needs the *_fp8 weights below); 0 = bf16 */
 } moe_config_t;
 
 /*
@@ -93,6 +95,11 @@ typedef struct {
   const void* rms_weight;    /* (L) bf16 gain, or NULL for ones; latent with up_proj_norm only */
   const void* w_up_gate;     /* (E, 2h, L'): per expert rows [0,h) = up, rows [h,2h) = gate; L' = L or D */
   const void* w_out;         /* (E, L', h): expert down-projection */
+  /* expert_fp8 only: the expert weights quantised row by row with moe_quantize_rowwise_fp8 */
+  const void* w_up_gate_fp8;    /* (E, 2h, L') e4m3 codes */
+  const float* w_up_gate_scale; /* (E * 2h) fp32 row scales */
+  const void* w_out_fp8;        /* (E, L', h) e4m3 codes */
+  const float* w_out_scale;     /* (E * L') fp32 row scales */
 } moe_weights_t;
 
 /* ---- host-only functions (no device, no stream) ------------------------- */
@@ -121,6 +128,14 @@ int moe_expert_capacity(const moe_config_t* cfg, int64_t T, int64_t* capacity);
 
 /* Rows of the permuted order: T * top_k (dropless) or num_experts * capacity. */
 int moe_permuted_rows(const moe_config_t* cfg, int64_t T, int64_t* rows);
+
+/* Rowwise e4m3 quantisation, section "Rowwise FP8 и MXFP8": for each row of x
+ * (rows, cols) bf16, scales[r] = amax / 448 in fp32 (1 for a zero row) and
+ * codes[r, c] = e4m3(x[r, c] / scales[r]) (fp32 division, nearest-even,
+ * saturating at 448).  cols a multiple of 16.  codes device (rows, cols) bytes;
+ * scales device (rows) fp32.  Device call on `stream`. */
+int moe_quantize_rowwise_fp8(const void* x, int64_t rows, int32_t cols, void* codes, float* scales,
+                             moe_stream_t stream);
 
 /* Workspace bytes that every entry point below needs for T tokens. */
 int moe_workspace_size(const moe_config_t* cfg, int64_t T, size_t* bytes);

@@ -614,3 +614,95 @@ def router_backward(cfg: OracleConfig, x: np.ndarray, w_router: np.ndarray, b_ro
         np.add.at(dlogits, (np.broadcast_to(rows, idx.shape), idx), d_raw * sig * (1.0 - sig))
     w_router = np.asarray(w_router, np.float64)
     return dlogits, dlogits @ w_router, dlogits.T @ x, dlogits.sum(axis=0)
+
+
+# --------------------------------------------------------------------------
+# Rowwise FP8 experts  [Olmo-core 3, §"Rowwise FP8 и MXFP8": pre-quantised
+# expert weights, quantised activations, the experts run on FP8 operands]
+# Reading: one float32 scale per row (amax / 448, the largest e4m3 value), the
+# row divided by it in float32 and rounded to e4m3 (nearest, ties to even,
+# saturating at 448); the GEMMs accumulate exactly and apply both rows' scales.
+# --------------------------------------------------------------------------
+
+def _e4m3_positive_values() -> np.ndarray:
+    """The non-negative finite e4m3 values in code order 0x00..0x7E (increasing)."""
+    vals = []
+    for code in range(0x7F):
+        e, m = (code >> 3) & 0xF, code & 7
+        vals.append(m / 8.0 * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    return np.array(vals, np.float64)
+
+
+_E4M3 = _e4m3_positive_values()
+
+
+def round_e4m3(v: np.ndarray) -> np.ndarray:
+    """Nearest e4m3 value, ties to the even code, magnitudes above 448 saturate to 448."""
+    v = np.asarray(v, np.float64)
+    a = np.minimum(np.abs(v), 448.0)
+    hi = np.clip(np.searchsorted(_E4M3, a, side="left"), 1, len(_E4M3) - 1)
+    lo = hi - 1
+    dlo, dhi = a - _E4M3[lo], _E4M3[hi] - a
+    pick_hi = (dhi < dlo) | ((dhi == dlo) & (hi % 2 == 0))
+    out = np.where(pick_hi, _E4M3[hi], _E4M3[lo])
+    out = np.where(a == _E4M3[hi], _E4M3[hi], out)
+    return np.sign(v) * out
+
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """Round to bfloat16 (nearest, ties to even) via float32."""
+    f = np.asarray(v, np.float32)
+    bits = f.view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x7FFF + ((bits >> 16) & 1)) & 0xFFFF0000
+    return bits.astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def quantize_rowwise_e4m3(x: np.ndarray):
+    """(codes as float64 values, float32 scales): scale = amax / 448 in float32 (1 for a zero row),
+    code = e4m3(x / scale) with the division in float32."""
+    x32 = np.asarray(x, np.float32)
+    amax = np.abs(x32).max(axis=1) if x32.size else np.zeros(x32.shape[0], np.float32)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    y = (x32 / scale[:, None]).astype(np.float32)
+    return round_e4m3(y), scale
+
+
+def quantize_expert_fp8(w_up: np.ndarray, w_gate: np.ndarray, w_out: np.ndarray):
+    """Rowwise-quantised expert weights, returned dequantised (code * scale) in float64."""
+    out = []
+    for w in (w_up, w_gate, w_out):
+        q, s = quantize_rowwise_e4m3(w)
+        out.append(q * s.astype(np.float64)[:, None])
+    return tuple(out)
+
+
+def expert_outputs_fp8(cfg: OracleConfig, x_routed: np.ndarray, perm: Permutation, expert: ExpertFn) -> np.ndarray:
+    """Experts on rowwise FP8 operands: x rows and weight rows quantised, H rounded to bf16
+    and quantised again before the down projection."""
+    xq, xs = quantize_rowwise_e4m3(np.asarray(x_routed, np.float64))
+    xd = xq * xs.astype(np.float64)[:, None]
+    y = np.zeros((perm.gather_token.size, x_routed.shape[1]), np.float64)
+    for e in range(cfg.num_experts):
+        lo, hi = int(perm.offsets[e]), int(perm.offsets[e + 1])
+        if hi == lo:
+            continue
+        wu, wg, wo = quantize_expert_fp8(*(np.asarray(a, np.float64) for a in expert(e)))
+        rows = xd[perm.gather_token[lo:hi]]
+        h = round_bf16(silu(rows @ wg.T) * (rows @ wu.T))
+        hq, hs = quantize_rowwise_e4m3(h)
+        y[lo:hi] = (hq * hs.astype(np.float64)[:, None]) @ wo.T
+    return y
+
+
+def layer_forward_fp8(cfg: OracleConfig, x: np.ndarray, wts: OracleWeights,
+                      forced_idx: Optional[np.ndarray] = None) -> np.ndarray:
+    """The layer forward with the experts on rowwise FP8 operands (bf16 x_routed as input)."""
+    x = np.asarray(x, np.float64)
+    x_routed = prepare_routed_input(cfg, x, wts.w_down_latent)
+    if cfg.is_latent:
+        x_routed = round_bf16(x_routed)   # the experts' input is stored in bf16
+    r = route(cfg, x, wts.w_router, wts.b_router, wts.score_bias, forced_idx)
+    perm = permute(r.idx, cfg.num_experts)
+    y = expert_outputs_fp8(cfg, x_routed, perm, wts.expert)
+    z = combine(y, perm.scatter_pos, r.weights)
+    return restore_routed_output(cfg, z, wts.w_up_latent, wts.rms_weight)

@@ -1,0 +1,60 @@
+"""GPU parity of the rowwise FP8 experts (page "Как устроен Olmo-core 3: обучение больших
+MoE-моделей", §"Rowwise FP8 и MXFP8") against the float64 oracle's FP8 path: the
+quantiser's codes and scales bit-exact, the layer within the layer bar."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_ref as ref
+from tests.oracle_bridge import assert_close_layer, check_topk, f64, oracle_config, oracle_weights, output_scale
+from token_routing_expert_gb300 import native
+from token_routing_expert_gb300.workloads import WorkloadSpec, generate
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("rows,cols,scale", [(1000, 256, 1.0), (77, 2048, 30.0), (5, 64, 1e-3)])
+def test_quantizer_bit_exact(rows, cols, scale):
+    g = np.random.default_rng(rows + cols)
+    x = torch.from_numpy((g.standard_normal((rows, cols)) * scale).astype(np.float32)).to(torch.bfloat16)
+    x[min(3, rows - 1)] = 0.0
+    codes, scales = native.moe_quantize_rowwise_fp8(x.cuda())
+    assert native.moe_get_status() == 0
+    want_q, want_s = ref.quantize_rowwise_e4m3(f64(x))
+    np.testing.assert_array_equal(scales.cpu().numpy(), want_s)
+    got_q = codes.cpu().view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(got_q, want_q)
+
+
+CASES = {
+    "olmoe_like_small": WorkloadSpec("olmoe_like_small", T=600, d_model=512, num_experts=8, top_k=2, hidden_size=256,
+                                     gating="topk_softmax", expert_fp8=True, seed=71),
+    "pair_tiles_fp8": WorkloadSpec("pair_tiles_fp8", T=2000, d_model=512, num_experts=4, top_k=2, hidden_size=320,
+                                   gating="sigmoid", normalize_expert_weights=1.0, expert_fp8=True, seed=72),
+    "latent_fp8": WorkloadSpec("latent_fp8", T=400, d_model=768, num_experts=16, top_k=4, hidden_size=192,
+                               latent_dim=256, gating="sigmoid", skew=True, expert_fp8=True, seed=73),
+}
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_fp8_layer_forward(name):
+    spec = CASES[name]
+    inp = generate(spec)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp).quantize_experts_fp8()
+    ws = native.workspace(cfg, spec.T)
+    out = native.moe_layer_forward(cfg, wts, inp["x"].cuda(), ws)
+    assert native.moe_get_status() == 0
+    inter = native.layer_intermediates(cfg, spec.T, ws)
+    oc, ow = oracle_config(spec), oracle_weights(spec, inp)
+    r = ref.route(oc, f64(inp["x"]), ow.w_router, ow.b_router, ow.score_bias)
+    gi = inter["idx"].cpu().numpy().astype(np.int64)
+    mism = check_topk(gi, r.keys, r.idx, spec.top_k)
+    forced = r.idx.copy()
+    forced[mism] = gi[mism]
+    want = ref.layer_forward_fp8(oc, f64(inp["x"]), ow, forced_idx=forced)
+    got = out.double().cpu().numpy()
+    assert_close_layer(got, want, "fp8 layer output", output_scale(spec))
+    # and the FP8 layer stays close to the bf16 one (e4m3 keeps 3 mantissa bits)
+    dense = ref.layer_forward(oc, f64(inp["x"]), ow, forced_idx=forced).out
+    assert np.linalg.norm(got - dense) / np.linalg.norm(dense) < 0.1

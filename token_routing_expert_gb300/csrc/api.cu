@@ -47,6 +47,7 @@ struct Plan {
   int64_t cap;        // slots per expert (capacity mode)
   int64_t rows;       // rows of the permuted order: R, or E * cap
   size_t gdense, sdense, odense;   // capacity mode: the dense stable permutation before slotting
+  size_t xq, xs, xpq, xps, hq, hs;  // rowwise e4m3 experts: codes and scales of x_routed, its rows, H
   int D, E, k, h, L, Lr;   // Lr: routed dim (L or D)
   bool latent;
   int router_bn, n_router_tiles;
@@ -114,6 +115,16 @@ void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->H = take((size_t)p->rows * p->h * 2);
   p->Y = take((size_t)p->rows * p->Lr * 2);
   p->zn = p->latent ? take((size_t)T * p->L * 2) : (size_t)-1;
+  if (c->expert_fp8) {
+    p->xq = take((size_t)T * p->Lr);
+    p->xs = take((size_t)T * 4);
+    p->xpq = take((size_t)p->rows * p->Lr);
+    p->xps = take((size_t)p->rows * 4);
+    p->hq = take((size_t)p->rows * p->h);
+    p->hs = take((size_t)p->rows * 4);
+  } else {
+    p->xq = p->xs = p->xpq = p->xps = p->hq = p->hs = (size_t)-1;
+  }
   size_t part = 0;
   if (p->down_splits > 1) part = std::max(part, (size_t)p->down_splits * T * p->L * 4);
   if (p->up_splits > 1) part = std::max(part, (size_t)p->up_splits * T * p->D * 4);
@@ -134,6 +145,7 @@ int check_config(const moe_config_t* c) {
   if (c->activation != 0) return MOE_ERR_UNSUPPORTED;
   if (c->d_model % 64 || c->hidden_size % 64 || (c->latent_dim > 0 && c->latent_dim % 64)) return MOE_ERR_UNSUPPORTED;
   if (c->num_experts > 1024 || c->top_k > 32) return MOE_ERR_UNSUPPORTED;
+  if (c->expert_fp8 != 0 && c->expert_fp8 != 1) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -227,12 +239,87 @@ int run_router(const moe_config_t* c, const moe_weights_t* w, const void* x, con
                                  wts, status, st));
 }
 
+// The experts on rowwise e4m3 operands: quantise x_routed per token, gather code rows and
+// scales, GEMM 1 (SwiGLU, scales in the epilogue) -> H bf16, quantise H per row, GEMM 2.
+int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
+                    const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
+                    cudaEvent_t* ev) {
+  int32_t* tile_off = at<int32_t>(ws, p.tile_off);
+  void* H = at<void>(ws, p.H);
+  void* xq = at<void>(ws, p.xq);
+  float* xs = at<float>(ws, p.xs);
+  void* xpq = at<void>(ws, p.xpq);
+  float* xps = at<float>(ws, p.xps);
+  void* hq = at<void>(ws, p.hq);
+  float* hs = at<float>(ws, p.hs);
+  const int pair = use_pair_tiles(p);
+  int s = cuda_status(launch_tile_table(offsets, p.E, pair ? 256 : 128, tile_off, st));
+  if (s == MOE_OK) s = cuda_status(launch_quantize_rowwise_e4m3(xr, p.T, p.Lr, xq, xs, st));
+  if (s == MOE_OK)
+    s = cuda_status(launch_gather_rows_e4m3(xq, xs, gather, (int)p.rows, (int)p.T, p.Lr, xpq, xps, p.capacity ? 1 : 0,
+                                            status, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 5, st);
+  GemmProblem g1{};
+  g1.A = xpq;
+  g1.B = w->w_up_gate_fp8;
+  g1.b_rows_total = (int64_t)p.E * 2 * p.h;
+  g1.M = (int)p.rows;
+  g1.N = p.h;
+  g1.K = p.Lr;
+  g1.num_groups = p.E;
+  g1.group_off = offsets;
+  g1.tile_off = tile_off;
+  g1.b_rows_per_group = 2 * p.h;
+  g1.b_gate_offset = p.h;
+  g1.epilogue = EPI_SWIGLU;
+  g1.bn = 256;
+  g1.splits = 1;
+  g1.pair_tiles = pair;
+  g1.e4m3 = 1;
+  g1.a_scale = xps;
+  g1.b_scale = w->w_up_gate_scale;
+  g1.out = H;
+  g1.ldo = p.h;
+  g1.status = status;
+  s = cuda_status(launch_gemm(g1, st));
+  if (s == MOE_OK) s = cuda_status(launch_quantize_rowwise_e4m3(H, p.rows, p.h, hq, hs, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 6, st);
+  GemmProblem g2{};
+  g2.A = hq;
+  g2.B = w->w_out_fp8;
+  g2.b_rows_total = (int64_t)p.E * p.Lr;
+  g2.M = (int)p.rows;
+  g2.N = p.Lr;
+  g2.K = p.h;
+  g2.num_groups = p.E;
+  g2.group_off = offsets;
+  g2.tile_off = tile_off;
+  g2.b_rows_per_group = p.Lr;
+  g2.epilogue = EPI_BF16;
+  g2.bn = 256;
+  g2.splits = 1;
+  g2.pair_tiles = pair;
+  g2.e4m3 = 1;
+  g2.a_scale = hs;
+  g2.b_scale = w->w_out_scale;
+  g2.out = y;
+  g2.ldo = p.Lr;
+  g2.status = status;
+  s = cuda_status(launch_gemm(g2, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 7, st);
+  return MOE_OK;
+}
+
 int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
                 const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
                 cudaEvent_t* ev = nullptr) {
   int32_t* tile_off = at<int32_t>(ws, p.tile_off);
   void* xp = at<void>(ws, p.xp);
   void* H = at<void>(ws, p.H);
+  if (c->expert_fp8) return run_experts_fp8(c, w, xr, gather, offsets, p, y, ws, status, st, ev);
   // large groups run on CTA pairs with 256-row tiles; small ones keep 128-row tiles,
   // which waste less of the last partial tile of each group
   const int pair = use_pair_tiles(p);
@@ -547,6 +634,8 @@ int moe_grouped_swiglu(const moe_config_t* c, const moe_weights_t* w, const void
   if (s != MOE_OK) return s;
   if (T == 0) return MOE_OK;
   if (!w || !w->w_up_gate || !w->w_out || !x_routed || !gather_idx || !offsets || !y) return MOE_ERR_INVALID_ARG;
+  if (c->expert_fp8 && (!w->w_up_gate_fp8 || !w->w_up_gate_scale || !w->w_out_fp8 || !w->w_out_scale))
+    return MOE_ERR_INVALID_ARG;
   int* status = status_ptr();
   if (!status) return MOE_ERR_NO_DEVICE;
   return run_experts(c, w, x_routed, gather_idx, offsets, p, y, ws, status, (cudaStream_t)stream);
@@ -606,6 +695,8 @@ int moe_layer_forward_staged(const moe_config_t* c, const moe_weights_t* w, cons
   if (!w || !x || !out || !w->w_router || !w->w_up_gate || !w->w_out) return MOE_ERR_INVALID_ARG;
   if (p.latent && (!w->w_down_latent || !w->w_up_latent)) return MOE_ERR_INVALID_ARG;
   if ((c->router_bias && !w->b_router) || (c->has_score_bias && !w->score_bias)) return MOE_ERR_INVALID_ARG;
+  if (c->expert_fp8 && (!w->w_up_gate_fp8 || !w->w_up_gate_scale || !w->w_out_fp8 || !w->w_out_scale))
+    return MOE_ERR_INVALID_ARG;
   if (x == out) return MOE_ERR_INVALID_ARG;
   int* status = status_ptr();
   if (!status) return MOE_ERR_NO_DEVICE;
@@ -674,6 +765,7 @@ int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
   k += p.capacity ? 4 : 3;                       // permute: count, scan, place (, capacity slots)
   k += 2;                                        // tile table, row gather
   k += 2;                                        // grouped GEMM 1 (SwiGLU), grouped GEMM 2
+  if (c->expert_fp8) k += 2;                     // e4m3 quantisation of x_routed and of H
   k += 1;                                        // combine (+ RMSNorm when latent)
   if (p.latent) k += p.up_splits > 1 ? 2 : 1;    // latent up (+ split-K reduce)
   *n = k;

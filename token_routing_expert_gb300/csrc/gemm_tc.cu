@@ -41,6 +41,8 @@ struct GemmParams {
   long long split_stride;
   int k_groups;            // > 0: K-grouped (group g contracts k-tiles [k_off[g], k_off[g+1]))
   const int* k_off;        // device (k_groups+1) k-tile offsets
+  const float* a_scale;    // e4m3 operands: scale of each A row
+  const float* b_scale;    // e4m3 operands: scale of each B row
   int* status;
 };
 
@@ -118,11 +120,15 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
 
 // Epilogue of one tile for the 32 rows a warp owns: TMEM -> registers -> global.
 // row_in_tile: this thread's row of the 128-row accumulator; rows: valid rows from row0.
-template <int BN, int EPI>
+// e4m3 operands: the accumulator is scaled by the A row's scale and each column's B-row
+// scale; cs / cs_gate point at the B-row scales of this tile's first column.
+template <int BN, int EPI, bool F8 = false>
 __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, int row_in_tile, int nt, int split,
-                                           const GemmParams& p, bool zero = false) {
+                                           const GemmParams& p, bool zero = false, const float* cs = nullptr,
+                                           const float* cs_gate = nullptr) {
   const bool row_ok = row_in_tile < rows;
   const long long row = (long long)row0 + row_in_tile;
+  const float rs = (F8 && row_ok) ? p.a_scale[row] : 1.0f;
   if (EPI == EPI_SWIGLU) {
     constexpr int HALF = BN / 2;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
@@ -135,6 +141,13 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
       tmem_ld_wait();
       const int col0 = nt * HALF + cc * 32;
       if (row_ok && col0 < p.N) {
+        if (F8) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            u[i] = __float_as_uint(__uint_as_float(u[i]) * rs * __ldg(cs + cc * 32 + i));
+            g[i] = __float_as_uint(__uint_as_float(g[i]) * rs * __ldg(cs_gate + cc * 32 + i));
+          }
+        }
         uint32_t packed[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -164,6 +177,10 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
       }
       const int col0 = nt * BN + cc * 32;
       if (!row_ok || col0 >= p.N) continue;
+      if (F8) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * rs * __ldg(cs + cc * 32 + i));
+      }
       if (EPI == EPI_F32) {
         float* out = reinterpret_cast<float*>(p.out) + (long long)split * p.split_stride + row * p.ldo + col0;
         if (col0 + 32 <= p.N && (p.ldo & 3) == 0) {
@@ -191,7 +208,7 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
   }
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool F8 = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
@@ -259,12 +276,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
           uint8_t* sb = sa + C::A_BYTES;
           mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
-          tma_load_2d(sa, &tmA, &full_bar[stage], kt * BK, c.row0);
+          const int kx = kt * (F8 ? 2 * BK : BK);   // 128 bytes of K per k-tile: 64 bf16 or 128 e4m3
+          tma_load_2d(sa, &tmA, &full_bar[stage], kx, c.row0);
           if (EPI == EPI_SWIGLU) {
-            tma_load_2d(sb, &tmB, &full_bar[stage], kt * BK, brow);
-            tma_load_2d(sb + C::B_BYTES / 2, &tmB, &full_bar[stage], kt * BK, brow + p.b_gate_offset);
+            tma_load_2d(sb, &tmB, &full_bar[stage], kx, brow);
+            tma_load_2d(sb + C::B_BYTES / 2, &tmB, &full_bar[stage], kx, brow + p.b_gate_offset);
           } else {
-            tma_load_2d(sb, &tmB, &full_bar[stage], kt * BK, brow);
+            tma_load_2d(sb, &tmB, &full_bar[stage], kx, brow);
           }
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -274,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- UMMA issuer ----------------
-      constexpr uint32_t idesc = umma_idesc_bf16_f32(BM, BN);
+      constexpr uint32_t idesc = F8 ? umma_idesc_e4m3_f32(BM, BN) : umma_idesc_bf16_f32(BM, BN);
       uint32_t stage = 0, phase = 0;
       int it = 0;
       for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
@@ -293,8 +311,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t b_desc = umma_sdesc_sw128(sa + C::A_BYTES);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            // advancing K by 16 bf16 = 32 bytes inside the swizzled row: +2 in 16-byte units
-            umma_bf16(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+            // one MMA takes 32 bytes of K (16 bf16 or 32 e4m3): +2 in 16-byte units inside the swizzled row
+            if (F8)
+              umma_e4m3(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+            else
+              umma_bf16(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -318,7 +339,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
-      store_tile<BN, EPI>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p, c.kt1 <= c.kt0);
+      const float* cs = nullptr;
+      const float* cs_gate = nullptr;
+      if (F8) {
+        const int brow = c.group * p.b_rows_per_group + c.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
+        cs = p.b_scale + brow;
+        cs_gate = cs + p.b_gate_offset;
+      }
+      store_tile<BN, EPI, F8>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p, c.kt1 <= c.kt0, cs, cs_gate);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
@@ -363,7 +391,7 @@ struct PairCfg {
   static constexpr int SMEM_BYTES = TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 1024;
 };
 
-template <int EPI>
+template <int EPI, bool F8 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmParams p) {
@@ -432,8 +460,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
           const uint32_t full0 = map_to_cta(smem_u32(&full_bar[stage]), 0);
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE_BYTES);
-          tma_load_2d_pair(sa, &tmA, full0, kt * BK, arow);
-          tma_load_2d_pair(sa + C::A_BYTES, &tmB, full0, kt * BK, brow);
+          const int kx = kt * (F8 ? 2 * BK : BK);
+          tma_load_2d_pair(sa, &tmA, full0, kx, arow);
+          tma_load_2d_pair(sa + C::A_BYTES, &tmB, full0, kx, brow);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -441,7 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- UMMA issuer (CTA 0) ----------------
-      constexpr uint32_t idesc = umma_idesc_bf16_f32(BM2, C::BN);
+      constexpr uint32_t idesc = F8 ? umma_idesc_e4m3_f32(BM2, C::BN) : umma_idesc_bf16_f32(BM2, C::BN);
       uint32_t stage = 0, phase = 0;
       int it = 0;
       for (int t = pair; t < total_tiles; t += npairs, ++it) {
@@ -459,8 +488,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t a_desc = umma_sdesc_sw128(sa);
           const uint64_t b_desc = umma_sdesc_sw128(sa + C::A_BYTES);
 #pragma unroll
-          for (int kk = 0; kk < BK / UMMA_K; ++kk)
-            umma_bf16_pair(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+            if (F8)
+              umma_e4m3_pair(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+            else
+              umma_bf16_pair(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+          }
           umma_commit_pair(&empty_bar[stage], 0x3);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -483,7 +516,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * C::ACC_STRIDE);
-      store_tile<C::BN, EPI>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt, 0, p);
+      const float* cs = nullptr;
+      const float* cs_gate = nullptr;
+      if (F8) {
+        const int brow = c.group * p.b_rows_per_group + c.nt * (EPI == EPI_SWIGLU ? C::BN / 2 : C::BN);
+        cs = p.b_scale + brow;
+        cs_gate = cs + p.b_gate_offset;
+      }
+      store_tile<C::BN, EPI, F8>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt, 0, p,
+                                 false, cs, cs_gate);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&tempty_bar[acc]), 0));
@@ -522,17 +563,18 @@ static PFN_tmapEncodeTiled get_encoder() {
   return fn;
 }
 
-// bf16 (rows, cols) row-major matrix, box of box_rows x 64 columns, 128-byte swizzle.
-static bool make_tmap_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows) {
+// (rows, cols) row-major matrix of bf16 (or e4m3 bytes), box of box_rows x 128 bytes, 128-byte swizzle.
+static bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows, bool e4m3) {
   PFN_tmapEncodeTiled enc = get_encoder();
   if (!enc) return false;
+  const int esize = e4m3 ? 1 : 2;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
-  cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * esize)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / esize), (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, e4m3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -564,11 +606,11 @@ int pick_splits(int tiles, int K) {
   return (kt + per - 1) / per;           // no empty split
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, bool F8 = false>
 static cudaError_t launch_impl(const GemmProblem& q, const CUtensorMap& ta, const CUtensorMap& tb,
                                const GemmParams& gp, int grid, cudaStream_t stream) {
   using C = GemmCfg<BN>;
-  auto kern = gemm_tc_kernel<BN, EPI>;
+  auto kern = gemm_tc_kernel<BN, EPI, F8>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -580,10 +622,10 @@ static cudaError_t launch_impl(const GemmProblem& q, const CUtensorMap& ta, cons
   return cudaGetLastError();
 }
 
-template <int EPI>
+template <int EPI, bool F8 = false>
 static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp, int tiles,
                                     cudaStream_t stream) {
-  auto kern = gemm_tc_pair_kernel<EPI>;
+  auto kern = gemm_tc_pair_kernel<EPI, F8>;
   static bool attr_set = false;
   static int max_pairs = 0;
   if (!attr_set) {
@@ -617,11 +659,14 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   if (q.k_groups > 0 && (q.num_groups > 0 || q.pair_tiles || q.splits > 1 || q.epilogue != EPI_F32))
     return cudaErrorInvalidValue;
   const bool pair = q.pair_tiles != 0;
+  const bool f8 = q.e4m3 != 0;
   if (pair && (q.bn != 256 || q.splits > 1 || q.epilogue == EPI_F32)) return cudaErrorInvalidValue;
+  if (f8 && (q.bn != 256 || q.splits > 1 || q.k_groups > 0 || q.epilogue == EPI_F32 || !q.a_scale || !q.b_scale))
+    return cudaErrorInvalidValue;
   const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
   CUtensorMap ta, tb;
-  if (!make_tmap_bf16(&ta, q.A, q.M, q.K, BM)) return cudaErrorInvalidValue;
-  if (!make_tmap_bf16(&tb, q.B, q.b_rows_total, q.K, b_box)) return cudaErrorInvalidValue;
+  if (!make_tmap(&ta, q.A, q.M, q.K, BM, f8)) return cudaErrorInvalidValue;
+  if (!make_tmap(&tb, q.B, q.b_rows_total, q.K, b_box, f8)) return cudaErrorInvalidValue;
 
   GemmParams gp;
   gp.M = q.M;
@@ -634,7 +679,8 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.b_gate_offset = q.b_gate_offset;
   const int out_cols_per_tile = q.epilogue == EPI_SWIGLU ? q.bn / 2 : q.bn;
   gp.n_tiles = (q.N + out_cols_per_tile - 1) / out_cols_per_tile;
-  gp.kt_total = (q.K + BK - 1) / BK;
+  const int k_per_tile = f8 ? 2 * BK : BK;   // elements of K per 128-byte k-tile
+  gp.kt_total = (q.K + k_per_tile - 1) / k_per_tile;
   gp.splits = std::max(1, q.splits);
   gp.kt_per_split = (gp.kt_total + gp.splits - 1) / gp.splits;
   gp.out = q.out;
@@ -642,10 +688,16 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.split_stride = q.split_stride;
   gp.k_groups = q.k_groups;
   gp.k_off = q.k_off;
+  gp.a_scale = q.a_scale;
+  gp.b_scale = q.b_scale;
   gp.status = q.status;
 
   if (pair) {
     const int tiles = q.num_groups == 0 ? ((q.M + BM2 - 1) / BM2) * gp.n_tiles : 0;
+    if (f8) {
+      if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU, true>(ta, tb, gp, tiles, stream);
+      return launch_pair_impl<EPI_BF16, true>(ta, tb, gp, tiles, stream);
+    }
     if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU>(ta, tb, gp, tiles, stream);
     return launch_pair_impl<EPI_BF16>(ta, tb, gp, tiles, stream);
   }
@@ -655,6 +707,10 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
     grid = std::min(grid, std::max(1, tiles));
   }
 
+  if (f8) {
+    if (q.epilogue == EPI_SWIGLU) return launch_impl<256, EPI_SWIGLU, true>(q, ta, tb, gp, grid, stream);
+    return launch_impl<256, EPI_BF16, true>(q, ta, tb, gp, grid, stream);
+  }
   switch (q.epilogue) {
     case EPI_SWIGLU:
       if (q.bn == 256) return launch_impl<256, EPI_SWIGLU>(q, ta, tb, gp, grid, stream);

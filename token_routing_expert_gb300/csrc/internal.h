@@ -33,6 +33,9 @@ struct GemmProblem {
   int k_groups;           // > 0: K-grouped GEMM (fp32 out only): group g multiplies A[:, K_g] by B[:, K_g]^T
                           //      and writes slice g (split_stride apart); K_g = k-tiles [k_off[g], k_off[g+1])
   const int* k_off;       // device (k_groups+1) offsets in 64-column k-tiles
+  int e4m3;               // 1: A and B are e4m3 bytes (kind::f8f6f4) with per-row scales below
+  const float* a_scale;   // (M) scale of each A row
+  const float* b_scale;   // (b_rows_total) scale of each B row
   int* status;
 };
 
@@ -89,6 +92,11 @@ cudaError_t launch_transpose_pad(const void* in, int A, int B, long long ld_in, 
 cudaError_t launch_column_sum(const float* d, int T, int E, float* out, cudaStream_t st);
 // out = sum of `splits` fp32 slices of n floats (n a multiple of 4), in slice order.
 cudaError_t launch_sum_slices_f32(const float* part, int splits, long long n, float* out, cudaStream_t st);
+cudaError_t launch_quantize_rowwise_e4m3(const void* x, long long rows, int cols, void* q, float* scale,
+                                         cudaStream_t st);
+cudaError_t launch_gather_rows_e4m3(const void* src, const float* src_scale, const int32_t* gather_idx, int R, int T,
+                                    int row_bytes, void* dst, float* dst_scale, int allow_padding, int* status,
+                                    cudaStream_t st);
 cudaError_t launch_splitk_reduce_bf16(const float* partials, int splits, int64_t slice, void* out,
                                       cudaStream_t stream);
 

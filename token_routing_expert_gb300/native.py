@@ -37,15 +37,16 @@ class moe_config_t(ctypes.Structure):
                 ("restore_weight_scale", ctypes.c_int32), ("expert_weight_scale", ctypes.c_float),
                 ("original_top_k", ctypes.c_int32), ("router_bias", ctypes.c_int32),
                 ("has_score_bias", ctypes.c_int32), ("activation", ctypes.c_int32),
-                ("capacity_factor", ctypes.c_float)]
+                ("capacity_factor", ctypes.c_float), ("expert_fp8", ctypes.c_int32)]
 
 
 class moe_weights_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("w_router", "b_router", "score_bias", "w_down_latent",
-                                                  "w_up_latent", "rms_weight", "w_up_gate", "w_out")]
+                                                  "w_up_latent", "rms_weight", "w_up_gate", "w_out",
+                                                  "w_up_gate_fp8", "w_up_gate_scale", "w_out_fp8", "w_out_scale")]
 
 
-EXPORTS = ["moe_expert_capacity", "moe_permuted_rows", "moe_validate_config", "moe_num_params", "moe_num_active_params", "moe_latent_proj_params",
+EXPORTS = ["moe_quantize_rowwise_fp8", "moe_expert_capacity", "moe_permuted_rows", "moe_validate_config", "moe_num_params", "moe_num_active_params", "moe_latent_proj_params",
            "moe_workspace_size", "moe_router", "moe_permute", "moe_grouped_swiglu", "moe_combine",
            "moe_latent_down", "moe_latent_restore", "moe_layer_forward", "moe_layer_forward_staged",
            "moe_layer_forward_launches", "moe_workspace_layout", "moe_get_status", "moe_status_string",
@@ -73,6 +74,7 @@ def load() -> ctypes.CDLL:
         "moe_latent_proj_params": [cfgp, ctypes.c_int, P(I64)],
         "moe_workspace_size": [cfgp, I64, P(SZ)],
         "moe_expert_capacity": [cfgp, I64, P(I64)],
+        "moe_quantize_rowwise_fp8": [VP, I64, ctypes.c_int32, VP, VP, VP],
         "moe_permuted_rows": [cfgp, I64, P(I64)],
         "moe_router": [cfgp, wp, VP, I64, VP, VP, VP, VP, SZ, VP],
         "moe_permute": [cfgp, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
@@ -118,19 +120,20 @@ def _check(code: int, where: str) -> None:
 def make_config(d_model, num_experts, top_k, hidden_size, latent_dim=0, up_proj_norm=True, rms_eps=1e-6,
                 gating="softmax", sigmoid_stability_epsilon=0.0, normalize_expert_weights=0.0,
                 restore_weight_scale=False, expert_weight_scale=0.0, original_top_k=0, router_bias=False,
-                has_score_bias=False, capacity_factor=0.0) -> moe_config_t:
+                has_score_bias=False, capacity_factor=0.0, expert_fp8=False) -> moe_config_t:
     g = GATING_NAMES[gating] if isinstance(gating, str) else int(gating)
     return moe_config_t(d_model, num_experts, top_k, hidden_size, latent_dim, int(up_proj_norm), rms_eps, g,
                         sigmoid_stability_epsilon, normalize_expert_weights, int(restore_weight_scale),
                         expert_weight_scale, original_top_k, int(router_bias), int(has_score_bias), 0,
-                        capacity_factor)
+                        capacity_factor, int(expert_fp8))
 
 
 def config_from_spec(spec: WorkloadSpec) -> moe_config_t:
     return make_config(spec.d_model, spec.num_experts, spec.top_k, spec.hidden_size, spec.latent_dim,
                        spec.up_proj_norm, spec.rms_eps, spec.gating, spec.sigmoid_stability_epsilon,
                        spec.normalize_expert_weights, spec.restore_weight_scale, spec.expert_weight_scale,
-                       spec.original_top_k, spec.skew, spec.score_bias_std > 0, spec.capacity_factor)
+                       spec.original_top_k, spec.skew, spec.score_bias_std > 0, spec.capacity_factor,
+                       spec.expert_fp8)
 
 
 # ---------------------------------------------------------------------------
@@ -218,6 +221,17 @@ class DeviceWeights:
     w_down_latent: Optional[torch.Tensor] = None
     w_up_latent: Optional[torch.Tensor] = None
     rms_weight: Optional[torch.Tensor] = None
+    w_up_gate_fp8: Optional[torch.Tensor] = None
+    w_up_gate_scale: Optional[torch.Tensor] = None
+    w_out_fp8: Optional[torch.Tensor] = None
+    w_out_scale: Optional[torch.Tensor] = None
+
+    def quantize_experts_fp8(self, stream=None) -> "DeviceWeights":
+        """Pre-quantises the expert weights row by row to e4m3 (moe_quantize_rowwise_fp8)."""
+        ug, wo = self.w_up_gate, self.w_out
+        self.w_up_gate_fp8, self.w_up_gate_scale = moe_quantize_rowwise_fp8(ug.reshape(-1, ug.shape[-1]), stream=stream)
+        self.w_out_fp8, self.w_out_scale = moe_quantize_rowwise_fp8(wo.reshape(-1, wo.shape[-1]), stream=stream)
+        return self
 
     @staticmethod
     def from_inputs(inp, device="cuda") -> "DeviceWeights":
@@ -236,7 +250,20 @@ class DeviceWeights:
             _ptr(self.w_router, bf, "w_router"), _ptr(self.b_router, f32, "b_router"),
             _ptr(self.score_bias, f32, "score_bias"), _ptr(self.w_down_latent, bf, "w_down_latent"),
             _ptr(self.w_up_latent, bf, "w_up_latent"), _ptr(self.rms_weight, bf, "rms_weight"),
-            _ptr(self.w_up_gate, bf, "w_up_gate"), _ptr(self.w_out, bf, "w_out"))
+            _ptr(self.w_up_gate, bf, "w_up_gate"), _ptr(self.w_out, bf, "w_out"),
+            _ptr(self.w_up_gate_fp8, torch.uint8, "w_up_gate_fp8"), _ptr(self.w_up_gate_scale, f32, "w_up_gate_scale"),
+            _ptr(self.w_out_fp8, torch.uint8, "w_out_fp8"), _ptr(self.w_out_scale, f32, "w_out_scale"))
+
+
+def moe_quantize_rowwise_fp8(x, codes=None, scales=None, stream=None):
+    """Rowwise e4m3 codes (uint8, same shape) and fp32 row scales of a 2-D bf16 CUDA tensor."""
+    rows, cols = x.shape
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=x.device) if codes is None else codes
+    scales = torch.empty(rows, dtype=torch.float32, device=x.device) if scales is None else scales
+    _check(load().moe_quantize_rowwise_fp8(_ptr(x, torch.bfloat16, "x"), rows, cols, _ptr(codes, torch.uint8, "codes"),
+                                           _ptr(scales, torch.float32, "scales"), _stream(stream)),
+           "moe_quantize_rowwise_fp8")
+    return codes, scales
 
 
 def workspace(cfg: moe_config_t, T: int, device="cuda") -> torch.Tensor:

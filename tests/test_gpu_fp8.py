@@ -7,6 +7,7 @@ import torch
 
 from oracle import moe_ref as ref
 from tests.oracle_bridge import assert_close_layer, check_topk, f64, oracle_config, oracle_weights, output_scale
+from tests.test_gpu_parity import DESIGNED_COUNTS, designed_routing
 from token_routing_expert_gb300 import native
 from token_routing_expert_gb300.workloads import WorkloadSpec, generate
 
@@ -58,3 +59,23 @@ def test_fp8_layer_forward(name):
     # and the FP8 layer stays close to the bf16 one (e4m3 keeps 3 mantissa bits)
     dense = ref.layer_forward(oc, f64(inp["x"]), ow, forced_idx=forced).out
     assert np.linalg.norm(got - dense) / np.linalg.norm(dense) < 0.1
+
+
+def test_fp8_grouped_swiglu_designed_counts():
+    # every kind of group on the CTA-pair path: empty, tail only, whole tiles only, whole tiles + tail
+    spec = WorkloadSpec("designed_counts_fp8", T=sum(DESIGNED_COUNTS), d_model=256,
+                        num_experts=len(DESIGNED_COUNTS), top_k=1, hidden_size=192, gating="softmax",
+                        expert_fp8=True, seed=74)
+    assert spec.rows >= 384 * spec.num_experts
+    inp = generate(spec)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp).quantize_experts_fp8()
+    ws = native.workspace(cfg, spec.T)
+    counts, offsets, gather, scatter = native.moe_permute(cfg, designed_routing(DESIGNED_COUNTS, 7), ws)
+    xr = torch.from_numpy(np.random.default_rng(8).standard_normal((spec.T, spec.d_model), dtype=np.float32)).to(
+        torch.bfloat16)
+    y = native.moe_grouped_swiglu(cfg, wts, xr.cuda(), gather, offsets, ws)
+    assert native.moe_get_status() == 0
+    perm = ref.Permutation(counts.cpu().numpy(), offsets.cpu().numpy(), gather.cpu().numpy(), scatter.cpu().numpy())
+    want = ref.expert_outputs_fp8(oracle_config(spec), f64(xr), perm, oracle_weights(spec, inp).expert)
+    assert_close_layer(y.double().cpu().numpy(), want, "fp8 grouped swiglu, designed counts")

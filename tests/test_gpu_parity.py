@@ -170,6 +170,37 @@ def test_grouped_swiglu(name):
     assert_close_layer(y.double().cpu().numpy(), want, "grouped swiglu")
 
 
+# Per-expert row counts that give the CTA-pair path every kind of group: empty, a tail only
+# (<= 128 and > 128 rows), whole 256-row tiles only, and whole tiles with a short or a long tail.
+DESIGNED_COUNTS = [0, 100, 200, 256, 300, 400, 512, 1304]
+
+
+def designed_routing(counts, seed):
+    """top-1 expert indices with exactly `counts` tokens per expert, in shuffled token order."""
+    e = np.repeat(np.arange(len(counts)), counts)
+    np.random.default_rng(seed).shuffle(e)
+    return torch.from_numpy(e.astype(np.int32).reshape(-1, 1)).cuda()
+
+
+def test_grouped_swiglu_designed_counts():
+    spec = WorkloadSpec("designed_counts", T=sum(DESIGNED_COUNTS), d_model=256, num_experts=len(DESIGNED_COUNTS),
+                        top_k=1, hidden_size=192, gating="softmax", seed=31)
+    assert spec.rows >= 384 * spec.num_experts                   # the CTA-pair path
+    inp = generate(spec)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp)
+    ws = native.workspace(cfg, spec.T)
+    counts, offsets, gather, scatter = native.moe_permute(cfg, designed_routing(DESIGNED_COUNTS, 5), ws)
+    assert counts.cpu().tolist() == DESIGNED_COUNTS
+    xr = torch.from_numpy(np.random.default_rng(6).standard_normal((spec.T, spec.d_model), dtype=np.float32)).to(
+        torch.bfloat16)
+    y = native.moe_grouped_swiglu(cfg, wts, xr.cuda(), gather, offsets, ws)
+    expect_ok()
+    perm = ref.Permutation(counts.cpu().numpy(), offsets.cpu().numpy(), gather.cpu().numpy(), scatter.cpu().numpy())
+    want = ref.expert_outputs(oracle_config(spec), f64(xr), perm, oracle_weights(spec, inp).expert)
+    assert_close_layer(y.double().cpu().numpy(), want, "grouped swiglu, designed counts")
+
+
 @pytest.mark.parametrize("name", ["tiny", "sigmoid_bias_restore", "latent_skew", "max_experts", "one_token",
                                   "pair_tiles"])
 def test_combine(name):

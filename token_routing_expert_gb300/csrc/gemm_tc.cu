@@ -4,7 +4,8 @@
 //   warp 0 (one lane)  : TMA producer, STAGES-deep ring of (A, B) k-tiles
 //   warp 1 (one lane)  : UMMA issuer (M=128, N=BN, K=16 per instruction),
 //                        accumulates into one of two TMEM accumulators
-//   warps 2..5         : epilogue, TMEM -> registers -> global, overlapping
+//   warps 2..9         : epilogue, TMEM -> registers -> global, two warps per
+//                        TMEM lane quadrant (alternate 32-column chunks), overlapping
 //                        the next tile's mainloop through the second accumulator
 // Grouped mode: the row ranges of the groups and their tile prefix sums are
 // read on the device, so no host synchronisation is needed to schedule them.
@@ -23,7 +24,8 @@ constexpr int BM = 128;
 constexpr int BK = 64;                 // 64 bf16 = 128 bytes: one 128-byte swizzle row
 constexpr int UMMA_K = 16;
 constexpr int kMaxGroups = 1024;
-constexpr int kThreads = 192;
+constexpr int kEpiWarps = 8;                   // two warps per TMEM lane quadrant, each half the columns
+constexpr int kThreads = 32 * (2 + kEpiWarps);
 
 struct GemmParams {
   int M, N, K;
@@ -122,10 +124,12 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
 // row_in_tile: this thread's row of the 128-row accumulator; rows: valid rows from row0.
 // e4m3 operands: the accumulator is scaled by the A row's scale and each column's B-row
 // scale; cs / cs_gate point at the B-row scales of this tile's first column.
+// With 8 epilogue warps two share a lane quadrant and `half` (0 or 1) picks every other
+// 32-column chunk.
 template <int BN, int EPI, bool F8 = false>
 __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, int row_in_tile, int nt, int split,
-                                           const GemmParams& p, bool zero = false, const float* cs = nullptr,
-                                           const float* cs_gate = nullptr) {
+                                           const GemmParams& p, int half, bool zero = false,
+                                           const float* cs = nullptr, const float* cs_gate = nullptr) {
   const bool row_ok = row_in_tile < rows;
   const long long row = (long long)row0 + row_in_tile;
   const float rs = (F8 && row_ok) ? p.a_scale[row] : 1.0f;
@@ -133,7 +137,7 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
     constexpr int HALF = BN / 2;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
 #pragma unroll 1
-    for (int cc = 0; cc < HALF / 32; ++cc) {
+    for (int cc = half; cc < HALF / 32; cc += kEpiWarps / 4) {
       uint32_t u[32], g[32];
       __syncwarp();
       tmem_ld_32x32b_x32(tbase + cc * 32, u);
@@ -165,7 +169,7 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
     }
   } else {
 #pragma unroll 1
-    for (int cc = 0; cc < BN / 32; ++cc) {
+    for (int cc = half; cc < BN / 32; cc += kEpiWarps / 4) {
       uint32_t v[32];
       __syncwarp();
       if (zero) {  // empty contraction (a K-grouped group without rows): the product is zero
@@ -245,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], 4 * 32);
+      mbar_init(&tempty_bar[a], kEpiWarps * 32);
     }
     fence_mbar_init();
   }
@@ -325,8 +329,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: warps 2..5 ----------------
+    // ---------------- epilogue: warps 2..9 ----------------
     const int quad = warp & 3;                    // TMEM lanes this warp may read
+    const int half = (warp - 2) >> 2;             // which alternate column chunks
     const int row_in_tile = quad * 32 + lane;
     int it = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
@@ -346,7 +351,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         cs = p.b_scale + brow;
         cs_gate = cs + p.b_gate_offset;
       }
-      store_tile<BN, EPI, F8>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p, c.kt1 <= c.kt0, cs, cs_gate);
+      store_tile<BN, EPI, F8>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p, half, c.kt1 <= c.kt0, cs,
+                              cs_gate);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
@@ -427,7 +433,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);    // one multicast commit per tile
-      mbar_init(&tempty_bar[a], 8);   // CTA 0 only: one lane of each of the 2 x 4 epilogue warps
+      mbar_init(&tempty_bar[a], 2 * kEpiWarps);   // CTA 0 only: one lane of each epilogue warp of both CTAs
     }
     fence_mbar_init();
   }
@@ -502,8 +508,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    // ---------------- epilogue: warps 2..5 of both CTAs ----------------
+    // ---------------- epilogue: warps 2..9 of both CTAs ----------------
     const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
     const int row_in_tile = quad * 32 + lane;
     int it = 0;
     for (int t = pair; t < total_tiles; t += npairs, ++it) {
@@ -524,7 +531,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         cs_gate = cs + p.b_gate_offset;
       }
       store_tile<C::BN, EPI, F8>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt, 0, p,
-                                 false, cs, cs_gate);
+                                 half, false, cs, cs_gate);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&tempty_bar[acc]), 0));

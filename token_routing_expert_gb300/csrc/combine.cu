@@ -79,19 +79,30 @@ __global__ void __launch_bounds__(32 * kRowWarps)
   uint4* zs = zs_all + (long long)warp * vec;
   uint4* dst = z + t * vec;
   float sumsq = 0.f;
-  // every lane runs every iteration (the shuffles need the whole warp); loads are guarded
+  // every lane runs every iteration (the shuffles need the whole warp); loads are guarded.
+  // The k rows are read eight at a time, all eight loads issued before the first is used,
+  // and accumulated in ascending j.
   for (int c0 = 0; c0 < vec; c0 += 32) {
     const int c = c0 + lane;
     const bool active = c < vec;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j = 0; j < k; ++j) {
-      const int p = __shfl_sync(0xffffffffu, my_p, j);
-      const float wj = __shfl_sync(0xffffffffu, my_w, j);
-      if (active) {
-        float f[8];
-        unpack8(y[(long long)p * vec + c], f);
+    for (int j0 = 0; j0 < k; j0 += 8) {
+      uint4 v[8];
+      float wj[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj, f[i], acc[i]);
+      for (int jj = 0; jj < 8; ++jj) {
+        const int p = __shfl_sync(0xffffffffu, my_p, (j0 + jj) & 31);
+        wj[jj] = __shfl_sync(0xffffffffu, my_w, (j0 + jj) & 31);
+        v[jj] = make_uint4(0u, 0u, 0u, 0u);
+        if (active && j0 + jj < k) v[jj] = __ldcs(y + (long long)p * vec + c);
+      }
+#pragma unroll
+      for (int jj = 0; jj < 8; ++jj) {
+        if (j0 + jj >= k) break;
+        float f[8];
+        unpack8(v[jj], f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[jj], f[i], acc[i]);
       }
     }
     if (!active) continue;

@@ -82,7 +82,15 @@ __global__ void __launch_bounds__(256) gather_rows_e4m3_kernel(const uint4* __re
     return;
   }
   const uint4* s = src + (long long)t * vec;
-  for (int c = lane; c < vec; c += 32) d[c] = s[c];
+  for (int c0 = lane; c0 < vec; c0 += 256) {   // eight 16-byte loads in flight per lane
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + 32 * i < vec) v[i] = __ldg(s + c0 + 32 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + 32 * i < vec) d[c0 + 32 * i] = v[i];
+  }
   if (lane == 0) dst_scale[p] = src_scale[t];
 }
 

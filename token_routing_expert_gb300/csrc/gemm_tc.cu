@@ -26,6 +26,7 @@ constexpr int UMMA_K = 16;
 constexpr int kMaxGroups = 1024;
 constexpr int kEpiWarps = 8;                   // two warps per TMEM lane quadrant, each half the columns
 constexpr int kThreads = 32 * (2 + kEpiWarps);
+constexpr int kEpiStageBytes = kEpiWarps * 2048;   // a 32 x 32 bf16 block per epilogue warp
 
 struct GemmParams {
   int M, N, K;
@@ -63,7 +64,8 @@ struct GemmCfg {
   static constexpr int HOLDER_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int ABORT_OFF = HOLDER_OFF + 4;
   static constexpr int TABLE_OFF = (ABORT_OFF + 4 + 15) & ~15;
-  static constexpr int SMEM_BYTES = TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 1024;  // + alignment slack
+  static constexpr int EPI_OFF = (TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 127) & ~127;  // epilogue staging
+  static constexpr int SMEM_BYTES = EPI_OFF + kEpiStageBytes + 1024;                  // + alignment slack
   static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=128, whole 32-column epilogue chunks");
 };
@@ -120,6 +122,28 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
   return c;
 }
 
+// Stores a warp's 32 x 32 bf16 block (thread i holds row i as 16 packed words) through a 2 KB
+// shared buffer, so that each global store instruction writes 8 rows x 64 contiguous bytes
+// instead of 32 rows x 16 bytes.  The 16-byte slots are XOR-swizzled by row: both the row-wise
+// writes and the column-wise reads hit 8 distinct bank groups per quarter warp.
+// out0: column 0 of the block's first row; valid: how many of the 32 rows exist.
+__device__ __forceinline__ void store_block_bf16(uint4* stg, const uint32_t (&packed)[16], __nv_bfloat16* out0,
+                                                 long long ldo, int valid, int lane) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    stg[lane * 4 + (i ^ ((lane >> 1) & 3))] =
+        make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+  __syncwarp();
+  const int q = lane & 3;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int r = s * 8 + (lane >> 2);
+    const uint4 v = stg[r * 4 + (q ^ ((r >> 1) & 3))];
+    if (r < valid) *reinterpret_cast<uint4*>(out0 + r * ldo + q * 8) = v;
+  }
+  __syncwarp();
+}
+
 // Epilogue of one tile for the 32 rows a warp owns: TMEM -> registers -> global.
 // row_in_tile: this thread's row of the 128-row accumulator; rows: valid rows from row0.
 // e4m3 operands: the accumulator is scaled by the A row's scale and each column's B-row
@@ -128,11 +152,14 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
 // 32-column chunk.
 template <int BN, int EPI, bool F8 = false>
 __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, int row_in_tile, int nt, int split,
-                                           const GemmParams& p, int half, bool zero = false,
+                                           const GemmParams& p, int half, uint4* stg, bool zero = false,
                                            const float* cs = nullptr, const float* cs_gate = nullptr) {
   const bool row_ok = row_in_tile < rows;
   const long long row = (long long)row0 + row_in_tile;
   const float rs = (F8 && row_ok) ? p.a_scale[row] : 1.0f;
+  const int lane = row_in_tile & 31;
+  const int valid = min(max(rows - (row_in_tile - lane), 0), 32);   // rows of this warp's 32 that exist
+  const long long wrow0 = (long long)row0 + (row_in_tile - lane);
   if (EPI == EPI_SWIGLU) {
     constexpr int HALF = BN / 2;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
@@ -144,7 +171,7 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
       tmem_ld_32x32b_x32(tbase + HALF + cc * 32, g);
       tmem_ld_wait();
       const int col0 = nt * HALF + cc * 32;
-      if (row_ok && col0 < p.N) {
+      if (valid > 0 && col0 < p.N) {
         if (F8) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -157,14 +184,12 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
         for (int i = 0; i < 16; ++i) {
           const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
           const float u0 = __uint_as_float(u[2 * i]), u1 = __uint_as_float(u[2 * i + 1]);
-          const float h0 = g0 / (1.0f + __expf(-g0)) * u0;
-          const float h1 = g1 / (1.0f + __expf(-g1)) * u1;
+          // silu(g) = g / (1 + e^-g); the approximate division returns 0 when e^-g overflows
+          const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * u0;
+          const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * u1;
           packed[i] = pack_bf16x2(h0, h1);
         }
-        uint4* dst = reinterpret_cast<uint4*>(out + row * p.ldo + col0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        store_block_bf16(stg, packed, out + wrow0 * p.ldo + col0, p.ldo, valid, lane);
       }
     }
   } else {
@@ -180,7 +205,11 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
         tmem_ld_wait();
       }
       const int col0 = nt * BN + cc * 32;
-      if (!row_ok || col0 >= p.N) continue;
+      if (EPI == EPI_BF16) {
+        if (valid == 0 || col0 >= p.N) continue;
+      } else if (!row_ok || col0 >= p.N) {
+        continue;
+      }
       if (F8) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * rs * __ldg(cs + cc * 32 + i));
@@ -199,14 +228,11 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
             if (col0 + i < p.N) out[i] = __uint_as_float(v[i]);
         }
       } else {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + row * p.ldo + col0;
         uint32_t packed[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) packed[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-        uint4* dst = reinterpret_cast<uint4*>(out);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          dst[i] = make_uint4(packed[4 * i], packed[4 * i + 1], packed[4 * i + 2], packed[4 * i + 3]);
+        store_block_bf16(stg, packed, reinterpret_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo + col0, p.ldo, valid,
+                         lane);
       }
     }
   }
@@ -333,6 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;                    // TMEM lanes this warp may read
     const int half = (warp - 2) >> 2;             // which alternate column chunks
     const int row_in_tile = quad * 32 + lane;
+    uint4* stg = reinterpret_cast<uint4*>(smem + C::EPI_OFF) + (warp - 2) * 128;
     int it = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
       const TileCoord c = decode_tile(t, p, s_toff, s_goff);
@@ -351,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         cs = p.b_scale + brow;
         cs_gate = cs + p.b_gate_offset;
       }
-      store_tile<BN, EPI, F8>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p, half, c.kt1 <= c.kt0, cs,
+      store_tile<BN, EPI, F8>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p, half, stg, c.kt1 <= c.kt0, cs,
                               cs_gate);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
@@ -394,7 +421,8 @@ struct PairCfg {
   static constexpr int HOLDER_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int ABORT_OFF = HOLDER_OFF + 4;
   static constexpr int TABLE_OFF = (ABORT_OFF + 4 + 15) & ~15;
-  static constexpr int SMEM_BYTES = TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 1024;
+  static constexpr int EPI_OFF = (TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 127) & ~127;
+  static constexpr int SMEM_BYTES = EPI_OFF + kEpiStageBytes + 1024;
 };
 
 template <int EPI, bool F8 = false>
@@ -465,9 +493,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!mbar_wait_cluster(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
           const uint32_t full0 = map_to_cta(smem_u32(&full_bar[stage]), 0);
-          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE_BYTES);
+          // a group's last tile with <= 128 rows has none in CTA 1: CTA 1 skips its A rows
+          // (its accumulator rows are never stored) and saves their L2 bytes
+          const bool a1 = c.rows > 128;
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE_BYTES - (a1 ? 0 : C::A_BYTES));
           const int kx = kt * (F8 ? 2 * BK : BK);
-          tma_load_2d_pair(sa, &tmA, full0, kx, arow);
+          if (rank == 0 || a1) tma_load_2d_pair(sa, &tmA, full0, kx, arow);
           tma_load_2d_pair(sa + C::A_BYTES, &tmB, full0, kx, brow);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -512,6 +543,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
     const int row_in_tile = quad * 32 + lane;
+    uint4* stg = reinterpret_cast<uint4*>(smem + C::EPI_OFF) + (warp - 2) * 128;
     int it = 0;
     for (int t = pair; t < total_tiles; t += npairs, ++it) {
       const TileCoord c = decode_tile<BM2>(t, p, s_toff, s_goff);
@@ -531,7 +563,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         cs_gate = cs + p.b_gate_offset;
       }
       store_tile<C::BN, EPI, F8>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt, 0, p,
-                                 half, false, cs, cs_gate);
+                                 half, stg, false, cs, cs_gate);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&tempty_bar[acc]), 0));

@@ -237,7 +237,8 @@ int moe_layer_forward(const moe_config_t* cfg, const moe_weights_t* w, const voi
  * stage boundaries:
  *   [0] start, [1] after the latent down-projection, [2] after the router
  *   GEMM, [3] after top-k, [4] after the permutation, [5] after the group
- *   tile table and the row gather, [6] after grouped GEMM 1 (SwiGLU),
+ *   tile table (and, for e4m3 experts, the quantisation of x_routed),
+ *   [6] after grouped GEMM 1 (SwiGLU, which gathers its input rows),
  *   [7] after grouped GEMM 2,
  *   [8] after the combine (+ RMSNorm), [9] after the latent up-projection.
  * Stages that a configuration does not have record at the same point as the

@@ -66,6 +66,10 @@ int64_t capacity_of(const moe_config_t* c, int64_t T) {
   return 8 * (int64_t)std::ceil(x / 8.0);
 }
 
+// Groups averaging >= 384 rows run on CTA pairs with 256-row tiles; smaller ones keep 128-row
+// tiles, which waste less of each group's last partial tile.  p.rows and p.E must be set.
+int use_pair_tiles(const Plan& p) { return p.rows >= (int64_t)384 * p.E ? 1 : 0; }
+
 void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->T = T;
   p->D = c->d_model;
@@ -111,15 +115,17 @@ void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
     p->gdense = p->sdense = p->odense = (size_t)-1;
   }
   p->xr = p->latent ? take((size_t)T * p->L * 2) : (size_t)-1;
-  p->xp = take((size_t)p->rows * p->Lr * 2);
+  // 128-row tiles read the routed rows from a permuted copy; CTA-pair tiles gather them
+  const bool gathered = use_pair_tiles(*p);
+  p->xp = !gathered && !c->expert_fp8 ? take((size_t)p->rows * p->Lr * 2) : (size_t)-1;
   p->H = take((size_t)p->rows * p->h * 2);
   p->Y = take((size_t)p->rows * p->Lr * 2);
   p->zn = p->latent ? take((size_t)T * p->L * 2) : (size_t)-1;
   if (c->expert_fp8) {
     p->xq = take((size_t)T * p->Lr);
     p->xs = take((size_t)T * 4);
-    p->xpq = take((size_t)p->rows * p->Lr);
-    p->xps = take((size_t)p->rows * 4);
+    p->xpq = gathered ? (size_t)-1 : take((size_t)p->rows * p->Lr);
+    p->xps = gathered ? (size_t)-1 : take((size_t)p->rows * 4);
     p->hq = take((size_t)p->rows * p->h);
     p->hs = take((size_t)p->rows * 4);
   } else {
@@ -166,7 +172,6 @@ int check_call(const moe_config_t* c, int64_t T, void* ws, size_t ws_bytes, Plan
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 // CTA-pair tiles (256 rows) pay off when the average group holds several of them.
-int use_pair_tiles(const Plan& p) { return p.rows >= (int64_t)384 * p.E ? 1 : 0; }
 
 template <typename T>
 T* at(void* ws, size_t off) {
@@ -239,8 +244,8 @@ int run_router(const moe_config_t* c, const moe_weights_t* w, const void* x, con
                                  wts, status, st));
 }
 
-// The experts on rowwise e4m3 operands: quantise x_routed per token, gather code rows and
-// scales, GEMM 1 (SwiGLU, scales in the epilogue) -> H bf16, quantise H per row, GEMM 2.
+// The experts on rowwise e4m3 operands: quantise x_routed per token, GEMM 1 on the code rows in
+// permuted order (SwiGLU, scales in the epilogue) -> H bf16, quantise H per row, GEMM 2.
 int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
                     const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
                     cudaEvent_t* ev) {
@@ -248,20 +253,24 @@ int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* x
   void* H = at<void>(ws, p.H);
   void* xq = at<void>(ws, p.xq);
   float* xs = at<float>(ws, p.xs);
-  void* xpq = at<void>(ws, p.xpq);
-  float* xps = at<float>(ws, p.xps);
   void* hq = at<void>(ws, p.hq);
   float* hs = at<float>(ws, p.hs);
   const int pair = use_pair_tiles(p);
   int s = cuda_status(launch_tile_table(offsets, p.E, pair ? 256 : 128, tile_off, st));
   if (s == MOE_OK) s = cuda_status(launch_quantize_rowwise_e4m3(xr, p.T, p.Lr, xq, xs, st));
-  if (s == MOE_OK)
-    s = cuda_status(launch_gather_rows_e4m3(xq, xs, gather, (int)p.rows, (int)p.T, p.Lr, xpq, xps, p.capacity ? 1 : 0,
-                                            status, st));
+  if (s == MOE_OK && !pair)   // 128-row tiles: a permuted copy of the code rows and their scales
+    s = cuda_status(launch_gather_rows_e4m3(xq, xs, gather, (int)p.rows, (int)p.T, p.Lr, at<void>(ws, p.xpq),
+                                            at<float>(ws, p.xps), p.capacity ? 1 : 0, status, st));
   if (s != MOE_OK) return s;
   mark(ev, 5, st);
   GemmProblem g1{};
-  g1.A = xpq;
+  if (pair) {               // the GEMM copies the code rows in permuted order itself
+    g1.a_gather = gather;
+    g1.a_src = xq;
+    g1.a_src_rows = (int)p.T;
+  } else {
+    g1.A = at<void>(ws, p.xpq);
+  }
   g1.B = w->w_up_gate_fp8;
   g1.b_rows_total = (int64_t)p.E * 2 * p.h;
   g1.M = (int)p.rows;
@@ -277,7 +286,7 @@ int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* x
   g1.splits = 1;
   g1.pair_tiles = pair;
   g1.e4m3 = 1;
-  g1.a_scale = xps;
+  g1.a_scale = pair ? xs : at<float>(ws, p.xps);   // gathered: per token, looked up through a_gather
   g1.b_scale = w->w_up_gate_scale;
   g1.out = H;
   g1.ldo = p.h;
@@ -317,7 +326,6 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
                 const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
                 cudaEvent_t* ev = nullptr) {
   int32_t* tile_off = at<int32_t>(ws, p.tile_off);
-  void* xp = at<void>(ws, p.xp);
   void* H = at<void>(ws, p.H);
   if (c->expert_fp8) return run_experts_fp8(c, w, xr, gather, offsets, p, y, ws, status, st, ev);
   // large groups run on CTA pairs with 256-row tiles; small ones keep 128-row tiles,
@@ -325,13 +333,23 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   const int pair = use_pair_tiles(p);
   int s = cuda_status(launch_tile_table(offsets, p.E, pair ? 256 : 128, tile_off, st));
   if (s != MOE_OK) return s;
-  // rows of the experts' input in permuted order (a TMA tile::gather4 A-load was
-  // measured 3x slower than this copy plus tiled loads)
-  s = cuda_status(launch_gather_rows(xr, gather, (int)p.rows, (int)p.T, p.Lr, xp, p.capacity ? 1 : 0, status, st));
-  if (s != MOE_OK) return s;
+  // CTA-pair tiles: GEMM 1 copies the rows of x_routed in permuted order itself (cp.async into
+  // its A stages).  128-row tiles read a permuted copy through TMA.  (A TMA tile::gather4 A-load
+  // was measured 3x slower than a separate copy.)
+  if (!pair) {
+    s = cuda_status(launch_gather_rows(xr, gather, (int)p.rows, (int)p.T, p.Lr, at<void>(ws, p.xp), p.capacity ? 1 : 0,
+                                       status, st));
+    if (s != MOE_OK) return s;
+  }
   mark(ev, 5, st);
   GemmProblem g1{};
-  g1.A = xp;
+  if (pair) {
+    g1.a_gather = gather;
+    g1.a_src = xr;
+    g1.a_src_rows = (int)p.T;
+  } else {
+    g1.A = at<void>(ws, p.xp);
+  }
   g1.B = w->w_up_gate;
   g1.b_rows_total = (int64_t)p.E * 2 * p.h;
   g1.M = (int)p.rows;
@@ -763,7 +781,8 @@ int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
   if (p.latent) k += p.down_splits > 1 ? 2 : 1;  // latent down (+ split-K reduce)
   k += p.router_splits > 1 ? 3 : 2;              // router GEMM, (split-K sum,) top-k
   k += p.capacity ? 4 : 3;                       // permute: count, scan, place (, capacity slots)
-  k += 2;                                        // tile table, row gather
+  k += use_pair_tiles(p) ? 1 : 2;                // tile table (+ row gather for 128-row tiles;
+                                                 // on CTA pairs grouped GEMM 1 gathers its rows)
   k += 2;                                        // grouped GEMM 1 (SwiGLU), grouped GEMM 2
   if (c->expert_fp8) k += 2;                     // e4m3 quantisation of x_routed and of H
   k += 1;                                        // combine (+ RMSNorm when latent)

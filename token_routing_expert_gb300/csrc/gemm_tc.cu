@@ -27,6 +27,12 @@ constexpr int kMaxGroups = 1024;
 constexpr int kEpiWarps = 8;                   // two warps per TMEM lane quadrant, each half the columns
 constexpr int kThreads = 32 * (2 + kEpiWarps);
 constexpr int kEpiStageBytes = kEpiWarps * 2048;   // a 32 x 32 bf16 block per epilogue warp
+// Gathered-A kernels add 4 warps that copy the A rows from their source rows (cp.async) and
+// one warp whose lane 0 hands each landed stage on to the MMA (see gather_a_relay).
+constexpr int kGatherWarps = 4;
+constexpr int kGatherThread0 = 32 * (2 + kEpiWarps);
+constexpr int kRelayWarp = 2 + kEpiWarps + kGatherWarps;
+constexpr int kThreadsGA = 32 * (kRelayWarp + 1);
 
 struct GemmParams {
   int M, N, K;
@@ -46,6 +52,10 @@ struct GemmParams {
   const int* k_off;        // device (k_groups+1) k-tile offsets
   const float* a_scale;    // e4m3 operands: scale of each A row
   const float* b_scale;    // e4m3 operands: scale of each B row
+  const int* a_gather;     // non-null: A row r is row a_gather[r] of a_src (-1: a zero row)
+  const uint8_t* a_src;    //   source rows (a_src_rows x K), a_ld_bytes apart
+  long long a_ld_bytes;
+  int a_src_rows;
   int* status;
 };
 
@@ -58,9 +68,9 @@ struct GemmCfg {
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int ACC_STRIDE = BN <= 32 ? 32 : BN <= 64 ? 64 : BN <= 128 ? 128 : 256;
   static constexpr int TMEM_COLS = 2 * ACC_STRIDE < 32 ? 32 : 2 * ACC_STRIDE;
-  // ring | barriers (full, empty, tmem_full x2, tmem_empty x2) | tmem holder | abort | group tables
+  // ring | barriers (full, empty, tmem_full x2, tmem_empty x2, gathered) | tmem holder | abort | group tables
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 4;
+  static constexpr int NUM_BARS = 3 * STAGES + 4;
   static constexpr int HOLDER_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int ABORT_OFF = HOLDER_OFF + 4;
   static constexpr int TABLE_OFF = (ABORT_OFF + 4 + 15) & ~15;
@@ -156,7 +166,15 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
                                            const float* cs = nullptr, const float* cs_gate = nullptr) {
   const bool row_ok = row_in_tile < rows;
   const long long row = (long long)row0 + row_in_tile;
-  const float rs = (F8 && row_ok) ? p.a_scale[row] : 1.0f;
+  float rs = 1.0f;
+  if (F8 && row_ok) {
+    if (p.a_gather) {   // gathered A: the scale belongs to the source row
+      const int src = p.a_gather[row];
+      rs = src >= 0 ? p.a_scale[src] : 1.0f;
+    } else {
+      rs = p.a_scale[row];
+    }
+  }
   const int lane = row_in_tile & 31;
   const int valid = min(max(rows - (row_in_tile - lane), 0), 32);   // rows of this warp's 32 that exist
   const long long wrow0 = (long long)row0 + (row_in_tile - lane);
@@ -238,8 +256,96 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
   }
 }
 
-template <int BN, int EPI, bool F8 = false>
-__global__ void __launch_bounds__(kThreads, 1)
+// Producer of a gathered A operand (4 warps).  For every k-tile it copies the CTA's 128
+// rows of the tile, row r from source row a_gather[row0 + r], into the stage's A region in the
+// 128-byte-swizzled layout a TMA load writes (16-byte chunk c of row r at c ^ (r mod 8)).
+// Thread t moves chunk (t & 7) of rows (t >> 3) + 16 j, so a warp instruction reads four whole
+// 128-byte lines.  Rows past the tile's valid rows and -1 rows are zero-filled without reads.
+// Each thread's copies for a stage end with a no-wait arrive on the CTA's gathered-rows barrier
+// of that stage (128 arrivals); gather_a_relay takes it from there.
+template <int ROWS, int NST, bool PAIR>
+__device__ __forceinline__ void gather_a_producer(const GemmParams& p, const int* s_toff, const int* s_goff,
+                                                  int t_first, int t_step, int total_tiles, int rank, uint8_t* smem,
+                                                  int stage_bytes, uint64_t* empty_bar, uint64_t* gath_bar,
+                                                  volatile int* abort_flag) {
+  const int t = threadIdx.x - kGatherThread0;
+  const int lane = t & 31;
+  const int chunk = t & 7;
+  uint32_t stage = 0, phase = 0;
+  bool ok = true;
+  for (int tile = t_first; tile < total_tiles && ok; tile += t_step) {
+    const TileCoord c = decode_tile<ROWS>(tile, p, s_toff, s_goff);
+    int tok[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int r = 128 * rank + (t >> 3) + 16 * j;   // row of the tile
+      int src = -1;
+      if (r < c.rows) {
+        src = __ldg(p.a_gather + c.row0 + r);
+        if (src < -1 || src >= p.a_src_rows) {
+          set_status(p.status, MOE_ERR_BOUNDS);
+          src = -1;
+        }
+      }
+      tok[j] = src;
+    }
+    for (int kt = c.kt0; kt < c.kt1; ++kt) {
+      int free_slot = 1;
+      if (lane == 0)
+        free_slot = (PAIR ? mbar_wait_cluster(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)
+                          : mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status))
+                        ? 1
+                        : 0;
+      if (!__shfl_sync(0xffffffffu, free_slot, 0)) {
+        ok = false;
+        break;
+      }
+      const uint32_t sa = smem_u32(smem + stage * stage_bytes);
+      const uint8_t* kb = p.a_src + (long long)kt * 128 + chunk * 16;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int r = (t >> 3) + 16 * j;
+        const int src = tok[j];
+        cp_async_16(sa + r * 128 + ((chunk ^ (r & 7)) << 4), kb + (long long)(src < 0 ? 0 : src) * p.a_ld_bytes,
+                    src < 0 ? 0u : 16u);
+      }
+      cp_async_arrive_noinc(&gath_bar[stage]);
+      if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1u; }
+    }
+  }
+  cp_async_wait_all();   // every copy lands before the CTA's shared memory can go away
+}
+
+// One thread per CTA: for every stage, in order, waits until the CTA's gathered rows have
+// landed, fences them into the async proxy (the tensor core reads shared memory through it)
+// and arrives on the stage's full barrier, which on a CTA pair is CTA 0's.  It issues no
+// copies itself, so neither the fence nor the arrive waits on copies of later stages.
+template <int ROWS, int NST, bool PAIR>
+__device__ __forceinline__ void gather_a_relay(const GemmParams& p, const int* s_toff, const int* s_goff, int t_first,
+                                               int t_step, int total_tiles, uint64_t* gath_bar, uint64_t* full_bar,
+                                               volatile int* abort_flag) {
+  uint32_t stage = 0, phase = 0;
+  for (int tile = t_first; tile < total_tiles; tile += t_step) {
+    const TileCoord c = decode_tile<ROWS>(tile, p, s_toff, s_goff);
+    for (int kt = c.kt0; kt < c.kt1; ++kt) {
+      if (!(PAIR ? mbar_wait_cluster(&gath_bar[stage], phase, abort_flag, p.status)
+                 : mbar_wait(&gath_bar[stage], phase, abort_flag, p.status)))
+        return;
+      fence_proxy_async_smem();
+      // CTA 1's rows stay in its own shared memory and its own tensor core reads them, so the
+      // arrive on CTA 0's barrier keeps the default CTA-scope release: a cluster-scope release
+      // cost ~0.5 us per stage here and halved the GEMM's speed
+      if (PAIR)
+        mbar_arrive_cluster(map_to_cta(smem_u32(&full_bar[stage]), 0));
+      else
+        mbar_arrive(&full_bar[stage]);
+      if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1u; }
+    }
+  }
+}
+
+template <int BN, int EPI, bool F8 = false, bool GA = false>
+__global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
   using C = GemmCfg<BN>;
@@ -249,6 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* empty_bar = full_bar + C::STAGES;
   uint64_t* tfull_bar = empty_bar + C::STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* gath_bar = tempty_bar + 2;   // gathered A only
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::HOLDER_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
   int* s_toff = reinterpret_cast<int*>(smem + C::TABLE_OFF);
@@ -270,8 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);
+      mbar_init(&full_bar[s], GA ? 2 : 1);   // producer arrive (+ the gathered rows' relay)
       mbar_init(&empty_bar[s], 1);
+      if (GA) mbar_init(&gath_bar[s], 32 * kGatherWarps);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -281,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) tmem_alloc(tmem_holder, C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
+    if (!GA) tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
   tc_fence_before();
@@ -305,9 +413,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
           uint8_t* sb = sa + C::A_BYTES;
-          mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+          mbar_arrive_expect_tx(&full_bar[stage], GA ? C::B_BYTES : C::STAGE_BYTES);
           const int kx = kt * (F8 ? 2 * BK : BK);   // 128 bytes of K per k-tile: 64 bf16 or 128 e4m3
-          tma_load_2d(sa, &tmA, &full_bar[stage], kx, c.row0);
+          if (!GA) tma_load_2d(sa, &tmA, &full_bar[stage], kx, c.row0);
           if (EPI == EPI_SWIGLU) {
             tma_load_2d(sb, &tmB, &full_bar[stage], kx, brow);
             tma_load_2d(sb + C::B_BYTES / 2, &tmB, &full_bar[stage], kx, brow + p.b_gate_offset);
@@ -354,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         umma_commit(&tfull_bar[acc]);
       }
     }
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ---------------- epilogue: warps 2..9 ----------------
     const int quad = warp & 3;                    // TMEM lanes this warp may read
     const int half = (warp - 2) >> 2;             // which alternate column chunks
@@ -382,6 +490,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                               cs_gate);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
+    }
+  } else if constexpr (GA) {
+    if (warp < kRelayWarp) {
+      // ---------------- gathered A rows: warps 10..13 ----------------
+      gather_a_producer<BM, C::STAGES, false>(p, s_toff, s_goff, blockIdx.x, gridDim.x, total_tiles, 0, smem,
+                                              C::STAGE_BYTES, empty_bar, gath_bar, abort_flag);
+    } else if (lane == 0) {
+      gather_a_relay<BM, C::STAGES, false>(p, s_toff, s_goff, blockIdx.x, gridDim.x, total_tiles, gath_bar, full_bar,
+                                           abort_flag);
     }
   }
 
@@ -417,7 +534,7 @@ struct PairCfg {
   static constexpr int ACC_STRIDE = 256;
   static constexpr int TMEM_COLS = 512;
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 4;
+  static constexpr int NUM_BARS = 3 * STAGES + 4;
   static constexpr int HOLDER_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int ABORT_OFF = HOLDER_OFF + 4;
   static constexpr int TABLE_OFF = (ABORT_OFF + 4 + 15) & ~15;
@@ -425,8 +542,8 @@ struct PairCfg {
   static constexpr int SMEM_BYTES = EPI_OFF + kEpiStageBytes + 1024;
 };
 
-template <int EPI, bool F8 = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <int EPI, bool F8 = false, bool GA = false>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmParams p) {
   using C = PairCfg;
@@ -436,6 +553,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   uint64_t* empty_bar = full_bar + C::STAGES;
   uint64_t* tfull_bar = empty_bar + C::STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* gath_bar = tempty_bar + 2;   // gathered A only
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::HOLDER_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
   int* s_toff = reinterpret_cast<int*>(smem + C::TABLE_OFF);
@@ -456,7 +574,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(&full_bar[s], 1);     // CTA 0 only: its producer's arrive + both CTAs' bytes
+      // CTA 0 only: its producer's arrive + both CTAs' bytes (+ both CTAs' gathered-rows relays)
+      mbar_init(&full_bar[s], GA ? 3 : 1);
+      if (GA) mbar_init(&gath_bar[s], 32 * kGatherWarps);
       mbar_init(&empty_bar[s], 1);    // one multicast commit per use
     }
     for (int a = 0; a < 2; ++a) {
@@ -467,7 +587,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&tmA);
+    if (!GA) tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
   }
   tc_fence_before();
@@ -496,9 +616,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // a group's last tile with <= 128 rows has none in CTA 1: CTA 1 skips its A rows
           // (its accumulator rows are never stored) and saves their L2 bytes
           const bool a1 = c.rows > 128;
-          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::STAGE_BYTES - (a1 ? 0 : C::A_BYTES));
+          if (rank == 0)
+            mbar_arrive_expect_tx(&full_bar[stage], GA ? 2 * C::B_BYTES : 2 * C::STAGE_BYTES - (a1 ? 0 : C::A_BYTES));
           const int kx = kt * (F8 ? 2 * BK : BK);
-          if (rank == 0 || a1) tma_load_2d_pair(sa, &tmA, full0, kx, arow);
+          if (!GA && (rank == 0 || a1)) tma_load_2d_pair(sa, &tmA, full0, kx, arow);
           tma_load_2d_pair(sa + C::A_BYTES, &tmB, full0, kx, brow);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -538,7 +659,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         umma_commit_pair(&tfull_bar[acc], 0x3);
       }
     }
-  } else {
+  } else if (warp < 2 + kEpiWarps) {
     // ---------------- epilogue: warps 2..9 of both CTAs ----------------
     const int quad = warp & 3;
     const int half = (warp - 2) >> 2;
@@ -567,6 +688,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&tempty_bar[acc]), 0));
+    }
+  } else if constexpr (GA) {
+    // ---------------- gathered A rows: warps 10..13 of both CTAs ----------------
+    if (warp < kRelayWarp) {
+      gather_a_producer<BM2, C::STAGES, true>(p, s_toff, s_goff, pair, npairs, total_tiles, (int)rank, smem,
+                                              C::STAGE_BYTES, empty_bar, gath_bar, abort_flag);
+    } else if (lane == 0) {
+      gather_a_relay<BM2, C::STAGES, true>(p, s_toff, s_goff, pair, npairs, total_tiles, gath_bar, full_bar,
+                                           abort_flag);
     }
   }
 
@@ -645,11 +775,11 @@ int pick_splits(int tiles, int K) {
   return (kt + per - 1) / per;           // no empty split
 }
 
-template <int BN, int EPI, bool F8 = false>
+template <int BN, int EPI, bool F8 = false, bool GA = false>
 static cudaError_t launch_impl(const GemmProblem& q, const CUtensorMap& ta, const CUtensorMap& tb,
                                const GemmParams& gp, int grid, cudaStream_t stream) {
   using C = GemmCfg<BN>;
-  auto kern = gemm_tc_kernel<BN, EPI, F8>;
+  auto kern = gemm_tc_kernel<BN, EPI, F8, GA>;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -657,14 +787,15 @@ static cudaError_t launch_impl(const GemmProblem& q, const CUtensorMap& ta, cons
     attr_set = true;
   }
   (void)q;
-  kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(ta, tb, gp);
+  kern<<<grid, GA ? kThreadsGA : kThreads, C::SMEM_BYTES, stream>>>(ta, tb, gp);
   return cudaGetLastError();
 }
 
-template <int EPI, bool F8 = false>
+template <int EPI, bool F8 = false, bool GA = false>
 static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp, int tiles,
                                     cudaStream_t stream) {
-  auto kern = gemm_tc_pair_kernel<EPI, F8>;
+  auto kern = gemm_tc_pair_kernel<EPI, F8, GA>;
+  constexpr int threads = GA ? kThreadsGA : kThreads;
   static bool attr_set = false;
   static int max_pairs = 0;
   if (!attr_set) {
@@ -672,7 +803,7 @@ static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * num_sms());
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = PairCfg::SMEM_BYTES;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -689,7 +820,7 @@ static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb
   }
   int pairs = max_pairs;
   if (tiles > 0) pairs = std::min(pairs, tiles);
-  kern<<<2 * pairs, kThreads, PairCfg::SMEM_BYTES, stream>>>(ta, tb, gp);
+  kern<<<2 * pairs, threads, PairCfg::SMEM_BYTES, stream>>>(ta, tb, gp);
   return cudaGetLastError();
 }
 
@@ -702,10 +833,17 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   if (pair && (q.bn != 256 || q.splits > 1 || q.epilogue == EPI_F32)) return cudaErrorInvalidValue;
   if (f8 && (q.bn != 256 || q.splits > 1 || q.k_groups > 0 || q.epilogue == EPI_F32 || !q.a_scale || !q.b_scale))
     return cudaErrorInvalidValue;
+  // gathered A: grouped SwiGLU only; A rows are copied from a_src by the kernel, no A tensor map
+  const bool ga = q.a_gather != nullptr;
+  if (ga && (q.epilogue != EPI_SWIGLU || q.num_groups == 0 || q.splits > 1 || !q.a_src || q.a_src_rows < 0))
+    return cudaErrorInvalidValue;
   const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
   CUtensorMap ta, tb;
-  if (!make_tmap(&ta, q.A, q.M, q.K, BM, f8)) return cudaErrorInvalidValue;
   if (!make_tmap(&tb, q.B, q.b_rows_total, q.K, b_box, f8)) return cudaErrorInvalidValue;
+  if (ga)
+    ta = tb;   // unused
+  else if (!make_tmap(&ta, q.A, q.M, q.K, BM, f8))
+    return cudaErrorInvalidValue;
 
   GemmParams gp;
   gp.M = q.M;
@@ -729,8 +867,20 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.k_off = q.k_off;
   gp.a_scale = q.a_scale;
   gp.b_scale = q.b_scale;
+  gp.a_gather = q.a_gather;
+  gp.a_src = static_cast<const uint8_t*>(q.a_src);
+  gp.a_ld_bytes = (long long)q.K * (f8 ? 1 : 2);
+  gp.a_src_rows = q.a_src_rows;
   gp.status = q.status;
 
+  if (ga) {
+    if (pair)
+      return f8 ? launch_pair_impl<EPI_SWIGLU, true, true>(ta, tb, gp, 0, stream)
+                : launch_pair_impl<EPI_SWIGLU, false, true>(ta, tb, gp, 0, stream);
+    const int grid = num_sms();
+    return f8 ? launch_impl<256, EPI_SWIGLU, true, true>(q, ta, tb, gp, grid, stream)
+              : launch_impl<256, EPI_SWIGLU, false, true>(q, ta, tb, gp, grid, stream);
+  }
   if (pair) {
     const int tiles = q.num_groups == 0 ? ((q.M + BM2 - 1) / BM2) * gp.n_tiles : 0;
     if (f8) {

@@ -36,6 +36,10 @@ struct GemmProblem {
   int e4m3;               // 1: A and B are e4m3 bytes (kind::f8f6f4) with per-row scales below
   const float* a_scale;   // (M) scale of each A row
   const float* b_scale;   // (b_rows_total) scale of each B row
+  const int* a_gather;    // non-NULL (grouped SwiGLU only): A row r is row a_gather[r] of a_src, -1 a zero
+                          // row; A is then unused.  e4m3: a_scale is per a_src row.
+  const void* a_src;      // (a_src_rows, K) bf16 or e4m3
+  int a_src_rows;
   int* status;
 };
 

@@ -221,8 +221,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
     for (int i = 0; i < 8; ++i)
       if (c0 + 32 * i < vec_per_row) v[i] = __ldg(s + c0 + 32 * i);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (c0 + 32 * i < vec_per_row) d[c0 + 32 * i] = v[i];
+    for (int i = 0; i < 8; ++i)   // streaming stores: keep the source rows, not the copy, in L2
+      if (c0 + 32 * i < vec_per_row) __stcs(d + c0 + 32 * i, v[i]);
   }
 }
 

@@ -435,8 +435,17 @@ def run_native(args):
     if spec.expert_fp8:
         # e4m3 tensor peak: the measured bf16 figure x the nominal e4m3 / bf16 ratio (4.5 / 2.25 PFLOP/s)
         gemm_peak, gemm_label = 2.0 * peak_tf, peak_label + " x 2 (nominal e4m3 / bf16 ratio)"
-    bound_layer = "hbm" if (alg_bytes / (peaks["hbm_gbs"] * 1e9)) > (flops / (peak_tf * 1e12)) else "tensor"
-    roof_ms = 1e3 * max(alg_bytes / (peaks["hbm_gbs"] * 1e9), flops / (peak_tf * 1e12))
+    # roofline of the layer: the slower of its FLOPs at the tensor peak and its bytes at HBM
+    # bandwidth; with e4m3 experts their FLOPs run at the e4m3 peak and their weights are 1 byte
+    expert_flops = 6 * spec.routed_dim * spec.hidden_size * spec.rows
+    t_flops = flops / (peak_tf * 1e12)
+    roof_bytes = alg_bytes
+    if spec.expert_fp8:
+        t_flops = (flops - expert_flops) / (peak_tf * 1e12) + expert_flops / (gemm_peak * 1e12)
+        roof_bytes = alg_bytes - touched * 3 * spec.routed_dim * spec.hidden_size
+    t_bytes = roof_bytes / (peaks["hbm_gbs"] * 1e9)
+    bound_layer = "hbm" if t_bytes > t_flops else "tensor"
+    roof_ms = 1e3 * max(t_bytes, t_flops)
 
     if rank != 0:
         return

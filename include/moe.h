@@ -252,6 +252,37 @@ int moe_layer_forward_staged(const moe_config_t* cfg, const moe_weights_t* w, co
 int moe_layer_forward_launches(const moe_config_t* cfg, int64_t T, int32_t* n);
 
 /*
+ * The layer forward over n_batches batches that live in HOST memory, with the
+ * copies overlapped.  The page has no counterpart: this is a library
+ * convenience for callers whose tokens arrive in host memory (a serving front
+ * end, a data loader) and who want the host <-> device traffic hidden behind
+ * the compute instead of paying it between batches.
+ *
+ *   x_host[b]    host (T, d_model) bf16 inputs, b < n_batches (pinned memory
+ *                lets the copies run asynchronously; pageable memory works but
+ *                each copy then blocks the host)
+ *   out_host[b]  host (T, d_model) bf16 outputs
+ *   ws           device workspace of moe_host_workspace_size(cfg, T) bytes:
+ *                the layer's workspace followed by two input and two output
+ *                staging buffers
+ *
+ * Batch b is copied in on an internal copy stream while batch b-1 computes on
+ * `stream`, and its output is copied out on a second internal stream while
+ * batch b+1 computes.  Everything is ordered after the work already on
+ * `stream`, and the call returns once it is all enqueued: out_host is complete
+ * when `stream` is (synchronise it before reading).  The internal streams and
+ * events are created on the first call on a device and reused, so calls on one
+ * device from several host threads at once race with each other.  Host
+ * buffers must stay valid until `stream` completes.  Errors as for
+ * moe_layer_forward; MOE_ERR_WORKSPACE when ws is smaller than
+ * moe_host_workspace_size.
+ */
+int moe_host_workspace_size(const moe_config_t* cfg, int64_t T, size_t* bytes);
+int moe_layer_forward_host_batches(const moe_config_t* cfg, const moe_weights_t* w, const void* const* x_host,
+                                   void* const* out_host, int32_t n_batches, int64_t T, void* ws, size_t ws_bytes,
+                                   moe_stream_t stream);
+
+/*
  * Backward of the weighted combine and of the grouped SwiGLU experts (training).
  * The page's SwiGLU backward (section "SwiGLU с квантизацией"): split into up
  * and gate, sigmoid, gate * sigmoid, its derivative and the two gradients in

@@ -767,6 +767,98 @@ int moe_layer_forward(const moe_config_t* c, const moe_weights_t* w, const void*
   return moe_layer_forward_staged(c, w, x, T, out, ws, ws_bytes, stream, nullptr);
 }
 
+
+// ---------------------------------------------------------------------------
+// Host batches: copies in and out overlapped with the compute of neighbouring batches
+// ---------------------------------------------------------------------------
+namespace {
+struct HostPipe {
+  cudaStream_t cin = nullptr, cout = nullptr;
+  cudaEvent_t start = nullptr, end = nullptr, h2d[2] = {nullptr, nullptr}, fwd[2] = {nullptr, nullptr},
+              d2h[2] = {nullptr, nullptr};
+};
+HostPipe g_pipe[kMaxDevices];
+
+int host_pipe(HostPipe** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_NO_DEVICE;
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.cin) {
+    HostPipe n;
+    bool ok = cudaStreamCreateWithFlags(&n.cin, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&n.cout, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&n.start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&n.end, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; i < 2 && ok; ++i)
+      ok = cudaEventCreateWithFlags(&n.h2d[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&n.fwd[i], cudaEventDisableTiming) == cudaSuccess &&
+           cudaEventCreateWithFlags(&n.d2h[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!ok) return MOE_ERR_CUDA;
+    hp = n;
+  }
+  *out = &hp;
+  return MOE_OK;
+}
+}  // namespace
+
+int moe_host_workspace_size(const moe_config_t* c, int64_t T, size_t* bytes) {
+  size_t lw = 0;
+  int s = moe_workspace_size(c, T, &lw);
+  if (s != MOE_OK) return s;
+  const size_t xb = align256((size_t)T * c->d_model * 2);
+  *bytes = align256(lw) + 4 * xb;
+  return MOE_OK;
+}
+
+int moe_layer_forward_host_batches(const moe_config_t* c, const moe_weights_t* w, const void* const* x_host,
+                                   void* const* out_host, int32_t n_batches, int64_t T, void* ws, size_t ws_bytes,
+                                   moe_stream_t stream) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (n_batches < 0 || T < 0) return MOE_ERR_INVALID_ARG;
+  if (n_batches == 0 || T == 0) return MOE_OK;
+  if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
+  for (int b = 0; b < n_batches; ++b)
+    if (!x_host[b] || !out_host[b]) return MOE_ERR_INVALID_ARG;
+  size_t need = 0, lw = 0;
+  if ((s = moe_host_workspace_size(c, T, &need)) != MOE_OK) return s;
+  if ((s = moe_workspace_size(c, T, &lw)) != MOE_OK) return s;
+  if (!ws || ws_bytes < need || (reinterpret_cast<uintptr_t>(ws) & 255u)) return MOE_ERR_WORKSPACE;
+  HostPipe* hp = nullptr;
+  if ((s = host_pipe(&hp)) != MOE_OK) return s;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t bytes = (size_t)T * c->d_model * 2;
+  const size_t xb = align256(bytes);
+  uint8_t* base = static_cast<uint8_t*>(ws) + align256(lw);
+  void* xs[2] = {base, base + xb};
+  void* os[2] = {base + 2 * xb, base + 3 * xb};
+  auto ck = [](cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; };
+  // the copy streams start after everything already enqueued on the caller's stream
+  if ((s = ck(cudaEventRecord(hp->start, st))) != MOE_OK) return s;
+  if ((s = ck(cudaStreamWaitEvent(hp->cin, hp->start, 0))) != MOE_OK) return s;
+  if ((s = ck(cudaStreamWaitEvent(hp->cout, hp->start, 0))) != MOE_OK) return s;
+  for (int b = 0; b < n_batches && s == MOE_OK; ++b) {
+    const int k = b & 1;
+    // input slot k is free once batch b-2's forward has read it
+    if (b >= 2 && (s = ck(cudaStreamWaitEvent(hp->cin, hp->fwd[k], 0))) != MOE_OK) break;
+    if ((s = ck(cudaMemcpyAsync(xs[k], x_host[b], bytes, cudaMemcpyHostToDevice, hp->cin))) != MOE_OK) break;
+    if ((s = ck(cudaEventRecord(hp->h2d[k], hp->cin))) != MOE_OK) break;
+    if ((s = ck(cudaStreamWaitEvent(st, hp->h2d[k], 0))) != MOE_OK) break;
+    // output slot k is free once batch b-2's result has been copied out
+    if (b >= 2 && (s = ck(cudaStreamWaitEvent(st, hp->d2h[k], 0))) != MOE_OK) break;
+    if ((s = moe_layer_forward(c, w, xs[k], T, os[k], ws, lw, stream)) != MOE_OK) break;
+    if ((s = ck(cudaEventRecord(hp->fwd[k], st))) != MOE_OK) break;
+    if ((s = ck(cudaStreamWaitEvent(hp->cout, hp->fwd[k], 0))) != MOE_OK) break;
+    if ((s = ck(cudaMemcpyAsync(out_host[b], os[k], bytes, cudaMemcpyDeviceToHost, hp->cout))) != MOE_OK) break;
+    if ((s = ck(cudaEventRecord(hp->d2h[k], hp->cout))) != MOE_OK) break;
+  }
+  // join: the caller's stream completes after the last copy out (also on an error, so that
+  // nothing enqueued here outlives the stream)
+  int j = ck(cudaEventRecord(hp->end, hp->cout));
+  if (j == MOE_OK) j = ck(cudaStreamWaitEvent(st, hp->end, 0));
+  return s != MOE_OK ? s : j;
+}
+
 int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
   int s = check_config(c);
   if (s != MOE_OK) return s;

@@ -52,7 +52,7 @@ EXPORTS = ["moe_quantize_rowwise_fp8", "moe_expert_capacity", "moe_permuted_rows
            "moe_layer_forward_launches", "moe_workspace_layout", "moe_get_status", "moe_status_string",
            "moe_permute_noalloc", "moe_accumulate_counts", "moe_load_imbalance", "moe_score_bias_update",
            "moe_backward_workspace_size", "moe_combine_backward", "moe_grouped_swiglu_backward",
-           "moe_router_backward"]
+           "moe_router_backward", "moe_host_workspace_size", "moe_layer_forward_host_batches"]
 
 _lib = None
 
@@ -85,6 +85,8 @@ def load() -> ctypes.CDLL:
         "moe_layer_forward": [cfgp, wp, VP, I64, VP, VP, SZ, VP],
         "moe_layer_forward_staged": [cfgp, wp, VP, I64, VP, VP, SZ, VP, P(VP)],
         "moe_layer_forward_launches": [cfgp, I64, P(ctypes.c_int32)],
+        "moe_host_workspace_size": [cfgp, I64, P(SZ)],
+        "moe_layer_forward_host_batches": [cfgp, wp, P(VP), P(VP), ctypes.c_int32, I64, VP, SZ, VP],
         "moe_workspace_layout": [cfgp, I64, P(I64)],
         "moe_get_status": [VP, P(ctypes.c_int32), ctypes.c_int],
         "moe_status_string": [ctypes.c_int],
@@ -362,6 +364,40 @@ def moe_layer_forward(cfg, weights: DeviceWeights, x, ws, out=None, stream=None)
                                     _ptr(out, torch.bfloat16, "out"), _ptr(ws, None, "ws"), ws.numel(),
                                     _stream(stream)), "moe_layer_forward")
     return out
+
+
+def _host_ptr(t: torch.Tensor, name: str) -> int:
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if not t.is_contiguous() or t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be a contiguous bf16 tensor")
+    return t.data_ptr()
+
+
+def host_workspace(cfg: moe_config_t, T: int, device="cuda") -> torch.Tensor:
+    """A device workspace of moe_host_workspace_size bytes."""
+    n = ctypes.c_size_t()
+    _check(load().moe_host_workspace_size(ctypes.byref(cfg), T, ctypes.byref(n)), "moe_host_workspace_size")
+    return torch.empty(max(1, n.value), dtype=torch.uint8, device=device)
+
+
+def moe_layer_forward_host_batches(cfg, weights: DeviceWeights, x_hosts, out_hosts, ws, stream=None):
+    """The layer over host batches (lists of host (T, d_model) bf16 tensors, pinned for asynchronous
+    copies); outputs are complete once the stream is."""
+    if len(x_hosts) != len(out_hosts) or not x_hosts:
+        raise ValueError("x_hosts and out_hosts must be non-empty lists of the same length")
+    T = x_hosts[0].shape[0]
+    for x, o in zip(x_hosts, out_hosts):
+        if tuple(x.shape) != (T, cfg.d_model) or tuple(o.shape) != (T, cfg.d_model):
+            raise ValueError("every batch must be (T, d_model)")
+    n = len(x_hosts)
+    xs = (ctypes.c_void_p * n)(*[_host_ptr(x, "x_host") for x in x_hosts])
+    os_ = (ctypes.c_void_p * n)(*[_host_ptr(o, "out_host") for o in out_hosts])
+    ws_ = weights.struct()
+    _check(load().moe_layer_forward_host_batches(ctypes.byref(cfg), ctypes.byref(ws_), xs, os_, n, T,
+                                                 _ptr(ws, None, "ws"), ws.numel(), _stream(stream)),
+           "moe_layer_forward_host_batches")
+    return out_hosts
 
 
 STAGES = ["latent_down", "router_gemm", "topk", "permute", "gather", "grouped_gemm1_swiglu",

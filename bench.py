@@ -319,6 +319,14 @@ def run_native(args):
     for s, name in enumerate(native.STAGES, start=1):
         stage_ms[name] = sum(evs[i][s - 1].elapsed_time(evs[i][s]) for i in range(args.steps)) / args.steps
     ms = max_over_ranks(ms, dist, "cuda")
+    # the memory-bound stages against their own minimum bytes (inputs read once, outputs written once)
+    Lr, R, E_ = spec.routed_dim, spec.rows, spec.num_experts
+    stage_bytes = {
+        "topk": T * E_ * 4 + T * spec.top_k * 8,                   # fp32 logits in; idx + weights out
+        "permute": spec.T * spec.top_k * 4 + R * 8 + (2 * E_ + 1) * 4,   # idx in; gather, scatter, counts, offsets
+        "combine": R * Lr * 2 + spec.T * spec.top_k * 8 + T * Lr * 2,  # Y rows, scatter + weights in; z out
+    }
+    stage_gbs = {k: v / (stage_ms[k] * 1e-3) / 1e9 for k, v in stage_bytes.items() if stage_ms[k] > 0}
 
     # end to end: pinned host input -> device, forward, output -> pinned host, every step
     x_host = inp["x"].pin_memory()
@@ -468,6 +476,8 @@ def run_native(args):
                   "algorithmic_flops": flops, "algorithmic_bytes": alg_bytes,
                   "dropped_assignments": dropped},
         "stages_ms": stage_ms,
+        "stages_gbs": {"values": stage_gbs, "bytes": stage_bytes,
+                       "hbm_peak": peaks["hbm_gbs"], "note": "each stage's own minimum bytes"},
         "balance": bal,
         "backward": bwd,
         "roofline": {"kernel": "grouped GEMM 1 (SwiGLU fused, tcgen05" + (", e4m3 operands)" if spec.expert_fp8 else ")"),

@@ -264,6 +264,16 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
 // Each thread's copies for a stage end with a no-wait arrive on the CTA's gathered-rows barrier
 // of that stage (128 arrivals); gather_a_relay takes it from there.
 template <int ROWS, int NST, bool PAIR>
+__device__ __forceinline__ void gather_a_load_rows(const GemmParams& p, const TileCoord& c, int t, int rank,
+                                                   int (&tok)[8]) {
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int r = 128 * rank + (t >> 3) + 16 * j;   // row of the tile
+    tok[j] = r < c.rows ? __ldg(p.a_gather + c.row0 + r) : -1;
+  }
+}
+
+template <int ROWS, int NST, bool PAIR>
 __device__ __forceinline__ void gather_a_producer(const GemmParams& p, const int* s_toff, const int* s_goff,
                                                   int t_first, int t_step, int total_tiles, int rank, uint8_t* smem,
                                                   int stage_bytes, uint64_t* empty_bar, uint64_t* gath_bar,
@@ -273,22 +283,24 @@ __device__ __forceinline__ void gather_a_producer(const GemmParams& p, const int
   const int chunk = t & 7;
   uint32_t stage = 0, phase = 0;
   bool ok = true;
+  // the source rows of the next tile are loaded while the current one is copied
+  int nxt[8];
+  if (t_first < total_tiles)
+    gather_a_load_rows<ROWS, NST, PAIR>(p, decode_tile<ROWS>(t_first, p, s_toff, s_goff), t, rank, nxt);
   for (int tile = t_first; tile < total_tiles && ok; tile += t_step) {
     const TileCoord c = decode_tile<ROWS>(tile, p, s_toff, s_goff);
     int tok[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const int r = 128 * rank + (t >> 3) + 16 * j;   // row of the tile
-      int src = -1;
-      if (r < c.rows) {
-        src = __ldg(p.a_gather + c.row0 + r);
-        if (src < -1 || src >= p.a_src_rows) {
-          set_status(p.status, MOE_ERR_BOUNDS);
-          src = -1;
-        }
+      int src = nxt[j];
+      if (src < -1 || src >= p.a_src_rows) {
+        set_status(p.status, MOE_ERR_BOUNDS);
+        src = -1;
       }
       tok[j] = src;
     }
+    if (tile + t_step < total_tiles)
+      gather_a_load_rows<ROWS, NST, PAIR>(p, decode_tile<ROWS>(tile + t_step, p, s_toff, s_goff), t, rank, nxt);
     for (int kt = c.kt0; kt < c.kt1; ++kt) {
       int free_slot = 1;
       if (lane == 0)

@@ -71,43 +71,67 @@ __device__ int block_exclusive_scan(int v, int* s_warp) {
   return before + x - v;
 }
 
-// One block of 1024 threads: thread e owns expert e.
+// One block of 1024 threads.  G = 1024 / E (rounded down to a power of two, at most 32)
+// threads share expert e: thread g of the group takes a contiguous run of the per-chunk
+// histograms, and a shuffle scan across the group's lanes turns them into each chunk's
+// exclusive prefix within the expert.  Then an exclusive scan over the experts' totals gives
+// the offsets; the placement adds offsets[e] to the chunk prefixes itself.
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ blk, int nblk, int E,
                                                           int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ offsets) {
   __shared__ int s_warp[32];
-  const int e = threadIdx.x;
+  __shared__ int s_tot[1024];
+  int G = 1;
+  while (G < 32 && E * G * 2 <= 1024) G <<= 1;
+  const int t = threadIdx.x;
+  const int e = t / G, g = t % G;
+  const int per = (nblk + G - 1) / G;
+  const int b0 = min(nblk, g * per), b1 = min(nblk, b0 + per);
+  // pass 1: the total of this thread's chunks (loads issued eight at a time, no stores between)
   int run = 0;
   if (e < E) {
-    // eight independent loads in flight, then their running sums
-    int b = 0;
-    for (; b + 8 <= nblk; b += 8) {
+    for (int b = b0; b < b1; b += 8) {
       int c[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) c[i] = blk[(long long)(b + i) * E + e];
+      for (int i = 0; i < 8; ++i) c[i] = b + i < b1 ? blk[(long long)(b + i) * E + e] : 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) run += c[i];
+    }
+  }
+  // the group's G lanes are consecutive (G divides 32): inclusive scan of the run totals
+  int incl = run;
+  for (int o = 1; o < G; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o, G);
+    if (g >= o) incl += y;
+  }
+  // pass 2: each chunk's exclusive prefix within the expert (the group's earlier chunks first)
+  if (e < E) {
+    int acc = incl - run;
+    for (int b = b0; b < b1; b += 8) {
+      int c[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = b + i < b1 ? blk[(long long)(b + i) * E + e] : 0;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        blk[(long long)(b + i) * E + e] = run;
-        run += c[i];
+        if (b + i < b1) blk[(long long)(b + i) * E + e] = acc;
+        acc += c[i];
       }
     }
-    for (; b < nblk; ++b) {
-      const int c = blk[(long long)b * E + e];
-      blk[(long long)b * E + e] = run;
-      run += c;
-    }
-    counts[e] = run;
   }
-  const int excl = block_exclusive_scan(e < E ? run : 0, s_warp);
-  if (e < E) {
-    offsets[e] = excl;
-    if (e == E - 1) offsets[E] = excl + run;
-    for (int b = 0; b < nblk; ++b) blk[(long long)b * E + e] += excl;
+  if (e < E && g == G - 1) s_tot[e] = incl;
+  __syncthreads();
+  const int tot = t < E ? s_tot[t] : 0;
+  const int excl = block_exclusive_scan(tot, s_warp);
+  if (t < E) {
+    counts[t] = tot;
+    offsets[t] = excl;
+    if (t == E - 1) offsets[E] = excl + tot;
   }
 }
 
 __global__ void __launch_bounds__(kPermThreads) perm_place_kernel(const int32_t* __restrict__ idx, int R, int E,
                                                                    int k, int chunk, const int32_t* __restrict__ blk,
+                                                                   const int32_t* __restrict__ offsets,
                                                                    int32_t* __restrict__ gather_idx,
                                                                    int32_t* __restrict__ scatter_idx) {
   extern __shared__ int32_t wh[];  // [kPermWarps][E]
@@ -130,9 +154,9 @@ __global__ void __launch_bounds__(kPermThreads) perm_place_kernel(const int32_t*
     if (valid && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
   }
   __syncthreads();
-  // bases: the chunk's base for expert e plus the counts of earlier warps
+  // bases: expert e's offset, plus its rows in earlier chunks, plus the counts of earlier warps
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = blk[(long long)blockIdx.x * E + e];
+    int run = offsets[e] + blk[(long long)blockIdx.x * E + e];
     for (int w = 0; w < kPermWarps; ++w) {
       const int c = wh[w * E + e];
       wh[w * E + e] = run;
@@ -170,7 +194,7 @@ cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, in
   perm_scan_kernel<<<1, 1024, 0, stream>>>(blk, nb, E, counts, offsets);
   if (nb > 0) {
     const size_t sm = (size_t)kPermWarps * E * sizeof(int32_t);
-    perm_place_kernel<<<nb, kPermThreads, sm, stream>>>(idx, R, E, k, chunk, blk, gather_idx, scatter_idx);
+    perm_place_kernel<<<nb, kPermThreads, sm, stream>>>(idx, R, E, k, chunk, blk, offsets, gather_idx, scatter_idx);
   }
   return cudaGetLastError();
 }

@@ -59,6 +59,8 @@ __global__ void __launch_bounds__(32 * kRowWarps)
     combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ scatter_idx, const float* __restrict__ w,
                    int T, int k, int vec, int R, float eps, const uint4* __restrict__ gain, uint4* __restrict__ z,
                    int allow_dropped, int* status) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   extern __shared__ uint4 zs_all[];
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -128,6 +130,8 @@ __global__ void __launch_bounds__(32 * kRowWarps)
 __global__ void __launch_bounds__(32 * kRowWarps)
     rmsnorm_kernel(const uint4* __restrict__ z, int T, int vec, float eps, const uint4* __restrict__ gain,
                    uint4* __restrict__ out) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long t = (long long)blockIdx.x * kRowWarps + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -146,6 +150,8 @@ __global__ void __launch_bounds__(32 * kRowWarps)
 
 __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __restrict__ part, int splits,
                                                              long long slice4, uint2* __restrict__ out) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < slice4;
        i += (long long)gridDim.x * blockDim.x) {
     float4 a = part[i];
@@ -169,11 +175,11 @@ cudaError_t launch_combine(const void* y, const int32_t* scatter_idx, const floa
       cudaError_t e = cudaFuncSetAttribute(combine_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
       if (e != cudaSuccess) return e;
     }
-    combine_kernel<true><<<grid, block, sm, stream>>>(static_cast<const uint4*>(y), scatter_idx, w, T, k, vec, R,
+    launch_pdl(combine_kernel<true>, grid, block, sm, stream, static_cast<const uint4*>(y), scatter_idx, w, T, k, vec, R,
                                                       eps, static_cast<const uint4*>(gain), static_cast<uint4*>(z),
                                                       allow_dropped, status);
   } else {
-    combine_kernel<false><<<grid, block, 0, stream>>>(static_cast<const uint4*>(y), scatter_idx, w, T, k, vec, R,
+    launch_pdl(combine_kernel<false>, grid, block, 0, stream, static_cast<const uint4*>(y), scatter_idx, w, T, k, vec, R,
                                                       eps, nullptr, static_cast<uint4*>(z), allow_dropped, status);
   }
   return cudaGetLastError();
@@ -181,7 +187,7 @@ cudaError_t launch_combine(const void* y, const int32_t* scatter_idx, const floa
 
 cudaError_t launch_rmsnorm(const void* z, int T, int L, float eps, const void* gain, void* out, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  rmsnorm_kernel<<<(T + kRowWarps - 1) / kRowWarps, 32 * kRowWarps, 0, stream>>>(
+  launch_pdl(rmsnorm_kernel, (T + kRowWarps - 1) / kRowWarps, 32 * kRowWarps, 0, stream, 
       static_cast<const uint4*>(z), T, L / 8, eps, static_cast<const uint4*>(gain), static_cast<uint4*>(out));
   return cudaGetLastError();
 }
@@ -191,7 +197,7 @@ cudaError_t launch_splitk_reduce_bf16(const float* partials, int splits, int64_t
   const long long slice4 = slice / 4;
   if (slice4 <= 0) return cudaSuccess;
   const int blocks = (int)std::min<long long>((slice4 + 255) / 256, 4096);
-  splitk_reduce_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(partials), splits, slice4,
+  launch_pdl(splitk_reduce_kernel, blocks, 256, 0, stream, reinterpret_cast<const float4*>(partials), splits, slice4,
                                                    static_cast<uint2*>(out));
   return cudaGetLastError();
 }

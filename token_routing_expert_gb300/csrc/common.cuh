@@ -117,6 +117,31 @@ __device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cluster_add
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch: a kernel launched with launch_pdl may be scheduled while the
+// previous kernel on its stream is still finishing.  Every such kernel calls pdl_wait() before it
+// touches memory (it returns once the previous kernel has completed and its writes are visible,
+// immediately when there is none) and then pdl_trigger(), which lets the next kernel be scheduled.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // cp.async (16-byte copies into shared memory) and the proxy fence that makes
 // them visible to tensor-core (async proxy) reads
 // ---------------------------------------------------------------------------

@@ -17,6 +17,8 @@ namespace moe {
 __global__ void __launch_bounds__(256) quantize_rowwise_e4m3_kernel(const uint4* __restrict__ x, long long rows,
                                                                      int vec, uint2* __restrict__ q,
                                                                      float* __restrict__ scale) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long r = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (r >= rows) return;
@@ -54,7 +56,7 @@ cudaError_t launch_quantize_rowwise_e4m3(const void* x, long long rows, int cols
   if (rows <= 0) return cudaSuccess;
   if (cols % 8) return cudaErrorInvalidValue;
   const long long blocks = (rows + 7) / 8;
-  quantize_rowwise_e4m3_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const uint4*>(x), rows, cols / 8,
+  launch_pdl(quantize_rowwise_e4m3_kernel, (unsigned)blocks, 256, 0, st, static_cast<const uint4*>(x), rows, cols / 8,
                                                                  static_cast<uint2*>(q), scale);
   return cudaGetLastError();
 }
@@ -67,6 +69,8 @@ __global__ void __launch_bounds__(256) gather_rows_e4m3_kernel(const uint4* __re
                                                                 int vec, uint4* __restrict__ dst,
                                                                 float* __restrict__ dst_scale, int allow_padding,
                                                                 int* status) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (p >= R) return;
@@ -99,7 +103,7 @@ cudaError_t launch_gather_rows_e4m3(const void* src, const float* src_scale, con
                                     cudaStream_t st) {
   if (R <= 0) return cudaSuccess;
   if (row_bytes % 16) return cudaErrorInvalidValue;
-  gather_rows_e4m3_kernel<<<(R + 7) / 8, 256, 0, st>>>(static_cast<const uint4*>(src), src_scale, gather_idx, R, T,
+  launch_pdl(gather_rows_e4m3_kernel, (R + 7) / 8, 256, 0, st, static_cast<const uint4*>(src), src_scale, gather_idx, R, T,
                                                        row_bytes / 16, static_cast<uint4*>(dst), dst_scale,
                                                        allow_padding, status);
   return cudaGetLastError();

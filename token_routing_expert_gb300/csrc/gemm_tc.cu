@@ -360,6 +360,8 @@ template <int BN, int EPI, bool F8 = false, bool GA = false>
 __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   using C = GemmCfg<BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -558,6 +560,8 @@ template <int EPI, bool F8 = false, bool GA = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmParams p) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   using C = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -799,7 +803,7 @@ static cudaError_t launch_impl(const GemmProblem& q, const CUtensorMap& ta, cons
     attr_set = true;
   }
   (void)q;
-  kern<<<grid, GA ? kThreadsGA : kThreads, C::SMEM_BYTES, stream>>>(ta, tb, gp);
+  launch_pdl(kern, grid, GA ? kThreadsGA : kThreads, C::SMEM_BYTES, stream, ta, tb, gp);
   return cudaGetLastError();
 }
 
@@ -832,7 +836,7 @@ static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb
   }
   int pairs = max_pairs;
   if (tiles > 0) pairs = std::min(pairs, tiles);
-  kern<<<2 * pairs, threads, PairCfg::SMEM_BYTES, stream>>>(ta, tb, gp);
+  launch_pdl(kern, 2 * pairs, threads, PairCfg::SMEM_BYTES, stream, ta, tb, gp);
   return cudaGetLastError();
 }
 

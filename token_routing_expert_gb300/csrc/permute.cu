@@ -32,6 +32,8 @@ int permute_chunk(int R) {
 __global__ void __launch_bounds__(kPermThreads) perm_count_kernel(const int32_t* __restrict__ idx, int R, int E,
                                                                    int chunk, int32_t* __restrict__ blk,
                                                                    int* status) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   extern __shared__ int32_t hist[];
   for (int i = threadIdx.x; i < E; i += blockDim.x) hist[i] = 0;
   __syncthreads();
@@ -79,6 +81,8 @@ __device__ int block_exclusive_scan(int v, int* s_warp) {
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ blk, int nblk, int E,
                                                           int32_t* __restrict__ counts,
                                                           int32_t* __restrict__ offsets) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   __shared__ int s_warp[32];
   __shared__ int s_tot[1024];
   int G = 1;
@@ -134,6 +138,8 @@ __global__ void __launch_bounds__(kPermThreads) perm_place_kernel(const int32_t*
                                                                    const int32_t* __restrict__ offsets,
                                                                    int32_t* __restrict__ gather_idx,
                                                                    int32_t* __restrict__ scatter_idx) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   extern __shared__ int32_t wh[];  // [kPermWarps][E]
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) wh[i] = 0;
@@ -189,12 +195,12 @@ cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, in
   if (chunk < 256 || chunk > kMaxChunk || chunk % 256) return cudaErrorInvalidValue;
   const int nb = permute_blocks(R, chunk);
   if (nb > 0) {
-    perm_count_kernel<<<nb, kPermThreads, E * sizeof(int32_t), stream>>>(idx, R, E, chunk, blk, status);
+    launch_pdl(perm_count_kernel, nb, kPermThreads, E * sizeof(int32_t), stream, idx, R, E, chunk, blk, status);
   }
-  perm_scan_kernel<<<1, 1024, 0, stream>>>(blk, nb, E, counts, offsets);
+  launch_pdl(perm_scan_kernel, 1, 1024, 0, stream, blk, nb, E, counts, offsets);
   if (nb > 0) {
     const size_t sm = (size_t)kPermWarps * E * sizeof(int32_t);
-    perm_place_kernel<<<nb, kPermThreads, sm, stream>>>(idx, R, E, k, chunk, blk, offsets, gather_idx, scatter_idx);
+    launch_pdl(perm_place_kernel, nb, kPermThreads, sm, stream, idx, R, E, k, chunk, blk, offsets, gather_idx, scatter_idx);
   }
   return cudaGetLastError();
 }
@@ -202,6 +208,8 @@ cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, in
 // tile_off[e] = sum over e' < e of ceil(count[e'] / rows_per_tile); tile_off[E] = total tiles.
 __global__ void __launch_bounds__(1024) tile_table_kernel(const int32_t* __restrict__ offsets, int E, int rows_per_tile,
                                                            int32_t* __restrict__ tile_off) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   __shared__ int s_warp[32];
   const int e = threadIdx.x;
   const int tiles = e < E ? (offsets[e + 1] - offsets[e] + rows_per_tile - 1) / rows_per_tile : 0;
@@ -214,7 +222,7 @@ __global__ void __launch_bounds__(1024) tile_table_kernel(const int32_t* __restr
 
 cudaError_t launch_tile_table(const int32_t* offsets, int E, int rows_per_tile, int32_t* tile_off,
                               cudaStream_t stream) {
-  tile_table_kernel<<<1, 1024, 0, stream>>>(offsets, E, rows_per_tile, tile_off);
+  launch_pdl(tile_table_kernel, 1, 1024, 0, stream, offsets, E, rows_per_tile, tile_off);
   return cudaGetLastError();
 }
 
@@ -223,6 +231,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                            const int32_t* __restrict__ gather_idx, int R, int T,
                                                            int vec_per_row, uint4* __restrict__ dst,
                                                            int allow_padding, int* status) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (p >= R) return;
@@ -254,7 +264,7 @@ cudaError_t launch_gather_rows(const void* src, const int32_t* gather_idx, int R
                                int allow_padding, int* status, cudaStream_t stream) {
   if (R <= 0) return cudaSuccess;
   const int warps = 8;
-  gather_rows_kernel<<<(R + warps - 1) / warps, 32 * warps, 0, stream>>>(
+  launch_pdl(gather_rows_kernel, (R + warps - 1) / warps, 32 * warps, 0, stream, 
       static_cast<const uint4*>(src), gather_idx, R, T, cols / 8, static_cast<uint4*>(dst), allow_padding, status);
   return cudaGetLastError();
 }
@@ -271,6 +281,8 @@ __global__ void __launch_bounds__(256) capacity_remap_kernel(const int32_t* __re
                                                               int32_t* __restrict__ offsets,
                                                               int32_t* __restrict__ gather_idx,
                                                               int32_t* __restrict__ scatter_idx) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   const long long slots = (long long)E * cap;
   const long long n = max(max(slots, (long long)R), (long long)E + 1);
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
@@ -298,7 +310,7 @@ cudaError_t launch_capacity_remap(const int32_t* idx, int R, int E, int cap, con
                                   int32_t* scatter_idx, cudaStream_t stream) {
   const long long n = std::max(std::max((long long)E * cap, (long long)R), (long long)E + 1);
   const int blocks = (int)std::min<long long>((n + 255) / 256, 4096);
-  capacity_remap_kernel<<<blocks, 256, 0, stream>>>(idx, R, E, cap, counts, off_dense, gather_dense, scatter_dense,
+  launch_pdl(capacity_remap_kernel, blocks, 256, 0, stream, idx, R, E, cap, counts, off_dense, gather_dense, scatter_dense,
                                                     offsets, gather_idx, scatter_idx);
   return cudaGetLastError();
 }

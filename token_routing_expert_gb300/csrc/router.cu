@@ -73,6 +73,8 @@ __device__ __forceinline__ void bitonic_step(float& k, int& e, float& w, int lan
 
 template <int NI>
 __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(const TopkParams p) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   __shared__ float s_key[kTopkWarps][kCand];
   __shared__ int s_e[kTopkWarps][kCand];
   __shared__ float s_w[kTopkWarps][kCand];
@@ -259,6 +261,8 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(const TopkParams 
 // logits[t, e] = sum over s of partials[s, t, e], in a fixed order (split-K router GEMM).
 __global__ void __launch_bounds__(256) sum_partials_kernel(const float4* __restrict__ part, int splits,
                                                             long long n4, float4* __restrict__ out) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
     float4 a = part[i];
     for (int s = 1; s < splits; ++s) {
@@ -273,7 +277,7 @@ cudaError_t launch_sum_slices_f32(const float* part, int splits, long long n, fl
   const long long n4 = n / 4;
   if (n4 <= 0) return cudaSuccess;
   const int blocks = (int)std::min<long long>((n4 + 255) / 256, 2048);
-  sum_partials_kernel<<<blocks, 256, 0, st>>>(reinterpret_cast<const float4*>(part), splits, n4,
+  launch_pdl(sum_partials_kernel, blocks, 256, 0, st, reinterpret_cast<const float4*>(part), splits, n4,
                                               reinterpret_cast<float4*>(out));
   return cudaGetLastError();
 }
@@ -289,7 +293,7 @@ cudaError_t launch_topk(const float* logits, int n_partials, int64_t partial_str
     float* sum = const_cast<float*>(logits) + (int64_t)n_partials * partial_stride;
     const long long n4 = partial_stride / 4;
     const int blocks = (int)std::min<long long>((n4 + 255) / 256, 2048);
-    sum_partials_kernel<<<blocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(logits), n_partials, n4,
+    launch_pdl(sum_partials_kernel, blocks, 256, 0, stream, reinterpret_cast<const float4*>(logits), n_partials, n4,
                                                     reinterpret_cast<float4*>(sum));
     logits = sum;
   }
@@ -297,13 +301,13 @@ cudaError_t launch_topk(const float* logits, int n_partials, int64_t partial_str
                restore, ews, orig_k, logits_out, idx, w, status};
   dim3 grid((T + kTopkWarps - 1) / kTopkWarps), block(32 * kTopkWarps);
   const int ni = (E + 31) / 32;
-  if (ni <= 1) topk_kernel<1><<<grid, block, 0, stream>>>(p);
-  else if (ni <= 2) topk_kernel<2><<<grid, block, 0, stream>>>(p);
-  else if (ni <= 4) topk_kernel<4><<<grid, block, 0, stream>>>(p);
-  else if (ni <= 8) topk_kernel<8><<<grid, block, 0, stream>>>(p);
-  else if (ni <= 16) topk_kernel<16><<<grid, block, 0, stream>>>(p);
-  else if (ni <= 28) topk_kernel<28><<<grid, block, 0, stream>>>(p);
-  else if (ni <= 32) topk_kernel<32><<<grid, block, 0, stream>>>(p);
+  if (ni <= 1) launch_pdl(topk_kernel<1>, grid, block, 0, stream, p);
+  else if (ni <= 2) launch_pdl(topk_kernel<2>, grid, block, 0, stream, p);
+  else if (ni <= 4) launch_pdl(topk_kernel<4>, grid, block, 0, stream, p);
+  else if (ni <= 8) launch_pdl(topk_kernel<8>, grid, block, 0, stream, p);
+  else if (ni <= 16) launch_pdl(topk_kernel<16>, grid, block, 0, stream, p);
+  else if (ni <= 28) launch_pdl(topk_kernel<28>, grid, block, 0, stream, p);
+  else if (ni <= 32) launch_pdl(topk_kernel<32>, grid, block, 0, stream, p);
   else return cudaErrorInvalidValue;
   return cudaGetLastError();
 }

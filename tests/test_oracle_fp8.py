@@ -34,3 +34,12 @@ def test_rowwise_quantiser_invariants():
     np.testing.assert_array_equal(np.abs(q[np.arange(50) != 7]).max(axis=1), 448.0)   # each row's max hits 448
     rel = np.abs(q * s[:, None] - x) / np.maximum(np.abs(x), 1e-30)
     assert (rel[np.abs(x) > s[:, None] * 2.0 ** -6] <= 2.0 ** -4 + 1e-6).all()         # e4m3: 3 mantissa bits
+
+
+def test_fp8_ambiguity_band_flags_rows_at_a_rounding_midpoint():
+    # bf16 keeps 8 significant bits: 1 + 2^-8 lies exactly halfway between 1 and 1 + 2^-7
+    from tests.oracle_bridge import _amax_ambiguous
+    rows = np.array([[0.5, 1.0 + 2.0 ** -8, -0.25],     # amax on a midpoint: either neighbour
+                     [0.5, 1.0 + 2.0 ** -7, -0.25],     # amax exactly representable
+                     [0.5, -(1.0 + 2.0 ** -8), 0.25]])  # the sign does not matter
+    np.testing.assert_array_equal(_amax_ambiguous(rows, 1e-5), [True, False, True])

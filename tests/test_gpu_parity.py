@@ -54,6 +54,10 @@ CASES = {
                                         hidden_size=320, gating="sigmoid", normalize_expert_weights=1.0, seed=21),
     "pair_tiles_latent": WorkloadSpec("pair_tiles_latent", T=2000, d_model=768, num_experts=4, top_k=2,
                                       hidden_size=192, latent_dim=256, gating="softmax", skew=True, seed=22),
+    # >= 1024 tokens and > 128 experts: the router GEMM runs on CTA pairs with 256-column fp32
+    # tiles, the last one ragged (320 = 256 + 64)
+    "router_pair": WorkloadSpec("router_pair", T=1500, d_model=512, num_experts=320, top_k=4, hidden_size=64,
+                                gating="sigmoid", score_bias_std=0.01, seed=23),
 }
 
 _cache = {}

@@ -207,6 +207,7 @@ int dense_gemm_bf16(const void* A, const void* B, int M, int N, int K, void* out
   q.out = out;
   q.ldo = N;
   q.split_stride = 0;
+  q.pair_tiles = M >= 1024 ? 1 : 0;   // 256-row tiles on CTA pairs: half the B bytes per CTA
   return cuda_status(launch_gemm(q, st));
 }
 
@@ -228,6 +229,10 @@ int run_router(const moe_config_t* c, const moe_weights_t* w, const void* x, con
   q.epilogue = EPI_F32;
   q.bn = p.router_bn;
   q.splits = p.router_splits;
+  if (p.router_splits == 1 && p.T >= 1024 && p.E > 128) {   // many experts: 256 x 256 tiles on CTA pairs
+    q.bn = 256;
+    q.pair_tiles = 1;
+  }
   q.out = gemm_out;
   q.ldo = p.E;
   q.split_stride = p.logit_slice;

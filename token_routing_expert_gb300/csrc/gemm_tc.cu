@@ -846,7 +846,8 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   const bool pair = q.pair_tiles != 0;
   const bool f8 = q.e4m3 != 0;
-  if (pair && (q.bn != 256 || q.splits > 1 || q.epilogue == EPI_F32)) return cudaErrorInvalidValue;
+  if (pair && (q.bn != 256 || q.splits > 1 || (q.epilogue == EPI_F32 && (q.e4m3 || q.num_groups > 0))))
+    return cudaErrorInvalidValue;
   if (f8 && (q.bn != 256 || q.splits > 1 || q.k_groups > 0 || q.epilogue == EPI_F32 || !q.a_scale || !q.b_scale))
     return cudaErrorInvalidValue;
   // gathered A: grouped SwiGLU only; A rows are copied from a_src by the kernel, no A tensor map
@@ -904,6 +905,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
       return launch_pair_impl<EPI_BF16, true>(ta, tb, gp, tiles, stream);
     }
     if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU>(ta, tb, gp, tiles, stream);
+    if (q.epilogue == EPI_F32) return launch_pair_impl<EPI_F32>(ta, tb, gp, tiles, stream);   // dense fp32 out
     return launch_pair_impl<EPI_BF16>(ta, tb, gp, tiles, stream);
   }
   int grid = num_sms();

@@ -58,6 +58,10 @@ CASES = {
     # tiles, the last one ragged (320 = 256 + 64)
     "router_pair": WorkloadSpec("router_pair", T=1500, d_model=512, num_experts=320, top_k=4, hidden_size=64,
                                 gating="sigmoid", score_bias_std=0.01, seed=23),
+    # 40 row tiles of the router GEMM: a 2-way split-K whose slices top-k adds itself (deeper splits,
+    # as in one_token, go through the separate sum)
+    "router_split2": WorkloadSpec("router_split2", T=5000, d_model=512, num_experts=48, top_k=4, hidden_size=64,
+                                  gating="topk_softmax", seed=24),
 }
 
 _cache = {}
@@ -317,6 +321,6 @@ def test_staged_forward_matches_and_records_every_stage(name):
     assert all(t >= 0 for t in times) and times[5] > 0   # grouped GEMM 1 took time
     n = native.moe_layer_forward_launches(cfg, spec.T)
     # 9 kernels on CTA-pair tiles (10 with 128-row tiles, which copy the routed rows first); a
-    # latent layer adds the two projections, each with a split-K reduce when split, and a
-    # split-K router adds the partial-logit sum
+    # latent layer adds the two projections, each with a split-K reduce when split, and a deep
+    # split-K router the sum of its partial logits (top-k adds up to 4 slices itself)
     assert 9 <= n <= 11 if not spec.latent_dim else 11 <= n <= 15

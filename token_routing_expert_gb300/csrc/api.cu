@@ -96,9 +96,11 @@ void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
     o += align256(bytes);
     return at;
   };
-  // split-K: router_splits partial slices plus one for their sum (slices padded to 16 bytes)
+  // split-K: router_splits partial slices (padded to 16 bytes); top-k adds up to kTopkFusedSlices
+  // of them itself, a deeper split gets one more slice for their sum
   p->logit_slice = ((int64_t)T * p->E + 3) & ~int64_t(3);
-  p->logits = take((size_t)(p->router_splits > 1 ? p->router_splits + 1 : 1) * p->logit_slice * 4);
+  const int slices = p->router_splits > kTopkFusedSlices ? p->router_splits + 1 : std::max(1, p->router_splits);
+  p->logits = take((size_t)slices * p->logit_slice * 4);
   p->idx = take((size_t)p->R * 4);
   p->wts = take((size_t)p->R * 4);
   p->counts = take((size_t)p->E * 4);
@@ -876,7 +878,7 @@ int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
   make_plan(c, T, std::min(num_sms(), kSizingSms), &p);
   int k = 0;
   if (p.latent) k += p.down_splits > 1 ? 2 : 1;  // latent down (+ split-K reduce)
-  k += p.router_splits > 1 ? 3 : 2;              // router GEMM, (split-K sum,) top-k
+  k += p.router_splits > kTopkFusedSlices ? 3 : 2;   // router GEMM, (sum of a deep split-K,) top-k
   k += p.capacity ? 4 : 3;                       // permute: count, scan, place (, capacity slots)
   k += use_pair_tiles(p) ? 1 : 2;                // tile table (+ row gather for 128-row tiles;
                                                  // on CTA pairs grouped GEMM 1 gathers its rows)

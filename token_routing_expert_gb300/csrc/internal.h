@@ -52,6 +52,9 @@ int pick_bn_f32(int n_cols);
 // split-K factor that fills the GPU for a dense GEMM with `tiles` output tiles and K.
 int pick_splits(int tiles, int K);
 
+// Split-K router slices that top-k adds up itself; with more, logits must hold one more slice
+// (partial_stride floats) for their sum.
+constexpr int kTopkFusedSlices = 4;
 cudaError_t launch_topk(const float* logits, int n_partials, int64_t partial_stride, const float* b_router,
                         const float* score_bias, int T, int E, int k, int gating, float sig_eps, float p_norm,
                         int restore, float ews, int orig_k, float* logits_out, int32_t* idx, float* w,

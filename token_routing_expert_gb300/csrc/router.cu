@@ -7,7 +7,7 @@
 // below, the keys >= tau (usually about k of them) are compacted with ballots
 // and ordered by one warp bitonic sort; more than 32 candidates (many equal
 // keys) fall back to k rounds of warp arg-max over all keys.  Split-K partial
-// logits are summed first, in a fixed order.
+// logits are summed as they are loaded, in slice order.
 // Page "Как устроен Olmo-core 3: обучение больших MoE-моделей",
 // §"Маршрутизация: как роутер выбирает экспертов" and
 // §"Разрешение равенства логитов и квантизация".
@@ -21,7 +21,9 @@
 namespace moe {
 
 struct TopkParams {
-  const float* logits;
+  const float* logits;         // n_partials slices, partial_stride floats apart (split-K), summed in order
+  int n_partials;
+  long long partial_stride;
   const float* b_router;
   const float* score_bias;
   int T, E, k, gating;
@@ -85,13 +87,22 @@ __global__ void __launch_bounds__(32 * kTopkWarps) topk_kernel(const TopkParams 
   const int E = p.E;
   const long long row = (long long)t * E;
 
-  // all NI loads of a lane are independent and issue back to back
+  // all NI loads of a lane are independent and issue back to back; split-K partial slices are
+  // added in slice order
   float lg[NI], key[NI], src[NI];
   const float* lrow = p.logits + row;
 #pragma unroll
   for (int i = 0; i < NI; ++i) {
     const int e = lane + 32 * i;
     lg[i] = e < E ? __ldg(lrow + e) : 0.f;
+  }
+  for (int sl = 1; sl < p.n_partials; ++sl) {
+    const float* prow = lrow + sl * p.partial_stride;
+#pragma unroll
+    for (int i = 0; i < NI; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) lg[i] += __ldg(prow + e);
+    }
   }
   if (p.b_router) {
 #pragma unroll
@@ -287,18 +298,20 @@ cudaError_t launch_topk(const float* logits, int n_partials, int64_t partial_str
                         int restore, float ews, int orig_k, float* logits_out, int32_t* idx, float* w,
                         int* status, cudaStream_t stream) {
   if (T <= 0) return cudaSuccess;
-  if (n_partials > 1) {
-    // the caller's buffer holds n_partials + 1 slices of partial_stride (a multiple of 4)
-    // floats; the sum goes to the last slice, and top-k copies it to logits_out if asked
+  // split-K: up to kTopkFusedSlices slices the kernel adds them itself as it loads; more (few
+  // tokens, a deep split) are first summed by a grid-wide kernel into the slice after the last
+  // one, which the caller's buffer then holds
+  if (n_partials > kTopkFusedSlices) {
     float* sum = const_cast<float*>(logits) + (int64_t)n_partials * partial_stride;
     const long long n4 = partial_stride / 4;
     const int blocks = (int)std::min<long long>((n4 + 255) / 256, 2048);
     launch_pdl(sum_partials_kernel, blocks, 256, 0, stream, reinterpret_cast<const float4*>(logits), n_partials, n4,
-                                                    reinterpret_cast<float4*>(sum));
+               reinterpret_cast<float4*>(sum));
     logits = sum;
+    n_partials = 1;
   }
-  TopkParams p{logits, b_router, score_bias, T, E, k, gating, sig_eps, p_norm,
-               restore, ews, orig_k, logits_out, idx, w, status};
+  TopkParams p{logits, std::max(1, n_partials), (long long)partial_stride, b_router, score_bias, T, E, k, gating,
+               sig_eps, p_norm, restore, ews, orig_k, logits_out, idx, w, status};
   dim3 grid((T + kTopkWarps - 1) / kTopkWarps), block(32 * kTopkWarps);
   const int ni = (E + 31) / 32;
   if (ni <= 1) launch_pdl(topk_kernel<1>, grid, block, 0, stream, p);

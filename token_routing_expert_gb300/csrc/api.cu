@@ -255,7 +255,7 @@ int run_router(const moe_config_t* c, const moe_weights_t* w, const void* x, con
 // permuted order (SwiGLU, scales in the epilogue) -> H bf16, quantise H per row, GEMM 2.
 int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
                     const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
-                    cudaEvent_t* ev) {
+                    cudaEvent_t* ev, bool tiles_ready) {
   int32_t* tile_off = at<int32_t>(ws, p.tile_off);
   void* H = at<void>(ws, p.H);
   void* xq = at<void>(ws, p.xq);
@@ -263,7 +263,7 @@ int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* x
   void* hq = at<void>(ws, p.hq);
   float* hs = at<float>(ws, p.hs);
   const int pair = use_pair_tiles(p);
-  int s = cuda_status(launch_tile_table(offsets, p.E, pair ? 256 : 128, tile_off, st));
+  int s = tiles_ready ? MOE_OK : cuda_status(launch_tile_table(offsets, p.E, pair ? 256 : 128, tile_off, st));
   if (s == MOE_OK) s = cuda_status(launch_quantize_rowwise_e4m3(xr, p.T, p.Lr, xq, xs, st));
   if (s == MOE_OK && !pair)   // 128-row tiles: a permuted copy of the code rows and their scales
     s = cuda_status(launch_gather_rows_e4m3(xq, xs, gather, (int)p.rows, (int)p.T, p.Lr, at<void>(ws, p.xpq),
@@ -329,16 +329,17 @@ int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* x
   return MOE_OK;
 }
 
+// tiles_ready: the tile table in the workspace was already written (by run_permute).
 int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
                 const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
-                cudaEvent_t* ev = nullptr) {
+                cudaEvent_t* ev = nullptr, bool tiles_ready = false) {
   int32_t* tile_off = at<int32_t>(ws, p.tile_off);
   void* H = at<void>(ws, p.H);
-  if (c->expert_fp8) return run_experts_fp8(c, w, xr, gather, offsets, p, y, ws, status, st, ev);
+  if (c->expert_fp8) return run_experts_fp8(c, w, xr, gather, offsets, p, y, ws, status, st, ev, tiles_ready);
   // large groups run on CTA pairs with 256-row tiles; small ones keep 128-row tiles,
   // which waste less of the last partial tile of each group
   const int pair = use_pair_tiles(p);
-  int s = cuda_status(launch_tile_table(offsets, p.E, pair ? 256 : 128, tile_off, st));
+  int s = tiles_ready ? MOE_OK : cuda_status(launch_tile_table(offsets, p.E, pair ? 256 : 128, tile_off, st));
   if (s != MOE_OK) return s;
   // CTA-pair tiles: GEMM 1 copies the rows of x_routed in permuted order itself (cp.async into
   // its A stages).  128-row tiles read a permuted copy through TMA.  (A TMA tile::gather4 A-load
@@ -402,11 +403,19 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
 }
 
 // The permutation, dense or into capacity slots.
+// tiles_done (optional): the dropless permutation also writes the grouped GEMMs' tile table into
+// the workspace, and *tiles_done says so.
 int run_permute(const int32_t* idx, const Plan& p, int32_t* counts, int32_t* offsets, int32_t* gather,
-                int32_t* scatter, void* ws, int* status, cudaStream_t st) {
-  if (!p.capacity)
-    return cuda_status(launch_permute(idx, (int)p.R, p.E, counts, offsets, gather, scatter, p.k,
-                                      permute_chunk((int)p.R), at<int32_t>(ws, p.blk), status, st));
+                int32_t* scatter, void* ws, int* status, cudaStream_t st, bool* tiles_done = nullptr) {
+  if (tiles_done) *tiles_done = false;
+  if (!p.capacity) {
+    int32_t* tile_off = tiles_done ? at<int32_t>(ws, p.tile_off) : nullptr;
+    const int s = cuda_status(launch_permute(idx, (int)p.R, p.E, counts, offsets, gather, scatter, p.k,
+                                             permute_chunk((int)p.R), at<int32_t>(ws, p.blk), status, st,
+                                             use_pair_tiles(p) ? 256 : 128, tile_off));
+    if (s == MOE_OK && tiles_done) *tiles_done = true;
+    return s;
+  }
   int32_t* gd = at<int32_t>(ws, p.gdense);
   int32_t* sd = at<int32_t>(ws, p.sdense);
   int32_t* od = at<int32_t>(ws, p.odense);
@@ -746,11 +755,12 @@ int moe_layer_forward_staged(const moe_config_t* c, const moe_weights_t* w, cons
   int32_t* offsets = at<int32_t>(ws, p.offsets);
   int32_t* gather = at<int32_t>(ws, p.gather);
   int32_t* scatter = at<int32_t>(ws, p.scatter);
-  s = run_permute(idx, p, counts, offsets, gather, scatter, ws, status, st);
+  bool tiles_ready = false;
+  s = run_permute(idx, p, counts, offsets, gather, scatter, ws, status, st, &tiles_ready);
   if (s != MOE_OK) return s;
   mark(ev, 4, st);
   void* Y = at<void>(ws, p.Y);
-  s = run_experts(c, w, xr, gather, offsets, p, Y, ws, status, st, ev);
+  s = run_experts(c, w, xr, gather, offsets, p, Y, ws, status, st, ev, tiles_ready);
   if (s != MOE_OK) return s;
   if (!p.latent) {
     s = cuda_status(launch_combine(Y, scatter, wts, (int)T, p.k, p.Lr, (int)p.rows, 0, 0.f, nullptr, out,
@@ -880,8 +890,9 @@ int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
   if (p.latent) k += p.down_splits > 1 ? 2 : 1;  // latent down (+ split-K reduce)
   k += p.router_splits > kTopkFusedSlices ? 3 : 2;   // router GEMM, (sum of a deep split-K,) top-k
   k += p.capacity ? 4 : 3;                       // permute: count, scan, place (, capacity slots)
-  k += use_pair_tiles(p) ? 1 : 2;                // tile table (+ row gather for 128-row tiles;
-                                                 // on CTA pairs grouped GEMM 1 gathers its rows)
+  k += p.capacity ? 1 : 0;                       // tile table (the dropless scan writes it itself)
+  k += use_pair_tiles(p) ? 0 : 1;                // row gather for 128-row tiles (on CTA pairs grouped
+                                                 // GEMM 1 gathers its rows)
   k += 2;                                        // grouped GEMM 1 (SwiGLU), grouped GEMM 2
   if (c->expert_fp8) k += 2;                     // e4m3 quantisation of x_routed and of H
   k += 1;                                        // combine (+ RMSNorm when latent)

@@ -80,7 +80,8 @@ __device__ int block_exclusive_scan(int v, int* s_warp) {
 // the offsets; the placement adds offsets[e] to the chunk prefixes itself.
 __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ blk, int nblk, int E,
                                                           int32_t* __restrict__ counts,
-                                                          int32_t* __restrict__ offsets) {
+                                                          int32_t* __restrict__ offsets, int rows_per_tile,
+                                                          int32_t* __restrict__ tile_off) {
   pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
   pdl_trigger();
   __shared__ int s_warp[32];
@@ -130,6 +131,15 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ b
     counts[t] = tot;
     offsets[t] = excl;
     if (t == E - 1) offsets[E] = excl + tot;
+  }
+  if (tile_off) {   // the grouped GEMMs' tile table as well (what tile_table_kernel computes)
+    __syncthreads();   // s_warp is reused
+    const int tiles = t < E ? (tot + rows_per_tile - 1) / rows_per_tile : 0;
+    const int texcl = block_exclusive_scan(tiles, s_warp);
+    if (t < E) {
+      tile_off[t] = texcl;
+      if (t == E - 1) tile_off[E] = texcl + tiles;
+    }
   }
 }
 
@@ -191,13 +201,13 @@ __global__ void __launch_bounds__(kPermThreads) perm_place_kernel(const int32_t*
 
 cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, int32_t* offsets,
                            int32_t* gather_idx, int32_t* scatter_idx, int k, int chunk, int32_t* blk, int* status,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, int rows_per_tile, int32_t* tile_off) {
   if (chunk < 256 || chunk > kMaxChunk || chunk % 256) return cudaErrorInvalidValue;
   const int nb = permute_blocks(R, chunk);
   if (nb > 0) {
     launch_pdl(perm_count_kernel, nb, kPermThreads, E * sizeof(int32_t), stream, idx, R, E, chunk, blk, status);
   }
-  launch_pdl(perm_scan_kernel, 1, 1024, 0, stream, blk, nb, E, counts, offsets);
+  launch_pdl(perm_scan_kernel, 1, 1024, 0, stream, blk, nb, E, counts, offsets, rows_per_tile, tile_off);
   if (nb > 0) {
     const size_t sm = (size_t)kPermWarps * E * sizeof(int32_t);
     launch_pdl(perm_place_kernel, nb, kPermThreads, sm, stream, idx, R, E, k, chunk, blk, offsets, gather_idx, scatter_idx);

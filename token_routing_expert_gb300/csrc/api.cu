@@ -441,7 +441,7 @@ int run_restore(const moe_config_t* c, const moe_weights_t* w, const void* z, bo
 // Workspace of the experts' backward.
 struct BwdPlan {
   int64_t rows, kpad;
-  size_t xp, ug, dh, h, dug, dxp, wo_t, wug_t, dy_t, h_t, dug_t, xp_t, k_off, tile_off, total;
+  size_t xp, ug, dh, h, dug, dxp, dy_t, h_t, dug_t, xp_t, k_off, tile_off, total;
 };
 
 void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
@@ -461,8 +461,6 @@ void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
   b->h = take((size_t)b->rows * h * 2);
   b->dug = take((size_t)b->rows * 2 * h * 2);
   b->dxp = take((size_t)b->rows * Lr * 2);
-  b->wo_t = take((size_t)E * h * Lr * 2);
-  b->wug_t = take((size_t)E * 2 * h * Lr * 2);
   b->dy_t = take((size_t)Lr * b->kpad * 2);
   b->h_t = take((size_t)h * b->kpad * 2);
   b->dug_t = take((size_t)2 * h * b->kpad * 2);
@@ -502,9 +500,10 @@ void make_router_bwd_plan(const moe_config_t* c, int64_t T, int sms, RouterBwdPl
 }
 
 // M-grouped bf16 GEMM out = A B^T over the experts' row groups.
+// b_mn: B is stored K rows x N columns per group (N contiguous) instead of N rows x K.
 int grouped_bf16(const void* A, int64_t rows, const void* B, int64_t b_rows_total, int b_rows_per_group, int N, int K,
                  const int32_t* offsets, const int32_t* tile_off, int E, int pair, void* out, int* status,
-                 cudaStream_t st) {
+                 cudaStream_t st, int b_mn = 0) {
   GemmProblem g{};
   g.A = A;
   g.B = B;
@@ -520,6 +519,7 @@ int grouped_bf16(const void* A, int64_t rows, const void* B, int64_t b_rows_tota
   g.bn = 256;
   g.splits = 1;
   g.pair_tiles = pair;
+  g.b_mn_major = b_mn;
   g.out = out;
   g.ldo = N;
   g.status = status;
@@ -1035,8 +1035,6 @@ int moe_grouped_swiglu_backward(const moe_config_t* c, const moe_weights_t* w, c
   void* H = at<void>(ws, b.h);
   void* dUG = at<void>(ws, b.dug);
   void* dXp = at<void>(ws, b.dxp);
-  void* woT = at<void>(ws, b.wo_t);
-  void* wugT = at<void>(ws, b.wug_t);
   void* dyT = at<void>(ws, b.dy_t);
   void* hT = at<void>(ws, b.h_t);
   void* dugT = at<void>(ws, b.dug_t);
@@ -1049,15 +1047,14 @@ int moe_grouped_swiglu_backward(const moe_config_t* c, const moe_weights_t* w, c
   if (s == MOE_OK)
     s = grouped_bf16(xp, rows, w->w_up_gate, (int64_t)E * 2 * h, 2 * h, 2 * h, Lr, offsets, tile_off, E, pair, UG,
                      status, st);
-  // per-expert transposes of the weights
-  if (s == MOE_OK) s = cuda_status(launch_transpose_experts(w->w_out, E, Lr, h, woT, st));
-  if (s == MOE_OK) s = cuda_status(launch_transpose_experts(w->w_up_gate, E, 2 * h, Lr, wugT, st));
-  // dH = dY W_out ; SwiGLU backward ; dXp = dUG W_up_gate ; dx = sum over a token's rows
+  // dH = dY W_out ; SwiGLU backward ; dXp = dUG W_up_gate ; dx = sum over a token's rows.  The weights
+  // are read as stored (K rows x N columns: MN-major B operands), with no transposed copy.
   if (s == MOE_OK)
-    s = grouped_bf16(dy, rows, woT, (int64_t)E * h, h, h, Lr, offsets, tile_off, E, pair, dH, status, st);
+    s = grouped_bf16(dy, rows, w->w_out, (int64_t)E * Lr, Lr, h, Lr, offsets, tile_off, E, pair, dH, status, st, 1);
   if (s == MOE_OK) s = cuda_status(launch_swiglu_backward(UG, dH, rows, h, dUG, H, st));
   if (s == MOE_OK)
-    s = grouped_bf16(dUG, rows, wugT, (int64_t)E * Lr, Lr, Lr, 2 * h, offsets, tile_off, E, pair, dXp, status, st);
+    s = grouped_bf16(dUG, rows, w->w_up_gate, (int64_t)E * 2 * h, 2 * h, Lr, 2 * h, offsets, tile_off, E, pair, dXp,
+                     status, st, 1);
   if (s == MOE_OK)
     s = cuda_status(launch_combine(dXp, scatter_idx, nullptr, (int)T, k, Lr, rows, 0, 0.f, nullptr, dx_routed,
                                    capacity ? 1 : 0, status, st));

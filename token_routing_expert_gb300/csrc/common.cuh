@@ -343,6 +343,20 @@ __device__ __forceinline__ uint64_t umma_sdesc_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory descriptor of an MN-major operand with 128-byte swizzle: atoms of 64 MN elements
+// (128 bytes, contiguous) x 8 K rows (1024 bytes); lbo_bytes between consecutive 64-element MN
+// blocks, 1024 bytes between consecutive groups of 8 K rows.  One K=16 MMA step spans two
+// 8-row groups: advance the start address by 2048 bytes per step.
+__device__ __forceinline__ uint64_t umma_sdesc_mn_sw128(uint32_t smem_addr, uint32_t lbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);       // start address
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset: next 64-element MN block
+  d |= (uint64_t)(1024u >> 4) << 32;                  // stride byte offset: next 8 K rows
+  d |= (uint64_t)1 << 46;                             // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;                             // swizzle: 128 B
+  return d;
+}
+
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane (base + i).
 __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(

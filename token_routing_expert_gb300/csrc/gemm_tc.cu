@@ -56,6 +56,7 @@ struct GemmParams {
   const uint8_t* a_src;    //   source rows (a_src_rows x K), a_ld_bytes apart
   long long a_ld_bytes;
   int a_src_rows;
+  int b_mn;                // 1: B is MN-major, group g's K rows [g * b_rows_per_group, ...) x N columns
   int* status;
 };
 
@@ -433,6 +434,10 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
           if (EPI == EPI_SWIGLU) {
             tma_load_2d(sb, &tmB, &full_bar[stage], kx, brow);
             tma_load_2d(sb + C::B_BYTES / 2, &tmB, &full_bar[stage], kx, brow + p.b_gate_offset);
+          } else if (p.b_mn) {   // MN-major B: 64 K rows x BN columns, as BN / 64 blocks of 64 columns (8 KB)
+            for (int b = 0; b < BN / 64; ++b)
+              tma_load_2d(sb + b * 8192, &tmB, &full_bar[stage], c.nt * BN + 64 * b,
+                          c.group * p.b_rows_per_group + kt * BK);
           } else {
             tma_load_2d(sb, &tmB, &full_bar[stage], kx, brow);
           }
@@ -460,14 +465,17 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint64_t a_desc = umma_sdesc_sw128(sa);
-          const uint64_t b_desc = umma_sdesc_sw128(sa + C::A_BYTES);
+          // K-major B advances 32 bytes per MMA inside the swizzled rows; MN-major B two 8-row groups
+          const uint64_t b_desc = p.b_mn ? umma_sdesc_mn_sw128(sa + C::A_BYTES, 8192) : umma_sdesc_sw128(sa + C::A_BYTES);
+          const uint64_t b_step = p.b_mn ? 2048 / 16 : 2;
+          const uint32_t id = idesc | (p.b_mn ? (1u << 16) : 0u);   // bit 16: B is MN-major
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             // one MMA takes 32 bytes of K (16 bf16 or 32 e4m3): +2 in 16-byte units inside the swizzled row
             if (F8)
-              umma_e4m3(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+              umma_e4m3(d_tmem, a_desc + 2ull * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
             else
-              umma_bf16(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+              umma_bf16(d_tmem, a_desc + 2ull * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -636,7 +644,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
             mbar_arrive_expect_tx(&full_bar[stage], GA ? 2 * C::B_BYTES : 2 * C::STAGE_BYTES - (a1 ? 0 : C::A_BYTES));
           const int kx = kt * (F8 ? 2 * BK : BK);
           if (!GA && (rank == 0 || a1)) tma_load_2d_pair(sa, &tmA, full0, kx, arow);
-          tma_load_2d_pair(sa + C::A_BYTES, &tmB, full0, kx, brow);
+          if (EPI != EPI_SWIGLU && p.b_mn) {   // MN-major B: this CTA's 128 columns as two 64-column blocks
+            for (int b = 0; b < 2; ++b)
+              tma_load_2d_pair(sa + C::A_BYTES + b * 8192, &tmB, full0, c.nt * C::BN + 128 * (int)rank + 64 * b,
+                               c.group * p.b_rows_per_group + kt * BK);
+          } else {
+            tma_load_2d_pair(sa + C::A_BYTES, &tmB, full0, kx, brow);
+          }
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
@@ -660,13 +674,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint64_t a_desc = umma_sdesc_sw128(sa);
-          const uint64_t b_desc = umma_sdesc_sw128(sa + C::A_BYTES);
+          const bool bmn = EPI != EPI_SWIGLU && p.b_mn;
+          const uint64_t b_desc = bmn ? umma_sdesc_mn_sw128(sa + C::A_BYTES, 8192) : umma_sdesc_sw128(sa + C::A_BYTES);
+          const uint64_t b_step = bmn ? 2048 / 16 : 2;
+          const uint32_t id = idesc | (bmn ? (1u << 16) : 0u);   // bit 16: B is MN-major
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             if (F8)
-              umma_e4m3_pair(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+              umma_e4m3_pair(d_tmem, a_desc + 2ull * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
             else
-              umma_bf16_pair(d_tmem, a_desc + 2ull * kk, b_desc + 2ull * kk, idesc, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+              umma_bf16_pair(d_tmem, a_desc + 2ull * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
           }
           umma_commit_pair(&empty_bar[stage], 0x3);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -854,9 +871,17 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   const bool ga = q.a_gather != nullptr;
   if (ga && (q.epilogue != EPI_SWIGLU || q.num_groups == 0 || q.splits > 1 || !q.a_src || q.a_src_rows < 0))
     return cudaErrorInvalidValue;
+  // MN-major B (bf16 / fp32 out, bf16 operands): group g's K rows x N columns; 64 x 64 boxes
+  if (q.b_mn_major && (f8 || ga || q.epilogue == EPI_SWIGLU || q.k_groups > 0 || q.bn % 64 || q.K % BK ||
+                       (q.num_groups > 0 && q.b_rows_per_group != q.K)))
+    return cudaErrorInvalidValue;
   const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
   CUtensorMap ta, tb;
-  if (!make_tmap(&tb, q.B, q.b_rows_total, q.K, b_box, f8)) return cudaErrorInvalidValue;
+  if (q.b_mn_major) {
+    if (!make_tmap(&tb, q.B, q.b_rows_total, q.N, BK, false)) return cudaErrorInvalidValue;
+  } else if (!make_tmap(&tb, q.B, q.b_rows_total, q.K, b_box, f8)) {
+    return cudaErrorInvalidValue;
+  }
   if (ga)
     ta = tb;   // unused
   else if (!make_tmap(&ta, q.A, q.M, q.K, BM, f8))
@@ -888,6 +913,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.a_src = static_cast<const uint8_t*>(q.a_src);
   gp.a_ld_bytes = (long long)q.K * (f8 ? 1 : 2);
   gp.a_src_rows = q.a_src_rows;
+  gp.b_mn = q.b_mn_major;
   gp.status = q.status;
 
   if (ga) {

@@ -36,6 +36,8 @@ struct GemmProblem {
   int e4m3;               // 1: A and B are e4m3 bytes (kind::f8f6f4) with per-row scales below
   const float* a_scale;   // (M) scale of each A row
   const float* b_scale;   // (b_rows_total) scale of each B row
+  int b_mn_major;         // 1 (bf16 operands, bf16 / fp32 out): B is stored K rows x N columns (N contiguous),
+                          //    group g's rows [g * K, (g + 1) * K); K a multiple of 64; no transposed copy needed
   const int* a_gather;    // non-NULL (grouped SwiGLU only): A row r is row a_gather[r] of a_src, -1 a zero
                           // row; A is then unused.  e4m3: a_scale is per a_src row.
   const void* a_src;      // (a_src_rows, K) bf16 or e4m3

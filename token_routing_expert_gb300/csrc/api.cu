@@ -181,12 +181,15 @@ T* at(void* ws, size_t off) {
 }
 
 // C = A * B^T, dense, with split-K through fp32 partials when the output has few tiles.
+// b_mn_rows > 0: B is stored K rows x N columns (MN-major) with only its first b_mn_rows rows
+// present (the ones up to K read as zeros).
 int dense_gemm_bf16(const void* A, const void* B, int M, int N, int K, void* out, int splits, float* part,
-                    int* status, cudaStream_t st) {
+                    int* status, cudaStream_t st, int b_mn_rows = 0) {
   GemmProblem q{};
   q.A = A;
   q.B = B;
-  q.b_rows_total = N;
+  q.b_rows_total = b_mn_rows > 0 ? b_mn_rows : N;
+  q.b_mn_major = b_mn_rows > 0 ? 1 : 0;
   q.M = M;
   q.N = N;
   q.K = K;
@@ -441,7 +444,7 @@ int run_restore(const moe_config_t* c, const moe_weights_t* w, const void* z, bo
 // Workspace of the experts' backward.
 struct BwdPlan {
   int64_t rows, kpad;
-  size_t xp, ug, dh, h, dug, dxp, dy_t, h_t, dug_t, xp_t, k_off, tile_off, total;
+  size_t xp, ug, dh, h, dug, dxp, dyp, k_off, poff, tile_off, scat, total;
 };
 
 void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
@@ -455,18 +458,18 @@ void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
     o += align256(bytes);
     return at;
   };
-  b->xp = take((size_t)b->rows * Lr * 2);
-  b->ug = take((size_t)b->rows * 2 * h * 2);
-  b->dh = take((size_t)b->rows * h * 2);
-  b->h = take((size_t)b->rows * h * 2);
-  b->dug = take((size_t)b->rows * 2 * h * 2);
-  b->dxp = take((size_t)b->rows * Lr * 2);
-  b->dy_t = take((size_t)Lr * b->kpad * 2);
-  b->h_t = take((size_t)h * b->kpad * 2);
-  b->dug_t = take((size_t)2 * h * b->kpad * 2);
-  b->xp_t = take((size_t)Lr * b->kpad * 2);
+  // every activation in the padded row layout: kpad rows, expert e from row 64 k_off[e]
+  b->xp = take((size_t)b->kpad * Lr * 2);
+  b->ug = take((size_t)b->kpad * 2 * h * 2);
+  b->dh = take((size_t)b->kpad * h * 2);
+  b->h = take((size_t)b->kpad * h * 2);
+  b->dug = take((size_t)b->kpad * 2 * h * 2);
+  b->dxp = take((size_t)b->kpad * Lr * 2);
+  b->dyp = take((size_t)b->kpad * Lr * 2);
   b->k_off = take((size_t)(E + 1) * 4);
+  b->poff = take((size_t)(E + 1) * 4);
   b->tile_off = take((size_t)(E + 1) * 4);
+  b->scat = take((size_t)T * c->top_k * 4);
   b->total = o;
 }
 
@@ -474,7 +477,7 @@ void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
 struct RouterBwdPlan {
   int64_t Epad, Tpad;
   int dx_splits, dw_splits;
-  size_t dl, wr_t, dl_t, x_t, part, total;
+  size_t dl, part, total;
 };
 
 void make_router_bwd_plan(const moe_config_t* c, int64_t T, int sms, RouterBwdPlan* b) {
@@ -490,9 +493,6 @@ void make_router_bwd_plan(const moe_config_t* c, int64_t T, int sms, RouterBwdPl
     return at;
   };
   b->dl = take((size_t)T * b->Epad * 2);
-  b->wr_t = take((size_t)D * b->Epad * 2);
-  b->dl_t = take((size_t)b->Epad * b->Tpad * 2);
-  b->x_t = take((size_t)D * b->Tpad * 2);
   const size_t dx_part = b->dx_splits > 1 ? (size_t)b->dx_splits * T * D * 4 : 0;
   const size_t dw_part = b->dw_splits > 1 ? (size_t)b->dw_splits * ((E * D + 3) / 4 * 4) * 4 : 0;
   b->part = take(std::max(dx_part, dw_part));
@@ -527,18 +527,24 @@ int grouped_bf16(const void* A, int64_t rows, const void* B, int64_t b_rows_tota
 }
 
 // K-grouped fp32 GEMM: out[e] (M x N) = A[:, K_e] B[:, K_e]^T.
+// K-grouped fp32 GEMM on the padded row layout: out[e] (M x N) = A[K_e rows]^T B[K_e rows], A stored
+// kpad rows x M columns and B kpad rows x N columns (both MN-major operands), K_e = the 64-row
+// tiles [k_off[e], k_off[e+1]).
 int kgrouped_f32(const void* A, int M, const void* B, int N, int64_t kpad, const int32_t* k_off, int E, float* out,
                  int* status, cudaStream_t st) {
   GemmProblem g{};
   g.A = A;
+  g.a_mn_major = 1;
   g.B = B;
-  g.b_rows_total = N;
+  g.b_mn_major = 1;
+  g.b_rows_total = kpad;
+  g.b_rows_per_group = 0;
   g.M = M;
   g.N = N;
   g.K = (int)kpad;
   g.num_groups = 0;
   g.epilogue = EPI_F32;
-  g.bn = pick_bn_f32(N);
+  g.bn = N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
   g.splits = 1;
   g.k_groups = E;
   g.k_off = k_off;
@@ -936,30 +942,30 @@ int moe_router_backward(const moe_config_t* c, const moe_weights_t* w, const voi
   if (c->expert_weight_scale != 0.f) scale *= c->expert_weight_scale;
   if (c->original_top_k > 0 && c->original_top_k != c->top_k) scale *= sqrtf((float)c->original_top_k / (float)c->top_k);
   void* dl = at<void>(ws, r.dl);
-  void* wrT = at<void>(ws, r.wr_t);
-  void* dlT = at<void>(ws, r.dl_t);
-  void* xT = at<void>(ws, r.x_t);
   float* part = at<float>(ws, r.part);
   s = cuda_status(launch_router_backward(logits, idx, dweights, (int)T, E, c->top_k, c->gating,
                                          c->sigmoid_stability_epsilon, c->normalize_expert_weights, scale, dlogits, dl,
                                          (int)r.Epad, st));
-  // dx = dlogits W_router
-  if (s == MOE_OK) s = cuda_status(launch_transpose_pad(w->w_router, E, D, D, r.Epad, wrT, st));
-  if (s == MOE_OK) s = dense_gemm_bf16(dl, wrT, (int)T, D, (int)r.Epad, dx, r.dx_splits, part, status, st);
-  // dW_router = dlogits^T x, contracted over the tokens
-  if (s == MOE_OK) s = cuda_status(launch_transpose_pad(dl, (int)T, (int)r.Epad, r.Epad, r.Tpad, dlT, st));
-  if (s == MOE_OK) s = cuda_status(launch_transpose_pad(x, (int)T, D, D, r.Tpad, xT, st));
+  // dx = dlogits W_router: W_router read as stored (E rows x D columns, an MN-major B; the rows up
+  // to the padded E read as zeros, as do dl's padding columns)
+  if (s == MOE_OK) s = dense_gemm_bf16(dl, w->w_router, (int)T, D, (int)r.Epad, dx, r.dx_splits, part, status, st, E);
+  // dW_router = dlogits^T x, contracted over the tokens: dl (T x Epad) and x (T x D) read as stored
+  // (MN-major A and B), the tokens up to the padded T read as zeros
   if (s == MOE_OK) {
     GemmProblem g{};
-    g.A = dlT;
-    g.B = xT;
-    g.b_rows_total = D;
+    g.A = dl;
+    g.a_mn_major = 1;
+    g.mn_rows = T;
+    g.a_cols = r.Epad;
+    g.B = x;
+    g.b_mn_major = 1;
+    g.b_rows_total = T;
     g.M = E;
     g.N = D;
     g.K = (int)r.Tpad;
     g.num_groups = 0;
     g.epilogue = EPI_F32;
-    g.bn = pick_bn_f32(D);
+    g.bn = D % 256 == 0 ? 256 : (D % 128 == 0 ? 128 : 64);
     g.splits = r.dw_splits;
     g.ldo = D;
     g.status = status;
@@ -1029,43 +1035,42 @@ int moe_grouped_swiglu_backward(const moe_config_t* c, const moe_weights_t* w, c
   const int pair = rows >= 384 * E ? 1 : 0;
   int32_t* tile_off = at<int32_t>(ws, b.tile_off);
   int32_t* k_off = at<int32_t>(ws, b.k_off);
+  int32_t* poff = at<int32_t>(ws, b.poff);
+  int32_t* scat = at<int32_t>(ws, b.scat);
   void* xp = at<void>(ws, b.xp);
   void* UG = at<void>(ws, b.ug);
   void* dH = at<void>(ws, b.dh);
   void* H = at<void>(ws, b.h);
   void* dUG = at<void>(ws, b.dug);
   void* dXp = at<void>(ws, b.dxp);
-  void* dyT = at<void>(ws, b.dy_t);
-  void* hT = at<void>(ws, b.h_t);
-  void* dugT = at<void>(ws, b.dug_t);
-  void* xpT = at<void>(ws, b.xp_t);
+  void* dYp = at<void>(ws, b.dyp);
+  const int prows = (int)b.kpad;   // rows of the padded layout (the ones past 64 k_off[E] are never read)
 
-  s = cuda_status(launch_tile_table(offsets, E, pair ? 256 : 128, tile_off, st));
-  if (s == MOE_OK) s = cuda_status(launch_tile_table(offsets, E, 64, k_off, st));  // 64-row k-tiles per expert
-  if (s == MOE_OK) s = cuda_status(launch_gather_rows(x_routed, gather_idx, rows, (int)T, Lr, xp, capacity, status, st));
-  // recomputed pre-activations [u | g]
+  // padded layout: offsets, the routed rows and dY copied into it, the scatter moved into it
+  s = cuda_status(launch_pad_offsets(offsets, E, pair ? 256 : 128, k_off, poff, tile_off, st));
   if (s == MOE_OK)
-    s = grouped_bf16(xp, rows, w->w_up_gate, (int64_t)E * 2 * h, 2 * h, 2 * h, Lr, offsets, tile_off, E, pair, UG,
+    s = cuda_status(launch_pad_rows(x_routed, gather_idx, offsets, k_off, E, (int)T, Lr, prows, xp, status, st));
+  if (s == MOE_OK) s = cuda_status(launch_pad_rows(dy, nullptr, offsets, k_off, E, rows, Lr, prows, dYp, status, st));
+  if (s == MOE_OK) s = cuda_status(launch_pad_scatter(scatter_idx, (int)T * k, offsets, poff, E, scat, st));
+  // recomputed pre-activations [u | g]; zero rows stay zero through every step below
+  if (s == MOE_OK)
+    s = grouped_bf16(xp, prows, w->w_up_gate, (int64_t)E * 2 * h, 2 * h, 2 * h, Lr, poff, tile_off, E, pair, UG,
                      status, st);
   // dH = dY W_out ; SwiGLU backward ; dXp = dUG W_up_gate ; dx = sum over a token's rows.  The weights
   // are read as stored (K rows x N columns: MN-major B operands), with no transposed copy.
   if (s == MOE_OK)
-    s = grouped_bf16(dy, rows, w->w_out, (int64_t)E * Lr, Lr, h, Lr, offsets, tile_off, E, pair, dH, status, st, 1);
-  if (s == MOE_OK) s = cuda_status(launch_swiglu_backward(UG, dH, rows, h, dUG, H, st));
+    s = grouped_bf16(dYp, prows, w->w_out, (int64_t)E * Lr, Lr, h, Lr, poff, tile_off, E, pair, dH, status, st, 1);
+  if (s == MOE_OK) s = cuda_status(launch_swiglu_backward(UG, dH, prows, h, dUG, H, st));
   if (s == MOE_OK)
-    s = grouped_bf16(dUG, rows, w->w_up_gate, (int64_t)E * 2 * h, 2 * h, Lr, 2 * h, offsets, tile_off, E, pair, dXp,
+    s = grouped_bf16(dUG, prows, w->w_up_gate, (int64_t)E * 2 * h, 2 * h, Lr, 2 * h, poff, tile_off, E, pair, dXp,
                      status, st, 1);
   if (s == MOE_OK)
-    s = cuda_status(launch_combine(dXp, scatter_idx, nullptr, (int)T, k, Lr, rows, 0, 0.f, nullptr, dx_routed,
+    s = cuda_status(launch_combine(dXp, scat, nullptr, (int)T, k, Lr, prows, 0, 0.f, nullptr, dx_routed,
                                    capacity ? 1 : 0, status, st));
-  // weight gradients: K-grouped over each expert's rows
-  const long long maxc = b.kpad;
-  if (s == MOE_OK) s = cuda_status(launch_group_transpose(dy, Lr, offsets, k_off, E, maxc, b.kpad, dyT, st));
-  if (s == MOE_OK) s = cuda_status(launch_group_transpose(H, h, offsets, k_off, E, maxc, b.kpad, hT, st));
-  if (s == MOE_OK) s = cuda_status(launch_group_transpose(dUG, 2 * h, offsets, k_off, E, maxc, b.kpad, dugT, st));
-  if (s == MOE_OK) s = cuda_status(launch_group_transpose(xp, Lr, offsets, k_off, E, maxc, b.kpad, xpT, st));
-  if (s == MOE_OK) s = kgrouped_f32(dyT, Lr, hT, h, b.kpad, k_off, E, dw_out, status, st);
-  if (s == MOE_OK) s = kgrouped_f32(dugT, 2 * h, xpT, Lr, b.kpad, k_off, E, dw_up_gate, status, st);
+  // weight gradients, K-grouped over each expert's 64-row tiles of the padded activations, read as
+  // stored (MN-major A and B)
+  if (s == MOE_OK) s = kgrouped_f32(dYp, Lr, H, h, b.kpad, k_off, E, dw_out, status, st);
+  if (s == MOE_OK) s = kgrouped_f32(dUG, 2 * h, xp, Lr, b.kpad, k_off, E, dw_up_gate, status, st);
   return s;
 }
 

@@ -5,14 +5,16 @@
 // up and gate, computes the sigmoid, gate * sigmoid, its derivative and the two
 // gradients in float32 and concatenates them back in the input dtype.
 //
-// Row kernels here are HBM-bound; the contractions run on the tcgen05 GEMM:
+// Row kernels here are HBM-bound; the contractions run on the tcgen05 GEMM, which reads every
+// operand as stored (weights and activations as MN-major operands where the contraction runs
+// along their rows), so nothing is transposed:
 //   UG  = Xp W_up_gate^T            (recomputed pre-activations, bf16)
-//   dH  = dY W_out                  (B = per-expert transpose of W_out)
-//   dXp = dUG W_up_gate             (B = per-expert transpose of W_up_gate)
-//   dW_out[e]     = dY_e^T H_e      (K-grouped over the expert's rows)
+//   dH  = dY W_out                  (W_out as an MN-major B)
+//   dXp = dUG W_up_gate             (W_up_gate as an MN-major B)
+//   dW_out[e]     = dY_e^T H_e      (K-grouped over the expert's rows, MN-major A and B)
 //   dW_up_gate[e] = dUG_e^T Xp_e    (K-grouped)
-// The K-grouped GEMMs read K-major copies dY^T, H^T, dUG^T, Xp^T whose
-// expert row ranges start on 64-column boundaries, zero-padded.
+// The activations live in a padded row layout (each expert from a 64-row boundary, zero rows
+// between), so that every 64-row k-tile of the K-grouped GEMMs belongs to one expert.
 #include <algorithm>
 
 #include "common.cuh"
@@ -21,113 +23,119 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// bf16 transposes: out[c][col] = in[src(col)][c] (zero where src(col) = -1).
-// A block moves a 64 (col) x 64 (c) tile: 16-byte coalesced loads of 64 source
-// rows into padded shared memory, an 8 x 8 register transpose per thread
-// (byte permutes), 16-byte coalesced stores of 64 output rows.
+// Padded row layout of the experts backward: expert e's rows start at row poff[e] = 64 k_off[e]
+// and are followed by zero rows up to the next multiple of 64, so every 64-row k-tile of the
+// weight-gradient GEMMs belongs to one expert and they read the activations as stored.
 // ---------------------------------------------------------------------------
-enum TransposeMode { TR_BATCHED = 0, TR_GROUPED = 1, TR_PADDED = 2 };
 
-struct TransposeArgs {
-  const uint16_t* in;
-  uint16_t* out;
-  long long ld_in;      // elements per input row
-  long long ld_out;     // elements per output row (a multiple of 64)
-  long long in_batch;   // batched: elements between input matrices
-  long long out_batch;  // batched: elements between output matrices
-  int A;                // batched / padded: source rows
-  const int32_t* off;   // grouped: row offsets of the experts (E+1)
-  const int32_t* k_off; // grouped: 64-column tile offsets of the experts (E+1)
-  int E;
-};
-
-template <int MODE>
-__global__ void __launch_bounds__(64) transpose_tile_kernel(const TransposeArgs a) {
-  __shared__ uint4 tile[64][9];   // 64 source rows x 8 x 16 B, padded against bank conflicts
-  __shared__ int s_src[64];
-  const int tid = threadIdx.x;
-  const long long col0 = (long long)blockIdx.x * 64;
-  const long long c0 = (long long)blockIdx.y * 64;
-  const uint16_t* in = a.in;
-  uint16_t* out = a.out;
-  if (MODE == TR_BATCHED) {
-    in += (long long)blockIdx.z * a.in_batch;
-    out += (long long)blockIdx.z * a.out_batch;
-  }
-  {
-    const long long col = col0 + tid;
-    int src;
-    if (MODE == TR_GROUPED) {
-      if (col0 >= 64ll * a.k_off[a.E]) return;   // whole block past the last expert
-      int lo = 0, hi = a.E - 1;                  // last expert e with 64 * k_off[e] <= col
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (64ll * a.k_off[mid] <= col) lo = mid; else hi = mid - 1;
-      }
-      const long long r = col - 64ll * a.k_off[lo];
-      src = r < (long long)(a.off[lo + 1] - a.off[lo]) ? a.off[lo] + (int)r : -1;
-    } else {
-      src = col < a.A ? (int)col : -1;
+// One block of 1024 threads: k_off = prefix of ceil(count / 64), poff = 64 k_off, and the tile
+// table of the M-grouped GEMMs over the padded groups (prefix of ceil(64 ceil(count / 64) / rpt)).
+__global__ void __launch_bounds__(1024) pad_offsets_kernel(const int32_t* __restrict__ off, int E, int rows_per_tile,
+                                                           int32_t* __restrict__ k_off, int32_t* __restrict__ poff,
+                                                           int32_t* __restrict__ tile_off) {
+  __shared__ int s_warp[32], s_warp2[32];
+  const int e = threadIdx.x;
+  const int cnt = e < E ? off[e + 1] - off[e] : 0;
+  const int kt = (cnt + 63) / 64;
+  const int excl = block_exclusive_scan(kt, s_warp);
+  const int tiles = (64 * kt + rows_per_tile - 1) / rows_per_tile;
+  const int texcl = block_exclusive_scan(tiles, s_warp2);
+  if (e < E) {
+    k_off[e] = excl;
+    poff[e] = 64 * excl;
+    tile_off[e] = texcl;
+    if (e == E - 1) {
+      k_off[E] = excl + kt;
+      poff[E] = 64 * (excl + kt);
+      tile_off[E] = texcl + tiles;
     }
-    s_src[tid] = src;
-  }
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int lin = i * 64 + tid;
-    const int r = lin >> 3, q = lin & 7;
-    const int src = s_src[r];
-    tile[r][q] = src >= 0 ? *reinterpret_cast<const uint4*>(in + (long long)src * a.ld_in + c0 + 8 * q)
-                          : make_uint4(0u, 0u, 0u, 0u);
-  }
-  __syncthreads();
-  const int ib = tid & 7;    // block of 8 source rows = 8 output columns
-  const int jb = tid >> 3;   // block of 8 channels = 8 output rows
-  uint32_t w[8][4];
-#pragma unroll
-  for (int r = 0; r < 8; ++r) {
-    const uint4 v = tile[8 * ib + r][jb];
-    w[r][0] = v.x; w[r][1] = v.y; w[r][2] = v.z; w[r][3] = v.w;
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const uint32_t sel = (j & 1) ? 0x7632u : 0x5410u;   // high or low halves of two source words
-    uint32_t o[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) o[q] = __byte_perm(w[2 * q][j >> 1], w[2 * q + 1][j >> 1], sel);
-    *reinterpret_cast<uint4*>(out + (c0 + 8 * jb + j) * a.ld_out + col0 + 8 * ib) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
-// out[e] = in[e]^T for in (E, A, B) -> out (E, B, A); A, B multiples of 64.
-cudaError_t launch_transpose_experts(const void* in, int E, int A, int B, void* out, cudaStream_t st) {
-  if ((A % 64) || (B % 64)) return cudaErrorInvalidValue;
-  TransposeArgs a{};
-  a.in = static_cast<const uint16_t*>(in);
-  a.out = static_cast<uint16_t*>(out);
-  a.ld_in = B;
-  a.ld_out = A;
-  a.in_batch = (long long)A * B;
-  a.out_batch = (long long)A * B;
-  a.A = A;
-  transpose_tile_kernel<TR_BATCHED><<<dim3(A / 64, B / 64, E), 64, 0, st>>>(a);
+// dst row pr (a warp each, pr < 64 k_off[E]) of expert e = the group whose 64-row tiles hold it,
+// r = pr - poff[e]: for r < count, source row gather[off[e] + r] (gather NULL: off[e] + r; -1: a
+// zero row); a zero row past the expert's count.
+__global__ void __launch_bounds__(256) pad_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ gather,
+                                                       const int32_t* __restrict__ off,
+                                                       const int32_t* __restrict__ k_off, int E, int src_rows,
+                                                       int vec, long long max_rows, uint4* __restrict__ dst,
+                                                       int* status) {
+  const int lane = threadIdx.x & 31;
+  const long long pr = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (pr >= max_rows || pr >= 64ll * k_off[E]) return;
+  const int kt = (int)(pr / 64);
+  int lo = 0, hi = E - 1;   // last e with k_off[e] <= kt (an expert with rows owns the tile)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (k_off[mid] <= kt) lo = mid; else hi = mid - 1;
+  }
+  const int r = (int)(pr - 64ll * k_off[lo]);
+  int srow = -1;
+  if (r < off[lo + 1] - off[lo]) {
+    srow = gather ? gather[off[lo] + r] : off[lo] + r;
+    if (srow < -1 || srow >= src_rows) {
+      if (lane == 0) set_status(status, MOE_ERR_BOUNDS);
+      srow = -1;
+    }
+  }
+  uint4* d = dst + pr * vec;
+  if (srow < 0) {
+    for (int c = lane; c < vec; c += 32) d[c] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const uint4* sr = src + (long long)srow * vec;
+  for (int c0 = lane; c0 < vec; c0 += 256) {   // eight 16-byte loads in flight per lane
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + 32 * i < vec) v[i] = __ldg(sr + c0 + 32 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + 32 * i < vec) d[c0 + 32 * i] = v[i];
+  }
+}
+
+// A scatter index into the dense row order, moved to the padded one (-1 stays -1).
+__global__ void __launch_bounds__(256) pad_scatter_kernel(const int32_t* __restrict__ scatter, int R,
+                                                          const int32_t* __restrict__ off,
+                                                          const int32_t* __restrict__ poff, int E,
+                                                          int32_t* __restrict__ out) {
+  const int f = blockIdx.x * blockDim.x + threadIdx.x;
+  if (f >= R) return;
+  const int p = scatter[f];
+  if (p < 0) {
+    out[f] = p;
+    return;
+  }
+  int lo = 0, hi = E - 1;   // last e with off[e] <= p: the expert that owns row p (never an empty one)
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (off[mid] <= p) lo = mid; else hi = mid - 1;
+  }
+  out[f] = p - off[lo] + poff[lo];
+}
+
+cudaError_t launch_pad_offsets(const int32_t* off, int E, int rows_per_tile, int32_t* k_off, int32_t* poff,
+                               int32_t* tile_off, cudaStream_t st) {
+  if (E > 1024) return cudaErrorInvalidValue;
+  pad_offsets_kernel<<<1, 1024, 0, st>>>(off, E, rows_per_tile, k_off, poff, tile_off);
   return cudaGetLastError();
 }
 
-// XT[c][col] for col in [0, 64 * k_off[E]): expert e's columns start at 64 * k_off[e];
-// its r-th column is row off[e] + r of X (rows x C) while r < off[e+1] - off[e], zero after.
-cudaError_t launch_group_transpose(const void* X, int C, const int32_t* off, const int32_t* k_off, int E,
-                                   long long max_cols, long long ld_out, void* XT, cudaStream_t st) {
-  if ((C % 64) || (ld_out % 64) || max_cols > ld_out) return cudaErrorInvalidValue;
-  TransposeArgs a{};
-  a.in = static_cast<const uint16_t*>(X);
-  a.out = static_cast<uint16_t*>(XT);
-  a.ld_in = C;
-  a.ld_out = ld_out;
-  a.off = off;
-  a.k_off = k_off;
-  a.E = E;
-  transpose_tile_kernel<TR_GROUPED><<<dim3((unsigned)((max_cols + 63) / 64), C / 64), 64, 0, st>>>(a);
+cudaError_t launch_pad_rows(const void* src, const int32_t* gather, const int32_t* off, const int32_t* k_off, int E,
+                            int src_rows, int cols, long long max_rows, void* dst, int* status, cudaStream_t st) {
+  if (max_rows <= 0) return cudaSuccess;
+  if (cols % 8) return cudaErrorInvalidValue;
+  pad_rows_kernel<<<(unsigned)((max_rows + 7) / 8), 256, 0, st>>>(static_cast<const uint4*>(src), gather, off, k_off, E,
+                                                                   src_rows, cols / 8, max_rows,
+                                                                   static_cast<uint4*>(dst), status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pad_scatter(const int32_t* scatter, int R, const int32_t* off, const int32_t* poff, int E,
+                               int32_t* out, cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  pad_scatter_kernel<<<(R + 255) / 256, 256, 0, st>>>(scatter, R, off, poff, E, out);
   return cudaGetLastError();
 }
 
@@ -381,20 +389,6 @@ cudaError_t launch_router_backward(const float* logits, const int32_t* idx, cons
   return cudaGetLastError();
 }
 
-// out (B x ld_out) = in (A x B, leading dimension ld_in)^T, columns A..ld_out-1 zero; bf16.
-// B and ld_out multiples of 64, ld_in a multiple of 8.
-cudaError_t launch_transpose_pad(const void* in, int A, int B, long long ld_in, long long ld_out, void* out,
-                                 cudaStream_t st) {
-  if ((B % 64) || (ld_out % 64) || (ld_in % 8) || ld_out < A) return cudaErrorInvalidValue;
-  TransposeArgs a{};
-  a.in = static_cast<const uint16_t*>(in);
-  a.out = static_cast<uint16_t*>(out);
-  a.ld_in = ld_in;
-  a.ld_out = ld_out;
-  a.A = A;
-  transpose_tile_kernel<TR_PADDED><<<dim3((unsigned)(ld_out / 64), B / 64), 64, 0, st>>>(a);
-  return cudaGetLastError();
-}
 
 // db[e] = sum over t of d[t, e]: 32 columns per block, 8 row groups reduced in shared memory.
 __global__ void __launch_bounds__(256) column_sum_kernel(const float* __restrict__ d, int T, int E,

@@ -116,6 +116,32 @@ __device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cluster_add
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Block-wide exclusive scan of one value per thread (blockDim.x == 1024); s_warp: 32 ints of
+// shared memory, not reused before a __syncthreads() after the call.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_warp[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = s_warp[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    s_warp[lane] = w;  // inclusive over warps
+  }
+  __syncthreads();
+  const int before = warp > 0 ? s_warp[warp - 1] : 0;
+  return before + x - v;
+}
+
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch: a kernel launched with launch_pdl may be scheduled while the
 // previous kernel on its stream is still finishing.  Every such kernel calls pdl_wait() before it

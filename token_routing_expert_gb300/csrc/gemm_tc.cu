@@ -57,6 +57,7 @@ struct GemmParams {
   long long a_ld_bytes;
   int a_src_rows;
   int b_mn;                // 1: B is MN-major, group g's K rows [g * b_rows_per_group, ...) x N columns
+  int a_mn;                // 1 (K-grouped, 1 CTA): A is MN-major, K rows x M columns
   int* status;
 };
 
@@ -430,7 +431,12 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
           uint8_t* sb = sa + C::A_BYTES;
           mbar_arrive_expect_tx(&full_bar[stage], GA ? C::B_BYTES : C::STAGE_BYTES);
           const int kx = kt * (F8 ? 2 * BK : BK);   // 128 bytes of K per k-tile: 64 bf16 or 128 e4m3
-          if (!GA) tma_load_2d(sa, &tmA, &full_bar[stage], kx, c.row0);
+          if (p.a_mn) {   // MN-major A: 64 K rows x 128 M columns as two 64-column blocks (8 KB each)
+            tma_load_2d(sa, &tmA, &full_bar[stage], c.row0, kt * BK);
+            tma_load_2d(sa + 8192, &tmA, &full_bar[stage], c.row0 + 64, kt * BK);
+          } else if (!GA) {
+            tma_load_2d(sa, &tmA, &full_bar[stage], kx, c.row0);
+          }
           if (EPI == EPI_SWIGLU) {
             tma_load_2d(sb, &tmB, &full_bar[stage], kx, brow);
             tma_load_2d(sb + C::B_BYTES / 2, &tmB, &full_bar[stage], kx, brow + p.b_gate_offset);
@@ -464,18 +470,21 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
           if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
-          const uint64_t a_desc = umma_sdesc_sw128(sa);
-          // K-major B advances 32 bytes per MMA inside the swizzled rows; MN-major B two 8-row groups
+          // a K-major operand advances 32 bytes per MMA inside its swizzled rows, an MN-major one by
+          // two 8-row K groups (2048 bytes)
+          const uint64_t a_desc = p.a_mn ? umma_sdesc_mn_sw128(sa, 8192) : umma_sdesc_sw128(sa);
           const uint64_t b_desc = p.b_mn ? umma_sdesc_mn_sw128(sa + C::A_BYTES, 8192) : umma_sdesc_sw128(sa + C::A_BYTES);
+          const uint64_t a_step = p.a_mn ? 2048 / 16 : 2;
           const uint64_t b_step = p.b_mn ? 2048 / 16 : 2;
-          const uint32_t id = idesc | (p.b_mn ? (1u << 16) : 0u);   // bit 16: B is MN-major
+          // bits 15 / 16 of the instruction descriptor: A / B is MN-major
+          const uint32_t id = idesc | (p.a_mn ? (1u << 15) : 0u) | (p.b_mn ? (1u << 16) : 0u);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-            // one MMA takes 32 bytes of K (16 bf16 or 32 e4m3): +2 in 16-byte units inside the swizzled row
+            // one MMA takes 32 bytes of K (16 bf16 or 32 e4m3)
             if (F8)
-              umma_e4m3(d_tmem, a_desc + 2ull * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+              umma_e4m3(d_tmem, a_desc + a_step * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
             else
-              umma_bf16(d_tmem, a_desc + 2ull * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+              umma_bf16(d_tmem, a_desc + a_step * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -871,9 +880,13 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   const bool ga = q.a_gather != nullptr;
   if (ga && (q.epilogue != EPI_SWIGLU || q.num_groups == 0 || q.splits > 1 || !q.a_src || q.a_src_rows < 0))
     return cudaErrorInvalidValue;
-  // MN-major B (bf16 / fp32 out, bf16 operands): group g's K rows x N columns; 64 x 64 boxes
-  if (q.b_mn_major && (f8 || ga || q.epilogue == EPI_SWIGLU || q.k_groups > 0 || q.bn % 64 || q.K % BK ||
-                       (q.num_groups > 0 && q.b_rows_per_group != q.K)))
+  // MN-major B (bf16 / fp32 out, bf16 operands): group g's K rows x N columns; 64 x 64 boxes.
+  // MN-major A: K-grouped only (1 CTA), K rows x M columns.
+  if (q.b_mn_major && (f8 || ga || q.epilogue == EPI_SWIGLU || q.bn % 64 || q.K % BK ||
+                       (q.num_groups > 0 && q.b_rows_per_group != q.K) || (q.k_groups > 0 && q.b_rows_per_group)))
+    return cudaErrorInvalidValue;
+  if (q.a_mn_major && (q.num_groups > 0 || pair || f8 || q.K % BK || (q.a_cols && q.a_cols < q.M) ||
+                       (q.mn_rows && q.mn_rows > q.K)))
     return cudaErrorInvalidValue;
   const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
   CUtensorMap ta, tb;
@@ -884,7 +897,8 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   }
   if (ga)
     ta = tb;   // unused
-  else if (!make_tmap(&ta, q.A, q.M, q.K, BM, f8))
+  else if (q.a_mn_major ? !make_tmap(&ta, q.A, q.mn_rows ? q.mn_rows : q.K, q.a_cols ? q.a_cols : q.M, BK, false)
+                        : !make_tmap(&ta, q.A, q.M, q.K, BM, f8))
     return cudaErrorInvalidValue;
 
   GemmParams gp;
@@ -914,6 +928,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.a_ld_bytes = (long long)q.K * (f8 ? 1 : 2);
   gp.a_src_rows = q.a_src_rows;
   gp.b_mn = q.b_mn_major;
+  gp.a_mn = q.a_mn_major;
   gp.status = q.status;
 
   if (ga) {

@@ -38,6 +38,9 @@ struct GemmProblem {
   const float* b_scale;   // (b_rows_total) scale of each B row
   int b_mn_major;         // 1 (bf16 operands, bf16 / fp32 out): B is stored K rows x N columns (N contiguous),
                           //    group g's rows [g * K, (g + 1) * K); K a multiple of 64; no transposed copy needed
+  int a_mn_major;         // 1 (1 CTA, K-grouped or dense): A is stored K rows x a_cols columns (M <= a_cols used)
+  int64_t mn_rows;        // MN-major A: rows present (0: K); rows up to K beyond them read as zeros
+  int64_t a_cols;         // MN-major A: columns per row (0: M)
   const int* a_gather;    // non-NULL (grouped SwiGLU only): A row r is row a_gather[r] of a_src, -1 a zero
                           // row; A is then unused.  e4m3: a_scale is per a_src row.
   const void* a_src;      // (a_src_rows, K) bf16 or e4m3
@@ -87,9 +90,15 @@ cudaError_t launch_combine(const void* y, const int32_t* scatter_idx, const floa
                            cudaStream_t stream);
 cudaError_t launch_rmsnorm(const void* z, int T, int L, float eps, const void* gain, void* out,
                            cudaStream_t stream);
-cudaError_t launch_transpose_experts(const void* in, int E, int A, int B, void* out, cudaStream_t st);
-cudaError_t launch_group_transpose(const void* X, int C, const int32_t* off, const int32_t* k_off, int E,
-                                   long long max_cols, long long ld_out, void* XT, cudaStream_t st);
+// Padded row layout of the experts backward (expert e from row 64 k_off[e], zero rows to the next
+// multiple of 64): its offsets (+ the M-grouped tile table), rows copied into it (gather optional,
+// max_rows >= 64 k_off[E]), and scatter indices moved into it.
+cudaError_t launch_pad_offsets(const int32_t* off, int E, int rows_per_tile, int32_t* k_off, int32_t* poff,
+                               int32_t* tile_off, cudaStream_t st);
+cudaError_t launch_pad_rows(const void* src, const int32_t* gather, const int32_t* off, const int32_t* k_off, int E,
+                            int src_rows, int cols, long long max_rows, void* dst, int* status, cudaStream_t st);
+cudaError_t launch_pad_scatter(const int32_t* scatter, int R, const int32_t* off, const int32_t* poff, int E,
+                               int32_t* out, cudaStream_t st);
 cudaError_t launch_swiglu_backward(const void* UG, const void* dH, long long rows, int h, void* dUG, void* H,
                                    cudaStream_t st);
 cudaError_t launch_combine_backward(const void* dz, const void* y, const int32_t* scatter_idx, const float* w, int T,
@@ -98,8 +107,6 @@ cudaError_t launch_zero_padding_rows(const int32_t* gather_idx, int rows, int co
 cudaError_t launch_router_backward(const float* logits, const int32_t* idx, const float* dw, int T, int E, int k,
                                    int gating, float sig_eps, float p_norm, float scale, float* dlogits,
                                    void* dl_bf16, int Epad, cudaStream_t st);
-cudaError_t launch_transpose_pad(const void* in, int A, int B, long long ld_in, long long ld_out, void* out,
-                                 cudaStream_t st);
 cudaError_t launch_column_sum(const float* d, int T, int E, float* out, cudaStream_t st);
 // out = sum of `splits` fp32 slices of n floats (n a multiple of 4), in slice order.
 cudaError_t launch_sum_slices_f32(const float* part, int splits, long long n, float* out, cudaStream_t st);

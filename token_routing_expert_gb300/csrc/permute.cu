@@ -48,30 +48,6 @@ __global__ void __launch_bounds__(kPermThreads) perm_count_kernel(const int32_t*
   for (int i = threadIdx.x; i < E; i += blockDim.x) blk[(long long)blockIdx.x * E + i] = hist[i];
 }
 
-// Block-wide exclusive scan of one value per thread (blockDim.x == 1024).
-__device__ int block_exclusive_scan(int v, int* s_warp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) s_warp[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = s_warp[lane];
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    s_warp[lane] = w;  // inclusive over warps
-  }
-  __syncthreads();
-  const int before = warp > 0 ? s_warp[warp - 1] : 0;
-  return before + x - v;
-}
 
 // One block of 1024 threads.  G = 1024 / E (rounded down to a power of two, at most 32)
 // threads share expert e: thread g of the group takes a contiguous run of the per-chunk

@@ -544,7 +544,8 @@ int kgrouped_f32(const void* A, int M, const void* B, int N, int64_t kpad, const
   g.K = (int)kpad;
   g.num_groups = 0;
   g.epilogue = EPI_F32;
-  g.bn = N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
+  g.pair_tiles = M >= 256 ? 1 : 0;   // 256 x 256 tiles on CTA pairs: half the B bytes per CTA
+  g.bn = g.pair_tiles || N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
   g.splits = 1;
   g.k_groups = E;
   g.k_off = k_off;

@@ -603,6 +603,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
       s_toff[i] = p.tile_off[i];
       s_goff[i] = p.group_off[i];
     }
+  } else if (p.k_groups > 0) {
+    for (int i = threadIdx.x; i <= p.k_groups; i += blockDim.x) s_goff[i] = p.k_off[i];
   }
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -629,7 +631,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int mtiles = p.num_groups > 0 ? s_toff[p.num_groups] : (p.M + BM2 - 1) / BM2;
-  const int total_tiles = mtiles * p.n_tiles;
+  const int total_tiles = mtiles * p.n_tiles * (p.k_groups > 0 ? p.k_groups : 1);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -652,7 +654,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
           if (rank == 0)
             mbar_arrive_expect_tx(&full_bar[stage], GA ? 2 * C::B_BYTES : 2 * C::STAGE_BYTES - (a1 ? 0 : C::A_BYTES));
           const int kx = kt * (F8 ? 2 * BK : BK);
-          if (!GA && (rank == 0 || a1)) tma_load_2d_pair(sa, &tmA, full0, kx, arow);
+          if (!GA && (rank == 0 || a1)) {
+            if (p.a_mn) {   // MN-major A: this CTA's 128 M columns as two 64-column blocks
+              tma_load_2d_pair(sa, &tmA, full0, arow, kt * BK);
+              tma_load_2d_pair(sa + 8192, &tmA, full0, arow + 64, kt * BK);
+            } else {
+              tma_load_2d_pair(sa, &tmA, full0, kx, arow);
+            }
+          }
           if (EPI != EPI_SWIGLU && p.b_mn) {   // MN-major B: this CTA's 128 columns as two 64-column blocks
             for (int b = 0; b < 2; ++b)
               tma_load_2d_pair(sa + C::A_BYTES + b * 8192, &tmB, full0, c.nt * C::BN + 128 * (int)rank + 64 * b,
@@ -682,17 +691,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
           if (!mbar_wait_cluster(&full_bar[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
-          const uint64_t a_desc = umma_sdesc_sw128(sa);
+          const bool amn = !GA && p.a_mn;
           const bool bmn = EPI != EPI_SWIGLU && p.b_mn;
+          const uint64_t a_desc = amn ? umma_sdesc_mn_sw128(sa, 8192) : umma_sdesc_sw128(sa);
           const uint64_t b_desc = bmn ? umma_sdesc_mn_sw128(sa + C::A_BYTES, 8192) : umma_sdesc_sw128(sa + C::A_BYTES);
+          const uint64_t a_step = amn ? 2048 / 16 : 2;
           const uint64_t b_step = bmn ? 2048 / 16 : 2;
-          const uint32_t id = idesc | (bmn ? (1u << 16) : 0u);   // bit 16: B is MN-major
+          // bits 15 / 16 of the instruction descriptor: A / B is MN-major
+          const uint32_t id = idesc | (amn ? (1u << 15) : 0u) | (bmn ? (1u << 16) : 0u);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             if (F8)
-              umma_e4m3_pair(d_tmem, a_desc + 2ull * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+              umma_e4m3_pair(d_tmem, a_desc + a_step * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
             else
-              umma_bf16_pair(d_tmem, a_desc + 2ull * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
+              umma_bf16_pair(d_tmem, a_desc + a_step * kk, b_desc + b_step * kk, id, (kt > c.kt0 || kk > 0) ? 1u : 0u);
           }
           umma_commit_pair(&empty_bar[stage], 0x3);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -725,8 +737,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
         cs = p.b_scale + brow;
         cs_gate = cs + p.b_gate_offset;
       }
-      store_tile<C::BN, EPI, F8>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt, 0, p,
-                                 half, stg, false, cs, cs_gate);
+      // K-grouped: the group's output slice, zeros for a group without rows
+      store_tile<C::BN, EPI, F8>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt, c.split,
+                                 p, half, stg, c.kt1 <= c.kt0, cs, cs_gate);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&tempty_bar[acc]), 0));
@@ -868,8 +881,7 @@ static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb
 
 cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   if (q.num_groups > kMaxGroups || q.k_groups > kMaxGroups) return cudaErrorInvalidValue;
-  if (q.k_groups > 0 && (q.num_groups > 0 || q.pair_tiles || q.splits > 1 || q.epilogue != EPI_F32))
-    return cudaErrorInvalidValue;
+  if (q.k_groups > 0 && (q.num_groups > 0 || q.splits > 1 || q.epilogue != EPI_F32)) return cudaErrorInvalidValue;
   const bool pair = q.pair_tiles != 0;
   const bool f8 = q.e4m3 != 0;
   if (pair && (q.bn != 256 || q.splits > 1 || (q.epilogue == EPI_F32 && (q.e4m3 || q.num_groups > 0))))
@@ -885,7 +897,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   if (q.b_mn_major && (f8 || ga || q.epilogue == EPI_SWIGLU || q.bn % 64 || q.K % BK ||
                        (q.num_groups > 0 && q.b_rows_per_group != q.K) || (q.k_groups > 0 && q.b_rows_per_group)))
     return cudaErrorInvalidValue;
-  if (q.a_mn_major && (q.num_groups > 0 || pair || f8 || q.K % BK || (q.a_cols && q.a_cols < q.M) ||
+  if (q.a_mn_major && (q.num_groups > 0 || f8 || q.K % BK || (q.a_cols && q.a_cols < q.M) ||
                        (q.mn_rows && q.mn_rows > q.K)))
     return cudaErrorInvalidValue;
   const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
@@ -940,7 +952,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
               : launch_impl<256, EPI_SWIGLU, false, true>(q, ta, tb, gp, grid, stream);
   }
   if (pair) {
-    const int tiles = q.num_groups == 0 ? ((q.M + BM2 - 1) / BM2) * gp.n_tiles : 0;
+    const int tiles = q.num_groups == 0 ? ((q.M + BM2 - 1) / BM2) * gp.n_tiles * std::max(1, q.k_groups) : 0;
     if (f8) {
       if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU, true>(ta, tb, gp, tiles, stream);
       return launch_pair_impl<EPI_BF16, true>(ta, tb, gp, tiles, stream);

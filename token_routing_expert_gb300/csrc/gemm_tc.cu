@@ -134,13 +134,14 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
   return c;
 }
 
-// Stores a warp's 32 x 32 bf16 block (thread i holds row i as 16 packed words) through a 2 KB
-// shared buffer, so that each global store instruction writes 8 rows x 64 contiguous bytes
-// instead of 32 rows x 16 bytes.  The 16-byte slots are XOR-swizzled by row: both the row-wise
-// writes and the column-wise reads hit 8 distinct bank groups per quarter warp.
-// out0: column 0 of the block's first row; valid: how many of the 32 rows exist.
-__device__ __forceinline__ void store_block_bf16(uint4* stg, const uint32_t (&packed)[16], __nv_bfloat16* out0,
-                                                 long long ldo, int valid, int lane) {
+// Stores a warp's block of 32 rows x 64 bytes (thread i holds row i as 16 words: 32 bf16 or 16
+// fp32) through a 2 KB shared buffer, so that each global store instruction writes 8 rows x 64
+// contiguous bytes instead of 32 rows x 16 bytes.  The 16-byte slots are XOR-swizzled by row:
+// both the row-wise writes and the column-wise reads hit 8 distinct bank groups per quarter warp.
+// out0: the block's first byte in its first row; ld_bytes: the row pitch in bytes; valid: how
+// many of the 32 rows exist.
+__device__ __forceinline__ void store_block_64b(uint4* stg, const uint32_t (&packed)[16], char* out0,
+                                                long long ld_bytes, int valid, int lane) {
 #pragma unroll
   for (int i = 0; i < 4; ++i)
     stg[lane * 4 + (i ^ ((lane >> 1) & 3))] =
@@ -151,9 +152,14 @@ __device__ __forceinline__ void store_block_bf16(uint4* stg, const uint32_t (&pa
   for (int s = 0; s < 4; ++s) {
     const int r = s * 8 + (lane >> 2);
     const uint4 v = stg[r * 4 + (q ^ ((r >> 1) & 3))];
-    if (r < valid) *reinterpret_cast<uint4*>(out0 + r * ldo + q * 8) = v;
+    if (r < valid) *reinterpret_cast<uint4*>(out0 + r * ld_bytes + q * 16) = v;
   }
   __syncwarp();
+}
+
+__device__ __forceinline__ void store_block_bf16(uint4* stg, const uint32_t (&packed)[16], __nv_bfloat16* out0,
+                                                 long long ldo, int valid, int lane) {
+  store_block_64b(stg, packed, reinterpret_cast<char*>(out0), ldo * 2, valid, lane);
 }
 
 // Epilogue of one tile for the 32 rows a warp owns: TMEM -> registers -> global.
@@ -225,24 +231,25 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
         tmem_ld_wait();
       }
       const int col0 = nt * BN + cc * 32;
-      if (EPI == EPI_BF16) {
-        if (valid == 0 || col0 >= p.N) continue;
-      } else if (!row_ok || col0 >= p.N) {
-        continue;
-      }
+      if (valid == 0 || col0 >= p.N) continue;   // warp-uniform
       if (F8) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * rs * __ldg(cs + cc * 32 + i));
       }
       if (EPI == EPI_F32) {
-        float* out = reinterpret_cast<float*>(p.out) + (long long)split * p.split_stride + row * p.ldo + col0;
-        if (col0 + 32 <= p.N && (p.ldo & 3) == 0) {
-          float4* dst = reinterpret_cast<float4*>(out);
+        float* base = reinterpret_cast<float*>(p.out) + (long long)split * p.split_stride;
+        if (col0 + 32 <= p.N && (p.ldo & 3) == 0 && (reinterpret_cast<uintptr_t>(base) & 15) == 0) {
+          // two 16-column halves, each a 32 x 64-byte block staged for row-contiguous stores
+          char* out0 = reinterpret_cast<char*>(base + wrow0 * p.ldo + col0);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                 __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-        } else {
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t words[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) words[i] = v[16 * hf + i];
+            store_block_64b(stg, words, out0 + 64 * hf, p.ldo * 4, valid, lane);
+          }
+        } else if (row_ok) {
+          float* out = base + row * p.ldo + col0;
 #pragma unroll
           for (int i = 0; i < 32; ++i)
             if (col0 + i < p.N) out[i] = __uint_as_float(v[i]);

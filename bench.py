@@ -375,31 +375,55 @@ def run_native(args):
         dy_d = torch.empty_like(y_d)
         dw_d = torch.empty_like(w_d)
         bws = native.backward_workspace(cfg, T)
+        # the training forward keeps the experts' pre-activations; timed against the plain forward
+        preact = torch.empty((native.moe_permuted_rows(cfg, T), 2 * spec.hidden_size), dtype=torch.bfloat16,
+                             device="cuda")
+        fwd_out = torch.empty((T, spec.d_model), dtype=torch.bfloat16, device="cuda")
+
+        def train_forward():
+            native.moe_layer_forward_preact(cfg, wts, x, ws, out=fwd_out, preact=preact)
+
+        def plain_forward():
+            native.moe_layer_forward(cfg, wts, x, ws, out=fwd_out)
+
+        def timed(fn):
+            for _ in range(3):
+                fn()
+            torch.cuda.synchronize()
+            t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            t0.record(stream)
+            for _ in range(args.steps):
+                fn()
+            t1.record(stream)
+            torch.cuda.synchronize()
+            return t0.elapsed_time(t1) / args.steps
+
+        fwd_plain_ms, fwd_train_ms = timed(plain_forward), timed(train_forward)
+        # the intermediates below are the last forward's (the same batch, so the same routing)
         dx_d = torch.empty((T, spec.routed_dim), dtype=torch.bfloat16, device="cuda")
         dwug = torch.empty((spec.num_experts, 2 * spec.hidden_size, spec.routed_dim), dtype=torch.float32, device="cuda")
         dwo = torch.empty((spec.num_experts, spec.routed_dim, spec.hidden_size), dtype=torch.float32, device="cuda")
 
         def backward_step():
             native.moe_combine_backward(cfg, dz, y_d, scatter_d, w_d, gather_idx=gather_d, dy=dy_d, dweights=dw_d)
+            native.moe_grouped_swiglu_backward_preact(cfg, wts, xr_d, gather_d, offsets_d, scatter_d, dy_d, preact,
+                                                      bws, dx_routed=dx_d, dw_up_gate=dwug, dw_out=dwo)
+
+        def backward_step_recompute():
+            native.moe_combine_backward(cfg, dz, y_d, scatter_d, w_d, gather_idx=gather_d, dy=dy_d, dweights=dw_d)
             native.moe_grouped_swiglu_backward(cfg, wts, xr_d, gather_d, offsets_d, scatter_d, dy_d, bws,
                                                dx_routed=dx_d, dw_up_gate=dwug, dw_out=dwo)
 
-        for _ in range(3):
-            backward_step()
-        torch.cuda.synchronize()
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        c0.record(stream)
-        for _ in range(args.steps):
-            backward_step()
-        c1.record(stream)
-        torch.cuda.synchronize()
+        bms = timed(backward_step)
+        bms_re = timed(backward_step_recompute)
         if native.moe_get_status() != 0:
             raise SystemExit("device status error in the backward")
-        bms = c0.elapsed_time(c1) / args.steps
         bflops = 12 * spec.rows * spec.routed_dim * spec.hidden_size
         bwd = {"ms": bms, "tflops": bflops / (bms * 1e-3) / 1e12, "algorithmic_flops": bflops,
-               "note": "combine backward + experts backward (dH, dX, dW_out, dW_up_gate GEMMs = 12 R L h FLOPs; "
-                       "the pre-activations are recomputed, 4 R L h more)"}
+               "ms_recompute": bms_re, "forward_ms": fwd_plain_ms, "forward_keep_preact_ms": fwd_train_ms,
+               "note": "combine backward + experts backward from the forward's kept pre-activations (dH, dX, "
+                       "dW_out, dW_up_gate GEMMs = 12 R L h FLOPs); ms_recompute recomputes them instead "
+                       "(4 R L h more); forward_keep_preact_ms is the layer forward that keeps them"}
         del bws
 
     # load-balancing counters on this batch's histogram (between-step work, timed on its own)

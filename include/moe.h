@@ -193,6 +193,21 @@ int moe_grouped_swiglu(const moe_config_t* cfg, const moe_weights_t* w, const vo
                        size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_grouped_swiglu that also keeps the pre-activations for the backward
+ * (training).  Section "SwiGLU с квантизацией": the SwiGLU function saves its
+ * input, the up and gate projections, and its backward works from them; here
+ * grouped GEMM 1 stores them from its epilogue next to H, so the backward does
+ * not recompute them.
+ *   preact device (rows, 2h) bf16 output: row p = [u | g], u = W_up[e] x and
+ *   g = W_gate[e] x rounded to bf16 (e4m3 experts: the scaled e4m3 products),
+ *   in y's row order; a padding slot (capacity mode) gets a zero row.
+ * hidden_size must be a multiple of 32 (else MOE_ERR_UNSUPPORTED).
+ */
+int moe_grouped_swiglu_preact(const moe_config_t* cfg, const moe_weights_t* w, const void* x_routed,
+                              const int32_t* gather_idx, const int32_t* offsets, int64_t T, void* y, void* preact,
+                              void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
  * Weighted un-permute / combine, section "Пересылка токенов между экспертами":
  * z[t] = sum_j weights[t, j] * y[scatter_idx[t*k + j]], accumulated in fp32, stored bf16.
  * In capacity mode a dropped assignment (scatter_idx -1) adds nothing.
@@ -229,6 +244,15 @@ int moe_latent_restore(const moe_config_t* cfg, const moe_weights_t* w, const vo
  */
 int moe_layer_forward(const moe_config_t* cfg, const moe_weights_t* w, const void* x, int64_t T, void* out,
                       void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * moe_layer_forward for training: identical results, and the experts'
+ * pre-activations are kept in `preact` (device, (rows, 2h) bf16, rows =
+ * moe_permuted_rows(cfg, T), as moe_grouped_swiglu_preact writes them) for
+ * moe_grouped_swiglu_backward_preact.  preact must not be NULL when T > 0.
+ */
+int moe_layer_forward_preact(const moe_config_t* cfg, const moe_weights_t* w, const void* x, int64_t T, void* out,
+                             void* preact, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * moe_layer_forward with stage timing: when stage_events is not NULL it
@@ -300,6 +324,11 @@ int moe_layer_forward_host_batches(const moe_config_t* cfg, const moe_weights_t*
  *   dw_up_gate (E, 2h, L') fp32 out and dw_out (E, L', h) fp32 out: weight
  *   gradients (an expert without rows gets zeros).  Pre-activations are
  *   recomputed; ws must hold moe_backward_workspace_size(cfg, T) bytes.
+ *
+ * moe_grouped_swiglu_backward_preact: the same from the forward's saved
+ *   pre-activations (preact device (rows, 2h) bf16, as moe_grouped_swiglu_preact
+ *   or moe_layer_forward_preact wrote them; NULL: recomputed), which saves the
+ *   recomputation GEMM (4 rows L' h FLOPs).
  */
 int moe_backward_workspace_size(const moe_config_t* cfg, int64_t T, size_t* bytes);
 
@@ -325,6 +354,11 @@ int moe_grouped_swiglu_backward(const moe_config_t* cfg, const moe_weights_t* w,
                                 const int32_t* gather_idx, const int32_t* offsets, const int32_t* scatter_idx,
                                 int64_t T, const void* dy, void* dx_routed, float* dw_up_gate, float* dw_out,
                                 void* ws, size_t ws_bytes, moe_stream_t stream);
+int moe_grouped_swiglu_backward_preact(const moe_config_t* cfg, const moe_weights_t* w, const void* x_routed,
+                                       const int32_t* gather_idx, const int32_t* offsets, const int32_t* scatter_idx,
+                                       int64_t T, const void* dy, const void* preact, void* dx_routed,
+                                       float* dw_up_gate, float* dw_out, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream);
 
 /*
  * Load-balancing counters, section "Счётчики и bias-корректировка" (run between

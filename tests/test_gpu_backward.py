@@ -34,8 +34,26 @@ def close(got, want, what):
     assert rel <= REL_L2 and mx <= 3e-2, f"{what}: rel_l2={rel:.3e} max_abs/scale={mx:.3e}"
 
 
+def check_preact(pre, x_np, gather_np, offsets, ow, E, h, what="preact"):
+    """The kept pre-activations [u | g] against the oracle's projections of each row's token
+    (zero rows for padding slots)."""
+    pre = pre.double().cpu().numpy()
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi == lo:
+            continue
+        w_up, w_gate, _ = ow.expert(e)
+        slots = gather_np[lo:hi]
+        live = slots >= 0
+        assert (pre[lo:hi][~live] == 0).all(), f"{what}: padding slots of expert {e} are not zero"
+        if live.any():
+            rows = x_np[slots[live]]
+            close(pre[lo:hi][live], np.concatenate([rows @ w_up.T, rows @ w_gate.T], axis=1), f"{what}[{e}]")
+
+
+@pytest.mark.parametrize("preact", [False, True], ids=["recompute", "saved_preact"])
 @pytest.mark.parametrize("name", list(CASES))
-def test_combine_and_experts_backward(name):
+def test_combine_and_experts_backward(name, preact):
     spec = CASES[name]
     inp = generate(spec)
     cfg = native.config_from_spec(spec)
@@ -46,11 +64,21 @@ def test_combine_and_experts_backward(name):
     _, idx, w = native.moe_router(cfg, wts, x, ws)
     counts, offsets, gather, scatter = native.moe_permute(cfg, idx, ws)
     y = native.moe_grouped_swiglu(cfg, wts, x, gather, offsets, ws)
+    pre = None
+    if preact:
+        y2, pre = native.moe_grouped_swiglu_preact(cfg, wts, x, gather, offsets, ws)
+        assert torch.equal(y2, y), "keeping the pre-activations changed the forward"
     g = np.random.default_rng(spec.seed + 1)
     dz = torch.from_numpy(g.standard_normal((T, Lr), dtype=np.float32)).to(torch.bfloat16).cuda()
     dy, dw = native.moe_combine_backward(cfg, dz, y, scatter, w, gather_idx=gather)
     bws = native.backward_workspace(cfg, T)
-    dx, dwug, dwo = native.moe_grouped_swiglu_backward(cfg, wts, x, gather, offsets, scatter, dy, bws)
+    # the workspace starts dirty: nothing may depend on rows the backward does not write
+    bws.fill_(0xFF)
+    if preact:
+        dx, dwug, dwo = native.moe_grouped_swiglu_backward_preact(cfg, wts, x, gather, offsets, scatter, dy, pre,
+                                                                  bws)
+    else:
+        dx, dwug, dwo = native.moe_grouped_swiglu_backward(cfg, wts, x, gather, offsets, scatter, dy, bws)
     assert native.moe_get_status() == 0
 
     oc, ow = oracle_config(spec), oracle_weights(spec, inp)
@@ -65,6 +93,8 @@ def test_combine_and_experts_backward(name):
     # experts' backward on the GPU's dy, in the dense (or slot) layout of the permutation
     dy_np = dy.double().cpu().numpy()
     x_np = f64(inp["x"])
+    if preact:
+        check_preact(pre, x_np, gather_np, offsets.cpu().numpy(), ow, E, h)
     dx_want = np.zeros((T, Lr))
     for e in range(E):
         lo, hi = int(offsets[e]), int(offsets[e + 1])
@@ -129,3 +159,22 @@ def test_router_backward(name):
     close(dw.double().cpu().numpy(), want_dw, "dW_router")
     if spec.skew:
         close(db.double().cpu().numpy(), want_db, "db_router")
+
+
+def test_layer_forward_preact_matches_forward():
+    """The training forward returns the plain forward's output bit for bit and the pre-activations
+    of the permutation it made (read back from the workspace)."""
+    spec = CASES["pair_tiles"]
+    inp = generate(spec)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp)
+    ws = native.workspace(cfg, spec.T)
+    x = inp["x"].cuda()
+    out = native.moe_layer_forward(cfg, wts, x, ws).clone()
+    out2, pre = native.moe_layer_forward_preact(cfg, wts, x, ws)
+    assert native.moe_get_status() == 0
+    assert torch.equal(out, out2)
+    inter = native.layer_intermediates(cfg, spec.T, ws)
+    ow = oracle_weights(spec, inp)
+    check_preact(pre, f64(inp["x"]), inter["gather_idx"].cpu().numpy(), inter["offsets"].cpu().numpy(), ow,
+                 spec.num_experts, spec.hidden_size, "layer preact")

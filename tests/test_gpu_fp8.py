@@ -81,3 +81,34 @@ def test_fp8_grouped_swiglu_designed_counts():
     perm = ref.Permutation(counts.cpu().numpy(), offsets.cpu().numpy(), gather.cpu().numpy(), scatter.cpu().numpy())
     want = ref.expert_outputs_fp8(oracle_config(spec), f64(xr), perm, oracle_weights(spec, inp).expert)
     assert_close_layer(y.double().cpu().numpy(), want, "fp8 grouped swiglu, designed counts")
+
+
+def test_fp8_preact():
+    """e4m3 experts keep the scaled e4m3 products as pre-activations: u = x_q W_up,q and
+    g = x_q W_gate,q with rowwise-dequantised operands (the quantiser is bit-exact, so only the
+    accumulation order differs)."""
+    spec = CASES["pair_tiles_fp8"]
+    inp = generate(spec)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp).quantize_experts_fp8()
+    ws = native.workspace(cfg, spec.T)
+    x = inp["x"].cuda()
+    _, idx, _ = native.moe_router(cfg, wts, x, ws)
+    counts, offsets, gather, scatter = native.moe_permute(cfg, idx, ws)
+    y = native.moe_grouped_swiglu(cfg, wts, x, gather, offsets, ws)
+    y2, pre = native.moe_grouped_swiglu_preact(cfg, wts, x, gather, offsets, ws)
+    assert native.moe_get_status() == 0
+    assert torch.equal(y, y2)
+    ow = oracle_weights(spec, inp)
+    xq, xs = ref.quantize_rowwise_e4m3(f64(inp["x"]))
+    xd = xq * xs.astype(np.float64)[:, None]
+    pre = pre.double().cpu().numpy()
+    off, gat = offsets.cpu().numpy(), gather.cpu().numpy()
+    for e in range(spec.num_experts):
+        lo, hi = int(off[e]), int(off[e + 1])
+        if hi == lo:
+            continue
+        wu, wg, _ = ref.quantize_expert_fp8(*ow.expert(e))
+        rows = xd[gat[lo:hi]]
+        want = np.concatenate([rows @ wu.T, rows @ wg.T], axis=1)
+        assert_close_layer(pre[lo:hi], want, f"fp8 preact[{e}]", float(np.abs(want).max()))

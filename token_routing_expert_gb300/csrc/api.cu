@@ -258,7 +258,7 @@ int run_router(const moe_config_t* c, const moe_weights_t* w, const void* x, con
 // permuted order (SwiGLU, scales in the epilogue) -> H bf16, quantise H per row, GEMM 2.
 int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
                     const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
-                    cudaEvent_t* ev, bool tiles_ready) {
+                    cudaEvent_t* ev, bool tiles_ready, void* preact) {
   int32_t* tile_off = at<int32_t>(ws, p.tile_off);
   void* H = at<void>(ws, p.H);
   void* xq = at<void>(ws, p.xq);
@@ -300,6 +300,8 @@ int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* x
   g1.b_scale = w->w_up_gate_scale;
   g1.out = H;
   g1.ldo = p.h;
+  g1.preact = preact;
+  g1.preact_ld = 2 * (int64_t)p.h;
   g1.status = status;
   s = cuda_status(launch_gemm(g1, st));
   if (s == MOE_OK) s = cuda_status(launch_quantize_rowwise_e4m3(H, p.rows, p.h, hq, hs, st));
@@ -333,12 +335,14 @@ int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* x
 }
 
 // tiles_ready: the tile table in the workspace was already written (by run_permute).
+// preact (optional): grouped GEMM 1 also stores the pre-activations [u | g] there, rows x 2h bf16.
 int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
                 const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
-                cudaEvent_t* ev = nullptr, bool tiles_ready = false) {
+                cudaEvent_t* ev = nullptr, bool tiles_ready = false, void* preact = nullptr) {
   int32_t* tile_off = at<int32_t>(ws, p.tile_off);
   void* H = at<void>(ws, p.H);
-  if (c->expert_fp8) return run_experts_fp8(c, w, xr, gather, offsets, p, y, ws, status, st, ev, tiles_ready);
+  if (c->expert_fp8)
+    return run_experts_fp8(c, w, xr, gather, offsets, p, y, ws, status, st, ev, tiles_ready, preact);
   // large groups run on CTA pairs with 256-row tiles; small ones keep 128-row tiles,
   // which waste less of the last partial tile of each group
   const int pair = use_pair_tiles(p);
@@ -377,6 +381,8 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   g1.pair_tiles = pair;
   g1.out = H;
   g1.ldo = p.h;
+  g1.preact = preact;
+  g1.preact_ld = 2 * (int64_t)p.h;
   g1.status = status;
   s = cuda_status(launch_gemm(g1, st));
   if (s != MOE_OK) return s;
@@ -444,7 +450,7 @@ int run_restore(const moe_config_t* c, const moe_weights_t* w, const void* z, bo
 // Workspace of the experts' backward.
 struct BwdPlan {
   int64_t rows, kpad;
-  size_t xp, ug, dh, h, dug, dxp, dyp, k_off, poff, tile_off, scat, total;
+  size_t xp, ug, dh, h, dug, dxp, k_off, poff, tile_off, scat, total;
 };
 
 void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
@@ -465,7 +471,6 @@ void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
   b->h = take((size_t)b->kpad * h * 2);
   b->dug = take((size_t)b->kpad * 2 * h * 2);
   b->dxp = take((size_t)b->kpad * Lr * 2);
-  b->dyp = take((size_t)b->kpad * Lr * 2);
   b->k_off = take((size_t)(E + 1) * 4);
   b->poff = take((size_t)(E + 1) * 4);
   b->tile_off = take((size_t)(E + 1) * 4);
@@ -501,11 +506,14 @@ void make_router_bwd_plan(const moe_config_t* c, int64_t T, int sms, RouterBwdPl
 
 // M-grouped bf16 GEMM out = A B^T over the experts' row groups.
 // b_mn: B is stored K rows x N columns per group (N contiguous) instead of N rows x K.
+// a_off (optional): group e's A rows start at A row a_off[e] (A has a_rows rows) instead of offsets[e].
 int grouped_bf16(const void* A, int64_t rows, const void* B, int64_t b_rows_total, int b_rows_per_group, int N, int K,
                  const int32_t* offsets, const int32_t* tile_off, int E, int pair, void* out, int* status,
-                 cudaStream_t st, int b_mn = 0) {
+                 cudaStream_t st, int b_mn = 0, const int32_t* a_off = nullptr, int64_t a_rows = 0) {
   GemmProblem g{};
   g.A = A;
+  g.a_off = a_off;
+  g.a_rows = a_off ? a_rows : 0;
   g.B = B;
   g.b_rows_total = b_rows_total;
   g.M = (int)rows;
@@ -530,11 +538,14 @@ int grouped_bf16(const void* A, int64_t rows, const void* B, int64_t b_rows_tota
 // K-grouped fp32 GEMM on the padded row layout: out[e] (M x N) = A[K_e rows]^T B[K_e rows], A stored
 // kpad rows x M columns and B kpad rows x N columns (both MN-major operands), K_e = the 64-row
 // tiles [k_off[e], k_off[e+1]).
+// a_off (optional): group e's K rows of A start at A row a_off[e] (A has a_rows rows) instead of 64 k_off[e].
 int kgrouped_f32(const void* A, int M, const void* B, int N, int64_t kpad, const int32_t* k_off, int E, float* out,
-                 int* status, cudaStream_t st) {
+                 int* status, cudaStream_t st, const int32_t* a_off = nullptr, int64_t a_rows = 0) {
   GemmProblem g{};
   g.A = A;
   g.a_mn_major = 1;
+  g.a_off = a_off;
+  g.mn_rows = a_off ? a_rows : 0;
   g.B = B;
   g.b_mn_major = 1;
   g.b_rows_total = kpad;
@@ -670,6 +681,12 @@ int moe_permute(const moe_config_t* c, const int32_t* idx, int64_t T, int32_t* c
 
 int moe_grouped_swiglu(const moe_config_t* c, const moe_weights_t* w, const void* x_routed, const int32_t* gather_idx,
                        const int32_t* offsets, int64_t T, void* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return moe_grouped_swiglu_preact(c, w, x_routed, gather_idx, offsets, T, y, nullptr, ws, ws_bytes, stream);
+}
+
+int moe_grouped_swiglu_preact(const moe_config_t* c, const moe_weights_t* w, const void* x_routed,
+                              const int32_t* gather_idx, const int32_t* offsets, int64_t T, void* y, void* preact,
+                              void* ws, size_t ws_bytes, moe_stream_t stream) {
   Plan p;
   int s = check_call(c, T, ws, ws_bytes, &p);
   if (s != MOE_OK) return s;
@@ -679,7 +696,9 @@ int moe_grouped_swiglu(const moe_config_t* c, const moe_weights_t* w, const void
     return MOE_ERR_INVALID_ARG;
   int* status = status_ptr();
   if (!status) return MOE_ERR_NO_DEVICE;
-  return run_experts(c, w, x_routed, gather_idx, offsets, p, y, ws, status, (cudaStream_t)stream);
+  if (preact && c->hidden_size % 32) return MOE_ERR_UNSUPPORTED;
+  return run_experts(c, w, x_routed, gather_idx, offsets, p, y, ws, status, (cudaStream_t)stream, nullptr, false,
+                     preact);
 }
 
 int moe_combine(const moe_config_t* c, const void* y, const int32_t* scatter_idx, const float* weights, int64_t T,
@@ -727,8 +746,9 @@ int moe_latent_restore(const moe_config_t* c, const moe_weights_t* w, const void
   return run_restore(c, w, z, false, p, out, ws, status, (cudaStream_t)stream);
 }
 
-int moe_layer_forward_staged(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* out,
-                             void* ws, size_t ws_bytes, moe_stream_t stream, void* const* stage_events) {
+namespace {
+int layer_forward(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* out, void* preact,
+                  void* ws, size_t ws_bytes, moe_stream_t stream, void* const* stage_events) {
   Plan p;
   int s = check_call(c, T, ws, ws_bytes, &p);
   if (s != MOE_OK) return s;
@@ -739,6 +759,7 @@ int moe_layer_forward_staged(const moe_config_t* c, const moe_weights_t* w, cons
   if (c->expert_fp8 && (!w->w_up_gate_fp8 || !w->w_up_gate_scale || !w->w_out_fp8 || !w->w_out_scale))
     return MOE_ERR_INVALID_ARG;
   if (x == out) return MOE_ERR_INVALID_ARG;
+  if (preact && c->hidden_size % 32) return MOE_ERR_UNSUPPORTED;
   int* status = status_ptr();
   if (!status) return MOE_ERR_NO_DEVICE;
   cudaStream_t st = (cudaStream_t)stream;
@@ -767,7 +788,7 @@ int moe_layer_forward_staged(const moe_config_t* c, const moe_weights_t* w, cons
   if (s != MOE_OK) return s;
   mark(ev, 4, st);
   void* Y = at<void>(ws, p.Y);
-  s = run_experts(c, w, xr, gather, offsets, p, Y, ws, status, st, ev, tiles_ready);
+  s = run_experts(c, w, xr, gather, offsets, p, Y, ws, status, st, ev, tiles_ready, preact);
   if (s != MOE_OK) return s;
   if (!p.latent) {
     s = cuda_status(launch_combine(Y, scatter, wts, (int)T, p.k, p.Lr, (int)p.rows, 0, 0.f, nullptr, out,
@@ -786,9 +807,22 @@ int moe_layer_forward_staged(const moe_config_t* c, const moe_weights_t* w, cons
   return s;
 }
 
+}  // namespace
+
+int moe_layer_forward_staged(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream, void* const* stage_events) {
+  return layer_forward(c, w, x, T, out, nullptr, ws, ws_bytes, stream, stage_events);
+}
+
 int moe_layer_forward(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* out, void* ws,
                       size_t ws_bytes, moe_stream_t stream) {
-  return moe_layer_forward_staged(c, w, x, T, out, ws, ws_bytes, stream, nullptr);
+  return layer_forward(c, w, x, T, out, nullptr, ws, ws_bytes, stream, nullptr);
+}
+
+int moe_layer_forward_preact(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* out,
+                             void* preact, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  if (!preact && T > 0) return MOE_ERR_INVALID_ARG;
+  return layer_forward(c, w, x, T, out, preact, ws, ws_bytes, stream, nullptr);
 }
 
 
@@ -1014,6 +1048,15 @@ int moe_grouped_swiglu_backward(const moe_config_t* c, const moe_weights_t* w, c
                                 const int32_t* gather_idx, const int32_t* offsets, const int32_t* scatter_idx,
                                 int64_t T, const void* dy, void* dx_routed, float* dw_up_gate, float* dw_out,
                                 void* ws, size_t ws_bytes, moe_stream_t stream) {
+  return moe_grouped_swiglu_backward_preact(c, w, x_routed, gather_idx, offsets, scatter_idx, T, dy, nullptr,
+                                            dx_routed, dw_up_gate, dw_out, ws, ws_bytes, stream);
+}
+
+int moe_grouped_swiglu_backward_preact(const moe_config_t* c, const moe_weights_t* w, const void* x_routed,
+                                       const int32_t* gather_idx, const int32_t* offsets, const int32_t* scatter_idx,
+                                       int64_t T, const void* dy, const void* preact, void* dx_routed,
+                                       float* dw_up_gate, float* dw_out, void* ws, size_t ws_bytes,
+                                       moe_stream_t stream) {
   int s = check_config(c);
   if (s != MOE_OK) return s;
   if (T < 0) return MOE_ERR_INVALID_ARG;
@@ -1044,33 +1087,37 @@ int moe_grouped_swiglu_backward(const moe_config_t* c, const moe_weights_t* w, c
   void* H = at<void>(ws, b.h);
   void* dUG = at<void>(ws, b.dug);
   void* dXp = at<void>(ws, b.dxp);
-  void* dYp = at<void>(ws, b.dyp);
   const int prows = (int)b.kpad;   // rows of the padded layout (the ones past 64 k_off[E] are never read)
 
-  // padded layout: offsets, the routed rows and dY copied into it, the scatter moved into it
+  // padded layout: offsets, the routed rows copied into it, the scatter moved into it
   s = cuda_status(launch_pad_offsets(offsets, E, pair ? 256 : 128, k_off, poff, tile_off, st));
   if (s == MOE_OK)
     s = cuda_status(launch_pad_rows(x_routed, gather_idx, offsets, k_off, E, (int)T, Lr, prows, xp, status, st));
-  if (s == MOE_OK) s = cuda_status(launch_pad_rows(dy, nullptr, offsets, k_off, E, rows, Lr, prows, dYp, status, st));
   if (s == MOE_OK) s = cuda_status(launch_pad_scatter(scatter_idx, (int)T * k, offsets, poff, E, scat, st));
-  // recomputed pre-activations [u | g]; zero rows stay zero through every step below
-  if (s == MOE_OK)
+  // pre-activations [u | g]: the forward's (dense rows), or recomputed in the padded layout
+  if (s == MOE_OK && !preact)
     s = grouped_bf16(xp, prows, w->w_up_gate, (int64_t)E * 2 * h, 2 * h, 2 * h, Lr, poff, tile_off, E, pair, UG,
                      status, st);
-  // dH = dY W_out ; SwiGLU backward ; dXp = dUG W_up_gate ; dx = sum over a token's rows.  The weights
-  // are read as stored (K rows x N columns: MN-major B operands), with no transposed copy.
+  // dH = dY W_out, dY read at its dense rows (each group's A rows from offsets[e]; what a tile reads
+  // past the group only reaches dH's padding rows, which the SwiGLU backward ignores) ; SwiGLU
+  // backward (zeros in the padding rows of dUG and H) ; dXp = dUG W_up_gate ; dx = sum over a
+  // token's rows.  The weights are read as stored (K rows x N columns: MN-major B operands).
   if (s == MOE_OK)
-    s = grouped_bf16(dYp, prows, w->w_out, (int64_t)E * Lr, Lr, h, Lr, poff, tile_off, E, pair, dH, status, st, 1);
-  if (s == MOE_OK) s = cuda_status(launch_swiglu_backward(UG, dH, prows, h, dUG, H, st));
+    s = grouped_bf16(dy, prows, w->w_out, (int64_t)E * Lr, Lr, h, Lr, poff, tile_off, E, pair, dH, status, st, 1,
+                     offsets, rows);
+  if (s == MOE_OK)
+    s = cuda_status(launch_swiglu_backward(preact ? preact : UG, preact ? 1 : 0, offsets, k_off, E, dH, prows, h, dUG,
+                                           H, st));
   if (s == MOE_OK)
     s = grouped_bf16(dUG, prows, w->w_up_gate, (int64_t)E * 2 * h, 2 * h, Lr, 2 * h, poff, tile_off, E, pair, dXp,
                      status, st, 1);
   if (s == MOE_OK)
     s = cuda_status(launch_combine(dXp, scat, nullptr, (int)T, k, Lr, prows, 0, 0.f, nullptr, dx_routed,
                                    capacity ? 1 : 0, status, st));
-  // weight gradients, K-grouped over each expert's 64-row tiles of the padded activations, read as
-  // stored (MN-major A and B)
-  if (s == MOE_OK) s = kgrouped_f32(dYp, Lr, H, h, b.kpad, k_off, E, dw_out, status, st);
+  // weight gradients, K-grouped over each expert's 64-row tiles, read as stored (MN-major A and B):
+  // dW_out from dY's dense rows (a tile's rows past the expert meet H's zero padding rows) and H,
+  // dW_up_gate from dUG and the padded routed rows
+  if (s == MOE_OK) s = kgrouped_f32(dy, Lr, H, h, b.kpad, k_off, E, dw_out, status, st, offsets, rows);
   if (s == MOE_OK) s = kgrouped_f32(dUG, 2 * h, xp, Lr, b.kpad, k_off, E, dw_up_gate, status, st);
   return s;
 }

@@ -8,10 +8,10 @@
 // Row kernels here are HBM-bound; the contractions run on the tcgen05 GEMM, which reads every
 // operand as stored (weights and activations as MN-major operands where the contraction runs
 // along their rows), so nothing is transposed:
-//   UG  = Xp W_up_gate^T            (recomputed pre-activations, bf16)
-//   dH  = dY W_out                  (W_out as an MN-major B)
+//   UG  = Xp W_up_gate^T            (pre-activations: the forward's, kept, or recomputed; bf16)
+//   dH  = dY W_out                  (W_out as an MN-major B; dY read at the dense rows)
 //   dXp = dUG W_up_gate             (W_up_gate as an MN-major B)
-//   dW_out[e]     = dY_e^T H_e      (K-grouped over the expert's rows, MN-major A and B)
+//   dW_out[e]     = dY_e^T H_e      (K-grouped over the expert's rows, MN-major A and B; dY dense)
 //   dW_up_gate[e] = dUG_e^T Xp_e    (K-grouped)
 // The activations live in a padded row layout (each expert from a 64-row boundary, zero rows
 // between), so that every 64-row k-tile of the K-grouped GEMMs belongs to one expert.
@@ -139,47 +139,109 @@ cudaError_t launch_pad_scatter(const int32_t* scatter, int R, const int32_t* off
   return cudaGetLastError();
 }
 
-// From UG = [u | g] (rows x 2h) and dH (rows x h): H = silu(g) u, dU = dH silu(g),
-// dG = dH u silu'(g), silu'(g) = s (1 + g (1 - s)), s = sigmoid(g); fp32, stored bf16.
-__global__ void __launch_bounds__(256) swiglu_backward_kernel(const uint4* __restrict__ UG, const uint4* __restrict__ dH,
-                                                               long long rows, int h8, uint4* __restrict__ dUG,
-                                                               uint4* __restrict__ H) {
-  const long long n = rows * h8;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
-    const long long p = i / h8;
-    const int c = (int)(i - p * h8);
-    const uint4 uv = UG[p * 2 * h8 + c], gv = UG[p * 2 * h8 + h8 + c], dv = dH[p * h8 + c];
-    const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
-    uint32_t du[4], dg[4], hh[4];
+// SwiGLU backward of one 16-byte chunk (8 columns): from u, g and dH, H = silu(g) u,
+// dU = dH silu(g), dG = dH u silu'(g), silu'(g) = s (1 + g (1 - s)), s = sigmoid(g); fp32,
+// stored bf16.
+__device__ __forceinline__ void swiglu_bwd_chunk(uint4 uv, uint4 gv, uint4 dv, uint4& du_out, uint4& dg_out,
+                                                 uint4& h_out) {
+  const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
+  uint32_t du[4], dg[4], hh[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      float u[2] = {bf16_lo(uw[q]), bf16_hi(uw[q])}, g[2] = {bf16_lo(gw[q]), bf16_hi(gw[q])};
-      float d[2] = {bf16_lo(dw[q]), bf16_hi(dw[q])}, ru[2], rg[2], rh[2];
+  for (int q = 0; q < 4; ++q) {
+    float u[2] = {bf16_lo(uw[q]), bf16_hi(uw[q])}, g[2] = {bf16_lo(gw[q]), bf16_hi(gw[q])};
+    float d[2] = {bf16_lo(dw[q]), bf16_hi(dw[q])}, ru[2], rg[2], rh[2];
 #pragma unroll
-      for (int z = 0; z < 2; ++z) {
-        const float s = 1.0f / (1.0f + expf(-g[z]));
-        const float si = g[z] * s;
-        rh[z] = si * u[z];
-        ru[z] = d[z] * si;
-        rg[z] = d[z] * u[z] * (s * (1.0f + g[z] * (1.0f - s)));
-      }
-      du[q] = pack_bf16x2(ru[0], ru[1]);
-      dg[q] = pack_bf16x2(rg[0], rg[1]);
-      hh[q] = pack_bf16x2(rh[0], rh[1]);
+    for (int z = 0; z < 2; ++z) {
+      const float s = 1.0f / (1.0f + expf(-g[z]));
+      const float si = g[z] * s;
+      rh[z] = si * u[z];
+      ru[z] = d[z] * si;
+      rg[z] = d[z] * u[z] * (s * (1.0f + g[z] * (1.0f - s)));
     }
-    dUG[p * 2 * h8 + c] = make_uint4(du[0], du[1], du[2], du[3]);
-    dUG[p * 2 * h8 + h8 + c] = make_uint4(dg[0], dg[1], dg[2], dg[3]);
-    H[p * h8 + c] = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+    du[q] = pack_bf16x2(ru[0], ru[1]);
+    dg[q] = pack_bf16x2(rg[0], rg[1]);
+    hh[q] = pack_bf16x2(rh[0], rh[1]);
+  }
+  du_out = make_uint4(du[0], du[1], du[2], du[3]);
+  dg_out = make_uint4(dg[0], dg[1], dg[2], dg[3]);
+  h_out = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+}
+
+// Warp per row of the padded layout (persistent blocks, the offsets in shared memory).  Row pr of
+// expert e, r = pr - 64 k_off[e]: for r < count, [u | g] from UG row off[e] + r (from_dense: the
+// forward's saved pre-activations, dense rows) or row pr (recomputed in the padded layout), dH
+// from row pr; dUG = [dU | dG] and H to row pr.  Rows past an expert's count get zeros whatever
+// dH holds there, so the GEMMs around this step may leave anything finite in dH's padding rows.
+__global__ void __launch_bounds__(256) swiglu_backward_kernel(const uint4* __restrict__ UG, int from_dense,
+                                                               const int32_t* __restrict__ off,
+                                                               const int32_t* __restrict__ k_off, int E,
+                                                               const uint4* __restrict__ dH, long long prows, int h8,
+                                                               uint4* __restrict__ dUG, uint4* __restrict__ H) {
+  extern __shared__ int32_t s_tab[];   // off[0..E], k_off[0..E]
+  int32_t* s_off = s_tab;
+  int32_t* s_koff = s_tab + E + 1;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
+    s_off[i] = off[i];
+    s_koff[i] = k_off[i];
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long used = prows < 64ll * s_koff[E] ? prows : 64ll * s_koff[E];   // rows past these are never read
+  for (long long pr = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pr < used; pr += nw) {
+    const int kt = (int)(pr / 64);
+    int lo = 0, hi = E - 1;   // last e with k_off[e] <= kt (an expert with rows owns the tile)
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_koff[mid] <= kt) lo = mid; else hi = mid - 1;
+    }
+    const int r = (int)(pr - 64ll * s_koff[lo]);
+    uint4* du = dUG + pr * 2 * h8;
+    uint4* hr = H + pr * h8;
+    if (r >= s_off[lo + 1] - s_off[lo]) {
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = lane; c < h8; c += 32) {
+        du[c] = z;
+        du[h8 + c] = z;
+        hr[c] = z;
+      }
+      continue;
+    }
+    const uint4* ug = UG + (from_dense ? (long long)s_off[lo] + r : pr) * 2 * h8;
+    const uint4* dh = dH + pr * h8;
+    for (int c0 = lane; c0 < h8; c0 += 64) {   // two chunks (six 16-byte loads) in flight per lane
+      const bool two = c0 + 32 < h8;
+      const uint4 u0 = ug[c0], g0 = ug[h8 + c0], d0 = dh[c0];
+      uint4 u1 = u0, g1 = g0, d1 = d0;
+      if (two) {
+        u1 = ug[c0 + 32];
+        g1 = ug[h8 + c0 + 32];
+        d1 = dh[c0 + 32];
+      }
+      uint4 a, b, c;
+      swiglu_bwd_chunk(u0, g0, d0, a, b, c);
+      du[c0] = a;
+      du[h8 + c0] = b;
+      hr[c0] = c;
+      if (two) {
+        swiglu_bwd_chunk(u1, g1, d1, a, b, c);
+        du[c0 + 32] = a;
+        du[h8 + c0 + 32] = b;
+        hr[c0 + 32] = c;
+      }
+    }
   }
 }
 
-cudaError_t launch_swiglu_backward(const void* UG, const void* dH, long long rows, int h, void* dUG, void* H,
-                                   cudaStream_t st) {
-  const long long n = rows * (h / 8);
-  if (n <= 0) return cudaSuccess;
-  const int blocks = (int)std::min<long long>((n + 255) / 256, 8192);
-  swiglu_backward_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(UG), static_cast<const uint4*>(dH), rows,
-                                                 h / 8, static_cast<uint4*>(dUG), static_cast<uint4*>(H));
+cudaError_t launch_swiglu_backward(const void* UG, int from_dense, const int32_t* off, const int32_t* k_off, int E,
+                                   const void* dH, long long prows, int h, void* dUG, void* H, cudaStream_t st) {
+  if (prows <= 0) return cudaSuccess;
+  if (h % 8 || E < 1 || E > 1024) return cudaErrorInvalidValue;
+  const long long want = (prows + 7) / 8;
+  const int blocks = (int)std::min<long long>(want, (long long)num_sms() * 8);
+  swiglu_backward_kernel<<<blocks, 256, 2 * (E + 1) * sizeof(int32_t), st>>>(
+      static_cast<const uint4*>(UG), from_dense, off, k_off, E, static_cast<const uint4*>(dH), prows, h / 8,
+      static_cast<uint4*>(dUG), static_cast<uint4*>(H));
   return cudaGetLastError();
 }
 

@@ -58,6 +58,9 @@ struct GemmParams {
   int a_src_rows;
   int b_mn;                // 1: B is MN-major, group g's K rows [g * b_rows_per_group, ...) x N columns
   int a_mn;                // 1 (K-grouped, 1 CTA): A is MN-major, K rows x M columns
+  const int* a_off;        // non-null: group g's A rows start at A row a_off[g] (see a_row_shift)
+  void* preact;            // SwiGLU: also store [u | g] (bf16) here, preact_ld elements per row
+  long long preact_ld;
   int* status;
 };
 
@@ -76,7 +79,7 @@ struct GemmCfg {
   static constexpr int HOLDER_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int ABORT_OFF = HOLDER_OFF + 4;
   static constexpr int TABLE_OFF = (ABORT_OFF + 4 + 15) & ~15;
-  static constexpr int EPI_OFF = (TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 127) & ~127;  // epilogue staging
+  static constexpr int EPI_OFF = (TABLE_OFF + 3 * (kMaxGroups + 1) * 4 + 127) & ~127;  // epilogue staging
   static constexpr int SMEM_BYTES = EPI_OFF + kEpiStageBytes + 1024;                  // + alignment slack
   static_assert(B_BYTES % 1024 == 0, "B tile must keep 1024-byte alignment");
   static_assert(BN % 32 == 0 && BN >= 32 && BN <= 256, "UMMA N for M=128, whole 32-column epilogue chunks");
@@ -132,6 +135,17 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
   c.kt0 = c.split * p.kt_per_split;
   c.kt1 = min(p.kt_total, c.kt0 + p.kt_per_split);
   return c;
+}
+
+// With a_off, the A rows of group g are read from a_off[g] on instead of the output's own rows:
+// M-grouped, output row r of group g multiplies A row r - group_off[g] + a_off[g]; K-grouped
+// (MN-major A), the group's K rows start at A row a_off[g] instead of 64 k_off[g].  The rows a
+// tile reads past the group's end are A's next rows (zeros past A's last row); the caller makes
+// the other operand zero there.
+__device__ __forceinline__ int a_row_shift(const GemmParams& p, const TileCoord& c, const int* s_goff,
+                                           const int* s_aoff) {
+  if (!p.a_off) return 0;
+  return s_aoff[c.group] - (p.k_groups > 0 ? BK * s_goff[c.group] : s_goff[c.group]);
 }
 
 // Stores a warp's block of 32 rows x 64 bytes (thread i holds row i as 16 words: 32 bf16 or 16
@@ -204,6 +218,17 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
             u[i] = __float_as_uint(__uint_as_float(u[i]) * rs * __ldg(cs + cc * 32 + i));
             g[i] = __float_as_uint(__uint_as_float(g[i]) * rs * __ldg(cs_gate + cc * 32 + i));
           }
+        }
+        if (p.preact) {   // the pre-activations [u | g] in bf16, kept for the backward
+          __nv_bfloat16* pre = reinterpret_cast<__nv_bfloat16*>(p.preact) + wrow0 * p.preact_ld + col0;
+          uint32_t pu[16], pg[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            pu[i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+            pg[i] = pack_bf16x2(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+          }
+          store_block_bf16(stg, pu, pre, p.preact_ld, valid, lane);
+          store_block_bf16(stg, pg, pre + p.N, p.preact_ld, valid, lane);
         }
         uint32_t packed[16];
 #pragma unroll
@@ -383,6 +408,7 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
   int* s_toff = reinterpret_cast<int*>(smem + C::TABLE_OFF);
   int* s_goff = s_toff + (kMaxGroups + 1);
+  int* s_aoff = s_goff + (kMaxGroups + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -397,6 +423,8 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
   } else if (p.k_groups > 0) {
     for (int i = threadIdx.x; i <= p.k_groups; i += blockDim.x) s_goff[i] = p.k_off[i];
   }
+  if (p.a_off)
+    for (int i = threadIdx.x; i <= max(p.num_groups, p.k_groups); i += blockDim.x) s_aoff[i] = p.a_off[i];
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < C::STAGES; ++s) {
@@ -430,6 +458,7 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
       uint32_t stage = 0, phase = 0;
       for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
         const TileCoord c = decode_tile(t, p, s_toff, s_goff);
+        const int ash = a_row_shift(p, c, s_goff, s_aoff);
         const int brow = c.group * p.b_rows_per_group + c.nt * (EPI == EPI_SWIGLU ? BN / 2 : BN);
         bool ok = true;
         for (int kt = c.kt0; kt < c.kt1; ++kt) {
@@ -439,10 +468,10 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
           mbar_arrive_expect_tx(&full_bar[stage], GA ? C::B_BYTES : C::STAGE_BYTES);
           const int kx = kt * (F8 ? 2 * BK : BK);   // 128 bytes of K per k-tile: 64 bf16 or 128 e4m3
           if (p.a_mn) {   // MN-major A: 64 K rows x 128 M columns as two 64-column blocks (8 KB each)
-            tma_load_2d(sa, &tmA, &full_bar[stage], c.row0, kt * BK);
-            tma_load_2d(sa + 8192, &tmA, &full_bar[stage], c.row0 + 64, kt * BK);
+            tma_load_2d(sa, &tmA, &full_bar[stage], c.row0, kt * BK + ash);
+            tma_load_2d(sa + 8192, &tmA, &full_bar[stage], c.row0 + 64, kt * BK + ash);
           } else if (!GA) {
-            tma_load_2d(sa, &tmA, &full_bar[stage], kx, c.row0);
+            tma_load_2d(sa, &tmA, &full_bar[stage], kx, c.row0 + ash);
           }
           if (EPI == EPI_SWIGLU) {
             tma_load_2d(sb, &tmB, &full_bar[stage], kx, brow);
@@ -576,7 +605,7 @@ struct PairCfg {
   static constexpr int HOLDER_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int ABORT_OFF = HOLDER_OFF + 4;
   static constexpr int TABLE_OFF = (ABORT_OFF + 4 + 15) & ~15;
-  static constexpr int EPI_OFF = (TABLE_OFF + 2 * (kMaxGroups + 1) * 4 + 127) & ~127;
+  static constexpr int EPI_OFF = (TABLE_OFF + 3 * (kMaxGroups + 1) * 4 + 127) & ~127;
   static constexpr int SMEM_BYTES = EPI_OFF + kEpiStageBytes + 1024;
 };
 
@@ -598,6 +627,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
   int* s_toff = reinterpret_cast<int*>(smem + C::TABLE_OFF);
   int* s_goff = s_toff + (kMaxGroups + 1);
+  int* s_aoff = s_goff + (kMaxGroups + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -613,6 +643,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
   } else if (p.k_groups > 0) {
     for (int i = threadIdx.x; i <= p.k_groups; i += blockDim.x) s_goff[i] = p.k_off[i];
   }
+  if (p.a_off)
+    for (int i = threadIdx.x; i <= max(p.num_groups, p.k_groups); i += blockDim.x) s_aoff[i] = p.a_off[i];
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < C::STAGES; ++s) {
@@ -648,6 +680,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
       for (int t = pair; t < total_tiles && ok; t += npairs) {
         const TileCoord c = decode_tile<BM2>(t, p, s_toff, s_goff);
         const int arow = c.row0 + 128 * (int)rank;
+        const int ash = a_row_shift(p, c, s_goff, s_aoff);
         const int brow = EPI == EPI_SWIGLU
                              ? c.group * p.b_rows_per_group + c.nt * 128 + (rank ? p.b_gate_offset : 0)
                              : c.group * p.b_rows_per_group + c.nt * C::BN + 128 * (int)rank;
@@ -663,10 +696,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
           const int kx = kt * (F8 ? 2 * BK : BK);
           if (!GA && (rank == 0 || a1)) {
             if (p.a_mn) {   // MN-major A: this CTA's 128 M columns as two 64-column blocks
-              tma_load_2d_pair(sa, &tmA, full0, arow, kt * BK);
-              tma_load_2d_pair(sa + 8192, &tmA, full0, arow + 64, kt * BK);
+              tma_load_2d_pair(sa, &tmA, full0, arow, kt * BK + ash);
+              tma_load_2d_pair(sa + 8192, &tmA, full0, arow + 64, kt * BK + ash);
             } else {
-              tma_load_2d_pair(sa, &tmA, full0, kx, arow);
+              tma_load_2d_pair(sa, &tmA, full0, kx, arow + ash);
             }
           }
           if (EPI != EPI_SWIGLU && p.b_mn) {   // MN-major B: this CTA's 128 columns as two 64-column blocks
@@ -907,6 +940,14 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   if (q.a_mn_major && (q.num_groups > 0 || f8 || q.K % BK || (q.a_cols && q.a_cols < q.M) ||
                        (q.mn_rows && q.mn_rows > q.K)))
     return cudaErrorInvalidValue;
+  // A rows read from a_off[g] on: grouped (M or K) bf16 operands, TMA-loaded A
+  if (q.a_off && (ga || f8 || (q.num_groups == 0 && q.k_groups == 0) || (q.k_groups > 0 && !q.a_mn_major) ||
+                  q.a_rows < 0))
+    return cudaErrorInvalidValue;
+  if (q.a_rows && (q.a_mn_major || !q.a_off)) return cudaErrorInvalidValue;
+  // pre-activations kept by the SwiGLU epilogue: whole 32-column chunks of u and of g
+  if (q.preact && (q.epilogue != EPI_SWIGLU || q.N % 32 || q.preact_ld < 2 * (int64_t)q.N || q.preact_ld % 8))
+    return cudaErrorInvalidValue;
   const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
   CUtensorMap ta, tb;
   if (q.b_mn_major) {
@@ -917,7 +958,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   if (ga)
     ta = tb;   // unused
   else if (q.a_mn_major ? !make_tmap(&ta, q.A, q.mn_rows ? q.mn_rows : q.K, q.a_cols ? q.a_cols : q.M, BK, false)
-                        : !make_tmap(&ta, q.A, q.M, q.K, BM, f8))
+                        : !make_tmap(&ta, q.A, q.a_rows ? q.a_rows : q.M, q.K, BM, f8))
     return cudaErrorInvalidValue;
 
   GemmParams gp;
@@ -948,6 +989,9 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.a_src_rows = q.a_src_rows;
   gp.b_mn = q.b_mn_major;
   gp.a_mn = q.a_mn_major;
+  gp.a_off = q.a_off;
+  gp.preact = q.preact;
+  gp.preact_ld = q.preact_ld;
   gp.status = q.status;
 
   if (ga) {

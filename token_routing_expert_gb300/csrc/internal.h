@@ -45,6 +45,13 @@ struct GemmProblem {
                           // row; A is then unused.  e4m3: a_scale is per a_src row.
   const void* a_src;      // (a_src_rows, K) bf16 or e4m3
   int a_src_rows;
+  const int* a_off;       // non-NULL (grouped bf16, TMA-loaded A): group g's A rows start at A row a_off[g]
+                          //   (M-grouped: in place of group_off[g]; K-grouped MN-major A: in place of
+                          //   64 k_off[g]); rows a tile reads past the group are A's next rows or, past
+                          //   A's end, zeros, so the other operand must be zero there
+  int64_t a_rows;         // with a_off, M-grouped: rows present in A (0: M)
+  void* preact;           // SwiGLU: non-NULL also stores [u | g] bf16, preact_ld elements per output row
+  int64_t preact_ld;
   int* status;
 };
 
@@ -99,8 +106,8 @@ cudaError_t launch_pad_rows(const void* src, const int32_t* gather, const int32_
                             int src_rows, int cols, long long max_rows, void* dst, int* status, cudaStream_t st);
 cudaError_t launch_pad_scatter(const int32_t* scatter, int R, const int32_t* off, const int32_t* poff, int E,
                                int32_t* out, cudaStream_t st);
-cudaError_t launch_swiglu_backward(const void* UG, const void* dH, long long rows, int h, void* dUG, void* H,
-                                   cudaStream_t st);
+cudaError_t launch_swiglu_backward(const void* UG, int from_dense, const int32_t* off, const int32_t* k_off, int E,
+                                   const void* dH, long long prows, int h, void* dUG, void* H, cudaStream_t st);
 cudaError_t launch_combine_backward(const void* dz, const void* y, const int32_t* scatter_idx, const float* w, int T,
                                     int k, int L, int rows, void* dy, float* dw, int* status, cudaStream_t st);
 cudaError_t launch_zero_padding_rows(const int32_t* gather_idx, int rows, int cols, void* dst, cudaStream_t st);

@@ -52,7 +52,8 @@ EXPORTS = ["moe_quantize_rowwise_fp8", "moe_expert_capacity", "moe_permuted_rows
            "moe_layer_forward_launches", "moe_workspace_layout", "moe_get_status", "moe_status_string",
            "moe_permute_noalloc", "moe_accumulate_counts", "moe_load_imbalance", "moe_score_bias_update",
            "moe_backward_workspace_size", "moe_combine_backward", "moe_grouped_swiglu_backward",
-           "moe_router_backward", "moe_host_workspace_size", "moe_layer_forward_host_batches"]
+           "moe_router_backward", "moe_host_workspace_size", "moe_layer_forward_host_batches",
+           "moe_grouped_swiglu_preact", "moe_layer_forward_preact", "moe_grouped_swiglu_backward_preact"]
 
 _lib = None
 
@@ -79,10 +80,12 @@ def load() -> ctypes.CDLL:
         "moe_router": [cfgp, wp, VP, I64, VP, VP, VP, VP, SZ, VP],
         "moe_permute": [cfgp, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
         "moe_grouped_swiglu": [cfgp, wp, VP, VP, VP, I64, VP, VP, SZ, VP],
+        "moe_grouped_swiglu_preact": [cfgp, wp, VP, VP, VP, I64, VP, VP, VP, SZ, VP],
         "moe_combine": [cfgp, VP, VP, VP, I64, VP, VP],
         "moe_latent_down": [cfgp, wp, VP, I64, VP, VP, SZ, VP],
         "moe_latent_restore": [cfgp, wp, VP, I64, VP, VP, SZ, VP],
         "moe_layer_forward": [cfgp, wp, VP, I64, VP, VP, SZ, VP],
+        "moe_layer_forward_preact": [cfgp, wp, VP, I64, VP, VP, VP, SZ, VP],
         "moe_layer_forward_staged": [cfgp, wp, VP, I64, VP, VP, SZ, VP, P(VP)],
         "moe_layer_forward_launches": [cfgp, I64, P(ctypes.c_int32)],
         "moe_host_workspace_size": [cfgp, I64, P(SZ)],
@@ -96,6 +99,7 @@ def load() -> ctypes.CDLL:
         "moe_router_backward": [cfgp, wp, VP, I64, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP],
         "moe_combine_backward": [cfgp, VP, VP, VP, VP, VP, I64, VP, VP, VP],
         "moe_grouped_swiglu_backward": [cfgp, wp, VP, VP, VP, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
+        "moe_grouped_swiglu_backward_preact": [cfgp, wp, VP, VP, VP, VP, I64, VP, VP, VP, VP, VP, VP, SZ, VP],
         "moe_load_imbalance": [VP, ctypes.c_int32, ctypes.c_int32, VP, VP],
         "moe_score_bias_update": [VP, ctypes.c_int32, ctypes.c_float, VP, VP],
     }
@@ -327,6 +331,25 @@ def moe_grouped_swiglu(cfg, weights: DeviceWeights, x_routed, gather_idx, offset
     return y
 
 
+def moe_grouped_swiglu_preact(cfg, weights: DeviceWeights, x_routed, gather_idx, offsets, ws, y=None, preact=None,
+                              stream=None):
+    """moe_grouped_swiglu that also returns the pre-activations [u | g] ((rows, 2h) bf16)."""
+    T = x_routed.shape[0]
+    Lr = x_routed.shape[1]
+    rows = moe_permuted_rows(cfg, T)
+    dev = x_routed.device
+    y = torch.empty((max(rows, 1), Lr), dtype=torch.bfloat16, device=dev) if y is None else y
+    preact = (torch.empty((max(rows, 1), 2 * cfg.hidden_size), dtype=torch.bfloat16, device=dev)
+              if preact is None else preact)
+    ws_ = weights.struct()
+    _check(load().moe_grouped_swiglu_preact(
+        ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x_routed, torch.bfloat16, "x_routed"),
+        _ptr(gather_idx, torch.int32, "gather_idx"), _ptr(offsets, torch.int32, "offsets"), T,
+        _ptr(y, torch.bfloat16, "y"), _ptr(preact, torch.bfloat16, "preact"), _ptr(ws, None, "ws"), ws.numel(),
+        _stream(stream)), "moe_grouped_swiglu_preact")
+    return y, preact
+
+
 def moe_combine(cfg, y, scatter_idx, w, T, z=None, stream=None):
     Lr = y.shape[1]
     z = torch.empty((T, Lr), dtype=torch.bfloat16, device=y.device) if z is None else z
@@ -364,6 +387,21 @@ def moe_layer_forward(cfg, weights: DeviceWeights, x, ws, out=None, stream=None)
                                     _ptr(out, torch.bfloat16, "out"), _ptr(ws, None, "ws"), ws.numel(),
                                     _stream(stream)), "moe_layer_forward")
     return out
+
+
+def moe_layer_forward_preact(cfg, weights: DeviceWeights, x, ws, out=None, preact=None, stream=None):
+    """The layer forward that keeps the experts' pre-activations: (out, preact (rows, 2h) bf16)."""
+    T = x.shape[0]
+    out = torch.empty((T, cfg.d_model), dtype=torch.bfloat16, device=x.device) if out is None else out
+    rows = moe_permuted_rows(cfg, T)
+    preact = (torch.empty((max(rows, 1), 2 * cfg.hidden_size), dtype=torch.bfloat16, device=x.device)
+              if preact is None else preact)
+    ws_ = weights.struct()
+    _check(load().moe_layer_forward_preact(ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x, torch.bfloat16, "x"), T,
+                                           _ptr(out, torch.bfloat16, "out"), _ptr(preact, torch.bfloat16, "preact"),
+                                           _ptr(ws, None, "ws"), ws.numel(), _stream(stream)),
+           "moe_layer_forward_preact")
+    return out, preact
 
 
 def _host_ptr(t: torch.Tensor, name: str) -> int:
@@ -462,6 +500,26 @@ def moe_grouped_swiglu_backward(cfg, weights: DeviceWeights, x_routed, gather_id
         _ptr(dx_routed, torch.bfloat16, "dx_routed"), _ptr(dw_up_gate, torch.float32, "dw_up_gate"),
         _ptr(dw_out, torch.float32, "dw_out"), _ptr(bws, None, "ws"), bws.numel(), _stream(stream)),
         "moe_grouped_swiglu_backward")
+    return dx_routed, dw_up_gate, dw_out
+
+
+def moe_grouped_swiglu_backward_preact(cfg, weights: DeviceWeights, x_routed, gather_idx, offsets, scatter_idx, dy,
+                                       preact, bws, dx_routed=None, dw_up_gate=None, dw_out=None, stream=None):
+    """moe_grouped_swiglu_backward from the forward's saved pre-activations (preact (rows, 2h) bf16)."""
+    T, Lr = x_routed.shape
+    E, h = cfg.num_experts, cfg.hidden_size
+    dev = x_routed.device
+    dx_routed = torch.empty((T, Lr), dtype=torch.bfloat16, device=dev) if dx_routed is None else dx_routed
+    dw_up_gate = torch.empty((E, 2 * h, Lr), dtype=torch.float32, device=dev) if dw_up_gate is None else dw_up_gate
+    dw_out = torch.empty((E, Lr, h), dtype=torch.float32, device=dev) if dw_out is None else dw_out
+    ws_ = weights.struct()
+    _check(load().moe_grouped_swiglu_backward_preact(
+        ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x_routed, torch.bfloat16, "x_routed"),
+        _ptr(gather_idx, torch.int32, "gather_idx"), _ptr(offsets, torch.int32, "offsets"),
+        _ptr(scatter_idx, torch.int32, "scatter_idx"), T, _ptr(dy, torch.bfloat16, "dy"),
+        _ptr(preact, torch.bfloat16, "preact"), _ptr(dx_routed, torch.bfloat16, "dx_routed"),
+        _ptr(dw_up_gate, torch.float32, "dw_up_gate"), _ptr(dw_out, torch.float32, "dw_out"),
+        _ptr(bws, None, "ws"), bws.numel(), _stream(stream)), "moe_grouped_swiglu_backward_preact")
     return dx_routed, dw_up_gate, dw_out
 
 

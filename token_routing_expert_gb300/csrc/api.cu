@@ -450,7 +450,7 @@ int run_restore(const moe_config_t* c, const moe_weights_t* w, const void* z, bo
 // Workspace of the experts' backward.
 struct BwdPlan {
   int64_t rows, kpad;
-  size_t xp, ug, dh, h, dug, dxp, k_off, poff, tile_off, scat, total;
+  size_t xp, ug, h, dug, dxp, k_off, poff, tile_off, scat, total;
 };
 
 void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
@@ -467,7 +467,6 @@ void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
   // every activation in the padded row layout: kpad rows, expert e from row 64 k_off[e]
   b->xp = take((size_t)b->kpad * Lr * 2);
   b->ug = take((size_t)b->kpad * 2 * h * 2);
-  b->dh = take((size_t)b->kpad * h * 2);
   b->h = take((size_t)b->kpad * h * 2);
   b->dug = take((size_t)b->kpad * 2 * h * 2);
   b->dxp = take((size_t)b->kpad * Lr * 2);
@@ -1083,7 +1082,6 @@ int moe_grouped_swiglu_backward_preact(const moe_config_t* c, const moe_weights_
   int32_t* scat = at<int32_t>(ws, b.scat);
   void* xp = at<void>(ws, b.xp);
   void* UG = at<void>(ws, b.ug);
-  void* dH = at<void>(ws, b.dh);
   void* H = at<void>(ws, b.h);
   void* dUG = at<void>(ws, b.dug);
   void* dXp = at<void>(ws, b.dxp);
@@ -1098,16 +1096,40 @@ int moe_grouped_swiglu_backward_preact(const moe_config_t* c, const moe_weights_
   if (s == MOE_OK && !preact)
     s = grouped_bf16(xp, prows, w->w_up_gate, (int64_t)E * 2 * h, 2 * h, 2 * h, Lr, poff, tile_off, E, pair, UG,
                      status, st);
-  // dH = dY W_out, dY read at its dense rows (each group's A rows from offsets[e]; what a tile reads
-  // past the group only reaches dH's padding rows, which the SwiGLU backward ignores) ; SwiGLU
-  // backward (zeros in the padding rows of dUG and H) ; dXp = dUG W_up_gate ; dx = sum over a
-  // token's rows.  The weights are read as stored (K rows x N columns: MN-major B operands).
-  if (s == MOE_OK)
-    s = grouped_bf16(dy, prows, w->w_out, (int64_t)E * Lr, Lr, h, Lr, poff, tile_off, E, pair, dH, status, st, 1,
-                     offsets, rows);
-  if (s == MOE_OK)
-    s = cuda_status(launch_swiglu_backward(preact ? preact : UG, preact ? 1 : 0, offsets, k_off, E, dH, prows, h, dUG,
-                                           H, st));
+  // dH = dY W_out with the SwiGLU backward in its epilogue: dY read at its dense rows (each group's
+  // A rows from offsets[e]; what a tile reads past the group only reaches padding rows, which get
+  // zeros), [u | g] read beside each dH chunk, dUG = [dU | dG] and H written in the padded layout.
+  // Then dXp = dUG W_up_gate and dx = the sum over a token's rows.  The weights are read as stored
+  // (K rows x N columns: MN-major B operands).
+  if (s == MOE_OK) {
+    GemmProblem g{};
+    g.A = dy;
+    g.a_off = offsets;
+    g.a_rows = rows;
+    g.B = w->w_out;
+    g.b_mn_major = 1;
+    g.b_rows_total = (int64_t)E * Lr;
+    g.b_rows_per_group = Lr;
+    g.M = prows;
+    g.N = h;
+    g.K = Lr;
+    g.num_groups = E;
+    g.group_off = poff;
+    g.tile_off = tile_off;
+    g.epilogue = EPI_SWIGLU_BWD;
+    g.bn = 256;
+    g.splits = 1;
+    g.pair_tiles = pair;
+    g.preact = preact ? const_cast<void*>(preact) : UG;
+    g.preact_ld = 2 * (int64_t)h;
+    g.preact_dense = preact ? 1 : 0;
+    g.out = dUG;
+    g.ldo = 2 * (int64_t)h;
+    g.out2 = H;
+    g.ldo2 = h;
+    g.status = status;
+    s = cuda_status(launch_gemm(g, st));
+  }
   if (s == MOE_OK)
     s = grouped_bf16(dUG, prows, w->w_up_gate, (int64_t)E * 2 * h, 2 * h, Lr, 2 * h, poff, tile_off, E, pair, dXp,
                      status, st, 1);

@@ -9,7 +9,9 @@
 // operand as stored (weights and activations as MN-major operands where the contraction runs
 // along their rows), so nothing is transposed:
 //   UG  = Xp W_up_gate^T            (pre-activations: the forward's, kept, or recomputed; bf16)
-//   dH  = dY W_out                  (W_out as an MN-major B; dY read at the dense rows)
+//   dH  = dY W_out                  (W_out as an MN-major B; dY read at the dense rows; the SwiGLU
+//                                    backward runs in this GEMM's epilogue: dUG and H out, dH is
+//                                    never stored)
 //   dXp = dUG W_up_gate             (W_up_gate as an MN-major B)
 //   dW_out[e]     = dY_e^T H_e      (K-grouped over the expert's rows, MN-major A and B; dY dense)
 //   dW_up_gate[e] = dUG_e^T Xp_e    (K-grouped)
@@ -139,149 +141,71 @@ cudaError_t launch_pad_scatter(const int32_t* scatter, int R, const int32_t* off
   return cudaGetLastError();
 }
 
-// SwiGLU backward of one 16-byte chunk (8 columns): from u, g and dH, H = silu(g) u,
-// dU = dH silu(g), dG = dH u silu'(g), silu'(g) = s (1 + g (1 - s)), s = sigmoid(g); fp32,
-// stored bf16.
-__device__ __forceinline__ void swiglu_bwd_chunk(uint4 uv, uint4 gv, uint4 dv, uint4& du_out, uint4& dg_out,
-                                                 uint4& h_out) {
-  const uint32_t uw[4] = {uv.x, uv.y, uv.z, uv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w}, dw[4] = {dv.x, dv.y, dv.z, dv.w};
-  uint32_t du[4], dg[4], hh[4];
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    float u[2] = {bf16_lo(uw[q]), bf16_hi(uw[q])}, g[2] = {bf16_lo(gw[q]), bf16_hi(gw[q])};
-    float d[2] = {bf16_lo(dw[q]), bf16_hi(dw[q])}, ru[2], rg[2], rh[2];
-#pragma unroll
-    for (int z = 0; z < 2; ++z) {
-      const float s = 1.0f / (1.0f + expf(-g[z]));
-      const float si = g[z] * s;
-      rh[z] = si * u[z];
-      ru[z] = d[z] * si;
-      rg[z] = d[z] * u[z] * (s * (1.0f + g[z] * (1.0f - s)));
-    }
-    du[q] = pack_bf16x2(ru[0], ru[1]);
-    dg[q] = pack_bf16x2(rg[0], rg[1]);
-    hh[q] = pack_bf16x2(rh[0], rh[1]);
-  }
-  du_out = make_uint4(du[0], du[1], du[2], du[3]);
-  dg_out = make_uint4(dg[0], dg[1], dg[2], dg[3]);
-  h_out = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-}
-
-// Warp per row of the padded layout (persistent blocks, the offsets in shared memory).  Row pr of
-// expert e, r = pr - 64 k_off[e]: for r < count, [u | g] from UG row off[e] + r (from_dense: the
-// forward's saved pre-activations, dense rows) or row pr (recomputed in the padded layout), dH
-// from row pr; dUG = [dU | dG] and H to row pr.  Rows past an expert's count get zeros whatever
-// dH holds there, so the GEMMs around this step may leave anything finite in dH's padding rows.
-__global__ void __launch_bounds__(256) swiglu_backward_kernel(const uint4* __restrict__ UG, int from_dense,
-                                                               const int32_t* __restrict__ off,
-                                                               const int32_t* __restrict__ k_off, int E,
-                                                               const uint4* __restrict__ dH, long long prows, int h8,
-                                                               uint4* __restrict__ dUG, uint4* __restrict__ H) {
-  extern __shared__ int32_t s_tab[];   // off[0..E], k_off[0..E]
-  int32_t* s_off = s_tab;
-  int32_t* s_koff = s_tab + E + 1;
-  for (int i = threadIdx.x; i <= E; i += blockDim.x) {
-    s_off[i] = off[i];
-    s_koff[i] = k_off[i];
-  }
-  __syncthreads();
-  const int lane = threadIdx.x & 31;
-  const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
-  const long long used = prows < 64ll * s_koff[E] ? prows : 64ll * s_koff[E];   // rows past these are never read
-  for (long long pr = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); pr < used; pr += nw) {
-    const int kt = (int)(pr / 64);
-    int lo = 0, hi = E - 1;   // last e with k_off[e] <= kt (an expert with rows owns the tile)
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (s_koff[mid] <= kt) lo = mid; else hi = mid - 1;
-    }
-    const int r = (int)(pr - 64ll * s_koff[lo]);
-    uint4* du = dUG + pr * 2 * h8;
-    uint4* hr = H + pr * h8;
-    if (r >= s_off[lo + 1] - s_off[lo]) {
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      for (int c = lane; c < h8; c += 32) {
-        du[c] = z;
-        du[h8 + c] = z;
-        hr[c] = z;
-      }
-      continue;
-    }
-    const uint4* ug = UG + (from_dense ? (long long)s_off[lo] + r : pr) * 2 * h8;
-    const uint4* dh = dH + pr * h8;
-    for (int c0 = lane; c0 < h8; c0 += 64) {   // two chunks (six 16-byte loads) in flight per lane
-      const bool two = c0 + 32 < h8;
-      const uint4 u0 = ug[c0], g0 = ug[h8 + c0], d0 = dh[c0];
-      uint4 u1 = u0, g1 = g0, d1 = d0;
-      if (two) {
-        u1 = ug[c0 + 32];
-        g1 = ug[h8 + c0 + 32];
-        d1 = dh[c0 + 32];
-      }
-      uint4 a, b, c;
-      swiglu_bwd_chunk(u0, g0, d0, a, b, c);
-      du[c0] = a;
-      du[h8 + c0] = b;
-      hr[c0] = c;
-      if (two) {
-        swiglu_bwd_chunk(u1, g1, d1, a, b, c);
-        du[c0 + 32] = a;
-        du[h8 + c0 + 32] = b;
-        hr[c0 + 32] = c;
-      }
-    }
-  }
-}
-
-cudaError_t launch_swiglu_backward(const void* UG, int from_dense, const int32_t* off, const int32_t* k_off, int E,
-                                   const void* dH, long long prows, int h, void* dUG, void* H, cudaStream_t st) {
-  if (prows <= 0) return cudaSuccess;
-  if (h % 8 || E < 1 || E > 1024) return cudaErrorInvalidValue;
-  const long long want = (prows + 7) / 8;
-  const int blocks = (int)std::min<long long>(want, (long long)num_sms() * 8);
-  swiglu_backward_kernel<<<blocks, 256, 2 * (E + 1) * sizeof(int32_t), st>>>(
-      static_cast<const uint4*>(UG), from_dense, off, k_off, E, static_cast<const uint4*>(dH), prows, h / 8,
-      static_cast<uint4*>(dUG), static_cast<uint4*>(H));
-  return cudaGetLastError();
-}
-
 // Warp per token: dy[p] = w[t, j] dz[t] (bf16) and dw[t, j] = <dz[t], y[p]> (fp32) for each
-// assignment with a row p (p = -1: dropped, dw = 0).
+// assignment with a row p (p = -1: dropped, dw = 0).  The token's dz row is held in registers,
+// 256 16-byte chunks (eight per lane) at a time, and each y row's chunks are loaded together.
 __global__ void __launch_bounds__(128) combine_backward_kernel(const uint4* __restrict__ dz, const uint4* __restrict__ y,
                                                                 const int32_t* __restrict__ scatter_idx,
                                                                 const float* __restrict__ w, int T, int k, int vec,
                                                                 int rows, uint4* __restrict__ dy,
                                                                 float* __restrict__ dw, int* status) {
-  const int lane = threadIdx.x & 31;
-  const long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  __shared__ float s_dot[4][32];
+  const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
+  const long long t = (long long)blockIdx.x * (blockDim.x >> 5) + wi;
   if (t >= T) return;
-  const uint4* dzr = dz + t * vec;
-  for (int j = 0; j < k; ++j) {
-    const int p = scatter_idx[t * k + j];
-    const float wj = w[t * k + j];
-    if (p < 0 || p >= rows) {
-      if (p != -1 && lane == 0) set_status(status, MOE_ERR_BOUNDS);
-      if (lane == 0) dw[t * k + j] = 0.f;
-      continue;
+  // lane j (< k) holds assignment j's row and weight; broadcast by shuffles
+  int my_p = -1;
+  float my_w = 0.f;
+  if (lane < k) {
+    my_p = scatter_idx[t * k + lane];
+    my_w = w[t * k + lane];
+    if (my_p < -1 || my_p >= rows) {
+      set_status(status, MOE_ERR_BOUNDS);
+      my_p = -1;
     }
-    float dot = 0.f;
-    for (int c = lane; c < vec; c += 32) {
-      const uint4 a = dzr[c], b = y[(long long)p * vec + c];
-      const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-      uint32_t o[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float a0 = bf16_lo(aw[q]), a1 = bf16_hi(aw[q]);
-        dot = fmaf(a0, bf16_lo(bw[q]), dot);
-        dot = fmaf(a1, bf16_hi(bw[q]), dot);
-        o[q] = pack_bf16x2(wj * a0, wj * a1);
-      }
-      dy[(long long)p * vec + c] = make_uint4(o[0], o[1], o[2], o[3]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    if (lane == 0) dw[t * k + j] = dot;
   }
+  s_dot[wi][lane] = 0.f;
+  __syncwarp();
+  const uint4* dzr = dz + t * vec;
+  for (int base = 0; base < vec; base += 256) {   // every lane runs every iteration (shuffles below)
+    const int c0 = base + lane;
+    uint4 a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + 32 * i < vec) a[i] = dzr[c0 + 32 * i];
+    for (int j = 0; j < k; ++j) {
+      const int p = __shfl_sync(0xffffffffu, my_p, j);
+      const float wj = __shfl_sync(0xffffffffu, my_w, j);
+      if (p < 0) continue;   // warp-uniform
+      const uint4* yr = y + (long long)p * vec;
+      uint4* dyr = dy + (long long)p * vec;
+      uint4 b[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (c0 + 32 * i < vec) b[i] = yr[c0 + 32 * i];
+      float dot = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (c0 + 32 * i < vec) {
+          const uint32_t aw[4] = {a[i].x, a[i].y, a[i].z, a[i].w}, bw[4] = {b[i].x, b[i].y, b[i].z, b[i].w};
+          uint32_t o[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float a0 = bf16_lo(aw[q]), a1 = bf16_hi(aw[q]);
+            dot = fmaf(a0, bf16_lo(bw[q]), dot);
+            dot = fmaf(a1, bf16_hi(bw[q]), dot);
+            o[q] = pack_bf16x2(wj * a0, wj * a1);
+          }
+          dyr[c0 + 32 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      if (lane == 0) s_dot[wi][j] += dot;
+    }
+  }
+  __syncwarp();
+  if (lane < k) dw[t * k + lane] = my_p < 0 ? 0.f : s_dot[wi][lane];
 }
 
 cudaError_t launch_combine_backward(const void* dz, const void* y, const int32_t* scatter_idx, const float* w, int T,

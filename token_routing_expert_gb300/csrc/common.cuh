@@ -409,4 +409,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 
+// SwiGLU backward of one element, in fp32 (page "Как устроен Olmo-core 3", §"SwiGLU с
+// квантизацией"): s = sigmoid(g), H = g s u, dU = dH g s, dG = dH u s (1 + g (1 - s)).
+// The sigmoid takes the fast exponential and division, as the forward's SwiGLU epilogue does
+// (a few ulp of fp32, far below the bf16 the results are stored in); when e^-g overflows the
+// division returns 0, the sigmoid's limit.
+__device__ __forceinline__ void swiglu_bwd_elem(float u, float g, float d, float& du, float& dg, float& hv) {
+  const float s = __fdividef(1.0f, 1.0f + __expf(-g));
+  const float si = g * s;
+  hv = si * u;
+  du = d * si;
+  dg = d * u * (s * (1.0f + g * (1.0f - s)));
+}
+
 }  // namespace moe

@@ -59,8 +59,12 @@ struct GemmParams {
   int b_mn;                // 1: B is MN-major, group g's K rows [g * b_rows_per_group, ...) x N columns
   int a_mn;                // 1 (K-grouped, 1 CTA): A is MN-major, K rows x M columns
   const int* a_off;        // non-null: group g's A rows start at A row a_off[g] (see a_row_shift)
-  void* preact;            // SwiGLU: also store [u | g] (bf16) here, preact_ld elements per row
+  void* preact;            // SwiGLU: also store [u | g] (bf16) here, preact_ld elements per row;
+                           // SwiGLU backward: read [u | g] from here
   long long preact_ld;
+  int preact_dense;        // SwiGLU backward: [u | g] rows at A's rows (shifted by a_off), else the output's
+  void* out2;              // SwiGLU backward: H
+  long long ldo2;
   int* status;
 };
 
@@ -176,16 +180,90 @@ __device__ __forceinline__ void store_block_bf16(uint4* stg, const uint32_t (&pa
   store_block_64b(stg, packed, reinterpret_cast<char*>(out0), ldo * 2, valid, lane);
 }
 
+// SwiGLU backward epilogue: the [u | g] pre-activations of a warp's 32 rows, 32 columns (64 bytes
+// of u and 64 of g per row) at a time.  swb_issue starts the loads, 8 rows x 64 contiguous bytes
+// per instruction, into pv[0..3] (u) and pv[4..7] (g), zeros for rows whose bit in `live` is
+// clear; swb_take later hands thread i row i as 16 words, through the warp's swizzled 2 KB buffer
+// (the converse of store_block_64b).  A chunk's loads are issued while the previous chunk is
+// computed, the first one before the accumulator is ready.
+struct SwbRows {
+  const char* pre;   // [u | g] of the warp's first row
+  uint32_t live;     // bit r: row r of the warp's 32 is a real row (else padding: zeros)
+  int valid;         // rows of the 32 inside the tile
+  long long wrow0;   // output row of the warp's first row
+};
+
+__device__ __forceinline__ SwbRows swb_rows(const GemmParams& p, int row0, int rows, int row_in_tile, int ash,
+                                            int live_end) {
+  const int lane = row_in_tile & 31;
+  SwbRows r;
+  r.valid = min(max(rows - (row_in_tile - lane), 0), 32);
+  r.wrow0 = (long long)row0 + (row_in_tile - lane);
+  r.live = __ballot_sync(0xffffffffu, lane < r.valid && r.wrow0 + lane + ash < (long long)live_end);
+  r.pre = reinterpret_cast<const char*>(p.preact) + (p.preact_dense ? r.wrow0 + ash : r.wrow0) * p.preact_ld * 2;
+  return r;
+}
+
+__device__ __forceinline__ void swb_issue(uint4 (&pv)[8], const SwbRows& r, const GemmParams& p, int col0, int lane) {
+  const int q = lane & 3;
+  const long long ld = p.preact_ld * 2;
+  const char* a0 = r.pre + (long long)col0 * 2;
+  const char* b0 = r.pre + (long long)(p.N + col0) * 2;
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    const int row = s * 8 + (lane >> 2);
+    const bool live = (r.live >> row) & 1u;
+    pv[s] = live ? __ldcs(reinterpret_cast<const uint4*>(a0 + row * ld + q * 16)) : make_uint4(0u, 0u, 0u, 0u);
+    pv[4 + s] = live ? __ldcs(reinterpret_cast<const uint4*>(b0 + row * ld + q * 16)) : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+__device__ __forceinline__ void swb_take(uint4* stg, const uint4 (&pv)[8], uint32_t (&a)[16], uint32_t (&b)[16],
+                                         int lane) {
+  const int q = lane & 3;
+#pragma unroll
+  for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int r = s * 8 + (lane >> 2);
+      stg[r * 4 + (q ^ ((r >> 1) & 3))] = pv[4 * pass + s];
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 v = stg[lane * 4 + (i ^ ((lane >> 1) & 3))];
+      uint32_t* d = pass ? b : a;
+      d[4 * i] = v.x;
+      d[4 * i + 1] = v.y;
+      d[4 * i + 2] = v.z;
+      d[4 * i + 3] = v.w;
+    }
+    __syncwarp();
+  }
+}
+
+// The first chunk's loads of a tile (called before the accumulator wait).
+template <int BN>
+__device__ __forceinline__ void swb_issue_first(uint4 (&pv)[8], const GemmParams& p, int row0, int rows,
+                                                int row_in_tile, int nt, int half, int ash, int live_end) {
+  const SwbRows r = swb_rows(p, row0, rows, row_in_tile, ash, live_end);
+  const int col0 = nt * BN + half * 32;
+  if (r.valid > 0 && col0 < p.N) swb_issue(pv, r, p, col0, row_in_tile & 31);
+}
+
 // Epilogue of one tile for the 32 rows a warp owns: TMEM -> registers -> global.
 // row_in_tile: this thread's row of the 128-row accumulator; rows: valid rows from row0.
 // e4m3 operands: the accumulator is scaled by the A row's scale and each column's B-row
 // scale; cs / cs_gate point at the B-row scales of this tile's first column.
 // With 8 epilogue warps two share a lane quadrant and `half` (0 or 1) picks every other
 // 32-column chunk.
+// SwiGLU backward: ash = the tile group's A row shift, live_end = the group's end among A's rows;
+// rows whose A row is past it are padding and get zeros.
 template <int BN, int EPI, bool F8 = false>
 __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, int row_in_tile, int nt, int split,
                                            const GemmParams& p, int half, uint4* stg, bool zero = false,
-                                           const float* cs = nullptr, const float* cs_gate = nullptr) {
+                                           const float* cs = nullptr, const float* cs_gate = nullptr, int ash = 0,
+                                           int live_end = 0, uint4* pv_in = nullptr) {
   const bool row_ok = row_in_tile < rows;
   const long long row = (long long)row0 + row_in_tile;
   float rs = 1.0f;
@@ -200,7 +278,42 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
   const int lane = row_in_tile & 31;
   const int valid = min(max(rows - (row_in_tile - lane), 0), 32);   // rows of this warp's 32 that exist
   const long long wrow0 = (long long)row0 + (row_in_tile - lane);
-  if (EPI == EPI_SWIGLU) {
+  if (EPI == EPI_SWIGLU_BWD) {
+    // dH chunk (rounded to bf16) with the [u | g] of the same rows and columns; pv_in holds the
+    // loads of the warp's first chunk, issued before the accumulator wait
+    uint4(&pv)[8] = *reinterpret_cast<uint4(*)[8]>(pv_in);
+    const SwbRows sr = swb_rows(p, row0, rows, row_in_tile, ash, live_end);
+    const bool me = (sr.live >> lane) & 1u;
+    __nv_bfloat16* dug = reinterpret_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo;
+    __nv_bfloat16* hout = reinterpret_cast<__nv_bfloat16*>(p.out2) + wrow0 * p.ldo2;
+#pragma unroll 1
+    for (int cc = half; cc < BN / 32; cc += kEpiWarps / 4) {
+      uint32_t v[32];
+      __syncwarp();
+      tmem_ld_32x32b_x32(tbase + cc * 32, v);
+      tmem_ld_wait();
+      const int col0 = nt * BN + cc * 32;
+      if (valid == 0 || col0 >= p.N) continue;   // warp-uniform
+      uint32_t uw[16], gw[16];
+      swb_take(stg, pv, uw, gw, lane);
+      const int ncol = col0 + 32 * (kEpiWarps / 4);
+      if (cc + kEpiWarps / 4 < BN / 32 && ncol < p.N) swb_issue(pv, sr, p, ncol, lane);
+      uint32_t pu[16], pg[16], ph[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t dpk = me ? pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])) : 0u;
+        float du0, dg0, h0, du1, dg1, h1;
+        swiglu_bwd_elem(bf16_lo(uw[i]), bf16_lo(gw[i]), bf16_lo(dpk), du0, dg0, h0);
+        swiglu_bwd_elem(bf16_hi(uw[i]), bf16_hi(gw[i]), bf16_hi(dpk), du1, dg1, h1);
+        pu[i] = pack_bf16x2(du0, du1);
+        pg[i] = pack_bf16x2(dg0, dg1);
+        ph[i] = pack_bf16x2(h0, h1);
+      }
+      store_block_bf16(stg, pu, dug + col0, p.ldo, valid, lane);
+      store_block_bf16(stg, pg, dug + p.N + col0, p.ldo, valid, lane);
+      store_block_bf16(stg, ph, hout + col0, p.ldo2, valid, lane);
+    }
+  } else if (EPI == EPI_SWIGLU) {
     constexpr int HALF = BN / 2;
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
 #pragma unroll 1
@@ -540,6 +653,13 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
       const TileCoord c = decode_tile(t, p, s_toff, s_goff);
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
+      int ash = 0, live_end = 0;
+      uint4 pv[8];
+      if (EPI == EPI_SWIGLU_BWD) {
+        ash = a_row_shift(p, c, s_goff, s_aoff);
+        live_end = s_aoff[c.group + 1];
+        swb_issue_first<BN>(pv, p, c.row0, c.rows, row_in_tile, c.nt, half, ash, live_end);
+      }
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull_bar[acc], use & 1u, abort_flag, p.status) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -554,7 +674,7 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
         cs_gate = cs + p.b_gate_offset;
       }
       store_tile<BN, EPI, F8>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p, half, stg, c.kt1 <= c.kt0, cs,
-                              cs_gate);
+                              cs_gate, ash, live_end, pv);
       tc_fence_before();
       mbar_arrive(&tempty_bar[acc]);
     }
@@ -764,6 +884,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
       const TileCoord c = decode_tile<BM2>(t, p, s_toff, s_goff);
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
+      int ash = 0, live_end = 0;
+      uint4 pv[8];
+      if (EPI == EPI_SWIGLU_BWD) {
+        ash = a_row_shift(p, c, s_goff, s_aoff);
+        live_end = s_aoff[c.group + 1];
+        swb_issue_first<C::BN>(pv, p, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt, half,
+                               ash, live_end);
+      }
       int ok = 1;
       if (lane == 0) ok = mbar_wait_cluster(&tfull_bar[acc], use & 1u, abort_flag, p.status) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -779,7 +907,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
       }
       // K-grouped: the group's output slice, zeros for a group without rows
       store_tile<C::BN, EPI, F8>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt, c.split,
-                                 p, half, stg, c.kt1 <= c.kt0, cs, cs_gate);
+                                 p, half, stg, c.kt1 <= c.kt0, cs, cs_gate, ash, live_end, pv);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&tempty_bar[acc]), 0));
@@ -945,8 +1073,15 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
                   q.a_rows < 0))
     return cudaErrorInvalidValue;
   if (q.a_rows && (q.a_mn_major || !q.a_off)) return cudaErrorInvalidValue;
-  // pre-activations kept by the SwiGLU epilogue: whole 32-column chunks of u and of g
-  if (q.preact && (q.epilogue != EPI_SWIGLU || q.N % 32 || q.preact_ld < 2 * (int64_t)q.N || q.preact_ld % 8))
+  // pre-activations kept by the SwiGLU epilogue (or read by the SwiGLU backward's): whole 32-column
+  // chunks of u and of g
+  if (q.preact && ((q.epilogue != EPI_SWIGLU && q.epilogue != EPI_SWIGLU_BWD) || q.N % 32 ||
+                   q.preact_ld < 2 * (int64_t)q.N || q.preact_ld % 8))
+    return cudaErrorInvalidValue;
+  // SwiGLU backward: M-grouped bf16 with A row offsets, [u | g] in, dUG (ldo >= 2N) and H out
+  if (q.epilogue == EPI_SWIGLU_BWD &&
+      (q.num_groups == 0 || !q.a_off || !q.preact || !q.out2 || f8 || ga || q.bn != 256 || q.splits > 1 ||
+       q.ldo < 2 * (int64_t)q.N || q.ldo % 8 || q.ldo2 < q.N || q.ldo2 % 8))
     return cudaErrorInvalidValue;
   const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
   CUtensorMap ta, tb;
@@ -992,6 +1127,9 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.a_off = q.a_off;
   gp.preact = q.preact;
   gp.preact_ld = q.preact_ld;
+  gp.preact_dense = q.preact_dense;
+  gp.out2 = q.out2;
+  gp.ldo2 = q.ldo2;
   gp.status = q.status;
 
   if (ga) {
@@ -1010,6 +1148,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
     }
     if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU>(ta, tb, gp, tiles, stream);
     if (q.epilogue == EPI_F32) return launch_pair_impl<EPI_F32>(ta, tb, gp, tiles, stream);   // dense fp32 out
+    if (q.epilogue == EPI_SWIGLU_BWD) return launch_pair_impl<EPI_SWIGLU_BWD>(ta, tb, gp, tiles, stream);
     return launch_pair_impl<EPI_BF16>(ta, tb, gp, tiles, stream);
   }
   int grid = num_sms();
@@ -1029,6 +1168,8 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
     case EPI_BF16:
       if (q.bn == 256) return launch_impl<256, EPI_BF16>(q, ta, tb, gp, grid, stream);
       break;
+    case EPI_SWIGLU_BWD:
+      return launch_impl<256, EPI_SWIGLU_BWD>(q, ta, tb, gp, grid, stream);
     case EPI_F32:
       switch (q.bn) {
         case 256: return launch_impl<256, EPI_F32>(q, ta, tb, gp, grid, stream);

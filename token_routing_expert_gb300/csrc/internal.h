@@ -7,7 +7,9 @@
 
 namespace moe {
 
-enum GemmEpilogue { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2 };
+// EPI_SWIGLU_BWD: the product is dH of the SwiGLU experts (rounded to bf16); the epilogue reads the
+// pre-activations [u | g] of the same rows and writes dUG = [dU | dG] to out and H to out2 (bf16).
+enum GemmEpilogue { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2, EPI_SWIGLU_BWD = 3 };
 
 // C[M, N] = A[M, K] * B[N, K]^T per group, A and B bf16 K-major, fp32 accumulate.
 // Groups (optional) are contiguous row ranges of A / C given by device
@@ -50,8 +52,13 @@ struct GemmProblem {
                           //   64 k_off[g]); rows a tile reads past the group are A's next rows or, past
                           //   A's end, zeros, so the other operand must be zero there
   int64_t a_rows;         // with a_off, M-grouped: rows present in A (0: M)
-  void* preact;           // SwiGLU: non-NULL also stores [u | g] bf16, preact_ld elements per output row
+  void* preact;           // SwiGLU: non-NULL also stores [u | g] bf16, preact_ld elements per output row;
+                          // SwiGLU backward: the [u | g] rows read (preact_dense: at A's rows, i.e. the
+                          // output row shifted by a_off as for A; else at the output's own rows)
   int64_t preact_ld;
+  int preact_dense;
+  void* out2;             // SwiGLU backward: H (bf16, ldo2 elements per row)
+  int64_t ldo2;
   int* status;
 };
 
@@ -106,8 +113,6 @@ cudaError_t launch_pad_rows(const void* src, const int32_t* gather, const int32_
                             int src_rows, int cols, long long max_rows, void* dst, int* status, cudaStream_t st);
 cudaError_t launch_pad_scatter(const int32_t* scatter, int R, const int32_t* off, const int32_t* poff, int E,
                                int32_t* out, cudaStream_t st);
-cudaError_t launch_swiglu_backward(const void* UG, int from_dense, const int32_t* off, const int32_t* k_off, int E,
-                                   const void* dH, long long prows, int h, void* dUG, void* H, cudaStream_t st);
 cudaError_t launch_combine_backward(const void* dz, const void* y, const int32_t* scatter_idx, const float* w, int T,
                                     int k, int L, int rows, void* dy, float* dw, int* status, cudaStream_t st);
 cudaError_t launch_zero_padding_rows(const int32_t* gather_idx, int rows, int cols, void* dst, cudaStream_t st);

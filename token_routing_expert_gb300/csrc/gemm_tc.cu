@@ -712,30 +712,121 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
 // ---------------------------------------------------------------------------
 constexpr int BM2 = 256;
 
-struct PairCfg {
+// SwiGLU backward: 4 stages, and a ring of [u | g] boxes for the epilogue (2 slots for each
+// half of the epilogue warps, 16 KB each: 128 rows x 32 columns of u and of g), with a full and
+// an empty barrier per slot.
+template <int EPI>
+struct PairCfgT {
+  static constexpr bool SWB = EPI == EPI_SWIGLU_BWD;
   static constexpr int BN = 256;
   static constexpr int A_BYTES = 128 * BK * 2;
   static constexpr int B_BYTES = (BN / 2) * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = 6;
+  static constexpr int STAGES = SWB ? 4 : 6;
   static constexpr int ACC_STRIDE = 256;
   static constexpr int TMEM_COLS = 512;
+  static constexpr int PRE_SLOTS = 2;                       // per half of the epilogue warps
+  static constexpr int PRE_SLOT_BYTES = 2 * 128 * 64;       // u box + g box
   static constexpr int BAR_OFF = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 3 * STAGES + 4;
+  static constexpr int NUM_BARS = 3 * STAGES + 4 + (SWB ? 2 * 2 * PRE_SLOTS : 0);
   static constexpr int HOLDER_OFF = BAR_OFF + NUM_BARS * 8;
   static constexpr int ABORT_OFF = HOLDER_OFF + 4;
   static constexpr int TABLE_OFF = (ABORT_OFF + 4 + 15) & ~15;
   static constexpr int EPI_OFF = (TABLE_OFF + 3 * (kMaxGroups + 1) * 4 + 127) & ~127;
-  static constexpr int SMEM_BYTES = EPI_OFF + kEpiStageBytes + 1024;
+  static constexpr int PRE_OFF = (EPI_OFF + kEpiStageBytes + 1023) & ~1023;
+  static constexpr int SMEM_BYTES = PRE_OFF + (SWB ? 2 * PRE_SLOTS * PRE_SLOT_BYTES : 0) + 1024;
+  static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
+
+// SwiGLU backward on CTA pairs: the [u | g] pre-activations reach the epilogue through TMA boxes
+// (128 rows x 32 columns of u and of g, 64-byte swizzle) in a 2-slot ring per half of the
+// epilogue warps.  The half's first warp issues chunk j + 2 once all four warps have taken
+// chunk j; the first two chunks of a tile are issued before its accumulator wait.  Chunk j of a
+// half covers columns (half + 2 j) * 32 of the tile; rows come from preact at the CTA's output
+// rows, shifted like A's when preact_dense.
+template <class C>
+__device__ __forceinline__ void swb_pre_issue(const GemmParams& p, const CUtensorMap* tmP, uint8_t* smem,
+                                              uint64_t* pre_full, uint64_t* pre_empty, int half, uint32_t& issued,
+                                              const TileCoord& c, int rank, int ash, int j, volatile int* abort_flag) {
+  const int col0 = c.nt * C::BN + (half + 2 * j) * 32;
+  if (col0 >= p.N) return;
+  const uint32_t n = issued++;
+  const int slot = half * C::PRE_SLOTS + (int)(n % C::PRE_SLOTS);
+  const uint32_t ph = (n / C::PRE_SLOTS) & 1u;
+  if (!mbar_wait(&pre_empty[slot], ph ^ 1u, abort_flag, p.status)) return;
+  uint8_t* dst = smem + C::PRE_OFF + slot * C::PRE_SLOT_BYTES;
+  const int drow = c.row0 + 128 * rank + (p.preact_dense ? ash : 0);
+  mbar_arrive_expect_tx(&pre_full[slot], C::PRE_SLOT_BYTES);
+  tma_load_2d(dst, tmP, &pre_full[slot], col0, drow);
+  tma_load_2d(dst + C::PRE_SLOT_BYTES / 2, tmP, &pre_full[slot], p.N + col0, drow);
+}
+
+template <class C>
+__device__ __forceinline__ void swb_pair_tile(uint32_t tbase, const TileCoord& c, int rank, int row_in_tile,
+                                              const GemmParams& p, int half, uint4* stg, uint8_t* smem,
+                                              const CUtensorMap* tmP, uint64_t* pre_full, uint64_t* pre_empty,
+                                              bool pre_issuer, uint32_t& issued, uint32_t& used, int ash,
+                                              int live_end, volatile int* abort_flag) {
+  const int lane = row_in_tile & 31;
+  const int crows = c.rows - 128 * rank;
+  const long long wrow0 = (long long)c.row0 + 128 * rank + (row_in_tile - lane);
+  const int valid = min(max(crows - (row_in_tile - lane), 0), 32);
+  const bool me = lane < valid && wrow0 + lane + ash < (long long)live_end;
+  __nv_bfloat16* dug = reinterpret_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo;
+  __nv_bfloat16* hout = reinterpret_cast<__nv_bfloat16*>(p.out2) + wrow0 * p.ldo2;
+  const int sw = (row_in_tile >> 1) & 3;   // the 64-byte swizzle of this row's 16-byte chunks
+#pragma unroll 1
+  for (int j = 0; j < C::BN / 64; ++j) {
+    const int cc = half + 2 * j;
+    uint32_t v[32];
+    __syncwarp();
+    tmem_ld_32x32b_x32(tbase + cc * 32, v);
+    tmem_ld_wait();
+    const int col0 = c.nt * C::BN + cc * 32;
+    if (crows <= 0 || col0 >= p.N) continue;   // the same for the whole half: no chunk was issued
+    const uint32_t n = used++;
+    const int slot = half * C::PRE_SLOTS + (int)(n % C::PRE_SLOTS);
+    mbar_wait(&pre_full[slot], (n / C::PRE_SLOTS) & 1u, abort_flag, p.status);
+    const uint8_t* su = smem + C::PRE_OFF + slot * C::PRE_SLOT_BYTES + row_in_tile * 64;
+    uint32_t uw[16], gw[16];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 a = *reinterpret_cast<const uint4*>(su + ((q ^ sw) << 4));
+      const uint4 b = *reinterpret_cast<const uint4*>(su + C::PRE_SLOT_BYTES / 2 + ((q ^ sw) << 4));
+      uw[4 * q] = a.x; uw[4 * q + 1] = a.y; uw[4 * q + 2] = a.z; uw[4 * q + 3] = a.w;
+      gw[4 * q] = b.x; gw[4 * q + 1] = b.y; gw[4 * q + 2] = b.z; gw[4 * q + 3] = b.w;
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&pre_empty[slot]);
+    if (pre_issuer && j + C::PRE_SLOTS < C::BN / 64)
+      swb_pre_issue<C>(p, tmP, smem, pre_full, pre_empty, half, issued, c, rank, ash, j + C::PRE_SLOTS, abort_flag);
+    if (valid == 0) continue;
+    uint32_t pu[16], pg[16], ph[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      // a padding row (its A row belongs to the next expert, or is past A) gets zeros
+      const uint32_t dpk = me ? pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])) : 0u;
+      const uint32_t u2 = me ? uw[i] : 0u, g2 = me ? gw[i] : 0u;
+      float du0, dg0, h0, du1, dg1, h1;
+      swiglu_bwd_elem(bf16_lo(u2), bf16_lo(g2), bf16_lo(dpk), du0, dg0, h0);
+      swiglu_bwd_elem(bf16_hi(u2), bf16_hi(g2), bf16_hi(dpk), du1, dg1, h1);
+      pu[i] = pack_bf16x2(du0, du1);
+      pg[i] = pack_bf16x2(dg0, dg1);
+      ph[i] = pack_bf16x2(h0, h1);
+    }
+    store_block_bf16(stg, pu, dug + col0, p.ldo, valid, lane);
+    store_block_bf16(stg, pg, dug + p.N + col0, p.ldo, valid, lane);
+    store_block_bf16(stg, ph, hout + col0, p.ldo2, valid, lane);
+  }
+}
 
 template <int EPI, bool F8 = false, bool GA = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const GemmParams p) {
+                        const __grid_constant__ CUtensorMap tmP, const GemmParams p) {
   pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
   pdl_trigger();
-  using C = PairCfg;
+  using C = PairCfgT<EPI>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -743,6 +834,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
   uint64_t* tfull_bar = empty_bar + C::STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* gath_bar = tempty_bar + 2;   // gathered A only
+  uint64_t* pre_full = tempty_bar + 2;   // SwiGLU backward only: [half][slot]
+  uint64_t* pre_empty = pre_full + 2 * C::PRE_SLOTS;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::HOLDER_OFF);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
   int* s_toff = reinterpret_cast<int*>(smem + C::TABLE_OFF);
@@ -777,12 +870,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
       mbar_init(&tfull_bar[a], 1);    // one multicast commit per tile
       mbar_init(&tempty_bar[a], 2 * kEpiWarps);   // CTA 0 only: one lane of each epilogue warp of both CTAs
     }
+    if constexpr (C::SWB) {
+      for (int i = 0; i < 2 * C::PRE_SLOTS; ++i) {
+        mbar_init(&pre_full[i], 1);                 // the half's issuing thread (+ the boxes' bytes)
+        mbar_init(&pre_empty[i], kEpiWarps / 2);    // one lane of each warp of the half
+      }
+    }
     fence_mbar_init();
   }
   if (warp == 1) tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
     if (!GA) tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if constexpr (C::SWB) tma_prefetch_desc(&tmP);
   }
   tc_fence_before();
   __syncthreads();
@@ -879,18 +979,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
     const int half = (warp - 2) >> 2;
     const int row_in_tile = quad * 32 + lane;
     uint4* stg = reinterpret_cast<uint4*>(smem + C::EPI_OFF) + (warp - 2) * 128;
+    // SwiGLU backward: the first warp of each half issues its half's [u | g] boxes; every warp of
+    // the half counts the chunks it has consumed, the issuer also those it has issued
+    const bool pre_issuer = C::SWB && ((warp - 2) & 3) == 0 && lane == 0;
+    uint32_t pre_issued = 0, pre_used = 0;
     int it = 0;
     for (int t = pair; t < total_tiles; t += npairs, ++it) {
       const TileCoord c = decode_tile<BM2>(t, p, s_toff, s_goff);
       const int acc = it & 1;
       const uint32_t use = (uint32_t)(it >> 1);
       int ash = 0, live_end = 0;
-      uint4 pv[8];
-      if (EPI == EPI_SWIGLU_BWD) {
+      if constexpr (C::SWB) {
         ash = a_row_shift(p, c, s_goff, s_aoff);
         live_end = s_aoff[c.group + 1];
-        swb_issue_first<C::BN>(pv, p, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt, half,
-                               ash, live_end);
+        // the tile's first two [u | g] chunks of this half, before the accumulator wait
+        if (pre_issuer && c.rows > 128 * (int)rank)
+          for (int j = 0; j < C::PRE_SLOTS; ++j)
+            swb_pre_issue<C>(p, &tmP, smem, pre_full, pre_empty, half, pre_issued, c, (int)rank, ash, j, abort_flag);
       }
       int ok = 1;
       if (lane == 0) ok = mbar_wait_cluster(&tfull_bar[acc], use & 1u, abort_flag, p.status) ? 1 : 0;
@@ -905,9 +1010,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
         cs = p.b_scale + brow;
         cs_gate = cs + p.b_gate_offset;
       }
-      // K-grouped: the group's output slice, zeros for a group without rows
-      store_tile<C::BN, EPI, F8>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt, c.split,
-                                 p, half, stg, c.kt1 <= c.kt0, cs, cs_gate, ash, live_end, pv);
+      if constexpr (C::SWB) {
+        swb_pair_tile<C>(tbase, c, (int)rank, row_in_tile, p, half, stg, smem, &tmP, pre_full, pre_empty, pre_issuer,
+                         pre_issued, pre_used, ash, live_end, abort_flag);
+      } else {
+        // K-grouped: the group's output slice, zeros for a group without rows
+        store_tile<C::BN, EPI, F8>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt,
+                                   c.split, p, half, stg, c.kt1 <= c.kt0, cs, cs_gate);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&tempty_bar[acc]), 0));
@@ -970,6 +1080,21 @@ static bool make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t co
   return r == CUDA_SUCCESS;
 }
 
+// bf16 tensor (rows x cols) read as box_cols x box_rows boxes with the given swizzle.
+static bool make_tmap_box(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols, int box_rows,
+                          CUtensorMapSwizzle swizzle) {
+  PFN_tmapEncodeTiled enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+  cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int num_sms() {
   int dev = 0, n = 0;
   cudaGetDevice(&dev);
@@ -1016,7 +1141,8 @@ static cudaError_t launch_impl(const GemmProblem& q, const CUtensorMap& ta, cons
 
 template <int EPI, bool F8 = false, bool GA = false>
 static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp, int tiles,
-                                    cudaStream_t stream) {
+                                    cudaStream_t stream, const CUtensorMap* tp = nullptr) {
+  using PairCfg = PairCfgT<EPI>;
   auto kern = gemm_tc_pair_kernel<EPI, F8, GA>;
   constexpr int threads = GA ? kThreadsGA : kThreads;
   static bool attr_set = false;
@@ -1043,7 +1169,7 @@ static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb
   }
   int pairs = max_pairs;
   if (tiles > 0) pairs = std::min(pairs, tiles);
-  launch_pdl(kern, 2 * pairs, threads, PairCfg::SMEM_BYTES, stream, ta, tb, gp);
+  launch_pdl(kern, 2 * pairs, threads, PairCfg::SMEM_BYTES, stream, ta, tb, tp ? *tp : ta, gp);
   return cudaGetLastError();
 }
 
@@ -1148,7 +1274,14 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
     }
     if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU>(ta, tb, gp, tiles, stream);
     if (q.epilogue == EPI_F32) return launch_pair_impl<EPI_F32>(ta, tb, gp, tiles, stream);   // dense fp32 out
-    if (q.epilogue == EPI_SWIGLU_BWD) return launch_pair_impl<EPI_SWIGLU_BWD>(ta, tb, gp, tiles, stream);
+    if (q.epilogue == EPI_SWIGLU_BWD) {
+      // the [u | g] rows as 128 x 32 boxes, 64-byte swizzle (the epilogue reads a row per lane)
+      CUtensorMap tp;
+      const int64_t prow = q.preact_dense ? q.a_rows : q.M;
+      if (!make_tmap_box(&tp, q.preact, prow, q.preact_ld, 32, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+      return launch_pair_impl<EPI_SWIGLU_BWD>(ta, tb, gp, tiles, stream, &tp);
+    }
     return launch_pair_impl<EPI_BF16>(ta, tb, gp, tiles, stream);
   }
   int grid = num_sms();

@@ -259,6 +259,8 @@ def run_native(args):
 
     native.load()
     spec = W.WORKLOADS[args.config]
+    if args.tokens > 0:
+        spec = spec.with_(T=args.tokens)
     if args.capacity_factor > 0:
         spec = spec.with_(capacity_factor=args.capacity_factor)
     if args.fp8:
@@ -548,6 +550,8 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--config", default="olmoe", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="tokens per step instead of the workload's own T (for small profiling captures)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--capacity-factor", type=float, default=0.0,
                     help="> 0: capacity-limited experts (dropping); default dropless")

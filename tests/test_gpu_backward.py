@@ -23,6 +23,9 @@ CASES = {
                                gating="topk_softmax", seed=53),
     "capacity": WorkloadSpec("capacity", T=400, d_model=256, num_experts=8, top_k=2, hidden_size=128,
                              gating="sigmoid", capacity_factor=0.75, seed=54),
+    # the routed dimension is the latent one: the experts backward runs in it
+    "latent_pair_tiles": WorkloadSpec("latent_pair_tiles", T=1600, d_model=384, num_experts=4, top_k=2,
+                                      hidden_size=192, latent_dim=256, gating="sigmoid", skew=True, seed=55),
 }
 
 
@@ -63,6 +66,9 @@ def test_combine_and_experts_backward(name, preact):
     x = inp["x"].cuda()
     _, idx, w = native.moe_router(cfg, wts, x, ws)
     counts, offsets, gather, scatter = native.moe_permute(cfg, idx, ws)
+    x_in = x
+    if spec.latent_dim:   # the experts' input is the latent projection of x
+        x = native.moe_latent_down(cfg, wts, x_in, ws).clone()
     y = native.moe_grouped_swiglu(cfg, wts, x, gather, offsets, ws)
     pre = None
     if preact:
@@ -92,7 +98,7 @@ def test_combine_and_experts_backward(name, preact):
 
     # experts' backward on the GPU's dy, in the dense (or slot) layout of the permutation
     dy_np = dy.double().cpu().numpy()
-    x_np = f64(inp["x"])
+    x_np = x.double().cpu().numpy()
     if preact:
         check_preact(pre, x_np, gather_np, offsets.cpu().numpy(), ow, E, h)
     dx_want = np.zeros((T, Lr))

@@ -616,6 +616,49 @@ def router_backward(cfg: OracleConfig, x: np.ndarray, w_router: np.ndarray, b_ro
     return dlogits, dlogits @ w_router, dlogits.T @ x, dlogits.sum(axis=0)
 
 
+
+# --------------------------------------------------------------------------
+# Backward of the latent projections  [Olmo-core 3, §"Латентная проекция
+# экспертов": prepare_routed_input (down-projection) and restore_routed_output
+# (RMSNorm, then the up-projection)]
+# The derivative of the forward as defined above; nothing on the page differs.
+# --------------------------------------------------------------------------
+
+def rms_norm_backward(z: np.ndarray, dn: np.ndarray, eps: float, gamma: Optional[np.ndarray] = None):
+    """Gradients of n = z r gamma, r = 1 / sqrt(mean(z^2) + eps), along the last axis:
+    dz = r (gamma dn) - z r^3 mean(z gamma dn), dgamma = sum over rows of dn z r."""
+    z = np.asarray(z, np.float64)
+    dn = np.asarray(dn, np.float64)
+    g = np.ones(z.shape[-1]) if gamma is None else np.asarray(gamma, np.float64)
+    r = 1.0 / np.sqrt((z * z).mean(axis=-1, keepdims=True) + eps)
+    gdn = dn * g
+    dz = r * gdn - z * r ** 3 * (z * gdn).mean(axis=-1, keepdims=True)
+    dgamma = (dn * z * r).reshape(-1, z.shape[-1]).sum(axis=0)
+    return dz, dgamma
+
+
+def restore_routed_output_backward(cfg: OracleConfig, z: np.ndarray, w_up_latent: np.ndarray,
+                                   dout: np.ndarray, rms_weight: Optional[np.ndarray] = None):
+    """Gradients of out = W_up n (n = RMSNorm(z) gamma, or z without the norm):
+    (dz, dW_up, dgamma; dgamma is None without the norm)."""
+    z = np.asarray(z, np.float64)
+    dout = np.asarray(dout, np.float64)
+    w_up_latent = np.asarray(w_up_latent, np.float64)
+    n = rms_norm(z, cfg.rms_eps, rms_weight) if cfg.up_proj_norm else z
+    dn = dout @ w_up_latent
+    dw_up = dout.T @ n
+    if not cfg.up_proj_norm:
+        return dn, dw_up, None
+    dz, dgamma = rms_norm_backward(z, dn, cfg.rms_eps, rms_weight)
+    return dz, dw_up, dgamma
+
+
+def prepare_routed_input_backward(x: np.ndarray, w_down_latent: np.ndarray, dx_routed: np.ndarray):
+    """Gradients of x_routed = x W_down^T: (dx, dW_down)."""
+    x = np.asarray(x, np.float64)
+    dx_routed = np.asarray(dx_routed, np.float64)
+    return dx_routed @ np.asarray(w_down_latent, np.float64), dx_routed.T @ x
+
 # --------------------------------------------------------------------------
 # Rowwise FP8 experts  [Olmo-core 3, §"Rowwise FP8 и MXFP8": pre-quantised
 # expert weights, quantised activations, the experts run on FP8 operands]

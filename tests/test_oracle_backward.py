@@ -93,3 +93,51 @@ def test_router_backward_finite_differences(gating, extra):
     np.testing.assert_allclose(db, _fd(loss, b), rtol=1e-6, atol=1e-8)
     # the selection-only bias carries no gradient
     np.testing.assert_allclose(_fd(loss, sb), 0.0, atol=1e-9)
+
+
+def test_rms_norm_backward_finite_differences():
+    rng = np.random.default_rng(11)
+    z, gamma, probe = rng.standard_normal((3, 6)), rng.standard_normal(6), rng.standard_normal((3, 6))
+    eps = 1e-3
+    loss = lambda: float((ref.rms_norm(z, eps, gamma) * probe).sum())   # noqa: E731
+    dz, dgamma = ref.rms_norm_backward(z, probe, eps, gamma)
+    np.testing.assert_allclose(dz, _fd(loss, z), rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dgamma, _fd(loss, gamma), rtol=1e-6, atol=1e-8)
+
+
+def test_rms_norm_backward_scale_invariance():
+    """Without eps the norm ignores the row's scale, so its input gradient is orthogonal to the row."""
+    rng = np.random.default_rng(12)
+    z, dn = rng.standard_normal((5, 16)), rng.standard_normal((5, 16))
+    dz, _ = ref.rms_norm_backward(z, dn, 0.0)
+    np.testing.assert_allclose((dz * z).sum(axis=1), 0.0, atol=1e-12)
+    # gamma = 1 and a constant row c: r = 1/|c|, dz = (dn - mean(dn)) / |c|
+    c = -2.5
+    zc = np.full((1, 8), c)
+    dz_c, dg_c = ref.rms_norm_backward(zc, dn[:1, :8], 0.0)
+    np.testing.assert_allclose(dz_c, (dn[:1, :8] - dn[:1, :8].mean()) / abs(c), rtol=1e-13)
+    np.testing.assert_allclose(dg_c, dn[0, :8] * np.sign(c), rtol=1e-13)
+
+
+def test_latent_projection_backward_finite_differences():
+    rng = np.random.default_rng(13)
+    T, D, L = 3, 5, 4
+    for norm in (1, 0):
+        cfg = ref.OracleConfig(d_model=D, num_experts=2, top_k=1, hidden_size=2, gating=0, latent_dim=L,
+                               up_proj_norm=norm, rms_eps=1e-3)
+        z, w_up, gamma = rng.standard_normal((T, L)), rng.standard_normal((D, L)), rng.standard_normal(L)
+        probe = rng.standard_normal((T, D))
+        loss = lambda: float((ref.restore_routed_output(cfg, z, w_up, gamma) * probe).sum())   # noqa: E731
+        dz, dw_up, dgamma = ref.restore_routed_output_backward(cfg, z, w_up, probe, gamma)
+        np.testing.assert_allclose(dz, _fd(loss, z), rtol=1e-6, atol=1e-8)
+        np.testing.assert_allclose(dw_up, _fd(loss, w_up), rtol=1e-6, atol=1e-8)
+        if norm:
+            np.testing.assert_allclose(dgamma, _fd(loss, gamma), rtol=1e-6, atol=1e-8)
+        else:
+            assert dgamma is None
+    x, w_down, probe = rng.standard_normal((T, D)), rng.standard_normal((L, D)), rng.standard_normal((T, L))
+    cfg = ref.OracleConfig(d_model=D, num_experts=2, top_k=1, hidden_size=2, gating=0, latent_dim=L)
+    loss = lambda: float((ref.prepare_routed_input(cfg, x, w_down) * probe).sum())   # noqa: E731
+    dx, dw_down = ref.prepare_routed_input_backward(x, w_down, probe)
+    np.testing.assert_allclose(dx, _fd(loss, x), rtol=1e-6, atol=1e-8)
+    np.testing.assert_allclose(dw_down, _fd(loss, w_down), rtol=1e-6, atol=1e-8)

@@ -361,6 +361,35 @@ int moe_grouped_swiglu_backward_preact(const moe_config_t* cfg, const moe_weight
                                        moe_stream_t stream);
 
 /*
+ * Backward of the latent projections (training; latent configs only), section
+ * "Латентная проекция экспертов": the derivative of restore_routed_output
+ * (bias-free RMSNorm with gain gamma, then the up-projection) and of
+ * prepare_routed_input (the down-projection).  ws: moe_backward_workspace_size
+ * bytes.
+ *
+ * moe_latent_restore_backward: from z (the combine's output, device (T, L)
+ *   bf16) and dout (device (T, D) bf16): n = RMSNorm(z) gamma recomputed as the
+ *   forward does (bf16; n = z without up_proj_norm), dn = dout W_up (bf16),
+ *   dW_up = dout^T n (device (D, L) fp32 out), and with the norm
+ *   dz = r gamma dn - z r^3 mean(z gamma dn), r = 1 / sqrt(mean(z^2) + eps)
+ *   (device (T, L) bf16 out) and dgamma = sum over tokens of dn z r
+ *   (drms_weight, device (L) fp32 out, or NULL to skip); without the norm dz = dn.
+ * moe_latent_down_backward: from x (device (T, D) bf16) and dx_routed (device
+ *   (T, L) bf16, e.g. from moe_grouped_swiglu_backward): dx = dx_routed W_down
+ *   (device (T, D) bf16 out; the router's share of the input gradient is
+ *   separate, moe_router_backward) and dW_down = dx_routed^T x (device (L, D)
+ *   fp32 out).
+ * Weight gradients are fp32 and contract over the tokens in one pass (no
+ * atomics: the same inputs give the same bits).
+ */
+int moe_latent_restore_backward(const moe_config_t* cfg, const moe_weights_t* w, const void* z, int64_t T,
+                                const void* dout, void* dz, float* dw_up, float* drms_weight, void* ws,
+                                size_t ws_bytes, moe_stream_t stream);
+int moe_latent_down_backward(const moe_config_t* cfg, const moe_weights_t* w, const void* x, int64_t T,
+                             const void* dx_routed, void* dx, float* dw_down, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
+/*
  * Load-balancing counters, section "Счётчики и bias-корректировка" (run between
  * training steps or batches; E <= 1024, one small kernel each).
  *

@@ -184,3 +184,48 @@ def test_layer_forward_preact_matches_forward():
     ow = oracle_weights(spec, inp)
     check_preact(pre, f64(inp["x"]), inter["gather_idx"].cpu().numpy(), inter["offsets"].cpu().numpy(), ow,
                  spec.num_experts, spec.hidden_size, "layer preact")
+
+
+LATENT_CASES = {
+    # (spec, with an RMSNorm gain)
+    "norm_gain_small": (WorkloadSpec("norm_gain_small", T=300, d_model=384, num_experts=4, top_k=2, hidden_size=64,
+                                     latent_dim=192, gating="softmax", seed=81), True),
+    "norm_pair_tiles": (WorkloadSpec("norm_pair_tiles", T=1200, d_model=512, num_experts=4, top_k=2, hidden_size=64,
+                                     latent_dim=256, gating="softmax", seed=82), False),
+    "no_norm": (WorkloadSpec("no_norm", T=257, d_model=256, num_experts=4, top_k=2, hidden_size=64, latent_dim=128,
+                             up_proj_norm=False, gating="softmax", seed=83), False),
+}
+
+
+@pytest.mark.parametrize("name", list(LATENT_CASES))
+def test_latent_projection_backward(name):
+    """Backward of the latent restore (RMSNorm + up-projection) and of the down-projection against
+    the oracle's derivative of the forward definition, on random z, dout and dx_routed."""
+    spec, with_gain = LATENT_CASES[name]
+    inp = generate(spec)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp)
+    T, D, L = spec.T, spec.d_model, spec.latent_dim
+    g = np.random.default_rng(spec.seed + 7)
+    bf = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)   # noqa: E731
+    gain = bf(1.0 + 0.3 * g.standard_normal(L)) if with_gain else None
+    if gain is not None:
+        wts.rms_weight = gain.cuda()
+    z, dout, dxr = bf(g.standard_normal((T, L))), bf(g.standard_normal((T, D))), bf(g.standard_normal((T, L)))
+    bws = native.backward_workspace(cfg, T)
+    bws.fill_(0xFF)
+    dz, dw_up, dg = native.moe_latent_restore_backward(cfg, wts, z.cuda(), dout.cuda(), bws)
+    dx, dw_down = native.moe_latent_down_backward(cfg, wts, inp["x"].cuda(), dxr.cuda(), bws)
+    assert native.moe_get_status() == 0
+    oc = oracle_config(spec)
+    want_dz, want_dwu, want_dg = ref.restore_routed_output_backward(oc, f64(z), f64(inp["w_up_latent"]), f64(dout),
+                                                                    None if gain is None else f64(gain))
+    close(dz.double().cpu().numpy(), want_dz, "dz")
+    close(dw_up.double().cpu().numpy(), want_dwu, "dW_up")
+    if spec.up_proj_norm:
+        close(dg.double().cpu().numpy(), want_dg, "dgamma")
+    else:
+        assert dg is None
+    want_dx, want_dwd = ref.prepare_routed_input_backward(f64(inp["x"]), f64(inp["w_down"]), f64(dxr))
+    close(dx.double().cpu().numpy(), want_dx, "dx (latent down-projection)")
+    close(dw_down.double().cpu().numpy(), want_dwd, "dW_down")

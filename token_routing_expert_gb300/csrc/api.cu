@@ -477,6 +477,61 @@ void make_bwd_plan(const moe_config_t* c, int64_t T, BwdPlan* b) {
   b->total = o;
 }
 
+// Workspace of the latent projections' backward.
+struct LatentBwdPlan {
+  int64_t Tpad;
+  int dn_splits, dx_splits, slab;
+  size_t n, dn, r, gpart, part, total;
+};
+
+void make_latent_bwd_plan(const moe_config_t* c, int64_t T, int sms, LatentBwdPlan* b) {
+  const int64_t D = c->d_model, L = c->latent_dim > 0 ? c->latent_dim : c->d_model;
+  b->Tpad = (T + 63) / 64 * 64;
+  b->dn_splits = splits_for((int)(((T + 127) / 128) * ((L + 255) / 256)), (int)D, sms);
+  b->dx_splits = splits_for((int)(((T + 127) / 128) * ((D + 255) / 256)), (int)L, sms);
+  b->slab = 256;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  b->n = take((size_t)T * L * 2);
+  b->dn = take((size_t)T * L * 2);
+  b->r = take((size_t)T * 4);
+  b->gpart = take((size_t)((T + b->slab - 1) / b->slab) * L * 4);
+  const size_t dn_part = b->dn_splits > 1 ? (size_t)b->dn_splits * T * L * 4 : 0;
+  const size_t dx_part = b->dx_splits > 1 ? (size_t)b->dx_splits * T * D * 4 : 0;
+  b->part = take(std::max(dn_part, dx_part));
+  b->total = o;
+}
+
+// A weight gradient (M x N fp32) = A^T B contracted over the T token rows of A (T x M) and B (T x N),
+// both read as stored (MN-major operands); rows up to the padded T read as zeros.
+int token_contraction_f32(const void* A, int M, const void* B, int N, int64_t T, int64_t Tpad, float* out,
+                          int* status, cudaStream_t st) {
+  GemmProblem g{};
+  g.A = A;
+  g.a_mn_major = 1;
+  g.mn_rows = T;
+  g.a_cols = M;
+  g.B = B;
+  g.b_mn_major = 1;
+  g.b_rows_total = T;
+  g.M = M;
+  g.N = N;
+  g.K = (int)Tpad;
+  g.num_groups = 0;
+  g.epilogue = EPI_F32;
+  g.pair_tiles = M >= 256 && N % 256 == 0 ? 1 : 0;
+  g.bn = g.pair_tiles || N % 256 == 0 ? 256 : (N % 128 == 0 ? 128 : 64);
+  g.splits = 1;
+  g.out = out;
+  g.ldo = N;
+  g.status = status;
+  return cuda_status(launch_gemm(g, st));
+}
+
 // Workspace of the router backward.
 struct RouterBwdPlan {
   int64_t Epad, Tpad;
@@ -950,7 +1005,73 @@ int moe_backward_workspace_size(const moe_config_t* c, int64_t T, size_t* bytes)
   RouterBwdPlan r;
   make_router_bwd_plan(c, T, kSizingSms, &r);
   *bytes = std::max(b.total, r.total);
+  if (c->latent_dim > 0) {
+    LatentBwdPlan l;
+    make_latent_bwd_plan(c, T, kSizingSms, &l);
+    *bytes = std::max(*bytes, l.total);
+  }
   return MOE_OK;
+}
+
+int moe_latent_restore_backward(const moe_config_t* c, const moe_weights_t* w, const void* z, int64_t T,
+                                const void* dout, void* dz, float* dw_up, float* drms_weight, void* ws,
+                                size_t ws_bytes, moe_stream_t stream) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (c->latent_dim <= 0 || T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (T > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  if (!w || !w->w_up_latent || !z || !dout || !dz || !dw_up) return MOE_ERR_INVALID_ARG;
+  LatentBwdPlan sizing, l;
+  make_latent_bwd_plan(c, T, kSizingSms, &sizing);
+  make_latent_bwd_plan(c, T, std::min(num_sms(), kSizingSms), &l);
+  if (!ws || ((uintptr_t)ws & 255) || ws_bytes < sizing.total) return MOE_ERR_WORKSPACE;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int D = c->d_model, L = c->latent_dim;
+  float* part = at<float>(ws, l.part);
+  // n: the norm's output as the forward computed it (bf16), or z itself without the norm
+  const void* n = z;
+  if (c->up_proj_norm) {
+    n = at<void>(ws, l.n);
+    s = cuda_status(launch_rmsnorm(z, (int)T, L, c->rms_eps, w->rms_weight, const_cast<void*>(n), st));
+    if (s != MOE_OK) return s;
+  }
+  // dn = dout W_up (W_up read as stored: D rows x L columns, an MN-major B)
+  void* dn = c->up_proj_norm ? at<void>(ws, l.dn) : dz;
+  s = dense_gemm_bf16(dout, w->w_up_latent, (int)T, L, D, dn, l.dn_splits, part, status, st, D);
+  // dW_up = dout^T n, contracted over the tokens
+  if (s == MOE_OK) s = token_contraction_f32(dout, D, n, L, T, l.Tpad, dw_up, status, st);
+  if (s == MOE_OK && c->up_proj_norm)
+    s = cuda_status(launch_rmsnorm_backward(z, dn, w->rms_weight, (int)T, L, c->rms_eps, dz, at<float>(ws, l.r),
+                                            at<float>(ws, l.gpart), l.slab, drms_weight, st));
+  return s;
+}
+
+int moe_latent_down_backward(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T,
+                             const void* dx_routed, void* dx, float* dw_down, void* ws, size_t ws_bytes,
+                             moe_stream_t stream) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (c->latent_dim <= 0 || T < 0) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (T > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
+  if (!w || !w->w_down_latent || !x || !dx_routed || !dx || !dw_down) return MOE_ERR_INVALID_ARG;
+  LatentBwdPlan sizing, l;
+  make_latent_bwd_plan(c, T, kSizingSms, &sizing);
+  make_latent_bwd_plan(c, T, std::min(num_sms(), kSizingSms), &l);
+  if (!ws || ((uintptr_t)ws & 255) || ws_bytes < sizing.total) return MOE_ERR_WORKSPACE;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const int D = c->d_model, L = c->latent_dim;
+  // dx = dx_routed W_down (W_down read as stored: L rows x D columns, an MN-major B)
+  s = dense_gemm_bf16(dx_routed, w->w_down_latent, (int)T, D, L, dx, l.dx_splits, at<float>(ws, l.part), status, st,
+                      L);
+  // dW_down = dx_routed^T x, contracted over the tokens
+  if (s == MOE_OK) s = token_contraction_f32(dx_routed, L, x, D, T, l.Tpad, dw_down, status, st);
+  return s;
 }
 
 int moe_router_backward(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, const float* logits,

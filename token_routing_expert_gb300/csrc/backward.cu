@@ -398,6 +398,94 @@ cudaError_t launch_column_sum(const float* d, int T, int E, float* out, cudaStre
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Backward of the latent up-projection's input norm (page "Как устроен Olmo-core 3",
+// §"Латентная проекция экспертов": bias-free RMSNorm of the experts' combined output, then the
+// up-projection).  n = z r gamma, r = 1 / sqrt(mean(z^2) + eps):
+//   dz = r gamma dn - z r^3 mean(z gamma dn)        (fp32, stored bf16)
+//   dgamma = sum over tokens of dn z r               (fp32, fixed summation order)
+// ---------------------------------------------------------------------------
+
+// Warp per row: both row sums in one pass, dz in a second (the row is re-read from L1 / L2);
+// r_out[t] = r for the gain's gradient.
+__global__ void __launch_bounds__(256) rmsnorm_backward_kernel(const uint4* __restrict__ z,
+                                                                const uint4* __restrict__ dn,
+                                                                const uint4* __restrict__ gamma, int T, int vec,
+                                                                float eps, uint4* __restrict__ dz,
+                                                                float* __restrict__ r_out) {
+  const int lane = threadIdx.x & 31;
+  const long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const uint4* zr = z + t * vec;
+  const uint4* dr = dn + t * vec;
+  const uint32_t one2 = 0x3F803F80u;   // two bf16 ones: the gain without a weight
+  float ss = 0.f, dot = 0.f;
+  for (int c = lane; c < vec; c += 32) {
+    const uint4 a = zr[c], b = dr[c];
+    const uint4 gv = gamma ? gamma[c] : make_uint4(one2, one2, one2, one2);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float z0 = bf16_lo(aw[q]), z1 = bf16_hi(aw[q]);
+      const float g0 = bf16_lo(gw[q]), g1 = bf16_hi(gw[q]);
+      ss = fmaf(z0, z0, fmaf(z1, z1, ss));
+      dot = fmaf(z0 * g0, bf16_lo(bw[q]), fmaf(z1 * g1, bf16_hi(bw[q]), dot));
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  }
+  const float n = (float)(8 * vec);
+  const float r = rsqrtf(ss / n + eps);
+  const float k3 = r * r * r * (dot / n);
+  for (int c = lane; c < vec; c += 32) {
+    const uint4 a = zr[c], b = dr[c];
+    const uint4 gv = gamma ? gamma[c] : make_uint4(one2, one2, one2, one2);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float g0 = bf16_lo(gw[q]), g1 = bf16_hi(gw[q]);
+      o[q] = pack_bf16x2(r * g0 * bf16_lo(bw[q]) - bf16_lo(aw[q]) * k3, r * g1 * bf16_hi(bw[q]) - bf16_hi(aw[q]) * k3);
+    }
+    dz[t * vec + c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (lane == 0) r_out[t] = r;
+}
+
+// part[s][l] = sum over the rows of slab s of dn[t][l] z[t][l] r[t] (a thread per column).
+__global__ void __launch_bounds__(256) rms_gain_grad_kernel(const __nv_bfloat16* __restrict__ z,
+                                                             const __nv_bfloat16* __restrict__ dn,
+                                                             const float* __restrict__ r, int T, int L, int slab,
+                                                             float* __restrict__ part) {
+  const int l = blockIdx.x * blockDim.x + threadIdx.x;
+  if (l >= L) return;
+  const int t0 = blockIdx.y * slab, t1 = min(T, t0 + slab);
+  float acc = 0.f;
+  for (int t = t0; t < t1; ++t)
+    acc = fmaf(__bfloat162float(dn[(long long)t * L + l]) * __bfloat162float(z[(long long)t * L + l]), r[t], acc);
+  part[(long long)blockIdx.y * L + l] = acc;
+}
+
+cudaError_t launch_rmsnorm_backward(const void* z, const void* dn, const void* gamma, int T, int L, float eps,
+                                    void* dz, float* r, float* gain_part, int slab, float* dgamma, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (L % 8) return cudaErrorInvalidValue;
+  rmsnorm_backward_kernel<<<(T + 7) / 8, 256, 0, st>>>(static_cast<const uint4*>(z), static_cast<const uint4*>(dn),
+                                                       static_cast<const uint4*>(gamma), T, L / 8, eps,
+                                                       static_cast<uint4*>(dz), r);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !dgamma) return e;
+  const int nslab = (T + slab - 1) / slab;
+  rms_gain_grad_kernel<<<dim3((L + 255) / 256, nslab), 256, 0, st>>>(
+      static_cast<const __nv_bfloat16*>(z), static_cast<const __nv_bfloat16*>(dn), r, T, L, slab, gain_part);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  return launch_column_sum(gain_part, nslab, L, dgamma, st);
+}
+
 // out = sum over s of part[s] (fp32), slices of n4 float4.
 cudaError_t launch_sum_slices_f32(const float* part, int splits, long long n, float* out, cudaStream_t st);
 

@@ -53,7 +53,8 @@ EXPORTS = ["moe_quantize_rowwise_fp8", "moe_expert_capacity", "moe_permuted_rows
            "moe_permute_noalloc", "moe_accumulate_counts", "moe_load_imbalance", "moe_score_bias_update",
            "moe_backward_workspace_size", "moe_combine_backward", "moe_grouped_swiglu_backward",
            "moe_router_backward", "moe_host_workspace_size", "moe_layer_forward_host_batches",
-           "moe_grouped_swiglu_preact", "moe_layer_forward_preact", "moe_grouped_swiglu_backward_preact"]
+           "moe_grouped_swiglu_preact", "moe_layer_forward_preact", "moe_grouped_swiglu_backward_preact",
+           "moe_latent_restore_backward", "moe_latent_down_backward"]
 
 _lib = None
 
@@ -97,6 +98,8 @@ def load() -> ctypes.CDLL:
         "moe_accumulate_counts": [VP, ctypes.c_int32, VP, VP],
         "moe_backward_workspace_size": [cfgp, I64, P(SZ)],
         "moe_router_backward": [cfgp, wp, VP, I64, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP],
+        "moe_latent_restore_backward": [cfgp, wp, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
+        "moe_latent_down_backward": [cfgp, wp, VP, I64, VP, VP, VP, VP, SZ, VP],
         "moe_combine_backward": [cfgp, VP, VP, VP, VP, VP, I64, VP, VP, VP],
         "moe_grouped_swiglu_backward": [cfgp, wp, VP, VP, VP, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
         "moe_grouped_swiglu_backward_preact": [cfgp, wp, VP, VP, VP, VP, I64, VP, VP, VP, VP, VP, VP, SZ, VP],
@@ -521,6 +524,39 @@ def moe_grouped_swiglu_backward_preact(cfg, weights: DeviceWeights, x_routed, ga
         _ptr(dw_up_gate, torch.float32, "dw_up_gate"), _ptr(dw_out, torch.float32, "dw_out"),
         _ptr(bws, None, "ws"), bws.numel(), _stream(stream)), "moe_grouped_swiglu_backward_preact")
     return dx_routed, dw_up_gate, dw_out
+
+
+def moe_latent_restore_backward(cfg, weights: DeviceWeights, z, dout, bws, stream=None):
+    """(dz (T, L) bf16, dw_up (D, L) fp32, drms_weight (L,) fp32 or None without the norm)."""
+    T, L = z.shape
+    D = cfg.d_model
+    dev = z.device
+    dz = torch.empty((T, L), dtype=torch.bfloat16, device=dev)
+    dw_up = torch.empty((D, L), dtype=torch.float32, device=dev)
+    dg = torch.empty(L, dtype=torch.float32, device=dev) if cfg.up_proj_norm else None
+    ws_ = weights.struct()
+    _check(load().moe_latent_restore_backward(
+        ctypes.byref(cfg), ctypes.byref(ws_), _ptr(z, torch.bfloat16, "z"), T, _ptr(dout, torch.bfloat16, "dout"),
+        _ptr(dz, torch.bfloat16, "dz"), _ptr(dw_up, torch.float32, "dw_up"),
+        None if dg is None else _ptr(dg, torch.float32, "drms_weight"), _ptr(bws, None, "ws"), bws.numel(),
+        _stream(stream)), "moe_latent_restore_backward")
+    return dz, dw_up, dg
+
+
+def moe_latent_down_backward(cfg, weights: DeviceWeights, x, dx_routed, bws, stream=None):
+    """(dx (T, D) bf16, dw_down (L, D) fp32)."""
+    T, D = x.shape
+    L = cfg.latent_dim
+    dev = x.device
+    dx = torch.empty((T, D), dtype=torch.bfloat16, device=dev)
+    dw_down = torch.empty((L, D), dtype=torch.float32, device=dev)
+    ws_ = weights.struct()
+    _check(load().moe_latent_down_backward(
+        ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x, torch.bfloat16, "x"), T,
+        _ptr(dx_routed, torch.bfloat16, "dx_routed"), _ptr(dx, torch.bfloat16, "dx"),
+        _ptr(dw_down, torch.float32, "dw_down"), _ptr(bws, None, "ws"), bws.numel(), _stream(stream)),
+        "moe_latent_down_backward")
+    return dx, dw_down
 
 
 def moe_router_backward(cfg, weights: DeviceWeights, x, logits, idx, dweights, bws, stream=None):

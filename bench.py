@@ -382,8 +382,10 @@ def run_native(args):
                              device="cuda")
         fwd_out = torch.empty((T, spec.d_model), dtype=torch.bfloat16, device="cuda")
 
+        logits_keep = torch.empty((T, spec.num_experts), dtype=torch.float32, device="cuda")
+
         def train_forward():
-            native.moe_layer_forward_preact(cfg, wts, x, ws, out=fwd_out, preact=preact)
+            native.moe_layer_forward_preact(cfg, wts, x, ws, out=fwd_out, preact=preact, logits=logits_keep)
 
         def plain_forward():
             native.moe_layer_forward(cfg, wts, x, ws, out=fwd_out)
@@ -418,15 +420,31 @@ def run_native(args):
 
         bms = timed(backward_step)
         bms_re = timed(backward_step_recompute)
+        del bws
+        # the whole layer's backward (router and, when latent, the projections as well) after the
+        # training forward above left its intermediates in ws
+        train_forward()
+        lbws = native.layer_backward_workspace(cfg, T)
+        dout = torch.randn((T, spec.d_model), device="cuda").to(torch.bfloat16)
+        ldx = torch.empty((T, spec.d_model), dtype=torch.bfloat16, device="cuda")
+
+        def layer_backward_step():
+            native.moe_layer_backward(cfg, wts, x, ws, preact, logits_keep, dout, lbws, dx=ldx)
+
+        lms = timed(layer_backward_step)
+        del lbws
         if native.moe_get_status() != 0:
             raise SystemExit("device status error in the backward")
+        lflops = (12 * spec.rows * spec.routed_dim * spec.hidden_size + 4 * T * spec.num_experts * spec.d_model
+                  + (8 * T * spec.d_model * spec.latent_dim if spec.latent_dim else 0))
         bflops = 12 * spec.rows * spec.routed_dim * spec.hidden_size
         bwd = {"ms": bms, "tflops": bflops / (bms * 1e-3) / 1e12, "algorithmic_flops": bflops,
                "ms_recompute": bms_re, "forward_ms": fwd_plain_ms, "forward_keep_preact_ms": fwd_train_ms,
+               "layer_ms": lms, "layer_tflops": lflops / (lms * 1e-3) / 1e12, "layer_algorithmic_flops": lflops,
                "note": "combine backward + experts backward from the forward's kept pre-activations (dH, dX, "
                        "dW_out, dW_up_gate GEMMs = 12 R L h FLOPs); ms_recompute recomputes them instead "
-                       "(4 R L h more); forward_keep_preact_ms is the layer forward that keeps them"}
-        del bws
+                       "(4 R L h more); forward_keep_preact_ms is the layer forward that keeps them; layer_ms is "
+                       "moe_layer_backward: the whole layer's backward (+ router and latent projections)"}
 
     # load-balancing counters on this batch's histogram (between-step work, timed on its own)
     counts = inter["counts"].clone()

@@ -249,10 +249,12 @@ int moe_layer_forward(const moe_config_t* cfg, const moe_weights_t* w, const voi
  * moe_layer_forward for training: identical results, and the experts'
  * pre-activations are kept in `preact` (device, (rows, 2h) bf16, rows =
  * moe_permuted_rows(cfg, T), as moe_grouped_swiglu_preact writes them) for
- * moe_grouped_swiglu_backward_preact.  preact must not be NULL when T > 0.
+ * moe_grouped_swiglu_backward_preact / moe_layer_backward.  preact must not be
+ * NULL when T > 0.  logits: device (T, E) fp32 output (x W_router^T + b_router,
+ * as moe_router returns them), or NULL.
  */
 int moe_layer_forward_preact(const moe_config_t* cfg, const moe_weights_t* w, const void* x, int64_t T, void* out,
-                             void* preact, void* ws, size_t ws_bytes, moe_stream_t stream);
+                             void* preact, float* logits, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * moe_layer_forward with stage timing: when stage_events is not NULL it
@@ -388,6 +390,41 @@ int moe_latent_restore_backward(const moe_config_t* cfg, const moe_weights_t* w,
 int moe_latent_down_backward(const moe_config_t* cfg, const moe_weights_t* w, const void* x, int64_t T,
                              const void* dx_routed, void* dx, float* dw_down, void* ws, size_t ws_bytes,
                              moe_stream_t stream);
+
+/*
+ * The whole layer's backward (training), after moe_layer_forward_preact on the
+ * same x and weights: every step's derivative, in order
+ *   [latent: z recomputed by the combine, moe_latent_restore_backward] ->
+ *   moe_combine_backward -> moe_grouped_swiglu_backward_preact ->
+ *   [latent: moe_latent_down_backward] -> moe_router_backward,
+ * and dx = the experts' share (through the down-projection when latent) plus
+ * the router's, summed in fp32 and stored bf16.  score_bias gets no gradient.
+ *   fwd_ws / fwd_ws_bytes: the forward's workspace, unchanged since; its
+ *     intermediates (moe_workspace_layout) are read, not written.
+ *   preact: the forward's kept pre-activations (NULL: recomputed);
+ *   logits: the forward's logits output (device (T, E) fp32, required);
+ *   dout device (T, D) bf16: the gradient of the layer output;
+ *   dx device (T, D) bf16 out;
+ *   g: the weight gradients (device fp32 outputs, shapes as the weights):
+ *     dw_router, db_router (NULL: skipped; written only with a router bias),
+ *     dw_up_gate, dw_out, and when latent dw_down_latent, dw_up_latent and
+ *     drms_weight (NULL: skipped; written only with up_proj_norm).
+ *   ws: moe_layer_backward_workspace_size(cfg, T) bytes, 256-byte aligned.
+ */
+typedef struct {
+  float* dw_router;        /* (E, D) */
+  float* db_router;        /* (E) or NULL */
+  float* dw_up_gate;       /* (E, 2h, L') */
+  float* dw_out;           /* (E, L', h) */
+  float* dw_down_latent;   /* (L, D), latent */
+  float* dw_up_latent;     /* (D, L), latent */
+  float* drms_weight;      /* (L) or NULL, latent with up_proj_norm */
+} moe_grads_t;
+
+int moe_layer_backward_workspace_size(const moe_config_t* cfg, int64_t T, size_t* bytes);
+int moe_layer_backward(const moe_config_t* cfg, const moe_weights_t* w, const void* x, int64_t T, const void* fwd_ws,
+                       size_t fwd_ws_bytes, const void* preact, const float* logits, const void* dout, void* dx,
+                       const moe_grads_t* g, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /*
  * Load-balancing counters, section "Счётчики и bias-корректировка" (run between

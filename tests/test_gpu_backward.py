@@ -229,3 +229,94 @@ def test_latent_projection_backward(name):
     want_dx, want_dwd = ref.prepare_routed_input_backward(f64(inp["x"]), f64(inp["w_down"]), f64(dxr))
     close(dx.double().cpu().numpy(), want_dx, "dx (latent down-projection)")
     close(dw_down.double().cpu().numpy(), want_dwd, "dW_down")
+
+
+LAYER_CASES = {
+    # (spec, with an RMSNorm gain)
+    "router_and_score_bias": (WorkloadSpec("router_and_score_bias", T=600, d_model=256, num_experts=8, top_k=2,
+                                           hidden_size=128, gating="sigmoid", skew=True, score_bias_std=0.01,
+                                           normalize_expert_weights=1.0, seed=91), False),
+    "latent_gain": (WorkloadSpec("latent_gain", T=400, d_model=384, num_experts=6, top_k=2, hidden_size=64,
+                                 latent_dim=192, gating="topk_softmax", seed=92), True),
+    "latent_pair_tiles": (WorkloadSpec("latent_pair_tiles", T=1600, d_model=384, num_experts=4, top_k=2,
+                                       hidden_size=128, latent_dim=256, gating="softmax", seed=93), False),
+}
+
+
+@pytest.mark.parametrize("name", list(LAYER_CASES))
+def test_layer_backward(name):
+    """moe_layer_backward after moe_layer_forward_preact: every gradient against the oracle's chain of
+    derivatives on the forward's own routing and expert outputs, and bit for bit against the
+    library's steps called one by one."""
+    spec, with_gain = LAYER_CASES[name]
+    inp = generate(spec)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp)
+    T, D, E, k = spec.T, spec.d_model, spec.num_experts, spec.top_k
+    latent = bool(spec.latent_dim)
+    g = np.random.default_rng(spec.seed + 3)
+    bf = lambda a: torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16)   # noqa: E731
+    gain = bf(1.0 + 0.3 * g.standard_normal(spec.latent_dim)) if with_gain else None
+    if gain is not None:
+        wts.rms_weight = gain.cuda()
+    x = inp["x"].cuda()
+    ws = native.workspace(cfg, T)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    out, pre = native.moe_layer_forward_preact(cfg, wts, x, ws, logits=logits)
+    dout = bf(g.standard_normal((T, D))).cuda()
+    bws = native.layer_backward_workspace(cfg, T)
+    bws.fill_(0xFF)
+    dx, grads = native.moe_layer_backward(cfg, wts, x, ws, pre, logits, dout, bws)
+    assert native.moe_get_status() == 0
+    inter = native.layer_intermediates(cfg, T, ws)
+
+    # the same steps called one by one
+    sws = native.backward_workspace(cfg, T)
+    y, w, sc, ga, off = inter["y"], inter["weights"], inter["scatter_idx"], inter["gather_idx"], inter["offsets"]
+    dz = dout
+    if latent:
+        z = native.moe_combine(cfg, y, sc, w, T)
+        dz, dwu, dg = native.moe_latent_restore_backward(cfg, wts, z, dout, sws)
+        assert torch.equal(dwu, grads["dw_up_latent"]) and torch.equal(dg, grads["drms_weight"])
+    dy, dwts = native.moe_combine_backward(cfg, dz, y, sc, w, gather_idx=ga)
+    xr = inter["x_routed"] if latent else x
+    dxr, dwug, dwo = native.moe_grouped_swiglu_backward_preact(cfg, wts, xr, ga, off, sc, dy, pre, sws)
+    assert torch.equal(dwug, grads["dw_up_gate"]) and torch.equal(dwo, grads["dw_out"])
+    dx_e = dxr
+    if latent:
+        dx_e, dwd = native.moe_latent_down_backward(cfg, wts, x, dxr, sws)
+        assert torch.equal(dwd, grads["dw_down_latent"])
+    _, dx_r, dwr, dbr = native.moe_router_backward(cfg, wts, x, logits, inter["idx"], dwts, sws)
+    assert torch.equal(dwr, grads["dw_router"])
+    if cfg.router_bias:
+        assert torch.equal(dbr, grads["db_router"])
+    assert torch.equal((dx_e.float() + dx_r.float()).to(torch.bfloat16), dx)
+
+    # the oracle's chain of derivatives on the forward's routing and expert outputs
+    oc, ow = oracle_config(spec), oracle_weights(spec, inp)
+    gamma = None if gain is None else f64(gain)
+    x_np, y_np, w_np = f64(inp["x"]), y.double().cpu().numpy(), w.double().cpu().numpy()
+    sc_np, ga_np = sc.cpu().numpy(), ga.cpu().numpy()
+    perm = ref.Permutation(inter["counts"].cpu().numpy(), off.cpu().numpy(), ga_np, sc_np)
+    dz_np = f64(dout.cpu())
+    if latent:
+        z_np = ref.combine(y_np, sc_np, w_np)
+        dz_np, want_dwu, want_dg = ref.restore_routed_output_backward(oc, z_np, ow.w_up_latent, dz_np, gamma)
+        close(grads["dw_up_latent"].double().cpu().numpy(), want_dwu, "dW_up")
+        close(grads["drms_weight"].double().cpu().numpy(), want_dg, "dgamma")
+    want_dy, want_dwts = ref.combine_backward(dz_np, y_np, sc_np, w_np)
+    xr_np = xr.double().cpu().numpy()
+    want_dxr, want_grads = ref.experts_backward(oc, xr_np, perm, ow.expert, want_dy)
+    for e in range(E):
+        close(grads["dw_up_gate"][e].double().cpu().numpy(), np.concatenate(want_grads[e][:2]), f"dW_up_gate[{e}]")
+        close(grads["dw_out"][e].double().cpu().numpy(), want_grads[e][2], f"dW_out[{e}]")
+    want_dx = want_dxr
+    if latent:
+        want_dx, want_dwd = ref.prepare_routed_input_backward(x_np, ow.w_down_latent, want_dxr)
+        close(grads["dw_down_latent"].double().cpu().numpy(), want_dwd, "dW_down")
+    _, want_dx_r, want_dwr, want_dbr = ref.router_backward(oc, x_np, ow.w_router, ow.b_router, ow.score_bias,
+                                                           inter["idx"].cpu().numpy(), want_dwts)
+    close(grads["dw_router"].double().cpu().numpy(), want_dwr, "dW_router")
+    if cfg.router_bias:
+        close(grads["db_router"].double().cpu().numpy(), want_dbr, "db_router")
+    close(dx.double().cpu().numpy(), want_dx + want_dx_r, "dx (layer)")

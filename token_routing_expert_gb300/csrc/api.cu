@@ -802,7 +802,7 @@ int moe_latent_restore(const moe_config_t* c, const moe_weights_t* w, const void
 
 namespace {
 int layer_forward(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* out, void* preact,
-                  void* ws, size_t ws_bytes, moe_stream_t stream, void* const* stage_events) {
+                  float* logits, void* ws, size_t ws_bytes, moe_stream_t stream, void* const* stage_events) {
   Plan p;
   int s = check_call(c, T, ws, ws_bytes, &p);
   if (s != MOE_OK) return s;
@@ -830,7 +830,7 @@ int layer_forward(const moe_config_t* c, const moe_weights_t* w, const void* x, 
   mark(ev, 1, st);
   int32_t* idx = at<int32_t>(ws, p.idx);
   float* wts = at<float>(ws, p.wts);
-  s = run_router(c, w, x, p, nullptr, idx, wts, ws, status, st, ev);
+  s = run_router(c, w, x, p, logits, idx, wts, ws, status, st, ev);
   if (s != MOE_OK) return s;
   mark(ev, 3, st);
   int32_t* counts = at<int32_t>(ws, p.counts);
@@ -865,18 +865,18 @@ int layer_forward(const moe_config_t* c, const moe_weights_t* w, const void* x, 
 
 int moe_layer_forward_staged(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* out,
                              void* ws, size_t ws_bytes, moe_stream_t stream, void* const* stage_events) {
-  return layer_forward(c, w, x, T, out, nullptr, ws, ws_bytes, stream, stage_events);
+  return layer_forward(c, w, x, T, out, nullptr, nullptr, ws, ws_bytes, stream, stage_events);
 }
 
 int moe_layer_forward(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* out, void* ws,
                       size_t ws_bytes, moe_stream_t stream) {
-  return layer_forward(c, w, x, T, out, nullptr, ws, ws_bytes, stream, nullptr);
+  return layer_forward(c, w, x, T, out, nullptr, nullptr, ws, ws_bytes, stream, nullptr);
 }
 
 int moe_layer_forward_preact(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, void* out,
-                             void* preact, void* ws, size_t ws_bytes, moe_stream_t stream) {
+                             void* preact, float* logits, void* ws, size_t ws_bytes, moe_stream_t stream) {
   if (!preact && T > 0) return MOE_ERR_INVALID_ARG;
-  return layer_forward(c, w, x, T, out, preact, ws, ws_bytes, stream, nullptr);
+  return layer_forward(c, w, x, T, out, preact, logits, ws, ws_bytes, stream, nullptr);
 }
 
 
@@ -1262,6 +1262,106 @@ int moe_grouped_swiglu_backward_preact(const moe_config_t* c, const moe_weights_
   // dW_up_gate from dUG and the padded routed rows
   if (s == MOE_OK) s = kgrouped_f32(dy, Lr, H, h, b.kpad, k_off, E, dw_out, status, st, offsets, rows);
   if (s == MOE_OK) s = kgrouped_f32(dUG, 2 * h, xp, Lr, b.kpad, k_off, E, dw_up_gate, status, st);
+  return s;
+}
+
+// Whole-layer backward: the buffers it keeps between its steps, then room for the steps' own
+// workspaces (the largest of them).
+struct LayerBwdPlan {
+  size_t zc, dz, dy, dwts, dlogits, dxr, dxo, sub, sub_bytes, total;
+};
+
+void make_layer_bwd_plan(const moe_config_t* c, int64_t T, LayerBwdPlan* b) {
+  const int64_t E = c->num_experts, k = c->top_k, D = c->d_model;
+  const bool latent = c->latent_dim > 0;
+  const int64_t Lr = latent ? c->latent_dim : D;
+  const int64_t rows = c->capacity_factor > 0.f ? E * capacity_of(c, T) : T * k;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o += align256(bytes);
+    return at;
+  };
+  b->zc = take(latent ? (size_t)T * Lr * 2 : 0);
+  b->dz = take(latent ? (size_t)T * Lr * 2 : 0);
+  b->dy = take((size_t)rows * Lr * 2);
+  b->dwts = take((size_t)T * k * 4);
+  b->dlogits = take((size_t)T * E * 4);
+  b->dxr = take((size_t)T * Lr * 2);
+  b->dxo = take((size_t)T * D * 2);
+  size_t sub = 0;
+  moe_backward_workspace_size(c, T, &sub);
+  b->sub = o;
+  b->sub_bytes = sub;
+  b->total = o + align256(sub);
+}
+
+int moe_layer_backward_workspace_size(const moe_config_t* c, int64_t T, size_t* bytes) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (T < 0 || !bytes) return MOE_ERR_INVALID_ARG;
+  LayerBwdPlan b;
+  make_layer_bwd_plan(c, T, &b);
+  *bytes = b.total;
+  return MOE_OK;
+}
+
+int moe_layer_backward(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, const void* fwd_ws,
+                       size_t fwd_ws_bytes, const void* preact, const float* logits, const void* dout, void* dx,
+                       const moe_grads_t* g, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Plan p;
+  int s = check_call(c, T, const_cast<void*>(fwd_ws), fwd_ws_bytes, &p);
+  if (s != MOE_OK) return s;
+  if (T == 0) return MOE_OK;
+  const bool latent = p.latent;
+  if (!w || !x || !logits || !dout || !dx || !g || !g->dw_router || !g->dw_up_gate || !g->dw_out)
+    return MOE_ERR_INVALID_ARG;
+  if (latent && (!g->dw_down_latent || !g->dw_up_latent)) return MOE_ERR_INVALID_ARG;
+  LayerBwdPlan b;
+  make_layer_bwd_plan(c, T, &b);
+  if (!ws || ((uintptr_t)ws & 255) || ws_bytes < b.total) return MOE_ERR_WORKSPACE;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  void* fws = const_cast<void*>(fwd_ws);
+  const int32_t* idx = at<int32_t>(fws, p.idx);
+  const float* wts = at<float>(fws, p.wts);
+  const int32_t* offsets = at<int32_t>(fws, p.offsets);
+  const int32_t* gather = at<int32_t>(fws, p.gather);
+  const int32_t* scatter = at<int32_t>(fws, p.scatter);
+  const void* Y = at<void>(fws, p.Y);
+  const void* xr = latent ? at<void>(fws, p.xr) : x;
+  void* sub = at<void>(ws, b.sub);
+  void* dy = at<void>(ws, b.dy);
+  float* dwts = at<float>(ws, b.dwts);
+  void* dxr = at<void>(ws, b.dxr);
+  void* dxo = at<void>(ws, b.dxo);
+  // d z: through the up-projection and its norm (z recomputed by the combine), or dout itself
+  const void* dz = dout;
+  if (latent) {
+    void* zc = at<void>(ws, b.zc);
+    s = cuda_status(launch_combine(Y, scatter, wts, (int)T, p.k, p.L, (int)p.rows, 0, 0.f, nullptr, zc,
+                                   p.capacity ? 1 : 0, status, st));
+    if (s == MOE_OK)
+      s = moe_latent_restore_backward(c, w, zc, T, dout, at<void>(ws, b.dz), g->dw_up_latent, g->drms_weight, sub,
+                                      b.sub_bytes, stream);
+    dz = at<void>(ws, b.dz);
+  }
+  if (s == MOE_OK) s = moe_combine_backward(c, dz, Y, scatter, gather, wts, T, dy, dwts, stream);
+  if (s == MOE_OK)
+    s = moe_grouped_swiglu_backward_preact(c, w, xr, gather, offsets, scatter, T, dy, preact, dxr, g->dw_up_gate,
+                                           g->dw_out, sub, b.sub_bytes, stream);
+  // the layer input's gradient: the experts' path (through the down-projection when latent) plus
+  // the router's
+  const void* dx_experts = dxr;
+  if (s == MOE_OK && latent) {
+    s = moe_latent_down_backward(c, w, x, T, dxr, dx, g->dw_down_latent, sub, b.sub_bytes, stream);
+    dx_experts = dx;
+  }
+  if (s == MOE_OK)
+    s = moe_router_backward(c, w, x, T, logits, idx, dwts, at<float>(ws, b.dlogits), dxo, g->dw_router, g->db_router,
+                            sub, b.sub_bytes, stream);
+  if (s == MOE_OK) s = cuda_status(launch_add_bf16(dx_experts, dxo, T * (int64_t)p.D, dx, st));
   return s;
 }
 

@@ -486,6 +486,29 @@ cudaError_t launch_rmsnorm_backward(const void* z, const void* dn, const void* g
   return launch_column_sum(gain_part, nslab, L, dgamma, st);
 }
 
+// out = a + b for bf16 tensors (fp32 add, rounded to bf16), n8 16-byte vectors.
+__global__ void __launch_bounds__(256) add_bf16_kernel(const uint4* __restrict__ a, const uint4* __restrict__ b,
+                                                        long long n8, uint4* __restrict__ out) {
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n8; i += (long long)gridDim.x * blockDim.x) {
+    const uint4 x = a[i], y = b[i];
+    const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) o[q] = pack_bf16x2(bf16_lo(xw[q]) + bf16_lo(yw[q]), bf16_hi(xw[q]) + bf16_hi(yw[q]));
+    out[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_add_bf16(const void* a, const void* b, long long n, void* out, cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (n % 8) return cudaErrorInvalidValue;
+  const long long n8 = n / 8;
+  const int blocks = (int)std::min<long long>((n8 + 255) / 256, (long long)num_sms() * 8);
+  add_bf16_kernel<<<blocks, 256, 0, st>>>(static_cast<const uint4*>(a), static_cast<const uint4*>(b), n8,
+                                          static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
 // out = sum over s of part[s] (fp32), slices of n4 float4.
 cudaError_t launch_sum_slices_f32(const float* part, int splits, long long n, float* out, cudaStream_t st);
 

@@ -117,6 +117,8 @@ cudaError_t launch_pad_scatter(const int32_t* scatter, int R, const int32_t* off
 // gain's gradient through gain_part ((T + slab - 1) / slab x L fp32 partial sums).
 cudaError_t launch_rmsnorm_backward(const void* z, const void* dn, const void* gamma, int T, int L, float eps,
                                     void* dz, float* r, float* gain_part, int slab, float* dgamma, cudaStream_t st);
+// out = a + b (bf16, n elements, a multiple of 8).
+cudaError_t launch_add_bf16(const void* a, const void* b, long long n, void* out, cudaStream_t st);
 cudaError_t launch_combine_backward(const void* dz, const void* y, const int32_t* scatter_idx, const float* w, int T,
                                     int k, int L, int rows, void* dy, float* dw, int* status, cudaStream_t st);
 cudaError_t launch_zero_padding_rows(const int32_t* gather_idx, int rows, int cols, void* dst, cudaStream_t st);

@@ -46,6 +46,11 @@ class moe_weights_t(ctypes.Structure):
                                                   "w_up_gate_fp8", "w_up_gate_scale", "w_out_fp8", "w_out_scale")]
 
 
+class moe_grads_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("dw_router", "db_router", "dw_up_gate", "dw_out", "dw_down_latent",
+                                                  "dw_up_latent", "drms_weight")]
+
+
 EXPORTS = ["moe_quantize_rowwise_fp8", "moe_expert_capacity", "moe_permuted_rows", "moe_validate_config", "moe_num_params", "moe_num_active_params", "moe_latent_proj_params",
            "moe_workspace_size", "moe_router", "moe_permute", "moe_grouped_swiglu", "moe_combine",
            "moe_latent_down", "moe_latent_restore", "moe_layer_forward", "moe_layer_forward_staged",
@@ -54,7 +59,8 @@ EXPORTS = ["moe_quantize_rowwise_fp8", "moe_expert_capacity", "moe_permuted_rows
            "moe_backward_workspace_size", "moe_combine_backward", "moe_grouped_swiglu_backward",
            "moe_router_backward", "moe_host_workspace_size", "moe_layer_forward_host_batches",
            "moe_grouped_swiglu_preact", "moe_layer_forward_preact", "moe_grouped_swiglu_backward_preact",
-           "moe_latent_restore_backward", "moe_latent_down_backward"]
+           "moe_latent_restore_backward", "moe_latent_down_backward", "moe_layer_backward_workspace_size",
+           "moe_layer_backward"]
 
 _lib = None
 
@@ -86,7 +92,7 @@ def load() -> ctypes.CDLL:
         "moe_latent_down": [cfgp, wp, VP, I64, VP, VP, SZ, VP],
         "moe_latent_restore": [cfgp, wp, VP, I64, VP, VP, SZ, VP],
         "moe_layer_forward": [cfgp, wp, VP, I64, VP, VP, SZ, VP],
-        "moe_layer_forward_preact": [cfgp, wp, VP, I64, VP, VP, VP, SZ, VP],
+        "moe_layer_forward_preact": [cfgp, wp, VP, I64, VP, VP, VP, VP, SZ, VP],
         "moe_layer_forward_staged": [cfgp, wp, VP, I64, VP, VP, SZ, VP, P(VP)],
         "moe_layer_forward_launches": [cfgp, I64, P(ctypes.c_int32)],
         "moe_host_workspace_size": [cfgp, I64, P(SZ)],
@@ -100,6 +106,8 @@ def load() -> ctypes.CDLL:
         "moe_router_backward": [cfgp, wp, VP, I64, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP],
         "moe_latent_restore_backward": [cfgp, wp, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
         "moe_latent_down_backward": [cfgp, wp, VP, I64, VP, VP, VP, VP, SZ, VP],
+        "moe_layer_backward_workspace_size": [cfgp, I64, P(SZ)],
+        "moe_layer_backward": [cfgp, wp, VP, I64, VP, SZ, VP, VP, VP, VP, P(moe_grads_t), VP, SZ, VP],
         "moe_combine_backward": [cfgp, VP, VP, VP, VP, VP, I64, VP, VP, VP],
         "moe_grouped_swiglu_backward": [cfgp, wp, VP, VP, VP, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
         "moe_grouped_swiglu_backward_preact": [cfgp, wp, VP, VP, VP, VP, I64, VP, VP, VP, VP, VP, VP, SZ, VP],
@@ -392,8 +400,9 @@ def moe_layer_forward(cfg, weights: DeviceWeights, x, ws, out=None, stream=None)
     return out
 
 
-def moe_layer_forward_preact(cfg, weights: DeviceWeights, x, ws, out=None, preact=None, stream=None):
-    """The layer forward that keeps the experts' pre-activations: (out, preact (rows, 2h) bf16)."""
+def moe_layer_forward_preact(cfg, weights: DeviceWeights, x, ws, out=None, preact=None, logits=None, stream=None):
+    """The layer forward that keeps the experts' pre-activations: (out, preact (rows, 2h) bf16).
+    logits (optional (T, E) fp32 tensor) also receives the router logits."""
     T = x.shape[0]
     out = torch.empty((T, cfg.d_model), dtype=torch.bfloat16, device=x.device) if out is None else out
     rows = moe_permuted_rows(cfg, T)
@@ -402,6 +411,7 @@ def moe_layer_forward_preact(cfg, weights: DeviceWeights, x, ws, out=None, preac
     ws_ = weights.struct()
     _check(load().moe_layer_forward_preact(ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x, torch.bfloat16, "x"), T,
                                            _ptr(out, torch.bfloat16, "out"), _ptr(preact, torch.bfloat16, "preact"),
+                                           None if logits is None else _ptr(logits, torch.float32, "logits"),
                                            _ptr(ws, None, "ws"), ws.numel(), _stream(stream)),
            "moe_layer_forward_preact")
     return out, preact
@@ -557,6 +567,39 @@ def moe_latent_down_backward(cfg, weights: DeviceWeights, x, dx_routed, bws, str
         _ptr(dw_down, torch.float32, "dw_down"), _ptr(bws, None, "ws"), bws.numel(), _stream(stream)),
         "moe_latent_down_backward")
     return dx, dw_down
+
+
+def layer_backward_workspace(cfg, T, device="cuda") -> torch.Tensor:
+    n = ctypes.c_size_t()
+    _check(load().moe_layer_backward_workspace_size(ctypes.byref(cfg), T, ctypes.byref(n)),
+           "moe_layer_backward_workspace_size")
+    return torch.empty(max(1, n.value), dtype=torch.uint8, device=device)
+
+
+def moe_layer_backward(cfg, weights: DeviceWeights, x, ws, preact, logits, dout, bws, dx=None, stream=None):
+    """The whole layer's backward after moe_layer_forward_preact(x, ws): (dx (T, D) bf16, a dict of the
+    fp32 weight gradients: dw_router, db_router, dw_up_gate, dw_out and, when latent, dw_down_latent,
+    dw_up_latent, drms_weight; entries the configuration has no weight for are None)."""
+    T, D = x.shape
+    E, h = cfg.num_experts, cfg.hidden_size
+    Lr = cfg.latent_dim or cfg.d_model
+    dev = x.device
+    f32 = lambda *shape: torch.empty(shape, dtype=torch.float32, device=dev)   # noqa: E731
+    grads = {"dw_router": f32(E, D), "db_router": f32(E) if cfg.router_bias else None,
+             "dw_up_gate": f32(E, 2 * h, Lr), "dw_out": f32(E, Lr, h),
+             "dw_down_latent": f32(Lr, D) if cfg.latent_dim else None,
+             "dw_up_latent": f32(D, Lr) if cfg.latent_dim else None,
+             "drms_weight": f32(Lr) if cfg.latent_dim and cfg.up_proj_norm else None}
+    g = moe_grads_t(*[None if grads[n] is None else _ptr(grads[n], torch.float32, n)
+                      for n, _ in moe_grads_t._fields_])
+    dx = torch.empty((T, D), dtype=torch.bfloat16, device=dev) if dx is None else dx
+    ws_ = weights.struct()
+    _check(load().moe_layer_backward(
+        ctypes.byref(cfg), ctypes.byref(ws_), _ptr(x, torch.bfloat16, "x"), T, _ptr(ws, None, "ws"), ws.numel(),
+        None if preact is None else _ptr(preact, torch.bfloat16, "preact"), _ptr(logits, torch.float32, "logits"),
+        _ptr(dout, torch.bfloat16, "dout"), _ptr(dx, torch.bfloat16, "dx"), ctypes.byref(g), _ptr(bws, None, "bws"),
+        bws.numel(), _stream(stream)), "moe_layer_backward")
+    return dx, grads
 
 
 def moe_router_backward(cfg, weights: DeviceWeights, x, logits, idx, dweights, bws, stream=None):

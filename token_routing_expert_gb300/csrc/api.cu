@@ -984,7 +984,8 @@ int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
   int k = 0;
   if (p.latent) k += p.down_splits > 1 ? 2 : 1;  // latent down (+ split-K reduce)
   k += p.router_splits > kTopkFusedSlices ? 3 : 2;   // router GEMM, (sum of a deep split-K,) top-k
-  k += p.capacity ? 4 : 3;                       // permute: count, scan, place (, capacity slots)
+  // permute: one cluster launch or count, scan, place (, capacity slots)
+  k += (permute_fits_cluster((int)p.R, p.E) ? 1 : 3) + (p.capacity ? 1 : 0);
   k += p.capacity ? 1 : 0;                       // tile table (the dropless scan writes it itself)
   k += use_pair_tiles(p) ? 0 : 1;                // row gather for 128-row tiles (on CTA pairs grouped
                                                  // GEMM 1 gathers its rows)

@@ -83,6 +83,8 @@ cudaError_t launch_topk(const float* logits, int n_partials, int64_t partial_str
 // permute_blocks(R, chunk) * E ints.
 // tile_off (optional, E + 1 ints): also the grouped GEMMs' tile table, prefix sums of
 // ceil(count / rows_per_tile), as launch_tile_table would write it.
+// The permutation of R assignments over E experts runs as one cluster launch (else three kernels).
+bool permute_fits_cluster(int R, int E);
 cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, int32_t* offsets,
                            int32_t* gather_idx, int32_t* scatter_idx, int k, int chunk, int32_t* blk_scratch,
                            int* status, cudaStream_t stream, int rows_per_tile = 0, int32_t* tile_off = nullptr);

@@ -4,10 +4,12 @@
 //   offsets[e] + #{f' < f : idx[f'] == e}
 // (page "Как устроен Olmo-core 3: обучение больших MoE-моделей",
 // §"Пересылка токенов между экспертами": indices sorted by expert, bins =
-// cumulative sum of the per-expert counts).  Three passes over chunks of
-// assignments (256 to 4096 per block): per-chunk histograms; per-expert scan over chunks plus
-// the exclusive scan over experts; placement, where each warp walks its
-// slice of the chunk in order and ranks equal experts with __match_any_sync.
+// cumulative sum of the per-expert counts).  Up to 16,384 assignments it is one launch on one
+// 8-CTA cluster (histograms exchanged through distributed shared memory); beyond, three passes
+// over chunks of assignments (256 to 4096 per block): per-chunk histograms; per-expert scan over
+// chunks plus the exclusive scan over experts; placement, where each warp walks its slice of the
+// chunk in order and ranks equal experts with __match_any_sync (the cluster kernel places the
+// same way).
 #include <algorithm>
 
 #include "common.cuh"
@@ -175,10 +177,168 @@ __global__ void __launch_bounds__(kPermThreads) perm_place_kernel(const int32_t*
   }
 }
 
+// ---------------------------------------------------------------------------
+// The same permutation in one launch, for up to kClusterCtas x kClusterChunk assignments: one
+// cluster of kClusterCtas CTAs, each owning a contiguous chunk.  The CTAs count their chunks into
+// shared memory, meet at a cluster barrier, read each other's histograms through distributed
+// shared memory (every CTA computes the expert offsets and its own chunk's prefix; CTA 0 writes
+// counts, offsets and the tile table), meet again so that no CTA leaves while another still
+// reads its histogram, and place their assignments as perm_place_kernel does.
+// ---------------------------------------------------------------------------
+constexpr int kClusterCtas = 8;
+constexpr int kClusterThreads = 1024;
+constexpr int kClusterWarps = kClusterThreads / 32;
+// Each of a CTA's 32 warps walks its slice serially, so the single cluster only pays off while the
+// slices are short: decode-sized batches (R = 512: 10.8 vs 13.7 us per layer's permutation);
+// at R = 65,536 the three-kernel path, 76 blocks wide, was 10 us faster.
+constexpr int kClusterChunk = 2048;
+
+__device__ __forceinline__ int ld_shared_cluster_i32(uint32_t cluster_addr) {
+  int v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kClusterThreads) perm_cluster_kernel(const int32_t* __restrict__ idx, int R, int E,
+                                                                        int k, int chunk, int32_t* __restrict__ counts,
+                                                                        int32_t* __restrict__ offsets,
+                                                                        int rows_per_tile,
+                                                                        int32_t* __restrict__ tile_off,
+                                                                        int32_t* __restrict__ gather_idx,
+                                                                        int32_t* __restrict__ scatter_idx,
+                                                                        int* status) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
+  extern __shared__ int32_t sm[];
+  int32_t* wh = sm;                          // [kClusterWarps][E]: per-warp counts, then bases
+  int32_t* hist = wh + kClusterWarps * E;    // [E]: this chunk's histogram (read by the other CTAs)
+  __shared__ int s_warp[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t rank = cluster_ctarank();
+  for (int i = threadIdx.x; i < kClusterWarps * E; i += blockDim.x) wh[i] = 0;
+  __syncthreads();
+  const int base = (int)rank * chunk;
+  const int end = min(R, base + chunk);
+  const int sub = (chunk + kClusterWarps - 1) / kClusterWarps;
+  const int s0 = min(end, base + warp * sub);
+  const int s1 = min(end, s0 + sub);
+  int32_t* mine = wh + warp * E;
+
+  // this warp's per-expert counts
+  for (int r0 = s0; r0 < s1; r0 += 32) {
+    const int r = r0 + lane;
+    const int e = r < s1 ? idx[r] : -1;
+    const bool valid = e >= 0 && e < E;
+    if (r < s1 && !valid) set_status(status, MOE_ERR_BOUNDS);
+    const unsigned grp = __match_any_sync(0xffffffffu, valid ? e : -1);
+    if (valid && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < kClusterWarps; ++w) c += wh[w * E + e];
+    hist[e] = c;
+  }
+  cluster_sync_all();   // every CTA's histogram is complete
+
+  // expert totals and this chunk's prefix within each expert, from all CTAs' histograms
+  // (E <= 1024: a thread per expert)
+  const uint32_t hist_addr = smem_u32(hist);
+  const int e = threadIdx.x;
+  int tot = 0, pre = 0;
+  if (e < E) {
+    for (int c = 0; c < kClusterCtas; ++c) {
+      const int h = ld_shared_cluster_i32(map_to_cta(hist_addr + 4u * (uint32_t)e, (uint32_t)c));
+      if (c < (int)rank) pre += h;
+      tot += h;
+    }
+  }
+  const int excl = block_exclusive_scan(tot, s_warp);
+  if (e < E) {
+    // per-warp bases: expert e's offset, its rows in earlier chunks, then the earlier warps' counts
+    int run = excl + pre;
+    for (int w = 0; w < kClusterWarps; ++w) {
+      const int c = wh[w * E + e];
+      wh[w * E + e] = run;
+      run += c;
+    }
+    if (rank == 0) {
+      counts[e] = tot;
+      offsets[e] = excl;
+      if (e == E - 1) offsets[E] = excl + tot;
+    }
+  }
+  if (tile_off) {
+    __syncthreads();   // s_warp is reused
+    const int tiles = e < E ? (tot + rows_per_tile - 1) / rows_per_tile : 0;
+    const int texcl = block_exclusive_scan(tiles, s_warp);
+    if (rank == 0 && e < E) {
+      tile_off[e] = texcl;
+      if (e == E - 1) tile_off[E] = texcl + tiles;
+    }
+  }
+  __syncthreads();   // the bases in wh are complete
+  cluster_sync_all();   // no CTA leaves while another still reads its histogram
+
+  // stable placement
+  const unsigned lt = (1u << lane) - 1u;
+  for (int r0 = s0; r0 < s1; r0 += 32) {
+    const int r = r0 + lane;
+    const int e = r < s1 ? idx[r] : -1;
+    const bool valid = e >= 0 && e < E;
+    const unsigned grp = __match_any_sync(0xffffffffu, valid ? e : -1);
+    int pos = 0;
+    if (valid) pos = mine[e] + __popc(grp & lt);
+    __syncwarp();
+    if (valid && lane == __ffs(grp) - 1) mine[e] += __popc(grp);
+    __syncwarp();
+    if (valid) {
+      gather_idx[pos] = r / k;
+      scatter_idx[r] = pos;
+    }
+  }
+}
+
+bool permute_fits_cluster(int R, int E) { return R > 0 && R <= kClusterCtas * kClusterChunk && E <= 1024; }
+
+cudaError_t launch_permute_cluster(const int32_t* idx, int R, int E, int32_t* counts, int32_t* offsets,
+                                   int32_t* gather_idx, int32_t* scatter_idx, int k, int* status,
+                                   cudaStream_t stream, int rows_per_tile, int32_t* tile_off) {
+  if (!permute_fits_cluster(R, E)) return cudaErrorInvalidValue;
+  const int chunk = (R + kClusterCtas - 1) / kClusterCtas;
+  const size_t smem = (size_t)(kClusterWarps + 1) * E * sizeof(int32_t);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(perm_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)((kClusterWarps + 1) * 1024 * sizeof(int32_t)));
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kClusterCtas);
+  cfg.blockDim = dim3(kClusterThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attrs[2];
+  attrs[0].id = cudaLaunchAttributeClusterDimension;
+  attrs[0].val.clusterDim.x = kClusterCtas;
+  attrs[0].val.clusterDim.y = 1;
+  attrs[0].val.clusterDim.z = 1;
+  attrs[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attrs[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attrs;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, perm_cluster_kernel, idx, R, E, k, chunk, counts, offsets, rows_per_tile, tile_off,
+                            gather_idx, scatter_idx, status);
+}
+
 cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, int32_t* offsets,
                            int32_t* gather_idx, int32_t* scatter_idx, int k, int chunk, int32_t* blk, int* status,
                            cudaStream_t stream, int rows_per_tile, int32_t* tile_off) {
   if (chunk < 256 || chunk > kMaxChunk || chunk % 256) return cudaErrorInvalidValue;
+  if (permute_fits_cluster(R, E))   // one launch: the whole permutation on one cluster
+    return launch_permute_cluster(idx, R, E, counts, offsets, gather_idx, scatter_idx, k, status, stream,
+                                  rows_per_tile, tile_off);
   const int nb = permute_blocks(R, chunk);
   if (nb > 0) {
     launch_pdl(perm_count_kernel, nb, kPermThreads, E * sizeof(int32_t), stream, idx, R, E, chunk, blk, status);

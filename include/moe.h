@@ -13,7 +13,7 @@
  *    (passed as void*), logits / routing weights / biases are fp32, indices
  *    are int32.  Weights follow the linear-layer layout (out, in).
  *  - Device work is enqueued on `stream` and is asynchronous; no entry point
- *    synchronises, except moe_get_status.
+ *    synchronises, except moe_get_status and moe_check_wait_timeout.
  *  - `ws` is a caller-owned device workspace of at least
  *    moe_workspace_size(cfg, T) bytes, 256-byte aligned.  Its contents on
  *    entry are irrelevant; entry points overwrite parts of it.
@@ -481,6 +481,18 @@ int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* idx, int64_t T, 
 /* Synchronises `stream`, then returns (and clears, if `clear`) the device
  * status word of the current device in *device_status. */
 int moe_get_status(moe_stream_t stream, int32_t* device_status, int clear);
+
+/*
+ * Health check of the device-side failure path (host function; synchronises
+ * the stream).  Every pipelined kernel waits on mbarriers with a bound: after
+ * 2 s it records MOE_ERR_TIMEOUT in the status word, raises its CTA's abort flag
+ * and returns instead of hanging.  This runs that same wait on a barrier nothing
+ * completes, for limit_ms (1..2000) milliseconds, reads the status word back and
+ * clears it again.  Returns MOE_OK when the wait gave up after the limit and
+ * reported MOE_ERR_TIMEOUT (*waited_ms = how long it waited), MOE_ERR_CUDA if
+ * not, or the status word's earlier error, left untouched.
+ */
+int moe_check_wait_timeout(int32_t limit_ms, int32_t* waited_ms, moe_stream_t stream);
 
 /* Static, human-readable name of a status code. */
 const char* moe_status_string(int status);

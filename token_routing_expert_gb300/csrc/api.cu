@@ -1366,6 +1366,26 @@ int moe_layer_backward(const moe_config_t* c, const moe_weights_t* w, const void
   return s;
 }
 
+int moe_check_wait_timeout(int32_t limit_ms, int32_t* waited_ms, moe_stream_t stream) {
+  if (limit_ms < 1 || limit_ms > 2000 || !waited_ms) return MOE_ERR_INVALID_ARG;
+  int* status = status_ptr();
+  if (!status) return MOE_ERR_NO_DEVICE;
+  cudaStream_t st = (cudaStream_t)stream;
+  int before = 0;
+  if (cudaMemcpyAsync(&before, status, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (before != MOE_OK) return before;   // an earlier error stays reported, untouched
+  int res[2] = {0, 0};
+  if (launch_wait_timeout_check((uint64_t)limit_ms * 1000000ull, status, res, st) != cudaSuccess) return MOE_ERR_CUDA;
+  int after = 0;
+  if (cudaMemcpyAsync(&after, status, sizeof(int), cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaMemsetAsync(status, 0, sizeof(int), st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  *waited_ms = res[1];
+  return (res[0] == 1 && after == MOE_ERR_TIMEOUT) ? MOE_OK : MOE_ERR_CUDA;
+}
+
 int moe_get_status(moe_stream_t stream, int32_t* device_status, int clear) {
   if (!device_status) return MOE_ERR_INVALID_ARG;
   int* status = status_ptr();

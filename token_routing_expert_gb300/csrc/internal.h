@@ -121,6 +121,10 @@ cudaError_t launch_rmsnorm_backward(const void* z, const void* dn, const void* g
                                     void* dz, float* r, float* gain_part, int slab, float* dgamma, cudaStream_t st);
 // out = a + b (bf16, n elements, a multiple of 8).
 cudaError_t launch_add_bf16(const void* a, const void* b, long long n, void* out, cudaStream_t st);
+// Runs a bounded mbarrier wait that nothing completes (limit_ns) and copies its result to the
+// host, synchronising the stream: result_host[0] = 1 if it gave up with the abort flag raised,
+// result_host[1] = milliseconds waited.  The wait records MOE_ERR_TIMEOUT in *status.
+cudaError_t launch_wait_timeout_check(uint64_t limit_ns, int* status, int* result_host, cudaStream_t st);
 cudaError_t launch_combine_backward(const void* dz, const void* y, const int32_t* scatter_idx, const float* w, int T,
                                     int k, int L, int rows, void* dy, float* dw, int* status, cudaStream_t st);
 cudaError_t launch_zero_padding_rows(const int32_t* gather_idx, int rows, int cols, void* dst, cudaStream_t st);

@@ -60,7 +60,7 @@ EXPORTS = ["moe_quantize_rowwise_fp8", "moe_expert_capacity", "moe_permuted_rows
            "moe_router_backward", "moe_host_workspace_size", "moe_layer_forward_host_batches",
            "moe_grouped_swiglu_preact", "moe_layer_forward_preact", "moe_grouped_swiglu_backward_preact",
            "moe_latent_restore_backward", "moe_latent_down_backward", "moe_layer_backward_workspace_size",
-           "moe_layer_backward"]
+           "moe_layer_backward", "moe_check_wait_timeout"]
 
 _lib = None
 
@@ -107,6 +107,7 @@ def load() -> ctypes.CDLL:
         "moe_latent_restore_backward": [cfgp, wp, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
         "moe_latent_down_backward": [cfgp, wp, VP, I64, VP, VP, VP, VP, SZ, VP],
         "moe_layer_backward_workspace_size": [cfgp, I64, P(SZ)],
+        "moe_check_wait_timeout": [ctypes.c_int32, P(ctypes.c_int32), VP],
         "moe_layer_backward": [cfgp, wp, VP, I64, VP, SZ, VP, VP, VP, VP, P(moe_grads_t), VP, SZ, VP],
         "moe_combine_backward": [cfgp, VP, VP, VP, VP, VP, I64, VP, VP, VP],
         "moe_grouped_swiglu_backward": [cfgp, wp, VP, VP, VP, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
@@ -567,6 +568,14 @@ def moe_latent_down_backward(cfg, weights: DeviceWeights, x, dx_routed, bws, str
         _ptr(dw_down, torch.float32, "dw_down"), _ptr(bws, None, "ws"), bws.numel(), _stream(stream)),
         "moe_latent_down_backward")
     return dx, dw_down
+
+
+def moe_check_wait_timeout(limit_ms: int = 20, stream=None) -> int:
+    """Runs a bounded wait that nothing completes; returns how many ms it waited before giving up
+    (raises if the timeout was not reported through the status word)."""
+    waited = ctypes.c_int32()
+    _check(load().moe_check_wait_timeout(limit_ms, ctypes.byref(waited), _stream(stream)), "moe_check_wait_timeout")
+    return waited.value
 
 
 def layer_backward_workspace(cfg, T, device="cuda") -> torch.Tensor:

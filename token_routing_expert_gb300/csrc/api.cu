@@ -593,8 +593,11 @@ int grouped_bf16(const void* A, int64_t rows, const void* B, int64_t b_rows_tota
 // kpad rows x M columns and B kpad rows x N columns (both MN-major operands), K_e = the 64-row
 // tiles [k_off[e], k_off[e+1]).
 // a_off (optional): group e's K rows of A start at A row a_off[e] (A has a_rows rows) instead of 64 k_off[e].
+// b_gather (optional, CTA pairs): B's K rows of group e are rows b_gather[b_goff[e] + r] of B itself
+// (b_rows rows), read by the kernel, instead of a padded copy.
 int kgrouped_f32(const void* A, int M, const void* B, int N, int64_t kpad, const int32_t* k_off, int E, float* out,
-                 int* status, cudaStream_t st, const int32_t* a_off = nullptr, int64_t a_rows = 0) {
+                 int* status, cudaStream_t st, const int32_t* a_off = nullptr, int64_t a_rows = 0,
+                 const int32_t* b_gather = nullptr, const int32_t* b_goff = nullptr, int64_t b_rows = 0) {
   GemmProblem g{};
   g.A = A;
   g.a_mn_major = 1;
@@ -618,6 +621,13 @@ int kgrouped_f32(const void* A, int M, const void* B, int N, int64_t kpad, const
   g.ldo = N;
   g.split_stride = (int64_t)M * N;
   g.status = status;
+  if (b_gather && g.pair_tiles) {
+    g.b_gather = b_gather;
+    g.b_src = B;
+    g.b_goff = b_goff;
+    g.b_src_rows = (int)b_rows;
+    g.B = nullptr;
+  }
   return cuda_status(launch_gemm(g, st));
 }
 
@@ -1209,9 +1219,15 @@ int moe_grouped_swiglu_backward_preact(const moe_config_t* c, const moe_weights_
   void* dXp = at<void>(ws, b.dxp);
   const int prows = (int)b.kpad;   // rows of the padded layout (the ones past 64 k_off[E] are never read)
 
-  // padded layout: offsets, the routed rows copied into it, the scatter moved into it
+  // padded layout: offsets, the scatter moved into it, and the routed rows copied into it where a GEMM
+  // cannot gather them itself (the recomputation of the pre-activations; 1-CTA weight-gradient tiles)
+  // dW_up_gate on CTA pairs can read x_routed through the gather indices itself.  That pays off when
+  // the padded copy it saves is dear: many small experts, whose padding adds many rows (latent
+  // prefill shape, 292 rows per expert: experts backward 10.26 -> 9.49 ms); with ~1,000 rows per
+  // expert the copy is cheaper than gathering in the GEMM (OlmoE shape: 1.40 ms copying vs 1.47)
+  const bool gather_b = preact != nullptr && 2 * h >= 256 && (int64_t)rows < 512 * (int64_t)E;
   s = cuda_status(launch_pad_offsets(offsets, E, pair ? 256 : 128, k_off, poff, tile_off, st));
-  if (s == MOE_OK)
+  if (s == MOE_OK && !gather_b)
     s = cuda_status(launch_pad_rows(x_routed, gather_idx, offsets, k_off, E, (int)T, Lr, prows, xp, status, st));
   if (s == MOE_OK) s = cuda_status(launch_pad_scatter(scatter_idx, (int)T * k, offsets, poff, E, scat, st));
   // pre-activations [u | g]: the forward's (dense rows), or recomputed in the padded layout
@@ -1262,7 +1278,13 @@ int moe_grouped_swiglu_backward_preact(const moe_config_t* c, const moe_weights_
   // dW_out from dY's dense rows (a tile's rows past the expert meet H's zero padding rows) and H,
   // dW_up_gate from dUG and the padded routed rows
   if (s == MOE_OK) s = kgrouped_f32(dy, Lr, H, h, b.kpad, k_off, E, dw_out, status, st, offsets, rows);
-  if (s == MOE_OK) s = kgrouped_f32(dUG, 2 * h, xp, Lr, b.kpad, k_off, E, dw_up_gate, status, st);
+  if (s == MOE_OK) {
+    if (gather_b)
+      s = kgrouped_f32(dUG, 2 * h, x_routed, Lr, b.kpad, k_off, E, dw_up_gate, status, st, nullptr, 0, gather_idx,
+                       offsets, T);
+    else
+      s = kgrouped_f32(dUG, 2 * h, xp, Lr, b.kpad, k_off, E, dw_up_gate, status, st);
+  }
   return s;
 }
 

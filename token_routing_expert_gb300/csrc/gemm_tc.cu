@@ -65,6 +65,11 @@ struct GemmParams {
   int preact_dense;        // SwiGLU backward: [u | g] rows at A's rows (shifted by a_off), else the output's
   void* out2;              // SwiGLU backward: H
   long long ldo2;
+  const int* b_gather;     // K-grouped, gathered B: group g's K row r is row b_gather[b_goff[g] + r] of b_src
+  const uint8_t* b_src;    //   (r < the group's count; zeros past it), b_ld_bytes apart
+  const int* b_goff;
+  long long b_ld_bytes;
+  int b_src_rows;
   int* status;
 };
 
@@ -738,6 +743,76 @@ struct PairCfgT {
   static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 };
 
+// Producer of a gathered, MN-major B operand of the K-grouped pair GEMM (4 warps of each CTA):
+// for every k-tile the group's 64 K rows, row r from source row b_gather[b_goff[g] + local row]
+// (zeros past the group's count), this CTA's 128 of the tile's 256 N columns as two 64-column
+// blocks, in the 128-byte-swizzled layout a TMA load of 64 x 64 boxes writes.  Thread t moves
+// chunk (t & 7) of rows (t >> 3) + 16 j of both blocks; the next k-tile's source rows are loaded
+// while the current one is copied.  Arrivals and the relay work as for a gathered A.
+template <int NST>
+__device__ __forceinline__ void gather_b_mn_producer(const GemmParams& p, const int* s_toff, const int* s_goff,
+                                                     int t_first, int t_step, int total_tiles, int rank,
+                                                     uint8_t* smem, int stage_bytes, int a_bytes, uint64_t* empty_bar,
+                                                     uint64_t* gath_bar, volatile int* abort_flag) {
+  const int t = threadIdx.x - kGatherThread0;
+  const int lane = t & 31;
+  const int chunk = t & 7;
+  uint32_t stage = 0, phase = 0;
+  bool ok = true;
+  for (int tile = t_first; tile < total_tiles && ok; tile += t_step) {
+    const TileCoord c = decode_tile<BM2>(tile, p, s_toff, s_goff);
+    const int goff = __ldg(p.b_goff + c.group);
+    const int cnt = __ldg(p.b_goff + c.group + 1) - goff;
+    const int col0 = c.nt * 256 + 128 * rank;   // this CTA's first N column
+    // loads only: the values are checked one k-tile later, so the loads' latency is not waited on
+    auto rows_of = [&](int kt, int (&raw)[4]) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int rl = (kt - c.kt0) * 64 + (t >> 3) + 16 * j;
+        raw[j] = rl < cnt ? __ldg(p.b_gather + goff + rl) : -1;
+      }
+    };
+    int nxt[4];
+    if (c.kt0 < c.kt1) rows_of(c.kt0, nxt);
+    for (int kt = c.kt0; kt < c.kt1; ++kt) {
+      int tok[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        int src = nxt[j];
+        if (src < -1 || src >= p.b_src_rows) {
+          set_status(p.status, MOE_ERR_BOUNDS);
+          src = -1;
+        }
+        tok[j] = src;
+      }
+      if (kt + 1 < c.kt1) rows_of(kt + 1, nxt);
+      int free_slot = 1;
+      if (lane == 0) free_slot = mbar_wait_cluster(&empty_bar[stage], phase ^ 1u, abort_flag, p.status) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, free_slot, 0)) {
+        ok = false;
+        break;
+      }
+      const uint32_t sb = smem_u32(smem + stage * stage_bytes + a_bytes);
+#pragma unroll
+      for (int b = 0; b < 2; ++b) {
+        const int col = col0 + 64 * b + 8 * chunk;
+        const bool col_ok = col < p.N;
+        const uint8_t* cb = p.b_src + (long long)col * 2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int r = (t >> 3) + 16 * j;
+          const int src = col_ok ? tok[j] : -1;
+          cp_async_16(sb + b * 8192 + r * 128 + ((chunk ^ (r & 7)) << 4),
+                      cb + (long long)(src < 0 ? 0 : src) * p.b_ld_bytes, src < 0 ? 0u : 16u);
+        }
+      }
+      cp_async_arrive_noinc(&gath_bar[stage]);
+      if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1u; }
+    }
+  }
+  cp_async_wait_all();   // every copy lands before the CTA's shared memory can go away
+}
+
 // SwiGLU backward on CTA pairs: the [u | g] pre-activations reach the epilogue through TMA boxes
 // (128 rows x 32 columns of u and of g, 64-byte swizzle) in a 2-slot ring per half of the
 // epilogue warps.  The half's first warp issues chunk j + 2 once all four warps have taken
@@ -820,8 +895,9 @@ __device__ __forceinline__ void swb_pair_tile(uint32_t tbase, const TileCoord& c
   }
 }
 
-template <int EPI, bool F8 = false, bool GA = false>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
+// GB: the B operand of a K-grouped fp32 GEMM is gathered by the kernel (gather_b_mn_producer).
+template <int EPI, bool F8 = false, bool GA = false, bool GB = false>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsGA : kThreads, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmP, const GemmParams p) {
   pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
@@ -862,8 +938,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
     *abort_flag = 0;
     for (int s = 0; s < C::STAGES; ++s) {
       // CTA 0 only: its producer's arrive + both CTAs' bytes (+ both CTAs' gathered-rows relays)
-      mbar_init(&full_bar[s], GA ? 3 : 1);
-      if (GA) mbar_init(&gath_bar[s], 32 * kGatherWarps);
+      mbar_init(&full_bar[s], GA || GB ? 3 : 1);
+      if (GA || GB) mbar_init(&gath_bar[s], 32 * kGatherWarps);
       mbar_init(&empty_bar[s], 1);    // one multicast commit per use
     }
     for (int a = 0; a < 2; ++a) {
@@ -881,7 +957,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
   if (warp == 1) tmem_alloc_pair(tmem_holder, C::TMEM_COLS);
   if (warp == 0 && lane == 0) {
     if (!GA) tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmB);
+    if (!GB) tma_prefetch_desc(&tmB);
     if constexpr (C::SWB) tma_prefetch_desc(&tmP);
   }
   tc_fence_before();
@@ -912,7 +988,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
           // (its accumulator rows are never stored) and saves their L2 bytes
           const bool a1 = c.rows > 128;
           if (rank == 0)
-            mbar_arrive_expect_tx(&full_bar[stage], GA ? 2 * C::B_BYTES : 2 * C::STAGE_BYTES - (a1 ? 0 : C::A_BYTES));
+            mbar_arrive_expect_tx(&full_bar[stage], GA ? 2 * C::B_BYTES
+                                                    : (GB ? 2 * C::A_BYTES : 2 * C::STAGE_BYTES) - (a1 ? 0 : C::A_BYTES));
           const int kx = kt * (F8 ? 2 * BK : BK);
           if (!GA && (rank == 0 || a1)) {
             if (p.a_mn) {   // MN-major A: this CTA's 128 M columns as two 64-column blocks
@@ -922,7 +999,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
               tma_load_2d_pair(sa, &tmA, full0, kx, arow + ash);
             }
           }
-          if (EPI != EPI_SWIGLU && p.b_mn) {   // MN-major B: this CTA's 128 columns as two 64-column blocks
+          if (GB) {
+            // B arrives through the gather warps
+          } else if (EPI != EPI_SWIGLU && p.b_mn) {   // MN-major B: this CTA's 128 columns, two 64-column blocks
             for (int b = 0; b < 2; ++b)
               tma_load_2d_pair(sa + C::A_BYTES + b * 8192, &tmB, full0, c.nt * C::BN + 128 * (int)rank + 64 * b,
                                c.group * p.b_rows_per_group + kt * BK);
@@ -1022,11 +1101,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA ? kThreadsGA : kT
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(&tempty_bar[acc]), 0));
     }
-  } else if constexpr (GA) {
-    // ---------------- gathered A rows: warps 10..13 of both CTAs ----------------
+  } else if constexpr (GA || GB) {
+    // ---------------- gathered A rows (or B rows): warps 10..13 of both CTAs ----------------
     if (warp < kRelayWarp) {
-      gather_a_producer<BM2, C::STAGES, true>(p, s_toff, s_goff, pair, npairs, total_tiles, (int)rank, smem,
-                                              C::STAGE_BYTES, empty_bar, gath_bar, abort_flag);
+      if constexpr (GA)
+        gather_a_producer<BM2, C::STAGES, true>(p, s_toff, s_goff, pair, npairs, total_tiles, (int)rank, smem,
+                                                C::STAGE_BYTES, empty_bar, gath_bar, abort_flag);
+      else
+        gather_b_mn_producer<C::STAGES>(p, s_toff, s_goff, pair, npairs, total_tiles, (int)rank, smem, C::STAGE_BYTES,
+                                        C::A_BYTES, empty_bar, gath_bar, abort_flag);
     } else if (lane == 0) {
       gather_a_relay<BM2, C::STAGES, true>(p, s_toff, s_goff, pair, npairs, total_tiles, gath_bar, full_bar,
                                            abort_flag);
@@ -1139,12 +1222,12 @@ static cudaError_t launch_impl(const GemmProblem& q, const CUtensorMap& ta, cons
   return cudaGetLastError();
 }
 
-template <int EPI, bool F8 = false, bool GA = false>
+template <int EPI, bool F8 = false, bool GA = false, bool GB = false>
 static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp, int tiles,
                                     cudaStream_t stream, const CUtensorMap* tp = nullptr) {
   using PairCfg = PairCfgT<EPI>;
-  auto kern = gemm_tc_pair_kernel<EPI, F8, GA>;
-  constexpr int threads = GA ? kThreadsGA : kThreads;
+  auto kern = gemm_tc_pair_kernel<EPI, F8, GA, GB>;
+  constexpr int threads = GA || GB ? kThreadsGA : kThreads;
   static bool attr_set = false;
   static int max_pairs = 0;
   if (!attr_set) {
@@ -1186,6 +1269,11 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   const bool ga = q.a_gather != nullptr;
   if (ga && (q.epilogue != EPI_SWIGLU || q.num_groups == 0 || q.splits > 1 || !q.a_src || q.a_src_rows < 0))
     return cudaErrorInvalidValue;
+  // gathered B: K-grouped fp32 on CTA pairs, MN-major bf16 B
+  const bool gb = q.b_gather != nullptr;
+  if (gb && (q.k_groups == 0 || !pair || !q.b_mn_major || q.epilogue != EPI_F32 || f8 || ga || !q.b_src ||
+             !q.b_goff || q.b_src_rows < 0 || q.N % 8))
+    return cudaErrorInvalidValue;
   // MN-major B (bf16 / fp32 out, bf16 operands): group g's K rows x N columns; 64 x 64 boxes.
   // MN-major A: K-grouped only (1 CTA), K rows x M columns.
   if (q.b_mn_major && (f8 || ga || q.epilogue == EPI_SWIGLU || q.bn % 64 || q.K % BK ||
@@ -1211,7 +1299,9 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
     return cudaErrorInvalidValue;
   const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
   CUtensorMap ta, tb;
-  if (q.b_mn_major) {
+  if (gb) {
+    // B is gathered by the kernel: no B tensor map (the A map fills the slot below)
+  } else if (q.b_mn_major) {
     if (!make_tmap(&tb, q.B, q.b_rows_total, q.N, BK, false)) return cudaErrorInvalidValue;
   } else if (!make_tmap(&tb, q.B, q.b_rows_total, q.K, b_box, f8)) {
     return cudaErrorInvalidValue;
@@ -1221,6 +1311,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   else if (q.a_mn_major ? !make_tmap(&ta, q.A, q.mn_rows ? q.mn_rows : q.K, q.a_cols ? q.a_cols : q.M, BK, false)
                         : !make_tmap(&ta, q.A, q.a_rows ? q.a_rows : q.M, q.K, BM, f8))
     return cudaErrorInvalidValue;
+  if (gb) tb = ta;   // unused
 
   GemmParams gp;
   gp.M = q.M;
@@ -1249,6 +1340,11 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.a_ld_bytes = (long long)q.K * (f8 ? 1 : 2);
   gp.a_src_rows = q.a_src_rows;
   gp.b_mn = q.b_mn_major;
+  gp.b_gather = q.b_gather;
+  gp.b_src = static_cast<const uint8_t*>(q.b_src);
+  gp.b_goff = q.b_goff;
+  gp.b_ld_bytes = (long long)q.N * 2;
+  gp.b_src_rows = q.b_src_rows;
   gp.a_mn = q.a_mn_major;
   gp.a_off = q.a_off;
   gp.preact = q.preact;
@@ -1273,6 +1369,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
       return launch_pair_impl<EPI_BF16, true>(ta, tb, gp, tiles, stream);
     }
     if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU>(ta, tb, gp, tiles, stream);
+    if (gb) return launch_pair_impl<EPI_F32, false, false, true>(ta, tb, gp, tiles, stream);   // K-grouped, B gathered
     if (q.epilogue == EPI_F32) return launch_pair_impl<EPI_F32>(ta, tb, gp, tiles, stream);   // dense fp32 out
     if (q.epilogue == EPI_SWIGLU_BWD) {
       // the [u | g] rows as 128 x 32 boxes, 64-byte swizzle (the epilogue reads a row per lane)

@@ -59,6 +59,12 @@ struct GemmProblem {
   int preact_dense;
   void* out2;             // SwiGLU backward: H (bf16, ldo2 elements per row)
   int64_t ldo2;
+  const int* b_gather;    // non-NULL (K-grouped, MN-major B, CTA pairs): B is gathered by the kernel: group g's
+                          //   K row r is row b_gather[b_goff[g] + r] of b_src (b_src_rows x N bf16) while
+                          //   r < b_goff[g+1] - b_goff[g], zeros past it; B is then unused
+  const void* b_src;
+  const int* b_goff;      // device (k_groups + 1) row offsets of the groups in b_gather
+  int b_src_rows;
   int* status;
 };
 

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -140,6 +142,18 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp) {
   __syncthreads();
   const int before = warp > 0 ? s_warp[warp - 1] : 0;
   return before + x - v;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel attributes (the shared-memory opt-in) and occupancy belong to a device: launchers keep
+// what they set up per device, so that one process can drive several GPUs.
+// ---------------------------------------------------------------------------
+constexpr int kMaxDeviceSlots = 64;
+
+inline int device_slot() {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDeviceSlots) return -1;
+  return d;
 }
 
 // ---------------------------------------------------------------------------

@@ -1211,11 +1211,12 @@ static cudaError_t launch_impl(const GemmProblem& q, const CUtensorMap& ta, cons
                                const GemmParams& gp, int grid, cudaStream_t stream) {
   using C = GemmCfg<BN>;
   auto kern = gemm_tc_kernel<BN, EPI, F8, GA>;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<int> ready[kMaxDeviceSlots];
+  const int dev = device_slot();
+  if (dev < 0 || !ready[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (dev >= 0) ready[dev].store(1);
   }
   (void)q;
   launch_pdl(kern, grid, GA ? kThreadsGA : kThreads, C::SMEM_BYTES, stream, ta, tb, gp);
@@ -1228,9 +1229,10 @@ static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb
   using PairCfg = PairCfgT<EPI>;
   auto kern = gemm_tc_pair_kernel<EPI, F8, GA, GB>;
   constexpr int threads = GA || GB ? kThreadsGA : kThreads;
-  static bool attr_set = false;
-  static int max_pairs = 0;
-  if (!attr_set) {
+  static std::atomic<int> max_pairs_of[kMaxDeviceSlots];   // 0: not set up on that device yet
+  const int dev = device_slot();
+  int max_pairs = dev >= 0 ? max_pairs_of[dev].load() : 0;
+  if (max_pairs == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -1248,7 +1250,7 @@ static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb
     e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
     if (e != cudaSuccess) return e;
     max_pairs = n > 0 ? n : 1;
-    attr_set = true;
+    if (dev >= 0) max_pairs_of[dev].store(max_pairs);
   }
   int pairs = max_pairs;
   if (tiles > 0) pairs = std::min(pairs, tiles);

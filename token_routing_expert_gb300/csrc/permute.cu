@@ -307,12 +307,13 @@ cudaError_t launch_permute_cluster(const int32_t* idx, int R, int E, int32_t* co
   if (!permute_fits_cluster(R, E)) return cudaErrorInvalidValue;
   const int chunk = (R + kClusterCtas - 1) / kClusterCtas;
   const size_t smem = (size_t)(kClusterWarps + 1) * E * sizeof(int32_t);
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<int> ready[kMaxDeviceSlots];
+  const int dev = device_slot();
+  if (dev < 0 || !ready[dev].load()) {
     cudaError_t e = cudaFuncSetAttribute(perm_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)((kClusterWarps + 1) * 1024 * sizeof(int32_t)));
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (dev >= 0) ready[dev].store(1);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kClusterCtas);

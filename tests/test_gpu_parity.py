@@ -125,9 +125,12 @@ def test_permute_on_router_output(name):
     _check_permute(idx, spec.num_experts, spec.top_k)
 
 
+# the permutation runs as one cluster launch up to 16,384 assignments and as three kernels beyond:
+# both sides of the boundary, and a last chunk of one assignment
 @pytest.mark.parametrize("T,k,E,kind", [(40000, 8, 896, "uniform"), (9000, 8, 64, "one_hot"),
                                          (5000, 4, 1000, "few"), (1, 1, 1, "uniform"), (3, 2, 1024, "uniform"),
-                                         (33000, 8, 256, "skew")])
+                                         (33000, 8, 256, "skew"), (2048, 8, 64, "skew"), (16385, 1, 64, "skew"),
+                                         (16384, 1, 1024, "uniform"), (2049, 8, 1000, "few")])
 def test_permute_patterns(T, k, E, kind):
     g = np.random.default_rng(T + E)
     if kind == "uniform":

@@ -329,3 +329,26 @@ def test_staged_forward_matches_and_records_every_stage(name):
     # each with a split-K reduce when split, and a deep split-K router the sum of its partial
     # logits (top-k adds up to 4 slices itself)
     assert 6 <= n <= 10 if not spec.latent_dim else 8 <= n <= 14
+
+
+@pytest.mark.parametrize("name", ["latent_decode_small", "pair_tiles"])
+def test_layer_forward_captures_into_a_cuda_graph(name):
+    """The layer forward enqueues nothing that breaks stream capture (no host synchronisation, no
+    allocation): a captured graph replays to the same bits as the direct call."""
+    spec, inp, cfg, wts = setup(name)
+    x = inp["x"].cuda()
+    ws = native.workspace(cfg, spec.T)
+    out = torch.empty((spec.T, spec.d_model), dtype=torch.bfloat16, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        native.moe_layer_forward(cfg, wts, x, ws, out=out)
+    torch.cuda.synchronize()
+    want = out.clone()
+    out.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        native.moe_layer_forward(cfg, wts, x, ws, out=out)
+    g.replay()
+    torch.cuda.synchronize()
+    expect_ok()
+    assert torch.equal(out, want)

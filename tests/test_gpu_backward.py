@@ -240,6 +240,9 @@ LAYER_CASES = {
                                  latent_dim=192, gating="topk_softmax", seed=92), True),
     "latent_pair_tiles": (WorkloadSpec("latent_pair_tiles", T=1600, d_model=384, num_experts=4, top_k=2,
                                        hidden_size=128, latent_dim=256, gating="softmax", seed=93), False),
+    # dropped assignments: their rows are padding slots, their weights get no gradient from the experts
+    "capacity": (WorkloadSpec("capacity_layer", T=500, d_model=256, num_experts=8, top_k=2, hidden_size=128,
+                              gating="sigmoid", skew=True, capacity_factor=0.75, seed=94), False),
 }
 
 
@@ -306,7 +309,23 @@ def test_layer_backward(name):
         close(grads["drms_weight"].double().cpu().numpy(), want_dg, "dgamma")
     want_dy, want_dwts = ref.combine_backward(dz_np, y_np, sc_np, w_np)
     xr_np = xr.double().cpu().numpy()
-    want_dxr, want_grads = ref.experts_backward(oc, xr_np, perm, ow.expert, want_dy)
+    if spec.capacity_factor:
+        # capacity slots: padding slots (gather -1) are no rows; the oracle's experts backward is the
+        # dropless one, so it runs on each expert's live slots
+        want_dxr, want_grads = np.zeros_like(xr_np), {}
+        for e in range(E):
+            lo, hi = int(off[e]), int(off[e + 1])
+            live = [q for q in range(lo, hi) if ga_np[q] >= 0]
+            w_up, w_gate, w_out = ow.expert(e)
+            if not live:
+                want_grads[e] = (np.zeros_like(w_up), np.zeros_like(w_gate), np.zeros_like(w_out))
+                continue
+            d_rows, dwu, dwg, dwo_e, _ = ref.swiglu_mlp_backward(xr_np[ga_np[live]], w_up, w_gate, w_out,
+                                                                  want_dy[live])
+            np.add.at(want_dxr, ga_np[live], d_rows)
+            want_grads[e] = (dwu, dwg, dwo_e)
+    else:
+        want_dxr, want_grads = ref.experts_backward(oc, xr_np, perm, ow.expert, want_dy)
     for e in range(E):
         close(grads["dw_up_gate"][e].double().cpu().numpy(), np.concatenate(want_grads[e][:2]), f"dW_up_gate[{e}]")
         close(grads["dw_out"][e].double().cpu().numpy(), want_grads[e][2], f"dW_out[{e}]")

@@ -243,6 +243,13 @@ LAYER_CASES = {
     # dropped assignments: their rows are padding slots, their weights get no gradient from the experts
     "capacity": (WorkloadSpec("capacity_layer", T=500, d_model=256, num_experts=8, top_k=2, hidden_size=128,
                               gating="sigmoid", skew=True, capacity_factor=0.75, seed=94), False),
+    # degenerate shapes: one token (most experts empty), one expert, every expert chosen by every token
+    "one_token": (WorkloadSpec("one_token_bwd", T=1, d_model=256, num_experts=8, top_k=2, hidden_size=128,
+                               gating="softmax", normalize_expert_weights=1.0, seed=95), False),
+    "single_expert": (WorkloadSpec("single_expert_bwd", T=130, d_model=128, num_experts=1, top_k=1,
+                                   hidden_size=64, gating="sigmoid", seed=96), False),
+    "all_experts": (WorkloadSpec("all_experts_bwd", T=150, d_model=192, num_experts=6, top_k=6, hidden_size=64,
+                                 gating="topk_softmax", seed=97), False),
 }
 
 

@@ -15,6 +15,10 @@ SPECS = [
                  normalize_expert_weights=1.0, seed=41),
     WorkloadSpec("host_pair_latent", T=2000, d_model=768, num_experts=4, top_k=2, hidden_size=192, latent_dim=256,
                  gating="sigmoid", seed=42),
+    WorkloadSpec("host_capacity", T=700, d_model=256, num_experts=8, top_k=2, hidden_size=128, gating="sigmoid",
+                 skew=True, capacity_factor=1.0, seed=43),
+    WorkloadSpec("host_fp8", T=900, d_model=512, num_experts=4, top_k=2, hidden_size=256, gating="topk_softmax",
+                 expert_fp8=True, seed=44),
 ]
 
 
@@ -24,6 +28,8 @@ def test_host_batches_match_device_forward(spec, n_batches):
     inp = generate(spec)
     cfg = native.config_from_spec(spec)
     wts = native.DeviceWeights.from_inputs(inp)
+    if spec.expert_fp8:
+        wts.quantize_experts_fp8()
     g = np.random.default_rng(spec.seed + n_batches)
     xs = [torch.from_numpy(g.standard_normal((spec.T, spec.d_model), dtype=np.float32)).to(torch.bfloat16).pin_memory()
           for _ in range(n_batches)]

@@ -749,3 +749,71 @@ def layer_forward_fp8(cfg: OracleConfig, x: np.ndarray, wts: OracleWeights,
     y = expert_outputs_fp8(cfg, x_routed, perm, wts.expert)
     z = combine(y, perm.scatter_pos, r.weights)
     return restore_routed_output(cfg, z, wts.w_up_latent, wts.rms_weight)
+
+
+# --------------------------------------------------------------------------
+# MXFP8 experts  [Olmo-core 3, §"Rowwise FP8 и MXFP8": the MXFP8 path of the
+# experts].  The page names the format only; the reading is the OCP
+# microscaling (MX) format: blocks of 32 consecutive values along the
+# contraction share one power-of-two scale X = 2^(floor(log2 amax) - 8)
+# (8 = the largest e4m3 exponent, 448 = 1.75 * 2^8), stored as its biased
+# exponent (E8M0, X = 2^(e - 127)); each value is rounded to e4m3 as v / X
+# (exact: X is a power of two), nearest, ties to even, saturating at 448.
+# An all-zero block takes e = 0.  The GEMMs accumulate exactly and apply the
+# two blocks' scales to each 32-wide partial product.
+# --------------------------------------------------------------------------
+
+MX_BLOCK = 32
+
+
+def quantize_mx_e4m3(x: np.ndarray):
+    """(codes as float64 values (rows, cols), scale exponents e (rows, cols / 32) as int):
+    x[r, c] ~ code[r, c] * 2^(e[r, c // 32] - 127)."""
+    x = np.asarray(x, np.float64)
+    rows, cols = x.shape
+    assert cols % MX_BLOCK == 0
+    blocks = x.reshape(rows, cols // MX_BLOCK, MX_BLOCK)
+    amax = np.abs(blocks).max(axis=2)
+    e = np.zeros(amax.shape, np.int64)
+    nz = amax > 0
+    e[nz] = np.floor(np.log2(amax[nz])).astype(np.int64) - 8 + 127
+    e = np.clip(e, 0, 254)
+    scale = np.ldexp(1.0, (e - 127).astype(np.int64))
+    codes = round_e4m3(blocks / scale[:, :, None]).reshape(rows, cols)
+    return codes, e
+
+
+def dequantize_mx(codes: np.ndarray, e: np.ndarray) -> np.ndarray:
+    rows, cols = codes.shape
+    scale = np.ldexp(1.0, (np.asarray(e) - 127).astype(np.int64))
+    return (codes.reshape(rows, cols // MX_BLOCK, MX_BLOCK) * scale[:, :, None]).reshape(rows, cols)
+
+
+def expert_outputs_mxfp8(cfg: OracleConfig, x_routed: np.ndarray, perm: Permutation, expert: ExpertFn) -> np.ndarray:
+    """Experts on MXFP8 operands: x rows and weight rows quantised in 32-wide blocks along the
+    contraction, H rounded to bf16 and quantised the same way before the down projection."""
+    xd = dequantize_mx(*quantize_mx_e4m3(np.asarray(x_routed, np.float64)))
+    y = np.zeros((perm.gather_token.size, x_routed.shape[1]), np.float64)
+    for e in range(cfg.num_experts):
+        lo, hi = int(perm.offsets[e]), int(perm.offsets[e + 1])
+        if hi == lo:
+            continue
+        wu, wg, wo = (dequantize_mx(*quantize_mx_e4m3(np.asarray(a, np.float64))) for a in expert(e))
+        rows = xd[perm.gather_token[lo:hi]]
+        h = round_bf16(silu(rows @ wg.T) * (rows @ wu.T))
+        y[lo:hi] = dequantize_mx(*quantize_mx_e4m3(h)) @ wo.T
+    return y
+
+
+def layer_forward_mxfp8(cfg: OracleConfig, x: np.ndarray, wts: OracleWeights,
+                        forced_idx: Optional[np.ndarray] = None) -> np.ndarray:
+    """The layer forward with the experts on MXFP8 operands (bf16 x_routed as input)."""
+    x = np.asarray(x, np.float64)
+    x_routed = prepare_routed_input(cfg, x, wts.w_down_latent)
+    if cfg.is_latent:
+        x_routed = round_bf16(x_routed)   # the experts' input is stored in bf16
+    r = route(cfg, x, wts.w_router, wts.b_router, wts.score_bias, forced_idx)
+    perm = permute(r.idx, cfg.num_experts)
+    y = expert_outputs_mxfp8(cfg, x_routed, perm, wts.expert)
+    z = combine(y, perm.scatter_pos, r.weights)
+    return restore_routed_output(cfg, z, wts.w_up_latent, wts.rms_weight)

@@ -43,3 +43,62 @@ def test_fp8_ambiguity_band_flags_rows_at_a_rounding_midpoint():
                      [0.5, 1.0 + 2.0 ** -7, -0.25],     # amax exactly representable
                      [0.5, -(1.0 + 2.0 ** -8), 0.25]])  # the sign does not matter
     np.testing.assert_array_equal(_amax_ambiguous(rows, 1e-5), [True, False, True])
+
+
+def test_mx_quantiser_closed_forms():
+    """MX blocks: the scale exponent is floor(log2 amax) - 8 + 127, codes = e4m3(v / 2^(e-127)); a block
+    whose values are e4m3 values times a power of two comes back exactly, an all-zero block has e = 0."""
+    g = np.random.default_rng(3)
+    codes = g.choice(ref._E4M3[ref._E4M3 <= 448], size=(4, 64)) * g.choice([-1.0, 1.0], size=(4, 64))
+    codes[:, 0] = 448.0                                   # block amax 448 = 1.75 * 2^8: floor(log2) = 8
+    codes[:, 32] = -448.0
+    x = codes * 2.0 ** np.array([-20, -3, 0, 7])[:, None]
+    q, e = ref.quantize_mx_e4m3(x)
+    np.testing.assert_array_equal(e, np.array([[107, 107], [124, 124], [127, 127], [134, 134]]))
+    np.testing.assert_array_equal(ref.dequantize_mx(q, e), x)
+    z = np.zeros((2, 32))
+    qz, ez = ref.quantize_mx_e4m3(z)
+    assert (qz == 0).all() and (ez == 0).all()
+
+
+def test_mx_quantiser_saturates_and_bounds_the_error():
+    """amax / X lies in [256, 512): values above 448 saturate; every other value is within half an
+    e4m3 step of v / X (relative 2^-4), and the scale is a power of two chosen per 32-value block."""
+    g = np.random.default_rng(4)
+    x = g.standard_normal((64, 256)) * np.exp(g.uniform(-8, 8, size=(64, 1)))
+    q, e = ref.quantize_mx_e4m3(x)
+    d = ref.dequantize_mx(q, e)
+    blocks = x.reshape(64, 8, 32)
+    scale = 2.0 ** (e - 127)
+    amax = np.abs(blocks).max(axis=2)
+    assert ((amax / scale >= 256) & (amax / scale < 512)).all()
+    v = blocks / scale[:, :, None]
+    sat = np.abs(v) > 448
+    assert (np.abs(q.reshape(64, 8, 32))[sat] == 448).all()
+    err = np.abs(d.reshape(64, 8, 32) - blocks)[~sat] / np.maximum(np.abs(blocks[~sat]), 2.0 ** -6 * scale.repeat(32).reshape(64, 8, 32)[~sat])
+    assert err.max() <= 2.0 ** -4 + 1e-12
+    # block-wise: each 32-wide block of a row has its own exponent
+    x2 = np.concatenate([np.full((1, 32), 1.0), np.full((1, 32), 1000.0)], axis=1)
+    _, e2 = ref.quantize_mx_e4m3(x2)
+    np.testing.assert_array_equal(e2, [[0 - 8 + 127, 9 - 8 + 127]])
+
+
+def test_mx_experts_reduce_to_the_exact_experts_on_representable_inputs():
+    """When x, the weights and H are all MX-representable, the MXFP8 experts equal the exact ones
+    (H rounded to bf16 and re-quantised in between)."""
+    cfg = ref.OracleConfig(d_model=64, num_experts=2, top_k=1, hidden_size=32)
+    g = np.random.default_rng(5)
+    pick = lambda shape: g.choice([-2.0, -1.0, -0.5, 0.5, 1.0, 2.0], size=shape)   # noqa: E731
+    x = pick((6, 64))
+    w = [(pick((32, 64)) / 8, pick((32, 64)) / 8, pick((64, 32)) / 8) for _ in range(2)]
+    perm = ref.permute(np.array([[0], [1], [0], [1], [1], [0]]), 2)
+    got = ref.expert_outputs_mxfp8(cfg, x, perm, lambda e: w[e])
+    h_exact = {}
+    want = np.zeros_like(got)
+    for e in range(2):
+        lo, hi = int(perm.offsets[e]), int(perm.offsets[e + 1])
+        rows = x[perm.gather_token[lo:hi]]
+        h = ref.round_bf16(ref.silu(rows @ w[e][1].T) * (rows @ w[e][0].T))
+        want[lo:hi] = ref.dequantize_mx(*ref.quantize_mx_e4m3(h)) @ w[e][2].T
+        h_exact[e] = h
+    np.testing.assert_allclose(got, want, rtol=0, atol=0)

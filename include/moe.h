@@ -48,6 +48,14 @@ enum {
   MOE_ERR_NO_DEVICE = 7    /* no usable sm_103 device for this call */
 };
 
+/* moe_config_t.expert_fp8: operands of the experts' GEMMs.  MXFP8 needs d_model (latent_dim when
+ * latent) and hidden_size to be multiples of 128, and no kept pre-activations. */
+enum {
+  MOE_EXPERT_BF16 = 0,
+  MOE_EXPERT_FP8_ROWWISE = 1,   /* e4m3 codes with one fp32 scale per row */
+  MOE_EXPERT_MXFP8 = 2          /* e4m3 codes with an E8M0 scale per 32 values of a row */
+};
+
 /* Gating functions, section "Маршрутизация: как роутер выбирает экспертов". */
 typedef enum {
   MOE_GATING_SOFTMAX = 0,      /* scores = softmax(logits) over experts; weights gathered from scores */
@@ -79,8 +87,9 @@ typedef struct {
   int32_t activation;              /* 0 = swiglu (the only expert activation supported) */
   float capacity_factor;           /* > 0: capacity-limited experts (section "Ёмкость эксперта и
                                       переполнение"); 0 = dropless */
-  int32_t expert_fp8;              /* 1: the experts' GEMMs run on rowwise e4m3 operands (section
-                                      "Rowwise FP8 и MXFP8"; needs the *_fp8 weights below); 0 = bf16 */
+  int32_t expert_fp8;              /* the experts' GEMM operands (section "Rowwise FP8 и MXFP8"):
+                                      MOE_EXPERT_BF16, MOE_EXPERT_FP8_ROWWISE or MOE_EXPERT_MXFP8;
+                                      the e4m3 modes need the *_fp8 weights below */
 } moe_config_t;
 
 /*
@@ -100,6 +109,10 @@ typedef struct {
   const float* w_up_gate_scale; /* (E * 2h) fp32 row scales */
   const void* w_out_fp8;        /* (E, L', h) e4m3 codes */
   const float* w_out_scale;     /* (E * L') fp32 row scales */
+  /* MOE_EXPERT_MXFP8 only: the *_fp8 codes above are moe_quantize_mxfp8 codes, and these are their
+   * E8M0 block scales, scale_ld = (cols / 32 + 15) / 16 * 16 bytes per row */
+  const void* w_up_gate_mx_scale; /* (E * 2h, scale_ld(L')) bytes */
+  const void* w_out_mx_scale;     /* (E * L', scale_ld(h)) bytes */
 } moe_weights_t;
 
 /* ---- host-only functions (no device, no stream) ------------------------- */
@@ -477,6 +490,18 @@ int moe_workspace_layout(const moe_config_t* cfg, int64_t T, int64_t offsets_out
  */
 int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* idx, int64_t T, int32_t* counts, int32_t* offsets,
                         int32_t* gather_idx, int32_t* scatter_idx, moe_stream_t stream);
+
+/*
+ * MXFP8 quantisation (section "Rowwise FP8 и MXFP8", read as the OCP microscaling
+ * format): each block of 32 consecutive values of a row shares the scale
+ * 2^(e - 127), e = floor(log2 amax) - 8 + 127 clamped to [0, 254] (0 for an
+ * all-zero block), stored as the byte e (E8M0); codes[r, c] = e4m3(x[r, c] /
+ * 2^(e - 127)), nearest-even, saturating at +-448.
+ *   x device (rows, cols) bf16, cols a multiple of 32; codes device (rows, cols)
+ *   bytes out; scales device (rows, scale_ld) bytes out, cols / 32 used per row.
+ */
+int moe_quantize_mxfp8(const void* x, int64_t rows, int32_t cols, void* codes, void* scales, int32_t scale_ld,
+                       moe_stream_t stream);
 
 /* Synchronises `stream`, then returns (and clears, if `clear`) the device
  * status word of the current device in *device_status. */

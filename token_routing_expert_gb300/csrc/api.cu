@@ -47,7 +47,9 @@ struct Plan {
   int64_t cap;        // slots per expert (capacity mode)
   int64_t rows;       // rows of the permuted order: R, or E * cap
   size_t gdense, sdense, odense;   // capacity mode: the dense stable permutation before slotting
-  size_t xq, xs, xpq, xps, hq, hs;  // rowwise e4m3 experts: codes and scales of x_routed, its rows, H
+  size_t xq, xs, xpq, xps, hq, hs;  // e4m3 experts: codes and scales of x_routed, its rows, H
+  bool mx;            // MXFP8 experts (block scales); else rowwise e4m3 when expert_fp8
+  int64_t sx_ld, sh_ld;   // MXFP8: bytes of block scales per row of x_routed / of H
   int D, E, k, h, L, Lr;   // Lr: routed dim (L or D)
   bool latent;
   int router_bn, n_router_tiles;
@@ -71,7 +73,17 @@ int64_t capacity_of(const moe_config_t* c, int64_t T) {
 // and gather their rows in grouped GEMM 1, which outweighs their padding down to ~200 rows per
 // group (OlmoE shape at T = 2,048, 256 rows per expert: 0.279 -> 0.262 ms; latent prefill, 292:
 // 5.08 -> 4.92 ms).  p.rows and p.E must be set.
-int use_pair_tiles(const Plan& p) { return p.rows >= (int64_t)192 * p.E ? 1 : 0; }
+// Bytes of MXFP8 block scales per row of `cols` values: cols / 32, rounded up to 16.
+int64_t mx_scale_ld(int64_t cols) { return (cols / 32 + 15) / 16 * 16; }
+
+// The quantised expert weights the config's expert_fp8 mode reads.
+bool fp8_weights_present(const moe_config_t* c, const moe_weights_t* w) {
+  if (!w->w_up_gate_fp8 || !w->w_out_fp8) return false;
+  return c->expert_fp8 == MOE_EXPERT_MXFP8 ? (w->w_up_gate_mx_scale && w->w_out_mx_scale)
+                                           : (w->w_up_gate_scale && w->w_out_scale);
+}
+
+int use_pair_tiles(const Plan& p) { return !p.mx && p.rows >= (int64_t)192 * p.E ? 1 : 0; }
 
 void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->T = T;
@@ -86,6 +98,9 @@ void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->capacity = c->capacity_factor > 0.f;
   p->cap = capacity_of(c, T);
   p->rows = p->capacity ? (int64_t)p->E * p->cap : p->R;
+  p->mx = c->expert_fp8 == MOE_EXPERT_MXFP8;
+  p->sx_ld = mx_scale_ld(p->Lr);
+  p->sh_ld = mx_scale_ld(p->h);
   const int mt = (int)((T + 127) / 128);
   p->router_bn = pick_bn_f32(p->E);
   p->n_router_tiles = (p->E + p->router_bn - 1) / p->router_bn;
@@ -126,7 +141,14 @@ void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->H = take((size_t)p->rows * p->h * 2);
   p->Y = take((size_t)p->rows * p->Lr * 2);
   p->zn = p->latent ? take((size_t)T * p->L * 2) : (size_t)-1;
-  if (c->expert_fp8) {
+  if (p->mx) {
+    p->xq = take((size_t)T * p->Lr);
+    p->xs = take((size_t)T * p->sx_ld);
+    p->xpq = take((size_t)p->rows * p->Lr);
+    p->xps = take((size_t)p->rows * p->sx_ld);
+    p->hq = take((size_t)p->rows * p->h);
+    p->hs = take((size_t)p->rows * p->sh_ld);
+  } else if (c->expert_fp8) {
     p->xq = take((size_t)T * p->Lr);
     p->xs = take((size_t)T * 4);
     p->xpq = gathered ? (size_t)-1 : take((size_t)p->rows * p->Lr);
@@ -156,7 +178,11 @@ int check_config(const moe_config_t* c) {
   if (c->activation != 0) return MOE_ERR_UNSUPPORTED;
   if (c->d_model % 64 || c->hidden_size % 64 || (c->latent_dim > 0 && c->latent_dim % 64)) return MOE_ERR_UNSUPPORTED;
   if (c->num_experts > 1024 || c->top_k > 32) return MOE_ERR_UNSUPPORTED;
-  if (c->expert_fp8 != 0 && c->expert_fp8 != 1) return MOE_ERR_INVALID_ARG;
+  if (c->expert_fp8 < 0 || c->expert_fp8 > MOE_EXPERT_MXFP8) return MOE_ERR_INVALID_ARG;
+  // MXFP8 experts contract 128-value k-tiles (four 32-value scale blocks) over d_model / latent_dim and hidden_size
+  if (c->expert_fp8 == MOE_EXPERT_MXFP8 &&
+      ((c->latent_dim > 0 ? c->latent_dim : c->d_model) % 128 || c->hidden_size % 128))
+    return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -337,6 +363,81 @@ int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* x
   return MOE_OK;
 }
 
+// The experts on MXFP8 operands: quantise x_routed in 32-value blocks, copy the code rows and
+// their scales in permuted order, GEMM 1 (block-scaled MMAs, SwiGLU epilogue) -> H bf16, quantise
+// H the same way, GEMM 2 -> Y bf16.
+int run_experts_mx(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
+                   const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
+                   cudaEvent_t* ev, bool tiles_ready) {
+  (void)c;
+  int32_t* tile_off = at<int32_t>(ws, p.tile_off);
+  void* H = at<void>(ws, p.H);
+  void* xq = at<void>(ws, p.xq);
+  void* xs = at<void>(ws, p.xs);
+  void* hq = at<void>(ws, p.hq);
+  void* hs = at<void>(ws, p.hs);
+  int s = tiles_ready ? MOE_OK : cuda_status(launch_tile_table(offsets, p.E, 128, tile_off, st));
+  if (s == MOE_OK) s = cuda_status(launch_quantize_mx_e4m3(xr, p.T, p.Lr, xq, xs, (int)p.sx_ld, st));
+  if (s == MOE_OK)
+    s = cuda_status(launch_gather_rows_mx(xq, xs, gather, (int)p.rows, (int)p.T, p.Lr, (int)p.sx_ld,
+                                          at<void>(ws, p.xpq), at<void>(ws, p.xps), p.capacity ? 1 : 0, status, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 5, st);
+  GemmProblem g1{};
+  g1.A = at<void>(ws, p.xpq);
+  g1.B = w->w_up_gate_fp8;
+  g1.b_rows_total = (int64_t)p.E * 2 * p.h;
+  g1.M = (int)p.rows;
+  g1.N = p.h;
+  g1.K = p.Lr;
+  g1.num_groups = p.E;
+  g1.group_off = offsets;
+  g1.tile_off = tile_off;
+  g1.b_rows_per_group = 2 * p.h;
+  g1.b_gate_offset = p.h;
+  g1.epilogue = EPI_SWIGLU;
+  g1.bn = 256;
+  g1.splits = 1;
+  g1.mx = 1;
+  g1.a_mx_scale = at<void>(ws, p.xps);
+  g1.a_mx_ld = p.sx_ld;
+  g1.b_mx_scale = w->w_up_gate_mx_scale;
+  g1.b_mx_ld = p.sx_ld;
+  g1.out = H;
+  g1.ldo = p.h;
+  g1.status = status;
+  s = cuda_status(launch_gemm(g1, st));
+  if (s == MOE_OK) s = cuda_status(launch_quantize_mx_e4m3(H, p.rows, p.h, hq, hs, (int)p.sh_ld, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 6, st);
+  GemmProblem g2{};
+  g2.A = hq;
+  g2.B = w->w_out_fp8;
+  g2.b_rows_total = (int64_t)p.E * p.Lr;
+  g2.M = (int)p.rows;
+  g2.N = p.Lr;
+  g2.K = p.h;
+  g2.num_groups = p.E;
+  g2.group_off = offsets;
+  g2.tile_off = tile_off;
+  g2.b_rows_per_group = p.Lr;
+  g2.epilogue = EPI_BF16;
+  g2.bn = 256;
+  g2.splits = 1;
+  g2.mx = 1;
+  g2.a_mx_scale = hs;
+  g2.a_mx_ld = p.sh_ld;
+  g2.b_mx_scale = w->w_out_mx_scale;
+  g2.b_mx_ld = p.sh_ld;
+  g2.out = y;
+  g2.ldo = p.Lr;
+  g2.status = status;
+  s = cuda_status(launch_gemm(g2, st));
+  if (s != MOE_OK) return s;
+  mark(ev, 7, st);
+  return MOE_OK;
+}
+
 // tiles_ready: the tile table in the workspace was already written (by run_permute).
 // preact (optional): grouped GEMM 1 also stores the pre-activations [u | g] there, rows x 2h bf16.
 int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
@@ -344,6 +445,10 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
                 cudaEvent_t* ev = nullptr, bool tiles_ready = false, void* preact = nullptr) {
   int32_t* tile_off = at<int32_t>(ws, p.tile_off);
   void* H = at<void>(ws, p.H);
+  if (p.mx) {
+    if (preact) return MOE_ERR_UNSUPPORTED;
+    return run_experts_mx(c, w, xr, gather, offsets, p, y, ws, status, st, ev, tiles_ready);
+  }
   if (c->expert_fp8)
     return run_experts_fp8(c, w, xr, gather, offsets, p, y, ws, status, st, ev, tiles_ready, preact);
   // large groups run on CTA pairs with 256-row tiles; small ones keep 128-row tiles,
@@ -759,7 +864,7 @@ int moe_grouped_swiglu_preact(const moe_config_t* c, const moe_weights_t* w, con
   if (s != MOE_OK) return s;
   if (T == 0) return MOE_OK;
   if (!w || !w->w_up_gate || !w->w_out || !x_routed || !gather_idx || !offsets || !y) return MOE_ERR_INVALID_ARG;
-  if (c->expert_fp8 && (!w->w_up_gate_fp8 || !w->w_up_gate_scale || !w->w_out_fp8 || !w->w_out_scale))
+  if (c->expert_fp8 && !fp8_weights_present(c, w))
     return MOE_ERR_INVALID_ARG;
   int* status = status_ptr();
   if (!status) return MOE_ERR_NO_DEVICE;
@@ -823,7 +928,7 @@ int layer_forward(const moe_config_t* c, const moe_weights_t* w, const void* x, 
   if (!w || !x || !out || !w->w_router || !w->w_up_gate || !w->w_out) return MOE_ERR_INVALID_ARG;
   if (p.latent && (!w->w_down_latent || !w->w_up_latent)) return MOE_ERR_INVALID_ARG;
   if ((c->router_bias && !w->b_router) || (c->has_score_bias && !w->score_bias)) return MOE_ERR_INVALID_ARG;
-  if (c->expert_fp8 && (!w->w_up_gate_fp8 || !w->w_up_gate_scale || !w->w_out_fp8 || !w->w_out_scale))
+  if (c->expert_fp8 && !fp8_weights_present(c, w))
     return MOE_ERR_INVALID_ARG;
   if (x == out) return MOE_ERR_INVALID_ARG;
   if (preact && c->hidden_size % 32) return MOE_ERR_UNSUPPORTED;
@@ -1409,6 +1514,14 @@ int moe_check_wait_timeout(int32_t limit_ms, int32_t* waited_ms, moe_stream_t st
     return MOE_ERR_CUDA;
   *waited_ms = res[1];
   return (res[0] == 1 && after == MOE_ERR_TIMEOUT) ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_quantize_mxfp8(const void* x, int64_t rows, int32_t cols, void* codes, void* scales, int32_t scale_ld,
+                       moe_stream_t stream) {
+  if (rows < 0 || cols <= 0 || cols % 32 || scale_ld < cols / 32) return MOE_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_OK;
+  if (!x || !codes || !scales) return MOE_ERR_INVALID_ARG;
+  return cuda_status(launch_quantize_mx_e4m3(x, rows, cols, codes, scales, scale_ld, (cudaStream_t)stream));
 }
 
 int moe_get_status(moe_stream_t stream, int32_t* device_status, int clear) {

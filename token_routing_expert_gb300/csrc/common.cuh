@@ -346,6 +346,37 @@ __device__ __forceinline__ void umma_e4m3_pair(uint32_t d_tmem, uint64_t a_desc,
       : "memory");
 }
 
+// D[tmem] (+)= A * B^T with e4m3 A and B scaled per 32-element K block (kind::mxf8f6f4.block_scale):
+// the block scales are UE8M0 bytes in tensor memory at sa_tmem (row i of A: lane i, column
+// sa_tmem + i / 32) and sb_tmem (row n of B: column sb_tmem + n / 32, lane n mod 32 of every lane
+// quadrant), byte 0 of each word.  One CTA, M = 128, K = 32 per instruction.
+__device__ __forceinline__ void umma_mx_e4m3(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sa_tmem, uint32_t sb_tmem, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sa_tmem), "r"(sb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4: e4m3 A and B (format 0), both K-major, M x N, UE8M0
+// scales (bit 23; the form with bit 23 clear is not valid for this kind).
+__host__ __device__ constexpr uint32_t umma_idesc_mx_e4m3(int M, int N) {
+  return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+
+// 32 lanes x 1 or 8 consecutive 32-bit columns from registers: thread i writes lane (base + i).
+__device__ __forceinline__ void tmem_st_32x32b_x1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Instruction descriptor, kind::f8f6f4: e4m3 A and B (format 0), f32 D, both K-major, M x N.
 __host__ __device__ constexpr uint32_t umma_idesc_e4m3_f32(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);

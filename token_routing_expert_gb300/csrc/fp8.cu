@@ -61,6 +61,61 @@ cudaError_t launch_quantize_rowwise_e4m3(const void* x, long long rows, int cols
   return cudaGetLastError();
 }
 
+// MXFP8 (OCP microscaling) quantisation, §"Rowwise FP8 и MXFP8": each block of 32 consecutive
+// values of a row shares the scale 2^(e - 127), e = floor(log2 amax) - 8 + 127 clamped to [0, 254]
+// (e = 0 for an all-zero block), stored as the byte e (E8M0); a value's code is e4m3(v * 2^(127 - e)),
+// the product exact in float32 (a power of two), rounded to nearest-even and saturating at +-448.
+// A thread per block: 64 bytes of bf16 in, 32 code bytes and one scale byte out.
+__global__ void __launch_bounds__(256) quantize_mx_e4m3_kernel(const uint4* __restrict__ x, long long rows, int nb,
+                                                                uint4* __restrict__ q, uint8_t* __restrict__ scales,
+                                                                int scale_ld) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
+  const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= rows * nb) return;
+  const long long r = b / nb;
+  const int kb = (int)(b - r * nb);
+  uint4 v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = x[b * 4 + i];
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+  }
+  const int eb = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+  const int e = amax > 0.f ? max(0, eb - 8) : 0;
+  const float mul = __uint_as_float((uint32_t)(254 - e) << 23);   // 2^(127 - e)
+  uint32_t out[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float2 lo = make_float2(bf16_lo(w[2 * h]) * mul, bf16_hi(w[2 * h]) * mul);
+      const float2 hi = make_float2(bf16_lo(w[2 * h + 1]) * mul, bf16_hi(w[2 * h + 1]) * mul);
+      const uint32_t a = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
+      const uint32_t c = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
+      out[2 * i + h] = (a & 0xFFFFu) | (c << 16);
+    }
+  }
+  q[b * 2] = make_uint4(out[0], out[1], out[2], out[3]);
+  q[b * 2 + 1] = make_uint4(out[4], out[5], out[6], out[7]);
+  scales[r * scale_ld + kb] = (uint8_t)e;
+}
+
+cudaError_t launch_quantize_mx_e4m3(const void* x, long long rows, int cols, void* q, void* scales, int scale_ld,
+                                    cudaStream_t st) {
+  if (rows <= 0) return cudaSuccess;
+  if (cols % 32 || scale_ld < cols / 32) return cudaErrorInvalidValue;
+  const long long n = rows * (cols / 32);
+  launch_pdl(quantize_mx_e4m3_kernel, (unsigned)((n + 255) / 256), 256, 0, st, static_cast<const uint4*>(x), rows,
+             cols / 32, static_cast<uint4*>(q), static_cast<uint8_t*>(scales), scale_ld);
+  return cudaGetLastError();
+}
+
 // dst[p] = src[gather_idx[p]] for e4m3 rows (row_bytes, a multiple of 16) and their scales;
 // a padding slot (-1, capacity mode) gets a zero row and scale 1.
 __global__ void __launch_bounds__(256) gather_rows_e4m3_kernel(const uint4* __restrict__ src,
@@ -106,6 +161,56 @@ cudaError_t launch_gather_rows_e4m3(const void* src, const float* src_scale, con
   launch_pdl(gather_rows_e4m3_kernel, (R + 7) / 8, 256, 0, st, static_cast<const uint4*>(src), src_scale, gather_idx, R, T,
                                                        row_bytes / 16, static_cast<uint4*>(dst), dst_scale,
                                                        allow_padding, status);
+  return cudaGetLastError();
+}
+
+// dst[p] = src[gather_idx[p]] for MXFP8 rows: the codes (vec 16-byte words) and the block scales
+// (svec 32-bit words); a padding slot (-1, capacity mode) gets zero codes and scales 2^0 (byte 127).
+__global__ void __launch_bounds__(256) gather_rows_mx_kernel(const uint4* __restrict__ src,
+                                                             const uint32_t* __restrict__ src_scale,
+                                                             const int32_t* __restrict__ gather_idx, int R, int T,
+                                                             int vec, int svec, uint4* __restrict__ dst,
+                                                             uint32_t* __restrict__ dst_scale, int allow_padding,
+                                                             int* status) {
+  pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (p >= R) return;
+  const int t = gather_idx[p];
+  uint4* d = dst + p * vec;
+  uint32_t* ds = dst_scale + p * svec;
+  if (t < 0 || t >= T) {
+    if (allow_padding && t == -1) {
+      for (int c = lane; c < vec; c += 32) d[c] = make_uint4(0u, 0u, 0u, 0u);
+      for (int c = lane; c < svec; c += 32) ds[c] = 0x7F7F7F7Fu;
+    } else if (lane == 0) {
+      set_status(status, MOE_ERR_BOUNDS);
+    }
+    return;
+  }
+  const uint4* s = src + (long long)t * vec;
+  for (int c0 = lane; c0 < vec; c0 += 256) {   // eight 16-byte loads in flight per lane
+    uint4 v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + 32 * i < vec) v[i] = __ldg(s + c0 + 32 * i);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (c0 + 32 * i < vec) d[c0 + 32 * i] = v[i];
+  }
+  const uint32_t* ss = src_scale + (long long)t * svec;
+  for (int c = lane; c < svec; c += 32) ds[c] = __ldg(ss + c);
+}
+
+cudaError_t launch_gather_rows_mx(const void* src, const void* src_scale, const int32_t* gather_idx, int R, int T,
+                                  int row_bytes, int scale_ld, void* dst, void* dst_scale, int allow_padding,
+                                  int* status, cudaStream_t st) {
+  if (R <= 0) return cudaSuccess;
+  if (row_bytes % 16 || scale_ld % 4) return cudaErrorInvalidValue;
+  launch_pdl(gather_rows_mx_kernel, (R + 7) / 8, 256, 0, st, static_cast<const uint4*>(src),
+             static_cast<const uint32_t*>(src_scale), gather_idx, R, T, row_bytes / 16, scale_ld / 4,
+             static_cast<uint4*>(dst), static_cast<uint32_t*>(dst_scale), allow_padding, status);
   return cudaGetLastError();
 }
 

@@ -70,6 +70,12 @@ struct GemmParams {
   const int* b_goff;
   long long b_ld_bytes;
   int b_src_rows;
+  const uint8_t* mx_a_scale;   // MXFP8 operands: E8M0 block scales of A's rows (mx_a_ld bytes apart)
+  long long mx_a_ld;
+  long long mx_a_rows;
+  const uint8_t* mx_b_scale;   //   and of B's rows
+  long long mx_b_ld;
+  long long mx_b_rows;
   int* status;
 };
 
@@ -705,6 +711,221 @@ __global__ void __launch_bounds__(GA ? kThreadsGA : kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, C::TMEM_COLS);
 }
 
+// ---------------------------------------------------------------------------
+// MXFP8 operands (OCP microscaling): A and B are e4m3 codes, and every 32 consecutive K values
+// of a row share one power-of-two scale 2^(s - 127), s an unsigned byte (E8M0).  The tensor core
+// applies the scales itself (tcgen05.mma ... kind::mxf8f6f4.block_scale): each MMA (K = 32) reads
+// one scale per A row and one per B row from tensor memory.
+//
+// One CTA, 128 x 256 tiles, a single accumulator (TMEM columns 0..255), the 4-stage ring of
+// GemmCfg<256> (16 KB of A codes + 32 KB of B codes per stage).  Stage s, MMA j of the stage's
+// four, takes its A scales from TMEM columns 256 + 64 s + 16 j .. +3 and its B scales from the
+// 8 columns after 256 + 64 s + 16 j + 8:
+//   A row m:  lane m, column (m / 32), byte 0;
+//   B row n:  column (n / 32), byte 0, lane (n % 32) of every lane quadrant (the quadrant of
+//             the accumulator row being computed is the one read).
+// Four scale-writer warps (one per lane quadrant) copy a stage's scales from global memory into
+// those columns with tcgen05.st once the stage's previous MMAs have finished (the empty barrier),
+// then arrive on the stage's scale barrier, which the MMA issuer waits on beside the TMA barrier.
+// Warps: 0 TMA producer, 1 MMA issuer, 2..9 epilogue, 10..13 scale writers.
+// ---------------------------------------------------------------------------
+constexpr int kMxScaleWarp0 = 2 + kEpiWarps;
+constexpr int kThreadsMX = 32 * (kMxScaleWarp0 + 4);
+
+__device__ __forceinline__ uint32_t mx_col_a(int stage, int j) { return 256u + 64u * stage + 16u * j; }
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreadsMX, 1)
+    gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  pdl_wait();
+  pdl_trigger();
+  using C = GemmCfg<256>;
+  static_assert(C::STAGES == 4, "the scale columns of TMEM hold four stages");
+  constexpr int BN = 256;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
+  uint64_t* empty_bar = full_bar + C::STAGES;
+  uint64_t* tfull_bar = empty_bar + C::STAGES;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* sfull_bar = tempty_bar + 2;   // the stage's scales are in TMEM
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::HOLDER_OFF);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::ABORT_OFF);
+  int* s_toff = reinterpret_cast<int*>(smem + C::TABLE_OFF);
+  int* s_goff = s_toff + (kMaxGroups + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  if (p.num_groups > 0)
+    for (int i = threadIdx.x; i <= p.num_groups; i += blockDim.x) {
+      s_toff[i] = p.tile_off[i];
+      s_goff[i] = p.group_off[i];
+    }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+      mbar_init(&sfull_bar[s], 4);   // one arrive per scale-writer warp
+    }
+    mbar_init(&tfull_bar[0], 1);
+    mbar_init(&tempty_bar[0], kEpiWarps * 32);
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_holder, 512);
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int mtiles = p.num_groups > 0 ? s_toff[p.num_groups] : (p.M + BM - 1) / BM;
+  const int total_tiles = mtiles * p.n_tiles;
+  constexpr int b_tile_rows = EPI == EPI_SWIGLU ? BN / 2 : BN;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      uint32_t stage = 0, phase = 0;
+      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+        const TileCoord c = decode_tile(t, p, s_toff, s_goff);
+        const int brow = c.group * p.b_rows_per_group + c.nt * b_tile_rows;
+        bool ok = true;
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
+          uint8_t* sa = smem + stage * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::A_BYTES;
+          mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+          const int kx = kt * 128;   // 128 e4m3 of K per k-tile
+          tma_load_2d(sa, &tmA, &full_bar[stage], kx, c.row0);
+          if (EPI == EPI_SWIGLU) {
+            tma_load_2d(sb, &tmB, &full_bar[stage], kx, brow);
+            tma_load_2d(sb + C::B_BYTES / 2, &tmB, &full_bar[stage], kx, brow + p.b_gate_offset);
+          } else {
+            tma_load_2d(sb, &tmB, &full_bar[stage], kx, brow);
+          }
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- UMMA issuer ----------------
+      constexpr uint32_t idesc = umma_idesc_mx_e4m3(BM, BN);
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+        const TileCoord c = decode_tile(t, p, s_toff, s_goff);
+        if (!mbar_wait(&tempty_bar[0], ((uint32_t)it & 1u) ^ 1u, abort_flag, p.status)) break;
+        tc_fence_after();
+        bool ok = true;
+        for (int kt = c.kt0; kt < c.kt1; ++kt) {
+          if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status) ||
+              !mbar_wait(&sfull_bar[stage], phase, abort_flag, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint64_t a_desc = umma_sdesc_sw128(sa);
+          const uint64_t b_desc = umma_sdesc_sw128(sa + C::A_BYTES);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // one MMA takes 32 e4m3 of K: 32 bytes further along the swizzled rows
+            const uint32_t ca = tmem_base + mx_col_a(stage, j);
+            umma_mx_e4m3(tmem_base, a_desc + 2 * j, b_desc + 2 * j, idesc, ca, ca + 8,
+                         (kt > c.kt0 || j > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[0]);
+      }
+    }
+  } else if (warp < kMxScaleWarp0) {
+    // ---------------- epilogue: warps 2..9 ----------------
+    const int quad = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row_in_tile = quad * 32 + lane;
+    uint4* stg = reinterpret_cast<uint4*>(smem + C::EPI_OFF) + (warp - 2) * 128;
+    int it = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++it) {
+      const TileCoord c = decode_tile(t, p, s_toff, s_goff);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull_bar[0], (uint32_t)it & 1u, abort_flag, p.status) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16);
+      store_tile<BN, EPI, false>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p, half, stg, c.kt1 <= c.kt0);
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[0]);
+    }
+  } else {
+    // ---------------- scale writers: warps 10..13, one per lane quadrant ----------------
+    const int quad = warp & 3;
+    const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+    uint32_t stage = 0, phase = 0;
+    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+      const TileCoord c = decode_tile(t, p, s_toff, s_goff);
+      // this lane's A row, and the B rows 32 i + lane (i = 0..7) of the tile
+      const long long arow = (long long)c.row0 + quad * 32 + lane;
+      const uint8_t* asrc = arow < p.mx_a_rows ? p.mx_a_scale + arow * p.mx_a_ld : nullptr;
+      const uint8_t* bsrc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int n = 32 * i + lane;
+        const long long brow = (long long)c.group * p.b_rows_per_group + c.nt * b_tile_rows +
+                               (EPI == EPI_SWIGLU && n >= BN / 2 ? p.b_gate_offset + n - BN / 2 : n);
+        bsrc[i] = brow < p.mx_b_rows ? p.mx_b_scale + brow * p.mx_b_ld : nullptr;
+      }
+      bool ok = true;
+      for (int kt = c.kt0; kt < c.kt1; ++kt) {
+        // the four scales of a row for this k-tile are one aligned 32-bit word; rows past the
+        // operand get 2^0 (their products are never stored)
+        const uint32_t wa = asrc ? *reinterpret_cast<const uint32_t*>(asrc + 4 * kt) : 0x7F7F7F7Fu;
+        uint32_t wb[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) wb[i] = bsrc[i] ? *reinterpret_cast<const uint32_t*>(bsrc[i] + 4 * kt) : 0x7F7F7F7Fu;
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status) ? 1 : 0;
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t col = mx_col_a(stage, j);
+          tmem_st_32x32b_x1(lane_base + col + quad, (wa >> (8 * j)) & 0xFFu);
+          uint32_t v[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) v[i] = (wb[i] >> (8 * j)) & 0xFFu;
+          tmem_st_32x32b_x8(lane_base + col + 8, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfull_bar[stage]);
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (*abort_flag) {
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < 50000ull) { }
+  }
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, 512);
+}
+
 
 // ---------------------------------------------------------------------------
 // CTA-pair variant: a cluster of two CTAs computes 256 x 256 tiles with
@@ -1223,6 +1444,22 @@ static cudaError_t launch_impl(const GemmProblem& q, const CUtensorMap& ta, cons
   return cudaGetLastError();
 }
 
+template <int EPI>
+static cudaError_t launch_mx_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp, int grid,
+                                  cudaStream_t stream) {
+  using C = GemmCfg<256>;
+  auto kern = gemm_mx_kernel<EPI>;
+  static std::atomic<int> ready[kMaxDeviceSlots];
+  const int dev = device_slot();
+  if (dev < 0 || !ready[dev].load()) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0) ready[dev].store(1);
+  }
+  launch_pdl(kern, grid, kThreadsMX, C::SMEM_BYTES, stream, ta, tb, gp);
+  return cudaGetLastError();
+}
+
 template <int EPI, bool F8 = false, bool GA = false, bool GB = false>
 static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp, int tiles,
                                     cudaStream_t stream, const CUtensorMap* tp = nullptr) {
@@ -1261,6 +1498,47 @@ static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb
 cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   if (q.num_groups > kMaxGroups || q.k_groups > kMaxGroups) return cudaErrorInvalidValue;
   if (q.k_groups > 0 && (q.num_groups > 0 || q.splits > 1 || q.epilogue != EPI_F32)) return cudaErrorInvalidValue;
+  if (q.mx) {
+    // MXFP8 operands: 128 x 256 tiles on one CTA, both code operands TMA-loaded, K-major, the
+    // block scales 32-bit aligned (four of them per 128-byte k-tile)
+    if (q.bn != 256 || q.splits > 1 || q.k_groups > 0 || q.pair_tiles || q.e4m3 || q.a_gather || q.b_gather ||
+        q.b_mn_major || q.a_mn_major || q.a_off || q.preact || q.K <= 0 || q.K % 128 || !q.a_mx_scale ||
+        !q.b_mx_scale || q.a_mx_ld % 4 || q.b_mx_ld % 4 || q.a_mx_ld < q.K / 32 || q.b_mx_ld < q.K / 32 ||
+        (reinterpret_cast<uintptr_t>(q.a_mx_scale) & 3) || (reinterpret_cast<uintptr_t>(q.b_mx_scale) & 3) ||
+        (q.epilogue != EPI_SWIGLU && q.epilogue != EPI_BF16) || q.M < 0)
+      return cudaErrorInvalidValue;
+    if (q.M == 0) return cudaSuccess;
+    CUtensorMap ta, tb;
+    if (!make_tmap(&tb, q.B, q.b_rows_total, q.K, q.epilogue == EPI_SWIGLU ? 128 : 256, true) ||
+        !make_tmap(&ta, q.A, q.M, q.K, BM, true))
+      return cudaErrorInvalidValue;
+    GemmParams gp{};
+    gp.M = q.M;
+    gp.N = q.N;
+    gp.K = q.K;
+    gp.num_groups = q.num_groups;
+    gp.group_off = q.group_off;
+    gp.tile_off = q.tile_off;
+    gp.b_rows_per_group = q.b_rows_per_group;
+    gp.b_gate_offset = q.b_gate_offset;
+    gp.n_tiles = (q.N + (q.epilogue == EPI_SWIGLU ? 127 : 255)) / (q.epilogue == EPI_SWIGLU ? 128 : 256);
+    gp.kt_total = q.K / 128;
+    gp.splits = 1;
+    gp.kt_per_split = gp.kt_total;
+    gp.out = q.out;
+    gp.ldo = q.ldo;
+    gp.mx_a_scale = static_cast<const uint8_t*>(q.a_mx_scale);
+    gp.mx_a_ld = q.a_mx_ld;
+    gp.mx_a_rows = q.M;
+    gp.mx_b_scale = static_cast<const uint8_t*>(q.b_mx_scale);
+    gp.mx_b_ld = q.b_mx_ld;
+    gp.mx_b_rows = q.b_rows_total;
+    gp.status = q.status;
+    int grid = num_sms();
+    if (q.num_groups == 0) grid = std::min(grid, ((q.M + BM - 1) / BM) * gp.n_tiles);
+    return q.epilogue == EPI_SWIGLU ? launch_mx_impl<EPI_SWIGLU>(ta, tb, gp, grid, stream)
+                                    : launch_mx_impl<EPI_BF16>(ta, tb, gp, grid, stream);
+  }
   const bool pair = q.pair_tiles != 0;
   const bool f8 = q.e4m3 != 0;
   if (pair && (q.bn != 256 || q.splits > 1 || (q.epilogue == EPI_F32 && (q.e4m3 || q.num_groups > 0))))

@@ -65,6 +65,13 @@ struct GemmProblem {
   const void* b_src;
   const int* b_goff;      // device (k_groups + 1) row offsets of the groups in b_gather
   int b_src_rows;
+  int mx;                 // 1: A and B are e4m3 codes with E8M0 block scales (one per 32 K values of a row,
+                          //    kind::mxf8f6f4.block_scale); K a multiple of 128; grouped or dense SwiGLU / bf16
+                          //    out on 128 x 256 tiles, TMA-loaded A
+  const void* a_mx_scale; // (M, a_mx_ld) bytes: row r's scale of K block b at [r * a_mx_ld + b]
+  int64_t a_mx_ld;        // a multiple of 4, >= K / 32
+  const void* b_mx_scale; // (b_rows_total, b_mx_ld) bytes
+  int64_t b_mx_ld;
   int* status;
 };
 
@@ -131,6 +138,9 @@ cudaError_t launch_add_bf16(const void* a, const void* b, long long n, void* out
 // host, synchronising the stream: result_host[0] = 1 if it gave up with the abort flag raised,
 // result_host[1] = milliseconds waited.  The wait records MOE_ERR_TIMEOUT in *status.
 cudaError_t launch_wait_timeout_check(uint64_t limit_ns, int* status, int* result_host, cudaStream_t st);
+// MXFP8 codes (rows x cols bytes) and E8M0 block scales (rows x scale_ld bytes, cols / 32 used).
+cudaError_t launch_quantize_mx_e4m3(const void* x, long long rows, int cols, void* q, void* scales, int scale_ld,
+                                    cudaStream_t st);
 cudaError_t launch_combine_backward(const void* dz, const void* y, const int32_t* scatter_idx, const float* w, int T,
                                     int k, int L, int rows, void* dy, float* dw, int* status, cudaStream_t st);
 cudaError_t launch_zero_padding_rows(const int32_t* gather_idx, int rows, int cols, void* dst, cudaStream_t st);
@@ -142,6 +152,11 @@ cudaError_t launch_column_sum(const float* d, int T, int E, float* out, cudaStre
 cudaError_t launch_sum_slices_f32(const float* part, int splits, long long n, float* out, cudaStream_t st);
 cudaError_t launch_quantize_rowwise_e4m3(const void* x, long long rows, int cols, void* q, float* scale,
                                          cudaStream_t st);
+// dst[p] = src[gather_idx[p]] for MXFP8 rows: row_bytes codes (a multiple of 16) and scale_ld scale bytes
+// (a multiple of 4) per row; a padding slot (-1, capacity mode) gets zero codes and scales 2^0.
+cudaError_t launch_gather_rows_mx(const void* src, const void* src_scale, const int32_t* gather_idx, int R, int T,
+                                  int row_bytes, int scale_ld, void* dst, void* dst_scale, int allow_padding,
+                                  int* status, cudaStream_t st);
 cudaError_t launch_gather_rows_e4m3(const void* src, const float* src_scale, const int32_t* gather_idx, int R, int T,
                                     int row_bytes, void* dst, float* dst_scale, int allow_padding, int* status,
                                     cudaStream_t st);

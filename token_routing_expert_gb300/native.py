@@ -43,7 +43,8 @@ class moe_config_t(ctypes.Structure):
 class moe_weights_t(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in ("w_router", "b_router", "score_bias", "w_down_latent",
                                                   "w_up_latent", "rms_weight", "w_up_gate", "w_out",
-                                                  "w_up_gate_fp8", "w_up_gate_scale", "w_out_fp8", "w_out_scale")]
+                                                  "w_up_gate_fp8", "w_up_gate_scale", "w_out_fp8", "w_out_scale",
+                                                  "w_up_gate_mx_scale", "w_out_mx_scale")]
 
 
 class moe_grads_t(ctypes.Structure):
@@ -60,7 +61,7 @@ EXPORTS = ["moe_quantize_rowwise_fp8", "moe_expert_capacity", "moe_permuted_rows
            "moe_router_backward", "moe_host_workspace_size", "moe_layer_forward_host_batches",
            "moe_grouped_swiglu_preact", "moe_layer_forward_preact", "moe_grouped_swiglu_backward_preact",
            "moe_latent_restore_backward", "moe_latent_down_backward", "moe_layer_backward_workspace_size",
-           "moe_layer_backward", "moe_check_wait_timeout"]
+           "moe_layer_backward", "moe_check_wait_timeout", "moe_quantize_mxfp8"]
 
 _lib = None
 
@@ -108,6 +109,7 @@ def load() -> ctypes.CDLL:
         "moe_latent_down_backward": [cfgp, wp, VP, I64, VP, VP, VP, VP, SZ, VP],
         "moe_layer_backward_workspace_size": [cfgp, I64, P(SZ)],
         "moe_check_wait_timeout": [ctypes.c_int32, P(ctypes.c_int32), VP],
+        "moe_quantize_mxfp8": [VP, I64, ctypes.c_int32, VP, VP, ctypes.c_int32, VP],
         "moe_layer_backward": [cfgp, wp, VP, I64, VP, SZ, VP, VP, VP, VP, P(moe_grads_t), VP, SZ, VP],
         "moe_combine_backward": [cfgp, VP, VP, VP, VP, VP, I64, VP, VP, VP],
         "moe_grouped_swiglu_backward": [cfgp, wp, VP, VP, VP, VP, I64, VP, VP, VP, VP, VP, SZ, VP],
@@ -133,6 +135,10 @@ def _status_string(code: int) -> str:
 def _check(code: int, where: str) -> None:
     if code != MOE_OK:
         raise MoEError(code, where)
+
+
+# moe_config_t.expert_fp8: operands of the experts' GEMMs
+EXPERT_BF16, EXPERT_FP8_ROWWISE, EXPERT_MXFP8 = 0, 1, 2
 
 
 def make_config(d_model, num_experts, top_k, hidden_size, latent_dim=0, up_proj_norm=True, rms_eps=1e-6,
@@ -243,12 +249,21 @@ class DeviceWeights:
     w_up_gate_scale: Optional[torch.Tensor] = None
     w_out_fp8: Optional[torch.Tensor] = None
     w_out_scale: Optional[torch.Tensor] = None
+    w_up_gate_mx_scale: Optional[torch.Tensor] = None
+    w_out_mx_scale: Optional[torch.Tensor] = None
 
     def quantize_experts_fp8(self, stream=None) -> "DeviceWeights":
         """Pre-quantises the expert weights row by row to e4m3 (moe_quantize_rowwise_fp8)."""
         ug, wo = self.w_up_gate, self.w_out
         self.w_up_gate_fp8, self.w_up_gate_scale = moe_quantize_rowwise_fp8(ug.reshape(-1, ug.shape[-1]), stream=stream)
         self.w_out_fp8, self.w_out_scale = moe_quantize_rowwise_fp8(wo.reshape(-1, wo.shape[-1]), stream=stream)
+        return self
+
+    def quantize_experts_mxfp8(self, stream=None) -> "DeviceWeights":
+        """Pre-quantises the expert weights to MXFP8 along their contraction (moe_quantize_mxfp8)."""
+        ug, wo = self.w_up_gate, self.w_out
+        self.w_up_gate_fp8, self.w_up_gate_mx_scale = moe_quantize_mxfp8(ug.reshape(-1, ug.shape[-1]), stream=stream)
+        self.w_out_fp8, self.w_out_mx_scale = moe_quantize_mxfp8(wo.reshape(-1, wo.shape[-1]), stream=stream)
         return self
 
     @staticmethod
@@ -270,7 +285,9 @@ class DeviceWeights:
             _ptr(self.w_up_latent, bf, "w_up_latent"), _ptr(self.rms_weight, bf, "rms_weight"),
             _ptr(self.w_up_gate, bf, "w_up_gate"), _ptr(self.w_out, bf, "w_out"),
             _ptr(self.w_up_gate_fp8, torch.uint8, "w_up_gate_fp8"), _ptr(self.w_up_gate_scale, f32, "w_up_gate_scale"),
-            _ptr(self.w_out_fp8, torch.uint8, "w_out_fp8"), _ptr(self.w_out_scale, f32, "w_out_scale"))
+            _ptr(self.w_out_fp8, torch.uint8, "w_out_fp8"), _ptr(self.w_out_scale, f32, "w_out_scale"),
+            _ptr(self.w_up_gate_mx_scale, torch.uint8, "w_up_gate_mx_scale"),
+            _ptr(self.w_out_mx_scale, torch.uint8, "w_out_mx_scale"))
 
 
 def moe_quantize_rowwise_fp8(x, codes=None, scales=None, stream=None):
@@ -568,6 +585,22 @@ def moe_latent_down_backward(cfg, weights: DeviceWeights, x, dx_routed, bws, str
         _ptr(dw_down, torch.float32, "dw_down"), _ptr(bws, None, "ws"), bws.numel(), _stream(stream)),
         "moe_latent_down_backward")
     return dx, dw_down
+
+
+def mx_scale_ld(cols: int) -> int:
+    """Bytes per row of MXFP8 block scales: cols / 32, rounded up to 16."""
+    return (cols // 32 + 15) // 16 * 16
+
+
+def moe_quantize_mxfp8(x, stream=None):
+    """(codes (rows, cols) uint8 e4m3 bits, scales (rows, mx_scale_ld(cols)) uint8 E8M0 exponents)."""
+    rows, cols = x.shape
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=x.device)
+    scales = torch.zeros((rows, mx_scale_ld(cols)), dtype=torch.uint8, device=x.device)
+    _check(load().moe_quantize_mxfp8(_ptr(x, torch.bfloat16, "x"), rows, cols, _ptr(codes, torch.uint8, "codes"),
+                                     _ptr(scales, torch.uint8, "scales"), scales.shape[1], _stream(stream)),
+           "moe_quantize_mxfp8")
+    return codes, scales
 
 
 def moe_check_wait_timeout(limit_ms: int = 20, stream=None) -> int:

@@ -55,7 +55,7 @@ class WorkloadSpec:
     up_proj_norm: bool = True
     rms_eps: float = 1e-6
     capacity_factor: float = 0.0         # > 0: capacity-limited experts
-    expert_fp8: bool = False             # experts on rowwise e4m3 operands
+    expert_fp8: int = 0                  # experts' operands: 0 bf16, 1 rowwise e4m3, 2 MXFP8
     x_std: float = 1.0
     w_std: float = 0.02
     seed: int = 0

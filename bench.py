@@ -67,7 +67,9 @@ def workload_desc(spec: W.WorkloadSpec) -> str:
         s += " skewed_load"
     if spec.capacity_factor:
         s += f" capacity_factor={spec.capacity_factor:g}"
-    if spec.expert_fp8:
+    if spec.expert_fp8 == 2:
+        s += " experts_mxfp8"
+    elif spec.expert_fp8:
         s += " experts_e4m3_rowwise"
     return s
 
@@ -264,13 +266,19 @@ def run_native(args):
     if args.capacity_factor > 0:
         spec = spec.with_(capacity_factor=args.capacity_factor)
     if args.fp8:
-        spec = spec.with_(expert_fp8=True)
+        spec = spec.with_(expert_fp8=native.EXPERT_FP8_ROWWISE)
+    if args.mxfp8:
+        spec = spec.with_(expert_fp8=native.EXPERT_MXFP8)
+    if args.backward and args.mxfp8:
+        raise SystemExit("--backward times the training path, which keeps bf16 pre-activations: not with --mxfp8")
     # each rank draws its own batch of tokens (weak scaling); weights are shared replicas
     inp = rank_inputs(spec, rank)
     cfg = native.config_from_spec(spec)
     wts = native.DeviceWeights.from_inputs(inp)
-    if spec.expert_fp8:
-        wts.quantize_experts_fp8()   # pre-quantised expert weights, outside the timed region
+    if spec.expert_fp8 == native.EXPERT_MXFP8:
+        wts.quantize_experts_mxfp8()   # pre-quantised expert weights, outside the timed region
+    elif spec.expert_fp8:
+        wts.quantize_experts_fp8()
     T = spec.T
     x = inp["x"].cuda()
     ws = native.workspace(cfg, T)
@@ -505,7 +513,9 @@ def run_native(args):
     roof_bytes = alg_bytes
     if spec.expert_fp8:
         t_flops = (flops - expert_flops) / (peak_tf * 1e12) + expert_flops / (gemm_peak * 1e12)
-        roof_bytes = alg_bytes - touched * 3 * spec.routed_dim * spec.hidden_size
+        # e4m3 weights: 1 byte a value instead of 2 (MXFP8 adds a scale byte per 32 values)
+        roof_bytes = alg_bytes - touched * 3 * spec.routed_dim * spec.hidden_size * (
+            31 / 32 if spec.expert_fp8 == native.EXPERT_MXFP8 else 1)
     t_bytes = roof_bytes / (peaks["hbm_gbs"] * 1e9)
     bound_layer = "hbm" if t_bytes > t_flops else "tensor"
     roof_ms = 1e3 * max(t_bytes, t_flops)
@@ -523,7 +533,8 @@ def run_native(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16 (experts e4m3 rowwise)" if spec.expert_fp8 else "bf16",
+        "dtype": ("bf16 (experts MXFP8: e4m3, E8M0 scale per 32 values)" if spec.expert_fp8 == native.EXPERT_MXFP8
+                  else "bf16 (experts e4m3 rowwise)" if spec.expert_fp8 else "bf16"),
         "data": "synthetic (seeded numpy PCG64 normals rounded to bf16; random-init weights)",
         "config": dict(bench_config(spec, world),
                        l2=("flushed between steps (working set below 2x L2)" if flush else
@@ -540,7 +551,9 @@ def run_native(args):
                        "hbm_peak": peaks["hbm_gbs"], "note": "each stage's own minimum bytes"},
         "balance": bal,
         "backward": bwd,
-        "roofline": {"kernel": "grouped GEMM 1 (SwiGLU fused, tcgen05" + (", e4m3 operands)" if spec.expert_fp8 else ")"),
+        "roofline": {"kernel": "grouped GEMM 1 (SwiGLU fused, tcgen05" + (
+                     ", MXFP8 block-scaled operands)" if spec.expert_fp8 == native.EXPERT_MXFP8 else
+                     ", e4m3 operands)" if spec.expert_fp8 else ")"),
                      "bound": "tensor", "achieved": achieved, "peak": gemm_peak, "unit": "TFLOP/s",
                      "frac": achieved / gemm_peak,
                      "traffic": None if spec.expert_fp8 or spec.capacity_factor else kernel_traffic(spec.name),
@@ -579,6 +592,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--backward", action="store_true", help="also time the combine + experts backward")
     ap.add_argument("--fp8", action="store_true", help="experts on rowwise e4m3 operands")
+    ap.add_argument("--mxfp8", action="store_true", help="experts on MXFP8 operands (E8M0 block scales)")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

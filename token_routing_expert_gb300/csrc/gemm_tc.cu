@@ -734,6 +734,79 @@ constexpr int kThreadsMX = 32 * (kMxScaleWarp0 + 4);
 
 __device__ __forceinline__ uint32_t mx_col_a(int stage, int j) { return 256u + 64u * stage + 16u * j; }
 
+__device__ __forceinline__ uint32_t uint4_word(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// The 16-byte words of block scales for k-tiles [4 g, 4 g + 4) of the tile: this lane's A row
+// (row 32 quad + lane of the tile) and B rows 32 i + lane, i = 0..7 (SwiGLU: rows 0..127 of the
+// tile are the up rows, 128..255 the gate rows); rows past an operand read 2^0 (byte 127), their
+// products are never stored.
+template <int EPI>
+__device__ __forceinline__ void mx_load_scales(const GemmParams& p, const TileCoord& c, int quad, int lane, int g,
+                                               uint4& a, uint4 (&b)[8]) {
+  constexpr int b_tile_rows = EPI == EPI_SWIGLU ? 128 : 256;
+  const uint4 one = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  const long long arow = (long long)c.row0 + quad * 32 + lane;
+  a = arow < p.mx_a_rows ? __ldg(reinterpret_cast<const uint4*>(p.mx_a_scale + arow * p.mx_a_ld) + g) : one;
+  const long long base = (long long)c.group * p.b_rows_per_group + (long long)c.nt * b_tile_rows;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int n = 32 * i + lane;
+    const long long brow = base + (EPI == EPI_SWIGLU && i >= 4 ? p.b_gate_offset + n - 128 : n);
+    b[i] = brow < p.mx_b_rows ? __ldg(reinterpret_cast<const uint4*>(p.mx_b_scale + brow * p.mx_b_ld) + g) : one;
+  }
+}
+
+// MXFP8 epilogue of one tile for the 32 rows a warp owns.  The warp reads its whole share of
+// the accumulator (every other 32-column chunk) into registers, already converted (SwiGLU: 64 h
+// values, bf16 out: 128 values, packed in bf16 pairs), and releases the accumulator before its
+// global stores, so the next tile's MMAs run while this tile is written out.
+template <int EPI>
+__device__ __forceinline__ void mx_store_tile(uint32_t tbase, const TileCoord& c, int row_in_tile,
+                                              const GemmParams& p, int half, uint4* stg, uint64_t* tempty) {
+  constexpr int CHUNKS = EPI == EPI_SWIGLU ? 2 : 4;   // 32-column output chunks of this warp
+  const int lane = row_in_tile & 31;
+  const int valid = min(max(c.rows - (row_in_tile - lane), 0), 32);
+  const long long wrow0 = (long long)c.row0 + (row_in_tile - lane);
+  uint32_t packed[CHUNKS][16];
+  __syncwarp();
+#pragma unroll
+  for (int q = 0; q < CHUNKS; ++q) {
+    const int cc = half + 2 * q;
+    if (EPI == EPI_SWIGLU) {   // u in columns [0, 128), g in [128, 256)
+      uint32_t u[32], g[32];
+      tmem_ld_32x32b_x32(tbase + cc * 32, u);
+      tmem_ld_32x32b_x32(tbase + 128 + cc * 32, g);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float g0 = __uint_as_float(g[2 * i]), g1 = __uint_as_float(g[2 * i + 1]);
+        // silu(g) = g / (1 + e^-g); the approximate division returns 0 when e^-g overflows
+        const float h0 = __fdividef(g0, 1.0f + __expf(-g0)) * __uint_as_float(u[2 * i]);
+        const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * __uint_as_float(u[2 * i + 1]);
+        packed[q][i] = pack_bf16x2(h0, h1);
+      }
+    } else {
+      uint32_t v[32];
+      tmem_ld_32x32b_x32(tbase + cc * 32, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        packed[q][i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    }
+  }
+  tc_fence_before();
+  mbar_arrive(tempty);
+  constexpr int out_cols = EPI == EPI_SWIGLU ? 128 : 256;   // output columns per tile
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo;
+#pragma unroll
+  for (int q = 0; q < CHUNKS; ++q) {
+    const int col0 = c.nt * out_cols + (half + 2 * q) * 32;
+    if (valid > 0 && col0 < p.N) store_block_bf16(stg, packed[q], out + col0, p.ldo, valid, lane);
+  }
+}
+
 template <int EPI>
 __global__ void __launch_bounds__(kThreadsMX, 1)
     gemm_mx_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -861,49 +934,50 @@ __global__ void __launch_bounds__(kThreadsMX, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(quad * 32) << 16);
-      store_tile<BN, EPI, false>(tbase, c.row0, c.rows, row_in_tile, c.nt, c.split, p, half, stg, c.kt1 <= c.kt0);
-      tc_fence_before();
-      mbar_arrive(&tempty_bar[0]);
+      mx_store_tile<EPI>(tmem_base + ((uint32_t)(quad * 32) << 16), c, row_in_tile, p, half, stg, &tempty_bar[0]);
     }
   } else {
     // ---------------- scale writers: warps 10..13, one per lane quadrant ----------------
+    // A row's scales for four k-tiles are one aligned 16-byte word; the words of the next group of
+    // four k-tiles are loaded while this group's are written, so an L2 round trip is paid once per
+    // four k-tiles and overlaps the MMAs instead of once per k-tile in series with them
     const int quad = warp & 3;
     const uint32_t lane_base = tmem_base + ((uint32_t)(quad * 32) << 16);
+    const int groups = (p.kt_total + 3) / 4;
     uint32_t stage = 0, phase = 0;
-    for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
-      const TileCoord c = decode_tile(t, p, s_toff, s_goff);
-      // this lane's A row, and the B rows 32 i + lane (i = 0..7) of the tile
-      const long long arow = (long long)c.row0 + quad * 32 + lane;
-      const uint8_t* asrc = arow < p.mx_a_rows ? p.mx_a_scale + arow * p.mx_a_ld : nullptr;
-      const uint8_t* bsrc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int n = 32 * i + lane;
-        const long long brow = (long long)c.group * p.b_rows_per_group + c.nt * b_tile_rows +
-                               (EPI == EPI_SWIGLU && n >= BN / 2 ? p.b_gate_offset + n - BN / 2 : n);
-        bsrc[i] = brow < p.mx_b_rows ? p.mx_b_scale + brow * p.mx_b_ld : nullptr;
+    int t = blockIdx.x, g = 0;
+    TileCoord c{};
+    uint4 ca{}, cb[8]{};
+    if (t < total_tiles) {
+      c = decode_tile(t, p, s_toff, s_goff);
+      mx_load_scales<EPI>(p, c, quad, lane, 0, ca, cb);
+    }
+    bool ok = true;
+    while (ok && t < total_tiles) {
+      int tn = t, gn = g + 1;
+      if (gn == groups) { tn = t + gridDim.x; gn = 0; }
+      TileCoord cn = c;
+      uint4 na{}, nb[8]{};
+      if (tn < total_tiles) {
+        if (tn != t) cn = decode_tile(tn, p, s_toff, s_goff);
+        mx_load_scales<EPI>(p, cn, quad, lane, gn, na, nb);
       }
-      bool ok = true;
-      for (int kt = c.kt0; kt < c.kt1; ++kt) {
-        // the four scales of a row for this k-tile are one aligned 32-bit word; rows past the
-        // operand get 2^0 (their products are never stored)
-        const uint32_t wa = asrc ? *reinterpret_cast<const uint32_t*>(asrc + 4 * kt) : 0x7F7F7F7Fu;
-        uint32_t wb[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) wb[i] = bsrc[i] ? *reinterpret_cast<const uint32_t*>(bsrc[i] + 4 * kt) : 0x7F7F7F7Fu;
+      for (int kk = 0; kk < 4; ++kk) {
+        if (!ok || 4 * g + kk >= c.kt1) break;
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status) ? 1 : 0;
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) { ok = false; break; }
         tc_fence_after();
+        const uint32_t wa = uint4_word(ca, kk);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint32_t col = mx_col_a(stage, j);
           tmem_st_32x32b_x1(lane_base + col + quad, (wa >> (8 * j)) & 0xFFu);
           uint32_t v[8];
 #pragma unroll
-          for (int i = 0; i < 8; ++i) v[i] = (wb[i] >> (8 * j)) & 0xFFu;
+          for (int i = 0; i < 8; ++i) v[i] = (uint4_word(cb[i], kk) >> (8 * j)) & 0xFFu;
           tmem_st_32x32b_x8(lane_base + col + 8, v);
         }
         tmem_st_wait();
@@ -912,7 +986,12 @@ __global__ void __launch_bounds__(kThreadsMX, 1)
         if (lane == 0) mbar_arrive(&sfull_bar[stage]);
         if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
       }
-      if (!ok) break;
+      ca = na;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) cb[i] = nb[i];
+      c = cn;
+      t = tn;
+      g = gn;
     }
   }
 
@@ -1499,12 +1578,12 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   if (q.num_groups > kMaxGroups || q.k_groups > kMaxGroups) return cudaErrorInvalidValue;
   if (q.k_groups > 0 && (q.num_groups > 0 || q.splits > 1 || q.epilogue != EPI_F32)) return cudaErrorInvalidValue;
   if (q.mx) {
-    // MXFP8 operands: 128 x 256 tiles on one CTA, both code operands TMA-loaded, K-major, the
-    // block scales 32-bit aligned (four of them per 128-byte k-tile)
+    // MXFP8 operands: 128 x 256 tiles on one CTA, both code operands TMA-loaded, K-major; the
+    // block-scale rows 16-byte aligned (read as 16 scales: four 128-value k-tiles)
     if (q.bn != 256 || q.splits > 1 || q.k_groups > 0 || q.pair_tiles || q.e4m3 || q.a_gather || q.b_gather ||
         q.b_mn_major || q.a_mn_major || q.a_off || q.preact || q.K <= 0 || q.K % 128 || !q.a_mx_scale ||
-        !q.b_mx_scale || q.a_mx_ld % 4 || q.b_mx_ld % 4 || q.a_mx_ld < q.K / 32 || q.b_mx_ld < q.K / 32 ||
-        (reinterpret_cast<uintptr_t>(q.a_mx_scale) & 3) || (reinterpret_cast<uintptr_t>(q.b_mx_scale) & 3) ||
+        !q.b_mx_scale || q.a_mx_ld % 16 || q.b_mx_ld % 16 || q.a_mx_ld < q.K / 32 || q.b_mx_ld < q.K / 32 ||
+        (reinterpret_cast<uintptr_t>(q.a_mx_scale) & 15) || (reinterpret_cast<uintptr_t>(q.b_mx_scale) & 15) ||
         (q.epilogue != EPI_SWIGLU && q.epilogue != EPI_BF16) || q.M < 0)
       return cudaErrorInvalidValue;
     if (q.M == 0) return cudaSuccess;

@@ -69,7 +69,7 @@ struct GemmProblem {
                           //    kind::mxf8f6f4.block_scale); K a multiple of 128; grouped or dense SwiGLU / bf16
                           //    out on 128 x 256 tiles, TMA-loaded A
   const void* a_mx_scale; // (M, a_mx_ld) bytes: row r's scale of K block b at [r * a_mx_ld + b]
-  int64_t a_mx_ld;        // a multiple of 4, >= K / 32
+  int64_t a_mx_ld;        // a multiple of 16, >= K / 32 (and both scale pointers 16-byte aligned)
   const void* b_mx_scale; // (b_rows_total, b_mx_ld) bytes
   int64_t b_mx_ld;
   int* status;

@@ -1,6 +1,7 @@
-"""Full-size parity of the two other modes bench.py times: rowwise FP8 experts
-(`--fp8`) and the capacity-factor layer (`--capacity-factor`), in the same
-launch configuration (one moe_layer_forward with the library's own workspace).
+"""Full-size parity of the other modes bench.py times: rowwise FP8 experts
+(`--fp8`), MXFP8 experts (`--mxfp8`) and the capacity-factor layer
+(`--capacity-factor`), in the same launch configuration (one moe_layer_forward
+with the library's own workspace).
 
 FP8: the top-k indices on all tokens (near-tie rule), and sampled tokens'
 outputs against the float64 oracle's FP8 layer run on those tokens alone (FP8
@@ -10,6 +11,11 @@ rounding midpoint may quantise that whole row with the neighbouring scale: such
 tokens are found from the oracle's own values and held to rel-L2 only.  A latent
 layer's quantiser input is itself computed (the down-projection), and is held to
 the FP8 bar: rel-L2 1e-2 over the sample, half an e4m3 step per token.
+
+MXFP8: as FP8, with the oracle's MXFP8 layer on the sampled tokens (the block
+scales belong to one token's row or one weight row, so tokens stay independent),
+held to the MXFP8 bar of the small-case tests: rel-L2 1e-2 over the sample and
+half an e4m3 step per token.
 
 Capacity: the capacity permutation over all tokens bit-exact against the
 oracle's on the GPU's indices.  Which assignments drop depends on every token,
@@ -35,7 +41,9 @@ def _run(spec):
     inp = generate(spec)
     cfg = native.config_from_spec(spec)
     wts = native.DeviceWeights.from_inputs(inp)
-    if spec.expert_fp8:
+    if spec.expert_fp8 == native.EXPERT_MXFP8:
+        wts.quantize_experts_mxfp8()
+    elif spec.expert_fp8:
         wts.quantize_experts_fp8()
     ws = native.workspace(cfg, spec.T)
     out = native.moe_layer_forward(cfg, wts, inp["x"].cuda(), ws)
@@ -61,6 +69,22 @@ def test_full_size_fp8(name):
     amb = fp8_ambiguous_tokens(oc, ow, xs, forced)
     assert_close_fp8_layer(out[sample], want, amb, f"{name} fp8 sampled layer output", output_scale(spec),
                            latent=bool(spec.latent_dim))
+
+
+@pytest.mark.parametrize("name", ["olmoe", "latent_prefill"])
+def test_full_size_mxfp8(name):
+    from tests.test_gpu_mxfp8 import assert_close_mx
+    spec = WORKLOADS[name].with_(expert_fp8=native.EXPERT_MXFP8)
+    inp, cfg, out, inter = _run(spec)
+    gi = inter["idx"].numpy().astype(np.int64)
+    oc, ow = oracle_config(spec), oracle_weights(spec, inp)
+    r = ref.route(oc, f64(inp["x"]), ow.w_router, ow.b_router, ow.score_bias)
+    mism = check_topk(gi, r.keys, r.idx, spec.top_k)
+    sample = np.sort(np.random.default_rng(4322).choice(spec.T, size=SAMPLE, replace=False))
+    forced = r.idx[sample].copy()
+    forced[mism[sample]] = gi[sample][mism[sample]]
+    want = ref.layer_forward_mxfp8(oc, f64(inp["x"][torch.from_numpy(sample)]), ow, forced_idx=forced)
+    assert_close_mx(out[sample], want, f"{name} mxfp8 sampled layer output")
 
 
 def test_full_size_capacity():

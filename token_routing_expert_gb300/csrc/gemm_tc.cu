@@ -787,13 +787,16 @@ __device__ __forceinline__ void mx_store_tile(uint32_t tbase, const TileCoord& c
         const float h1 = __fdividef(g1, 1.0f + __expf(-g1)) * __uint_as_float(u[2 * i + 1]);
         packed[q][i] = pack_bf16x2(h0, h1);
       }
-    } else {
-      uint32_t v[32];
-      tmem_ld_32x32b_x32(tbase + cc * 32, v);
-      tmem_ld_wait();
+    } else {   // 16 columns at a time: fewer live registers beside the 64 packed words
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        packed[q][i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[16];
+        tmem_ld_32x32b_x16(tbase + cc * 32 + 16 * h, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          packed[q][8 * h + i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+      }
     }
   }
   tc_fence_before();

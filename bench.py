@@ -546,7 +546,9 @@ def run_native(args):
                   "dropped_assignments": dropped},
         "stages_ms": stage_ms,
         "stages_note": "a separate pass over the same steps with events at the stage boundaries (they break the "
-                       "launch overlap between kernels, so the stages add up to a little more than ms_per_step)",
+                       "launch overlap between kernels, so the stages add up to a little more than ms_per_step)"
+                       + ("; e4m3 experts: quantising x_routed counts in 'gather', quantising H in 'grouped_gemm2'"
+                          if spec.expert_fp8 else ""),
         "stages_gbs": {"values": stage_gbs, "bytes": stage_bytes,
                        "hbm_peak": peaks["hbm_gbs"], "note": "each stage's own minimum bytes"},
         "balance": bal,

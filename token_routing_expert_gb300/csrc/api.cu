@@ -333,9 +333,10 @@ int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* x
   g1.preact_ld = 2 * (int64_t)p.h;
   g1.status = status;
   s = cuda_status(launch_gemm(g1, st));
-  if (s == MOE_OK) s = cuda_status(launch_quantize_rowwise_e4m3(H, p.rows, p.h, hq, hs, st));
   if (s != MOE_OK) return s;
-  mark(ev, 6, st);
+  mark(ev, 6, st);   // the stage of GEMM 1 alone; quantising H counts with GEMM 2
+  s = cuda_status(launch_quantize_rowwise_e4m3(H, p.rows, p.h, hq, hs, st));
+  if (s != MOE_OK) return s;
   GemmProblem g2{};
   g2.A = hq;
   g2.B = w->w_out_fp8;
@@ -407,9 +408,10 @@ int run_experts_mx(const moe_config_t* c, const moe_weights_t* w, const void* xr
   g1.ldo = p.h;
   g1.status = status;
   s = cuda_status(launch_gemm(g1, st));
-  if (s == MOE_OK) s = cuda_status(launch_quantize_mx_e4m3(H, p.rows, p.h, hq, hs, (int)p.sh_ld, st));
   if (s != MOE_OK) return s;
-  mark(ev, 6, st);
+  mark(ev, 6, st);   // the stage of GEMM 1 alone; quantising H counts with GEMM 2
+  s = cuda_status(launch_quantize_mx_e4m3(H, p.rows, p.h, hq, hs, (int)p.sh_ld, st));
+  if (s != MOE_OK) return s;
   GemmProblem g2{};
   g2.A = hq;
   g2.B = w->w_out_fp8;

@@ -547,7 +547,9 @@ def run_native(args):
         "stages_ms": stage_ms,
         "stages_note": "a separate pass over the same steps with events at the stage boundaries (they break the "
                        "launch overlap between kernels, so the stages add up to a little more than ms_per_step)"
-                       + ("; e4m3 experts: quantising x_routed counts in 'gather', quantising H in 'grouped_gemm2'"
+                       + ("; MXFP8 experts: quantising x_routed counts in 'gather', GEMM 1's epilogue quantises H"
+                          if spec.expert_fp8 == native.EXPERT_MXFP8 else
+                          "; e4m3 experts: quantising x_routed counts in 'gather', quantising H in 'grouped_gemm2'"
                           if spec.expert_fp8 else ""),
         "stages_gbs": {"values": stage_gbs, "bytes": stage_bytes,
                        "hbm_peak": peaks["hbm_gbs"], "note": "each stage's own minimum bytes"},

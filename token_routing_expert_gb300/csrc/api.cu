@@ -365,14 +365,13 @@ int run_experts_fp8(const moe_config_t* c, const moe_weights_t* w, const void* x
 }
 
 // The experts on MXFP8 operands: quantise x_routed in 32-value blocks, copy the code rows and
-// their scales in permuted order, GEMM 1 (block-scaled MMAs, SwiGLU epilogue) -> H bf16, quantise
-// H the same way, GEMM 2 -> Y bf16.
+// their scales in permuted order, GEMM 1 (block-scaled MMAs; the SwiGLU epilogue rounds H to bf16
+// and writes it as MXFP8 codes and scales), GEMM 2 -> Y bf16.
 int run_experts_mx(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
                    const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
                    cudaEvent_t* ev, bool tiles_ready) {
   (void)c;
   int32_t* tile_off = at<int32_t>(ws, p.tile_off);
-  void* H = at<void>(ws, p.H);
   void* xq = at<void>(ws, p.xq);
   void* xs = at<void>(ws, p.xs);
   void* hq = at<void>(ws, p.hq);
@@ -404,14 +403,14 @@ int run_experts_mx(const moe_config_t* c, const moe_weights_t* w, const void* xr
   g1.a_mx_ld = p.sx_ld;
   g1.b_mx_scale = w->w_up_gate_mx_scale;
   g1.b_mx_ld = p.sx_ld;
-  g1.out = H;
+  g1.mx_out_codes = hq;   // the SwiGLU epilogue quantises H itself: one 32-column chunk is one block
+  g1.mx_out_scale = hs;
+  g1.mx_out_ld = p.sh_ld;
   g1.ldo = p.h;
   g1.status = status;
   s = cuda_status(launch_gemm(g1, st));
   if (s != MOE_OK) return s;
-  mark(ev, 6, st);   // the stage of GEMM 1 alone; quantising H counts with GEMM 2
-  s = cuda_status(launch_quantize_mx_e4m3(H, p.rows, p.h, hq, hs, (int)p.sh_ld, st));
-  if (s != MOE_OK) return s;
+  mark(ev, 6, st);
   GemmProblem g2{};
   g2.A = hq;
   g2.B = w->w_out_fp8;
@@ -1110,7 +1109,8 @@ int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
   k += use_pair_tiles(p) ? 0 : 1;                // row gather for 128-row tiles (on CTA pairs grouped
                                                  // GEMM 1 gathers its rows)
   k += 2;                                        // grouped GEMM 1 (SwiGLU), grouped GEMM 2
-  if (c->expert_fp8) k += 2;                     // e4m3 quantisation of x_routed and of H
+  if (c->expert_fp8) k += p.mx ? 1 : 2;          // e4m3 quantisation of x_routed and of H (MXFP8: H is
+                                                 // quantised by GEMM 1's epilogue)
   k += 1;                                        // combine (+ RMSNorm when latent)
   if (p.latent) k += p.up_splits > 1 ? 2 : 1;    // latent up (+ split-K reduce)
   *n = k;

@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -452,6 +453,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+
+// One MXFP8 block (OCP microscaling, page "Как устроен Olmo-core 3", §"Rowwise FP8 и MXFP8"):
+// 32 bf16 values (16 words of pairs, element 2i in the low half of w[i]) share the scale
+// 2^(e - 127), e = floor(log2 amax) - 8 + 127 clamped to [0, 254] (e = 0 for an all-zero block);
+// code = e4m3(v * 2^(127 - e)), the product exact in fp32 (a power of two), nearest-even and
+// saturating.  Writes the 32 codes as 8 words (byte i of the block at byte i % 4 of word i / 4)
+// and returns e.
+__device__ __forceinline__ uint32_t mx_quantize_block(const uint32_t (&w)[16], uint32_t (&codes)[8]) {
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[i])), fabsf(bf16_hi(w[i]))));
+  const int eb = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
+  const int e = amax > 0.f ? max(0, eb - 8) : 0;
+  const float mul = __uint_as_float((uint32_t)(254 - e) << 23);   // 2^(127 - e)
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float2 lo = make_float2(bf16_lo(w[2 * i]) * mul, bf16_hi(w[2 * i]) * mul);
+    const float2 hi = make_float2(bf16_lo(w[2 * i + 1]) * mul, bf16_hi(w[2 * i + 1]) * mul);
+    const uint32_t a = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t c = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
+    codes[i] = (a & 0xFFFFu) | (c << 16);
+  }
+  return (uint32_t)e;
+}
 
 // SwiGLU backward of one element, in fp32 (page "Как устроен Olmo-core 3", §"SwiGLU с
 // квантизацией"): s = sigmoid(g), H = g s u, dU = dH g s, dG = dH u s (1 + g (1 - s)).

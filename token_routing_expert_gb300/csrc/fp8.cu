@@ -75,32 +75,16 @@ __global__ void __launch_bounds__(256) quantize_mx_e4m3_kernel(const uint4* __re
   if (b >= rows * nb) return;
   const long long r = b / nb;
   const int kb = (int)(b - r * nb);
-  uint4 v[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = x[b * 4 + i];
-  float amax = 0.f;
+  uint32_t w[16], out[8];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+    const uint4 v = x[b * 4 + i];
+    w[4 * i] = v.x;
+    w[4 * i + 1] = v.y;
+    w[4 * i + 2] = v.z;
+    w[4 * i + 3] = v.w;
   }
-  const int eb = (int)((__float_as_uint(amax) >> 23) & 0xFFu);
-  const int e = amax > 0.f ? max(0, eb - 8) : 0;
-  const float mul = __uint_as_float((uint32_t)(254 - e) << 23);   // 2^(127 - e)
-  uint32_t out[8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const float2 lo = make_float2(bf16_lo(w[2 * h]) * mul, bf16_hi(w[2 * h]) * mul);
-      const float2 hi = make_float2(bf16_lo(w[2 * h + 1]) * mul, bf16_hi(w[2 * h + 1]) * mul);
-      const uint32_t a = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
-      const uint32_t c = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
-      out[2 * i + h] = (a & 0xFFFFu) | (c << 16);
-    }
-  }
+  const uint32_t e = mx_quantize_block(w, out);
   q[b * 2] = make_uint4(out[0], out[1], out[2], out[3]);
   q[b * 2 + 1] = make_uint4(out[4], out[5], out[6], out[7]);
   scales[r * scale_ld + kb] = (uint8_t)e;

@@ -76,6 +76,9 @@ struct GemmParams {
   const uint8_t* mx_b_scale;   //   and of B's rows
   long long mx_b_ld;
   long long mx_b_rows;
+  uint8_t* mx_out_codes;       // MXFP8 SwiGLU: H leaves as MXFP8 codes (ldo bytes per row) and block
+  uint8_t* mx_out_scale;       //   scales (mx_out_ld bytes per row) instead of bf16
+  long long mx_out_ld;
   int* status;
 };
 
@@ -761,7 +764,9 @@ __device__ __forceinline__ void mx_load_scales(const GemmParams& p, const TileCo
 // MXFP8 epilogue of one tile for the 32 rows a warp owns.  The warp reads its whole share of
 // the accumulator (every other 32-column chunk) into registers, already converted (SwiGLU: 64 h
 // values, bf16 out: 128 values, packed in bf16 pairs), and releases the accumulator before its
-// global stores, so the next tile's MMAs run while this tile is written out.
+// global stores, so the next tile's MMAs run while this tile is written out.  With mx_out_codes
+// (SwiGLU), each thread's 32 h values of a chunk, rounded to bf16, are one MXFP8 block of its row:
+// they leave as 32 e4m3 codes and a scale byte, the next GEMM's A operand.
 template <int EPI>
 __device__ __forceinline__ void mx_store_tile(uint32_t tbase, const TileCoord& c, int row_in_tile,
                                               const GemmParams& p, int half, uint4* stg, uint64_t* tempty) {
@@ -802,6 +807,22 @@ __device__ __forceinline__ void mx_store_tile(uint32_t tbase, const TileCoord& c
   tc_fence_before();
   mbar_arrive(tempty);
   constexpr int out_cols = EPI == EPI_SWIGLU ? 128 : 256;   // output columns per tile
+  if (EPI == EPI_SWIGLU && p.mx_out_codes) {
+    const long long row = wrow0 + lane;
+#pragma unroll
+    for (int q = 0; q < CHUNKS; ++q) {
+      const int col0 = c.nt * out_cols + (half + 2 * q) * 32;
+      if (lane < valid && col0 < p.N) {
+        uint32_t codes[8];
+        const uint32_t e = mx_quantize_block(packed[q], codes);
+        uint4* dst = reinterpret_cast<uint4*>(p.mx_out_codes + row * p.ldo + col0);
+        dst[0] = make_uint4(codes[0], codes[1], codes[2], codes[3]);
+        dst[1] = make_uint4(codes[4], codes[5], codes[6], codes[7]);
+        p.mx_out_scale[row * p.mx_out_ld + col0 / 32] = (uint8_t)e;
+      }
+    }
+    return;
+  }
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo;
 #pragma unroll
   for (int q = 0; q < CHUNKS; ++q) {
@@ -1587,7 +1608,9 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
         q.b_mn_major || q.a_mn_major || q.a_off || q.preact || q.K <= 0 || q.K % 128 || !q.a_mx_scale ||
         !q.b_mx_scale || q.a_mx_ld % 16 || q.b_mx_ld % 16 || q.a_mx_ld < q.K / 32 || q.b_mx_ld < q.K / 32 ||
         (reinterpret_cast<uintptr_t>(q.a_mx_scale) & 15) || (reinterpret_cast<uintptr_t>(q.b_mx_scale) & 15) ||
-        (q.epilogue != EPI_SWIGLU && q.epilogue != EPI_BF16) || q.M < 0)
+        (q.epilogue != EPI_SWIGLU && q.epilogue != EPI_BF16) || q.M < 0 ||
+        (q.mx_out_codes && (q.epilogue != EPI_SWIGLU || !q.mx_out_scale || q.N % 32 || q.ldo % 16 ||
+                            (reinterpret_cast<uintptr_t>(q.mx_out_codes) & 15) || q.mx_out_ld < q.N / 32)))
       return cudaErrorInvalidValue;
     if (q.M == 0) return cudaSuccess;
     CUtensorMap ta, tb;
@@ -1615,6 +1638,9 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
     gp.mx_b_scale = static_cast<const uint8_t*>(q.b_mx_scale);
     gp.mx_b_ld = q.b_mx_ld;
     gp.mx_b_rows = q.b_rows_total;
+    gp.mx_out_codes = static_cast<uint8_t*>(q.mx_out_codes);
+    gp.mx_out_scale = static_cast<uint8_t*>(q.mx_out_scale);
+    gp.mx_out_ld = q.mx_out_ld;
     gp.status = q.status;
     int grid = num_sms();
     if (q.num_groups == 0) grid = std::min(grid, ((q.M + BM - 1) / BM) * gp.n_tiles);

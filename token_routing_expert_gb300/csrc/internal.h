@@ -72,6 +72,9 @@ struct GemmProblem {
   int64_t a_mx_ld;        // a multiple of 16, >= K / 32 (and both scale pointers 16-byte aligned)
   const void* b_mx_scale; // (b_rows_total, b_mx_ld) bytes
   int64_t b_mx_ld;
+  void* mx_out_codes;     // MXFP8 SwiGLU only, non-NULL: H is written as MXFP8 (codes (M, ldo) bytes, ldo a
+  void* mx_out_scale;     //   multiple of 16; scales (M, mx_out_ld) bytes) instead of bf16 to out
+  int64_t mx_out_ld;
   int* status;
 };
 

@@ -63,6 +63,11 @@ CASES = {
     "capacity": WorkloadSpec("capacity_mx", T=512, d_model=256, num_experts=8, top_k=2, hidden_size=128,
                              gating="softmax", skew=True, capacity_factor=1.0, expert_fp8=native.EXPERT_MXFP8,
                              seed=84),
+    # degenerate shapes: one token; one expert taking every row (several full tiles and a tail)
+    "one_token": WorkloadSpec("one_token_mx", T=1, d_model=256, num_experts=4, top_k=2, hidden_size=128,
+                              gating="softmax", expert_fp8=native.EXPERT_MXFP8, seed=86),
+    "single_expert": WorkloadSpec("single_expert_mx", T=700, d_model=384, num_experts=1, top_k=1, hidden_size=256,
+                                  gating="softmax", expert_fp8=native.EXPERT_MXFP8, seed=87),
 }
 
 

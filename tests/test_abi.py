@@ -88,6 +88,21 @@ def test_validate_config_codes(lib):
     c = native.make_config(256, 8, 2, 128)
     c.activation = 1
     assert native.moe_validate_config(c) == 2
+    # e4m3 expert modes: 0 bf16, 1 rowwise, 2 MXFP8; MXFP8 contracts 128-value k-tiles
+    assert native.moe_validate_config(native.make_config(256, 8, 2, 128, expert_fp8=native.EXPERT_MXFP8)) == 0
+    assert native.moe_validate_config(native.make_config(256, 8, 2, 128, expert_fp8=3)) == 1
+    assert native.moe_validate_config(native.make_config(256, 8, 2, 128, expert_fp8=-1)) == 1
+    for c in (native.make_config(192, 8, 2, 128, expert_fp8=native.EXPERT_MXFP8),   # d_model % 128
+              native.make_config(256, 8, 2, 192, expert_fp8=native.EXPERT_MXFP8),   # hidden % 128
+              native.make_config(256, 8, 2, 128, latent_dim=192, expert_fp8=native.EXPERT_MXFP8)):
+        assert native.moe_validate_config(c) == 2
+    assert native.moe_validate_config(native.make_config(192, 8, 2, 192, expert_fp8=native.EXPERT_FP8_ROWWISE)) == 0
+
+
+def test_mx_scale_rows():
+    # E8M0 scale rows: cols / 32 bytes, padded to 16 (a row's scales for four 128-value k-tiles are
+    # read as one 16-byte word)
+    assert [native.mx_scale_ld(c) for c in (32, 128, 512, 640, 1024, 2048, 7168)] == [16, 16, 16, 32, 32, 64, 224]
 
 
 @pytest.mark.parametrize("name", list(WORKLOADS))
@@ -104,6 +119,10 @@ def test_workspace_plan(lib, name):
     present = [o for o in lay if o >= 0]
     assert all(o % 256 == 0 and o < size for o in present)
     assert (lay[7] >= 0) == bool(spec.latent_dim) and (lay[9] >= 0) == bool(spec.latent_dim)
+    # MXFP8 experts: H and Y in bf16 plus the permuted code rows of x_routed and H's codes
+    if spec.routed_dim % 128 == 0 and spec.hidden_size % 128 == 0:
+        mx = native.moe_workspace_size(native.config_from_spec(spec.with_(expert_fp8=native.EXPERT_MXFP8)), spec.T)
+        assert mx >= R * (Lr + spec.hidden_size) * 3
 
 
 def test_host_errors_enqueue_nothing(lib):

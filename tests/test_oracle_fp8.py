@@ -102,3 +102,30 @@ def test_mx_experts_reduce_to_the_exact_experts_on_representable_inputs():
         want[lo:hi] = ref.dequantize_mx(*ref.quantize_mx_e4m3(h)) @ w[e][2].T
         h_exact[e] = h
     np.testing.assert_allclose(got, want, rtol=0, atol=0)
+
+
+def test_mx_experts_hand_computed_h_rounding():
+    """One token through one expert, every operand MX-representable and every value worked out by
+    hand.  x = (1, 1, 0, ...); gate rows 0, 1 give g = 32 + 32 = 64, where silu(64) = 64 exactly
+    in float64 (e^-64 is below half an ulp); up rows give u0 = 1 + 0.0625 and u1 = 2.  So
+    h = (68, 128, 0, ...), exact in bf16.  H's first block has amax 128 = 2^7, so its scale is
+    2^(7 - 8) = 1/2 and 68 / (1/2) = 136 lies halfway between the e4m3 neighbours 128 and 144: the
+    tie goes to the even code 128, and h0 comes back as 64.  W_out copies H's first two columns, so
+    the output is (64, 128, 0, ...) where the unquantised expert gives (68, 128, 0, ...)."""
+    D, h = 64, 32
+    cfg = ref.OracleConfig(d_model=D, num_experts=1, top_k=1, hidden_size=h)
+    x = np.zeros((1, D))
+    x[0, :2] = 1.0
+    w_up, w_gate, w_out = np.zeros((h, D)), np.zeros((h, D)), np.zeros((D, h))
+    w_up[0, :2] = [1.0, 0.0625]
+    w_up[1, 0] = 2.0
+    w_gate[0, :2] = w_gate[1, :2] = 32.0
+    w_out[0, 0] = w_out[1, 1] = 1.0
+    perm = ref.permute(np.array([[0]]), 1)
+    got = ref.expert_outputs_mxfp8(cfg, x, perm, lambda e: (w_up, w_gate, w_out))
+    want = np.zeros((1, D))
+    want[0, :2] = [64.0, 128.0]
+    np.testing.assert_array_equal(got, want)
+    exact = ref.expert_outputs(cfg, x, perm, lambda e: (w_up, w_gate, w_out))
+    assert exact[0, 0] == 68.0 and exact[0, 1] == 128.0
+

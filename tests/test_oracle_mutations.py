@@ -11,10 +11,12 @@ from tests import test_oracle_layer as L
 from tests import test_oracle_permute as P
 from tests import test_oracle_balance as B
 from tests import test_oracle_router as R
+from tests import test_oracle_fp8 as F
 
 _ORIG_PERMUTE = ref.permute
 _ORIG_GATE_SCORES = ref.gate_scores
 _ORIG_TOP_K = ref.top_k
+_ORIG_QUANTIZE_MX = ref.quantize_mx_e4m3
 
 
 def _silu_dropped(g):
@@ -96,6 +98,45 @@ def _imbalance_min_over_mean(counts):
     return float(c.min() / c.mean()) if c.mean() > 0 else float("nan")
 
 
+def _mx_offset_seven(x):
+    # wrong: scale exponent floor(log2 amax) - 7 (amax / scale in [128, 256))
+    x = np.asarray(x, np.float64)
+    rows, cols = x.shape
+    blocks = x.reshape(rows, cols // ref.MX_BLOCK, ref.MX_BLOCK)
+    amax = np.abs(blocks).max(axis=2)
+    e = np.zeros(amax.shape, np.int64)
+    nz = amax > 0
+    e[nz] = np.floor(np.log2(amax[nz])).astype(np.int64) - 7 + 127
+    e = np.clip(e, 0, 254)
+    codes = ref.round_e4m3(blocks / np.ldexp(1.0, e - 127)[:, :, None]).reshape(rows, cols)
+    return codes, e
+
+
+def _mx_one_scale_per_row(x):
+    # wrong: the whole row shares the scale of its largest block
+    codes, e = _ORIG_QUANTIZE_MX(x)
+    e_row = np.repeat(e.max(axis=1, keepdims=True), e.shape[1], axis=1)
+    x = np.asarray(x, np.float64)
+    rows, cols = x.shape
+    blocks = x.reshape(rows, cols // ref.MX_BLOCK, ref.MX_BLOCK)
+    codes = ref.round_e4m3(blocks / np.ldexp(1.0, e_row - 127)[:, :, None]).reshape(rows, cols)
+    return codes, e_row
+
+
+def _mx_experts_h_unquantised(cfg, x_routed, perm, expert):
+    # wrong: H goes to the down projection without its MXFP8 round trip
+    xd = ref.dequantize_mx(*ref.quantize_mx_e4m3(np.asarray(x_routed, np.float64)))
+    y = np.zeros((perm.gather_token.size, x_routed.shape[1]))
+    for e in range(cfg.num_experts):
+        lo, hi = int(perm.offsets[e]), int(perm.offsets[e + 1])
+        if hi == lo:
+            continue
+        wu, wg, wo = (ref.dequantize_mx(*ref.quantize_mx_e4m3(np.asarray(a, np.float64))) for a in expert(e))
+        rows = xd[perm.gather_token[lo:hi]]
+        y[lo:hi] = ref.round_bf16(ref.silu(rows @ wg.T) * (rows @ wu.T)) @ wo.T
+    return y
+
+
 CASES = [
     ("score_bias_update", _bias_update_wrong_sign, lambda: B.test_score_bias_update_hand_values()),
     ("load_imbalance", _imbalance_min_over_mean, lambda: B.test_load_imbalance_hand_values()),
@@ -109,6 +150,9 @@ CASES = [
     ("rms_norm", _rms_sum, lambda: L.test_rms_norm_matches_library()),
     ("normalise_and_scale", _scale_then_normalise, lambda: R.test_normalisation_and_scalings(ref.GATING_SIGMOID)),
     ("gate_scores", _no_epsilon_scores, lambda: R.test_sigmoid_scores_match_library_plus_epsilon()),
+    ("quantize_mx_e4m3", _mx_offset_seven, lambda: F.test_mx_quantiser_closed_forms()),
+    ("quantize_mx_e4m3", _mx_one_scale_per_row, lambda: F.test_mx_quantiser_saturates_and_bounds_the_error()),
+    ("expert_outputs_mxfp8", _mx_experts_h_unquantised, lambda: F.test_mx_experts_hand_computed_h_rounding()),
 ]
 
 

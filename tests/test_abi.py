@@ -139,6 +139,13 @@ def test_host_errors_enqueue_nothing(lib):
     # empty batch: nothing to do, and no device needed
     assert lib.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 16, 0, 32, None, 0, None) == 0
     assert native.load().moe_status_string(5) == b"device wait timed out"
+    # MXFP8 quantiser: shape errors are found on the host; no rows is a no-op
+    q = lib.moe_quantize_mxfp8
+    assert q(16, 4, 48, 32, 32, 16, None) == 1        # cols not a multiple of 32
+    assert q(16, 4, 64, 32, 32, 1, None) == 1         # scale_ld < cols / 32
+    assert q(16, -1, 64, 32, 32, 16, None) == 1       # negative rows
+    assert q(None, 4, 64, 32, 32, 16, None) == 1      # no input
+    assert q(None, 0, 64, None, None, 16, None) == 0  # empty
 
 
 def test_capacity_and_permuted_rows(lib):

@@ -479,7 +479,9 @@ int moe_workspace_layout(const moe_config_t* cfg, int64_t T, int64_t offsets_out
  * which every GPU that loads this library keeps until the process exits.
  * Limit: ceil(T * top_k / 4096) * num_experts <= 524288 (for 896 experts,
  * T * top_k up to about 2.39 million); larger calls, and capacity-mode
- * configurations, return MOE_ERR_UNSUPPORTED and enqueue nothing.
+ * configurations, return MOE_ERR_UNSUPPORTED and enqueue nothing.  Within the
+ * limit it splits the assignments into moe_permute's chunks when their
+ * histograms fit the array, else into chunks of 4096.
  * The first call on each device looks up the array's device address (a
  * runtime query, no allocation); make that first call before any stream
  * capture.  The call allocates and frees nothing.

@@ -665,6 +665,11 @@ def prepare_routed_input_backward(x: np.ndarray, w_down_latent: np.ndarray, dx_r
 # Reading: one float32 scale per row (amax / 448, the largest e4m3 value), the
 # row divided by it in float32 and rounded to e4m3 (nearest, ties to even,
 # saturating at 448); the GEMMs accumulate exactly and apply both rows' scales.
+# What is quantised: [Olmo-core 3, §"SwiGLU с квантизацией"] has the SwiGLU
+# forward produce the activation and, from it, its quantised representations,
+# so H is the activation in the input dtype (bf16) before it is quantised; and
+# the experts' input is the bf16 tensor the layer hands them (in the latent
+# case the dense down-projection's bf16 output).
 # --------------------------------------------------------------------------
 
 def _e4m3_positive_values() -> np.ndarray:

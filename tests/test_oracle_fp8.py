@@ -129,3 +129,78 @@ def test_mx_experts_hand_computed_h_rounding():
     exact = ref.expert_outputs(cfg, x, perm, lambda e: (w_up, w_gate, w_out))
     assert exact[0, 0] == 68.0 and exact[0, 1] == 128.0
 
+
+
+# ---------------------------------------------------------------------------
+# Rowwise FP8 experts.  Every value below is worked out by hand.  A row scale is amax / 448 in
+# float32; it is exact when amax = 7 * 2^m (448 = 7 * 2^6), so the rows are built that way.
+# ---------------------------------------------------------------------------
+
+def _fp8_hand_expert(D=64, h=32):
+    """x = (7, 4, 0, ...): scale 7 / 448 = 2^-6, codes (448, 256).  Gate rows 0, 1 = (7, 3.75):
+    scale 2^-6, codes (448, 240), g = 49 + 15 = 64, and silu(64) = 64 exactly in float64 (e^-64 is
+    below half an ulp of 1).  Up row 0 = (7/32, -15/128): scale 2^-11, codes (448, -240),
+    u0 = 49/32 - 15/32 = 17/16.  Up row 1 = (7/8, 7/32): scale 2^-9, codes (448, 112), u1 = 7.
+    So H = (68, 448, 0, ...), exact in bf16.  H's row amax 448 gives the row scale 1, and 68 lies
+    halfway between the e4m3 neighbours 64 and 72: the tie goes to the even code, 64.  W_out rows
+    0, 1 hold 7/8 in columns 0, 1 (scale 2^-9, code 448), so y = 7/8 * (64, 448) = (56, 392),
+    where the unquantised expert gives 7/8 * (68, 448) = (59.5, 392)."""
+    w_up, w_gate, w_out = np.zeros((h, D)), np.zeros((h, D)), np.zeros((D, h))
+    w_gate[0, :2] = w_gate[1, :2] = [7.0, 3.75]
+    w_up[0, :2] = [7.0 / 32, -15.0 / 128]
+    w_up[1, :2] = [7.0 / 8, 7.0 / 32]
+    w_out[0, 0] = w_out[1, 1] = 7.0 / 8
+    return w_up, w_gate, w_out
+
+
+def test_rowwise_expert_weights_round_trip_when_representable():
+    """quantize_expert_fp8 returns rows whose amax is 7 * 2^m and whose other entries are e4m3
+    codes times that row's scale unchanged; the scale belongs to the row, not the column."""
+    g = np.random.default_rng(6)
+    codes = ref._E4M3[ref._E4M3 <= 448]
+
+    def rows(n, cols):
+        c = g.choice(codes, size=(n, cols)) * g.choice([-1.0, 1.0], size=(n, cols))
+        c[np.arange(n), g.integers(0, cols, n)] = 448.0 * g.choice([-1.0, 1.0], size=n)   # each row's amax code
+        return c * 2.0 ** g.integers(-14, 2, size=(n, 1)) / 64.0                          # scale 2^m / 64
+    mats = (rows(16, 48), rows(16, 48), rows(48, 16))
+    for got, want in zip(ref.quantize_expert_fp8(*mats), mats):
+        np.testing.assert_array_equal(got, want)
+    _, s = ref.quantize_rowwise_e4m3(mats[0])
+    np.testing.assert_array_equal(s, np.abs(mats[0]).max(axis=1) / 448.0)
+
+
+def test_fp8_experts_hand_computed_h_tie():
+    cfg = ref.OracleConfig(d_model=64, num_experts=1, top_k=1, hidden_size=32)
+    x = np.zeros((1, 64))
+    x[0, :2] = [7.0, 4.0]
+    w = _fp8_hand_expert()
+    perm = ref.permute(np.array([[0]]), 1)
+    got = ref.expert_outputs_fp8(cfg, x, perm, lambda e: w)
+    want = np.zeros((1, 64))
+    want[0, :2] = [56.0, 392.0]
+    np.testing.assert_array_equal(got, want)
+    exact = ref.expert_outputs(cfg, x, perm, lambda e: w)
+    assert exact[0, 0] == 59.5 and exact[0, 1] == 392.0
+
+
+def test_fp8_latent_layer_hand_computed():
+    """The latent FP8 layer quantises the experts' bf16 input.  x = (1, 1, 0, ...) and W_down rows
+    (7, 2^-6, 0, ...), (4, 0, ...) give x_routed = (7 + 2^-6, 4): 7 + 2^-6 lies halfway between the
+    bf16 neighbours 7 and 7 + 2^-5 and goes to the even one, 7.  From there the expert above gives
+    (56, 392).  One expert with softmax gating has weight 1; with the norm off and W_up the
+    identity the layer output is z itself."""
+    D = L = 64
+    cfg = ref.OracleConfig(d_model=D, num_experts=1, top_k=1, hidden_size=32, latent_dim=L, up_proj_norm=False)
+    x = np.zeros((1, D))
+    x[0, :2] = 1.0
+    w_down = np.zeros((L, D))
+    w_down[0, :2] = [7.0, 2.0 ** -6]
+    w_down[1, 0] = 4.0
+    w = _fp8_hand_expert(D=L)
+    wts = ref.OracleWeights(w_router=np.zeros((1, D)), expert=lambda e: w, w_down_latent=w_down,
+                            w_up_latent=np.eye(D, L))
+    got = ref.layer_forward_fp8(cfg, x, wts)
+    want = np.zeros((1, D))
+    want[0, :2] = [56.0, 392.0]
+    np.testing.assert_array_equal(got, want)

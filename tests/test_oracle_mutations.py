@@ -137,6 +137,46 @@ def _mx_experts_h_unquantised(cfg, x_routed, perm, expert):
     return y
 
 
+_ORIG_QUANTIZE_ROWWISE = ref.quantize_rowwise_e4m3
+_ORIG_LAYER_FP8 = ref.layer_forward_fp8
+
+
+def _rowwise_per_column(x):
+    # wrong: one scale per column (amax over the rows) instead of one per row; returned as
+    # dequantised values with unit row scales so that callers multiply them back unchanged
+    x32 = np.asarray(x, np.float32)
+    amax = np.abs(x32).max(axis=0) if x32.size else np.zeros(x32.shape[1], np.float32)
+    scale = np.where(amax > 0, amax / np.float32(448.0), np.float32(1.0)).astype(np.float32)
+    codes = ref.round_e4m3((x32 / scale[None, :]).astype(np.float32))
+    return codes * scale.astype(np.float64)[None, :], np.ones(x32.shape[0], np.float32)
+
+
+def _fp8_experts_h_unquantised(cfg, x_routed, perm, expert):
+    # wrong: H goes to the down projection without its rowwise e4m3 round trip
+    xq, xs = ref.quantize_rowwise_e4m3(np.asarray(x_routed, np.float64))
+    xd = xq * xs.astype(np.float64)[:, None]
+    y = np.zeros((perm.gather_token.size, x_routed.shape[1]))
+    for e in range(cfg.num_experts):
+        lo, hi = int(perm.offsets[e]), int(perm.offsets[e + 1])
+        if hi == lo:
+            continue
+        wu, wg, wo = ref.quantize_expert_fp8(*(np.asarray(a, np.float64) for a in expert(e)))
+        rows = xd[perm.gather_token[lo:hi]]
+        y[lo:hi] = ref.round_bf16(ref.silu(rows @ wg.T) * (rows @ wu.T)) @ wo.T
+    return y
+
+
+def _fp8_layer_unrounded_latent_input(cfg, x, wts, forced_idx=None):
+    # wrong: the latent projection's output reaches the quantiser without its bf16 rounding
+    x = np.asarray(x, np.float64)
+    x_routed = ref.prepare_routed_input(cfg, x, wts.w_down_latent)
+    r = ref.route(cfg, x, wts.w_router, wts.b_router, wts.score_bias, forced_idx)
+    perm = ref.permute(r.idx, cfg.num_experts)
+    y = ref.expert_outputs_fp8(cfg, x_routed, perm, wts.expert)
+    z = ref.combine(y, perm.scatter_pos, r.weights)
+    return ref.restore_routed_output(cfg, z, wts.w_up_latent, wts.rms_weight)
+
+
 CASES = [
     ("score_bias_update", _bias_update_wrong_sign, lambda: B.test_score_bias_update_hand_values()),
     ("load_imbalance", _imbalance_min_over_mean, lambda: B.test_load_imbalance_hand_values()),
@@ -153,6 +193,11 @@ CASES = [
     ("quantize_mx_e4m3", _mx_offset_seven, lambda: F.test_mx_quantiser_closed_forms()),
     ("quantize_mx_e4m3", _mx_one_scale_per_row, lambda: F.test_mx_quantiser_saturates_and_bounds_the_error()),
     ("expert_outputs_mxfp8", _mx_experts_h_unquantised, lambda: F.test_mx_experts_hand_computed_h_rounding()),
+    ("quantize_rowwise_e4m3", _rowwise_per_column,
+     lambda: F.test_rowwise_expert_weights_round_trip_when_representable()),
+    ("quantize_rowwise_e4m3", _rowwise_per_column, lambda: F.test_fp8_experts_hand_computed_h_tie()),
+    ("expert_outputs_fp8", _fp8_experts_h_unquantised, lambda: F.test_fp8_experts_hand_computed_h_tie()),
+    ("layer_forward_fp8", _fp8_layer_unrounded_latent_input, lambda: F.test_fp8_latent_layer_hand_computed()),
 ]
 
 

@@ -1,5 +1,6 @@
 // C ABI of the MoE layer forward: argument checks, workspace plan, and the
 // order of kernel launches.  See include/moe.h for the contract.
+#include <atomic>
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -15,17 +16,21 @@ __device__ int g_status;
 namespace {
 
 constexpr int kMaxDevices = 64;
-int* g_status_ptr[kMaxDevices] = {nullptr};
+std::atomic<int*> g_status_ptr[kMaxDevices];
 
+// Device address of g_status on the current device, looked up once per device; concurrent first
+// calls store the same address.
 int* status_ptr() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  if (!g_status_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
-    g_status_ptr[dev] = static_cast<int*>(p);
+  int* p = g_status_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* q = nullptr;
+    if (cudaGetSymbolAddress(&q, g_status) != cudaSuccess) return nullptr;
+    p = static_cast<int*>(q);
+    g_status_ptr[dev].store(p, std::memory_order_release);
   }
-  return g_status_ptr[dev];
+  return p;
 }
 
 // Bound on the SM count used to size split-K buffers (the GPU's own count is

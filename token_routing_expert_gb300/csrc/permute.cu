@@ -11,6 +11,7 @@
 // chunk in order and ranks equal experts with __match_any_sync (the cluster kernel places the
 // same way).
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -473,20 +474,24 @@ static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
 
 namespace {
 constexpr int kMaxScratchDevices = 64;
-int32_t* g_permute_scratch_addr[kMaxScratchDevices] = {nullptr};
+std::atomic<int32_t*> g_permute_scratch_addr[kMaxScratchDevices];
 }  // namespace
 
 // Device address of g_permute_scratch on the current device, looked up once per
-// device (the host-side symbol is only a stand-in, never a device address).
+// device (the host-side symbol is only a stand-in, never a device address).  Two
+// host threads that make a device's first call at once both look it up and store
+// the same address.
 static int scratch_address(int32_t** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxScratchDevices) return MOE_ERR_NO_DEVICE;
-  if (!g_permute_scratch_addr[dev]) {
+  int32_t* p = g_permute_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_permute_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
-    g_permute_scratch_addr[dev] = static_cast<int32_t*>(ptr);
+    p = static_cast<int32_t*>(ptr);
+    g_permute_scratch_addr[dev].store(p, std::memory_order_release);
   }
-  *out = g_permute_scratch_addr[dev];
+  *out = p;
   return MOE_OK;
 }
 
@@ -502,9 +507,14 @@ extern "C" int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* idx, 
   if (T > 0 && (!idx || !gather_idx || !scatter_idx)) return MOE_ERR_INVALID_ARG;
   if (T * cfg->top_k > (int64_t)0x7fffffff - 128) return MOE_ERR_UNSUPPORTED;
   const int R = (int)(T * cfg->top_k);
-  // the histograms need one int per (chunk, expert): beyond the static array, refuse
-  const int64_t need = (int64_t)std::max(1, moe::permute_blocks(R, moe::kMaxChunk)) * cfg->num_experts;
+  const int64_t E = cfg->num_experts;
+  // the histograms need one int per (chunk, expert): with the largest chunks, beyond the
+  // static array, refuse; otherwise take moe_permute's own chunk size when its histograms fit
+  // (more, smaller chunks spread the passes over more SMs; the result does not depend on it)
+  const int64_t need = (int64_t)std::max(1, moe::permute_blocks(R, moe::kMaxChunk)) * E;
   if (need > moe::kNoAllocScratchInts) return MOE_ERR_UNSUPPORTED;
+  int chunk = moe::permute_chunk(R);
+  if ((int64_t)std::max(1, moe::permute_blocks(R, chunk)) * E > moe::kNoAllocScratchInts) chunk = moe::kMaxChunk;
   int32_t* scratch = nullptr;
   s = moe::scratch_address(&scratch);
   if (s != MOE_OK) return s;
@@ -512,7 +522,7 @@ extern "C" int moe_permute_noalloc(const moe_config_t* cfg, const int32_t* idx, 
   if (!status) return MOE_ERR_NO_DEVICE;
   // every histogram entry the scan reads is written by this call first: nothing to clear
   return moe::launch_permute(idx, R, cfg->num_experts, counts, offsets, gather_idx, scatter_idx, cfg->top_k,
-                             moe::kMaxChunk, scratch, status, (cudaStream_t)stream) == cudaSuccess
+                             chunk, scratch, status, (cudaStream_t)stream) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }

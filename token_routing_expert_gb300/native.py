@@ -319,6 +319,22 @@ def moe_router(cfg, weights: DeviceWeights, x, ws, logits=None, idx=None, w=None
     return logits, idx, w
 
 
+def _check_permute_outputs(cfg, idx, counts, offsets, gather_idx, scatter_idx, rows, what):
+    """The C ABI cannot see buffer sizes: undersized outputs would be written past their end."""
+    T = idx.shape[0]
+    if idx.dim() != 2 or idx.shape[1] != cfg.top_k:
+        raise ValueError(f"{what}: idx must be (T, top_k={cfg.top_k}), got {tuple(idx.shape)}")
+    E, R = cfg.num_experts, T * cfg.top_k
+    for name, t, n in (("counts", counts, E), ("offsets", offsets, E + 1), ("gather_idx", gather_idx, rows),
+                       ("scatter_idx", scatter_idx, R)):
+        if t.numel() < n:
+            raise ValueError(f"{what}: {name} holds {t.numel()} entries, needs {n}")
+        if t.device != idx.device:
+            raise ValueError(f"{what}: {name} is on {t.device}, idx on {idx.device}")
+    if idx.is_cuda and idx.device.index != torch.cuda.current_device():
+        raise ValueError(f"{what}: tensors are on {idx.device}, the current device is cuda:{torch.cuda.current_device()}")
+
+
 def moe_permute(cfg, idx, ws, counts=None, offsets=None, gather_idx=None, scatter_idx=None, stream=None):
     T = idx.shape[0]
     R = T * cfg.top_k
@@ -329,6 +345,7 @@ def moe_permute(cfg, idx, ws, counts=None, offsets=None, gather_idx=None, scatte
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if offsets is None else offsets
     gather_idx = torch.empty(max(rows, 1), dtype=torch.int32, device=dev) if gather_idx is None else gather_idx
     scatter_idx = torch.empty(max(R, 1), dtype=torch.int32, device=dev) if scatter_idx is None else scatter_idx
+    _check_permute_outputs(cfg, idx, counts, offsets, gather_idx, scatter_idx, rows, "moe_permute")
     _check(load().moe_permute(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"), T,
                               _ptr(counts, torch.int32, "counts"), _ptr(offsets, torch.int32, "offsets"),
                               _ptr(gather_idx, torch.int32, "gather_idx"), _ptr(scatter_idx, torch.int32, "scatter_idx"),
@@ -339,6 +356,7 @@ def moe_permute(cfg, idx, ws, counts=None, offsets=None, gather_idx=None, scatte
 def moe_permute_noalloc(cfg, idx, counts, offsets, gather_idx, scatter_idx, stream=None):
     """moe_permute with no workspace (the library's static scratch); outputs are the caller's tensors."""
     T = idx.shape[0]
+    _check_permute_outputs(cfg, idx, counts, offsets, gather_idx, scatter_idx, T * cfg.top_k, "moe_permute_noalloc")
     _check(load().moe_permute_noalloc(ctypes.byref(cfg), _ptr(idx, torch.int32, "idx"), T,
                                       _ptr(counts, torch.int32, "counts"), _ptr(offsets, torch.int32, "offsets"),
                                       _ptr(gather_idx, torch.int32, "gather_idx"),

@@ -6,8 +6,11 @@
 A step is one moe_layer_forward (latent down-projection, router GEMM, top-k,
 permutation, grouped SwiGLU GEMMs, combine, RMSNorm + up-projection) over
 one batch of T synthetic tokens resident in HBM.  The default workload is
-the OlmoE-shaped layer (T=8192, d_model=2048, 64 experts, top-8, hidden
-1024, topk_softmax gating).  With N > 1 (torchrun), every rank runs its own
+the largest one, the skewed latent ultra-sparse prefill (T=32768,
+d_model=7168, latent_dim=2048, 896 experts, top-8, hidden 1024, sigmoid
+gating), which runs every step of the path.  The same invocation also times
+the latent decode batch (T=64, the same layer shape, bound by HBM) and
+reports it in the line's ``decode`` object.  With N > 1 (torchrun), every rank runs its own
 replica on its own batch: tokens are independent, so there is no collective
 on the data path (weak scaling); the barrier and the max over ranks are the
 only communication.
@@ -218,7 +221,11 @@ def run_reference(args):
         return
     spec = W.WORKLOADS[args.config]
     inp = W.generate(spec)
-    n = min(spec.T, args.ref_tokens)
+    # each step is a bounded sample: as many tokens (up to --ref-tokens) as keep the K timed
+    # steps near --ref-seconds, from the rate of a short calibration call
+    probe = min(spec.T, 8)
+    rate, _, _ = oracle_sample_rate(spec, inp, probe, 0.0, max_reps=1)
+    n = int(max(1, min(spec.T, args.ref_tokens, rate * args.ref_seconds / max(args.steps, 1))))
     for _ in range(args.warmup):
         oracle_sample_rate(spec, inp, n, 0.0, max_reps=1)
     rates = []
@@ -239,6 +246,53 @@ def run_reference(args):
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
+
+
+def decode_pass(args, native, name, peaks, dist):
+    """Times the decode-shaped workload (bound by HBM) in the same invocation: K plain forwards,
+    CUDA events on the launching stream; returns the line's ``decode`` object."""
+    spec = W.WORKLOADS[name]
+    inp = W.generate(spec)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp)
+    x = inp["x"].cuda()
+    ws = native.workspace(cfg, spec.T)
+    out = torch.empty((spec.T, spec.d_model), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(args.warmup, 1)):
+        native.moe_layer_forward(cfg, wts, x, ws, out=out)
+    torch.cuda.synchronize()
+    if native.moe_get_status() != 0:
+        raise SystemExit("device status error in the decode warm-up")
+    touched = int((native.layer_intermediates(cfg, spec.T, ws)["counts"] > 0).sum().item())
+    alg_bytes = W.algorithmic_bytes(spec, touched)
+    L2 = torch.cuda.get_device_properties(torch.cuda.current_device()).L2_cache_size
+    flush = alg_bytes < 2 * L2
+    flush_buf = torch.empty(2 * L2 // 4 + 1024, dtype=torch.float32, device="cuda") if flush else None
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        if flush:
+            flush_buf.fill_(float(i))
+        ev[i][0].record(stream)
+        native.moe_layer_forward(cfg, wts, x, ws, out=out)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if native.moe_get_status() != 0:
+        raise SystemExit("device status error in the decode pass")
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev) / args.steps, dist, "cuda")
+    gbs = alg_bytes / (ms * 1e-3) / 1e9
+    flops = W.algorithmic_flops(spec)
+    roof_ms = 1e3 * max(alg_bytes / (peaks["hbm_gbs"] * 1e9), flops / (peaks["bf16_tflops"] * 1e12))
+    del wts, ws, x, out, flush_buf
+    torch.cuda.empty_cache()
+    return {"workload": workload_desc(spec), "ms_per_step": ms, "tokens_per_s": spec.T / (ms * 1e-3),
+            "gbs": gbs, "hbm_peak": peaks["hbm_gbs"], "frac_hbm_peak": gbs / peaks["hbm_gbs"],
+            "bound": "hbm", "roofline_ms": roof_ms, "frac_of_roofline": roof_ms / ms,
+            "experts_touched": touched, "algorithmic_bytes": alg_bytes, "algorithmic_flops": flops,
+            "steps": args.steps, "l2": "flushed between steps" if flush else "no flush (bytes per step > 2x L2)",
+            "note": "algorithmic bytes = touched expert weights + router + latent weights + x + out, each once; "
+                    "events around each forward"}
 
 
 def run_native(args):
@@ -484,6 +538,10 @@ def run_native(args):
     bal["bound"] = f"launch latency ({spec.num_experts} counters)"
 
     peaks, peak_kind = read_peaks()
+    decode = None
+    if args.decode_config and args.decode_config != spec.name and args.tokens == 0 and not (
+            spec.expert_fp8 or spec.capacity_factor):
+        decode = decode_pass(args, native, args.decode_config, peaks, dist)
     flops = W.algorithmic_flops(spec)
     dropped = 0
     if spec.capacity_factor > 0:
@@ -555,6 +613,7 @@ def run_native(args):
                        "hbm_peak": peaks["hbm_gbs"], "note": "each stage's own minimum bytes"},
         "balance": bal,
         "backward": bwd,
+        "decode": decode,
         "roofline": {"kernel": "grouped GEMM 1 (SwiGLU fused, tcgen05" + (
                      ", MXFP8 block-scaled operands)" if spec.expert_fp8 == native.EXPERT_MXFP8 else
                      ", e4m3 operands)" if spec.expert_fp8 else ")"),
@@ -584,13 +643,17 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", default="olmoe", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--config", default="latent_prefill", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--decode-config", default="latent_decode",
+                    help="decode-shaped workload timed in the same run ('' to skip)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per step instead of the workload's own T (for small profiling captures)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--capacity-factor", type=float, default=0.0,
                     help="> 0: capacity-limited experts (dropping); default dropless")
-    ap.add_argument("--ref-tokens", type=int, default=256, help="oracle tokens per step (reference arm)")
+    ap.add_argument("--ref-tokens", type=int, default=256, help="at most this many oracle tokens per step (reference arm)")
+    ap.add_argument("--ref-seconds", type=float, default=60.0,
+                    help="reference arm: per-step sample sized so the K timed steps take about this long")
     ap.add_argument("--cpu-tokens", type=int, default=512, help="oracle sample for the cpu_baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -5,7 +5,10 @@ All tokens: top-k indices against the float64 router (near-tie rule) and the
 permutation, counts and offsets bit-exact against the oracle's counting sort
 of the GPU's indices.  Sampled tokens: the layer output against the float64
 oracle run on those tokens alone (tokens are independent), with the GPU's
-choice adopted for near-tie tokens.
+choice adopted for near-tie tokens.  The sample is 96 random tokens plus,
+for each of the 16 least-loaded experts that received any token, its first
+and last 8 tokens: those experts' rows sit in mostly empty tail tiles of
+the grouped GEMMs, which a random sample of a skewed load rarely reaches.
 """
 import numpy as np
 import pytest
@@ -19,6 +22,20 @@ from token_routing_expert_gb300.workloads import WORKLOADS, generate
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
 SAMPLE = 96
+COLD_EXPERTS = 16
+COLD_TOKENS = 8     # first and last this many tokens of each cold expert
+
+
+def cold_expert_tokens(idx: np.ndarray, counts: np.ndarray) -> np.ndarray:
+    """Tokens routed to the least-loaded experts that received any token (first and last few each)."""
+    touched = np.nonzero(counts > 0)[0]
+    cold = touched[np.argsort(counts[touched], kind="stable")[:COLD_EXPERTS]]
+    toks = []
+    for e in cold:
+        t = np.nonzero((idx == e).any(axis=1))[0]
+        toks.append(t[:COLD_TOKENS])
+        toks.append(t[-COLD_TOKENS:])
+    return np.unique(np.concatenate(toks)) if toks else np.zeros(0, np.int64)
 
 
 @pytest.mark.parametrize("name", ["olmoe", "sigmoid_wide", "latent_prefill", "latent_decode"])
@@ -51,7 +68,8 @@ def test_full_size_workload(name):
     np.testing.assert_array_equal(gather, p.gather_token)
     np.testing.assert_array_equal(scatter, p.scatter_pos)
 
-    sample = np.sort(np.random.default_rng(1234).choice(T, size=min(SAMPLE, T), replace=False))
+    sample = np.random.default_rng(1234).choice(T, size=min(SAMPLE, T), replace=False)
+    sample = np.union1d(sample, cold_expert_tokens(gi, counts))
     forced = r.idx[sample].copy()
     forced[mism[sample]] = gi[sample][mism[sample]]
     res = ref.layer_forward(oc, f64(inp["x"][torch.from_numpy(sample)]), ow, forced_idx=forced)

@@ -317,6 +317,8 @@ def run_native(args):
     spec = W.WORKLOADS[args.config]
     if args.tokens > 0:
         spec = spec.with_(T=args.tokens)
+    if args.experts > 0:
+        spec = spec.with_(num_experts=args.experts)
     if args.capacity_factor > 0:
         spec = spec.with_(capacity_factor=args.capacity_factor)
     if args.fp8:
@@ -539,7 +541,7 @@ def run_native(args):
 
     peaks, peak_kind = read_peaks()
     decode = None
-    if args.decode_config and args.decode_config != spec.name and args.tokens == 0 and not (
+    if args.decode_config and args.decode_config != spec.name and args.tokens == 0 and args.experts == 0 and not (
             spec.expert_fp8 or spec.capacity_factor):
         decode = decode_pass(args, native, args.decode_config, peaks, dist)
     flops = W.algorithmic_flops(spec)
@@ -619,7 +621,8 @@ def run_native(args):
                      ", e4m3 operands)" if spec.expert_fp8 else ")"),
                      "bound": "tensor", "achieved": achieved, "peak": gemm_peak, "unit": "TFLOP/s",
                      "frac": achieved / gemm_peak,
-                     "traffic": None if spec.expert_fp8 or spec.capacity_factor else kernel_traffic(spec.name),
+                     "traffic": (None if spec.expert_fp8 or spec.capacity_factor or args.tokens or args.experts
+                                 else kernel_traffic(spec.name)),
                      "peak_source": gemm_label},
         "e2e": {"value": job_tokens_per_s(world, T, e2e_ms), "unit": "tokens/s",
                 "h2d_bytes_per_step": x_host.numel() * 2, "d2h_bytes_per_step": out_hosts[0].numel() * 2,
@@ -648,6 +651,8 @@ def main():
                     help="decode-shaped workload timed in the same run ('' to skip)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="tokens per step instead of the workload's own T (for small profiling captures)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="number of experts instead of the workload's own (for small profiling captures)")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--capacity-factor", type=float, default=0.0,
                     help="> 0: capacity-limited experts (dropping); default dropless")

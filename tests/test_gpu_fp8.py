@@ -6,8 +6,8 @@ import pytest
 import torch
 
 from oracle import moe_ref as ref
-from tests.oracle_bridge import (assert_close_fp8_layer, assert_close_layer, check_topk, f64, fp8_ambiguous_tokens,
-                                 oracle_config, oracle_weights, output_scale)
+from tests.oracle_bridge import (assert_close_fp8_layer, assert_close_layer, assert_close_relative, check_topk, f64,
+                                 fp8_ambiguous_tokens, oracle_config, oracle_weights)
 from tests.test_gpu_parity import DESIGNED_COUNTS, designed_routing
 from token_routing_expert_gb300 import native
 from token_routing_expert_gb300.workloads import WorkloadSpec, generate
@@ -57,7 +57,7 @@ def test_fp8_layer_forward(name):
     want = ref.layer_forward_fp8(oc, f64(inp["x"]), ow, forced_idx=forced)
     got = out.double().cpu().numpy()
     amb = fp8_ambiguous_tokens(oc, ow, f64(inp["x"]), forced)
-    assert_close_fp8_layer(got, want, amb, "fp8 layer output", output_scale(spec), latent=bool(spec.latent_dim))
+    assert_close_fp8_layer(got, want, amb, "fp8 layer output", latent=bool(spec.latent_dim))
     # and the FP8 layer stays close to the bf16 one (e4m3 keeps 3 mantissa bits)
     dense = ref.layer_forward(oc, f64(inp["x"]), ow, forced_idx=forced).out
     assert np.linalg.norm(got - dense) / np.linalg.norm(dense) < 0.1
@@ -111,4 +111,4 @@ def test_fp8_preact():
         wu, wg, _ = ref.quantize_expert_fp8(*ow.expert(e))
         rows = xd[gat[lo:hi]]
         want = np.concatenate([rows @ wu.T, rows @ wg.T], axis=1)
-        assert_close_layer(pre[lo:hi], want, f"fp8 preact[{e}]", float(np.abs(want).max()))
+        assert_close_relative(pre[lo:hi], want, f"fp8 preact[{e}]")

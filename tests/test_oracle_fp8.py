@@ -204,3 +204,16 @@ def test_fp8_latent_layer_hand_computed():
     want = np.zeros((1, D))
     want[0, :2] = [56.0, 392.0]
     np.testing.assert_array_equal(got, want)
+
+
+def test_bf16_half_ulp_bound_is_the_rounding_error():
+    """half_ulp_bf16 bounds |v - bf16(v)| and is reached at rounding midpoints (the parity bar's
+    allowance for a bf16 output's own rounding)."""
+    from tests.oracle_bridge import half_ulp_bf16
+    v = np.random.default_rng(7).standard_normal(50000) * np.exp(np.random.default_rng(8).uniform(-20, 20, 50000))
+    v = v.astype(np.float32).astype(np.float64)    # a GPU result is rounded to bf16 from float32
+    assert (np.abs(ref.round_bf16(v) - v) <= half_ulp_bf16(v)).all()
+    mid = np.array([1.0 + 2.0 ** -8, 8.0 + 2.0 ** -5, -(4.0 + 2.0 ** -6)])       # halfway between bf16 neighbours
+    np.testing.assert_array_equal(np.abs(ref.round_bf16(mid) - mid), half_ulp_bf16(mid))
+    np.testing.assert_array_equal(half_ulp_bf16(np.array([0.0, 1.0, 7.99, 8.0, 15.9])),
+                                  [0.0, 2.0 ** -8, 2.0 ** -6, 2.0 ** -5, 2.0 ** -5])

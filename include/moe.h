@@ -466,6 +466,17 @@ int moe_score_bias_update(int64_t* accum, int32_t num_experts, float bias_gamma,
  * [9] z or normalised z (T, L') bf16 (latent only, else -1). */
 int moe_workspace_layout(const moe_config_t* cfg, int64_t T, int64_t offsets_out[10]);
 
+/* Whether moe_layer_forward keeps the experts' rows y (offset [8] above) in fp32 instead of bf16
+ * for this configuration: *is_fp32 = 1 when the layer is not latent, its experts are bf16, and
+ * its routing weights can add up to more than one per token (sigmoid gating without a p-norm,
+ * a p-norm with p > 1, restore_weight_scale, expert_weight_scale or original_top_k).  The
+ * combine multiplies y's rounding error by up to that sum, and bf16 y would then put more error
+ * into the bf16 output than the output's own rounding.  The page's experts return bf16
+ * (section "Вычисления экспертов и точность"); this is a deviation toward more precision.
+ * moe_layer_forward_preact (the training forward) always keeps y in bf16, which the backward
+ * reads; the workspace reserves 4 bytes per value of y whenever *is_fp32 is 1. */
+int moe_layer_expert_rows_fp32(const moe_config_t* cfg, int32_t* is_fp32);
+
 /*
  * moe_permute without a workspace: for callers that may not allocate device
  * memory at all.  The page has no counterpart; this is a library convenience.

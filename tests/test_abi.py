@@ -158,3 +158,21 @@ def test_capacity_and_permuted_rows(lib):
     assert native.moe_permuted_rows(native.make_config(256, 8, 2, 128), 96) == 192
     assert native.moe_permuted_rows(native.make_config(256, 8, 2, 128, capacity_factor=1.0), 100) == 8 * 32
     assert native.moe_validate_config(native.make_config(256, 8, 2, 128, capacity_factor=-1.0)) == 1
+
+
+def test_fp32_expert_rows_follow_the_weight_sum(lib):
+    """moe_layer_expert_rows_fp32: fp32 y exactly when a non-latent bf16 layer's routing weights can
+    add up to more than one per token."""
+    f = native.moe_layer_expert_rows_fp32
+    assert f(native.config_from_spec(WORKLOADS["sigmoid_wide"]))          # L1 then x 8
+    assert not f(native.config_from_spec(WORKLOADS["olmoe"]))             # topk_softmax: sums to 1
+    assert not f(native.config_from_spec(WORKLOADS["tiny"]))              # softmax, L1
+    assert not f(native.config_from_spec(WORKLOADS["latent_prefill"]))    # latent: z is normalised
+    assert not f(native.config_from_spec(WORKLOADS["sigmoid_wide"].with_(expert_fp8=1)))
+    assert f(native.make_config(64, 16, 4, 64, gating="sigmoid"))        # sigmoid scores add up to 4
+    assert f(native.make_config(64, 16, 4, 64, gating="softmax", normalize_expert_weights=2.0))   # up to 2
+    assert not f(native.make_config(64, 16, 4, 64, gating="softmax", normalize_expert_weights=1.0))
+    assert f(native.make_config(64, 16, 4, 64, gating="softmax", expert_weight_scale=1.5))
+    assert not f(native.make_config(64, 16, 4, 64, gating="softmax", expert_weight_scale=0.5))
+    assert f(native.make_config(64, 16, 4, 64, gating="topk_softmax", original_top_k=8))
+    assert not f(native.make_config(64, 16, 1, 64, gating="sigmoid"))    # one sigmoid score: at most 1 + eps

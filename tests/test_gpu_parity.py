@@ -19,7 +19,7 @@ import pytest
 import torch
 
 from oracle import moe_ref as ref
-from tests.oracle_bridge import assert_close_layer, check_topk, f64, oracle_config, oracle_weights
+from tests.oracle_bridge import assert_close_layer, check_topk, f64, half_ulp_bf16, oracle_config, oracle_weights
 from token_routing_expert_gb300 import native
 from token_routing_expert_gb300.workloads import WORKLOADS, WorkloadSpec, generate
 
@@ -52,6 +52,10 @@ CASES = {
                                gating="topk_softmax", seed=20),
     "pair_tiles_ragged_h": WorkloadSpec("pair_tiles_ragged_h", T=2500, d_model=512, num_experts=8, top_k=2,
                                         hidden_size=320, gating="sigmoid", normalize_expert_weights=1.0, seed=21),
+    # CTA pairs with the weights restored x top_k: the inference forward keeps fp32 expert rows
+    "pair_tiles_restore": WorkloadSpec("pair_tiles_restore", T=3000, d_model=512, num_experts=8, top_k=4,
+                                       hidden_size=256, gating="sigmoid", normalize_expert_weights=1.0,
+                                       restore_weight_scale=True, seed=25),
     "pair_tiles_latent": WorkloadSpec("pair_tiles_latent", T=2000, d_model=768, num_experts=4, top_k=2,
                                       hidden_size=192, latent_dim=256, gating="softmax", skew=True, seed=22),
     # >= 1024 tokens and > 128 experts: the router GEMM runs on CTA pairs with 256-column fp32
@@ -212,6 +216,52 @@ def test_grouped_swiglu_designed_counts():
     assert_close_layer(y.double().cpu().numpy(), want, "grouped swiglu, designed counts")
 
 
+# Group sizes around the narrow-tile bound (a group's last CTA-pair tile with <= 128 rows runs with
+# the tile's rows as the MMA's N, rounded up to 32): tails of 1, 16, 31, 32, 33, ... rows next to
+# full 256-row tiles, empty groups, and enough rows in all (>= 192 per expert) for the CTA-pair path.
+NARROW_COUNTS = [1, 16, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 200, 255, 256, 257, 0, 300, 383, 384, 385,
+                 513, 640, 1000, 1301]
+
+
+@pytest.mark.parametrize("h", [192, 320])
+def test_grouped_swiglu_narrow_tails(h):
+    E = len(NARROW_COUNTS)
+    spec = WorkloadSpec("narrow_tails", T=sum(NARROW_COUNTS), d_model=256, num_experts=E, top_k=1, hidden_size=h,
+                        gating="softmax", seed=33 + h)
+    assert spec.rows >= 192 * E                                   # the CTA-pair path
+    inp = generate(spec)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp)
+    ws = native.workspace(cfg, spec.T)
+    counts, offsets, gather, scatter = native.moe_permute(cfg, designed_routing(NARROW_COUNTS, 9), ws)
+    assert counts.cpu().tolist() == NARROW_COUNTS
+    xr = torch.from_numpy(np.random.default_rng(h).standard_normal((spec.T, spec.d_model), dtype=np.float32)).to(
+        torch.bfloat16)
+    y = native.moe_grouped_swiglu(cfg, wts, xr.cuda(), gather, offsets, ws)
+    expect_ok()
+    perm = ref.Permutation(counts.cpu().numpy(), offsets.cpu().numpy(), gather.cpu().numpy(), scatter.cpu().numpy())
+    ow = oracle_weights(spec, inp)
+    want = ref.expert_outputs(oracle_config(spec), f64(xr), perm, ow.expert)
+    got = y.double().cpu().numpy()
+    off = offsets.cpu().numpy()
+    for e, n in enumerate(NARROW_COUNTS):                        # every group on its own, tails included
+        if n:
+            assert_close_layer(got[off[e]:off[e + 1]], want[off[e]:off[e + 1]], f"narrow tails, expert {e} ({n} rows)")
+    # the training forward's kept pre-activations take the same tiles
+    pre = torch.empty((spec.rows, 2 * h), dtype=torch.bfloat16, device="cuda")
+    y2, _ = native.moe_grouped_swiglu_preact(cfg, wts, xr.cuda(), gather, offsets, ws, preact=pre)
+    expect_ok()
+    assert torch.equal(y2, y)
+    x_np, g_np = f64(xr), gather.cpu().numpy()
+    pre_np = pre.double().cpu().numpy()
+    for e, n in enumerate(NARROW_COUNTS):
+        if n:
+            w_up, w_gate, _ = ow.expert(e)
+            rows = x_np[g_np[off[e]:off[e + 1]]]
+            assert_close_layer(pre_np[off[e]:off[e + 1]], np.concatenate([rows @ w_up.T, rows @ w_gate.T], axis=1),
+                               f"narrow tails, pre-activations of expert {e}")
+
+
 @pytest.mark.parametrize("name", ["tiny", "sigmoid_bias_restore", "latent_skew", "max_experts", "one_token",
                                   "pair_tiles"])
 def test_combine(name):
@@ -274,6 +324,35 @@ def run_layer_and_compare(spec, inp, cfg, wts):
 def test_layer_forward(name):
     spec, inp, cfg, wts = setup(name)
     run_layer_and_compare(spec, inp, cfg, wts)
+
+
+@pytest.mark.parametrize("name", ["sigmoid_bias_restore", "softmax_p2_scales", "router_pair", "pair_tiles_restore"])
+def test_inference_forward_keeps_fp32_expert_rows(name):
+    """Layers whose routing weights can add up to more than one keep y in fp32 in the inference
+    forward: its rows round to the training forward's bf16 rows bit for bit (the same fp32 products),
+    and the output error beyond its own bf16 rounding stays far under the bar."""
+    spec, inp, cfg, wts = setup(name)
+    assert native.moe_layer_expert_rows_fp32(cfg)
+    T = spec.T
+    x = inp["x"].cuda()
+    ws = native.workspace(cfg, T)
+    out = native.moe_layer_forward(cfg, wts, x, ws)
+    expect_ok()
+    y32 = native.layer_intermediates(cfg, T, ws)["y_f32"].clone()
+    native.moe_layer_forward_preact(cfg, wts, x, ws)
+    expect_ok()
+    y16 = native.layer_intermediates(cfg, T, ws)["y"]
+    assert torch.equal(y32.to(torch.bfloat16), y16)
+    oc, ow = oracle_config(spec), oracle_weights(spec, inp)
+    gi = native.layer_intermediates(cfg, T, ws)["idx"].cpu().numpy().astype(np.int64)
+    r = ref.route(oc, f64(inp["x"]), ow.w_router, ow.b_router, ow.score_bias)
+    mism = check_topk(gi, r.keys, r.idx, spec.top_k)
+    forced = r.idx.copy()
+    forced[mism] = gi[mism]
+    want = ref.layer_forward(oc, f64(inp["x"]), ow, forced_idx=forced).out
+    got = out.double().cpu().numpy()
+    excess = (np.abs(got - want) - half_ulp_bf16(want)).max()
+    assert excess <= 2e-3, f"{name}: error beyond the output's half-ulp {excess:.3e}"
 
 
 def test_layer_forward_repeatable_and_stream_ordered():

@@ -57,6 +57,7 @@ struct Plan {
   int64_t sx_ld, sh_ld;   // MXFP8: bytes of block scales per row of x_routed / of H
   int D, E, k, h, L, Lr;   // Lr: routed dim (L or D)
   bool latent;
+  bool y32;           // the inference forward's expert rows y are fp32 (fp32_expert_rows)
   int router_bn, n_router_tiles;
   int router_splits, down_splits, up_splits;
   int64_t logit_slice;
@@ -73,13 +74,40 @@ int64_t capacity_of(const moe_config_t* c, int64_t T) {
   return 8 * (int64_t)std::ceil(x / 8.0);
 }
 
+// Bytes of MXFP8 block scales per row of `cols` values: cols / 32, rounded up to 16.
+int64_t mx_scale_ld(int64_t cols) { return (cols / 32 + 15) / 16 * 16; }
+
+// Upper bound of sum_j |w[t, j]| over a token's routing weights, from the gating and the
+// scalings: softmax probabilities sum to at most 1, sigmoid scores to k (1 + eps); a p-norm
+// normalisation leaves at most k^(1 - 1/p) (p >= 1); restore_weight_scale multiplies by k,
+// expert_weight_scale by |s|, original_top_k by sqrt(k0 / k).
+double weight_sum_bound(const moe_config_t* c) {
+  const double k = c->top_k;
+  double s = c->gating == MOE_GATING_SIGMOID ? k * (1.0 + std::fabs((double)c->sigmoid_stability_epsilon)) : 1.0;
+  const double pn = c->normalize_expert_weights;
+  if (pn > 0) s = pn >= 1.0 ? std::pow(k, 1.0 - 1.0 / pn) : 1.0;
+  if (c->restore_weight_scale) s *= k;
+  if (c->expert_weight_scale != 0.f) s *= std::fabs((double)c->expert_weight_scale);
+  if (c->original_top_k > 0 && c->original_top_k != c->top_k) s *= std::sqrt((double)c->original_top_k / k);
+  return s;
+}
+
+// The inference forward keeps the expert rows y in fp32 when the combine can magnify their
+// rounding: a bf16 y carries a relative error up to 2^-9, the combine multiplies it by up to the
+// weights' sum, and a layer whose weights can add up to more than one would then carry more error
+// into its bf16 output than that output's own rounding (sigmoid-gated, L1-normalised weights
+// restored x 8: 3.2e-2 from bf16 y alone at |out| ~ 15).  A latent layer normalises z before its
+// output and keeps bf16 y, as do the e4m3 experts and the training forward (whose kept bf16 y the
+// backward reads).
+bool fp32_expert_rows(const moe_config_t* c) {
+  return c->latent_dim == 0 && !c->expert_fp8 && weight_sum_bound(c) > 1.0 + 1e-6;
+}
+
 // Groups averaging >= 192 rows run on CTA pairs with 256-row tiles; smaller ones keep 128-row
 // tiles, which waste less of each group's last partial tile.  Pairs read half the bytes per FLOP
 // and gather their rows in grouped GEMM 1, which outweighs their padding down to ~200 rows per
 // group (OlmoE shape at T = 2,048, 256 rows per expert: 0.279 -> 0.262 ms; latent prefill, 292:
 // 5.08 -> 4.92 ms).  p.rows and p.E must be set.
-// Bytes of MXFP8 block scales per row of `cols` values: cols / 32, rounded up to 16.
-int64_t mx_scale_ld(int64_t cols) { return (cols / 32 + 15) / 16 * 16; }
 
 // The quantised expert weights the config's expert_fp8 mode reads.
 bool fp8_weights_present(const moe_config_t* c, const moe_weights_t* w) {
@@ -89,6 +117,12 @@ bool fp8_weights_present(const moe_config_t* c, const moe_weights_t* w) {
 }
 
 int use_pair_tiles(const Plan& p) { return !p.mx && p.rows >= (int64_t)192 * p.E ? 1 : 0; }
+
+// A group's last CTA-pair tile with at most this many rows runs narrow (the weights as the MMA's
+// rows, the tile's rows as its N): see GemmProblem::narrow_max.  Measured over 64 to 224 (latent
+// prefill, sigmoid-wide and OlmoE shapes), 128 was best or within noise of it on all three.
+constexpr int kNarrowRows = 128;
+int narrow_rows() { return kNarrowRows; }
 
 void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->T = T;
@@ -104,6 +138,7 @@ void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->cap = capacity_of(c, T);
   p->rows = p->capacity ? (int64_t)p->E * p->cap : p->R;
   p->mx = c->expert_fp8 == MOE_EXPERT_MXFP8;
+  p->y32 = fp32_expert_rows(c);
   p->sx_ld = mx_scale_ld(p->Lr);
   p->sh_ld = mx_scale_ld(p->h);
   const int mt = (int)((T + 127) / 128);
@@ -144,7 +179,7 @@ void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   const bool gathered = use_pair_tiles(*p);
   p->xp = !gathered && !c->expert_fp8 ? take((size_t)p->rows * p->Lr * 2) : (size_t)-1;
   p->H = take((size_t)p->rows * p->h * 2);
-  p->Y = take((size_t)p->rows * p->Lr * 2);
+  p->Y = take((size_t)p->rows * p->Lr * (p->y32 ? 4 : 2));
   p->zn = p->latent ? take((size_t)T * p->L * 2) : (size_t)-1;
   if (p->mx) {
     p->xq = take((size_t)T * p->Lr);
@@ -446,17 +481,20 @@ int run_experts_mx(const moe_config_t* c, const moe_weights_t* w, const void* xr
 
 // tiles_ready: the tile table in the workspace was already written (by run_permute).
 // preact (optional): grouped GEMM 1 also stores the pre-activations [u | g] there, rows x 2h bf16.
+// y32: y is written in fp32 (bf16 experts only).
 int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, const int32_t* gather,
                 const int32_t* offsets, const Plan& p, void* y, void* ws, int* status, cudaStream_t st,
-                cudaEvent_t* ev = nullptr, bool tiles_ready = false, void* preact = nullptr) {
+                cudaEvent_t* ev = nullptr, bool tiles_ready = false, void* preact = nullptr, bool y32 = false) {
   int32_t* tile_off = at<int32_t>(ws, p.tile_off);
   void* H = at<void>(ws, p.H);
   if (p.mx) {
     if (preact) return MOE_ERR_UNSUPPORTED;
     return run_experts_mx(c, w, xr, gather, offsets, p, y, ws, status, st, ev, tiles_ready);
   }
-  if (c->expert_fp8)
+  if (c->expert_fp8) {
+    if (y32) return MOE_ERR_UNSUPPORTED;
     return run_experts_fp8(c, w, xr, gather, offsets, p, y, ws, status, st, ev, tiles_ready, preact);
+  }
   // large groups run on CTA pairs with 256-row tiles; small ones keep 128-row tiles,
   // which waste less of the last partial tile of each group
   const int pair = use_pair_tiles(p);
@@ -497,6 +535,7 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   g1.ldo = p.h;
   g1.preact = preact;
   g1.preact_ld = 2 * (int64_t)p.h;
+  g1.narrow_max = pair ? narrow_rows() : 0;
   g1.status = status;
   s = cuda_status(launch_gemm(g1, st));
   if (s != MOE_OK) return s;
@@ -512,12 +551,14 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   g2.group_off = offsets;
   g2.tile_off = tile_off;
   g2.b_rows_per_group = p.Lr;
-  g2.epilogue = EPI_BF16;
+  g2.epilogue = y32 ? EPI_F32 : EPI_BF16;
   g2.bn = 256;
   g2.splits = 1;
   g2.pair_tiles = pair;
   g2.out = y;
   g2.ldo = p.Lr;
+  g2.split_stride = 0;
+  g2.narrow_max = pair ? narrow_rows() : 0;
   g2.status = status;
   s = cuda_status(launch_gemm(g2, st));
   if (s != MOE_OK) return s;
@@ -831,6 +872,14 @@ int moe_workspace_layout(const moe_config_t* c, int64_t T, int64_t o[10]) {
   return MOE_OK;
 }
 
+int moe_layer_expert_rows_fp32(const moe_config_t* c, int32_t* is_fp32) {
+  int s = check_config(c);
+  if (s != MOE_OK) return s;
+  if (!is_fp32) return MOE_ERR_INVALID_ARG;
+  *is_fp32 = fp32_expert_rows(c) ? 1 : 0;
+  return MOE_OK;
+}
+
 int moe_router(const moe_config_t* c, const moe_weights_t* w, const void* x, int64_t T, float* logits, int32_t* idx,
                float* weights, void* ws, size_t ws_bytes, moe_stream_t stream) {
   Plan p;
@@ -966,11 +1015,12 @@ int layer_forward(const moe_config_t* c, const moe_weights_t* w, const void* x, 
   if (s != MOE_OK) return s;
   mark(ev, 4, st);
   void* Y = at<void>(ws, p.Y);
-  s = run_experts(c, w, xr, gather, offsets, p, Y, ws, status, st, ev, tiles_ready, preact);
+  const bool y32 = p.y32 && !preact;   // the training forward keeps bf16 y for the backward
+  s = run_experts(c, w, xr, gather, offsets, p, Y, ws, status, st, ev, tiles_ready, preact, y32);
   if (s != MOE_OK) return s;
   if (!p.latent) {
     s = cuda_status(launch_combine(Y, scatter, wts, (int)T, p.k, p.Lr, (int)p.rows, 0, 0.f, nullptr, out,
-                                   p.capacity ? 1 : 0, status, st));
+                                   p.capacity ? 1 : 0, status, st, y32 ? 1 : 0));
     mark(ev, 8, st);
     mark(ev, 9, st);
     return s;

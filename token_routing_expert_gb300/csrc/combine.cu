@@ -1,6 +1,6 @@
 // Weighted combine, RMSNorm and split-K reduction (HBM-bound row kernels).
 //
-// combine:  z[t] = sum_j w[t, j] * y[scatter_idx[t*k + j]], fp32 accumulate,
+// combine:  z[t] = sum_j w[t, j] * y[scatter_idx[t*k + j]], y bf16 or fp32, fp32 accumulate,
 //           bf16 store (page "Как устроен Olmo-core 3: обучение больших
 //           MoE-моделей", §"Пересылка токенов между экспертами": restore the
 //           original order by the saved indices).
@@ -54,7 +54,8 @@ __device__ __forceinline__ void store_normalised(const uint4* zs, int vec, float
   }
 }
 
-template <bool RMS>
+// Y32: the expert rows are fp32 (two 16-byte vectors per 8 values) instead of bf16.
+template <bool RMS, bool Y32 = false>
 __global__ void __launch_bounds__(32 * kRowWarps)
     combine_kernel(const uint4* __restrict__ y, const int32_t* __restrict__ scatter_idx, const float* __restrict__ w,
                    int T, int k, int vec, int R, float eps, const uint4* __restrict__ gain, uint4* __restrict__ z,
@@ -88,23 +89,51 @@ __global__ void __launch_bounds__(32 * kRowWarps)
     const int c = c0 + lane;
     const bool active = c < vec;
     float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int j0 = 0; j0 < k; j0 += 8) {
-      uint4 v[8];
-      float wj[8];
+    if (Y32) {
+      // fp32 rows: four at a time (two 16-byte loads each), in ascending j
+      for (int j0 = 0; j0 < k; j0 += 4) {
+        uint4 v[4][2];
+        float wj[4];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        const int p = __shfl_sync(0xffffffffu, my_p, (j0 + jj) & 31);
-        wj[jj] = __shfl_sync(0xffffffffu, my_w, (j0 + jj) & 31);
-        v[jj] = make_uint4(0u, 0u, 0u, 0u);
-        if (active && j0 + jj < k) v[jj] = __ldcs(y + (long long)p * vec + c);
+        for (int jj = 0; jj < 4; ++jj) {
+          const int p = __shfl_sync(0xffffffffu, my_p, (j0 + jj) & 31);
+          wj[jj] = __shfl_sync(0xffffffffu, my_w, (j0 + jj) & 31);
+          v[jj][0] = v[jj][1] = make_uint4(0u, 0u, 0u, 0u);
+          if (active && j0 + jj < k) {
+            const uint4* src = y + ((long long)p * vec + c) * 2;
+            v[jj][0] = __ldcs(src);
+            v[jj][1] = __ldcs(src + 1);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          if (j0 + jj >= k) break;
+          const float f[8] = {__uint_as_float(v[jj][0].x), __uint_as_float(v[jj][0].y), __uint_as_float(v[jj][0].z),
+                              __uint_as_float(v[jj][0].w), __uint_as_float(v[jj][1].x), __uint_as_float(v[jj][1].y),
+                              __uint_as_float(v[jj][1].z), __uint_as_float(v[jj][1].w)};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[jj], f[i], acc[i]);
+        }
       }
+    } else {
+      for (int j0 = 0; j0 < k; j0 += 8) {
+        uint4 v[8];
+        float wj[8];
 #pragma unroll
-      for (int jj = 0; jj < 8; ++jj) {
-        if (j0 + jj >= k) break;
-        float f[8];
-        unpack8(v[jj], f);
+        for (int jj = 0; jj < 8; ++jj) {
+          const int p = __shfl_sync(0xffffffffu, my_p, (j0 + jj) & 31);
+          wj[jj] = __shfl_sync(0xffffffffu, my_w, (j0 + jj) & 31);
+          v[jj] = make_uint4(0u, 0u, 0u, 0u);
+          if (active && j0 + jj < k) v[jj] = __ldcs(y + (long long)p * vec + c);
+        }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[jj], f[i], acc[i]);
+        for (int jj = 0; jj < 8; ++jj) {
+          if (j0 + jj >= k) break;
+          float f[8];
+          unpack8(v[jj], f);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) acc[i] = fmaf(wj[jj], f[i], acc[i]);
+        }
       }
     }
     if (!active) continue;
@@ -165,10 +194,16 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float4* __rest
 
 cudaError_t launch_combine(const void* y, const int32_t* scatter_idx, const float* w, int T, int k, int L, int R,
                            int rms, float eps, const void* gain, void* z, int allow_dropped, int* status,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, int y_f32) {
   if (T <= 0) return cudaSuccess;
   const int vec = L / 8;
   const dim3 grid((T + kRowWarps - 1) / kRowWarps), block(32 * kRowWarps);
+  if (y_f32) {
+    if (rms) return cudaErrorInvalidValue;
+    launch_pdl(combine_kernel<false, true>, grid, block, 0, stream, static_cast<const uint4*>(y), scatter_idx, w, T, k,
+                                                      vec, R, eps, nullptr, static_cast<uint4*>(z), allow_dropped, status);
+    return cudaGetLastError();
+  }
   if (rms) {
     const size_t sm = (size_t)kRowWarps * vec * sizeof(uint4);
     if (sm > 48 * 1024) {

@@ -79,6 +79,7 @@ struct GemmParams {
   uint8_t* mx_out_codes;       // MXFP8 SwiGLU: H leaves as MXFP8 codes (ldo bytes per row) and block
   uint8_t* mx_out_scale;       //   scales (mx_out_ld bytes per row) instead of bf16
   long long mx_out_ld;
+  int narrow_max;              // > 0: tiles of at most this many rows run narrow (see narrow_cols)
   int* status;
 };
 
@@ -153,6 +154,14 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
   c.kt0 = c.split * p.kt_per_split;
   c.kt1 = min(p.kt_total, c.kt0 + p.kt_per_split);
   return c;
+}
+
+// A narrow tile (CTA pairs, grouped): a group's last tile with at most p.narrow_max rows.  Its MMA
+// takes the tile's weight rows as the 256 M rows (128 per CTA) and the tile's rows as N, rounded up
+// to a multiple of 32 (CTA r holds rows [r N/2, (r + 1) N/2) of the tile), so the tensor core spends
+// time on the rows that exist instead of on 256 padded ones.  Returns that N, or 0 for a normal tile.
+__device__ __forceinline__ int narrow_cols(const GemmParams& p, const TileCoord& c) {
+  return (p.narrow_max > 0 && c.rows > 0 && c.rows <= p.narrow_max) ? (c.rows + 31) & ~31 : 0;
 }
 
 // With a_off, the A rows of group g are read from a_off[g] on instead of the output's own rows:
@@ -427,10 +436,14 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
 template <int ROWS, int NST, bool PAIR>
 __device__ __forceinline__ void gather_a_load_rows(const GemmParams& p, const TileCoord& c, int t, int rank,
                                                    int (&tok)[8]) {
+  // a narrow tile's CTA holds N/2 of its rows (the MMA's B operand), else 128
+  const int nn = PAIR ? narrow_cols(p, c) : 0;
+  const int base = nn ? rank * (nn >> 1) : 128 * rank;
+  const int lim = nn ? min(c.rows, base + (nn >> 1)) : c.rows;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const int r = 128 * rank + (t >> 3) + 16 * j;   // row of the tile
-    tok[j] = r < c.rows ? __ldg(p.a_gather + c.row0 + r) : -1;
+    const int r = base + (t >> 3) + 16 * j;   // row of the tile
+    tok[j] = r < lim ? __ldg(p.a_gather + c.row0 + r) : -1;
   }
 }
 
@@ -450,6 +463,7 @@ __device__ __forceinline__ void gather_a_producer(const GemmParams& p, const int
     gather_a_load_rows<ROWS, NST, PAIR>(p, decode_tile<ROWS>(t_first, p, s_toff, s_goff), t, rank, nxt);
   for (int tile = t_first; tile < total_tiles && ok; tile += t_step) {
     const TileCoord c = decode_tile<ROWS>(tile, p, s_toff, s_goff);
+    const int nn = PAIR ? narrow_cols(p, c) : 0;
     int tok[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -475,8 +489,11 @@ __device__ __forceinline__ void gather_a_producer(const GemmParams& p, const int
       }
       const uint32_t sa = smem_u32(smem + stage * stage_bytes);
       const uint8_t* kb = p.a_src + (long long)kt * 128 + chunk * 16;
+      // a narrow tile's MMA reads only its N/2 rows of the stage
+      const int jn = PAIR && nn ? (nn >> 5) : 8;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
+        if (j >= jn) break;
         const int r = (t >> 3) + 16 * j;
         const int src = tok[j];
         cp_async_16(sa + r * 128 + ((chunk ^ (r & 7)) << 4), kb + (long long)(src < 0 ? 0 : src) * p.a_ld_bytes,
@@ -1219,6 +1236,73 @@ __device__ __forceinline__ void swb_pair_tile(uint32_t tbase, const TileCoord& c
   }
 }
 
+// Epilogue of a narrow tile (see narrow_cols): TMEM lane l of quadrant q holds one weight row of this
+// CTA, column j the tile's row j.  SwiGLU: the CTA's 128 weight rows are, per quadrant, 16 up rows
+// then the 16 gate rows of the same h (loaded as 16-row boxes), so lanes l and l + 16 hold u and g of
+// one h; each pair trades half its columns (one shuffle per value) and both compute silu(g) * u,
+// exactly as the normal epilogue does, for 16 rows each.  bf16 or fp32 out: lane l is output column
+// nt * 256 + 128 rank + 32 q + l.  Values go straight to global memory: for each column j one store
+// instruction writes 32 or 64 contiguous bytes of one or two output rows.
+template <int EPI>
+__device__ __forceinline__ void store_narrow(uint32_t tbase, const TileCoord& c, int rank, int quad, int half,
+                                             int lane, const GemmParams& p, int nn) {
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+  if (EPI == EPI_SWIGLU) {
+    const bool lo = lane < 16;
+    const int hcol = c.nt * 128 + 64 * rank + 16 * quad + (lane & 15);
+    const bool col_ok = hcol < p.N;
+    __nv_bfloat16* pre = reinterpret_cast<__nv_bfloat16*>(p.preact);
+#pragma unroll 1
+    for (int cc = half; cc * 32 < nn; cc += kEpiWarps / 4) {
+      uint32_t v[32];
+      __syncwarp();
+      tmem_ld_32x32b_x32(tbase + cc * 32, v);
+      tmem_ld_wait();
+      const int t0 = cc * 32 + (lo ? 0 : 16);   // this lane's first row of the tile
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        // lo lanes keep columns 0-15 (their u) and take g from lane + 16; hi lanes keep 16-31 (g)
+        const uint32_t give = lo ? v[16 + j] : v[j];
+        const uint32_t got = __shfl_xor_sync(0xffffffffu, give, 16);
+        const float u = __uint_as_float(lo ? v[j] : got);
+        const float g = __uint_as_float(lo ? got : v[16 + j]);
+        const int t = t0 + j;
+        if (t < c.rows && col_ok) {
+          const long long row = (long long)c.row0 + t;
+          // silu(g) = g / (1 + e^-g); the approximate division returns 0 when e^-g overflows
+          out[row * p.ldo + hcol] = __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * u);
+          if (pre) {
+            pre[row * p.preact_ld + hcol] = __float2bfloat16_rn(u);
+            pre[row * p.preact_ld + p.N + hcol] = __float2bfloat16_rn(g);
+          }
+        }
+      }
+    }
+  } else {
+    const int col = c.nt * 256 + 128 * rank + 32 * quad + lane;
+    const bool col_ok = col < p.N;
+    float* out32 = reinterpret_cast<float*>(p.out);
+#pragma unroll 1
+    for (int cc = half; cc * 32 < nn; cc += kEpiWarps / 4) {
+      uint32_t v[32];
+      __syncwarp();
+      tmem_ld_32x32b_x32(tbase + cc * 32, v);
+      tmem_ld_wait();
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int t = cc * 32 + j;
+        if (t < c.rows && col_ok) {
+          const long long o = ((long long)c.row0 + t) * p.ldo + col;
+          if (EPI == EPI_F32)
+            out32[o] = __uint_as_float(v[j]);
+          else
+            out[o] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
+      }
+    }
+  }
+}
+
 // GB: the B operand of a K-grouped fp32 GEMM is gathered by the kernel (gather_b_mn_producer).
 template <int EPI, bool F8 = false, bool GA = false, bool GB = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsGA : kThreads, 1)
@@ -1304,17 +1388,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
         const int brow = EPI == EPI_SWIGLU
                              ? c.group * p.b_rows_per_group + c.nt * 128 + (rank ? p.b_gate_offset : 0)
                              : c.group * p.b_rows_per_group + c.nt * C::BN + 128 * (int)rank;
+        // narrow tile: the weights fill the second region as the MMA's A operand, the tile's rows
+        // (N/2 per CTA) the first; bf16 / fp32 out loads those rows as 32-row boxes of tmP
+        const int nn = (EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_F32) && !F8 ? narrow_cols(p, c) : 0;
+        const int nrow0 = c.row0 + (int)rank * (nn >> 1);
+        const int nbox = nn ? (min(max(c.rows - (int)rank * (nn >> 1), 0), nn >> 1) + 31) >> 5 : 0;
+        const int nbox_both = nn ? ((min(c.rows, nn >> 1) + 31) >> 5) + ((max(c.rows - (nn >> 1), 0) + 31) >> 5) : 0;
         for (int kt = c.kt0; kt < c.kt1; ++kt) {
           if (!mbar_wait_cluster(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
           const uint32_t full0 = map_to_cta(smem_u32(&full_bar[stage]), 0);
+          const int kx = kt * (F8 ? 2 * BK : BK);
+          if (nn) {
+            if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::B_BYTES + (GA ? 0 : nbox_both * 4096));
+            if (EPI == EPI_SWIGLU) {
+              // per quadrant q: 16 up rows, then the gate rows of the same 16 h
+              const int r0 = c.group * p.b_rows_per_group + c.nt * 128 + 64 * (int)rank;
+              for (int q = 0; q < 4; ++q) {
+                tma_load_2d_pair(sa + C::A_BYTES + q * 4096, &tmP, full0, kx, r0 + 16 * q);
+                tma_load_2d_pair(sa + C::A_BYTES + q * 4096 + 2048, &tmP, full0, kx, r0 + 16 * q + p.b_gate_offset);
+              }
+            } else {
+              tma_load_2d_pair(sa + C::A_BYTES, &tmB, full0, kx, brow);
+            }
+            if (!GA)
+              for (int b = 0; b < nbox; ++b) tma_load_2d_pair(sa + b * 4096, &tmP, full0, kx, nrow0 + 32 * b);
+            if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+            continue;
+          }
           // a group's last tile with <= 128 rows has none in CTA 1: CTA 1 skips its A rows
           // (its accumulator rows are never stored) and saves their L2 bytes
           const bool a1 = c.rows > 128;
           if (rank == 0)
             mbar_arrive_expect_tx(&full_bar[stage], GA ? 2 * C::B_BYTES
                                                     : (GB ? 2 * C::A_BYTES : 2 * C::STAGE_BYTES) - (a1 ? 0 : C::A_BYTES));
-          const int kx = kt * (F8 ? 2 * BK : BK);
           if (!GA && (rank == 0 || a1)) {
             if (p.a_mn) {   // MN-major A: this CTA's 128 M columns as two 64-column blocks
               tma_load_2d_pair(sa, &tmA, full0, arow, kt * BK + ash);
@@ -1344,6 +1451,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
       int it = 0;
       for (int t = pair; t < total_tiles; t += npairs, ++it) {
         const TileCoord c = decode_tile<BM2>(t, p, s_toff, s_goff);
+        const int nn = (EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_F32) && !F8 ? narrow_cols(p, c) : 0;
         const int acc = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
         if (!mbar_wait_cluster(&tempty_bar[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
@@ -1356,12 +1464,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
           const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
           const bool amn = !GA && p.a_mn;
           const bool bmn = EPI != EPI_SWIGLU && p.b_mn;
-          const uint64_t a_desc = amn ? umma_sdesc_mn_sw128(sa, 8192) : umma_sdesc_sw128(sa);
-          const uint64_t b_desc = bmn ? umma_sdesc_mn_sw128(sa + C::A_BYTES, 8192) : umma_sdesc_sw128(sa + C::A_BYTES);
+          uint64_t a_desc = amn ? umma_sdesc_mn_sw128(sa, 8192) : umma_sdesc_sw128(sa);
+          uint64_t b_desc = bmn ? umma_sdesc_mn_sw128(sa + C::A_BYTES, 8192) : umma_sdesc_sw128(sa + C::A_BYTES);
           const uint64_t a_step = amn ? 2048 / 16 : 2;
           const uint64_t b_step = bmn ? 2048 / 16 : 2;
           // bits 15 / 16 of the instruction descriptor: A / B is MN-major
-          const uint32_t id = idesc | (amn ? (1u << 15) : 0u) | (bmn ? (1u << 16) : 0u);
+          uint32_t id = idesc | (amn ? (1u << 15) : 0u) | (bmn ? (1u << 16) : 0u);
+          if (nn) {   // narrow tile: the weights (second region) are A, the tile's rows B, N = nn
+            a_desc = umma_sdesc_sw128(sa + C::A_BYTES);
+            b_desc = umma_sdesc_sw128(sa);
+            id = umma_idesc_bf16_f32(BM2, nn);
+          }
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             if (F8)
@@ -1413,9 +1526,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
         cs = p.b_scale + brow;
         cs_gate = cs + p.b_gate_offset;
       }
+      const int nn = (EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_F32) && !F8 ? narrow_cols(p, c) : 0;
       if constexpr (C::SWB) {
         swb_pair_tile<C>(tbase, c, (int)rank, row_in_tile, p, half, stg, smem, &tmP, pre_full, pre_empty, pre_issuer,
                          pre_issued, pre_used, ash, live_end, abort_flag);
+      } else if (nn) {
+        store_narrow<EPI>(tbase, c, (int)rank, quad, half, lane, p, nn);
       } else {
         // K-grouped: the group's output slice, zeros for a group without rows
         store_tile<C::BN, EPI, F8>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt,
@@ -1649,8 +1765,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   }
   const bool pair = q.pair_tiles != 0;
   const bool f8 = q.e4m3 != 0;
-  if (pair && (q.bn != 256 || q.splits > 1 || (q.epilogue == EPI_F32 && (q.e4m3 || q.num_groups > 0))))
-    return cudaErrorInvalidValue;
+  if (pair && (q.bn != 256 || q.splits > 1 || (q.epilogue == EPI_F32 && q.e4m3))) return cudaErrorInvalidValue;
   if (f8 && (q.bn != 256 || q.splits > 1 || q.k_groups > 0 || q.epilogue == EPI_F32 || !q.a_scale || !q.b_scale))
     return cudaErrorInvalidValue;
   // gathered A: grouped SwiGLU only; A rows are copied from a_src by the kernel, no A tensor map
@@ -1684,6 +1799,18 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   if (q.epilogue == EPI_SWIGLU_BWD &&
       (q.num_groups == 0 || !q.a_off || !q.preact || !q.out2 || f8 || ga || q.bn != 256 || q.splits > 1 ||
        q.ldo < 2 * (int64_t)q.N || q.ldo % 8 || q.ldo2 < q.N || q.ldo2 % 8))
+    return cudaErrorInvalidValue;
+  // narrow tiles (see narrow_cols): grouped CTA-pair GEMMs on bf16 operands, SwiGLU with gathered A
+  // rows or bf16 out with TMA-loaded A; tmP then holds 16-row boxes of the SwiGLU weights, or 32-row
+  // boxes of A
+  const bool narrow = q.narrow_max > 0;
+  if (narrow && (!pair || q.num_groups == 0 || f8 || q.splits > 1 || q.a_off || q.b_mn_major || q.a_mn_major ||
+                 q.k_groups > 0 || q.narrow_max % 32 || q.narrow_max > 256 ||
+                 !((q.epilogue == EPI_SWIGLU && ga) || ((q.epilogue == EPI_BF16 || q.epilogue == EPI_F32) && !ga))))
+    return cudaErrorInvalidValue;
+  CUtensorMap tn;
+  if (narrow && !(q.epilogue == EPI_SWIGLU ? make_tmap(&tn, q.B, q.b_rows_total, q.K, 16, false)
+                                           : make_tmap(&tn, q.A, q.M, q.K, 32, false)))
     return cudaErrorInvalidValue;
   const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
   CUtensorMap ta, tb;
@@ -1740,12 +1867,13 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.preact_dense = q.preact_dense;
   gp.out2 = q.out2;
   gp.ldo2 = q.ldo2;
+  gp.narrow_max = narrow ? q.narrow_max : 0;
   gp.status = q.status;
 
   if (ga) {
     if (pair)
       return f8 ? launch_pair_impl<EPI_SWIGLU, true, true>(ta, tb, gp, 0, stream)
-                : launch_pair_impl<EPI_SWIGLU, false, true>(ta, tb, gp, 0, stream);
+                : launch_pair_impl<EPI_SWIGLU, false, true>(ta, tb, gp, 0, stream, narrow ? &tn : nullptr);
     const int grid = num_sms();
     return f8 ? launch_impl<256, EPI_SWIGLU, true, true>(q, ta, tb, gp, grid, stream)
               : launch_impl<256, EPI_SWIGLU, false, true>(q, ta, tb, gp, grid, stream);
@@ -1758,7 +1886,8 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
     }
     if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU>(ta, tb, gp, tiles, stream);
     if (gb) return launch_pair_impl<EPI_F32, false, false, true>(ta, tb, gp, tiles, stream);   // K-grouped, B gathered
-    if (q.epilogue == EPI_F32) return launch_pair_impl<EPI_F32>(ta, tb, gp, tiles, stream);   // dense fp32 out
+    if (q.epilogue == EPI_F32)   // fp32 out: dense, or grouped (the layer's fp32 expert rows)
+      return launch_pair_impl<EPI_F32>(ta, tb, gp, tiles, stream, narrow ? &tn : nullptr);
     if (q.epilogue == EPI_SWIGLU_BWD) {
       // the [u | g] rows as 128 x 32 boxes, 64-byte swizzle (the epilogue reads a row per lane)
       CUtensorMap tp;
@@ -1767,7 +1896,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
         return cudaErrorInvalidValue;
       return launch_pair_impl<EPI_SWIGLU_BWD>(ta, tb, gp, tiles, stream, &tp);
     }
-    return launch_pair_impl<EPI_BF16>(ta, tb, gp, tiles, stream);
+    return launch_pair_impl<EPI_BF16>(ta, tb, gp, tiles, stream, narrow ? &tn : nullptr);
   }
   int grid = num_sms();
   if (q.num_groups == 0) {

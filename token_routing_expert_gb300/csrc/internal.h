@@ -75,6 +75,10 @@ struct GemmProblem {
   void* mx_out_codes;     // MXFP8 SwiGLU only, non-NULL: H is written as MXFP8 (codes (M, ldo) bytes, ldo a
   void* mx_out_scale;     //   multiple of 16; scales (M, mx_out_ld) bytes) instead of bf16 to out
   int64_t mx_out_ld;
+  int narrow_max;         // > 0 (grouped, CTA pairs, bf16 operands, SwiGLU with gathered A or bf16 out; a
+                          //    multiple of 32, <= 256): a group's tile with at most this many rows runs with the
+                          //    operands swapped, the weights as the MMA's 256 rows and the tile's rows as its N
+                          //    (rounded up to 32), so its tensor-core work follows the rows it has
   int* status;
 };
 
@@ -117,9 +121,10 @@ cudaError_t launch_capacity_remap(const int32_t* idx, int R, int E, int cap, con
                                   const int32_t* scatter_dense, int32_t* offsets, int32_t* gather_idx,
                                   int32_t* scatter_idx, cudaStream_t stream);
 
+// y_f32: the expert rows y are fp32 (no RMSNorm then); else bf16.
 cudaError_t launch_combine(const void* y, const int32_t* scatter_idx, const float* w, int T, int k, int L,
                            int R, int rms, float eps, const void* gain, void* z, int allow_dropped, int* status,
-                           cudaStream_t stream);
+                           cudaStream_t stream, int y_f32 = 0);
 cudaError_t launch_rmsnorm(const void* z, int T, int L, float eps, const void* gain, void* out,
                            cudaStream_t stream);
 // Padded row layout of the experts backward (expert e from row 64 k_off[e], zero rows to the next

@@ -61,7 +61,7 @@ EXPORTS = ["moe_quantize_rowwise_fp8", "moe_expert_capacity", "moe_permuted_rows
            "moe_router_backward", "moe_host_workspace_size", "moe_layer_forward_host_batches",
            "moe_grouped_swiglu_preact", "moe_layer_forward_preact", "moe_grouped_swiglu_backward_preact",
            "moe_latent_restore_backward", "moe_latent_down_backward", "moe_layer_backward_workspace_size",
-           "moe_layer_backward", "moe_check_wait_timeout", "moe_quantize_mxfp8"]
+           "moe_layer_backward", "moe_check_wait_timeout", "moe_quantize_mxfp8", "moe_layer_expert_rows_fp32"]
 
 _lib = None
 
@@ -99,6 +99,7 @@ def load() -> ctypes.CDLL:
         "moe_host_workspace_size": [cfgp, I64, P(SZ)],
         "moe_layer_forward_host_batches": [cfgp, wp, P(VP), P(VP), ctypes.c_int32, I64, VP, SZ, VP],
         "moe_workspace_layout": [cfgp, I64, P(I64)],
+        "moe_layer_expert_rows_fp32": [cfgp, P(ctypes.c_int32)],
         "moe_get_status": [VP, P(ctypes.c_int32), ctypes.c_int],
         "moe_status_string": [ctypes.c_int],
         "moe_permute_noalloc": [cfgp, VP, I64, VP, VP, VP, VP, VP],
@@ -203,6 +204,12 @@ def moe_permuted_rows(cfg: moe_config_t, T: int) -> int:
     out = ctypes.c_int64()
     _check(load().moe_permuted_rows(ctypes.byref(cfg), T, ctypes.byref(out)), "moe_permuted_rows")
     return out.value
+
+
+def moe_layer_expert_rows_fp32(cfg: moe_config_t) -> bool:
+    out = ctypes.c_int32()
+    _check(load().moe_layer_expert_rows_fp32(ctypes.byref(cfg), ctypes.byref(out)), "moe_layer_expert_rows_fp32")
+    return bool(out.value)
 
 
 def moe_workspace_layout(cfg: moe_config_t, T: int):
@@ -725,6 +732,8 @@ def layer_intermediates(cfg, T, ws):
         return ws[off:off + n * size].view(dtype).view(*shape)
 
     out = {
+        # y: the training forward's bf16 rows; after moe_layer_forward of a configuration that keeps
+        # them in fp32 (moe_layer_expert_rows_fp32), "y_f32" holds them
         "idx": view(o[1], R, torch.int32, (T, k)),
         "weights": view(o[2], R, torch.float32, (T, k)),
         "counts": view(o[3], E, torch.int32, (E,)),
@@ -733,6 +742,8 @@ def layer_intermediates(cfg, T, ws):
         "scatter_idx": view(o[6], R, torch.int32, (R,)),
         "y": view(o[8], rows * Lr, torch.bfloat16, (rows, Lr)),
     }
+    if moe_layer_expert_rows_fp32(cfg):
+        out["y_f32"] = view(o[8], rows * Lr, torch.float32, (rows, Lr))
     if o[7] >= 0:
         out["x_routed"] = view(o[7], T * cfg.latent_dim, torch.bfloat16, (T, cfg.latent_dim))
     if o[9] >= 0:

@@ -185,6 +185,18 @@ inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, siz
 __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
 }
+// The same with an L2 cache policy (createpolicy) for the line it reads.
+__device__ __forceinline__ void cp_async_16_hint(uint32_t dst, const void* src, uint32_t src_bytes, uint64_t policy) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2, %3;" ::"r"(dst), "l"(src),
+               "r"(src_bytes), "l"(policy)
+               : "memory");
+}
+// An L2 policy that keeps the lines it is attached to past the others (evict_last).
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
 // The barrier receives one arrival once all of this thread's earlier cp.async copies have
 // landed; the thread does not wait.  The arrival counts against the barrier's initial count.
 __device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {

@@ -80,6 +80,8 @@ struct GemmParams {
   uint8_t* mx_out_scale;       //   scales (mx_out_ld bytes per row) instead of bf16
   long long mx_out_ld;
   int narrow_max;              // > 0: tiles of at most this many rows run narrow (see narrow_cols)
+  const int* tile_seq;         // M-grouped: the order of the row tiles (NULL: expert order)
+  int a_keep;                  // gathered A: its source rows are read with an evict_last L2 policy
   int* status;
 };
 
@@ -134,7 +136,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
   c.split = t % p.splits;
   const int rest = t / p.splits;
   c.nt = rest % p.n_tiles;
-  const int mt = rest / p.n_tiles;
+  const int mt = p.tile_seq ? __ldg(p.tile_seq + rest / p.n_tiles) : rest / p.n_tiles;
   int row_base = 0, row_end = p.M, mt_local = mt;
   c.group = 0;
   if (p.num_groups > 0) {
@@ -455,6 +457,7 @@ __device__ __forceinline__ void gather_a_producer(const GemmParams& p, const int
   const int t = threadIdx.x - kGatherThread0;
   const int lane = t & 31;
   const int chunk = t & 7;
+  const uint64_t keep = l2_policy_evict_last();
   uint32_t stage = 0, phase = 0;
   bool ok = true;
   // the source rows of the next tile are loaded while the current one is copied
@@ -496,8 +499,12 @@ __device__ __forceinline__ void gather_a_producer(const GemmParams& p, const int
         if (j >= jn) break;
         const int r = (t >> 3) + 16 * j;
         const int src = tok[j];
-        cp_async_16(sa + r * 128 + ((chunk ^ (r & 7)) << 4), kb + (long long)(src < 0 ? 0 : src) * p.a_ld_bytes,
-                    src < 0 ? 0u : 16u);
+        const uint32_t d = sa + r * 128 + ((chunk ^ (r & 7)) << 4);
+        const uint8_t* g = kb + (long long)(src < 0 ? 0 : src) * p.a_ld_bytes;
+        if (p.a_keep)
+          cp_async_16_hint(d, g, src < 0 ? 0u : 16u, keep);
+        else
+          cp_async_16(d, g, src < 0 ? 0u : 16u);
       }
       cp_async_arrive_noinc(&gath_bar[stage]);
       if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1u; }
@@ -1366,7 +1373,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
   if (warp == 0 && lane == 0) {
     if (!GA) tma_prefetch_desc(&tmA);
     if (!GB) tma_prefetch_desc(&tmB);
-    if constexpr (C::SWB) tma_prefetch_desc(&tmP);
+    if (C::SWB || p.narrow_max > 0) tma_prefetch_desc(&tmP);
   }
   tc_fence_before();
   __syncthreads();
@@ -1868,6 +1875,8 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.out2 = q.out2;
   gp.ldo2 = q.ldo2;
   gp.narrow_max = narrow ? q.narrow_max : 0;
+  gp.tile_seq = q.num_groups > 0 && q.k_groups == 0 ? q.tile_seq : nullptr;
+  gp.a_keep = ga ? q.a_keep : 0;
   gp.status = q.status;
 
   if (ga) {

@@ -75,6 +75,10 @@ struct GemmProblem {
   void* mx_out_codes;     // MXFP8 SwiGLU only, non-NULL: H is written as MXFP8 (codes (M, ldo) bytes, ldo a
   void* mx_out_scale;     //   multiple of 16; scales (M, mx_out_ld) bytes) instead of bf16 to out
   int64_t mx_out_ld;
+  int a_keep;             // gathered A: 1 reads the source rows with an evict_last L2 policy (for a_src that
+                          //   fits the L2 beside the streamed weights, so its rows are not fetched again)
+  const int* tile_seq;    // grouped, M tiles: non-NULL runs the row tiles in this order (tile_seq[s] = the
+                          //   s-th to run, numbered as tile_off counts them) instead of expert order
   int narrow_max;         // > 0 (grouped, CTA pairs, bf16 operands, SwiGLU with gathered A or bf16 out; a
                           //    multiple of 32, <= 256): a group's tile with at most this many rows runs with the
                           //    operands swapped, the weights as the MMA's 256 rows and the tile's rows as its N
@@ -101,8 +105,8 @@ cudaError_t launch_topk(const float* logits, int n_partials, int64_t partial_str
 
 // chunk: assignments per block, a multiple of 256 in [256, 4096]; blk_scratch holds
 // permute_blocks(R, chunk) * E ints.
-// tile_off (optional, E + 1 ints): also the grouped GEMMs' tile table, prefix sums of
-// ceil(count / rows_per_tile), as launch_tile_table would write it.
+// tile_off (optional, E + 1 ints and then one per row tile): also the grouped GEMMs' tile table,
+// prefix sums of ceil(count / rows_per_tile) and the row-tile order, as launch_tile_table writes them.
 // The permutation of R assignments over E experts runs as one cluster launch (else three kernels).
 bool permute_fits_cluster(int R, int E);
 cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, int32_t* offsets,

@@ -62,9 +62,10 @@ CASES = {
     # tiles, the last one ragged (320 = 256 + 64)
     "router_pair": WorkloadSpec("router_pair", T=1500, d_model=512, num_experts=320, top_k=4, hidden_size=64,
                                 gating="sigmoid", score_bias_std=0.01, seed=23),
-    # 40 row tiles of the router GEMM: a 2-way split-K whose slices top-k adds itself (deeper splits,
-    # as in one_token, go through the separate sum)
-    "router_split2": WorkloadSpec("router_split2", T=5000, d_model=512, num_experts=48, top_k=4, hidden_size=64,
+    # more than 128 experts and few row tiles: the router GEMM takes a 3-way split-K whose slices
+    # top-k adds itself (up to 128 experts the router's epilogue runs the top-k; a deeper split, as
+    # in the latent decode workload, goes through the separate sum)
+    "router_split2": WorkloadSpec("router_split2", T=1000, d_model=512, num_experts=160, top_k=4, hidden_size=64,
                                   gating="topk_softmax", seed=24),
 }
 
@@ -81,6 +82,55 @@ def setup(name):
 
 def expect_ok():
     assert native.moe_get_status() == 0
+
+
+# Up to 128 experts and with enough row tiles to fill the GPU (T above 76 x 128), the router GEMM's
+# epilogue selects the top-k: every gating, E not a multiple of 32, top_k at the epilogue's limit,
+# ties between equal logits (experts sharing a router row), a ragged last row tile.
+FUSED_ROUTER = {
+    "fused_softmax_e100": WorkloadSpec("fused_softmax_e100", T=12001, d_model=256, num_experts=100, top_k=8,
+                                       hidden_size=64, gating="softmax", normalize_expert_weights=1.0, seed=41),
+    "fused_sigmoid_e33": WorkloadSpec("fused_sigmoid_e33", T=10113, d_model=320, num_experts=33, top_k=5,
+                                      hidden_size=64, gating="sigmoid", sigmoid_stability_epsilon=1e-6,
+                                      score_bias_std=0.01, normalize_expert_weights=2.0, expert_weight_scale=1.5,
+                                      seed=42),
+    "fused_topk_softmax_e128": WorkloadSpec("fused_topk_softmax_e128", T=16384, d_model=512, num_experts=128,
+                                            top_k=1, hidden_size=64, gating="topk_softmax", original_top_k=4,
+                                            seed=43),
+}
+
+
+@pytest.mark.parametrize("name", list(FUSED_ROUTER))
+def test_router_fused_epilogue(name):
+    spec = FUSED_ROUTER[name]
+    inp = generate(spec)
+    if name == "fused_sigmoid_e33":   # experts 3 and 7 share expert 0's router row: equal keys
+        inp["w_router"][3] = inp["w_router"][0]
+        inp["w_router"][7] = inp["w_router"][0]
+        inp["score_bias"] = None
+        spec = spec.with_(score_bias_std=0.0)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp)
+    T, E, k = spec.T, spec.num_experts, spec.top_k
+    ws = native.workspace(cfg, T)
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    _, idx, w = native.moe_router(cfg, wts, inp["x"].cuda(), ws, logits=logits)
+    expect_ok()
+    oc, ow = oracle_config(spec), oracle_weights(spec, inp)
+    rf = ref.route(oc, f64(inp["x"]), ow.w_router, ow.b_router, ow.score_bias)
+    want_logits = ref.router_logits(f64(inp["x"]), ow.w_router, ow.b_router)
+    assert np.all(np.abs(logits.double().cpu().numpy() - want_logits) <= 1e-5 + 1e-5 * np.abs(want_logits))
+    gi = idx.cpu().numpy().astype(np.int64)
+    mism = check_topk(gi, rf.keys, rf.idx, k)
+    gw = w.double().cpu().numpy()
+    ok = ~mism
+    assert np.all(np.abs(gw[ok] - rf.weights[ok]) <= 1e-5 + 1e-5 * np.abs(rf.weights[ok]))
+    if name == "fused_sigmoid_e33":   # equal keys: the lower expert index first
+        for t in range(T):
+            row = list(gi[t])
+            for a, b in ((0, 3), (0, 7), (3, 7)):
+                if a in row and b in row:
+                    assert row.index(a) < row.index(b)
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -216,25 +266,25 @@ def test_grouped_swiglu_designed_counts():
     assert_close_layer(y.double().cpu().numpy(), want, "grouped swiglu, designed counts")
 
 
-# Group sizes around the narrow-tile bound (a group's last CTA-pair tile with <= 128 rows runs with
-# the tile's rows as the MMA's N, rounded up to 32): tails of 1, 16, 31, 32, 33, ... rows next to
-# full 256-row tiles, empty groups, and enough rows in all (>= 192 per expert) for the CTA-pair path.
-NARROW_COUNTS = [1, 16, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 200, 255, 256, 257, 0, 300, 383, 384, 385,
-                 513, 640, 1000, 1301]
+# Group tails of every size class on the CTA-pair path (256-row tiles): 1, 16, 31, 32, 33, ... rows
+# alone or after full tiles, CTA 1 empty or partly filled, empty groups, and enough rows in all
+# (>= 192 per expert) for the pair tiles.
+TAIL_COUNTS = [1, 16, 31, 32, 33, 63, 64, 65, 100, 127, 128, 129, 200, 255, 256, 257, 0, 300, 383, 384, 385,
+               513, 640, 1000, 1301]
 
 
 @pytest.mark.parametrize("h", [192, 320])
-def test_grouped_swiglu_narrow_tails(h):
-    E = len(NARROW_COUNTS)
-    spec = WorkloadSpec("narrow_tails", T=sum(NARROW_COUNTS), d_model=256, num_experts=E, top_k=1, hidden_size=h,
+def test_grouped_swiglu_group_tails(h):
+    E = len(TAIL_COUNTS)
+    spec = WorkloadSpec("group_tails", T=sum(TAIL_COUNTS), d_model=256, num_experts=E, top_k=1, hidden_size=h,
                         gating="softmax", seed=33 + h)
     assert spec.rows >= 192 * E                                   # the CTA-pair path
     inp = generate(spec)
     cfg = native.config_from_spec(spec)
     wts = native.DeviceWeights.from_inputs(inp)
     ws = native.workspace(cfg, spec.T)
-    counts, offsets, gather, scatter = native.moe_permute(cfg, designed_routing(NARROW_COUNTS, 9), ws)
-    assert counts.cpu().tolist() == NARROW_COUNTS
+    counts, offsets, gather, scatter = native.moe_permute(cfg, designed_routing(TAIL_COUNTS, 9), ws)
+    assert counts.cpu().tolist() == TAIL_COUNTS
     xr = torch.from_numpy(np.random.default_rng(h).standard_normal((spec.T, spec.d_model), dtype=np.float32)).to(
         torch.bfloat16)
     y = native.moe_grouped_swiglu(cfg, wts, xr.cuda(), gather, offsets, ws)
@@ -244,9 +294,9 @@ def test_grouped_swiglu_narrow_tails(h):
     want = ref.expert_outputs(oracle_config(spec), f64(xr), perm, ow.expert)
     got = y.double().cpu().numpy()
     off = offsets.cpu().numpy()
-    for e, n in enumerate(NARROW_COUNTS):                        # every group on its own, tails included
+    for e, n in enumerate(TAIL_COUNTS):                        # every group on its own, tails included
         if n:
-            assert_close_layer(got[off[e]:off[e + 1]], want[off[e]:off[e + 1]], f"narrow tails, expert {e} ({n} rows)")
+            assert_close_layer(got[off[e]:off[e + 1]], want[off[e]:off[e + 1]], f"group tails, expert {e} ({n} rows)")
     # the training forward's kept pre-activations take the same tiles
     pre = torch.empty((spec.rows, 2 * h), dtype=torch.bfloat16, device="cuda")
     y2, _ = native.moe_grouped_swiglu_preact(cfg, wts, xr.cuda(), gather, offsets, ws, preact=pre)
@@ -254,12 +304,12 @@ def test_grouped_swiglu_narrow_tails(h):
     assert torch.equal(y2, y)
     x_np, g_np = f64(xr), gather.cpu().numpy()
     pre_np = pre.double().cpu().numpy()
-    for e, n in enumerate(NARROW_COUNTS):
+    for e, n in enumerate(TAIL_COUNTS):
         if n:
             w_up, w_gate, _ = ow.expert(e)
             rows = x_np[g_np[off[e]:off[e + 1]]]
             assert_close_layer(pre_np[off[e]:off[e + 1]], np.concatenate([rows @ w_up.T, rows @ w_gate.T], axis=1),
-                               f"narrow tails, pre-activations of expert {e}")
+                               f"group tails, pre-activations of expert {e}")
 
 
 @pytest.mark.parametrize("name", ["tiny", "sigmoid_bias_restore", "latent_skew", "max_experts", "one_token",
@@ -402,12 +452,13 @@ def test_staged_forward_matches_and_records_every_stage(name):
     times = [evs[i].elapsed_time(evs[i + 1]) for i in range(9)]
     assert all(t >= 0 for t in times) and times[5] > 0   # grouped GEMM 1 took time
     n = native.moe_layer_forward_launches(cfg, spec.T)
-    # router GEMM, top-k, the permutation (one cluster launch up to 16,384 assignments, else
-    # three kernels), grouped GEMMs 1 and 2, the combine: 6 kernels on CTA-pair tiles (7 with
-    # 128-row tiles, which copy the routed rows first); a latent layer adds the two projections,
-    # each with a split-K reduce when split, and a deep split-K router the sum of its partial
-    # logits (top-k adds up to 4 slices itself)
-    assert 6 <= n <= 10 if not spec.latent_dim else 8 <= n <= 14
+    # router GEMM (with the top-k in its epilogue up to 128 experts, else a top-k kernel), the
+    # permutation (one cluster launch up to 16,384 assignments, else three kernels), grouped GEMMs 1
+    # and 2, the combine: 5 kernels on CTA-pair tiles with a fused router (one more with 128-row
+    # tiles, which copy the routed rows first); a latent layer adds the two projections, each with
+    # a split-K reduce when split, and a deep split-K router the sum of its partial logits (top-k
+    # adds up to 4 slices itself)
+    assert 5 <= n <= 10 if not spec.latent_dim else 7 <= n <= 14
 
 
 @pytest.mark.parametrize("name", ["latent_decode_small", "pair_tiles"])

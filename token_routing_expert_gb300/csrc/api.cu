@@ -56,6 +56,7 @@ struct Plan {
   bool mx;            // MXFP8 experts (block scales); else rowwise e4m3 when expert_fp8
   int64_t sx_ld, sh_ld;   // MXFP8: bytes of block scales per row of x_routed / of H
   int D, E, k, h, L, Lr;   // Lr: routed dim (L or D)
+  int sms;            // the SM count the plan was made for
   bool latent;
   bool y32;           // the inference forward's expert rows y are fp32 (fp32_expert_rows)
   int router_bn, n_router_tiles;
@@ -118,18 +119,15 @@ bool fp8_weights_present(const moe_config_t* c, const moe_weights_t* w) {
 
 int use_pair_tiles(const Plan& p) { return !p.mx && p.rows >= (int64_t)192 * p.E ? 1 : 0; }
 
-// A group's last CTA-pair tile with at most this many rows runs narrow (the weights as the MMA's
-// rows, the tile's rows as its N): see GemmProblem::narrow_max.  Measured over 64 to 224 (latent
-// prefill, sigmoid-wide and OlmoE shapes), 128 was best or within noise of it on all three.
-constexpr int kNarrowRows = 128;
 // Routed input rows up to this size are kept in the L2 while grouped GEMM 1 gathers them: each row
 // is read by top_k experts' tiles, far apart in time, while the weights stream through (OlmoE
 // shape, 33.5 MB of rows: 812 -> 752 MB of DRAM traffic per GEMM 1, the time unchanged).
 constexpr int64_t kKeepBytes = int64_t(48) << 20;
-int narrow_rows() { return kNarrowRows; }
+
 
 void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->T = T;
+  p->sms = sms;
   p->D = c->d_model;
   p->E = c->num_experts;
   p->k = c->top_k;
@@ -167,9 +165,7 @@ void make_plan(const moe_config_t* c, int64_t T, int sms, Plan* p) {
   p->wts = take((size_t)p->R * 4);
   p->counts = take((size_t)p->E * 4);
   p->offsets = take((size_t)(p->E + 1) * 4);
-  // tile table: the prefix of row tiles per expert (E + 1), then the row-tile order (one entry per
-  // row tile: at most rows / 128 + E)
-  p->tile_off = take((size_t)(p->E + 1 + p->rows / 128 + p->E + 1) * 4);
+  p->tile_off = take((size_t)(p->E + 1) * 4);
   p->blk = take((size_t)std::max(1, permute_blocks((int)p->R, permute_chunk((int)p->R))) * p->E * 4);
   p->gather = take((size_t)std::max(p->R, p->rows) * 4);
   p->scatter = take((size_t)p->R * 4);
@@ -295,8 +291,46 @@ void mark(cudaEvent_t* ev, int i, cudaStream_t st) {
   if (ev && ev[i]) cudaEventRecord(ev[i], st);
 }
 
+// Up to 128 experts and top_k <= kRouterFusedK, when the row tiles alone fill the GPU (no split-K
+// would be taken), the router GEMM's tiles hold every expert of their rows and its epilogue does
+// the gating, top-k, weights and scalings: no logits round trip, one launch less.  With fewer row
+// tiles the split-K GEMM and the top-k kernel are faster (OlmoE shape, T = 8,192: 64 row tiles,
+// 28.6 us split and separate against 43.6 us fused, on different boxes).
+bool router_fused(const Plan& p) {
+  return p.E <= 128 && p.k <= kRouterFusedK && splits_for((int)((p.T + 127) / 128), p.D, p.sms) == 1;
+}
+
 int run_router(const moe_config_t* c, const moe_weights_t* w, const void* x, const Plan& p, float* logits_user,
                int32_t* idx, float* wts, void* ws, int* status, cudaStream_t st, cudaEvent_t* ev = nullptr) {
+  if (router_fused(p)) {
+    GemmProblem q{};
+    q.A = x;
+    q.B = w->w_router;
+    q.b_rows_total = p.E;
+    q.M = (int)p.T;
+    q.N = p.E;
+    q.K = p.D;
+    q.epilogue = EPI_ROUTER;
+    q.bn = p.E <= 32 ? 32 : p.E <= 64 ? 64 : 128;
+    q.splits = 1;
+    q.ldo = p.E;
+    q.router.b_router = c->router_bias ? static_cast<const float*>(w->b_router) : nullptr;
+    q.router.score_bias = c->has_score_bias ? static_cast<const float*>(w->score_bias) : nullptr;
+    q.router.logits = logits_user;
+    q.router.idx = idx;
+    q.router.w = wts;
+    q.router.gating = c->gating;
+    q.router.k = p.k;
+    q.router.restore = c->restore_weight_scale;
+    q.router.orig_k = c->original_top_k;
+    q.router.sig_eps = c->sigmoid_stability_epsilon;
+    q.router.p_norm = c->normalize_expert_weights;
+    q.router.ews = c->expert_weight_scale;
+    q.status = status;
+    const int s = cuda_status(launch_gemm(q, st));
+    mark(ev, 2, st);
+    return s;
+  }
   float* gemm_out = (p.router_splits == 1 && logits_user) ? logits_user : at<float>(ws, p.logits);
   GemmProblem q{};
   q.A = x;
@@ -541,8 +575,6 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   g1.ldo = p.h;
   g1.preact = preact;
   g1.preact_ld = 2 * (int64_t)p.h;
-  g1.narrow_max = pair ? narrow_rows() : 0;
-  g1.tile_seq = pair ? tile_off + p.E + 1 : nullptr;
   g1.a_keep = pair && (int64_t)p.T * p.Lr * 2 <= kKeepBytes ? 1 : 0;
   g1.status = status;
   s = cuda_status(launch_gemm(g1, st));
@@ -566,8 +598,6 @@ int run_experts(const moe_config_t* c, const moe_weights_t* w, const void* xr, c
   g2.out = y;
   g2.ldo = p.Lr;
   g2.split_stride = 0;
-  g2.narrow_max = pair ? narrow_rows() : 0;
-  g2.tile_seq = pair ? tile_off + p.E + 1 : nullptr;
   g2.status = status;
   s = cuda_status(launch_gemm(g2, st));
   if (s != MOE_OK) return s;
@@ -1166,7 +1196,8 @@ int moe_layer_forward_launches(const moe_config_t* c, int64_t T, int32_t* n) {
   make_plan(c, T, std::min(num_sms(), kSizingSms), &p);
   int k = 0;
   if (p.latent) k += p.down_splits > 1 ? 2 : 1;  // latent down (+ split-K reduce)
-  k += p.router_splits > kTopkFusedSlices ? 3 : 2;   // router GEMM, (sum of a deep split-K,) top-k
+  // router GEMM (with the top-k in its epilogue up to 128 experts), or GEMM, (sum of a deep split-K,) top-k
+  k += router_fused(p) ? 1 : p.router_splits > kTopkFusedSlices ? 3 : 2;
   // permute: one cluster launch or count, scan, place (, capacity slots)
   k += (permute_fits_cluster((int)p.R, p.E) ? 1 : 3) + (p.capacity ? 1 : 0);
   k += p.capacity ? 1 : 0;                       // tile table (the dropless scan writes it itself)

@@ -13,6 +13,8 @@
 // the B tile holds BN/2 "up" rows and BN/2 "gate" rows of the same expert and
 // the epilogue writes silu(gate) * up as bf16.
 #include <algorithm>
+#include <cfloat>
+#include <climits>
 #include <cstdio>
 
 #include "common.cuh"
@@ -79,9 +81,8 @@ struct GemmParams {
   uint8_t* mx_out_codes;       // MXFP8 SwiGLU: H leaves as MXFP8 codes (ldo bytes per row) and block
   uint8_t* mx_out_scale;       //   scales (mx_out_ld bytes per row) instead of bf16
   long long mx_out_ld;
-  int narrow_max;              // > 0: tiles of at most this many rows run narrow (see narrow_cols)
-  const int* tile_seq;         // M-grouped: the order of the row tiles (NULL: expert order)
   int a_keep;                  // gathered A: its source rows are read with an evict_last L2 policy
+  RouterEpilogue router;       // EPI_ROUTER
   int* status;
 };
 
@@ -136,7 +137,7 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
   c.split = t % p.splits;
   const int rest = t / p.splits;
   c.nt = rest % p.n_tiles;
-  const int mt = p.tile_seq ? __ldg(p.tile_seq + rest / p.n_tiles) : rest / p.n_tiles;
+  const int mt = rest / p.n_tiles;
   int row_base = 0, row_end = p.M, mt_local = mt;
   c.group = 0;
   if (p.num_groups > 0) {
@@ -156,14 +157,6 @@ __device__ __forceinline__ TileCoord decode_tile(int t, const GemmParams& p, con
   c.kt0 = c.split * p.kt_per_split;
   c.kt1 = min(p.kt_total, c.kt0 + p.kt_per_split);
   return c;
-}
-
-// A narrow tile (CTA pairs, grouped): a group's last tile with at most p.narrow_max rows.  Its MMA
-// takes the tile's weight rows as the 256 M rows (128 per CTA) and the tile's rows as N, rounded up
-// to a multiple of 32 (CTA r holds rows [r N/2, (r + 1) N/2) of the tile), so the tensor core spends
-// time on the rows that exist instead of on 256 padded ones.  Returns that N, or 0 for a normal tile.
-__device__ __forceinline__ int narrow_cols(const GemmParams& p, const TileCoord& c) {
-  return (p.narrow_max > 0 && c.rows > 0 && c.rows <= p.narrow_max) ? (c.rows + 31) & ~31 : 0;
 }
 
 // With a_off, the A rows of group g are read from a_off[g] on instead of the output's own rows:
@@ -284,11 +277,150 @@ __device__ __forceinline__ void swb_issue_first(uint4 (&pv)[8], const GemmParams
 // 32-column chunk.
 // SwiGLU backward: ash = the tile group's A row shift, live_end = the group's end among A's rows;
 // rows whose A row is past it are padding and get zeros.
+// Router epilogue (EPI_ROUTER): the tile holds every logit of its 128 rows.  The four warps of half
+// 0 take one row per thread; half 1 has nothing to do.  A thread streams its row's columns from
+// TMEM (twice for softmax gating: the row maximum and the sum of exponentials first), adds the
+// router bias, stores the logits if asked, forms score and selection key as the top-k kernel does,
+// and keeps the kRouterFusedK best (key descending, lower expert index first on equal keys) in
+// registers: columns arrive in ascending expert order, and a candidate goes to the first place
+// whose key it strictly exceeds, the entries below moving down.  The first k entries are the
+// choice; weights, the p-norm and the scalings follow as in the top-k kernel, summed over the k
+// entries in order.
+template <int BN>
+__device__ __forceinline__ void router_epilogue(uint32_t tbase, int row0, int rows, int row_in_tile,
+                                                const GemmParams& p, int half) {
+  if (half != 0) return;
+  constexpr int KM = kRouterFusedK;
+  const RouterEpilogue& r = p.router;
+  const bool live = row_in_tile < rows;
+  const long long t = (long long)row0 + row_in_tile;
+  const int E = p.N;
+  float m = -FLT_MAX, inv = 1.f;
+  if (r.gating == MOE_GATING_SOFTMAX) {
+    float ssum = 0.f;
+#pragma unroll 1
+    for (int pass = 0; pass < 2; ++pass) {
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld_32x32b_x32(tbase + cc * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int e = cc * 32 + i;
+          if (e >= E) continue;
+          const float l = __uint_as_float(v[i]) + (r.b_router ? __ldg(r.b_router + e) : 0.f);
+          if (pass == 0)
+            m = fmaxf(m, l);
+          else
+            ssum += __expf(l - m);
+        }
+      }
+    }
+    inv = __fdividef(1.0f, ssum);
+  }
+  float tk[KM], ts[KM];
+  int te[KM];
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    tk[j] = -INFINITY;
+    ts[j] = 0.f;
+    te[j] = INT_MAX;
+  }
+#pragma unroll 1
+  for (int cc = 0; cc < BN / 32; ++cc) {
+    uint32_t v[32];
+    __syncwarp();
+    tmem_ld_32x32b_x32(tbase + cc * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = cc * 32 + i;
+      if (e >= E) continue;
+      const float l = __uint_as_float(v[i]) + (r.b_router ? __ldg(r.b_router + e) : 0.f);
+      if (r.logits && live) r.logits[t * E + e] = l;
+      float sc = l;   // topk_softmax selects on the logits and weights the selected ones
+      if (r.gating == MOE_GATING_SIGMOID)
+        sc = __fdividef(1.0f, 1.0f + __expf(-l)) + r.sig_eps;
+      else if (r.gating == MOE_GATING_SOFTMAX)
+        sc = __expf(l - m) * inv;
+      float kv = sc;
+      if (r.score_bias) kv += __ldg(r.score_bias + e);
+      if (!(kv == kv)) kv = -INFINITY;   // NaN never outranks a number
+      if (kv > tk[KM - 1]) {
+        // the candidate takes the first place whose key it strictly exceeds; from there on every
+        // entry moves down one place (the list stays in order, equal keys keep their order)
+        float ck = kv, cs = sc;
+        int ce = e;
+        bool moving = false;
+#pragma unroll
+        for (int j = 0; j < KM; ++j) {
+          if (moving || ck > tk[j]) {
+            const float tk0 = tk[j], ts0 = ts[j];
+            const int te0 = te[j];
+            tk[j] = ck; ts[j] = cs; te[j] = ce;
+            ck = tk0; cs = ts0; ce = te0;
+            moving = true;
+          }
+        }
+      }
+    }
+  }
+  if (!live) return;
+  const int k = r.k;
+  float w[KM];
+#pragma unroll
+  for (int j = 0; j < KM; ++j) w[j] = ts[j];
+  if (r.gating == MOE_GATING_TOPK_SOFTMAX) {
+    float mx = -FLT_MAX;
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < k) mx = fmaxf(mx, w[j]);
+    float se = 0.f;
+#pragma unroll
+    for (int j = 0; j < KM; ++j) {
+      w[j] = j < k ? expf(w[j] - mx) : 0.f;
+      se += w[j];
+    }
+#pragma unroll
+    for (int j = 0; j < KM; ++j) w[j] = w[j] / se;
+  }
+  if (r.p_norm > 0.f) {
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < KM; ++j)
+      if (j < k) acc += r.p_norm == 1.0f ? fabsf(w[j]) : r.p_norm == 2.0f ? w[j] * w[j] : powf(fabsf(w[j]), r.p_norm);
+    const float nrm = r.p_norm == 1.0f ? acc : r.p_norm == 2.0f ? sqrtf(acc) : powf(acc, 1.0f / r.p_norm);
+#pragma unroll
+    for (int j = 0; j < KM; ++j) w[j] = w[j] / nrm;
+  }
+#pragma unroll
+  for (int j = 0; j < KM; ++j) {
+    if (j >= k) break;
+    float wj = w[j];
+    if (r.restore) wj *= (float)k;
+    if (r.ews != 0.f) wj *= r.ews;
+    if (r.orig_k > 0 && r.orig_k != k) wj *= sqrtf((float)r.orig_k / (float)k);
+    int ej = te[j];
+    if (ej < 0 || ej >= E) {   // fewer than k experts (cannot happen for a validated config)
+      set_status(p.status, MOE_ERR_BOUNDS);
+      ej = 0;
+    }
+    r.idx[t * k + j] = ej;
+    r.w[t * k + j] = wj;
+  }
+}
+
 template <int BN, int EPI, bool F8 = false>
 __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, int row_in_tile, int nt, int split,
                                            const GemmParams& p, int half, uint4* stg, bool zero = false,
                                            const float* cs = nullptr, const float* cs_gate = nullptr, int ash = 0,
                                            int live_end = 0, uint4* pv_in = nullptr) {
+  if constexpr (EPI == EPI_ROUTER) {
+    router_epilogue<BN>(tbase, row0, rows, row_in_tile, p, half);
+    return;
+  }
   const bool row_ok = row_in_tile < rows;
   const long long row = (long long)row0 + row_in_tile;
   float rs = 1.0f;
@@ -438,14 +570,10 @@ __device__ __forceinline__ void store_tile(uint32_t tbase, int row0, int rows, i
 template <int ROWS, int NST, bool PAIR>
 __device__ __forceinline__ void gather_a_load_rows(const GemmParams& p, const TileCoord& c, int t, int rank,
                                                    int (&tok)[8]) {
-  // a narrow tile's CTA holds N/2 of its rows (the MMA's B operand), else 128
-  const int nn = PAIR ? narrow_cols(p, c) : 0;
-  const int base = nn ? rank * (nn >> 1) : 128 * rank;
-  const int lim = nn ? min(c.rows, base + (nn >> 1)) : c.rows;
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const int r = base + (t >> 3) + 16 * j;   // row of the tile
-    tok[j] = r < lim ? __ldg(p.a_gather + c.row0 + r) : -1;
+    const int r = 128 * rank + (t >> 3) + 16 * j;   // row of the tile
+    tok[j] = r < c.rows ? __ldg(p.a_gather + c.row0 + r) : -1;
   }
 }
 
@@ -466,7 +594,6 @@ __device__ __forceinline__ void gather_a_producer(const GemmParams& p, const int
     gather_a_load_rows<ROWS, NST, PAIR>(p, decode_tile<ROWS>(t_first, p, s_toff, s_goff), t, rank, nxt);
   for (int tile = t_first; tile < total_tiles && ok; tile += t_step) {
     const TileCoord c = decode_tile<ROWS>(tile, p, s_toff, s_goff);
-    const int nn = PAIR ? narrow_cols(p, c) : 0;
     int tok[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -492,19 +619,23 @@ __device__ __forceinline__ void gather_a_producer(const GemmParams& p, const int
       }
       const uint32_t sa = smem_u32(smem + stage * stage_bytes);
       const uint8_t* kb = p.a_src + (long long)kt * 128 + chunk * 16;
-      // a narrow tile's MMA reads only its N/2 rows of the stage
-      const int jn = PAIR && nn ? (nn >> 5) : 8;
+      // the copies of a stage, with or without the keep policy (two loops: no per-copy test)
+      if (p.a_keep) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        if (j >= jn) break;
-        const int r = (t >> 3) + 16 * j;
-        const int src = tok[j];
-        const uint32_t d = sa + r * 128 + ((chunk ^ (r & 7)) << 4);
-        const uint8_t* g = kb + (long long)(src < 0 ? 0 : src) * p.a_ld_bytes;
-        if (p.a_keep)
-          cp_async_16_hint(d, g, src < 0 ? 0u : 16u, keep);
-        else
-          cp_async_16(d, g, src < 0 ? 0u : 16u);
+        for (int j = 0; j < 8; ++j) {
+          const int r = (t >> 3) + 16 * j;
+          const int src = tok[j];
+          cp_async_16_hint(sa + r * 128 + ((chunk ^ (r & 7)) << 4),
+                           kb + (long long)(src < 0 ? 0 : src) * p.a_ld_bytes, src < 0 ? 0u : 16u, keep);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int r = (t >> 3) + 16 * j;
+          const int src = tok[j];
+          cp_async_16(sa + r * 128 + ((chunk ^ (r & 7)) << 4), kb + (long long)(src < 0 ? 0 : src) * p.a_ld_bytes,
+                      src < 0 ? 0u : 16u);
+        }
       }
       cp_async_arrive_noinc(&gath_bar[stage]);
       if (++stage == (uint32_t)NST) { stage = 0; phase ^= 1u; }
@@ -1243,73 +1374,6 @@ __device__ __forceinline__ void swb_pair_tile(uint32_t tbase, const TileCoord& c
   }
 }
 
-// Epilogue of a narrow tile (see narrow_cols): TMEM lane l of quadrant q holds one weight row of this
-// CTA, column j the tile's row j.  SwiGLU: the CTA's 128 weight rows are, per quadrant, 16 up rows
-// then the 16 gate rows of the same h (loaded as 16-row boxes), so lanes l and l + 16 hold u and g of
-// one h; each pair trades half its columns (one shuffle per value) and both compute silu(g) * u,
-// exactly as the normal epilogue does, for 16 rows each.  bf16 or fp32 out: lane l is output column
-// nt * 256 + 128 rank + 32 q + l.  Values go straight to global memory: for each column j one store
-// instruction writes 32 or 64 contiguous bytes of one or two output rows.
-template <int EPI>
-__device__ __forceinline__ void store_narrow(uint32_t tbase, const TileCoord& c, int rank, int quad, int half,
-                                             int lane, const GemmParams& p, int nn) {
-  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-  if (EPI == EPI_SWIGLU) {
-    const bool lo = lane < 16;
-    const int hcol = c.nt * 128 + 64 * rank + 16 * quad + (lane & 15);
-    const bool col_ok = hcol < p.N;
-    __nv_bfloat16* pre = reinterpret_cast<__nv_bfloat16*>(p.preact);
-#pragma unroll 1
-    for (int cc = half; cc * 32 < nn; cc += kEpiWarps / 4) {
-      uint32_t v[32];
-      __syncwarp();
-      tmem_ld_32x32b_x32(tbase + cc * 32, v);
-      tmem_ld_wait();
-      const int t0 = cc * 32 + (lo ? 0 : 16);   // this lane's first row of the tile
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        // lo lanes keep columns 0-15 (their u) and take g from lane + 16; hi lanes keep 16-31 (g)
-        const uint32_t give = lo ? v[16 + j] : v[j];
-        const uint32_t got = __shfl_xor_sync(0xffffffffu, give, 16);
-        const float u = __uint_as_float(lo ? v[j] : got);
-        const float g = __uint_as_float(lo ? got : v[16 + j]);
-        const int t = t0 + j;
-        if (t < c.rows && col_ok) {
-          const long long row = (long long)c.row0 + t;
-          // silu(g) = g / (1 + e^-g); the approximate division returns 0 when e^-g overflows
-          out[row * p.ldo + hcol] = __float2bfloat16_rn(__fdividef(g, 1.0f + __expf(-g)) * u);
-          if (pre) {
-            pre[row * p.preact_ld + hcol] = __float2bfloat16_rn(u);
-            pre[row * p.preact_ld + p.N + hcol] = __float2bfloat16_rn(g);
-          }
-        }
-      }
-    }
-  } else {
-    const int col = c.nt * 256 + 128 * rank + 32 * quad + lane;
-    const bool col_ok = col < p.N;
-    float* out32 = reinterpret_cast<float*>(p.out);
-#pragma unroll 1
-    for (int cc = half; cc * 32 < nn; cc += kEpiWarps / 4) {
-      uint32_t v[32];
-      __syncwarp();
-      tmem_ld_32x32b_x32(tbase + cc * 32, v);
-      tmem_ld_wait();
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int t = cc * 32 + j;
-        if (t < c.rows && col_ok) {
-          const long long o = ((long long)c.row0 + t) * p.ldo + col;
-          if (EPI == EPI_F32)
-            out32[o] = __uint_as_float(v[j]);
-          else
-            out[o] = __float2bfloat16_rn(__uint_as_float(v[j]));
-        }
-      }
-    }
-  }
-}
-
 // GB: the B operand of a K-grouped fp32 GEMM is gathered by the kernel (gather_b_mn_producer).
 template <int EPI, bool F8 = false, bool GA = false, bool GB = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsGA : kThreads, 1)
@@ -1373,7 +1437,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
   if (warp == 0 && lane == 0) {
     if (!GA) tma_prefetch_desc(&tmA);
     if (!GB) tma_prefetch_desc(&tmB);
-    if (C::SWB || p.narrow_max > 0) tma_prefetch_desc(&tmP);
+    if constexpr (C::SWB) tma_prefetch_desc(&tmP);
   }
   tc_fence_before();
   __syncthreads();
@@ -1395,34 +1459,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
         const int brow = EPI == EPI_SWIGLU
                              ? c.group * p.b_rows_per_group + c.nt * 128 + (rank ? p.b_gate_offset : 0)
                              : c.group * p.b_rows_per_group + c.nt * C::BN + 128 * (int)rank;
-        // narrow tile: the weights fill the second region as the MMA's A operand, the tile's rows
-        // (N/2 per CTA) the first; bf16 / fp32 out loads those rows as 32-row boxes of tmP
-        const int nn = (EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_F32) && !F8 ? narrow_cols(p, c) : 0;
-        const int nrow0 = c.row0 + (int)rank * (nn >> 1);
-        const int nbox = nn ? (min(max(c.rows - (int)rank * (nn >> 1), 0), nn >> 1) + 31) >> 5 : 0;
-        const int nbox_both = nn ? ((min(c.rows, nn >> 1) + 31) >> 5) + ((max(c.rows - (nn >> 1), 0) + 31) >> 5) : 0;
         for (int kt = c.kt0; kt < c.kt1; ++kt) {
           if (!mbar_wait_cluster(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
           const uint32_t full0 = map_to_cta(smem_u32(&full_bar[stage]), 0);
           const int kx = kt * (F8 ? 2 * BK : BK);
-          if (nn) {
-            if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], 2 * C::B_BYTES + (GA ? 0 : nbox_both * 4096));
-            if (EPI == EPI_SWIGLU) {
-              // per quadrant q: 16 up rows, then the gate rows of the same 16 h
-              const int r0 = c.group * p.b_rows_per_group + c.nt * 128 + 64 * (int)rank;
-              for (int q = 0; q < 4; ++q) {
-                tma_load_2d_pair(sa + C::A_BYTES + q * 4096, &tmP, full0, kx, r0 + 16 * q);
-                tma_load_2d_pair(sa + C::A_BYTES + q * 4096 + 2048, &tmP, full0, kx, r0 + 16 * q + p.b_gate_offset);
-              }
-            } else {
-              tma_load_2d_pair(sa + C::A_BYTES, &tmB, full0, kx, brow);
-            }
-            if (!GA)
-              for (int b = 0; b < nbox; ++b) tma_load_2d_pair(sa + b * 4096, &tmP, full0, kx, nrow0 + 32 * b);
-            if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
-            continue;
-          }
           // a group's last tile with <= 128 rows has none in CTA 1: CTA 1 skips its A rows
           // (its accumulator rows are never stored) and saves their L2 bytes
           const bool a1 = c.rows > 128;
@@ -1458,7 +1499,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
       int it = 0;
       for (int t = pair; t < total_tiles; t += npairs, ++it) {
         const TileCoord c = decode_tile<BM2>(t, p, s_toff, s_goff);
-        const int nn = (EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_F32) && !F8 ? narrow_cols(p, c) : 0;
         const int acc = it & 1;
         const uint32_t use = (uint32_t)(it >> 1);
         if (!mbar_wait_cluster(&tempty_bar[acc], (use & 1u) ^ 1u, abort_flag, p.status)) break;
@@ -1471,17 +1511,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
           const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
           const bool amn = !GA && p.a_mn;
           const bool bmn = EPI != EPI_SWIGLU && p.b_mn;
-          uint64_t a_desc = amn ? umma_sdesc_mn_sw128(sa, 8192) : umma_sdesc_sw128(sa);
-          uint64_t b_desc = bmn ? umma_sdesc_mn_sw128(sa + C::A_BYTES, 8192) : umma_sdesc_sw128(sa + C::A_BYTES);
+          const uint64_t a_desc = amn ? umma_sdesc_mn_sw128(sa, 8192) : umma_sdesc_sw128(sa);
+          const uint64_t b_desc = bmn ? umma_sdesc_mn_sw128(sa + C::A_BYTES, 8192) : umma_sdesc_sw128(sa + C::A_BYTES);
           const uint64_t a_step = amn ? 2048 / 16 : 2;
           const uint64_t b_step = bmn ? 2048 / 16 : 2;
           // bits 15 / 16 of the instruction descriptor: A / B is MN-major
-          uint32_t id = idesc | (amn ? (1u << 15) : 0u) | (bmn ? (1u << 16) : 0u);
-          if (nn) {   // narrow tile: the weights (second region) are A, the tile's rows B, N = nn
-            a_desc = umma_sdesc_sw128(sa + C::A_BYTES);
-            b_desc = umma_sdesc_sw128(sa);
-            id = umma_idesc_bf16_f32(BM2, nn);
-          }
+          const uint32_t id = idesc | (amn ? (1u << 15) : 0u) | (bmn ? (1u << 16) : 0u);
 #pragma unroll
           for (int kk = 0; kk < BK / UMMA_K; ++kk) {
             if (F8)
@@ -1533,12 +1568,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
         cs = p.b_scale + brow;
         cs_gate = cs + p.b_gate_offset;
       }
-      const int nn = (EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_F32) && !F8 ? narrow_cols(p, c) : 0;
       if constexpr (C::SWB) {
         swb_pair_tile<C>(tbase, c, (int)rank, row_in_tile, p, half, stg, smem, &tmP, pre_full, pre_empty, pre_issuer,
                          pre_issued, pre_used, ash, live_end, abort_flag);
-      } else if (nn) {
-        store_narrow<EPI>(tbase, c, (int)rank, quad, half, lane, p, nn);
       } else {
         // K-grouped: the group's output slice, zeros for a group without rows
         store_tile<C::BN, EPI, F8>(tbase, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, c.nt,
@@ -1772,6 +1804,12 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   }
   const bool pair = q.pair_tiles != 0;
   const bool f8 = q.e4m3 != 0;
+  // router epilogue: dense 1-CTA tiles holding all N columns, no split-K
+  if (q.epilogue == EPI_ROUTER &&
+      (pair || f8 || q.splits > 1 || q.num_groups > 0 || q.k_groups > 0 || q.a_gather || q.b_mn_major ||
+       q.a_mn_major || q.N > q.bn || q.router.k < 1 || q.router.k > kRouterFusedK || !q.router.idx || !q.router.w ||
+       (q.bn != 32 && q.bn != 64 && q.bn != 128)))
+    return cudaErrorInvalidValue;
   if (pair && (q.bn != 256 || q.splits > 1 || (q.epilogue == EPI_F32 && q.e4m3))) return cudaErrorInvalidValue;
   if (f8 && (q.bn != 256 || q.splits > 1 || q.k_groups > 0 || q.epilogue == EPI_F32 || !q.a_scale || !q.b_scale))
     return cudaErrorInvalidValue;
@@ -1806,18 +1844,6 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   if (q.epilogue == EPI_SWIGLU_BWD &&
       (q.num_groups == 0 || !q.a_off || !q.preact || !q.out2 || f8 || ga || q.bn != 256 || q.splits > 1 ||
        q.ldo < 2 * (int64_t)q.N || q.ldo % 8 || q.ldo2 < q.N || q.ldo2 % 8))
-    return cudaErrorInvalidValue;
-  // narrow tiles (see narrow_cols): grouped CTA-pair GEMMs on bf16 operands, SwiGLU with gathered A
-  // rows or bf16 out with TMA-loaded A; tmP then holds 16-row boxes of the SwiGLU weights, or 32-row
-  // boxes of A
-  const bool narrow = q.narrow_max > 0;
-  if (narrow && (!pair || q.num_groups == 0 || f8 || q.splits > 1 || q.a_off || q.b_mn_major || q.a_mn_major ||
-                 q.k_groups > 0 || q.narrow_max % 32 || q.narrow_max > 256 ||
-                 !((q.epilogue == EPI_SWIGLU && ga) || ((q.epilogue == EPI_BF16 || q.epilogue == EPI_F32) && !ga))))
-    return cudaErrorInvalidValue;
-  CUtensorMap tn;
-  if (narrow && !(q.epilogue == EPI_SWIGLU ? make_tmap(&tn, q.B, q.b_rows_total, q.K, 16, false)
-                                           : make_tmap(&tn, q.A, q.M, q.K, 32, false)))
     return cudaErrorInvalidValue;
   const int b_box = (q.epilogue == EPI_SWIGLU || pair) ? q.bn / 2 : q.bn;
   CUtensorMap ta, tb;
@@ -1874,15 +1900,14 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.preact_dense = q.preact_dense;
   gp.out2 = q.out2;
   gp.ldo2 = q.ldo2;
-  gp.narrow_max = narrow ? q.narrow_max : 0;
-  gp.tile_seq = q.num_groups > 0 && q.k_groups == 0 ? q.tile_seq : nullptr;
   gp.a_keep = ga ? q.a_keep : 0;
+  gp.router = q.router;
   gp.status = q.status;
 
   if (ga) {
     if (pair)
       return f8 ? launch_pair_impl<EPI_SWIGLU, true, true>(ta, tb, gp, 0, stream)
-                : launch_pair_impl<EPI_SWIGLU, false, true>(ta, tb, gp, 0, stream, narrow ? &tn : nullptr);
+                : launch_pair_impl<EPI_SWIGLU, false, true>(ta, tb, gp, 0, stream);
     const int grid = num_sms();
     return f8 ? launch_impl<256, EPI_SWIGLU, true, true>(q, ta, tb, gp, grid, stream)
               : launch_impl<256, EPI_SWIGLU, false, true>(q, ta, tb, gp, grid, stream);
@@ -1896,7 +1921,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
     if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU>(ta, tb, gp, tiles, stream);
     if (gb) return launch_pair_impl<EPI_F32, false, false, true>(ta, tb, gp, tiles, stream);   // K-grouped, B gathered
     if (q.epilogue == EPI_F32)   // fp32 out: dense, or grouped (the layer's fp32 expert rows)
-      return launch_pair_impl<EPI_F32>(ta, tb, gp, tiles, stream, narrow ? &tn : nullptr);
+      return launch_pair_impl<EPI_F32>(ta, tb, gp, tiles, stream);
     if (q.epilogue == EPI_SWIGLU_BWD) {
       // the [u | g] rows as 128 x 32 boxes, 64-byte swizzle (the epilogue reads a row per lane)
       CUtensorMap tp;
@@ -1905,7 +1930,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
         return cudaErrorInvalidValue;
       return launch_pair_impl<EPI_SWIGLU_BWD>(ta, tb, gp, tiles, stream, &tp);
     }
-    return launch_pair_impl<EPI_BF16>(ta, tb, gp, tiles, stream, narrow ? &tn : nullptr);
+    return launch_pair_impl<EPI_BF16>(ta, tb, gp, tiles, stream);
   }
   int grid = num_sms();
   if (q.num_groups == 0) {
@@ -1926,6 +1951,13 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
       break;
     case EPI_SWIGLU_BWD:
       return launch_impl<256, EPI_SWIGLU_BWD>(q, ta, tb, gp, grid, stream);
+    case EPI_ROUTER:
+      switch (q.bn) {
+        case 128: return launch_impl<128, EPI_ROUTER>(q, ta, tb, gp, grid, stream);
+        case 64: return launch_impl<64, EPI_ROUTER>(q, ta, tb, gp, grid, stream);
+        case 32: return launch_impl<32, EPI_ROUTER>(q, ta, tb, gp, grid, stream);
+      }
+      break;
     case EPI_F32:
       switch (q.bn) {
         case 256: return launch_impl<256, EPI_F32>(q, ta, tb, gp, grid, stream);

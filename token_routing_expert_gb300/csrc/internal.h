@@ -9,7 +9,21 @@ namespace moe {
 
 // EPI_SWIGLU_BWD: the product is dH of the SwiGLU experts (rounded to bf16); the epilogue reads the
 // pre-activations [u | g] of the same rows and writes dUG = [dU | dG] to out and H to out2 (bf16).
-enum GemmEpilogue { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2, EPI_SWIGLU_BWD = 3 };
+enum GemmEpilogue { EPI_F32 = 0, EPI_BF16 = 1, EPI_SWIGLU = 2, EPI_SWIGLU_BWD = 3, EPI_ROUTER = 4 };
+
+// Router GEMM tiles that hold every expert of their rows (one n-tile, no split-K) can run the
+// gating, top-k, weights, normalisation and scalings in their epilogue (EPI_ROUTER), for top_k up
+// to this many.
+constexpr int kRouterFusedK = 8;
+struct RouterEpilogue {
+  const float* b_router;     // (E) or NULL: added to the logits
+  const float* score_bias;   // (E) or NULL: added to the scores for selection only
+  float* logits;             // (T, E) or NULL: the logits (with the router bias) are also stored
+  int32_t* idx;              // (T, k)
+  float* w;                  // (T, k)
+  int gating, k, restore, orig_k;
+  float sig_eps, p_norm, ews;
+};
 
 // C[M, N] = A[M, K] * B[N, K]^T per group, A and B bf16 K-major, fp32 accumulate.
 // Groups (optional) are contiguous row ranges of A / C given by device
@@ -77,12 +91,7 @@ struct GemmProblem {
   int64_t mx_out_ld;
   int a_keep;             // gathered A: 1 reads the source rows with an evict_last L2 policy (for a_src that
                           //   fits the L2 beside the streamed weights, so its rows are not fetched again)
-  const int* tile_seq;    // grouped, M tiles: non-NULL runs the row tiles in this order (tile_seq[s] = the
-                          //   s-th to run, numbered as tile_off counts them) instead of expert order
-  int narrow_max;         // > 0 (grouped, CTA pairs, bf16 operands, SwiGLU with gathered A or bf16 out; a
-                          //    multiple of 32, <= 256): a group's tile with at most this many rows runs with the
-                          //    operands swapped, the weights as the MMA's 256 rows and the tile's rows as its N
-                          //    (rounded up to 32), so its tensor-core work follows the rows it has
+  RouterEpilogue router;  // EPI_ROUTER
   int* status;
 };
 
@@ -105,8 +114,8 @@ cudaError_t launch_topk(const float* logits, int n_partials, int64_t partial_str
 
 // chunk: assignments per block, a multiple of 256 in [256, 4096]; blk_scratch holds
 // permute_blocks(R, chunk) * E ints.
-// tile_off (optional, E + 1 ints and then one per row tile): also the grouped GEMMs' tile table,
-// prefix sums of ceil(count / rows_per_tile) and the row-tile order, as launch_tile_table writes them.
+// tile_off (optional, E + 1 ints): also the grouped GEMMs' tile table, prefix sums of
+// ceil(count / rows_per_tile), as launch_tile_table would write it.
 // The permutation of R assignments over E experts runs as one cluster launch (else three kernels).
 bool permute_fits_cluster(int R, int E);
 cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, int32_t* offsets,

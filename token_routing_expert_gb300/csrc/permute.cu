@@ -24,44 +24,6 @@ constexpr int kPermWarps = kPermThreads / 32;
 
 int permute_blocks(int R, int chunk) { return (R + chunk - 1) / chunk; }
 
-// The grouped GEMMs' row-tile order, written after tile_off.  An expert with several row tiles
-// reuses its weights from L2 across them, so its tiles are bound by the tensor cores; an expert
-// with one row tile reads its weights once from HBM, and its tiles are bound by HBM.  Run in
-// expert order, the two kinds come in bursts (a hot expert's tiles fill the GPU for a while, then
-// a run of single-tile experts leaves the tensor cores waiting on HBM).  The two streams, each in
-// expert order, are merged evenly instead: the multi-tile stream's i-th row tile has key
-// (2i + 1) / nH, the single-tile stream's j-th (2j + 1) / nC, and tiles run in key order (the
-// multi-tile stream first on equal keys).  seq[s] = the s-th row tile to run, as its index in
-// expert order (tile_off's numbering).  Every thread of one block calls it; tiles / texcl are the
-// thread's expert's row tiles and their exclusive prefix (0 for threads past E); only threads with
-// `write` store.
-__device__ void write_tile_seq(int tiles, int texcl, int E, int* s_warp, int* s_tot, int32_t* seq, bool write) {
-  const int e = threadIdx.x;
-  const bool hot = tiles >= 2, cold = tiles == 1;
-  __syncthreads();
-  const int h_excl = block_exclusive_scan(hot ? tiles : 0, s_warp);
-  if (threadIdx.x == blockDim.x - 1) s_tot[0] = h_excl + (hot ? tiles : 0);
-  __syncthreads();
-  const int c_excl = block_exclusive_scan(cold ? 1 : 0, s_warp);
-  if (threadIdx.x == blockDim.x - 1) s_tot[1] = c_excl + (cold ? 1 : 0);
-  __syncthreads();
-  const long long nH = s_tot[0], nC = s_tot[1];
-  if (!write || e >= E) return;
-  for (int l = 0; l < tiles; ++l) {
-    long long pos = texcl + l;
-    if (nH > 0 && nC > 0) {
-      if (hot) {   // single-tile j runs before multi-tile i iff (2j + 1) nH < (2i + 1) nC
-        const long long i = h_excl + l, x = (2 * i + 1) * nC - 1 - nH;
-        pos = i + (x >= 0 ? min(x / (2 * nH) + 1, nC) : 0);
-      } else {     // multi-tile i runs before single-tile j iff (2i + 1) nC <= (2j + 1) nH
-        const long long j = c_excl, y = (2 * j + 1) * nH - nC;
-        pos = j + (y >= 0 ? min(y / (2 * nC) + 1, nH) : 0);
-      }
-    }
-    seq[pos] = texcl + l;
-  }
-}
-
 // Assignments per block: about 76 blocks (the scan walks one histogram per block,
 // so more blocks cost more than they gain), 256 to 4096, a multiple of 256 (each
 // of the 8 warps walks chunk / 8 assignments).
@@ -157,7 +119,6 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ b
       tile_off[t] = texcl;
       if (t == E - 1) tile_off[E] = texcl + tiles;
     }
-    write_tile_seq(tiles, texcl, E, s_warp, s_tot, tile_off + E + 1, true);
   }
 }
 
@@ -316,8 +277,6 @@ __global__ void __launch_bounds__(kClusterThreads) perm_cluster_kernel(const int
       tile_off[e] = texcl;
       if (e == E - 1) tile_off[E] = texcl + tiles;
     }
-    __shared__ int s_tot2[2];
-    write_tile_seq(tiles, texcl, E, s_warp, s_tot2, tile_off + E + 1, rank == 0);
   }
   __syncthreads();   // the bases in wh are complete
   cluster_sync_all();   // no CTA leaves while another still reads its histogram
@@ -394,14 +353,12 @@ cudaError_t launch_permute(const int32_t* idx, int R, int E, int32_t* counts, in
   return cudaGetLastError();
 }
 
-// tile_off[e] = sum over e' < e of ceil(count[e'] / rows_per_tile); tile_off[E] = total tiles;
-// then the row-tile order (write_tile_seq) from tile_off[E + 1] on.
+// tile_off[e] = sum over e' < e of ceil(count[e'] / rows_per_tile); tile_off[E] = total tiles.
 __global__ void __launch_bounds__(1024) tile_table_kernel(const int32_t* __restrict__ offsets, int E, int rows_per_tile,
                                                            int32_t* __restrict__ tile_off) {
   pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
   pdl_trigger();
   __shared__ int s_warp[32];
-  __shared__ int s_tot[2];
   const int e = threadIdx.x;
   const int tiles = e < E ? (offsets[e + 1] - offsets[e] + rows_per_tile - 1) / rows_per_tile : 0;
   const int excl = block_exclusive_scan(tiles, s_warp);
@@ -409,7 +366,6 @@ __global__ void __launch_bounds__(1024) tile_table_kernel(const int32_t* __restr
     tile_off[e] = excl;
     if (e == E - 1) tile_off[E] = excl + tiles;
   }
-  write_tile_seq(tiles, excl, E, s_warp, s_tot, tile_off + E + 1, true);
 }
 
 cudaError_t launch_tile_table(const int32_t* offsets, int E, int rows_per_tile, int32_t* tile_off,

@@ -19,7 +19,8 @@ import pytest
 import torch
 
 from oracle import moe_ref as ref
-from tests.oracle_bridge import assert_close_layer, check_topk, f64, half_ulp_bf16, oracle_config, oracle_weights
+from tests.oracle_bridge import (MAX_ABS, assert_close_layer, check_topk, f64, half_ulp_bf16, oracle_config,
+                                 oracle_weights)
 from token_routing_expert_gb300 import native
 from token_routing_expert_gb300.workloads import WORKLOADS, WorkloadSpec, generate
 
@@ -62,6 +63,18 @@ CASES = {
     # tiles, the last one ragged (320 = 256 + 64)
     "router_pair": WorkloadSpec("router_pair", T=1500, d_model=512, num_experts=320, top_k=4, hidden_size=64,
                                 gating="sigmoid", score_bias_std=0.01, seed=23),
+    # wide pair tiles (two 256-column n-tiles per tile, each k-tile of A feeding both): grouped GEMM 2
+    # over d_model = 2048 (4 wide tiles per 256-row tile), skewed loads for ragged group tails
+    "wide_tiles": WorkloadSpec("wide_tiles", T=4096, d_model=2048, num_experts=16, top_k=4, hidden_size=1024,
+                               gating="sigmoid", skew=True, seed=40),
+    # the same with the weights restored x top_k: grouped GEMM 2 writes fp32 rows (256-column tiles)
+    "wide_tiles_restore": WorkloadSpec("wide_tiles_restore", T=4096, d_model=2048, num_experts=16, top_k=4,
+                                       hidden_size=1024, gating="sigmoid", normalize_expert_weights=1.0,
+                                       restore_weight_scale=True, seed=41),
+    # the latent projections (dense) and grouped GEMM 2 on wide tiles: T = 10,240 rows, latent 2048,
+    # d_model 4096
+    "wide_tiles_latent": WorkloadSpec("wide_tiles_latent", T=10240, d_model=4096, num_experts=32, top_k=2,
+                                      hidden_size=1024, latent_dim=2048, gating="softmax", skew=True, seed=42),
     # more than 128 experts and few row tiles: the router GEMM takes a 3-way split-K whose slices
     # top-k adds itself (up to 128 experts the router's epilogue runs the top-k; a deeper split, as
     # in the latent decode workload, goes through the separate sum)
@@ -133,6 +146,15 @@ def test_router_fused_epilogue(name):
                     assert row.index(a) < row.index(b)
 
 
+def router_logit_tol(x, w_router, logits):
+    """The bar for fp32 router logits against the float64 oracle: 1e-5 absolute and relative, plus
+    the usual statistical estimate of a length-d fp32 dot product's rounding error,
+    2^-24 * sqrt(d) * sum_i |x_i w_i| (bf16 products are exact in fp32; only the sums round).  The
+    last term matters for long rows: d = 4096 logits of size ~2 carry ~3e-5 of accumulated rounding."""
+    d = x.shape[1]
+    return 1e-5 + 1e-5 * np.abs(logits) + 2.0 ** -24 * np.sqrt(d) * (np.abs(x) @ np.abs(w_router).T)
+
+
 @pytest.mark.parametrize("name", list(CASES))
 def test_router(name):
     spec, inp, cfg, wts = setup(name)
@@ -145,13 +167,17 @@ def test_router(name):
     oc, ow = oracle_config(spec), oracle_weights(spec, inp)
     r = ref.route(oc, f64(inp["x"]), ow.w_router, ow.b_router, ow.score_bias)
     lg = logits.double().cpu().numpy()
-    assert np.all(np.abs(lg - r.logits) <= 1e-5 + 1e-5 * np.abs(r.logits)), np.abs(lg - r.logits).max()
+    tol = router_logit_tol(f64(inp["x"]), ow.w_router, r.logits)
+    assert np.all(np.abs(lg - r.logits) <= tol), np.abs(lg - r.logits).max()
     gi = idx.cpu().numpy().astype(np.int64)
     check_topk(gi, r.keys, r.idx, k)
     # the weights of the GPU's own choice, computed by the oracle
     rf = ref.route(oc, f64(inp["x"]), ow.w_router, ow.b_router, ow.score_bias, forced_idx=gi)
     gw = w.double().cpu().numpy()
-    assert np.all(np.abs(gw - rf.weights) <= 1e-5 + 1e-5 * np.abs(rf.weights)), np.abs(gw - rf.weights).max()
+    # a logit error dl moves a softmax or sigmoid weight (and its normalisation) by at most 2 |w| max|dl|
+    dl = (tol - 1e-5 - 1e-5 * np.abs(r.logits)).max(axis=1, keepdims=True)
+    wtol = 1e-5 + 1e-5 * np.abs(rf.weights) + 2 * np.abs(rf.weights) * dl
+    assert np.all(np.abs(gw - rf.weights) <= wtol), np.abs(gw - rf.weights).max()
     # without a logits output the choice is the same
     _, idx2, w2 = native.moe_router(cfg, wts, x, ws)
     expect_ok()
@@ -330,7 +356,7 @@ def test_combine(name):
     assert np.all(np.abs(got - want) <= 2.0 ** -8 * np.abs(want) + 1e-5), np.abs(got - want).max()
 
 
-@pytest.mark.parametrize("name", ["latent_skew", "latent_decode_small", "pair_tiles_latent"])
+@pytest.mark.parametrize("name", ["latent_skew", "latent_decode_small", "pair_tiles_latent", "wide_tiles_latent"])
 def test_latent_down_and_restore(name):
     spec, inp, cfg, wts = setup(name)
     T, D, L = spec.T, spec.d_model, spec.latent_dim
@@ -376,11 +402,13 @@ def test_layer_forward(name):
     run_layer_and_compare(spec, inp, cfg, wts)
 
 
-@pytest.mark.parametrize("name", ["sigmoid_bias_restore", "softmax_p2_scales", "router_pair", "pair_tiles_restore"])
+@pytest.mark.parametrize("name", ["sigmoid_bias_restore", "softmax_p2_scales", "router_pair", "pair_tiles_restore",
+                                  "wide_tiles_restore"])
 def test_inference_forward_keeps_fp32_expert_rows(name):
     """Layers whose routing weights can add up to more than one keep y in fp32 in the inference
     forward: its rows round to the training forward's bf16 rows bit for bit (the same fp32 products),
-    and the output error beyond its own bf16 rounding stays far under the bar."""
+    and the output error beyond its own bf16 rounding stays within a quarter of the bar (what is
+    left is mostly H's bf16 rounding ahead of grouped GEMM 2, which grows with h: 5e-3 at h = 1024)."""
     spec, inp, cfg, wts = setup(name)
     assert native.moe_layer_expert_rows_fp32(cfg)
     T = spec.T
@@ -402,7 +430,7 @@ def test_inference_forward_keeps_fp32_expert_rows(name):
     want = ref.layer_forward(oc, f64(inp["x"]), ow, forced_idx=forced).out
     got = out.double().cpu().numpy()
     excess = (np.abs(got - want) - half_ulp_bf16(want)).max()
-    assert excess <= 2e-3, f"{name}: error beyond the output's half-ulp {excess:.3e}"
+    assert excess <= MAX_ABS / 4, f"{name}: error beyond the output's half-ulp {excess:.3e}"
 
 
 def test_layer_forward_repeatable_and_stream_ordered():

@@ -1196,17 +1196,53 @@ __global__ void __launch_bounds__(kThreadsMX, 1)
 // ---------------------------------------------------------------------------
 constexpr int BM2 = 256;
 
+// Wide-tile epilogue for one 256-column accumulator with bf16 out (bf16 operands): the warp takes
+// its whole share of the accumulator (4 chunks of 32 columns) into registers as packed bf16,
+// releases the accumulator, and only then stores, so the next tile's MMAs into this accumulator
+// start while the stores drain.  Releasing after the stores, as the 256-column tiles do, left
+// grouped GEMM 2 slower on wide tiles than on 256-column ones.
+__device__ __forceinline__ void drain_wide_bf16(uint32_t tb, int row0, int rows, int row_in_tile, int nt,
+                                                const GemmParams& p, int half, uint4* stg, uint64_t* tempty) {
+  const int lane = row_in_tile & 31;
+  const int valid = min(max(rows - (row_in_tile - lane), 0), 32);
+  const long long wrow0 = (long long)row0 + (row_in_tile - lane);
+  uint32_t pk[4][16];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t v[32];
+    tmem_ld_32x32b_x32(tb + (half + 2 * i) * 32, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < 16; ++q) pk[i][q] = pack_bf16x2(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive_cluster(map_to_cta(smem_u32(tempty), 0));
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + wrow0 * p.ldo;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int col0 = nt * 256 + (half + 2 * i) * 32;
+    if (valid > 0 && col0 < p.N) store_block_bf16(stg, pk[i], out + col0, p.ldo, valid, lane);
+  }
+}
+
 // SwiGLU backward: 4 stages, and a ring of [u | g] boxes for the epilogue (2 slots for each
 // half of the epilogue warps, 16 KB each: 128 rows x 32 columns of u and of g), with a full and
 // an empty barrier per slot.
-template <int EPI>
+// W2 (wide tiles, bf16 out): a tile spans two adjacent 256-column n-tiles that share each k-tile
+// of A; a stage holds A and both n-tiles' B halves (48 KB, 4 stages), and the two accumulators
+// (TMEM columns 0-255 and 256-511) hold the tile's two n-tiles instead of alternating between tiles.
+template <int EPI, bool W2 = false>
 struct PairCfgT {
   static constexpr bool SWB = EPI == EPI_SWIGLU_BWD;
-  static constexpr int BN = 256;
+  static_assert(!(W2 && SWB), "wide tiles: forward epilogues only");
+  static constexpr int BN = 256;                            // columns of one accumulator
+  static constexpr int NB = W2 ? 2 : 1;                     // n-tiles per tile
   static constexpr int A_BYTES = 128 * BK * 2;
-  static constexpr int B_BYTES = (BN / 2) * BK * 2;
+  static constexpr int B_BYTES = NB * (BN / 2) * BK * 2;
+  static constexpr int B_PART = (BN / 2) * BK * 2;          // one n-tile's B half
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES = SWB ? 4 : 6;
+  static constexpr int STAGES = W2 ? 4 : (SWB ? 4 : 6);
   static constexpr int ACC_STRIDE = 256;
   static constexpr int TMEM_COLS = 512;
   static constexpr int PRE_SLOTS = 2;                       // per half of the epilogue warps
@@ -1375,13 +1411,16 @@ __device__ __forceinline__ void swb_pair_tile(uint32_t tbase, const TileCoord& c
 }
 
 // GB: the B operand of a K-grouped fp32 GEMM is gathered by the kernel (gather_b_mn_producer).
-template <int EPI, bool F8 = false, bool GA = false, bool GB = false>
+// W2: wide tiles (PairCfgT); p.n_tiles counts tiles of two n-tiles, tile nt covering n-tiles 2 nt
+// and 2 nt + 1.
+template <int EPI, bool F8 = false, bool GA = false, bool GB = false, bool W2 = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsGA : kThreads, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmP, const GemmParams p) {
   pdl_wait();   // the previous kernel on the stream is done (programmatic launch, see launch_pdl)
   pdl_trigger();
-  using C = PairCfgT<EPI>;
+  using C = PairCfgT<EPI, W2>;
+  static_assert(!W2 || (EPI == EPI_BF16 && !F8 && !GA && !GB), "wide tiles: bf16 out, TMA-loaded operands");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
@@ -1456,9 +1495,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
         const TileCoord c = decode_tile<BM2>(t, p, s_toff, s_goff);
         const int arow = c.row0 + 128 * (int)rank;
         const int ash = a_row_shift(p, c, s_goff, s_aoff);
+        // B rows of the tile's first n-tile (a wide tile's second n-tile starts 256 rows later)
+        const int nt0 = W2 ? 2 * c.nt : c.nt;
         const int brow = EPI == EPI_SWIGLU
-                             ? c.group * p.b_rows_per_group + c.nt * 128 + (rank ? p.b_gate_offset : 0)
-                             : c.group * p.b_rows_per_group + c.nt * C::BN + 128 * (int)rank;
+                             ? c.group * p.b_rows_per_group + nt0 * 128 + (rank ? p.b_gate_offset : 0)
+                             : c.group * p.b_rows_per_group + nt0 * C::BN + 128 * (int)rank;
         for (int kt = c.kt0; kt < c.kt1; ++kt) {
           if (!mbar_wait_cluster(&empty_bar[stage], phase ^ 1u, abort_flag, p.status)) { ok = false; break; }
           uint8_t* sa = smem + stage * C::STAGE_BYTES;
@@ -1486,13 +1527,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
                                c.group * p.b_rows_per_group + kt * BK);
           } else {
             tma_load_2d_pair(sa + C::A_BYTES, &tmB, full0, kx, brow);
+            if (W2) tma_load_2d_pair(sa + C::A_BYTES + C::B_PART, &tmB, full0, kx, brow + C::BN);
           }
           if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && rank == 0) {
+    if (lane == 0 && rank == 0 && W2) {
+      // ---------------- UMMA issuer, wide tiles (CTA 0) ----------------
+      // Each k-tile feeds accumulator 0 (B part 0) and accumulator 1 (B part 1).  The epilogue
+      // frees accumulator 0 first; until accumulator 1 is free as well, the MMAs into accumulator 0
+      // run ahead by up to the ring's depth, so the tensor pipe keeps working while the epilogue
+      // reads the previous tile's second half.
+      constexpr uint32_t idesc = umma_idesc_bf16_f32(BM2, C::BN);
+      uint32_t stage = 0, phase = 0;        // ring position of the next k-tile for accumulator 1
+      uint32_t a_stage = 0, a_phase = 0;    // ring position of the next k-tile for accumulator 0
+      int it = 0;
+      auto mma_k_tile = [&](uint32_t st, int acc, bool acc_in) {
+        const uint32_t sa = smem_u32(smem + st * C::STAGE_BYTES);
+        const uint64_t a_desc = umma_sdesc_sw128(sa);
+        const uint64_t b_desc = umma_sdesc_sw128(sa + C::A_BYTES + acc * C::B_PART);
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * C::ACC_STRIDE);
+#pragma unroll
+        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+          umma_bf16_pair(d_tmem, a_desc + 2 * kk, b_desc + 2 * kk, idesc, (acc_in || kk > 0) ? 1u : 0u);
+      };
+      for (int t = pair; t < total_tiles; t += npairs, ++it) {
+        const TileCoord c = decode_tile<BM2>(t, p, s_toff, s_goff);
+        const uint32_t par = ((uint32_t)it & 1u) ^ 1u;   // each accumulator is used once per tile
+        if (!mbar_wait_cluster(&tempty_bar[0], par, abort_flag, p.status)) break;
+        tc_fence_after();
+        bool ok = true, have1 = false;
+        int ka = c.kt0;
+        for (int kb = c.kt0; kb < c.kt1; ++kb) {
+          // accumulator 0's MMAs for k-tile kb, and beyond it while accumulator 1 is busy
+          while (ka <= kb ||
+                 (!have1 && ka < c.kt1 && ka - kb < C::STAGES && !mbar_test(&tempty_bar[1], par))) {
+            if (!mbar_wait_cluster(&full_bar[a_stage], a_phase, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            mma_k_tile(a_stage, 0, ka > c.kt0);
+            ++ka;
+            if (++a_stage == C::STAGES) { a_stage = 0; a_phase ^= 1u; }
+          }
+          if (!ok) break;
+          if (!have1) {
+            if (!mbar_wait_cluster(&tempty_bar[1], par, abort_flag, p.status)) { ok = false; break; }
+            tc_fence_after();
+            have1 = true;
+          }
+          mma_k_tile(stage, 1, kb > c.kt0);
+          umma_commit_pair(&empty_bar[stage], 0x3);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull_bar[0], 0x3);
+        umma_commit_pair(&tfull_bar[1], 0x3);
+      }
+    } else if (lane == 0 && rank == 0) {
       // ---------------- UMMA issuer (CTA 0) ----------------
       constexpr uint32_t idesc = F8 ? umma_idesc_e4m3_f32(BM2, C::BN) : umma_idesc_bf16_f32(BM2, C::BN);
       uint32_t stage = 0, phase = 0;
@@ -1554,6 +1646,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GA || GB ? kThreadsG
         if (pre_issuer && c.rows > 128 * (int)rank)
           for (int j = 0; j < C::PRE_SLOTS; ++j)
             swb_pre_issue<C>(p, &tmP, smem, pre_full, pre_empty, half, pre_issued, c, (int)rank, ash, j, abort_flag);
+      }
+      if constexpr (W2) {
+        // the tile's two n-tiles in turn, each accumulator released as soon as it has been read
+        int ok = 1;
+#pragma unroll 1
+        for (int j = 0; j < 2 && ok; ++j) {
+          if (lane == 0) ok = mbar_wait_cluster(&tfull_bar[j], (uint32_t)it & 1u, abort_flag, p.status) ? 1 : 0;
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t tb = tmem_base + ((uint32_t)(quad * 32) << 16) + (uint32_t)(j * C::ACC_STRIDE);
+          drain_wide_bf16(tb, c.row0 + 128 * (int)rank, c.rows - 128 * (int)rank, row_in_tile, 2 * c.nt + j, p, half,
+                          stg, &tempty_bar[j]);
+        }
+        if (!ok) break;
+        continue;
       }
       int ok = 1;
       if (lane == 0) ok = mbar_wait_cluster(&tfull_bar[acc], use & 1u, abort_flag, p.status) ? 1 : 0;
@@ -1718,11 +1826,11 @@ static cudaError_t launch_mx_impl(const CUtensorMap& ta, const CUtensorMap& tb, 
   return cudaGetLastError();
 }
 
-template <int EPI, bool F8 = false, bool GA = false, bool GB = false>
+template <int EPI, bool F8 = false, bool GA = false, bool GB = false, bool W2 = false>
 static cudaError_t launch_pair_impl(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& gp, int tiles,
                                     cudaStream_t stream, const CUtensorMap* tp = nullptr) {
-  using PairCfg = PairCfgT<EPI>;
-  auto kern = gemm_tc_pair_kernel<EPI, F8, GA, GB>;
+  using PairCfg = PairCfgT<EPI, W2>;
+  auto kern = gemm_tc_pair_kernel<EPI, F8, GA, GB, W2>;
   constexpr int threads = GA || GB ? kThreadsGA : kThreads;
   static std::atomic<int> max_pairs_of[kMaxDeviceSlots];   // 0: not set up on that device yet
   const int dev = device_slot();
@@ -1904,6 +2012,20 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
   gp.router = q.router;
   gp.status = q.status;
 
+  // Wide pair tiles (two n-tiles per tile, each k-tile of A feeding both) for the bf16-out GEMMs
+  // with TMA-loaded A over an even number of n-tiles, at least two tiles per CTA pair: the latent
+  // projections and grouped GEMM 2.  A stage then brings 48 KB per 1024 MMA cycles instead of
+  // 32 KB per 512, and shared memory, which also feeds the MMAs their operands, is no longer the
+  // limit (latent prefill: latent down-projection 0.605 -> 0.528 ms, up 0.611 -> 0.571 ms; on
+  // another box grouped GEMM 2 1.088 -> 1.045 ms).  Measured slower and not used: grouped GEMM 1
+  // with its gathered rows (OlmoE shape 0.376 -> 0.394 ms, latent prefill 2.05 -> 2.10 ms) and
+  // fp32 out, whose epilogue does not release the accumulator early (sigmoid-wide grouped GEMM 2
+  // 1.83 -> 1.89 ms, the 896-expert router 0.309 -> 0.315 ms).
+  const bool wide = pair && !ga && !f8 && !gb && q.k_groups == 0 && gp.splits == 1 && !q.b_mn_major &&
+                    !q.a_mn_major && q.epilogue == EPI_BF16 && gp.n_tiles % 2 == 0 &&
+                    (int64_t)((q.M + BM2 - 1) / BM2) * (gp.n_tiles / 2) >= num_sms();
+  if (wide) gp.n_tiles /= 2;
+
   if (ga) {
     if (pair)
       return f8 ? launch_pair_impl<EPI_SWIGLU, true, true>(ta, tb, gp, 0, stream)
@@ -1918,6 +2040,7 @@ cudaError_t launch_gemm(const GemmProblem& q, cudaStream_t stream) {
       if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU, true>(ta, tb, gp, tiles, stream);
       return launch_pair_impl<EPI_BF16, true>(ta, tb, gp, tiles, stream);
     }
+    if (wide) return launch_pair_impl<EPI_BF16, false, false, false, true>(ta, tb, gp, tiles, stream);
     if (q.epilogue == EPI_SWIGLU) return launch_pair_impl<EPI_SWIGLU>(ta, tb, gp, tiles, stream);
     if (gb) return launch_pair_impl<EPI_F32, false, false, true>(ta, tb, gp, tiles, stream);   // K-grouped, B gathered
     if (q.epilogue == EPI_F32)   // fp32 out: dense, or grouped (the layer's fp32 expert rows)

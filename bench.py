@@ -351,6 +351,12 @@ def run_native(args):
     inter = native.layer_intermediates(cfg, T, ws)
     touched = int((inter["counts"] > 0).sum().item())
     alg_bytes = W.algorithmic_bytes(spec, touched)
+    # rows the grouped GEMMs compute: each expert's rows rounded up to whole row tiles (256-row
+    # CTA-pair tiles from 192 rows per expert on average, 128-row tiles below, as the library plans)
+    counts_h = inter["counts"].long().cpu()
+    rows_h = int(counts_h.sum().item())
+    tile_rows = 256 if (rows_h >= 192 * spec.num_experts and spec.expert_fp8 != native.EXPERT_MXFP8) else 128
+    padded_rows = int(((counts_h + tile_rows - 1) // tile_rows).sum().item()) * tile_rows
     flush = alg_bytes < 2 * L2
     flush_buf = torch.empty(2 * L2 // 4 + 1024, dtype=torch.float32, device="cuda") if flush else None
 
@@ -621,6 +627,10 @@ def run_native(args):
                      ", e4m3 operands)" if spec.expert_fp8 else ")"),
                      "bound": "tensor", "achieved": achieved, "peak": gemm_peak, "unit": "TFLOP/s",
                      "frac": achieved / gemm_peak,
+                     **({} if spec.capacity_factor else {
+                         "rows": rows_h, "tile_rows": tile_rows, "padded_rows": padded_rows,
+                         "padding_frac": 1.0 - rows_h / padded_rows if padded_rows else 0.0,
+                         "achieved_on_padded_rows": achieved * padded_rows / rows_h if rows_h else 0.0}),
                      "traffic": (None if spec.expert_fp8 or spec.capacity_factor or args.tokens or args.experts
                                  else kernel_traffic(spec.name)),
                      "peak_source": gemm_label},

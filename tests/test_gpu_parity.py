@@ -67,6 +67,10 @@ CASES = {
     # over d_model = 2048 (4 wide tiles per 256-row tile), skewed loads for ragged group tails
     "wide_tiles": WorkloadSpec("wide_tiles", T=4096, d_model=2048, num_experts=16, top_k=4, hidden_size=1024,
                                gating="sigmoid", skew=True, seed=40),
+    # wide tiles over a ragged d_model: 1344 = 5 x 256 + 64, so the last wide tile's second n-tile
+    # holds 64 real columns (its other B rows are the next expert's or past the weights' end)
+    "wide_tiles_ragged_n": WorkloadSpec("wide_tiles_ragged_n", T=4096, d_model=1344, num_experts=16, top_k=4,
+                                        hidden_size=512, gating="softmax", skew=True, seed=44),
     # the same with the weights restored x top_k: grouped GEMM 2 writes fp32 rows (256-column tiles)
     "wide_tiles_restore": WorkloadSpec("wide_tiles_restore", T=4096, d_model=2048, num_experts=16, top_k=4,
                                        hidden_size=1024, gating="sigmoid", normalize_expert_weights=1.0,
@@ -75,6 +79,9 @@ CASES = {
     # d_model 4096
     "wide_tiles_latent": WorkloadSpec("wide_tiles_latent", T=10240, d_model=4096, num_experts=32, top_k=2,
                                       hidden_size=1024, latent_dim=2048, gating="softmax", skew=True, seed=42),
+    # more than 128 experts, 20,000 tokens (many blocks of top-k warps), E = 196: ragged lanes
+    "router_many_tokens": WorkloadSpec("router_many_tokens", T=20000, d_model=256, num_experts=196, top_k=6,
+                                       hidden_size=64, gating="sigmoid", score_bias_std=0.01, seed=43),
     # more than 128 experts and few row tiles: the router GEMM takes a 3-way split-K whose slices
     # top-k adds itself (up to 128 experts the router's epilogue runs the top-k; a deeper split, as
     # in the latent decode workload, goes through the separate sum)

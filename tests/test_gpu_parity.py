@@ -75,9 +75,9 @@ CASES = {
     "wide_tiles_restore": WorkloadSpec("wide_tiles_restore", T=4096, d_model=2048, num_experts=16, top_k=4,
                                        hidden_size=1024, gating="sigmoid", normalize_expert_weights=1.0,
                                        restore_weight_scale=True, seed=41),
-    # the latent projections (dense) and grouped GEMM 2 on wide tiles: T = 10,240 rows, latent 2048,
-    # d_model 4096
-    "wide_tiles_latent": WorkloadSpec("wide_tiles_latent", T=10240, d_model=4096, num_experts=32, top_k=2,
+    # the latent projections (dense) and grouped GEMM 2 on wide tiles: T = 10,000 rows (the last
+    # 256-row tile holds 16), latent 2048, d_model 4096
+    "wide_tiles_latent": WorkloadSpec("wide_tiles_latent", T=10000, d_model=4096, num_experts=32, top_k=2,
                                       hidden_size=1024, latent_dim=2048, gating="softmax", skew=True, seed=42),
     # more than 128 experts, 20,000 tokens (many blocks of top-k warps), E = 196: ragged lanes
     "router_many_tokens": WorkloadSpec("router_many_tokens", T=20000, d_model=256, num_experts=196, top_k=6,
@@ -343,6 +343,33 @@ def test_grouped_swiglu_group_tails(h):
             rows = x_np[g_np[off[e]:off[e + 1]]]
             assert_close_layer(pre_np[off[e]:off[e + 1]], np.concatenate([rows @ w_up.T, rows @ w_gate.T], axis=1),
                                f"group tails, pre-activations of expert {e}")
+
+
+def test_grouped_gemm2_group_tails_on_wide_tiles():
+    """Grouped GEMM 2 on wide pair tiles (d_model 1024: two 256-column n-tiles per tile, 79 row
+    tiles) over every kind of group: empty, 1-row, tails of every size class, whole tiles."""
+    counts = TAIL_COUNTS * 3
+    E = len(counts)
+    spec = WorkloadSpec("gemm2_tails_wide", T=sum(counts), d_model=1024, num_experts=E, top_k=1, hidden_size=128,
+                        gating="softmax", seed=45)
+    assert spec.rows >= 192 * E and ((spec.rows + 255) // 256) * 2 >= 152   # pair tiles, wide for GEMM 2
+    inp = generate(spec)
+    cfg = native.config_from_spec(spec)
+    wts = native.DeviceWeights.from_inputs(inp)
+    ws = native.workspace(cfg, spec.T)
+    counts_d, offsets, gather, scatter = native.moe_permute(cfg, designed_routing(counts, 11), ws)
+    assert counts_d.cpu().tolist() == counts
+    xr = torch.from_numpy(np.random.default_rng(12).standard_normal((spec.T, spec.d_model), dtype=np.float32)).to(
+        torch.bfloat16)
+    y = native.moe_grouped_swiglu(cfg, wts, xr.cuda(), gather, offsets, ws)
+    expect_ok()
+    perm = ref.Permutation(counts_d.cpu().numpy(), offsets.cpu().numpy(), gather.cpu().numpy(), scatter.cpu().numpy())
+    want = ref.expert_outputs(oracle_config(spec), f64(xr), perm, oracle_weights(spec, inp).expert)
+    got = y.double().cpu().numpy()
+    off = offsets.cpu().numpy()
+    for e, n in enumerate(counts):
+        if n:
+            assert_close_layer(got[off[e]:off[e + 1]], want[off[e]:off[e + 1]], f"wide GEMM 2 tails, expert {e} ({n} rows)")
 
 
 @pytest.mark.parametrize("name", ["tiny", "sigmoid_bias_restore", "latent_skew", "max_experts", "one_token",

@@ -206,6 +206,39 @@ def test_fp8_latent_layer_hand_computed():
     np.testing.assert_array_equal(got, want)
 
 
+def test_mx_latent_layer_hand_computed():
+    """The latent MXFP8 layer quantises the experts' bf16 input, worked out by hand.  x = (1, 1, 0, ...)
+    and W_down rows (1.1875, -2^-9, 0, ...), (1, 0, ...) give x_routed = (1.1875 - 2^-9, 1).  bf16
+    rounds the first to 1.1875 (2^-9 is under half its step of 2^-7).  That row's block amax is
+    1.1875, so its scale is 2^(0 - 8) and 1.1875 / 2^-8 = 304, halfway between the e4m3 neighbours
+    288 and 320: the tie goes to the even code 320, so the expert sees x = (1.25, 1).  (Without the
+    bf16 rounding, 303.5 goes to 288 and x0 = 1.125.)  Gate rows 0, 1 = (32, 32): g = 72 and
+    silu(72) = 72 in float64.  Up rows (1, 1/16) and (2, 0): u = (1.3125, 2.5).  So H = (94.5, 180),
+    exact in bf16; its block amax 180 gives the scale 1/2, and 189 rounds to the e4m3 code 192,
+    360 to 352: H = (96, 176).  W_out copies H's first two columns; one expert with softmax gating
+    has weight 1, and with the norm off and W_up the identity the output is (96, 176, 0, ...).  Every
+    weight row is MX-representable (codes 256 and 16 under power-of-two scales)."""
+    D = L = 64
+    h = 32
+    cfg = ref.OracleConfig(d_model=D, num_experts=1, top_k=1, hidden_size=h, latent_dim=L, up_proj_norm=False)
+    x = np.zeros((1, D))
+    x[0, :2] = 1.0
+    w_down = np.zeros((L, D))
+    w_down[0, :2] = [1.1875, -(2.0 ** -9)]
+    w_down[1, 0] = 1.0
+    w_up, w_gate, w_out = np.zeros((h, L)), np.zeros((h, L)), np.zeros((L, h))
+    w_up[0, :2] = [1.0, 0.0625]
+    w_up[1, 0] = 2.0
+    w_gate[0, :2] = w_gate[1, :2] = 32.0
+    w_out[0, 0] = w_out[1, 1] = 1.0
+    wts = ref.OracleWeights(w_router=np.zeros((1, D)), expert=lambda e: (w_up, w_gate, w_out), w_down_latent=w_down,
+                            w_up_latent=np.eye(D, L))
+    got = ref.layer_forward_mxfp8(cfg, x, wts)
+    want = np.zeros((1, D))
+    want[0, :2] = [96.0, 176.0]
+    np.testing.assert_array_equal(got, want)
+
+
 def test_bf16_half_ulp_bound_is_the_rounding_error():
     """half_ulp_bf16 bounds |v - bf16(v)| and is reached at rounding midpoints (the parity bar's
     allowance for a bf16 output's own rounding)."""

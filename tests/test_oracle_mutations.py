@@ -177,6 +177,17 @@ def _fp8_layer_unrounded_latent_input(cfg, x, wts, forced_idx=None):
     return ref.restore_routed_output(cfg, z, wts.w_up_latent, wts.rms_weight)
 
 
+def _mx_layer_unrounded_latent_input(cfg, x, wts, forced_idx=None):
+    # wrong: the latent projection's output reaches the MX quantiser without its bf16 rounding
+    x = np.asarray(x, np.float64)
+    x_routed = ref.prepare_routed_input(cfg, x, wts.w_down_latent)
+    r = ref.route(cfg, x, wts.w_router, wts.b_router, wts.score_bias, forced_idx)
+    perm = ref.permute(r.idx, cfg.num_experts)
+    y = ref.expert_outputs_mxfp8(cfg, x_routed, perm, wts.expert)
+    z = ref.combine(y, perm.scatter_pos, r.weights)
+    return ref.restore_routed_output(cfg, z, wts.w_up_latent, wts.rms_weight)
+
+
 CASES = [
     ("score_bias_update", _bias_update_wrong_sign, lambda: B.test_score_bias_update_hand_values()),
     ("load_imbalance", _imbalance_min_over_mean, lambda: B.test_load_imbalance_hand_values()),
@@ -198,6 +209,7 @@ CASES = [
     ("quantize_rowwise_e4m3", _rowwise_per_column, lambda: F.test_fp8_experts_hand_computed_h_tie()),
     ("expert_outputs_fp8", _fp8_experts_h_unquantised, lambda: F.test_fp8_experts_hand_computed_h_tie()),
     ("layer_forward_fp8", _fp8_layer_unrounded_latent_input, lambda: F.test_fp8_latent_layer_hand_computed()),
+    ("layer_forward_mxfp8", _mx_layer_unrounded_latent_input, lambda: F.test_mx_latent_layer_hand_computed()),
 ]
 
 
